@@ -1,0 +1,168 @@
+/*
+ * ctr_oracle.c -- plain CPU oracle for dense (groups = 1) transposed convolution.
+ *
+ * TEST INFRASTRUCTURE.  Only the test suite, the smoke check and the CPU-baseline leg of
+ * the benchmark load this file's library.  The product library never links, loads or
+ * calls it, and it shares no code, header or table with the CUDA path.
+ *
+ * What it computes: the scatter form of ConvTranspose, in double precision.
+ *
+ *   for every batch b, input channel ic, input position i, output channel oc, tap t
+ *       o = i*s - p + t                                  (per spatial dimension)
+ *       if 0 <= o < L_out:  acc[b, oc, o] += x[b, ic, i] * w[ic, oc, t]
+ *   y[b, oc, o] = bias[oc] + acc[b, oc, o]               (bias = 0 when absent)
+ *
+ * with L_out = (L_in - 1)*s - 2p + k + op per dimension and the weight in the un-flipped
+ * torch layout w[C_in][C_out][k...].  Sources:
+ *   - "[ExecuTorch][WebGPU] Add optimized conv2d op" (PR #20849), Implementation: the
+ *     transposed kernel reads the weight un-flipped as [IC, OC/groups, KH, KW] and a tap
+ *     reaches an output when (oh + pH - kh*dH) is divisible by the stride and in range --
+ *     the gather reading of the same scatter sum;
+ *   - "[XNNPACK] Lower dense transposed convs as one polyphase conv + depth to space"
+ *     (PR #25037), Summary: the clean-upscale output size (H-1)s - 2p + k + op;
+ *   - "[WebGPU] optimizations for audio models" (PR #33978), ConvTranspose commits: the
+ *     output starts from the bias (or zeros) and every tap contribution is summed onto it;
+ *     an empty spatial input leaves the bias (or zeros) in a non-empty output.
+ *
+ * 1-D is the 2-D code with a unit height (k = s = 1, p = op = 0 along y).
+ *
+ * Accumulation is in double; the caller rounds the result to the I/O precision.  OpenMP
+ * splits the work into items (b, oc, chunk of input positions); every item owns a private
+ * accumulator and the chunks are summed in a fixed order at the end, so the result does
+ * not depend on the number of threads.  The chunk count depends on the problem only.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Output length of one spatial dimension (may be <= 0 for invalid geometry). */
+int64_t ctr_oracle_output_size(int64_t L_in, int64_t k, int64_t s, int64_t p, int64_t op)
+{
+    return (L_in - 1) * s - 2 * p + k + op;
+}
+
+/* Threads the oracle's parallel loops use (for reporting). */
+int ctr_oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Number of (input position, tap) pairs, over all spatial dimensions, that land inside
+ * the output: the count of scalar contributions per (input channel, output channel)
+ * pair.  Returns -1 on invalid geometry. */
+int64_t ctr_oracle_landed_pairs(int ndim, const int64_t *in_sp, const int64_t *ker,
+                                const int64_t *str, const int64_t *pad, const int64_t *opad)
+{
+    if (ndim < 1 || ndim > 2) return -1;
+    int64_t total = 1;
+    for (int d = 0; d < ndim; ++d) {
+        int64_t L_out = ctr_oracle_output_size(in_sp[d], ker[d], str[d], pad[d], opad[d]);
+        int64_t n = 0;
+        for (int64_t i = 0; i < in_sp[d]; ++i)
+            for (int64_t t = 0; t < ker[d]; ++t) {
+                int64_t o = i * str[d] - pad[d] + t;
+                if (o >= 0 && o < L_out) ++n;
+            }
+        total *= n;
+    }
+    return total;
+}
+
+/*
+ * y = ConvTranspose(x, w) + bias, all in double.
+ *   x    [B][C_in][in_sp[0]]([in_sp[1]])            contiguous
+ *   w    [C_in][C_out][ker[0]]([ker[1]])            contiguous, un-flipped torch layout
+ *   bias [C_out] or NULL
+ *   y    [B][C_out][L_out[0]]([L_out[1]])           contiguous, written in full
+ * Returns 0 on success, -1 on invalid arguments, -2 when out of host memory.
+ */
+int ctr_oracle_conv_transpose(int ndim, int64_t B, int64_t C_in, int64_t C_out,
+                              const int64_t *in_sp, const int64_t *ker, const int64_t *str,
+                              const int64_t *pad, const int64_t *opad,
+                              const double *x, const double *w, const double *bias, double *y)
+{
+    if (ndim < 1 || ndim > 2 || B < 0 || C_in < 1 || C_out < 1) return -1;
+
+    /* Unit height for 1-D. */
+    int64_t H = 1, kh = 1, sh = 1, ph = 0, oph = 0;
+    int64_t W = in_sp[0], kw = ker[0], sw = str[0], pw = pad[0], opw = opad[0];
+    if (ndim == 2) {
+        H = in_sp[0]; kh = ker[0]; sh = str[0]; ph = pad[0]; oph = opad[0];
+        W = in_sp[1]; kw = ker[1]; sw = str[1]; pw = pad[1]; opw = opad[1];
+    }
+    if (H < 0 || W < 0 || kh < 1 || kw < 1 || sh < 1 || sw < 1 || ph < 0 || pw < 0 ||
+        oph < 0 || opw < 0)
+        return -1;
+    const int64_t Ho = ctr_oracle_output_size(H, kh, sh, ph, oph);
+    const int64_t Wo = ctr_oracle_output_size(W, kw, sw, pw, opw);
+    if (Ho <= 0 || Wo <= 0) return -1;
+
+    const int64_t npos = H * W;          /* input positions per (b, ic) */
+    const int64_t nout = Ho * Wo;        /* output positions per (b, oc) */
+    const int64_t ntap = kh * kw;
+
+    /* Chunks of input positions per (b, oc): enough items for the cores when B*C_out is
+     * small.  A function of the problem only. */
+    int64_t nchunk = 1;
+    if (B * C_out < 32) nchunk = (32 + B * C_out - 1) / (B * C_out);
+    if (nchunk > npos) nchunk = npos > 0 ? npos : 1;
+    const int64_t nitem = B * C_out * nchunk;
+
+    double *part = NULL;
+    if (nitem > 0) {
+        part = (double *)calloc((size_t)(nitem * nout), sizeof(double));
+        if (!part) return -2;
+    }
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t item = 0; item < nitem; ++item) {
+        const int64_t chunk = item % nchunk;
+        const int64_t oc = (item / nchunk) % C_out;
+        const int64_t b = item / (nchunk * C_out);
+        const int64_t pos_lo = npos * chunk / nchunk;
+        const int64_t pos_hi = npos * (chunk + 1) / nchunk;
+        double *acc = part + item * nout;
+        for (int64_t ic = 0; ic < C_in; ++ic) {
+            const double *xp = x + (b * C_in + ic) * npos;
+            const double *wp = w + (ic * C_out + oc) * ntap;
+            for (int64_t pos = pos_lo; pos < pos_hi; ++pos) {
+                const int64_t iy = pos / W, ix = pos % W;
+                const double xv = xp[pos];
+                for (int64_t ty = 0; ty < kh; ++ty) {
+                    const int64_t oy = iy * sh - ph + ty;
+                    if (oy < 0 || oy >= Ho) continue;
+                    /* Taps tx with 0 <= ix*sw - pw + tx < Wo: the range check of the
+                     * definition, written as loop bounds. */
+                    const int64_t ox0 = ix * sw - pw;
+                    int64_t tx_lo = ox0 < 0 ? -ox0 : 0;
+                    int64_t tx_hi = Wo - ox0 < kw ? Wo - ox0 : kw;
+                    double *arow = acc + oy * Wo + ox0;
+                    const double *wrow = wp + ty * kw;
+                    for (int64_t tx = tx_lo; tx < tx_hi; ++tx) arow[tx] += xv * wrow[tx];
+                }
+            }
+        }
+    }
+
+    /* y = bias + sum of the chunk accumulators, chunks in increasing order. */
+#pragma omp parallel for schedule(static)
+    for (int64_t bo = 0; bo < B * C_out; ++bo) {
+        const int64_t oc = bo % C_out;
+        const double bv = bias ? bias[oc] : 0.0;
+        double *yp = y + bo * nout;
+        for (int64_t o = 0; o < nout; ++o) yp[o] = bv;
+        for (int64_t c = 0; c < nchunk; ++c) {
+            const double *acc = part + (bo * nchunk + c) * nout;
+            for (int64_t o = 0; o < nout; ++o) yp[o] += acc[o];
+        }
+    }
+    free(part);
+    return 0;
+}
