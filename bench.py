@@ -1,0 +1,463 @@
+"""Benchmark: ConvTranspose GFLOP/s and fraction of roofline per call on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--all]
+
+One step is one ctr_forward over one batch of the workload (input staging, the tensor-core
+GEMM with its fused output stage, and for split-K plans the reduce), with the weight packed
+beforehand as a deployed layer would have it.  The default workload is the codec-decoder
+upsampler (1x512x2000 -> 1x256x16000, kernel 16, stride 8, padding 4, fp32 I/O).
+
+Timing: W untimed warm-up steps and a ~1 s soak of the same step, then exactly K steps
+bracketed by a barrier and torch.cuda.synchronize() on both sides, each step between CUDA
+events on the launching stream.  Consecutive steps rotate over enough sets of input,
+packed weight, workspace and output buffers to exceed twice the L2 size, so no step reads
+data the previous one left in L2.  Under torchrun every rank runs the same workload on its
+own GPU (weak scaling, no collective on the data path); rank 0 prints one JSON line with
+the maximum time over ranks.
+
+--impl reference times the CPU oracle (double precision, OpenMP on the host cores) on a
+bounded sample of the same workload: the reference arm of this benchmark.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+DEFAULT_WORKLOAD = "codec_upsampler_f32"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Nominal dense tensor throughput relative to bf16 (tf32 1.1 vs bf16 2.25 PFLOP/s).
+TF32_OVER_BF16 = 1.1 / 2.25
+KERNEL_SOURCES = ["transposed_convolution_gb300/csrc/gemm_tc.cu",
+                  "transposed_convolution_gb300/csrc/epilogue.cuh",
+                  "transposed_convolution_gb300/csrc/ptx.cuh"]
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch of the GEMM kernel from the committed ncu summary, or None when
+    there is none or the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "gemm_tc_%s.md" % workload)
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    try:
+        return int(float(vals["dram_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples every 200 ms while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        rows = [s for (t, s) in self.samples if t0 <= t <= t1]
+        mhz, maxmhz, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                maxmhz.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": max(maxmhz),
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import transposed_convolution_gb300 as ctr
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    layers = workloads.make_workload(args.workload)
+    if len(layers) != 1:
+        return run_ours_stack(args, rank, world, local_rank, layers)
+    li = layers[0]
+    L = li.layer
+    tdt = torch.bfloat16 if L.dtype == "bf16" else torch.float32
+
+    def t(a):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev).to(tdt)
+
+    # Buffer sets to rotate over: more than twice the L2 size in total.
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20
+    x0, w0, b0 = t(li.x), t(li.w), t(li.bias)
+    probe = ctr.Plan(L.B, L.C_in, L.C_out, L.in_sp, L.kernel, L.stride, L.padding,
+                     L.output_padding, dtype=tdt, negative_slope=L.act_slope, device=dev)
+    y_bytes = int(np.prod(probe.out_shape)) * L.elem_bytes
+    set_bytes = (x0.numel() * L.elem_bytes + probe.packed_bytes + probe.workspace_bytes + y_bytes)
+    nsets = max(2, int(math.ceil(2.0 * l2 / set_bytes)) + 1)
+    probe.close()
+    sets = []
+    for i in range(nsets):
+        p = ctr.Plan(L.B, L.C_in, L.C_out, L.in_sp, L.kernel, L.stride, L.padding,
+                     L.output_padding, dtype=tdt, negative_slope=L.act_slope, device=dev)
+        p.prepack(w0)
+        sets.append({"plan": p, "x": x0.clone(), "b": None if b0 is None else b0.clone(),
+                     "y": torch.empty(p.out_shape, dtype=tdt, device=dev)})
+    torch.cuda.synchronize()
+
+    # Prepack time (reported separately; not part of a step).
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    sets[0]["plan"].prepack(w0)
+    e1.record()
+    torch.cuda.synchronize()
+    prepack_ms = e0.elapsed_time(e1)
+
+    def step(i, evs=None):
+        s = sets[i % nsets]
+        if evs is not None:
+            ctr.ctr_plan_set_timing_events(s["plan"].handle, evs[0].cuda_event, evs[1].cuda_event)
+        s["plan"].forward(s["x"], s["b"], y=s["y"])
+        if evs is not None:
+            ctr.ctr_plan_set_timing_events(s["plan"].handle, None, None)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    sets[0]["plan"].check()
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    soak_t0 = time.time()
+    i = 0
+    while time.time() - soak_t0 < args.soak:
+        for _ in range(50):
+            step(i)
+            i += 1
+        torch.cuda.synchronize()
+
+    # Timed region: exactly K steps.
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    for a, b in kev:       # create the driver events before handing them to the library
+        a.record()
+        b.record()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = ctr.ctr_launch_count()
+    wall0 = time.time()
+    for k in range(K):
+        ev[k][0].record()
+        step(k, kev[k])
+        ev[k][1].record()
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    launches = ctr.ctr_launch_count() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    time.sleep(0.25)
+    sampler.stop()
+    for s in sets:
+        s["plan"].check()
+
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_ms = [a.elapsed_time(b) for a, b in kev]
+    total_ms = sum(step_ms)
+    kern_avg = sum(kern_ms) / K
+
+    if world > 1:
+        tt = torch.tensor([total_ms, kern_avg], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms, kern_avg = float(tt[0]), float(tt[1])
+
+    # End to end through the public API: pinned host x -> device, forward, y -> pinned host.
+    x_host = torch.from_numpy(np.ascontiguousarray(li.x)).to(tdt).pin_memory()
+    y_host = torch.empty(sets[0]["y"].shape, dtype=tdt).pin_memory()
+    e2e_ms = []
+    for k in range(max(3, min(K, 50))):
+        s = sets[k % nsets]
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        s["x"].copy_(x_host, non_blocking=True)
+        s["plan"].forward(s["x"], s["b"], y=s["y"])
+        y_host.copy_(s["y"], non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    e2e_ms = statistics.median(e2e_ms[1:]) if len(e2e_ms) > 1 else e2e_ms[0]
+
+    # Parity of this run's output against the oracle (computed after timing).
+    parity = None
+    if rank == 0 and args.parity:
+        import oracle
+        ref = oracle.conv_transpose(li.x, li.w, li.bias, L.stride, L.padding, L.output_padding)
+        if L.act_slope is not None:
+            ref = oracle.leaky_relu(ref, L.act_slope)
+        parity = oracle.rel_l2(sets[(K - 1) % nsets]["y"].float().cpu().numpy(), ref)
+
+    flops = 2.0 * L.useful_macs
+    ms_per_step = total_ms / K
+    peaks, peak_src = load_peaks()
+    if L.dtype == "bf16":
+        peak_tflops = peaks["bf16_tflops"]
+        peak_note = "bf16 dense, %s burst" % peak_src
+    else:
+        peak_tflops = peaks["bf16_tflops"] * TF32_OVER_BF16 / 3.0
+        peak_note = ("3xTF32: %s bf16 burst x nominal tf32/bf16 (1.1/2.25) / 3 products "
+                     "per useful MAC" % peak_src)
+    t_tensor = flops / (peak_tflops * 1e12)
+    t_hbm = L.compulsory_bytes / (peaks["hbm_gbs"] * 1e9)
+    bound = "tensor" if t_tensor >= t_hbm else "hbm"
+    kern_s = kern_avg / 1e3
+    if bound == "tensor":
+        achieved, peak, unit = flops / kern_s / 1e12, peak_tflops, "TFLOP/s"
+    else:
+        achieved, peak, unit = L.compulsory_bytes / kern_s / 1e9, peaks["hbm_gbs"], "GB/s"
+    traffic = profiled_traffic(args.workload)
+    t_roof = max(t_tensor, t_hbm)
+    clocks = sampler.summary(soak_t0, wall1 + 0.25)
+
+    plan_desc = sets[0]["plan"].describe()
+    result = {
+        "metric": "ConvTranspose GFLOP/s and % of roofline (tensor peak vs HBM) per call",
+        "value": round(world * flops / (ms_per_step / 1e3) / 1e9, 1),
+        "unit": "GFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "3xtf32-fp32acc" if L.dtype == "f32" else "bf16-fp32acc",
+        "data": "synthetic (seeded; workloads.py)",
+        "config": {"workload": args.workload, "shape": L.describe(),
+                   "l2": "rotating %d buffer sets, %.0f MB > 2x L2 (%.0f MB)"
+                         % (nsets, nsets * set_bytes / 1e6, l2 / 1e6),
+                   "parallelism": "replica per GPU" if world > 1 else "single GPU",
+                   "plan": plan_desc},
+        "pct_of_roofline": round(100.0 * t_roof / (ms_per_step / 1e3), 2),
+        "roofline_us": round(t_roof * 1e6, 3),
+        "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 2),
+                     "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "gemm_tc_kernel", "kernel_us": round(kern_avg * 1e3, 3),
+                     "peak_source": peak_note},
+        "e2e": {"value": round(world * flops / (e2e_ms / 1e3) / 1e9, 1), "unit": "GFLOP/s",
+                "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
+                "d2h_bytes_per_step": int(y_host.numel() * y_host.element_size()),
+                "ms_per_step": round(e2e_ms, 5)},
+        "gpu_launches": int(launches),
+        "launches_per_step": launches / K,
+        "clocks": clocks,
+        "prepack_ms": round(prepack_ms, 4),
+        "parity_rel_l2": parity,
+        "wall_s_timed": round(wall1 - wall0, 4),
+    }
+    for s in sets:
+        s["plan"].close()
+    return result
+
+
+def run_ours_stack(args, rank, world, local_rank, layers):
+    raise SystemExit("stack workloads are benchmarked through --workload of a single layer")
+
+
+# ------------------------------------------------------------------ oracle (CPU) arm
+
+def oracle_sample(name, budget_s):
+    """Time the oracle on a bounded sample of the workload: the first layer on a prefix of
+    the input positions (all of them when that fits the budget).  Returns (seconds per
+    call, useful flops per call, sample description)."""
+    import oracle
+    li = workloads.make_workload(name)[0]
+    L = li.layer
+    x = li.x
+    desc = "full layer"
+    # Shrink the last input dimension until one call is at most budget/3 seconds.
+    for _ in range(12):
+        t0 = time.time()
+        oracle.conv_transpose(x, li.w, li.bias, L.stride, L.padding, L.output_padding)
+        dt = time.time() - t0
+        if dt <= budget_s / 3 or x.shape[-1] <= 8:
+            break
+        x = x[..., : max(8, x.shape[-1] // 2)]
+        desc = "input prefix %s of %s" % (x.shape[-1], L.in_sp[-1])
+    macs = L.B * L.C_in * L.C_out * int(np.prod(L.kernel))
+    macs *= int(np.prod(x.shape[2:]))
+    return dt, 2.0 * macs, desc, (x, li)
+
+
+def time_oracle(name, budget_s=12.0):
+    import oracle
+    dt, flops, desc, (x, li) = oracle_sample(name, budget_s)
+    L = li.layer
+    reps, total = 0, 0.0
+    while total < budget_s and reps < 50:
+        t0 = time.time()
+        oracle.conv_transpose(x, li.w, li.bias, L.stride, L.padding, L.output_padding)
+        total += time.time() - t0
+        reps += 1
+    sec = total / reps
+    return {"value": round(flops / sec / 1e9, 3), "unit": "GFLOP/s", "cores": oracle.threads(),
+            "kind": "oracle", "sample": "%s of %s, %d calls, %.2f s each" % (desc, name, reps, sec),
+            "sec_per_call": sec}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    K, W = args.steps, args.warmup
+    import oracle
+    _, flops, desc, (x, li) = oracle_sample(args.workload, 8.0)
+    L = li.layer
+    for _ in range(min(W, 1)):
+        oracle.conv_transpose(x, li.w, li.bias, L.stride, L.padding, L.output_padding)
+    times = []
+    for _ in range(K):
+        t0 = time.time()
+        oracle.conv_transpose(x, li.w, li.bias, L.stride, L.padding, L.output_padding)
+        times.append(time.time() - t0)
+        if sum(times) > 120:
+            break
+    sec = sum(times) / len(times)
+    v = round(flops / sec / 1e9, 3)
+    return {
+        "impl": "reference",
+        "metric": "ConvTranspose GFLOP/s and % of roofline (tensor peak vs HBM) per call",
+        "value": v, "unit": "GFLOP/s", "n_gpus": world, "steps": len(times), "warmup": W,
+        "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; workloads.py)",
+        "config": {"workload": args.workload, "shape": L.describe(), "sample": desc},
+        "cpu_baseline": {"value": v, "unit": "GFLOP/s", "cores": oracle.threads(),
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": v, "unit": "GFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=workloads.WORKLOAD_ORDER)
+    ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed load before timing")
+    ap.add_argument("--no-parity", dest="parity", action="store_false")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        torch.distributed.init_process_group(backend=backend)
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if args.cpu_baseline and world == 1:
+            cb = time_oracle(args.workload)
+            res["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,203 @@
+/*
+ * ctr.h -- C ABI of the GB300 (sm_103a) transposed-convolution library.
+ *
+ * The operation is dense (groups = 1) 1-D or 2-D ConvTranspose, in the scatter form
+ *
+ *     y[b, oc, i*s - p + t] += x[b, ic, i] * w[ic, oc, t]      (per spatial dimension)
+ *     y[b, oc, o]           += bias[oc]
+ *
+ * with L_out = (L_in - 1)*s - 2p + k + op per spatial dimension and the weight in the
+ * un-flipped torch layout [C_in][C_out][k...].  Sources:
+ *   - "[ExecuTorch][WebGPU] Add optimized conv2d op" (PR #20849), Implementation and
+ *     Constraints: the gather condition, the un-flipped [IC, OC, KH, KW] weight, the optional
+ *     bias, output_padding < stride;
+ *   - "[XNNPACK] Lower dense transposed convs as one polyphase conv + depth to space"
+ *     (PR #25037), Summary: the polyphase lowering for k = m*s (one stride-1 conv with m
+ *     taps, phase-major, then the phase interleave and the padding slice), which is the
+ *     library's main path;
+ *   - "[WebGPU] optimizations for audio models" (PR #33978), ConvTranspose commits: the
+ *     X[M, C_in] x W[C_in, k*C_out] GEMM plus col2im path, the prepacked constant weight,
+ *     f32 intermediates, the bias added once, the empty-input case.
+ *
+ * Call sequence:
+ *     ctr_plan_create -> (ctr_plan_set_*) -> ctr_packed_weight_bytes / ctr_workspace_bytes
+ *     -> ctr_prepack_weight (once per weight) -> ctr_plan_bind_workspace
+ *     -> ctr_forward (any number of times) -> ctr_plan_check -> ctr_plan_destroy
+ *
+ * Conventions for every call:
+ *   - Every call returns a ctr_status (or a size / string); nothing throws or aborts.
+ *   - Device pointers are plain CUDA device addresses in the current device's context.
+ *     Streams are cudaStream_t values passed as void* (NULL = the legacy default stream).
+ *   - The caller owns every device buffer: x, w, w_packed, bias, y and the workspace.  The
+ *     library never frees, keeps or aliases them beyond the call (and, for the workspace,
+ *     the binding).  The plan owns its host metadata and a 4-byte device status word.
+ *   - ctr_forward and ctr_prepack_weight are asynchronous on the given stream and never
+ *     allocate, free or synchronise.
+ *   - Tensors are contiguous, row-major, in the plan's I/O dtype:
+ *         x    [N][C_in][L_in]            or [N][C_in][H][W]
+ *         w    [C_in][C_out][k]           or [C_in][C_out][kH][kW]
+ *         bias [C_out]                    (may be NULL)
+ *         y    [N][C_out][L_out]          or [N][C_out][H_out][W_out]
+ *     and each must start on a 16-byte boundary (CTR_ERR_MISALIGNED otherwise).
+ *   - A plan is not thread-safe: calls on one plan must not overlap on the host.  Two
+ *     ctr_forward calls on one plan that run concurrently on the GPU (different streams)
+ *     share its workspace and race; serialise them or use one plan per stream.
+ */
+#ifndef CTR_H
+#define CTR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct ctr_plan_s *ctr_plan_t;
+
+typedef enum {
+    CTR_OK = 0,
+    CTR_ERR_INVALID_ARG = 1,     /* a size, geometry or handle is invalid */
+    CTR_ERR_UNSUPPORTED = 2,     /* valid ConvTranspose this library does not implement */
+    CTR_ERR_MISALIGNED = 3,      /* a pointer is not 16-byte aligned */
+    CTR_ERR_NO_WORKSPACE = 4,    /* workspace needed but unbound or too small */
+    CTR_ERR_CUDA = 5,            /* a CUDA runtime or launch error */
+    CTR_ERR_DEVICE_TIMEOUT = 6,  /* a bounded device-side wait gave up (see ctr_plan_check) */
+    CTR_ERR_NOT_PREPARED = 7     /* ctr_forward before ctr_prepack_weight on this plan */
+} ctr_status;
+
+typedef enum {
+    CTR_F32 = 0,   /* fp32 I/O; tensor-core products as 3xTF32 (hi/lo split), fp32 accumulate */
+    CTR_BF16 = 1   /* bf16 I/O; bf16 tensor-core products, fp32 accumulate, one final rounding */
+} ctr_dtype;
+
+typedef enum {
+    CTR_ACT_NONE = 0,
+    CTR_ACT_LEAKY_RELU = 1       /* y = y >= 0 ? y : slope * y, after the bias, before rounding */
+} ctr_act;
+
+typedef enum {
+    CTR_PATH_AUTO = 0,
+    CTR_PATH_POLYPHASE = 1,      /* polyphase implicit GEMM on tcgen05 (taps zero-padded to m*s) */
+    CTR_PATH_COL2IM = 2,         /* tcgen05 GEMM into an fp32 column buffer, then col2im */
+    CTR_PATH_GATHER = 3          /* direct gather on CUDA cores */
+} ctr_path;
+
+/*
+ * Create a plan.  Host only: validates the geometry, picks the path and the tiling.  The
+ * only CUDA call reads the current device's SM count; without a GPU it assumes 152 SMs, so
+ * plans can be created and inspected on a machine without one.
+ *   out            receives the plan (set to NULL on failure)
+ *   ndim           1 or 2 spatial dimensions
+ *   N, C_in, C_out batch and channels: N >= 0, C_in >= 1, C_out >= 1
+ *   in_spatial     ndim input sizes, each >= 0 (0 = empty input: y = bias or zeros)
+ *   kernel         ndim kernel sizes >= 1
+ *   stride         ndim strides >= 1
+ *   padding        ndim paddings >= 0 (symmetric per dimension; ONNX begin/end pads differ)
+ *   output_padding ndim values with 0 <= op < stride (may be NULL = zeros)
+ *   dtype          ctr_dtype
+ * Every output size must be >= 1.  Dilation and groups are not parameters: dilation 1 and
+ * groups 1 only.  Returns CTR_ERR_INVALID_ARG on any violation.
+ */
+ctr_status ctr_plan_create(ctr_plan_t *out, int ndim, int64_t N, int64_t C_in, int64_t C_out,
+                           const int64_t *in_spatial, const int64_t *kernel,
+                           const int64_t *stride, const int64_t *padding,
+                           const int64_t *output_padding, int dtype);
+
+/* Fuse an activation into the output stage (default CTR_ACT_NONE).  Host only. */
+ctr_status ctr_plan_set_activation(ctr_plan_t plan, int act, float negative_slope);
+
+/*
+ * Force a path (default CTR_PATH_AUTO) and optionally the split-K factor of the tensor-core
+ * paths (0 = automatic, else 1..16).  Host only.  Must come before ctr_packed_weight_bytes,
+ * ctr_workspace_bytes and ctr_prepack_weight, because the packed layout and the workspace
+ * depend on the path; calling it after ctr_prepack_weight returns CTR_ERR_INVALID_ARG.
+ */
+ctr_status ctr_plan_set_path(ctr_plan_t plan, int path, int split_k);
+
+/* The path the plan will run (a ctr_path other than AUTO), or -1 for a NULL plan. */
+int ctr_plan_get_path(ctr_plan_t plan);
+
+/* Write the ndim output sizes into out_spatial. */
+ctr_status ctr_plan_output_shape(ctr_plan_t plan, int64_t *out_spatial);
+
+/* Bytes of the packed weight buffer ctr_prepack_weight writes (0 for a NULL plan). */
+size_t ctr_packed_weight_bytes(ctr_plan_t plan);
+
+/* Bytes of device workspace ctr_forward needs (may be 0; 0 for a NULL plan). */
+size_t ctr_workspace_bytes(ctr_plan_t plan);
+
+/*
+ * Bind a caller-owned device workspace of at least ctr_workspace_bytes(plan) bytes,
+ * 256-byte aligned.  The binding lasts until the next bind or ctr_plan_destroy; the
+ * workspace must stay allocated meanwhile.  Binding NULL with 0 bytes is allowed when the
+ * plan needs no workspace.
+ */
+ctr_status ctr_plan_bind_workspace(ctr_plan_t plan, void *dev_ptr, size_t bytes);
+
+/*
+ * Pack a weight for this plan (once per weight; asynchronous on stream).
+ *   w         device, [C_in][C_out][k...] in the plan's dtype
+ *   w_packed  device, ctr_packed_weight_bytes(plan) bytes, written in full
+ * The packed weight is valid only for plans with the same geometry, dtype and path.  The
+ * first call on a plan also allocates the plan's 4-byte device status word on the current
+ * device (the only allocation the library makes).
+ */
+ctr_status ctr_prepack_weight(ctr_plan_t plan, const void *w, void *w_packed, void *stream);
+
+/*
+ * y = ConvTranspose(x, w) + bias, then the plan's activation, rounded once to the I/O dtype.
+ *   x         device input, [N][C_in][spatial...]
+ *   w_packed  device, written by ctr_prepack_weight for this plan's geometry
+ *   bias      device [C_out] or NULL
+ *   y         device output, [N][C_out][out spatial...], written in full
+ *   stream    cudaStream_t as void*
+ * Asynchronous; launch failures return CTR_ERR_CUDA.  Device-side errors (a bounded wait
+ * that gave up) are reported by ctr_plan_check.  x and y must not overlap.
+ */
+ctr_status ctr_forward(ctr_plan_t plan, const void *x, const void *w_packed, const void *bias,
+                       void *y, void *stream);
+
+/*
+ * Synchronise stream, then read and clear the plan's device status word.  Returns CTR_OK,
+ * CTR_ERR_DEVICE_TIMEOUT when a kernel's bounded wait gave up since the last check (its
+ * output is then incomplete), or CTR_ERR_CUDA.
+ */
+ctr_status ctr_plan_check(ctr_plan_t plan, void *stream);
+
+/*
+ * Limit, in nanoseconds, of every bounded device-side wait of the tensor-core kernels
+ * (default 4e9).  A test hook: a tiny limit makes the waits give up on a healthy run, so
+ * the timeout path can be exercised without a fault.  Host only.
+ */
+ctr_status ctr_plan_set_wait_limit_ns(ctr_plan_t plan, uint64_t limit_ns);
+
+/*
+ * Measurement hook: when both are non-NULL, every later ctr_forward records the
+ * caller-owned CUDA events `before` and `after` (cudaEvent_t as void*) on its stream
+ * immediately before and after the plan's main kernel (the tensor-core GEMM on the polyphase
+ * and col2im paths, the gather kernel otherwise), so cudaEventElapsedTime gives that
+ * kernel's own duration.  Pass NULL, NULL to stop.  Host only; the events must outlive
+ * the calls that record them.
+ */
+ctr_status ctr_plan_set_timing_events(ctr_plan_t plan, void *before, void *after);
+
+/* Human-readable summary of the plan's path and tiling into buf (NUL-terminated). */
+ctr_status ctr_plan_describe(ctr_plan_t plan, char *buf, size_t len);
+
+/* Free the plan's host metadata and status word.  NULL is ignored.  Does not synchronise:
+ * call it only after the plan's work on the GPU has finished. */
+void ctr_plan_destroy(ctr_plan_t plan);
+
+/* Static description of a status code. */
+const char *ctr_status_string(ctr_status status);
+
+/* Number of GPU kernels this library has launched in this process (a monotonic counter
+ * for benchmarks and tests). */
+uint64_t ctr_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CTR_H */

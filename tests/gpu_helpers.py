@@ -1,0 +1,61 @@
+"""Helpers of the GPU tests: run the library through the C ABI on torch CUDA tensors, with
+NaN guard bands around the output, and compare with the oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import transposed_convolution_gb300 as ctr
+
+GUARD = 64  # elements of NaN before and after y (keeps 16-byte alignment for fp32 and bf16)
+
+
+def tdtype(dtype: str):
+    return torch.bfloat16 if dtype == "bf16" else torch.float32
+
+
+def to_dev(a, dtype: str):
+    if a is None:
+        return None
+    return torch.from_numpy(np.ascontiguousarray(np.asarray(a, dtype=np.float32))).to(
+        "cuda").to(tdtype(dtype)).contiguous()
+
+
+def run_plan(x, w, bias, stride, padding, output_padding, dtype="f32", slope=None,
+             path=ctr.CTR_PATH_AUTO, split_k=0, check_guards=True, expect_path=None):
+    """Run one ConvTranspose through the library.  x, w, bias: numpy arrays holding values of
+    the I/O dtype.  Returns (y as float64 numpy, plan description)."""
+    x = np.asarray(x)
+    ndim = x.ndim - 2
+    plan = ctr.Plan(x.shape[0], x.shape[1], w.shape[1], tuple(x.shape[2:]), tuple(w.shape[2:]),
+                    stride, padding, output_padding, dtype=tdtype(dtype), negative_slope=slope,
+                    path=path, split_k=split_k)
+    try:
+        if expect_path is not None:
+            assert plan.path == expect_path, plan.describe()
+        plan.prepack(to_dev(w, dtype))
+        n = int(np.prod(plan.out_shape))
+        buf = torch.full((n + 2 * GUARD,), float("nan"), dtype=tdtype(dtype), device="cuda")
+        y = buf[GUARD:GUARD + n].view(plan.out_shape)
+        plan.forward(to_dev(x, dtype), to_dev(bias, dtype), y=y)
+        plan.check()
+        if check_guards:
+            g = torch.cat([buf[:GUARD], buf[GUARD + n:]]).float().cpu().numpy()
+            assert np.all(np.isnan(g)), "library wrote outside y"
+        out = y.float().cpu().numpy().astype(np.float64)
+        return out, plan.describe()
+    finally:
+        plan.close()
+
+
+def reference(x, w, bias, stride, padding, output_padding, dtype="f32", slope=None):
+    """Oracle result rounded like the library's output: double sum + bias, then LeakyReLU,
+    then one rounding to the I/O dtype."""
+    y = oracle.conv_transpose(x, w, bias, stride, padding, output_padding)
+    if slope is not None:
+        y = oracle.leaky_relu(y, slope)
+    return oracle.round_bf16(y) if dtype == "bf16" else oracle.round_f32(y)
+
+
+TOL = {"f32": 1e-5, "bf16": 1e-2}

@@ -1,0 +1,135 @@
+"""The C ABI's host half, without a GPU: the library builds, loads and exports every symbol
+include/ctr.h declares; plan validation, output shapes, path choice and workspace sizing.
+No call here launches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ctr():
+    from transposed_convolution_gb300 import build
+    build.build()
+    import transposed_convolution_gb300 as t
+    t.load_library()
+    return t
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "ctr.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ctr_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("ctr_plan_create", "ctr_prepack_weight", "ctr_forward", "ctr_plan_destroy",
+                     "ctr_packed_weight_bytes", "ctr_workspace_bytes", "ctr_plan_bind_workspace",
+                     "ctr_plan_output_shape", "ctr_plan_check", "ctr_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(ctr):
+    raw = ctypes.CDLL(ctr.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(raw, name), "missing export " + name
+        assert name in ctr.SIGNATURES, "binding lacks " + name
+
+
+def _plan(ctr, *args, **kw):
+    return ctr.ctr_plan_create(*args, **kw)
+
+
+def test_output_shapes_and_paths_of_the_workloads(ctr):
+    import workloads
+    expect_path = {"tiny_1d_f32": ctr.CTR_PATH_GATHER}
+    for name, layers in workloads.WORKLOADS.items():
+        for layer in layers:
+            h = _plan(ctr, layer.ndim, layer.B, layer.C_in, layer.C_out, layer.in_sp, layer.kernel,
+                      layer.stride, layer.padding, layer.output_padding,
+                      ctr.CTR_BF16 if layer.dtype == "bf16" else ctr.CTR_F32)
+            try:
+                assert ctr.ctr_plan_output_shape(h, layer.ndim) == layer.out_sp
+                assert ctr.ctr_plan_get_path(h) == expect_path.get(name, ctr.CTR_PATH_POLYPHASE)
+                if ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_POLYPHASE:
+                    assert ctr.ctr_workspace_bytes(h) > 0
+                    assert ctr.ctr_packed_weight_bytes(h) > 0
+                assert "path=" in ctr.ctr_plan_describe(h)
+            finally:
+                ctr.ctr_plan_destroy(h)
+
+
+def test_col2im_chosen_when_kernel_not_multiple_of_stride(ctr):
+    h = _plan(ctr, 1, 2, 32, 32, [50], [3], [2], [1], [1], ctr.CTR_F32)
+    assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_COL2IM
+    ctr.ctr_plan_destroy(h)
+    h = _plan(ctr, 1, 2, 8, 16, [50], [3], [2], [1], [1], ctr.CTR_F32)   # C_in < 16
+    assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_GATHER
+    ctr.ctr_plan_destroy(h)
+
+
+@pytest.mark.parametrize("args", [
+    (3, 1, 4, 4, [8], [2], [2], [0], [0]),        # ndim
+    (1, -1, 4, 4, [8], [2], [2], [0], [0]),       # N < 0
+    (1, 1, 0, 4, [8], [2], [2], [0], [0]),        # C_in = 0
+    (1, 1, 4, 0, [8], [2], [2], [0], [0]),        # C_out = 0
+    (1, 1, 4, 4, [-1], [2], [2], [0], [0]),       # L_in < 0
+    (1, 1, 4, 4, [8], [0], [2], [0], [0]),        # k = 0
+    (1, 1, 4, 4, [8], [2], [0], [0], [0]),        # s = 0
+    (1, 1, 4, 4, [8], [2], [2], [-1], [0]),       # p < 0
+    (1, 1, 4, 4, [8], [2], [2], [0], [2]),        # op >= s
+    (1, 1, 4, 4, [1], [2], [2], [1], [0]),        # L_out = 0
+    (2, 1, 4, 4, [8, 8], [2, 2], [2, 2], [0, 0], [0, -1]),
+])
+def test_invalid_arguments_rejected(ctr, args):
+    with pytest.raises(ctr.CtrError) as e:
+        _plan(ctr, *args, dtype=ctr.CTR_F32)
+    assert e.value.status == ctr.CTR_ERR_INVALID_ARG
+
+
+def test_empty_input_is_a_valid_plan(ctr):
+    h = _plan(ctr, 1, 1, 4, 4, [0], [4], [2], [0], [0], ctr.CTR_F32)
+    assert ctr.ctr_plan_output_shape(h, 1) == (2,)
+    ctr.ctr_plan_destroy(h)
+
+
+def test_host_side_errors_without_gpu(ctr):
+    h = _plan(ctr, 1, 1, 64, 64, [100], [4], [2], [1], [0], ctr.CTR_F32)
+    try:
+        # forward before prepack: rejected before any CUDA call
+        st = ctr.lib.ctr_forward(h, ctypes.c_void_p(256), ctypes.c_void_p(256), None,
+                                 ctypes.c_void_p(256), None)
+        assert st == ctr.CTR_ERR_NOT_PREPARED
+        assert ctr.lib.ctr_plan_bind_workspace(h, ctypes.c_void_p(4096 + 16), 1 << 30) == \
+            ctr.CTR_ERR_MISALIGNED
+        assert ctr.lib.ctr_plan_bind_workspace(h, ctypes.c_void_p(4096), 16) == \
+            ctr.CTR_ERR_NO_WORKSPACE
+        assert ctr.lib.ctr_plan_set_path(h, 9, 0) == ctr.CTR_ERR_INVALID_ARG
+        assert ctr.lib.ctr_plan_set_activation(h, 7, 0.1) == ctr.CTR_ERR_INVALID_ARG
+        # forcing each path re-plans
+        for p in (ctr.CTR_PATH_GATHER, ctr.CTR_PATH_COL2IM, ctr.CTR_PATH_POLYPHASE):
+            ctr.ctr_plan_set_path(h, p, 0)
+            assert ctr.ctr_plan_get_path(h) == p
+        ctr.ctr_plan_set_path(h, ctr.CTR_PATH_POLYPHASE, 3)
+        assert "splits=3" in ctr.ctr_plan_describe(h)
+    finally:
+        ctr.ctr_plan_destroy(h)
+    for s in range(8):
+        assert ctr.ctr_status_string(s)
+    ctr.ctr_plan_destroy(None)
+
+
+def test_null_plan_queries(ctr):
+    assert ctr.lib.ctr_packed_weight_bytes(None) == 0
+    assert ctr.lib.ctr_workspace_bytes(None) == 0
+    assert ctr.lib.ctr_plan_get_path(None) == -1
+    assert ctr.lib.ctr_plan_create(None, 1, 1, 1, 1, None, None, None, None, None, 0) == \
+        ctr.CTR_ERR_INVALID_ARG
+
+
+def test_no_kernel_launched_by_host_calls(ctr):
+    assert ctr.ctr_launch_count() == 0

@@ -1,0 +1,357 @@
+"""GB300 (sm_103a) dense transposed convolution: Python binding of the C ABI in ``include/ctr.h``.
+
+The binding only marshals arguments: every step of the computation runs in the CUDA kernels
+of ``_build/libctr.so``.  PyTorch provides device memory and streams.  There is no CPU or
+PyTorch fallback: if the library has not been built the first call raises ImportError, and
+any non-OK status from the library raises ``CtrError``.
+
+Low level (same names as the C ABI): ``ctr_plan_create``, ``ctr_plan_set_activation``,
+``ctr_plan_set_path``, ``ctr_plan_get_path``, ``ctr_plan_output_shape``,
+``ctr_packed_weight_bytes``, ``ctr_workspace_bytes``, ``ctr_plan_bind_workspace``,
+``ctr_prepack_weight``, ``ctr_forward``, ``ctr_plan_check``, ``ctr_plan_set_wait_limit_ns``,
+``ctr_plan_set_timing_events``, ``ctr_plan_describe``, ``ctr_plan_destroy``,
+``ctr_status_string``, ``ctr_launch_count``.
+
+High level: ``Plan`` (a plan with its packed weight and workspace held as torch tensors) and
+``conv_transpose(x, w, bias, stride, padding, output_padding, negative_slope)``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB as _LIB_PATH
+
+CTR_OK = 0
+CTR_ERR_INVALID_ARG = 1
+CTR_ERR_UNSUPPORTED = 2
+CTR_ERR_MISALIGNED = 3
+CTR_ERR_NO_WORKSPACE = 4
+CTR_ERR_CUDA = 5
+CTR_ERR_DEVICE_TIMEOUT = 6
+CTR_ERR_NOT_PREPARED = 7
+
+CTR_F32 = 0
+CTR_BF16 = 1
+CTR_ACT_NONE = 0
+CTR_ACT_LEAKY_RELU = 1
+CTR_PATH_AUTO = 0
+CTR_PATH_POLYPHASE = 1
+CTR_PATH_COL2IM = 2
+CTR_PATH_GATHER = 3
+PATH_NAMES = {CTR_PATH_POLYPHASE: "polyphase", CTR_PATH_COL2IM: "col2im", CTR_PATH_GATHER: "gather"}
+
+# Every symbol include/ctr.h declares, with (restype, argtypes).
+_vp = ctypes.c_void_p
+_i64p = ctypes.POINTER(ctypes.c_int64)
+SIGNATURES = {
+    "ctr_plan_create": (ctypes.c_int, [ctypes.POINTER(_vp), ctypes.c_int, ctypes.c_int64,
+                                       ctypes.c_int64, ctypes.c_int64, _i64p, _i64p, _i64p, _i64p,
+                                       _i64p, ctypes.c_int]),
+    "ctr_plan_set_activation": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_float]),
+    "ctr_plan_set_path": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int]),
+    "ctr_plan_get_path": (ctypes.c_int, [_vp]),
+    "ctr_plan_output_shape": (ctypes.c_int, [_vp, _i64p]),
+    "ctr_packed_weight_bytes": (ctypes.c_size_t, [_vp]),
+    "ctr_workspace_bytes": (ctypes.c_size_t, [_vp]),
+    "ctr_plan_bind_workspace": (ctypes.c_int, [_vp, _vp, ctypes.c_size_t]),
+    "ctr_prepack_weight": (ctypes.c_int, [_vp, _vp, _vp, _vp]),
+    "ctr_forward": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp]),
+    "ctr_plan_check": (ctypes.c_int, [_vp, _vp]),
+    "ctr_plan_set_wait_limit_ns": (ctypes.c_int, [_vp, ctypes.c_uint64]),
+    "ctr_plan_set_timing_events": (ctypes.c_int, [_vp, _vp, _vp]),
+    "ctr_plan_describe": (ctypes.c_int, [_vp, ctypes.c_char_p, ctypes.c_size_t]),
+    "ctr_plan_destroy": (None, [_vp]),
+    "ctr_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "ctr_launch_count": (ctypes.c_uint64, []),
+}
+
+
+class CtrError(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (where or "ctr", status_string(status), status))
+
+
+_lib = None
+LIB_PATH = _LIB_PATH
+
+
+def load_library():
+    """Load ``_build/libctr.so`` once.  Raises ImportError when it has not been built: there
+    is no fallback implementation."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise ImportError(
+                "transposed_convolution_gb300: %s is missing; build it first with "
+                "`python -m transposed_convolution_gb300.build` (nvcc, sm_103a)" % _LIB_PATH)
+        lib = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+class _LazyLib:
+    def __getattr__(self, name):
+        return getattr(load_library(), name)
+
+
+lib = _LazyLib()
+
+
+def status_string(status: int) -> str:
+    return lib.ctr_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != CTR_OK:
+        raise CtrError(status, where)
+
+
+def _arr(vals):
+    return (ctypes.c_int64 * len(vals))(*[int(v) for v in vals])
+
+
+# ------------------------------------------------------------------ C-ABI names
+
+ctr_status_string = status_string
+
+
+def ctr_launch_count() -> int:
+    return int(lib.ctr_launch_count())
+
+
+def ctr_plan_create(ndim, N, C_in, C_out, in_spatial, kernel, stride, padding,
+                    output_padding=None, dtype=CTR_F32):
+    """Returns a plan handle (int).  Raises CtrError on a non-OK status."""
+    h = _vp()
+    op = _arr(output_padding) if output_padding is not None else None
+    st = lib.ctr_plan_create(ctypes.byref(h), int(ndim), int(N), int(C_in), int(C_out),
+                             _arr(in_spatial), _arr(kernel), _arr(stride), _arr(padding), op,
+                             int(dtype))
+    _check(st, "ctr_plan_create")
+    return h.value
+
+
+def ctr_plan_set_activation(plan, act, negative_slope=0.0):
+    _check(lib.ctr_plan_set_activation(plan, int(act), float(negative_slope)),
+           "ctr_plan_set_activation")
+
+
+def ctr_plan_set_path(plan, path, split_k=0):
+    _check(lib.ctr_plan_set_path(plan, int(path), int(split_k)), "ctr_plan_set_path")
+
+
+def ctr_plan_get_path(plan) -> int:
+    return int(lib.ctr_plan_get_path(plan))
+
+
+def ctr_plan_output_shape(plan, ndim):
+    out = (ctypes.c_int64 * ndim)()
+    _check(lib.ctr_plan_output_shape(plan, out), "ctr_plan_output_shape")
+    return tuple(int(v) for v in out)
+
+
+def ctr_packed_weight_bytes(plan) -> int:
+    return int(lib.ctr_packed_weight_bytes(plan))
+
+
+def ctr_workspace_bytes(plan) -> int:
+    return int(lib.ctr_workspace_bytes(plan))
+
+
+def ctr_plan_bind_workspace(plan, ptr, nbytes):
+    _check(lib.ctr_plan_bind_workspace(plan, ptr, int(nbytes)), "ctr_plan_bind_workspace")
+
+
+def ctr_prepack_weight(plan, w_ptr, w_packed_ptr, stream):
+    _check(lib.ctr_prepack_weight(plan, w_ptr, w_packed_ptr, stream), "ctr_prepack_weight")
+
+
+def ctr_forward(plan, x_ptr, w_packed_ptr, bias_ptr, y_ptr, stream):
+    _check(lib.ctr_forward(plan, x_ptr, w_packed_ptr, bias_ptr, y_ptr, stream), "ctr_forward")
+
+
+def ctr_plan_check(plan, stream):
+    _check(lib.ctr_plan_check(plan, stream), "ctr_plan_check")
+
+
+def ctr_plan_set_wait_limit_ns(plan, limit_ns):
+    _check(lib.ctr_plan_set_wait_limit_ns(plan, int(limit_ns)), "ctr_plan_set_wait_limit_ns")
+
+
+def ctr_plan_set_timing_events(plan, before, after):
+    """before/after: cudaEvent_t handles (ints) or None."""
+    _check(lib.ctr_plan_set_timing_events(plan, before, after), "ctr_plan_set_timing_events")
+
+
+def ctr_plan_describe(plan) -> str:
+    buf = ctypes.create_string_buffer(512)
+    _check(lib.ctr_plan_describe(plan, buf, 512), "ctr_plan_describe")
+    return buf.value.decode()
+
+
+def ctr_plan_destroy(plan):
+    lib.ctr_plan_destroy(plan)
+
+
+# ------------------------------------------------------------------ torch-level helpers
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(dt):
+    torch = _torch()
+    if dt == torch.float32:
+        return CTR_F32
+    if dt == torch.bfloat16:
+        return CTR_BF16
+    raise TypeError("transposed_convolution_gb300 supports float32 and bfloat16, got %s" % dt)
+
+
+def _stream_ptr(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _tuple(v, n):
+    if isinstance(v, int):
+        return (v,) * n
+    v = tuple(int(a) for a in v)
+    if len(v) != n:
+        raise ValueError("expected %d values, got %d" % (n, len(v)))
+    return v
+
+
+class Plan:
+    """A ConvTranspose plan with its packed weight and workspace as device tensors."""
+
+    def __init__(self, N, C_in, C_out, in_spatial, kernel, stride=1, padding=0,
+                 output_padding=0, dtype=None, negative_slope=None, path=CTR_PATH_AUTO,
+                 split_k=0, device=None):
+        torch = _torch()
+        self.ndim = len(in_spatial)
+        self.dtype = dtype if dtype is not None else torch.float32
+        self.device = torch.device(device if device is not None else "cuda")
+        self.N, self.C_in, self.C_out = int(N), int(C_in), int(C_out)
+        self.in_spatial = tuple(int(v) for v in in_spatial)
+        self.kernel = _tuple(kernel, self.ndim)
+        self.stride = _tuple(stride, self.ndim)
+        self.padding = _tuple(padding, self.ndim)
+        self.output_padding = _tuple(output_padding, self.ndim)
+        self.handle = ctr_plan_create(self.ndim, self.N, self.C_in, self.C_out, self.in_spatial,
+                                      self.kernel, self.stride, self.padding,
+                                      self.output_padding, _dtype_code(self.dtype))
+        try:
+            if negative_slope is not None:
+                ctr_plan_set_activation(self.handle, CTR_ACT_LEAKY_RELU, negative_slope)
+            if path != CTR_PATH_AUTO or split_k:
+                ctr_plan_set_path(self.handle, path, split_k)
+            self.out_spatial = ctr_plan_output_shape(self.handle, self.ndim)
+            self.path = ctr_plan_get_path(self.handle)
+            self.packed_bytes = ctr_packed_weight_bytes(self.handle)
+            self.workspace_bytes = ctr_workspace_bytes(self.handle)
+            self.workspace = None
+            if self.workspace_bytes:
+                self.workspace = torch.empty(self.workspace_bytes, dtype=torch.uint8,
+                                             device=self.device)
+                ctr_plan_bind_workspace(self.handle, _ptr(self.workspace), self.workspace_bytes)
+        except Exception:
+            ctr_plan_destroy(self.handle)
+            self.handle = None
+            raise
+        self.w_packed = None
+
+    @property
+    def out_shape(self):
+        return (self.N, self.C_out) + tuple(self.out_spatial)
+
+    def describe(self) -> str:
+        return ctr_plan_describe(self.handle)
+
+    def prepack(self, w, stream=None):
+        """Pack the weight [C_in, C_out, k...] (device, plan dtype) into self.w_packed."""
+        torch = _torch()
+        w = self._checked(w, (self.C_in, self.C_out) + self.kernel, "w")
+        self.w_packed = torch.empty(max(self.packed_bytes, 16), dtype=torch.uint8,
+                                    device=self.device)
+        ctr_prepack_weight(self.handle, _ptr(w), _ptr(self.w_packed), _stream_ptr(stream))
+        return self.w_packed
+
+    def forward(self, x, bias=None, y=None, stream=None):
+        torch = _torch()
+        if self.w_packed is None:
+            raise RuntimeError("Plan.forward before Plan.prepack")
+        x = self._checked(x, (self.N, self.C_in) + self.in_spatial, "x")
+        if bias is not None:
+            bias = self._checked(bias, (self.C_out,), "bias")
+        if y is None:
+            y = torch.empty(self.out_shape, dtype=self.dtype, device=self.device)
+        else:
+            y = self._checked(y, self.out_shape, "y")
+        ctr_forward(self.handle, _ptr(x), _ptr(self.w_packed), _ptr(bias), _ptr(y),
+                    _stream_ptr(stream))
+        return y
+
+    def check(self, stream=None):
+        ctr_plan_check(self.handle, _stream_ptr(stream))
+
+    def set_wait_limit_ns(self, ns):
+        ctr_plan_set_wait_limit_ns(self.handle, ns)
+
+    def _checked(self, t, shape, name):
+        if tuple(t.shape) != tuple(shape):
+            raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+        if t.dtype != self.dtype:
+            raise TypeError("%s has dtype %s, expected %s" % (name, t.dtype, self.dtype))
+        if t.device.type != "cuda":
+            raise ValueError("%s must be a CUDA tensor" % name)
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % name)
+        return t
+
+    def close(self):
+        if getattr(self, "handle", None):
+            ctr_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+_plan_cache = {}
+
+
+def conv_transpose(x, w, bias=None, stride=1, padding=0, output_padding=0, negative_slope=None,
+                   path=CTR_PATH_AUTO, split_k=0):
+    """ConvTranspose1d/2d of torch CUDA tensors (float32 or bfloat16), like
+    torch.nn.functional.conv_transpose{1,2}d with groups = 1 and dilation = 1, plus an
+    optional fused LeakyReLU.  Plans and packed weights are cached per (shapes, weight)."""
+    ndim = x.dim() - 2
+    key = (tuple(x.shape), tuple(w.shape), x.dtype, str(x.device), w.data_ptr(), w._version,
+           _tuple(stride, ndim), _tuple(padding, ndim), _tuple(output_padding, ndim),
+           negative_slope, path, split_k)
+    plan = _plan_cache.get(key)
+    if plan is None:
+        if len(_plan_cache) > 64:
+            _plan_cache.clear()
+        plan = Plan(x.shape[0], x.shape[1], w.shape[1], tuple(x.shape[2:]), tuple(w.shape[2:]),
+                    stride, padding, output_padding, dtype=x.dtype, negative_slope=negative_slope,
+                    path=path, split_k=split_k, device=x.device)
+        plan.prepack(w.contiguous())
+        _plan_cache[key] = plan
+    return plan.forward(x.contiguous(), None if bias is None else bias.contiguous())

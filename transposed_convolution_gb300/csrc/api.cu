@@ -1,0 +1,532 @@
+// api.cu -- the library's C ABI: plan validation, path and tile choice, workspace layout,
+// tensor-map encoding and the launch sequence of ctr_forward.
+//
+// Path choice follows the three lowerings on the source pages:
+//   - polyphase ("[XNNPACK] Lower dense transposed convs as one polyphase conv + depth to
+//     space", Summary): when every kernel size is a multiple of its stride and the phase
+//     GEMM fills at least a 64-row MMA with K >= 16;
+//   - GEMM + col2im ("[WebGPU] optimizations for audio models", ConvTranspose commit): for
+//     group-1 convolutions with at least 16 input channels whose kernel is not a multiple
+//     of the stride;
+//   - the direct gather kernel ("[ExecuTorch][WebGPU] Add optimized conv2d op",
+//     Implementation) for everything else, i.e. tiny channel counts.
+#include <algorithm>
+#include <atomic>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <cudaTypedefs.h>
+
+#include "ctr_internal.h"
+
+using ctr::EpiParams;
+using ctr::GemmParams;
+using ctr::Prec;
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t next_pow2(int64_t v) {
+    int64_t r = 1;
+    while (r < v) r <<= 1;
+    return r;
+}
+
+int query_num_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 152;
+    }
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 152;
+    }
+    return n > 0 ? n : 152;
+}
+
+Prec prec_of(const ctr_plan_s *pl) { return pl->dtype == CTR_BF16 ? Prec::BF16 : Prec::TF32x3; }
+int esize_io(const ctr_plan_s *pl) { return pl->dtype == CTR_BF16 ? 2 : 4; }
+// Elements of one 128-byte K slice in the GEMM operands.
+int bk_elems(const ctr_plan_s *pl) { return pl->dtype == CTR_BF16 ? 64 : 32; }
+// Bytes per element of one GEMM operand plane, and number of planes (hi/lo for 3xTF32).
+int op_esize(const ctr_plan_s *pl) { return pl->dtype == CTR_BF16 ? 2 : 4; }
+int op_planes(const ctr_plan_s *pl) { return pl->dtype == CTR_BF16 ? 1 : 2; }
+
+bool is_tc_path(int path) { return path == CTR_PATH_POLYPHASE || path == CTR_PATH_COL2IM; }
+
+// Estimated clocks of one K slice of a 128 x BN tile on one SM (tensor-pipe time).
+double slice_clocks(Prec prec, int bn) { return prec == Prec::TF32x3 ? 6.0 * bn : 2.0 * bn; }
+
+// K slices per tensor-core accumulation group in 3xTF32 mode (256 fp32 K elements).  The
+// tensor core's fp32 accumulation over a long K chain drifts well beyond fp32 summation
+// with round-to-nearest (measured on GB300: rel_l2 2.3e-5 over 3300-element chains), so
+// the kernel moves the partial sum out of TMEM every group and adds it in registers with
+// round-to-nearest; the drift then scales with the group length only.
+constexpr int kTf32Group = 8;
+constexpr int kNoGroup = 1 << 30;
+
+// Choose the column tile and the split-K factor: fewest estimated clocks over
+// BN in {128, 256} and splits in 1..16, counting whole waves of tiles over the SMs and
+// the extra pass that sums split-K partials.  Grouped accumulation needs BN = 128 (the
+// running sums of a 128-column row fit in one thread's registers).
+int tf32_group() {
+    // Diagnostic override of the group length (slices); 0 or negative disables grouping.
+    const char *e = std::getenv("CTR_TF32_GROUP");
+    if (!e || !*e) return kTf32Group;
+    const int v = std::atoi(e);
+    return v > 0 ? v : kNoGroup;
+}
+
+void choose_tiling(ctr_plan_s *pl) {
+    const Prec prec = prec_of(pl);
+    const int group = prec == Prec::TF32x3 ? tf32_group() : kNoGroup;
+    const int kb_total = (int)(pl->K_total * op_esize(pl) / ctr::kBKBytes);
+    const int num_m = (int)(pl->M_pad / ctr::kBM);
+    double best = 1e300;
+    int best_bn = 128, best_sp = 1;
+    // A forced split-K factor is clamped to the number of K slices.
+    const int forced = pl->forced_split > 0 ? std::min(pl->forced_split, kb_total) : 0;
+    for (int bn : {128, 256}) {
+        const int64_t num_n = std::max<int64_t>(1, ceil_div(pl->N_total, bn));
+        for (int sp = 1; sp <= 16; ++sp) {
+            if (forced > 0 && sp != forced) continue;
+            if (sp > kb_total) break;
+            if (sp > 1 && forced == 0 && kb_total / sp < 4) break;
+            const int64_t tiles = (int64_t)num_m * num_n * sp;
+            const int64_t waves = ceil_div(tiles, pl->num_sms);
+            const double kbs = (double)ceil_div(kb_total, sp);
+            if (bn == 256 && kbs > group) continue;
+            double t = (double)waves * (kbs + 6.0) * slice_clocks(prec, bn);
+            if (sp > 1 || pl->path == CTR_PATH_COL2IM) {
+                // partials written once and read once, ~3.5 KB per clock for the whole GPU
+                t += (double)(sp + 1) * pl->M_pad * num_n * bn * 4.0 / 3500.0;
+            }
+            if (t < best * 0.98) {
+                best = t;
+                best_bn = bn;
+                best_sp = sp;
+            }
+        }
+    }
+    pl->block_n = best_bn;
+    pl->splits = best_sp;
+    pl->kb_group = best_bn == 128 ? group : kNoGroup;
+    pl->num_m_tiles = num_m;
+    pl->num_n_tiles = (int)std::max<int64_t>(1, ceil_div(pl->N_total, best_bn));
+    pl->num_tiles = (int64_t)pl->num_m_tiles * pl->num_n_tiles * pl->splits;
+}
+
+// Derive the GEMM geometry, tiling, packed size and workspace layout from the path.
+void layout_plan(ctr_plan_s *pl) {
+    pl->packed_bytes = 0;
+    pl->ws_bytes_needed = 0;
+    pl->ws_off_stage = pl->ws_stage_bytes = pl->ws_off_raw = pl->ws_raw_bytes = 0;
+    pl->splits = 1;
+    pl->block_n = 0;
+    pl->num_tiles = 0;
+    if (pl->path == CTR_PATH_GATHER) {
+        pl->packed_bytes = (size_t)(pl->C_in * pl->C_out * pl->k[0] * pl->k[1]) * esize_io(pl);
+        pl->S = pl->S_pad = 0;
+        return;
+    }
+    const int bk = bk_elems(pl);
+    pl->C_in_pad = round_up(pl->C_in, bk);
+    if (pl->path == CTR_PATH_POLYPHASE) {
+        for (int d = 0; d < 2; ++d) {
+            pl->m[d] = ceil_div(pl->k[d], pl->s[d]);
+            pl->Qv[d] = ceil_div(pl->out[d] + pl->p[d], pl->s[d]);
+            pl->P[d] = std::max(pl->in[d] + 2 * (pl->m[d] - 1), pl->Qv[d] + pl->m[d] - 1);
+        }
+        pl->S = (int)(pl->s[0] * pl->s[1]);
+    } else {  // col2im: plain GEMM over input positions, rows (oc, tap)
+        for (int d = 0; d < 2; ++d) {
+            pl->m[d] = 1;
+            pl->Qv[d] = pl->in[d];
+            pl->P[d] = pl->in[d];
+        }
+        pl->S = (int)(pl->k[0] * pl->k[1]);
+    }
+    pl->S_pad = (int)(pl->S <= ctr::kBM ? next_pow2(pl->S) : round_up(pl->S, ctr::kBM));
+    pl->M_rows = pl->C_out * pl->S_pad;
+    pl->M_pad = round_up(pl->M_rows, ctr::kBM);
+    pl->K_total = pl->m[0] * pl->m[1] * pl->C_in_pad;
+    pl->N_total = pl->B * pl->P[0] * pl->P[1];
+    choose_tiling(pl);
+    pl->packed_bytes = (size_t)pl->M_pad * pl->K_total * op_esize(pl) * op_planes(pl);
+    pl->ws_off_stage = 0;
+    pl->ws_stage_bytes = (size_t)pl->N_total * pl->C_in_pad * op_esize(pl) * op_planes(pl);
+    size_t off = align256(pl->ws_stage_bytes);
+    if (pl->path == CTR_PATH_COL2IM || pl->splits > 1) {
+        pl->ws_off_raw = off;
+        pl->ws_raw_bytes = (size_t)pl->splits * pl->M_pad *
+                           ((size_t)pl->num_n_tiles * pl->block_n) * sizeof(float);
+        off = align256(off + pl->ws_raw_bytes);
+    }
+    pl->ws_bytes_needed = (pl->ws_stage_bytes || pl->ws_raw_bytes) ? off : 0;
+}
+
+int choose_path(const ctr_plan_s *pl) {
+    if (pl->forced_path != CTR_PATH_AUTO) return pl->forced_path;
+    const bool kdiv = (pl->k[0] % pl->s[0] == 0) && (pl->k[1] % pl->s[1] == 0);
+    const int64_t S = pl->s[0] * pl->s[1];
+    const int64_t mprod = ceil_div(pl->k[0], pl->s[0]) * ceil_div(pl->k[1], pl->s[1]);
+    const int64_t T = pl->k[0] * pl->k[1];
+    if (kdiv) return (S * pl->C_out >= 64 && pl->C_in * mprod >= 16) ? CTR_PATH_POLYPHASE
+                                                                    : CTR_PATH_GATHER;
+    return (pl->C_in >= 16 && T * pl->C_out >= 64) ? CTR_PATH_COL2IM : CTR_PATH_GATHER;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
+
+// 2-D tiled tensor map over a row-major [rows][inner] matrix, box [box_rows][128 bytes],
+// 128-byte swizzle (the K-major SWIZZLE_128B operand layout of tcgen05.mma), zero fill.
+bool encode_2d(CUtensorMap *map, const void *base, bool bf16, uint64_t inner, uint64_t rows,
+               uint32_t box_rows) {
+    auto fn = get_encode_fn();
+    if (!fn) return false;
+    const uint32_t es = bf16 ? 2 : 4;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner * es};
+    cuuint32_t box[2] = {(cuuint32_t)(ctr::kBKBytes / es), box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                    2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+EpiParams make_epi(const ctr_plan_s *pl, const void *bias, void *y) {
+    EpiParams e;
+    e.S = pl->S;
+    e.S_pad = pl->S_pad;
+    e.sy = (int)pl->s[0];
+    e.sx = (int)pl->s[1];
+    e.py = (int)pl->p[0];
+    e.px = (int)pl->p[1];
+    e.Py = pl->P[0];
+    e.Px = pl->P[1];
+    e.Qvy = pl->Qv[0];
+    e.Qvx = pl->Qv[1];
+    e.B = pl->B;
+    e.C_out = pl->C_out;
+    e.Hout = pl->out[0];
+    e.Wout = pl->out[1];
+    e.bias = bias;
+    e.y = y;
+    e.out_bf16 = pl->dtype == CTR_BF16 ? 1 : 0;
+    e.act = pl->act;
+    e.slope = pl->slope;
+    return e;
+}
+
+}  // namespace
+
+namespace ctr {
+void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+}  // namespace ctr
+
+extern "C" {
+
+const char *ctr_status_string(ctr_status s) {
+    switch (s) {
+        case CTR_OK: return "ok";
+        case CTR_ERR_INVALID_ARG: return "invalid argument";
+        case CTR_ERR_UNSUPPORTED: return "unsupported configuration";
+        case CTR_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case CTR_ERR_NO_WORKSPACE: return "workspace unbound or too small";
+        case CTR_ERR_CUDA: return "CUDA error";
+        case CTR_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait gave up";
+        case CTR_ERR_NOT_PREPARED: return "plan used before ctr_prepack_weight";
+    }
+    return "unknown status";
+}
+
+uint64_t ctr_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+ctr_status ctr_plan_create(ctr_plan_t *out, int ndim, int64_t N, int64_t C_in, int64_t C_out,
+                           const int64_t *in_spatial, const int64_t *kernel,
+                           const int64_t *stride, const int64_t *padding,
+                           const int64_t *output_padding, int dtype) {
+    if (!out) return CTR_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (ndim != 1 && ndim != 2) return CTR_ERR_INVALID_ARG;
+    if (!in_spatial || !kernel || !stride || !padding) return CTR_ERR_INVALID_ARG;
+    if (N < 0 || C_in < 1 || C_out < 1) return CTR_ERR_INVALID_ARG;
+    if (dtype != CTR_F32 && dtype != CTR_BF16) return CTR_ERR_INVALID_ARG;
+    const int64_t kLim = (int64_t)1 << 31;
+    if (N >= kLim || C_in >= kLim || C_out >= kLim) return CTR_ERR_INVALID_ARG;
+
+    ctr_plan_s *pl = new (std::nothrow) ctr_plan_s();
+    if (!pl) return CTR_ERR_INVALID_ARG;
+    pl->ndim = ndim;
+    pl->B = N;
+    pl->C_in = C_in;
+    pl->C_out = C_out;
+    pl->dtype = dtype;
+    pl->act = CTR_ACT_NONE;
+    pl->slope = 0.0f;
+    pl->forced_path = CTR_PATH_AUTO;
+    pl->forced_split = 0;
+    pl->wait_limit_ns = 4000000000ull;
+    // Unit leading dimension for 1-D.
+    pl->in[0] = 1; pl->k[0] = 1; pl->s[0] = 1; pl->p[0] = 0; pl->op[0] = 0;
+    for (int d = 0; d < ndim; ++d) {
+        const int dd = d + (2 - ndim);
+        pl->in[dd] = in_spatial[d];
+        pl->k[dd] = kernel[d];
+        pl->s[dd] = stride[d];
+        pl->p[dd] = padding[d];
+        pl->op[dd] = output_padding ? output_padding[d] : 0;
+    }
+    int64_t total_out = N * C_out, total_in = N * C_in, total_w = C_in * C_out;
+    for (int d = 0; d < 2; ++d) {
+        const bool ok = pl->in[d] >= 0 && pl->in[d] < kLim && pl->k[d] >= 1 &&
+                        pl->k[d] < kLim && pl->s[d] >= 1 && pl->s[d] < kLim && pl->p[d] >= 0 &&
+                        pl->p[d] < kLim && pl->op[d] >= 0 && pl->op[d] < pl->s[d];
+        if (!ok) { delete pl; return CTR_ERR_INVALID_ARG; }
+        pl->out[d] = (pl->in[d] - 1) * pl->s[d] - 2 * pl->p[d] + pl->k[d] + pl->op[d];
+        if (pl->out[d] < 1 || pl->out[d] >= kLim) { delete pl; return CTR_ERR_INVALID_ARG; }
+        total_out *= pl->out[d];
+        total_in *= std::max<int64_t>(pl->in[d], 1);
+        total_w *= pl->k[d];
+        if (total_out >= ((int64_t)1 << 46) || total_in >= ((int64_t)1 << 46) ||
+            total_w >= ((int64_t)1 << 46)) {
+            delete pl;
+            return CTR_ERR_INVALID_ARG;
+        }
+    }
+    pl->num_sms = query_num_sms();
+    pl->path = choose_path(pl);
+    layout_plan(pl);
+    *out = pl;
+    return CTR_OK;
+}
+
+ctr_status ctr_plan_set_activation(ctr_plan_t pl, int act, float slope) {
+    if (!pl || (act != CTR_ACT_NONE && act != CTR_ACT_LEAKY_RELU)) return CTR_ERR_INVALID_ARG;
+    pl->act = act;
+    pl->slope = slope;
+    return CTR_OK;
+}
+
+ctr_status ctr_plan_set_path(ctr_plan_t pl, int path, int split_k) {
+    if (!pl || path < CTR_PATH_AUTO || path > CTR_PATH_GATHER || split_k < 0 || split_k > 16)
+        return CTR_ERR_INVALID_ARG;
+    if (pl->prepared) return CTR_ERR_INVALID_ARG;
+    pl->forced_path = path;
+    pl->forced_split = split_k;
+    pl->path = choose_path(pl);
+    layout_plan(pl);
+    return CTR_OK;
+}
+
+int ctr_plan_get_path(ctr_plan_t pl) { return pl ? pl->path : -1; }
+
+ctr_status ctr_plan_output_shape(ctr_plan_t pl, int64_t *out_spatial) {
+    if (!pl || !out_spatial) return CTR_ERR_INVALID_ARG;
+    for (int d = 0; d < pl->ndim; ++d) out_spatial[d] = pl->out[d + (2 - pl->ndim)];
+    return CTR_OK;
+}
+
+size_t ctr_packed_weight_bytes(ctr_plan_t pl) { return pl ? pl->packed_bytes : 0; }
+size_t ctr_workspace_bytes(ctr_plan_t pl) { return pl ? pl->ws_bytes_needed : 0; }
+
+ctr_status ctr_plan_bind_workspace(ctr_plan_t pl, void *ptr, size_t bytes) {
+    if (!pl) return CTR_ERR_INVALID_ARG;
+    if (ptr == nullptr && bytes != 0) return CTR_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(ptr) & 255u) != 0) return CTR_ERR_MISALIGNED;
+    if (bytes < pl->ws_bytes_needed) return CTR_ERR_NO_WORKSPACE;
+    pl->ws = ptr;
+    pl->ws_bytes = bytes;
+    return CTR_OK;
+}
+
+ctr_status ctr_plan_set_wait_limit_ns(ctr_plan_t pl, uint64_t limit_ns) {
+    if (!pl) return CTR_ERR_INVALID_ARG;
+    pl->wait_limit_ns = limit_ns;
+    return CTR_OK;
+}
+
+ctr_status ctr_plan_set_timing_events(ctr_plan_t pl, void *before, void *after) {
+    if (!pl || (before == nullptr) != (after == nullptr)) return CTR_ERR_INVALID_ARG;
+    pl->ev_before = static_cast<cudaEvent_t>(before);
+    pl->ev_after = static_cast<cudaEvent_t>(after);
+    return CTR_OK;
+}
+
+ctr_status ctr_plan_describe(ctr_plan_t pl, char *buf, size_t len) {
+    if (!pl || !buf || len == 0) return CTR_ERR_INVALID_ARG;
+    const char *pname = pl->path == CTR_PATH_POLYPHASE ? "polyphase"
+                        : pl->path == CTR_PATH_COL2IM  ? "col2im"
+                                                       : "gather";
+    if (is_tc_path(pl->path)) {
+        snprintf(buf, len,
+                 "path=%s prec=%s M=%lld(pad %lld, %d tiles) N=%lld(BN %d, %d tiles) "
+                 "K=%lld splits=%d group=%d tiles=%lld sms=%d S=%d/%d taps=%lldx%lld "
+                 "pitch=%lldx%lld packed=%zu ws=%zu",
+                 pname, pl->dtype == CTR_BF16 ? "bf16" : "3xtf32", (long long)pl->M_rows,
+                 (long long)pl->M_pad, pl->num_m_tiles, (long long)pl->N_total, pl->block_n,
+                 pl->num_n_tiles, (long long)pl->K_total, pl->splits,
+                 pl->kb_group == kNoGroup ? 0 : pl->kb_group, (long long)pl->num_tiles,
+                 pl->num_sms, pl->S, pl->S_pad, (long long)pl->m[0], (long long)pl->m[1],
+                 (long long)pl->P[0], (long long)pl->P[1], pl->packed_bytes,
+                 pl->ws_bytes_needed);
+    } else {
+        snprintf(buf, len, "path=%s dtype=%s packed=%zu ws=0", pname,
+                 pl->dtype == CTR_BF16 ? "bf16" : "f32", pl->packed_bytes);
+    }
+    return CTR_OK;
+}
+
+ctr_status ctr_prepack_weight(ctr_plan_t pl, const void *w, void *w_packed, void *stream) {
+    if (!pl || !w || !w_packed) return CTR_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(w_packed)) return CTR_ERR_MISALIGNED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (!pl->d_status) {
+        if (cudaGetDevice(&pl->status_device) != cudaSuccess) return CTR_ERR_CUDA;
+        if (cudaMalloc(&pl->d_status, sizeof(uint32_t)) != cudaSuccess) {
+            pl->d_status = nullptr;
+            return CTR_ERR_CUDA;
+        }
+        if (cudaMemset(pl->d_status, 0, sizeof(uint32_t)) != cudaSuccess) return CTR_ERR_CUDA;
+    }
+    cudaError_t e = pl->path == CTR_PATH_GATHER ? ctr::launch_copy_weight(pl, w, w_packed, st)
+                                                : ctr::launch_prepack(pl, w, w_packed, st);
+    if (e != cudaSuccess) return CTR_ERR_CUDA;
+    pl->prepared = 1;
+    return CTR_OK;
+}
+
+ctr_status ctr_forward(ctr_plan_t pl, const void *x, const void *w_packed, const void *bias,
+                       void *y, void *stream) {
+    if (!pl) return CTR_ERR_INVALID_ARG;
+    if (!pl->prepared) return CTR_ERR_NOT_PREPARED;
+    if (!w_packed || !y || (!x && pl->B * pl->C_in * pl->in[0] * pl->in[1] > 0))
+        return CTR_ERR_INVALID_ARG;
+    if ((x && !aligned16(x)) || !aligned16(w_packed) || !aligned16(y) ||
+        (bias && !aligned16(bias)))
+        return CTR_ERR_MISALIGNED;
+    if (pl->ws_bytes_needed > 0 && (!pl->ws || pl->ws_bytes < pl->ws_bytes_needed))
+        return CTR_ERR_NO_WORKSPACE;
+    if (pl->B == 0) return CTR_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    const bool timed = pl->ev_before != nullptr;
+    if (pl->path == CTR_PATH_GATHER) {
+        if (timed && cudaEventRecord(pl->ev_before, st) != cudaSuccess) return CTR_ERR_CUDA;
+        if (ctr::launch_gather(pl, x, w_packed, bias, y, st) != cudaSuccess) return CTR_ERR_CUDA;
+        if (timed && cudaEventRecord(pl->ev_after, st) != cudaSuccess) return CTR_ERR_CUDA;
+        return CTR_OK;
+    }
+    if (pl->N_total == 0) {  // empty input on the col2im path: y = bias or zeros
+        return ctr::launch_fill_bias(pl, bias, y, st) == cudaSuccess ? CTR_OK : CTR_ERR_CUDA;
+    }
+
+    char *ws = static_cast<char *>(pl->ws);
+    void *xs = ws + pl->ws_off_stage;
+    float *raw = pl->ws_raw_bytes ? reinterpret_cast<float *>(ws + pl->ws_off_raw) : nullptr;
+    if (ctr::launch_stage_x(pl, x, xs, st) != cudaSuccess) return CTR_ERR_CUDA;
+
+    const bool bf16 = pl->dtype == CTR_BF16;
+    const size_t a_plane = (size_t)pl->M_pad * pl->K_total * op_esize(pl);
+    const size_t b_plane = (size_t)pl->N_total * pl->C_in_pad * op_esize(pl);
+    CUtensorMap maps[4];
+    bool ok = encode_2d(&maps[0], w_packed, bf16, pl->K_total, pl->M_pad, ctr::kBM) &&
+              encode_2d(&maps[1], xs, bf16, pl->C_in_pad, pl->N_total, pl->block_n);
+    if (!bf16) {
+        ok = ok &&
+             encode_2d(&maps[2], static_cast<const char *>(w_packed) + a_plane, false,
+                       pl->K_total, pl->M_pad, ctr::kBM) &&
+             encode_2d(&maps[3], static_cast<char *>(xs) + b_plane, false, pl->C_in_pad,
+                       pl->N_total, pl->block_n);
+    } else {
+        maps[2] = maps[0];
+        maps[3] = maps[1];
+    }
+    if (!ok) return CTR_ERR_CUDA;
+
+    GemmParams gp;
+    std::memset(&gp, 0, sizeof(gp));
+    gp.num_m_tiles = pl->num_m_tiles;
+    gp.num_n_tiles = pl->num_n_tiles;
+    gp.splits = pl->splits;
+    gp.num_tiles = pl->num_tiles;
+    gp.kb_total = (int)(pl->K_total * op_esize(pl) / ctr::kBKBytes);
+    gp.kb_per_tap = (int)(pl->C_in_pad * op_esize(pl) / ctr::kBKBytes);
+    gp.kb_group = pl->kb_group;
+    gp.mx = (int)pl->m[1];
+    gp.Px = pl->P[1];
+    const bool fused = pl->path == CTR_PATH_POLYPHASE && pl->splits == 1;
+    gp.epi_mode = fused ? ctr::EPI_POLYPHASE : ctr::EPI_RAW;
+    gp.epi = make_epi(pl, bias, y);
+    gp.raw = raw;
+    gp.raw_ld = (int64_t)pl->num_n_tiles * pl->block_n;
+    gp.raw_split_stride = pl->M_pad * gp.raw_ld;
+    gp.status = pl->d_status;
+    gp.wait_limit_ns = pl->wait_limit_ns;
+    if (timed && cudaEventRecord(pl->ev_before, st) != cudaSuccess) return CTR_ERR_CUDA;
+    if (ctr::launch_gemm_tc(pl, maps, gp, st) != cudaSuccess) return CTR_ERR_CUDA;
+    if (timed && cudaEventRecord(pl->ev_after, st) != cudaSuccess) return CTR_ERR_CUDA;
+
+    if (pl->path == CTR_PATH_POLYPHASE && !fused) {
+        if (ctr::launch_splitk_reduce(pl, raw, gp.epi, gp.raw_ld, gp.raw_split_stride, st) !=
+            cudaSuccess)
+            return CTR_ERR_CUDA;
+    } else if (pl->path == CTR_PATH_COL2IM) {
+        if (ctr::launch_col2im(pl, raw, gp.raw_ld, bias, y, st) != cudaSuccess)
+            return CTR_ERR_CUDA;
+    }
+    return CTR_OK;
+}
+
+ctr_status ctr_plan_check(ctr_plan_t pl, void *stream) {
+    if (!pl) return CTR_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return CTR_ERR_CUDA;
+    if (!pl->d_status) return CTR_OK;
+    uint32_t v = 0;
+    if (cudaMemcpy(&v, pl->d_status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return CTR_ERR_CUDA;
+    if (v != 0) {
+        if (cudaMemset(pl->d_status, 0, sizeof(uint32_t)) != cudaSuccess) return CTR_ERR_CUDA;
+        return CTR_ERR_DEVICE_TIMEOUT;
+    }
+    return CTR_OK;
+}
+
+void ctr_plan_destroy(ctr_plan_t pl) {
+    if (!pl) return;
+    if (pl->d_status) {
+        int cur = 0;
+        cudaGetDevice(&cur);
+        if (cur != pl->status_device) cudaSetDevice(pl->status_device);
+        cudaFree(pl->d_status);
+        if (cur != pl->status_device) cudaSetDevice(cur);
+    }
+    delete pl;
+}
+
+}  // extern "C"

@@ -1,0 +1,383 @@
+// aux_kernels.cu -- the non-tensor-core kernels of the library:
+//   prepack      torch weight -> phase-major GEMM rows (polyphase) or (oc, tap) rows (col2im)
+//   stage_x      NC(H)W input -> channels-last rows with zero halos (tf32 hi/lo or bf16)
+//   splitk_reduce  fixed-order sum of split-K partials, then the fused output stage
+//   col2im       gather of the valid taps from the fp32 column buffer
+//   gather       direct ConvTranspose for tiny channel counts
+//   fill_bias    y = bias (or zeros) for an empty input on the col2im path
+//   copy_weight  the gather path's "packed" weight (a plain copy)
+#include <algorithm>
+#include <cuda_bf16.h>
+
+#include "ctr_internal.h"
+#include "epilogue.cuh"
+#include "ptx.cuh"
+
+namespace ctr {
+namespace {
+
+constexpr int kBlock = 256;
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+unsigned grid_for(int64_t n, int block) {
+    const int64_t g = ceil_div(n, block);
+    return (unsigned)std::min<int64_t>(std::max<int64_t>(g, 1), (int64_t)1 << 30);
+}
+
+// Geometry of a plan as plain values for the kernels below (2-D form).
+struct Geo {
+    int64_t B, C_in, C_out;
+    int64_t H, W, ky, kx, sy, sx, py, px, Ho, Wo;
+    int act;
+    float slope;
+    int bf16;
+};
+
+Geo geo_of(const ctr_plan_s *pl) {
+    Geo g;
+    g.B = pl->B;
+    g.C_in = pl->C_in;
+    g.C_out = pl->C_out;
+    g.H = pl->in[0];
+    g.W = pl->in[1];
+    g.ky = pl->k[0];
+    g.kx = pl->k[1];
+    g.sy = pl->s[0];
+    g.sx = pl->s[1];
+    g.py = pl->p[0];
+    g.px = pl->p[1];
+    g.Ho = pl->out[0];
+    g.Wo = pl->out[1];
+    g.act = pl->act;
+    g.slope = pl->slope;
+    g.bf16 = pl->dtype == CTR_BF16 ? 1 : 0;
+    return g;
+}
+
+// -------------------------------------------------------------------------- gather
+// y[b, oc, oy, ox] = bias[oc] + sum over ic and the taps that reach (oy, ox): a tap ty
+// contributes when (oy + py - ty) is a multiple of sy and the quotient is a valid input row
+// ("[ExecuTorch][WebGPU] Add optimized conv2d op", Implementation: the gather form with the
+// un-flipped weight).  fp32 accumulation on CUDA cores; one thread per output element.
+__global__ void gather_kernel(const void *__restrict__ x, const void *__restrict__ w,
+                              const void *__restrict__ bias, void *__restrict__ y, Geo g,
+                              int64_t total) {
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t ox = idx % g.Wo;
+        int64_t t = idx / g.Wo;
+        const int64_t oy = t % g.Ho;
+        t /= g.Ho;
+        const int64_t oc = t % g.C_out;
+        const int64_t b = t / g.C_out;
+        float acc = 0.0f;
+        const int64_t ry = oy + g.py, rx = ox + g.px;
+        for (int64_t ty = ry % g.sy; ty < g.ky; ty += g.sy) {
+            const int64_t iy = (ry - ty) / g.sy;
+            if (iy < 0) break;
+            if (iy >= g.H) continue;
+            for (int64_t tx = rx % g.sx; tx < g.kx; tx += g.sx) {
+                const int64_t ix = (rx - tx) / g.sx;
+                if (ix < 0) break;
+                if (ix >= g.W) continue;
+                const int64_t xoff = ((b * g.C_in) * g.H + iy) * g.W + ix;
+                const int64_t woff = ((oc * g.ky) + ty) * g.kx + tx;
+                const int64_t xstride = g.H * g.W;
+                const int64_t wstride = g.C_out * g.ky * g.kx;
+                for (int64_t ic = 0; ic < g.C_in; ++ic)
+                    acc = fmaf(load_io(x, xoff + ic * xstride, g.bf16),
+                               load_io(w, woff + ic * wstride, g.bf16), acc);
+            }
+        }
+        if (bias) acc += load_io(bias, oc, g.bf16);
+        store_io(y, idx, apply_act(acc, g.act, g.slope), g.bf16);
+    }
+}
+
+__global__ void fill_bias_kernel(const void *__restrict__ bias, void *__restrict__ y, Geo g,
+                                 int64_t total) {
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t oc = (idx / (g.Ho * g.Wo)) % g.C_out;
+        const float v = bias ? load_io(bias, oc, g.bf16) : 0.0f;
+        store_io(y, idx, apply_act(v, g.act, g.slope), g.bf16);
+    }
+}
+
+__global__ void copy_bytes_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
+                                  int64_t n16, const uint8_t *__restrict__ src_tail,
+                                  uint8_t *__restrict__ dst_tail, int tail) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16;
+         i += (int64_t)gridDim.x * blockDim.x)
+        dst[i] = src[i];
+    if (blockIdx.x == 0 && (int)threadIdx.x < tail) dst_tail[threadIdx.x] = src_tail[threadIdx.x];
+}
+
+// -------------------------------------------------------------------------- prepack
+struct PackGeo {
+    int64_t M_pad, K_total, C_in_pad, C_in, C_out;
+    int64_t ky, kx, sy, sx, my, mx;
+    int S, S_pad;
+    int polyphase;
+    int bf16;
+};
+
+// Polyphase rows ("[XNNPACK] Lower dense transposed convs as one polyphase conv + depth to
+// space", Summary: phase-major ordering, taps flipped within a phase):
+//   A[r = oc*S_pad + jy*sx + jx, k = (uy*mx + ux)*C_in_pad + ic]
+//       = w[ic, oc, sy*(my-1-uy) + jy, sx*(mx-1-ux) + jx]    (0 past the kernel: the kernel
+//                                                               is zero-padded to m*s taps)
+// col2im rows ("[WebGPU] optimizations for audio models", ConvTranspose commit: W[C_in,
+// kH*kW*C_out] prepacked to the GEMM layout):  A[r = oc*S_pad + t, k = ic] = w[ic, oc, t].
+// Padding rows and channels are zero.  fp32 weights are split into tf32 hi and lo planes.
+__global__ void prepack_kernel(const void *__restrict__ w, void *__restrict__ wp, PackGeo pg) {
+    const int64_t total = pg.M_pad * pg.K_total;
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = idx / pg.K_total;
+        const int64_t kk = idx - r * pg.K_total;
+        const int64_t g = kk / pg.C_in_pad;
+        const int64_t ic = kk - g * pg.C_in_pad;
+        const int64_t oc = r / pg.S_pad;
+        const int64_t j = r - oc * pg.S_pad;
+        float v = 0.0f;
+        if (oc < pg.C_out && j < pg.S && ic < pg.C_in) {
+            int64_t ty, tx;
+            if (pg.polyphase) {
+                const int64_t jy = j / pg.sx, jx = j - (j / pg.sx) * pg.sx;
+                const int64_t uy = g / pg.mx, ux = g - (g / pg.mx) * pg.mx;
+                ty = pg.sy * (pg.my - 1 - uy) + jy;
+                tx = pg.sx * (pg.mx - 1 - ux) + jx;
+            } else {
+                ty = j / pg.kx;
+                tx = j - ty * pg.kx;
+            }
+            if (ty < pg.ky && tx < pg.kx)
+                v = load_io(w, ((ic * pg.C_out + oc) * pg.ky + ty) * pg.kx + tx, pg.bf16);
+        }
+        if (pg.bf16) {
+            static_cast<__nv_bfloat16 *>(wp)[idx] = __float2bfloat16_rn(v);  // exact: v is bf16
+        } else {
+            const float hi = ptx::to_tf32(v);
+            const float lo = ptx::to_tf32(v - hi);
+            static_cast<float *>(wp)[idx] = hi;
+            static_cast<float *>(wp)[total + idx] = lo;
+        }
+    }
+}
+
+// -------------------------------------------------------------------------- stage_x
+struct StageGeo {
+    int64_t B, C_in, C_in_pad, H, W, Py, Px, hy, hx, N_total;
+    int bf16;
+};
+
+// xs[n][c] with n = (b*Py + py')*Px + px': x[b, c, py' - hy, px' - hx] inside the input and
+// c < C_in, zero elsewhere (the halos are the polyphase conv's padding m - 1).  A 32 x 32
+// tile goes through shared memory so both the NCHW reads and the channels-last writes are
+// coalesced.  fp32 input is written as tf32 hi and lo planes.
+__global__ void stage_x_kernel(const void *__restrict__ x, void *__restrict__ xs, StageGeo sg) {
+    __shared__ float tile[32][33];
+    const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
+    const int64_t n0 = (int64_t)blockIdx.x * 32;
+    const int64_t c0 = (int64_t)blockIdx.y * 32;
+    const int64_t plane = sg.Py * sg.Px;
+    {
+        const int64_t n = n0 + tx;
+        int64_t xbase = -1;
+        if (n < sg.N_total) {
+            const int64_t b = n / plane;
+            const int64_t rem = n - b * plane;
+            const int64_t yy = rem / sg.Px - sg.hy;
+            const int64_t xx = rem - (rem / sg.Px) * sg.Px - sg.hx;
+            if (yy >= 0 && yy < sg.H && xx >= 0 && xx < sg.W)
+                xbase = (b * sg.C_in * sg.H + yy) * sg.W + xx;
+        }
+        for (int i = ty; i < 32; i += 8) {
+            const int64_t c = c0 + i;
+            float v = 0.0f;
+            if (xbase >= 0 && c < sg.C_in) v = load_io(x, xbase + c * sg.H * sg.W, sg.bf16);
+            tile[i][tx] = v;
+        }
+    }
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8) {
+        const int64_t n = n0 + i;
+        if (n >= sg.N_total) break;
+        const int64_t o = n * sg.C_in_pad + c0 + tx;
+        const float v = tile[tx][i];
+        if (sg.bf16) {
+            static_cast<__nv_bfloat16 *>(xs)[o] = __float2bfloat16_rn(v);
+        } else {
+            const float hi = ptx::to_tf32(v);
+            const float lo = ptx::to_tf32(v - hi);
+            static_cast<float *>(xs)[o] = hi;
+            static_cast<float *>(xs)[sg.N_total * sg.C_in_pad + o] = lo;
+        }
+    }
+}
+
+// -------------------------------------------------------------------------- split-K reduce
+// Each warp sums the split-K partials of one 32 x 32 block of D in a fixed order (z = 0, 1,
+// ...), stages it in shared memory and runs the same output stage as the fused epilogue.
+__global__ void splitk_reduce_kernel(const float *__restrict__ raw, EpiParams ep, int64_t ld,
+                                     int64_t split_stride, int splits, int64_t row_blocks,
+                                     int64_t col_blocks) {
+    __shared__ float sm_all[4][32 * kEpiLd];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float *sm = sm_all[warp];
+    const int64_t blk = (int64_t)blockIdx.x * 4 + warp;
+    if (blk >= row_blocks * col_blocks) return;
+    const int64_t r0 = (blk / col_blocks) * 32;
+    const int64_t c0 = (blk % col_blocks) * 32;
+    for (int i = 0; i < 32; ++i) {
+        const float *p = raw + (r0 + i) * ld + c0 + lane;
+        float s = p[0];
+        for (int z = 1; z < splits; ++z) s += p[(int64_t)z * split_stride];
+        sm[i * kEpiLd + lane] = s;
+    }
+    __syncwarp();
+    emit_block(sm, r0, c0, ep, lane);
+}
+
+// -------------------------------------------------------------------------- col2im
+// y[b, oc, oy, ox] = bias + sum of col[(oc, ty, tx), (b, iy, ix)] over the taps that reach
+// (oy, ox) (the same divisibility rule as the gather kernel), summed over split-K partials
+// in a fixed order.  Only reachable taps are visited ("[WebGPU] optimizations for audio
+// models", review commit: each chunk gathers only into the box its rows reach).
+__global__ void col2im_kernel(const float *__restrict__ col, int64_t ld, int64_t split_stride,
+                              int splits, int S_pad, const void *__restrict__ bias,
+                              void *__restrict__ y, Geo g, int64_t total) {
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t ox = idx % g.Wo;
+        int64_t t = idx / g.Wo;
+        const int64_t oy = t % g.Ho;
+        t /= g.Ho;
+        const int64_t oc = t % g.C_out;
+        const int64_t b = t / g.C_out;
+        float acc = bias ? load_io(bias, oc, g.bf16) : 0.0f;
+        const int64_t ry = oy + g.py, rx = ox + g.px;
+        for (int64_t ty = ry % g.sy; ty < g.ky; ty += g.sy) {
+            const int64_t iy = (ry - ty) / g.sy;
+            if (iy < 0) break;
+            if (iy >= g.H) continue;
+            for (int64_t tx = rx % g.sx; tx < g.kx; tx += g.sx) {
+                const int64_t ix = (rx - tx) / g.sx;
+                if (ix < 0) break;
+                if (ix >= g.W) continue;
+                const int64_t r = oc * S_pad + ty * g.kx + tx;
+                const int64_t n = (b * g.H + iy) * g.W + ix;
+                const float *p = col + r * ld + n;
+                for (int z = 0; z < splits; ++z) acc += p[(int64_t)z * split_stride];
+            }
+        }
+        store_io(y, idx, apply_act(acc, g.act, g.slope), g.bf16);
+    }
+}
+
+}  // namespace
+
+// ============================================================================ launchers
+
+cudaError_t launch_gather(const ctr_plan_s *pl, const void *x, const void *w, const void *bias,
+                          void *y, cudaStream_t st) {
+    const Geo g = geo_of(pl);
+    const int64_t total = g.B * g.C_out * g.Ho * g.Wo;
+    if (total == 0) return cudaSuccess;
+    gather_kernel<<<grid_for(total, kBlock), kBlock, 0, st>>>(x, w, bias, y, g, total);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fill_bias(const ctr_plan_s *pl, const void *bias, void *y, cudaStream_t st) {
+    const Geo g = geo_of(pl);
+    const int64_t total = g.B * g.C_out * g.Ho * g.Wo;
+    if (total == 0) return cudaSuccess;
+    fill_bias_kernel<<<grid_for(total, kBlock), kBlock, 0, st>>>(bias, y, g, total);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_weight(const ctr_plan_s *pl, const void *w, void *w_packed,
+                               cudaStream_t st) {
+    const int64_t bytes = (int64_t)pl->packed_bytes;
+    const int64_t n16 = bytes / 16;
+    const int tail = (int)(bytes - n16 * 16);
+    copy_bytes_kernel<<<grid_for(std::max<int64_t>(n16, 1), kBlock), kBlock, 0, st>>>(
+        static_cast<const uint4 *>(w), static_cast<uint4 *>(w_packed), n16,
+        static_cast<const uint8_t *>(w) + n16 * 16, static_cast<uint8_t *>(w_packed) + n16 * 16,
+        tail);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prepack(const ctr_plan_s *pl, const void *w, void *w_packed, cudaStream_t st) {
+    PackGeo pg;
+    pg.M_pad = pl->M_pad;
+    pg.K_total = pl->K_total;
+    pg.C_in_pad = pl->C_in_pad;
+    pg.C_in = pl->C_in;
+    pg.C_out = pl->C_out;
+    pg.ky = pl->k[0];
+    pg.kx = pl->k[1];
+    pg.sy = pl->s[0];
+    pg.sx = pl->s[1];
+    pg.my = pl->m[0];
+    pg.mx = pl->m[1];
+    pg.S = pl->S;
+    pg.S_pad = pl->S_pad;
+    pg.polyphase = pl->path == CTR_PATH_POLYPHASE ? 1 : 0;
+    pg.bf16 = pl->dtype == CTR_BF16 ? 1 : 0;
+    const int64_t total = pg.M_pad * pg.K_total;
+    prepack_kernel<<<grid_for(total, kBlock), kBlock, 0, st>>>(w, w_packed, pg);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_stage_x(const ctr_plan_s *pl, const void *x, void *xs, cudaStream_t st) {
+    StageGeo sg;
+    sg.B = pl->B;
+    sg.C_in = pl->C_in;
+    sg.C_in_pad = pl->C_in_pad;
+    sg.H = pl->in[0];
+    sg.W = pl->in[1];
+    sg.Py = pl->P[0];
+    sg.Px = pl->P[1];
+    sg.hy = pl->m[0] - 1;
+    sg.hx = pl->m[1] - 1;
+    sg.N_total = pl->N_total;
+    sg.bf16 = pl->dtype == CTR_BF16 ? 1 : 0;
+    if (sg.N_total == 0) return cudaSuccess;
+    dim3 grid((unsigned)ceil_div(sg.N_total, 32), (unsigned)(sg.C_in_pad / 32));
+    stage_x_kernel<<<grid, dim3(32, 8), 0, st>>>(x, xs, sg);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_splitk_reduce(const ctr_plan_s *pl, const float *raw, const EpiParams &ep,
+                                 int64_t raw_ld, int64_t split_stride, cudaStream_t st) {
+    const int64_t row_blocks = ceil_div(std::min<int64_t>(pl->M_rows, pl->M_pad), 32);
+    const int64_t col_blocks = raw_ld / 32;
+    const int64_t blocks = ceil_div(row_blocks * col_blocks, 4);
+    splitk_reduce_kernel<<<(unsigned)blocks, 128, 0, st>>>(raw, ep, raw_ld, split_stride,
+                                                           pl->splits, row_blocks, col_blocks);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_col2im(const ctr_plan_s *pl, const float *col, int64_t col_ld,
+                          const void *bias, void *y, cudaStream_t st) {
+    const Geo g = geo_of(pl);
+    const int64_t total = g.B * g.C_out * g.Ho * g.Wo;
+    if (total == 0) return cudaSuccess;
+    const int64_t split_stride = pl->M_pad * col_ld;
+    col2im_kernel<<<grid_for(total, kBlock), kBlock, 0, st>>>(col, col_ld, split_stride,
+                                                              pl->splits, pl->S_pad, bias, y, g,
+                                                              total);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace ctr

@@ -1,0 +1,133 @@
+// ctr_internal.h -- plan state and kernel parameter blocks shared by the library's
+// translation units (host and device).  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/ctr.h"
+
+namespace ctr {
+
+// Tile shape of the tensor-core GEMM: 128 rows (TMEM lanes) x BN columns, K in 128-byte
+// slices (64 bf16 or 32 fp32 per row).
+constexpr int kBM = 128;
+constexpr int kBKBytes = 128;
+
+enum class Prec : int { BF16 = 0, TF32x3 = 1 };
+enum EpiMode : int { EPI_POLYPHASE = 0, EPI_RAW = 1 };
+
+// Output mapping of a GEMM result D[r, n] (shared by the fused epilogue and the split-K
+// reduce).  Everything is in the 2-D form; 1-D plans have sy = 1, py = 0, Py = Qvy = 1,
+// Hout = 1.
+//   row r    -> oc = r / S_pad, j = r % S_pad (phase, valid when j < S), jy = j / sx,
+//               jx = j % sx
+//   column n -> b = n / (Py*Px), qy = (n / Px) % Py, qx = n % Px (valid when b < B,
+//               qy < Qvy, qx < Qvx)
+//   output   -> y[b, oc, sy*qy + jy - py, sx*qx + jx - px] when inside [0, Hout) x [0, Wout)
+struct EpiParams {
+    int S, S_pad, sx, sy, px, py;
+    int64_t Px, Py, Qvx, Qvy;
+    int64_t B, C_out, Hout, Wout;
+    const void *bias;   // [C_out] in the I/O dtype, or nullptr
+    void *y;
+    int out_bf16;       // 1: bf16 I/O, 0: fp32
+    int act;            // ctr_act
+    float slope;
+};
+
+struct GemmParams {
+    int num_m_tiles, num_n_tiles, splits;
+    int64_t num_tiles;
+    int kb_total;       // K slices over all taps
+    int kb_per_tap;     // K slices per tap (C_in_pad * esize / 128)
+    int kb_group;       // K slices per tensor-core accumulation group (see gemm_tc.cu)
+    int mx;             // taps along x: tap g -> (uy, ux) = (g / mx, g % mx)
+    int64_t Px;         // column shift of one tap step along y
+    int epi_mode;
+    EpiParams epi;
+    float *raw;         // EPI_RAW: D goes to raw[z][r][n] with leading dimension raw_ld
+    int64_t raw_ld;
+    int64_t raw_split_stride;
+    uint32_t *status;   // device status word (bit flags of bounded waits that gave up)
+    uint64_t wait_limit_ns;
+};
+
+// Status-word bits set by device code.
+constexpr uint32_t kStatusTimeoutProducer = 1u << 0;
+constexpr uint32_t kStatusTimeoutMma = 1u << 1;
+constexpr uint32_t kStatusTimeoutEpilogue = 1u << 2;
+constexpr uint32_t kStatusTimeoutDrain = 1u << 3;
+
+}  // namespace ctr
+
+struct ctr_plan_s {
+    // Geometry in the 2-D form (index 0 = y/height, 1 = x/width).
+    int ndim;
+    int64_t B, C_in, C_out;
+    int64_t in[2], k[2], s[2], p[2], op[2], out[2];
+    int dtype;
+    int act;
+    float slope;
+    int path;           // chosen ctr_path (never AUTO)
+    int forced_path;
+    int forced_split;
+    int prepared;       // ctr_prepack_weight ran (status word allocated)
+    int num_sms;
+
+    // Tensor-core GEMM geometry (polyphase and col2im paths).
+    int64_t m[2];       // taps per phase per dim (polyphase), 1 for col2im
+    int64_t Qv[2];      // valid phase columns per dim
+    int64_t P[2];       // staged pitch per dim (with halos)
+    int S, S_pad;       // phases (polyphase) or taps (col2im) per output channel, padded
+    int64_t C_in_pad;
+    int64_t M_rows, M_pad;
+    int64_t K_total;    // GEMM K = taps * C_in_pad
+    int64_t N_total;    // GEMM columns = B * P[0] * P[1]
+    int block_n;
+    int splits;
+    int kb_group;       // K slices per accumulation group; >= slices per tile = no flush
+    int num_m_tiles, num_n_tiles;
+    int64_t num_tiles;
+
+    size_t packed_bytes;
+    size_t ws_bytes_needed;
+    size_t ws_off_stage;   // staged x (channels-last with halos)
+    size_t ws_stage_bytes;
+    size_t ws_off_raw;     // split-K partials or the col2im column buffer
+    size_t ws_raw_bytes;
+    void *ws;
+    size_t ws_bytes;
+
+    uint32_t *d_status;
+    int status_device;
+    uint64_t wait_limit_ns;
+    cudaEvent_t ev_before, ev_after;   // optional timing events around the main kernel
+};
+
+namespace ctr {
+
+// Launch wrappers (each returns the cudaGetLastError() of its launches).
+cudaError_t launch_gather(const ctr_plan_s *pl, const void *x, const void *w, const void *bias,
+                          void *y, cudaStream_t st);
+cudaError_t launch_copy_weight(const ctr_plan_s *pl, const void *w, void *w_packed,
+                               cudaStream_t st);
+cudaError_t launch_prepack(const ctr_plan_s *pl, const void *w, void *w_packed, cudaStream_t st);
+cudaError_t launch_stage_x(const ctr_plan_s *pl, const void *x, void *xs, cudaStream_t st);
+cudaError_t launch_splitk_reduce(const ctr_plan_s *pl, const float *raw, const EpiParams &ep,
+                                 int64_t raw_ld, int64_t split_stride, cudaStream_t st);
+cudaError_t launch_col2im(const ctr_plan_s *pl, const float *col, int64_t col_ld,
+                          const void *bias, void *y, cudaStream_t st);
+cudaError_t launch_fill_bias(const ctr_plan_s *pl, const void *bias, void *y, cudaStream_t st);
+cudaError_t launch_gemm_tc(const ctr_plan_s *pl, const CUtensorMap *maps, const GemmParams &gp,
+                           cudaStream_t st);
+
+// Counter of launched kernels (monotonic, process-wide).
+void count_launches(uint64_t n);
+
+// Bytes of dynamic shared memory a GEMM instantiation uses.
+size_t gemm_smem_bytes(Prec prec, int block_n);
+
+}  // namespace ctr
