@@ -162,54 +162,68 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     layers = workloads.make_workload(args.workload)
-    if len(layers) != 1:
-        return run_ours_stack(args, rank, world, local_rank, layers)
-    li = layers[0]
-    L = li.layer
-    tdt = torch.bfloat16 if L.dtype == "bf16" else torch.float32
+    Ls = [li.layer for li in layers]
+    tdts = [torch.bfloat16 if L.dtype == "bf16" else torch.float32 for L in Ls]
 
-    def t(a):
+    def t(a, tdt):
         return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev).to(tdt)
 
     # Buffer sets to rotate over: more than twice the L2 size in total.
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20
-    x0, w0, b0 = t(li.x), t(li.w), t(li.bias)
-    probe = ctr.Plan(L.B, L.C_in, L.C_out, L.in_sp, L.kernel, L.stride, L.padding,
-                     L.output_padding, dtype=tdt, negative_slope=L.act_slope, device=dev)
-    y_bytes = int(np.prod(probe.out_shape)) * L.elem_bytes
-    set_bytes = (x0.numel() * L.elem_bytes + probe.packed_bytes + probe.workspace_bytes + y_bytes)
+    w_dev = [t(li.w, tdt) for li, tdt in zip(layers, tdts)]
+    b_dev = [t(li.bias, tdt) for li, tdt in zip(layers, tdts)]
+    x_dev = t(layers[0].x, tdts[0])
+
+    def make_plans():
+        return [ctr.Plan(L.B, L.C_in, L.C_out, L.in_sp, L.kernel, L.stride, L.padding,
+                         L.output_padding, dtype=tdt, negative_slope=L.act_slope, device=dev)
+                for L, tdt in zip(Ls, tdts)]
+
+    probe = make_plans()
+    set_bytes = x_dev.numel() * Ls[0].elem_bytes
+    for p, L in zip(probe, Ls):
+        set_bytes += p.packed_bytes + p.workspace_bytes + int(np.prod(p.out_shape)) * L.elem_bytes
+    for p in probe:
+        p.close()
     nsets = max(2, int(math.ceil(2.0 * l2 / set_bytes)) + 1)
-    probe.close()
     sets = []
-    for i in range(nsets):
-        p = ctr.Plan(L.B, L.C_in, L.C_out, L.in_sp, L.kernel, L.stride, L.padding,
-                     L.output_padding, dtype=tdt, negative_slope=L.act_slope, device=dev)
-        p.prepack(w0)
-        sets.append({"plan": p, "x": x0.clone(), "b": None if b0 is None else b0.clone(),
-                     "y": torch.empty(p.out_shape, dtype=tdt, device=dev)})
+    for _ in range(nsets):
+        plans = make_plans()
+        for p, w in zip(plans, w_dev):
+            p.prepack(w)
+        ys = [torch.empty(p.out_shape, dtype=tdt, device=dev) for p, tdt in zip(plans, tdts)]
+        sets.append({"plans": plans, "x": x_dev.clone(), "y": ys,
+                     "b": [None if b is None else b.clone() for b in b_dev]})
     torch.cuda.synchronize()
 
-    # Prepack time (reported separately; not part of a step).
+    # Prepack time of the whole workload (reported separately; not part of a step).
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    sets[0]["plan"].prepack(w0)
+    for p, w in zip(sets[0]["plans"], w_dev):
+        p.prepack(w)
     e1.record()
     torch.cuda.synchronize()
     prepack_ms = e0.elapsed_time(e1)
 
-    def step(i, evs=None):
-        s = sets[i % nsets]
-        if evs is not None:
-            ctr.ctr_plan_set_timing_events(s["plan"].handle, evs[0].cuda_event, evs[1].cuda_event)
-        s["plan"].forward(s["x"], s["b"], y=s["y"])
-        if evs is not None:
-            ctr.ctr_plan_set_timing_events(s["plan"].handle, None, None)
+    def run_set(s, x=None, kevs=None):
+        inp = s["x"] if x is None else x
+        for li_idx, p in enumerate(s["plans"]):
+            if kevs is not None:
+                ctr.ctr_plan_set_timing_events(p.handle, kevs[li_idx][0].cuda_event,
+                                               kevs[li_idx][1].cuda_event)
+            p.forward(inp, s["b"][li_idx], y=s["y"][li_idx])
+            if kevs is not None:
+                ctr.ctr_plan_set_timing_events(p.handle, None, None)
+            inp = s["y"][li_idx]
+        return inp
 
     for i in range(args.warmup):
-        step(i)
+        run_set(sets[i % nsets])
     torch.cuda.synchronize()
-    sets[0]["plan"].check()
+    for s in sets:
+        for p in s["plans"]:
+            p.check()
 
     sampler = ClockSampler(local_rank)
     sampler.start()
@@ -218,19 +232,21 @@ def run_ours(args, rank, world, local_rank):
     i = 0
     while time.time() - soak_t0 < args.soak:
         for _ in range(50):
-            step(i)
+            run_set(sets[i % nsets])
             i += 1
         torch.cuda.synchronize()
 
     # Timed region: exactly K steps.
     K = args.steps
+    nl = len(Ls)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(K)]
-    for a, b in kev:       # create the driver events before handing them to the library
-        a.record()
-        b.record()
+    kev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(nl)] for _ in range(K)]
+    for row in kev:       # create the driver events before handing them to the library
+        for a, b in row:
+            a.record()
+            b.record()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -238,7 +254,7 @@ def run_ours(args, rank, world, local_rank):
     wall0 = time.time()
     for k in range(K):
         ev[k][0].record()
-        step(k, kev[k])
+        run_set(sets[k % nsets], kevs=kev[k])
         ev[k][1].record()
     torch.cuda.synchronize()
     wall1 = time.time()
@@ -248,66 +264,84 @@ def run_ours(args, rank, world, local_rank):
     time.sleep(0.25)
     sampler.stop()
     for s in sets:
-        s["plan"].check()
+        for p in s["plans"]:
+            p.check()
 
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    kern_ms = [a.elapsed_time(b) for a, b in kev]
+    kern_ms = [sum(kev[k][j][0].elapsed_time(kev[k][j][1]) for k in range(K)) / K
+               for j in range(nl)]
     total_ms = sum(step_ms)
-    kern_avg = sum(kern_ms) / K
-
     if world > 1:
-        tt = torch.tensor([total_ms, kern_avg], dtype=torch.float64, device=dev)
+        tt = torch.tensor([total_ms] + kern_ms, dtype=torch.float64, device=dev)
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms, kern_avg = float(tt[0]), float(tt[1])
+        total_ms, kern_ms = float(tt[0]), [float(v) for v in tt[1:]]
 
-    # End to end through the public API: pinned host x -> device, forward, y -> pinned host.
-    x_host = torch.from_numpy(np.ascontiguousarray(li.x)).to(tdt).pin_memory()
-    y_host = torch.empty(sets[0]["y"].shape, dtype=tdt).pin_memory()
+    # End to end through the public API: pinned host x -> device, every layer, y -> pinned host.
+    x_host = torch.from_numpy(np.ascontiguousarray(layers[0].x)).to(tdts[0]).pin_memory()
+    y_host = torch.empty(sets[0]["y"][-1].shape, dtype=tdts[-1]).pin_memory()
     e2e_ms = []
     for k in range(max(3, min(K, 50))):
         s = sets[k % nsets]
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         s["x"].copy_(x_host, non_blocking=True)
-        s["plan"].forward(s["x"], s["b"], y=s["y"])
-        y_host.copy_(s["y"], non_blocking=True)
+        out = run_set(s)
+        y_host.copy_(out, non_blocking=True)
         b.record()
         torch.cuda.synchronize()
         e2e_ms.append(a.elapsed_time(b))
-    e2e_ms = statistics.median(e2e_ms[1:]) if len(e2e_ms) > 1 else e2e_ms[0]
+    e2e_ms = statistics.median(e2e_ms[1:])
 
-    # Parity of this run's output against the oracle (computed after timing).
+    # Parity of this run's output against the oracle, layer by layer with the library's
+    # own previous output as input (computed after timing).
     parity = None
     if rank == 0 and args.parity:
         import oracle
-        ref = oracle.conv_transpose(li.x, li.w, li.bias, L.stride, L.padding, L.output_padding)
-        if L.act_slope is not None:
-            ref = oracle.leaky_relu(ref, L.act_slope)
-        parity = oracle.rel_l2(sets[(K - 1) % nsets]["y"].float().cpu().numpy(), ref)
+        s = sets[(K - 1) % nsets]
+        xin = layers[0].x
+        errs = []
+        for j, (li, L) in enumerate(zip(layers, Ls)):
+            ref = oracle.conv_transpose(xin, li.w, li.bias, L.stride, L.padding, L.output_padding)
+            if L.act_slope is not None:
+                ref = oracle.leaky_relu(ref, L.act_slope)
+            got = s["y"][j].float().cpu().numpy()
+            errs.append(oracle.rel_l2(got, ref))
+            xin = got
+        parity = max(errs)
 
-    flops = 2.0 * L.useful_macs
+    flops = sum(2.0 * L.useful_macs for L in Ls)
+    bytes_c = sum(L.compulsory_bytes for L in Ls)
     ms_per_step = total_ms / K
     peaks, peak_src = load_peaks()
-    if L.dtype == "bf16":
-        peak_tflops = peaks["bf16_tflops"]
-        peak_note = "bf16 dense, %s burst" % peak_src
-    else:
-        peak_tflops = peaks["bf16_tflops"] * TF32_OVER_BF16 / 3.0
-        peak_note = ("3xTF32: %s bf16 burst x nominal tf32/bf16 (1.1/2.25) / 3 products "
-                     "per useful MAC" % peak_src)
-    t_tensor = flops / (peak_tflops * 1e12)
+
+    def layer_peak(L):
+        if L.dtype == "bf16":
+            return peaks["bf16_tflops"], "bf16 dense, %s burst" % peak_src
+        return (peaks["bf16_tflops"] * TF32_OVER_BF16 / 3.0,
+                "3xTF32: %s bf16 burst x nominal tf32/bf16 (1.1/2.25) / 3 products per useful "
+                "MAC" % peak_src)
+
+    t_roof = 0.0
+    for L in Ls:
+        pk, _ = layer_peak(L)
+        t_roof += max(2.0 * L.useful_macs / (pk * 1e12), L.compulsory_bytes / (peaks["hbm_gbs"] * 1e9))
+    # Dominant kernel: the layer whose main kernel takes longest.
+    j = max(range(nl), key=lambda q: kern_ms[q])
+    L = Ls[j]
+    pk, peak_note = layer_peak(L)
+    t_tensor = 2.0 * L.useful_macs / (pk * 1e12)
     t_hbm = L.compulsory_bytes / (peaks["hbm_gbs"] * 1e9)
     bound = "tensor" if t_tensor >= t_hbm else "hbm"
-    kern_s = kern_avg / 1e3
+    kern_s = kern_ms[j] / 1e3
     if bound == "tensor":
-        achieved, peak, unit = flops / kern_s / 1e12, peak_tflops, "TFLOP/s"
+        achieved, peak, unit = 2.0 * L.useful_macs / kern_s / 1e12, pk, "TFLOP/s"
     else:
         achieved, peak, unit = L.compulsory_bytes / kern_s / 1e9, peaks["hbm_gbs"], "GB/s"
-    traffic = profiled_traffic(args.workload)
-    t_roof = max(t_tensor, t_hbm)
+        peak_note = "HBM copy bandwidth, %s" % peak_src
+    traffic = profiled_traffic(args.workload) if nl == 1 else None
     clocks = sampler.summary(soak_t0, wall1 + 0.25)
+    kname = "gemm_tc_kernel" if sets[0]["plans"][j].path != ctr.CTR_PATH_GATHER else "gather_kernel"
 
-    plan_desc = sets[0]["plan"].describe()
     result = {
         "metric": "ConvTranspose GFLOP/s and % of roofline (tensor peak vs HBM) per call",
         "value": round(world * flops / (ms_per_step / 1e3) / 1e9, 1),
@@ -319,19 +353,20 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "3xtf32-fp32acc" if L.dtype == "f32" else "bf16-fp32acc",
+        "dtype": "3xtf32-fp32acc" if Ls[0].dtype == "f32" else "bf16-fp32acc",
         "data": "synthetic (seeded; workloads.py)",
-        "config": {"workload": args.workload, "shape": L.describe(),
+        "config": {"workload": args.workload, "shape": "; ".join(L.describe() for L in Ls),
                    "l2": "rotating %d buffer sets, %.0f MB > 2x L2 (%.0f MB)"
                          % (nsets, nsets * set_bytes / 1e6, l2 / 1e6),
                    "parallelism": "replica per GPU" if world > 1 else "single GPU",
-                   "plan": plan_desc},
+                   "plan": " | ".join(p.describe() for p in sets[0]["plans"])},
         "pct_of_roofline": round(100.0 * t_roof / (ms_per_step / 1e3), 2),
         "roofline_us": round(t_roof * 1e6, 3),
         "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 2),
                      "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "gemm_tc_kernel", "kernel_us": round(kern_avg * 1e3, 3),
+                     "kernel": kname, "layer": j, "kernel_us": round(kern_ms[j] * 1e3, 3),
                      "peak_source": peak_note},
+        "layer_kernel_us": [round(v * 1e3, 3) for v in kern_ms],
         "e2e": {"value": round(world * flops / (e2e_ms / 1e3) / 1e9, 1), "unit": "GFLOP/s",
                 "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
                 "d2h_bytes_per_step": int(y_host.numel() * y_host.element_size()),
@@ -341,15 +376,13 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks,
         "prepack_ms": round(prepack_ms, 4),
         "parity_rel_l2": parity,
+        "compulsory_bytes": bytes_c,
         "wall_s_timed": round(wall1 - wall0, 4),
     }
     for s in sets:
-        s["plan"].close()
+        for p in s["plans"]:
+            p.close()
     return result
-
-
-def run_ours_stack(args, rank, world, local_rank, layers):
-    raise SystemExit("stack workloads are benchmarked through --workload of a single layer")
 
 
 # ------------------------------------------------------------------ oracle (CPU) arm

@@ -18,6 +18,7 @@
 #include <cudaTypedefs.h>
 
 #include "ctr_internal.h"
+#include "epilogue.cuh"
 
 using ctr::EpiParams;
 using ctr::GemmParams;
@@ -239,6 +240,16 @@ EpiParams make_epi(const ctr_plan_s *pl, const void *bias, void *y) {
     e.out_bf16 = pl->dtype == CTR_BF16 ? 1 : 0;
     e.act = pl->act;
     e.slope = pl->slope;
+    // Row groups hold min(sx, 32) rows; a staging pitch congruent to that length modulo 32
+    // makes the output-order reads of the staging block conflict-free.
+    e.epi_ld = 32 + (int)(std::min<int64_t>(pl->s[1], 32) % 32);
+    if (e.epi_ld > ctr::kEpiLdMax) e.epi_ld = 33;
+    const int64_t sx = pl->s[1];
+    const bool pow2 = (sx & (sx - 1)) == 0;
+    e.fast = (pl->S == pl->S_pad && pow2 && (sx <= 32 || sx % 32 == 0)) ? 1 : 0;
+    e.nj = (int)std::min<int64_t>(sx, 32);
+    e.lg_nj = 0;
+    while ((1 << e.lg_nj) < e.nj) ++e.lg_nj;
     return e;
 }
 

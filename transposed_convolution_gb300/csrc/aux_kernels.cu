@@ -174,57 +174,82 @@ struct StageGeo {
 };
 
 // xs[n][c] with n = (b*Py + py')*Px + px': x[b, c, py' - hy, px' - hx] inside the input and
-// c < C_in, zero elsewhere (the halos are the polyphase conv's padding m - 1).  A 32 x 32
-// tile goes through shared memory so both the NCHW reads and the channels-last writes are
-// coalesced.  fp32 input is written as tf32 hi and lo planes.
-__global__ void stage_x_kernel(const void *__restrict__ x, void *__restrict__ xs, StageGeo sg) {
-    __shared__ float tile[32][33];
-    const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
-    const int64_t n0 = (int64_t)blockIdx.x * 32;
+// c < C_in, zero elsewhere (the halos are the polyphase conv's padding m - 1).  A block
+// moves 256 consecutive staged positions x 32 channels through shared memory: each warp
+// reads 4 channels along positions (32 loads in flight per lane, coalesced along x) and
+// then writes 32 positions along channels (coalesced along c).  Positions are decoded once
+// per lane and advanced incrementally.  fp32 input is written as tf32 hi and lo planes.
+constexpr int kStagePos = 256;
+
+__global__ void __launch_bounds__(256) stage_x_kernel(const void *__restrict__ x,
+                                                      void *__restrict__ xs, StageGeo sg) {
+    __shared__ float tile[kStagePos][33];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t n0 = (int64_t)blockIdx.x * kStagePos;
     const int64_t c0 = (int64_t)blockIdx.y * 32;
     const int64_t plane = sg.Py * sg.Px;
-    {
-        const int64_t n = n0 + tx;
-        int64_t xbase = -1;
-        if (n < sg.N_total) {
-            const int64_t b = n / plane;
-            const int64_t rem = n - b * plane;
-            const int64_t yy = rem / sg.Px - sg.hy;
-            const int64_t xx = rem - (rem / sg.Px) * sg.Px - sg.hx;
-            if (yy >= 0 && yy < sg.H && xx >= 0 && xx < sg.W)
-                xbase = (b * sg.C_in * sg.H + yy) * sg.W + xx;
+    const int64_t hw = sg.H * sg.W;
+    // This lane's first position and its staged coordinates.
+    int64_t n = n0 + lane;
+    int64_t b = n / plane;
+    int64_t rem = n - b * plane;
+    int64_t py = rem / sg.Px;
+    int64_t px = rem - py * sg.Px;
+    int64_t xoff[kStagePos / 32];  // x offset of channel 0 at each of the lane's positions, -1 = zero
+#pragma unroll
+    for (int j = 0; j < kStagePos / 32; ++j) {
+        const int64_t yy = py - sg.hy, xx = px - sg.hx;
+        const bool in = n + 32 * j < sg.N_total && yy >= 0 && yy < sg.H && xx >= 0 && xx < sg.W;
+        xoff[j] = in ? (b * sg.C_in * sg.H + yy) * sg.W + xx : -1;
+        px += 32;
+        while (px >= sg.Px) {
+            px -= sg.Px;
+            if (++py == sg.Py) {
+                py = 0;
+                ++b;
+            }
         }
-        for (int i = ty; i < 32; i += 8) {
-            const int64_t c = c0 + i;
+    }
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+        const int ci = warp * 4 + cc;
+        const int64_t c = c0 + ci;
+        const bool cvalid = c < sg.C_in;
+#pragma unroll
+        for (int j = 0; j < kStagePos / 32; ++j) {
             float v = 0.0f;
-            if (xbase >= 0 && c < sg.C_in) v = load_io(x, xbase + c * sg.H * sg.W, sg.bf16);
-            tile[i][tx] = v;
+            if (cvalid && xoff[j] >= 0) v = load_io(x, xoff[j] + c * hw, sg.bf16);
+            tile[lane + 32 * j][ci] = v;
         }
     }
     __syncthreads();
-    for (int i = ty; i < 32; i += 8) {
-        const int64_t n = n0 + i;
-        if (n >= sg.N_total) break;
-        const int64_t o = n * sg.C_in_pad + c0 + tx;
-        const float v = tile[tx][i];
+    const int64_t lo_off = sg.N_total * sg.C_in_pad;
+#pragma unroll 4
+    for (int p = warp; p < kStagePos; p += 8) {
+        const int64_t np = n0 + p;
+        if (np >= sg.N_total) break;
+        const int64_t o = np * sg.C_in_pad + c0 + lane;
+        const float v = tile[p][lane];
         if (sg.bf16) {
             static_cast<__nv_bfloat16 *>(xs)[o] = __float2bfloat16_rn(v);
         } else {
             const float hi = ptx::to_tf32(v);
-            const float lo = ptx::to_tf32(v - hi);
             static_cast<float *>(xs)[o] = hi;
-            static_cast<float *>(xs)[sg.N_total * sg.C_in_pad + o] = lo;
+            static_cast<float *>(xs)[lo_off + o] = ptx::to_tf32(v - hi);
         }
     }
 }
 
 // -------------------------------------------------------------------------- split-K reduce
 // Each warp sums the split-K partials of one 32 x 32 block of D in a fixed order (z = 0, 1,
-// ...), stages it in shared memory and runs the same output stage as the fused epilogue.
+// ...), stages it column-major in shared memory and runs the same output stage as the fused
+// epilogue.
 __global__ void splitk_reduce_kernel(const float *__restrict__ raw, EpiParams ep, int64_t ld,
                                      int64_t split_stride, int splits, int64_t row_blocks,
                                      int64_t col_blocks) {
-    __shared__ float sm_all[4][32 * kEpiLd];
+    __shared__ float sm_all[4][32 * kEpiLdMax];
+    __shared__ int64_t goff_all[4][32];
+    __shared__ float gbias_all[4][32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float *sm = sm_all[warp];
     const int64_t blk = (int64_t)blockIdx.x * 4 + warp;
@@ -235,10 +260,11 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ raw, EpiParams ep
         const float *p = raw + (r0 + i) * ld + c0 + lane;
         float s = p[0];
         for (int z = 1; z < splits; ++z) s += p[(int64_t)z * split_stride];
-        sm[i * kEpiLd + lane] = s;
+        sm[lane * ep.epi_ld + i] = s;
     }
     __syncwarp();
-    emit_block(sm, r0, c0, ep, lane);
+    const WarpRows rows = warp_rows(r0, ep, lane, gbias_all[warp], goff_all[warp]);
+    emit_block(sm, rows, col_cursor(c0, ep), ep, lane);
 }
 
 // -------------------------------------------------------------------------- col2im
@@ -350,8 +376,8 @@ cudaError_t launch_stage_x(const ctr_plan_s *pl, const void *x, void *xs, cudaSt
     sg.N_total = pl->N_total;
     sg.bf16 = pl->dtype == CTR_BF16 ? 1 : 0;
     if (sg.N_total == 0) return cudaSuccess;
-    dim3 grid((unsigned)ceil_div(sg.N_total, 32), (unsigned)(sg.C_in_pad / 32));
-    stage_x_kernel<<<grid, dim3(32, 8), 0, st>>>(x, xs, sg);
+    dim3 grid((unsigned)ceil_div(sg.N_total, kStagePos), (unsigned)(sg.C_in_pad / 32));
+    stage_x_kernel<<<grid, 256, 0, st>>>(x, xs, sg);
     count_launches(1);
     return cudaGetLastError();
 }

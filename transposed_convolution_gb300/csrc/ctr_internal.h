@@ -36,6 +36,9 @@ struct EpiParams {
     int out_bf16;       // 1: bf16 I/O, 0: fp32
     int act;            // ctr_act
     float slope;
+    int epi_ld;         // pitch (floats) of the column-major staging block, 32..63
+    int fast;           // 1: S == S_pad and sx is a power of two with sx <= 32 or 32 | sx
+    int nj, lg_nj;      // rows per row group in the fast path: min(sx, 32), its log2
 };
 
 struct GemmParams {

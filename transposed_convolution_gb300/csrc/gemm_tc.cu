@@ -40,8 +40,9 @@ namespace {
 
 constexpr int kThreads = 192;
 constexpr int kEpiWarps = 4;
-constexpr int kEpiBytes = kEpiWarps * 32 * kEpiLd * 4;
-constexpr int kSmemBudget = 225 * 1024;
+constexpr int kEpiTabBytes = 32 * (4 + 8);  // per epilogue warp: group bias + offset tables
+constexpr int kEpiBytes = kEpiWarps * (32 * kEpiLdMax * 4 + kEpiTabBytes);
+constexpr int kSmemBudget = 227 * 1024;
 constexpr uint64_t kDrainLimitNs = 2000000000ull;
 
 template <Prec P, int BN>
@@ -255,9 +256,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad + 31
-        float *sm = epi_smem + (warp - 2) * 32 * kEpiLd;
+        float *sm = epi_smem + (warp - 2) * 32 * kEpiLdMax;
+        uint8_t *tab = reinterpret_cast<uint8_t *>(epi_smem + kEpiWarps * 32 * kEpiLdMax) +
+                       (warp - 2) * kEpiTabBytes;
+        int64_t *goff = reinterpret_cast<int64_t *>(tab);
+        float *gbias = reinterpret_cast<float *>(tab + 32 * 8);
+        const bool fused = gp.epi_mode == EPI_POLYPHASE;
+        const int ld = fused ? gp.epi.epi_ld : 33;
         int grp = 0;
-        // Wait for accumulation group `grp` to land in TMEM; uniform across the warp.
+        // Wait for accumulation group g to land in TMEM; uniform across the warp.
         auto wait_group = [&](int g) -> bool {
             int ok = 1;
             if (lane == 0) {
@@ -274,17 +281,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&tmem_empty[g & 1]);
         };
-        // Output stage for one 32-column chunk already staged in sm.
-        auto store_chunk = [&](const TileCoord &tc, int c) {
+        // This lane's row of a 32-column chunk -> column-major staging block.
+        auto stage_row = [&](const float (&v)[32]) {
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc) sm[cc * ld + lane] = v[cc];
             __syncwarp();
+        };
+        // Output stage of one staged 32-column chunk.
+        auto store_chunk = [&](const TileCoord &tc, int c, const WarpRows &rows, ColCursor &cur) {
             const int64_t r0 = tc.m0 + 32 * quad;
             const int64_t n0 = tc.n0 + 32 * c;
-            if (gp.epi_mode == EPI_POLYPHASE) {
-                emit_block(sm, r0, n0, gp.epi, lane);
+            if (fused) {
+                emit_block(sm, rows, cur, gp.epi, lane);
+                col_advance(cur, 32, gp.epi);
             } else {
                 float *dst = gp.raw + (int64_t)tc.z * gp.raw_split_stride + r0 * gp.raw_ld + n0 + lane;
 #pragma unroll 4
-                for (int i = 0; i < 32; ++i) dst[(int64_t)i * gp.raw_ld] = sm[i * kEpiLd + lane];
+                for (int i = 0; i < 32; ++i) dst[(int64_t)i * gp.raw_ld] = sm[lane * ld + i];
             }
             __syncwarp();
         };
@@ -292,22 +305,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int64_t t = blockIdx.x; ok && t < gp.num_tiles; t += gridDim.x) {
             const TileCoord tc = decode_tile(t, gp, BN);
             const int ngroups = (tc.kb1 - tc.kb0 + gp.kb_group - 1) / gp.kb_group;
-            if (ngroups == 1 || BN != 128) {
+            WarpRows rows{};
+            ColCursor cur{};
+            if (fused) {
+                rows = warp_rows(tc.m0 + 32 * quad, gp.epi, lane, gbias, goff);
+                cur = col_cursor(tc.n0, gp.epi);
+            }
+            if (P != Prec::TF32x3 || BN != 128 || ngroups == 1) {
                 // One accumulation group: straight from TMEM to the output stage.
                 if (!(ok = wait_group(grp))) break;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t v[32];
+                    uint32_t u[32];
                     ptx::tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(32 * quad) << 16) +
-                                                (uint32_t)((grp & 1) * BN + 32 * c), v);
+                                                (uint32_t)((grp & 1) * BN + 32 * c), u);
                     ptx::tmem_wait_ld();
+                    float v[32];
 #pragma unroll
-                    for (int cc = 0; cc < 32; ++cc) sm[lane * kEpiLd + cc] = __uint_as_float(v[cc]);
-                    store_chunk(tc, c);
+                    for (int cc = 0; cc < 32; ++cc) v[cc] = __uint_as_float(u[cc]);
+                    if (c == BN / 32 - 1) release_group(grp);  // TMEM no longer needed
+                    stage_row(v);
+                    store_chunk(tc, c, rows, cur);
                 }
-                release_group(grp);
                 ++grp;
-            } else {
+            } else if constexpr (P == Prec::TF32x3 && BN == 128) {
                 // Several groups: each group's partial leaves TMEM and is added, with fp32
                 // round-to-nearest, into running sums held in registers (this thread's row,
                 // all 128 columns of the tile).  Keeps every tensor-core accumulation chain
@@ -317,22 +338,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = wait_group(grp))) break;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        uint32_t v[32];
+                        uint32_t u[32];
                         ptx::tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(32 * quad) << 16) +
-                                                    (uint32_t)((grp & 1) * BN + 32 * c), v);
+                                                    (uint32_t)((grp & 1) * BN + 32 * c), u);
                         ptx::tmem_wait_ld();
 #pragma unroll
                         for (int cc = 0; cc < 32; ++cc)
-                            sum[c][cc] = g == 0 ? __uint_as_float(v[cc]) : sum[c][cc] + __uint_as_float(v[cc]);
+                            sum[c][cc] = g == 0 ? __uint_as_float(u[cc]) : sum[c][cc] + __uint_as_float(u[cc]);
                     }
                     release_group(grp);
                 }
                 if (!ok) break;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-#pragma unroll
-                    for (int cc = 0; cc < 32; ++cc) sm[lane * kEpiLd + cc] = sum[c][cc];
-                    store_chunk(tc, c);
+                    stage_row(sum[c]);
+                    store_chunk(tc, c, rows, cur);
                 }
             }
         }

@@ -51,16 +51,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Wait until the phase of `bar` with the given parity has completed.  Bounded: gives up
-// after limit_ns nanoseconds of global time, or as soon as *abort becomes non-zero (abort
+// once limit_ns nanoseconds of global time have passed (at once when limit_ns is 0 and the
+// phase is not complete on the first poll), or as soon as *abort becomes non-zero (abort
 // may be null).  Returns true when the phase completed.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
                                           const volatile int *abort) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (limit_ns == 0) return false;
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t i = 1;; ++i) {
+    for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
         if (abort && *abort) return false;
-        if ((i & 63u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 
