@@ -159,6 +159,32 @@ ctr_status ctr_forward(ctr_plan_t plan, const void *x, const void *w_packed, con
                        void *y, void *stream);
 
 /*
+ * ctr_forward for callers that cannot allocate device memory (a host framework whose
+ * allocator owns all device memory, code running while a CUDA graph is captured, real-time
+ * audio callbacks).  The source pages have no counterpart of this call.
+ *   plan      a plan from ctr_plan_create; no ctr_prepack_weight, workspace binding or other
+ *             device allocation is needed for it
+ *   x, bias   device inputs as for ctr_forward (bias may be NULL)
+ *   w         device weight in its torch layout [C_in][C_out][k...] (not packed: every call
+ *             packs it into the library's scratch)
+ *   y         device output as for ctr_forward
+ *   stream    cudaStream_t as void*
+ * Scratch (packed weight, staged input, split-K partials, a status word) lives in one
+ * static 32 MiB device array that the CUDA driver reserves on each device that loads the
+ * library and keeps until the process exits.  Plans needing more than that (the packed
+ * weight plus ctr_workspace_bytes plus 256 bytes) get CTR_ERR_NO_WORKSPACE before anything
+ * runs.  This call performs no cudaMalloc, cudaFree or other allocation.  Its first call on
+ * a device looks up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  Every call shares the one
+ * array: calls whose GPU work overlaps (different streams, or several host threads) race on
+ * it and must be serialised by the caller.  Bounded-wait timeouts are recorded in the
+ * array's status word, which this call clears and never reads back (it does not
+ * synchronise).  Returns as ctr_forward otherwise.
+ */
+ctr_status ctr_forward_noalloc(ctr_plan_t plan, const void *x, const void *w, const void *bias,
+                               void *y, void *stream);
+
+/*
  * Synchronise stream, then read and clear the plan's device status word.  Returns CTR_OK,
  * CTR_ERR_DEVICE_TIMEOUT when a kernel's bounded wait gave up since the last check (its
  * output is then incomplete), or CTR_ERR_CUDA.

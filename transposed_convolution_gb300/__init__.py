@@ -8,7 +8,8 @@ any non-OK status from the library raises ``CtrError``.
 Low level (same names as the C ABI): ``ctr_plan_create``, ``ctr_plan_set_activation``,
 ``ctr_plan_set_path``, ``ctr_plan_get_path``, ``ctr_plan_output_shape``,
 ``ctr_packed_weight_bytes``, ``ctr_workspace_bytes``, ``ctr_plan_bind_workspace``,
-``ctr_prepack_weight``, ``ctr_forward``, ``ctr_plan_check``, ``ctr_plan_set_wait_limit_ns``,
+``ctr_prepack_weight``, ``ctr_forward``, ``ctr_forward_noalloc``, ``ctr_plan_check``,
+``ctr_plan_set_wait_limit_ns``,
 ``ctr_plan_set_timing_events``, ``ctr_plan_describe``, ``ctr_plan_destroy``,
 ``ctr_status_string``, ``ctr_launch_count``.
 
@@ -57,6 +58,7 @@ SIGNATURES = {
     "ctr_plan_bind_workspace": (ctypes.c_int, [_vp, _vp, ctypes.c_size_t]),
     "ctr_prepack_weight": (ctypes.c_int, [_vp, _vp, _vp, _vp]),
     "ctr_forward": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp]),
+    "ctr_forward_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp]),
     "ctr_plan_check": (ctypes.c_int, [_vp, _vp]),
     "ctr_plan_set_wait_limit_ns": (ctypes.c_int, [_vp, ctypes.c_uint64]),
     "ctr_plan_set_timing_events": (ctypes.c_int, [_vp, _vp, _vp]),
@@ -174,6 +176,13 @@ def ctr_prepack_weight(plan, w_ptr, w_packed_ptr, stream):
 
 def ctr_forward(plan, x_ptr, w_packed_ptr, bias_ptr, y_ptr, stream):
     _check(lib.ctr_forward(plan, x_ptr, w_packed_ptr, bias_ptr, y_ptr, stream), "ctr_forward")
+
+
+def ctr_forward_noalloc(plan, x_ptr, w_ptr, bias_ptr, y_ptr, stream):
+    """The allocation-free forward: scratch in the library's static device array, weight
+    passed in its torch layout and packed on every call (see include/ctr.h)."""
+    _check(lib.ctr_forward_noalloc(plan, x_ptr, w_ptr, bias_ptr, y_ptr, stream),
+           "ctr_forward_noalloc")
 
 
 def ctr_plan_check(plan, stream):

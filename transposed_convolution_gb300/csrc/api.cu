@@ -184,6 +184,11 @@ int choose_path(const ctr_plan_s *pl) {
     return (pl->C_in >= 16 && T * pl->C_out >= 64) ? CTR_PATH_COL2IM : CTR_PATH_GATHER;
 }
 
+}  // namespace
+
+namespace ctr {
+namespace {
+
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static bool tried = false;
@@ -200,6 +205,8 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     }
     return fn;
 }
+
+}  // namespace
 
 // 2-D tiled tensor map over a row-major [rows][inner] matrix, box [box_rows][128 bytes],
 // 128-byte swizzle (the K-major SWIZZLE_128B operand layout of tcgen05.mma), zero fill.
@@ -253,7 +260,10 @@ EpiParams make_epi(const ctr_plan_s *pl, const void *bias, void *y) {
     return e;
 }
 
-}  // namespace
+}  // namespace ctr
+
+using ctr::encode_2d;
+using ctr::make_epi;
 
 namespace ctr {
 void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }

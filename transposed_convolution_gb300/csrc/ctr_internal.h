@@ -127,6 +127,14 @@ cudaError_t launch_fill_bias(const ctr_plan_s *pl, const void *bias, void *y, cu
 cudaError_t launch_gemm_tc(const ctr_plan_s *pl, const CUtensorMap *maps, const GemmParams &gp,
                            cudaStream_t st);
 
+// 2-D tiled tensor map over a row-major [rows][inner] operand matrix, box [box_rows][128
+// bytes], 128-byte swizzle, zero fill (api.cu).
+bool encode_2d(CUtensorMap *map, const void *base, bool bf16, uint64_t inner, uint64_t rows,
+               uint32_t box_rows);
+
+// Output mapping of a tensor-core plan (api.cu).
+EpiParams make_epi(const ctr_plan_s *pl, const void *bias, void *y);
+
 // Counter of launched kernels (monotonic, process-wide).
 void count_launches(uint64_t n);
 
