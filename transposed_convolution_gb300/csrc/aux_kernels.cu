@@ -248,8 +248,7 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ raw, EpiParams ep
                                      int64_t split_stride, int splits, int64_t row_blocks,
                                      int64_t col_blocks) {
     __shared__ float sm_all[4][32 * kEpiLdMax];
-    __shared__ int64_t goff_all[4][32];
-    __shared__ float gbias_all[4][32];
+    __shared__ GroupTables tab_all[4];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float *sm = sm_all[warp];
     const int64_t blk = (int64_t)blockIdx.x * 4 + warp;
@@ -263,7 +262,7 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ raw, EpiParams ep
         sm[lane * ep.epi_ld + i] = s;
     }
     __syncwarp();
-    const WarpRows rows = warp_rows(r0, ep, lane, gbias_all[warp], goff_all[warp]);
+    const WarpRows rows = warp_rows(r0, ep, lane, &tab_all[warp]);
     emit_block(sm, rows, col_cursor(c0, ep), ep, lane);
 }
 

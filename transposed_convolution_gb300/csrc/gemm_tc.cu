@@ -40,7 +40,7 @@ namespace {
 
 constexpr int kThreads = 192;
 constexpr int kEpiWarps = 4;
-constexpr int kEpiTabBytes = 32 * (4 + 8);  // per epilogue warp: group bias + offset tables
+constexpr int kEpiTabBytes = (int)sizeof(GroupTables);  // per epilogue warp
 constexpr int kEpiBytes = kEpiWarps * (32 * kEpiLdMax * 4 + kEpiTabBytes);
 constexpr int kSmemBudget = 227 * 1024;
 constexpr uint64_t kDrainLimitNs = 2000000000ull;
@@ -257,10 +257,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ epilogue
         const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad + 31
         float *sm = epi_smem + (warp - 2) * 32 * kEpiLdMax;
-        uint8_t *tab = reinterpret_cast<uint8_t *>(epi_smem + kEpiWarps * 32 * kEpiLdMax) +
-                       (warp - 2) * kEpiTabBytes;
-        int64_t *goff = reinterpret_cast<int64_t *>(tab);
-        float *gbias = reinterpret_cast<float *>(tab + 32 * 8);
+        GroupTables *tab = reinterpret_cast<GroupTables *>(
+            reinterpret_cast<uint8_t *>(epi_smem + kEpiWarps * 32 * kEpiLdMax) +
+            (warp - 2) * kEpiTabBytes);
         const bool fused = gp.epi_mode == EPI_POLYPHASE;
         const int ld = fused ? gp.epi.epi_ld : 33;
         int grp = 0;
@@ -308,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             WarpRows rows{};
             ColCursor cur{};
             if (fused) {
-                rows = warp_rows(tc.m0 + 32 * quad, gp.epi, lane, gbias, goff);
+                rows = warp_rows(tc.m0 + 32 * quad, gp.epi, lane, tab);
                 cur = col_cursor(tc.n0, gp.epi);
             }
             if (P != Prec::TF32x3 || BN != 128 || ngroups == 1) {
