@@ -155,6 +155,21 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ our arm
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of a list of floats over all ranks of the default process group
+    (the slowest rank sets the job's time)."""
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def aggregate_rate(world, units_per_rank, ms):
+    """Whole-job throughput: the units every rank processed in `ms` milliseconds, in units/s
+    divided by 1e9 (GFLOP/s for FLOP units)."""
+    return world * units_per_rank / (ms / 1e3) / 1e9
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import transposed_convolution_gb300 as ctr
@@ -272,9 +287,7 @@ def run_ours(args, rank, world, local_rank):
                for j in range(nl)]
     total_ms = sum(step_ms)
     if world > 1:
-        tt = torch.tensor([total_ms] + kern_ms, dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms, kern_ms = float(tt[0]), [float(v) for v in tt[1:]]
+        total_ms, *kern_ms = max_over_ranks([total_ms] + kern_ms, dev)
 
     # End to end through the public API: pinned host x -> device, every layer, y -> pinned host.
     x_host = torch.from_numpy(np.ascontiguousarray(layers[0].x)).to(tdts[0]).pin_memory()
@@ -344,7 +357,7 @@ def run_ours(args, rank, world, local_rank):
 
     result = {
         "metric": "ConvTranspose GFLOP/s and % of roofline (tensor peak vs HBM) per call",
-        "value": round(world * flops / (ms_per_step / 1e3) / 1e9, 1),
+        "value": round(aggregate_rate(world, flops, ms_per_step), 1),
         "unit": "GFLOP/s",
         "n_gpus": world,
         "steps": K,
@@ -367,7 +380,7 @@ def run_ours(args, rank, world, local_rank):
                      "kernel": kname, "layer": j, "kernel_us": round(kern_ms[j] * 1e3, 3),
                      "peak_source": peak_note},
         "layer_kernel_us": [round(v * 1e3, 3) for v in kern_ms],
-        "e2e": {"value": round(world * flops / (e2e_ms / 1e3) / 1e9, 1), "unit": "GFLOP/s",
+        "e2e": {"value": round(aggregate_rate(world, flops, e2e_ms), 1), "unit": "GFLOP/s",
                 "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
                 "d2h_bytes_per_step": int(y_host.numel() * y_host.element_size()),
                 "ms_per_step": round(e2e_ms, 5)},

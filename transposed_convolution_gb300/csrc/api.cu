@@ -62,7 +62,7 @@ int op_planes(const ctr_plan_s *pl) { return pl->dtype == CTR_BF16 ? 1 : 2; }
 
 bool is_tc_path(int path) { return path == CTR_PATH_POLYPHASE || path == CTR_PATH_COL2IM; }
 
-// Estimated clocks of one K slice of a 128 x BN tile on one SM (tensor-pipe time).
+// Estimated clocks of one K slice of a 128-position x BN-row tile on one SM (tensor pipe).
 double slice_clocks(Prec prec, int bn) { return prec == Prec::TF32x3 ? 6.0 * bn : 2.0 * bn; }
 
 // K slices per tensor-core accumulation group in 3xTF32 mode (256 fp32 K elements).  The
@@ -73,10 +73,6 @@ double slice_clocks(Prec prec, int bn) { return prec == Prec::TF32x3 ? 6.0 * bn 
 constexpr int kTf32Group = 8;
 constexpr int kNoGroup = 1 << 30;
 
-// Choose the column tile and the split-K factor: fewest estimated clocks over
-// BN in {128, 256} and splits in 1..16, counting whole waves of tiles over the SMs and
-// the extra pass that sums split-K partials.  Grouped accumulation needs BN = 128 (the
-// running sums of a 128-column row fit in one thread's registers).
 int tf32_group() {
     // Diagnostic override of the group length (slices); 0 or negative disables grouping.
     const char *e = std::getenv("CTR_TF32_GROUP");
@@ -85,29 +81,41 @@ int tf32_group() {
     return v > 0 ? v : kNoGroup;
 }
 
+// Choose the phase-row tile BN in {64, 128, 256} and the split-K factor: fewest estimated
+// clocks, counting whole waves of tiles over the SMs, a tile's time as the largest of its
+// MMA time, its operand-load time and its output time, and the extra pass over split-K
+// partials.  Grouped
+// accumulation needs BN <= 128 (the running sums of a thread's 128 columns fit its
+// registers).
 void choose_tiling(ctr_plan_s *pl) {
     const Prec prec = prec_of(pl);
     const int group = prec == Prec::TF32x3 ? tf32_group() : kNoGroup;
     const int kb_total = (int)(pl->K_total * op_esize(pl) / ctr::kBKBytes);
-    const int num_m = (int)(pl->M_pad / ctr::kBM);
+    const int64_t num_p = std::max<int64_t>(1, ceil_div(pl->N_total, ctr::kBM));
     double best = 1e300;
     int best_bn = 128, best_sp = 1;
     // A forced split-K factor is clamped to the number of K slices.
     const int forced = pl->forced_split > 0 ? std::min(pl->forced_split, kb_total) : 0;
-    for (int bn : {128, 256}) {
-        const int64_t num_n = std::max<int64_t>(1, ceil_div(pl->N_total, bn));
+    for (int bn : {64, 128, 256}) {
+        const int64_t num_r = std::max<int64_t>(1, ceil_div(pl->M_rows, bn));
         for (int sp = 1; sp <= 16; ++sp) {
             if (forced > 0 && sp != forced) continue;
             if (sp > kb_total) break;
             if (sp > 1 && forced == 0 && kb_total / sp < 4) break;
-            const int64_t tiles = (int64_t)num_m * num_n * sp;
-            const int64_t waves = ceil_div(tiles, pl->num_sms);
             const double kbs = (double)ceil_div(kb_total, sp);
-            if (bn == 256 && kbs > group) continue;
-            double t = (double)waves * (kbs + 6.0) * slice_clocks(prec, bn);
+            if (bn > ctr::kMaxGroupedBN && kbs > group) continue;
+            const int64_t tiles = num_p * num_r * sp;
+            const int64_t waves = ceil_div(tiles, pl->num_sms);
+            // Per tile: tensor-pipe time, operand loads at ~50 B per clock per SM from L2,
+            // and output writes at ~20 B per clock per SM (the HBM share of one SM).
+            const double mma = kbs * slice_clocks(prec, bn);
+            const double load = kbs * (ctr::kBM + bn) * (double)ctr::kBKBytes * op_planes(pl) / 50.0;
+            const double epi = ctr::kBM * (double)bn * esize_io(pl) / 20.0 + 300.0;
+            const double tile = std::max(mma, std::max(load, epi));
+            double t = (double)waves * tile + 2000.0;
             if (sp > 1 || pl->path == CTR_PATH_COL2IM) {
                 // partials written once and read once, ~3.5 KB per clock for the whole GPU
-                t += (double)(sp + 1) * pl->M_pad * num_n * bn * 4.0 / 3500.0;
+                t += (double)(sp + 1) * num_p * ctr::kBM * num_r * bn * 4.0 / 3500.0;
             }
             if (t < best * 0.98) {
                 best = t;
@@ -118,10 +126,10 @@ void choose_tiling(ctr_plan_s *pl) {
     }
     pl->block_n = best_bn;
     pl->splits = best_sp;
-    pl->kb_group = best_bn == 128 ? group : kNoGroup;
-    pl->num_m_tiles = num_m;
-    pl->num_n_tiles = (int)std::max<int64_t>(1, ceil_div(pl->N_total, best_bn));
-    pl->num_tiles = (int64_t)pl->num_m_tiles * pl->num_n_tiles * pl->splits;
+    pl->kb_group = best_bn <= ctr::kMaxGroupedBN ? group : kNoGroup;
+    pl->num_p_tiles = (int)num_p;
+    pl->num_r_tiles = (int)std::max<int64_t>(1, ceil_div(pl->M_rows, best_bn));
+    pl->num_tiles = (int64_t)pl->num_p_tiles * pl->num_r_tiles * pl->splits;
 }
 
 // Derive the GEMM geometry, tiling, packed size and workspace layout from the path.
@@ -156,7 +164,7 @@ void layout_plan(ctr_plan_s *pl) {
     }
     pl->S_pad = (int)(pl->S <= ctr::kBM ? next_pow2(pl->S) : round_up(pl->S, ctr::kBM));
     pl->M_rows = pl->C_out * pl->S_pad;
-    pl->M_pad = round_up(pl->M_rows, ctr::kBM);
+    pl->M_pad = round_up(pl->M_rows, 64);
     pl->K_total = pl->m[0] * pl->m[1] * pl->C_in_pad;
     pl->N_total = pl->B * pl->P[0] * pl->P[1];
     choose_tiling(pl);
@@ -166,8 +174,7 @@ void layout_plan(ctr_plan_s *pl) {
     size_t off = align256(pl->ws_stage_bytes);
     if (pl->path == CTR_PATH_COL2IM || pl->splits > 1) {
         pl->ws_off_raw = off;
-        pl->ws_raw_bytes = (size_t)pl->splits * pl->M_pad *
-                           ((size_t)pl->num_n_tiles * pl->block_n) * sizeof(float);
+        pl->ws_raw_bytes = (size_t)ctr::raw_split_stride_of(pl) * pl->splits * sizeof(float);
         off = align256(off + pl->ws_raw_bytes);
     }
     pl->ws_bytes_needed = (pl->ws_stage_bytes || pl->ws_raw_bytes) ? off : 0;
@@ -247,17 +254,110 @@ EpiParams make_epi(const ctr_plan_s *pl, const void *bias, void *y) {
     e.out_bf16 = pl->dtype == CTR_BF16 ? 1 : 0;
     e.act = pl->act;
     e.slope = pl->slope;
-    // Row groups hold min(sx, 32) rows; a staging pitch congruent to that length modulo 32
-    // makes the output-order reads of the staging block conflict-free.
-    e.epi_ld = 32 + (int)(std::min<int64_t>(pl->s[1], 32) % 32);
-    if (e.epi_ld > ctr::kEpiLdMax) e.epi_ld = 33;
-    const int64_t sx = pl->s[1];
-    const bool pow2 = (sx & (sx - 1)) == 0;
-    e.fast = (pl->S == pl->S_pad && pow2 && (sx <= 32 || sx % 32 == 0)) ? 1 : 0;
-    e.nj = (int)std::min<int64_t>(sx, 32);
-    e.lg_nj = 0;
-    while ((1 << e.lg_nj) < e.nj) ++e.lg_nj;
+    // Output-stage variant: whole phase sets per 32-column chunk when S = S_pad is a power
+    // of two <= 32 (1-D, or 2-D with sx = sy = 2 or 4), 32 consecutive phases of one
+    // channel when a 1-D S is a multiple of 32, else the generic per-element stage.
+    const int64_t sx = pl->s[1], sy = pl->s[0];
+    const bool whole = pl->S == pl->S_pad;
+    int nx = 0;  // run length of the fast variants
+    e.kind = EPI_KIND_GENERIC;
+    if (whole && sy == 1) {
+        switch (sx) {
+            case 1: e.kind = EPI_KIND_1D_S1; nx = 1; break;
+            case 2: e.kind = EPI_KIND_1D_S2; nx = 2; break;
+            case 4: e.kind = EPI_KIND_1D_S4; nx = 4; break;
+            case 8: e.kind = EPI_KIND_1D_S8; nx = 8; break;
+            case 16: e.kind = EPI_KIND_1D_S16; nx = 16; break;
+            case 32: e.kind = EPI_KIND_1D_S32; nx = 32; break;
+            default:
+                if (sx % 32 == 0) {
+                    e.kind = EPI_KIND_1D_LARGE;
+                    nx = 32;
+                }
+        }
+    } else if (whole && sx == sy && (sx == 2 || sx == 4)) {
+        e.kind = sx == 2 ? EPI_KIND_2D_S2x2 : EPI_KIND_2D_S4x4;
+        nx = (int)sx;
+    }
+    // Widest aligned store of an interior run: the run length, the run-to-run step of one
+    // position (sx elements), the padding offset and the output row pitch must all be
+    // multiples of it, so every thread and row share the same alignment.
+    const int es = pl->dtype == CTR_BF16 ? 2 : 4;
+    e.store_bytes = es;
+    for (int w : {16, 8, 4}) {
+        if (nx > 0 && (nx * es) % w == 0 && (sx * es) % w == 0 && (pl->p[1] * es) % w == 0 &&
+            (pl->out[1] * es) % w == 0) {
+            e.store_bytes = w;
+            break;
+        }
+    }
     return e;
+}
+
+int64_t raw_ld_of(const ctr_plan_s *pl) { return (int64_t)pl->num_r_tiles * pl->block_n; }
+
+int64_t raw_split_stride_of(const ctr_plan_s *pl) {
+    return (int64_t)pl->num_p_tiles * kBM * raw_ld_of(pl);
+}
+
+// The tensor-core paths after validation: stage x, encode the operand maps, run the GEMM
+// (with timing events around it when given), then the split-K reduce or col2im.  ws holds
+// the staged input and the raw partials at the plan's offsets; status is the device status
+// word the GEMM reports bounded-wait timeouts into.
+cudaError_t run_tc_path(const ctr_plan_s *pl, const void *x, const void *w_packed,
+                        const void *bias, void *y, char *ws, uint32_t *status,
+                        cudaEvent_t ev_before, cudaEvent_t ev_after, cudaStream_t st) {
+    cudaError_t e;
+    void *xs = ws + pl->ws_off_stage;
+    float *raw = pl->ws_raw_bytes ? reinterpret_cast<float *>(ws + pl->ws_off_raw) : nullptr;
+    if ((e = launch_stage_x(pl, x, xs, st)) != cudaSuccess) return e;
+
+    const bool bf16 = pl->dtype == CTR_BF16;
+    const int es = bf16 ? 2 : 4;
+    const size_t w_plane = (size_t)pl->M_pad * pl->K_total * es;
+    const size_t x_plane = (size_t)pl->N_total * pl->C_in_pad * es;
+    // maps: staged input (128-position boxes), packed weight (block_n-row boxes), lo planes.
+    CUtensorMap maps[4];
+    bool ok = encode_2d(&maps[0], xs, bf16, pl->C_in_pad, pl->N_total, kBM) &&
+              encode_2d(&maps[1], w_packed, bf16, pl->K_total, pl->M_pad, pl->block_n);
+    if (!bf16) {
+        ok = ok &&
+             encode_2d(&maps[2], static_cast<char *>(xs) + x_plane, false, pl->C_in_pad,
+                       pl->N_total, kBM) &&
+             encode_2d(&maps[3], static_cast<const char *>(w_packed) + w_plane, false,
+                       pl->K_total, pl->M_pad, pl->block_n);
+    } else {
+        maps[2] = maps[0];
+        maps[3] = maps[1];
+    }
+    if (!ok) return cudaErrorInvalidValue;
+
+    GemmParams gp;
+    std::memset(&gp, 0, sizeof(gp));
+    gp.num_p_tiles = pl->num_p_tiles;
+    gp.num_r_tiles = pl->num_r_tiles;
+    gp.splits = pl->splits;
+    gp.num_tiles = pl->num_tiles;
+    gp.kb_total = (int)(pl->K_total * es / kBKBytes);
+    gp.kb_per_tap = (int)(pl->C_in_pad * es / kBKBytes);
+    gp.kb_group = pl->kb_group;
+    gp.mx = (int)pl->m[1];
+    gp.Px = pl->P[1];
+    const bool fused = pl->path == CTR_PATH_POLYPHASE && pl->splits == 1;
+    gp.epi_mode = fused ? EPI_POLYPHASE : EPI_RAW;
+    gp.epi = make_epi(pl, bias, y);
+    gp.raw = raw;
+    gp.raw_ld = raw_ld_of(pl);
+    gp.raw_split_stride = raw_split_stride_of(pl);
+    gp.status = status;
+    gp.wait_limit_ns = pl->wait_limit_ns;
+    if (ev_before && (e = cudaEventRecord(ev_before, st)) != cudaSuccess) return e;
+    if ((e = launch_gemm_tc(pl, maps, gp, st)) != cudaSuccess) return e;
+    if (ev_after && (e = cudaEventRecord(ev_after, st)) != cudaSuccess) return e;
+    if (pl->path == CTR_PATH_POLYPHASE && !fused)
+        return launch_splitk_reduce(pl, raw, gp.epi, gp.raw_ld, gp.raw_split_stride, st);
+    if (pl->path == CTR_PATH_COL2IM) return launch_col2im(pl, raw, gp.raw_ld, bias, y, st);
+    return cudaSuccess;
 }
 
 }  // namespace ctr
@@ -404,17 +504,18 @@ ctr_status ctr_plan_describe(ctr_plan_t pl, char *buf, size_t len) {
                         : pl->path == CTR_PATH_COL2IM  ? "col2im"
                                                        : "gather";
     if (is_tc_path(pl->path)) {
+        const EpiParams ep = make_epi(pl, nullptr, nullptr);
         snprintf(buf, len,
-                 "path=%s prec=%s M=%lld(pad %lld, %d tiles) N=%lld(BN %d, %d tiles) "
+                 "path=%s prec=%s rows=%lld(pad %lld, BN %d, %d tiles) positions=%lld(%d tiles) "
                  "K=%lld splits=%d group=%d tiles=%lld sms=%d S=%d/%d taps=%lldx%lld "
-                 "pitch=%lldx%lld packed=%zu ws=%zu",
+                 "pitch=%lldx%lld epi=%d/%dB packed=%zu ws=%zu",
                  pname, pl->dtype == CTR_BF16 ? "bf16" : "3xtf32", (long long)pl->M_rows,
-                 (long long)pl->M_pad, pl->num_m_tiles, (long long)pl->N_total, pl->block_n,
-                 pl->num_n_tiles, (long long)pl->K_total, pl->splits,
+                 (long long)pl->M_pad, pl->block_n, pl->num_r_tiles, (long long)pl->N_total,
+                 pl->num_p_tiles, (long long)pl->K_total, pl->splits,
                  pl->kb_group == kNoGroup ? 0 : pl->kb_group, (long long)pl->num_tiles,
                  pl->num_sms, pl->S, pl->S_pad, (long long)pl->m[0], (long long)pl->m[1],
-                 (long long)pl->P[0], (long long)pl->P[1], pl->packed_bytes,
-                 pl->ws_bytes_needed);
+                 (long long)pl->P[0], (long long)pl->P[1], ep.kind, ep.store_bytes,
+                 pl->packed_bytes, pl->ws_bytes_needed);
     } else {
         snprintf(buf, len, "path=%s dtype=%s packed=%zu ws=0", pname,
                  pl->dtype == CTR_BF16 ? "bf16" : "f32", pl->packed_bytes);
@@ -466,61 +567,9 @@ ctr_status ctr_forward(ctr_plan_t pl, const void *x, const void *w_packed, const
         return ctr::launch_fill_bias(pl, bias, y, st) == cudaSuccess ? CTR_OK : CTR_ERR_CUDA;
     }
 
-    char *ws = static_cast<char *>(pl->ws);
-    void *xs = ws + pl->ws_off_stage;
-    float *raw = pl->ws_raw_bytes ? reinterpret_cast<float *>(ws + pl->ws_off_raw) : nullptr;
-    if (ctr::launch_stage_x(pl, x, xs, st) != cudaSuccess) return CTR_ERR_CUDA;
-
-    const bool bf16 = pl->dtype == CTR_BF16;
-    const size_t a_plane = (size_t)pl->M_pad * pl->K_total * op_esize(pl);
-    const size_t b_plane = (size_t)pl->N_total * pl->C_in_pad * op_esize(pl);
-    CUtensorMap maps[4];
-    bool ok = encode_2d(&maps[0], w_packed, bf16, pl->K_total, pl->M_pad, ctr::kBM) &&
-              encode_2d(&maps[1], xs, bf16, pl->C_in_pad, pl->N_total, pl->block_n);
-    if (!bf16) {
-        ok = ok &&
-             encode_2d(&maps[2], static_cast<const char *>(w_packed) + a_plane, false,
-                       pl->K_total, pl->M_pad, ctr::kBM) &&
-             encode_2d(&maps[3], static_cast<char *>(xs) + b_plane, false, pl->C_in_pad,
-                       pl->N_total, pl->block_n);
-    } else {
-        maps[2] = maps[0];
-        maps[3] = maps[1];
-    }
-    if (!ok) return CTR_ERR_CUDA;
-
-    GemmParams gp;
-    std::memset(&gp, 0, sizeof(gp));
-    gp.num_m_tiles = pl->num_m_tiles;
-    gp.num_n_tiles = pl->num_n_tiles;
-    gp.splits = pl->splits;
-    gp.num_tiles = pl->num_tiles;
-    gp.kb_total = (int)(pl->K_total * op_esize(pl) / ctr::kBKBytes);
-    gp.kb_per_tap = (int)(pl->C_in_pad * op_esize(pl) / ctr::kBKBytes);
-    gp.kb_group = pl->kb_group;
-    gp.mx = (int)pl->m[1];
-    gp.Px = pl->P[1];
-    const bool fused = pl->path == CTR_PATH_POLYPHASE && pl->splits == 1;
-    gp.epi_mode = fused ? ctr::EPI_POLYPHASE : ctr::EPI_RAW;
-    gp.epi = make_epi(pl, bias, y);
-    gp.raw = raw;
-    gp.raw_ld = (int64_t)pl->num_n_tiles * pl->block_n;
-    gp.raw_split_stride = pl->M_pad * gp.raw_ld;
-    gp.status = pl->d_status;
-    gp.wait_limit_ns = pl->wait_limit_ns;
-    if (timed && cudaEventRecord(pl->ev_before, st) != cudaSuccess) return CTR_ERR_CUDA;
-    if (ctr::launch_gemm_tc(pl, maps, gp, st) != cudaSuccess) return CTR_ERR_CUDA;
-    if (timed && cudaEventRecord(pl->ev_after, st) != cudaSuccess) return CTR_ERR_CUDA;
-
-    if (pl->path == CTR_PATH_POLYPHASE && !fused) {
-        if (ctr::launch_splitk_reduce(pl, raw, gp.epi, gp.raw_ld, gp.raw_split_stride, st) !=
-            cudaSuccess)
-            return CTR_ERR_CUDA;
-    } else if (pl->path == CTR_PATH_COL2IM) {
-        if (ctr::launch_col2im(pl, raw, gp.raw_ld, bias, y, st) != cudaSuccess)
-            return CTR_ERR_CUDA;
-    }
-    return CTR_OK;
+    const cudaError_t e = ctr::run_tc_path(pl, x, w_packed, bias, y, static_cast<char *>(pl->ws),
+                                           pl->d_status, pl->ev_before, pl->ev_after, st);
+    return e == cudaSuccess ? CTR_OK : CTR_ERR_CUDA;
 }
 
 ctr_status ctr_plan_check(ctr_plan_t pl, void *stream) {

@@ -241,33 +241,42 @@ __global__ void __launch_bounds__(256) stage_x_kernel(const void *__restrict__ x
 }
 
 // -------------------------------------------------------------------------- split-K reduce
-// Each warp sums the split-K partials of one 32 x 32 block of D in a fixed order (z = 0, 1,
-// ...), stages it column-major in shared memory and runs the same output stage as the fused
-// epilogue.
+// One thread per (phase position n, 32-row chunk r0): sums the split-K partials
+// raw[z][n][r0 .. r0+31] in a fixed order (z = 0, 1, ...) with 16-byte loads, then runs the
+// same output stage as the fused epilogue.
 __global__ void splitk_reduce_kernel(const float *__restrict__ raw, EpiParams ep, int64_t ld,
-                                     int64_t split_stride, int splits, int64_t row_blocks,
-                                     int64_t col_blocks) {
-    __shared__ float sm_all[4][32 * kEpiLdMax];
-    __shared__ GroupTables tab_all[4];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float *sm = sm_all[warp];
-    const int64_t blk = (int64_t)blockIdx.x * 4 + warp;
-    if (blk >= row_blocks * col_blocks) return;
-    const int64_t r0 = (blk / col_blocks) * 32;
-    const int64_t c0 = (blk % col_blocks) * 32;
-    for (int i = 0; i < 32; ++i) {
-        const float *p = raw + (r0 + i) * ld + c0 + lane;
-        float s = p[0];
-        for (int z = 1; z < splits; ++z) s += p[(int64_t)z * split_stride];
-        sm[lane * ep.epi_ld + i] = s;
+                                     int64_t split_stride, int splits, int64_t n_rows,
+                                     int64_t r_chunks) {
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= n_rows * r_chunks) return;
+    const int64_t n = idx / r_chunks;
+    const int64_t r0 = (idx - n * r_chunks) * 32;
+    const float4 *p = reinterpret_cast<const float4 *>(raw + n * ld + r0);
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 a = p[i];
+        v[4 * i] = a.x;
+        v[4 * i + 1] = a.y;
+        v[4 * i + 2] = a.z;
+        v[4 * i + 3] = a.w;
     }
-    __syncwarp();
-    const WarpRows rows = warp_rows(r0, ep, lane, &tab_all[warp]);
-    emit_block(sm, rows, col_cursor(c0, ep), ep, lane);
+    for (int z = 1; z < splits; ++z) {
+        const float4 *q = reinterpret_cast<const float4 *>(raw + z * split_stride + n * ld + r0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 a = q[i];
+            v[4 * i] += a.x;
+            v[4 * i + 1] += a.y;
+            v[4 * i + 2] += a.z;
+            v[4 * i + 3] += a.w;
+        }
+    }
+    emit_cols(v, decode_pos(n, ep), r0, ep);
 }
 
 // -------------------------------------------------------------------------- col2im
-// y[b, oc, oy, ox] = bias + sum of col[(oc, ty, tx), (b, iy, ix)] over the taps that reach
+// y[b, oc, oy, ox] = bias + sum of col[(b, iy, ix), (oc, ty, tx)] over the taps that reach
 // (oy, ox) (the same divisibility rule as the gather kernel), summed over split-K partials
 // in a fixed order.  Only reachable taps are visited ("[WebGPU] optimizations for audio
 // models", review commit: each chunk gathers only into the box its rows reach).
@@ -294,7 +303,7 @@ __global__ void col2im_kernel(const float *__restrict__ col, int64_t ld, int64_t
                 if (ix >= g.W) continue;
                 const int64_t r = oc * S_pad + ty * g.kx + tx;
                 const int64_t n = (b * g.H + iy) * g.W + ix;
-                const float *p = col + r * ld + n;
+                const float *p = col + n * ld + r;
                 for (int z = 0; z < splits; ++z) acc += p[(int64_t)z * split_stride];
             }
         }
@@ -383,11 +392,12 @@ cudaError_t launch_stage_x(const ctr_plan_s *pl, const void *x, void *xs, cudaSt
 
 cudaError_t launch_splitk_reduce(const ctr_plan_s *pl, const float *raw, const EpiParams &ep,
                                  int64_t raw_ld, int64_t split_stride, cudaStream_t st) {
-    const int64_t row_blocks = ceil_div(std::min<int64_t>(pl->M_rows, pl->M_pad), 32);
-    const int64_t col_blocks = raw_ld / 32;
-    const int64_t blocks = ceil_div(row_blocks * col_blocks, 4);
-    splitk_reduce_kernel<<<(unsigned)blocks, 128, 0, st>>>(raw, ep, raw_ld, split_stride,
-                                                           pl->splits, row_blocks, col_blocks);
+    const int64_t n_rows = pl->N_total;
+    const int64_t r_chunks = ceil_div(std::min<int64_t>(pl->M_rows, raw_ld), 32);
+    const int64_t total = n_rows * r_chunks;
+    if (total == 0) return cudaSuccess;
+    splitk_reduce_kernel<<<grid_for(total, 128), 128, 0, st>>>(raw, ep, raw_ld, split_stride,
+                                                             pl->splits, n_rows, r_chunks);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -397,7 +407,7 @@ cudaError_t launch_col2im(const ctr_plan_s *pl, const float *col, int64_t col_ld
     const Geo g = geo_of(pl);
     const int64_t total = g.B * g.C_out * g.Ho * g.Wo;
     if (total == 0) return cudaSuccess;
-    const int64_t split_stride = pl->M_pad * col_ld;
+    const int64_t split_stride = raw_split_stride_of(pl);
     col2im_kernel<<<grid_for(total, kBlock), kBlock, 0, st>>>(col, col_ld, split_stride,
                                                               pl->splits, pl->S_pad, bias, y, g,
                                                               total);

@@ -19,14 +19,21 @@ constexpr int kBKBytes = 128;
 enum class Prec : int { BF16 = 0, TF32x3 = 1 };
 enum EpiMode : int { EPI_POLYPHASE = 0, EPI_RAW = 1 };
 
-// Output mapping of a GEMM result D[r, n] (shared by the fused epilogue and the split-K
+// Output-stage variants (chosen per plan on the host; see epilogue.cuh).
+enum EpiKind : int {
+    EPI_KIND_GENERIC = 0,
+    EPI_KIND_1D_S1, EPI_KIND_1D_S2, EPI_KIND_1D_S4, EPI_KIND_1D_S8, EPI_KIND_1D_S16,
+    EPI_KIND_1D_S32, EPI_KIND_2D_S2x2, EPI_KIND_2D_S4x4, EPI_KIND_1D_LARGE
+};
+
+// Output mapping of a GEMM result D[n, r] (shared by the fused epilogue and the split-K
 // reduce).  Everything is in the 2-D form; 1-D plans have sy = 1, py = 0, Py = Qvy = 1,
 // Hout = 1.
-//   row r    -> oc = r / S_pad, j = r % S_pad (phase, valid when j < S), jy = j / sx,
-//               jx = j % sx
-//   column n -> b = n / (Py*Px), qy = (n / Px) % Py, qx = n % Px (valid when b < B,
-//               qy < Qvy, qx < Qvx)
-//   output   -> y[b, oc, sy*qy + jy - py, sx*qx + jx - px] when inside [0, Hout) x [0, Wout)
+//   position n -> b = n / (Py*Px), qy = (n / Px) % Py, qx = n % Px (valid when b < B,
+//                 qy < Qvy, qx < Qvx)
+//   row r      -> oc = r / S_pad, j = r % S_pad (phase, valid when j < S), jy = j / sx,
+//                 jx = j % sx
+//   output     -> y[b, oc, sy*qy + jy - py, sx*qx + jx - px] when inside [0, Hout) x [0, Wout)
 struct EpiParams {
     int S, S_pad, sx, sy, px, py;
     int64_t Px, Py, Qvx, Qvy;
@@ -36,22 +43,24 @@ struct EpiParams {
     int out_bf16;       // 1: bf16 I/O, 0: fp32
     int act;            // ctr_act
     float slope;
-    int epi_ld;         // pitch (floats) of the column-major staging block, 32..63
-    int fast;           // 1: S == S_pad and sx is a power of two with sx <= 32 or 32 | sx
-    int nj, lg_nj;      // rows per row group in the fast path: min(sx, 32), its log2
+    int kind;           // EpiKind
+    int store_bytes;    // width of the aligned vector stores of interior runs (16, 8, 4, 2)
 };
 
+// The tensor-core GEMM D[n, r] = sum_k Xs[n + shift(k), k] * A[r, k]: n runs over staged
+// phase positions (TMEM lanes, 128 per tile), r over packed weight rows (TMEM columns, BN per
+// tile).
 struct GemmParams {
-    int num_m_tiles, num_n_tiles, splits;
+    int num_p_tiles, num_r_tiles, splits;
     int64_t num_tiles;
     int kb_total;       // K slices over all taps
     int kb_per_tap;     // K slices per tap (C_in_pad * esize / 128)
     int kb_group;       // K slices per tensor-core accumulation group (see gemm_tc.cu)
     int mx;             // taps along x: tap g -> (uy, ux) = (g / mx, g % mx)
-    int64_t Px;         // column shift of one tap step along y
+    int64_t Px;         // position shift of one tap step along y
     int epi_mode;
     EpiParams epi;
-    float *raw;         // EPI_RAW: D goes to raw[z][r][n] with leading dimension raw_ld
+    float *raw;         // EPI_RAW: D goes to raw[z][n][r] with leading dimension raw_ld
     int64_t raw_ld;
     int64_t raw_split_stride;
     uint32_t *status;   // device status word (bit flags of bounded waits that gave up)
@@ -89,10 +98,11 @@ struct ctr_plan_s {
     int64_t M_rows, M_pad;
     int64_t K_total;    // GEMM K = taps * C_in_pad
     int64_t N_total;    // GEMM columns = B * P[0] * P[1]
-    int block_n;
+    int block_n;        // phase rows per tile (MMA N): 64, 128 or 256
     int splits;
     int kb_group;       // K slices per accumulation group; >= slices per tile = no flush
-    int num_m_tiles, num_n_tiles;
+    int num_p_tiles;    // tiles of 128 staged positions
+    int num_r_tiles;    // tiles of block_n packed weight rows
     int64_t num_tiles;
 
     size_t packed_bytes;
@@ -121,6 +131,9 @@ cudaError_t launch_prepack(const ctr_plan_s *pl, const void *w, void *w_packed, 
 cudaError_t launch_stage_x(const ctr_plan_s *pl, const void *x, void *xs, cudaStream_t st);
 cudaError_t launch_splitk_reduce(const ctr_plan_s *pl, const float *raw, const EpiParams &ep,
                                  int64_t raw_ld, int64_t split_stride, cudaStream_t st);
+// Leading dimension (floats) and split stride of the raw [z][n][r] buffer of a plan.
+int64_t raw_ld_of(const ctr_plan_s *pl);
+int64_t raw_split_stride_of(const ctr_plan_s *pl);
 cudaError_t launch_col2im(const ctr_plan_s *pl, const float *col, int64_t col_ld,
                           const void *bias, void *y, cudaStream_t st);
 cudaError_t launch_fill_bias(const ctr_plan_s *pl, const void *bias, void *y, cudaStream_t st);
@@ -135,10 +148,18 @@ bool encode_2d(CUtensorMap *map, const void *base, bool bf16, uint64_t inner, ui
 // Output mapping of a tensor-core plan (api.cu).
 EpiParams make_epi(const ctr_plan_s *pl, const void *bias, void *y);
 
+// Staging, GEMM and reduce/col2im of a tensor-core plan with explicit scratch (api.cu).
+cudaError_t run_tc_path(const ctr_plan_s *pl, const void *x, const void *w_packed,
+                        const void *bias, void *y, char *ws, uint32_t *status,
+                        cudaEvent_t ev_before, cudaEvent_t ev_after, cudaStream_t st);
+
 // Counter of launched kernels (monotonic, process-wide).
 void count_launches(uint64_t n);
 
 // Bytes of dynamic shared memory a GEMM instantiation uses.
 size_t gemm_smem_bytes(Prec prec, int block_n);
+
+// Largest phase-row tile whose accumulation groups fit the epilogue's registers.
+constexpr int kMaxGroupedBN = 128;
 
 }  // namespace ctr

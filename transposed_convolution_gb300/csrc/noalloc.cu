@@ -82,55 +82,7 @@ extern "C" ctr_status ctr_forward_noalloc(ctr_plan_t pl, const void *x, const vo
     if (pl->N_total == 0)
         return ctr::launch_fill_bias(pl, bias, y, st) == cudaSuccess ? CTR_OK : CTR_ERR_CUDA;
 
-    char *ws = scratch + ws_off;
-    void *xs = ws + pl->ws_off_stage;
-    float *raw = pl->ws_raw_bytes ? reinterpret_cast<float *>(ws + pl->ws_off_raw) : nullptr;
-    if (ctr::launch_stage_x(pl, x, xs, st) != cudaSuccess) return CTR_ERR_CUDA;
-
-    const bool bf16 = pl->dtype == CTR_BF16;
-    const int es = bf16 ? 2 : 4;
-    const size_t a_plane = (size_t)pl->M_pad * pl->K_total * es;
-    const size_t b_plane = (size_t)pl->N_total * pl->C_in_pad * es;
-    CUtensorMap maps[4];
-    bool ok = ctr::encode_2d(&maps[0], w_packed, bf16, pl->K_total, pl->M_pad, ctr::kBM) &&
-              ctr::encode_2d(&maps[1], xs, bf16, pl->C_in_pad, pl->N_total, pl->block_n);
-    if (!bf16) {
-        ok = ok &&
-             ctr::encode_2d(&maps[2], static_cast<char *>(w_packed) + a_plane, false, pl->K_total,
-                            pl->M_pad, ctr::kBM) &&
-             ctr::encode_2d(&maps[3], static_cast<char *>(xs) + b_plane, false, pl->C_in_pad,
-                            pl->N_total, pl->block_n);
-    } else {
-        maps[2] = maps[0];
-        maps[3] = maps[1];
-    }
-    if (!ok) return CTR_ERR_CUDA;
-
-    ctr::GemmParams gp{};
-    gp.num_m_tiles = pl->num_m_tiles;
-    gp.num_n_tiles = pl->num_n_tiles;
-    gp.splits = pl->splits;
-    gp.num_tiles = pl->num_tiles;
-    gp.kb_total = (int)(pl->K_total * es / ctr::kBKBytes);
-    gp.kb_per_tap = (int)(pl->C_in_pad * es / ctr::kBKBytes);
-    gp.kb_group = pl->kb_group;
-    gp.mx = (int)pl->m[1];
-    gp.Px = pl->P[1];
-    const bool fused = pl->path == CTR_PATH_POLYPHASE && pl->splits == 1;
-    gp.epi_mode = fused ? ctr::EPI_POLYPHASE : ctr::EPI_RAW;
-    gp.epi = ctr::make_epi(pl, bias, y);
-    gp.raw = raw;
-    gp.raw_ld = (int64_t)pl->num_n_tiles * pl->block_n;
-    gp.raw_split_stride = pl->M_pad * gp.raw_ld;
-    gp.status = status;
-    gp.wait_limit_ns = pl->wait_limit_ns;
-    if (ctr::launch_gemm_tc(pl, maps, gp, st) != cudaSuccess) return CTR_ERR_CUDA;
-    if (pl->path == CTR_PATH_POLYPHASE && !fused) {
-        if (ctr::launch_splitk_reduce(pl, raw, gp.epi, gp.raw_ld, gp.raw_split_stride, st) !=
-            cudaSuccess)
-            return CTR_ERR_CUDA;
-    } else if (pl->path == CTR_PATH_COL2IM) {
-        if (ctr::launch_col2im(pl, raw, gp.raw_ld, bias, y, st) != cudaSuccess) return CTR_ERR_CUDA;
-    }
-    return CTR_OK;
+    const cudaError_t e = ctr::run_tc_path(pl, x, w_packed, bias, y, scratch + ws_off, status,
+                                           nullptr, nullptr, st);
+    return e == cudaSuccess ? CTR_OK : CTR_ERR_CUDA;
 }
