@@ -115,6 +115,15 @@ ctr_status ctr_plan_set_activation(ctr_plan_t plan, int act, float negative_slop
  */
 ctr_status ctr_plan_set_path(ctr_plan_t plan, int path, int split_k);
 
+/*
+ * Force the phase-row tile of the tensor-core paths: the number of packed weight rows one
+ * output tile covers, i.e. the MMA N extent (0 = automatic, else 64, 128 or 256).  A tuning
+ * and test override with no counterpart on the pages; every value gives the same result
+ * bit for bit.  Host only, with the same ordering rule as ctr_plan_set_path; returns
+ * CTR_ERR_INVALID_ARG for another value or after ctr_prepack_weight.
+ */
+ctr_status ctr_plan_set_tile(ctr_plan_t plan, int block_n);
+
 /* The path the plan will run (a ctr_path other than AUTO), or -1 for a NULL plan. */
 int ctr_plan_get_path(ctr_plan_t plan);
 
@@ -204,7 +213,8 @@ ctr_status ctr_plan_set_wait_limit_ns(ctr_plan_t plan, uint64_t limit_ns);
  * immediately before and after the plan's main kernel (the tensor-core GEMM on the polyphase
  * and col2im paths, the gather kernel otherwise), so cudaEventElapsedTime gives that
  * kernel's own duration.  Pass NULL, NULL to stop.  Host only; the events must outlive
- * the calls that record them.
+ * the calls that record them.  A ctr_forward captured into a CUDA graph records them as
+ * external event nodes, so they time every replay.
  */
 ctr_status ctr_plan_set_timing_events(ctr_plan_t plan, void *before, void *after);
 

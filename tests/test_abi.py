@@ -116,6 +116,13 @@ def test_host_side_errors_without_gpu(ctr):
             assert ctr.ctr_plan_get_path(h) == p
         ctr.ctr_plan_set_path(h, ctr.CTR_PATH_POLYPHASE, 3)
         assert "splits=3" in ctr.ctr_plan_describe(h)
+        # forcing the phase-row tile re-plans; other widths are rejected
+        for bn in (64, 128, 256):
+            ctr.ctr_plan_set_tile(h, bn)
+            assert "BN %d," % bn in ctr.ctr_plan_describe(h)
+        for bad in (32, 96, 512, -1):
+            assert ctr.lib.ctr_plan_set_tile(h, bad) == ctr.CTR_ERR_INVALID_ARG
+        ctr.ctr_plan_set_tile(h, 0)
     finally:
         ctr.ctr_plan_destroy(h)
     for s in range(8):

@@ -94,6 +94,32 @@ def test_tiles_and_split_k_bit_exact(dtype, split_k):
     np.testing.assert_array_equal(y, reference(x, w, b, 3, 2, 1, dtype), err_msg=desc)
 
 
+@pytest.mark.parametrize("block_n", [64, 128, 256])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_every_tile_width_bit_exact(dtype, block_n):
+    """Each phase-row tile width of the GEMM (its own kernel instantiation: slice width,
+    stage count, TMEM accumulators, and at 256 columns in 3xTF32 the TMEM-resident group
+    sums) with enough K for several accumulation groups, with and without split-K."""
+    rng = np.random.default_rng(11 + block_n)
+    mag = 2 if dtype == "f32" else 1
+    # K = 2 taps x 300 channels: 20 fp32 slices of 128 bytes (three groups) or 10 bf16 ones.
+    cases = [(2, 300, 70, 150, 8, 4, 2, 0), (1, 96, 33, 131, 16, 8, 4, 3)]
+    for (B, ci, co, L, k, s, p, op) in cases:
+        if dtype == "bf16":
+            ci = min(ci, 120)
+        x, w, b = _int_inputs(rng, (B, ci, L), (ci, co, k), co, mag)
+        ref = reference(x, w, b, s, p, op, dtype)
+        for split_k in (1, 2):
+            y, desc = run_plan(x, w, b, s, p, op, dtype, path=ctr.CTR_PATH_POLYPHASE,
+                               split_k=split_k, block_n=block_n)
+            assert "BN %d," % block_n in desc, desc
+            np.testing.assert_array_equal(y, ref, err_msg=desc)
+    x, w, b = _int_inputs(rng, (1, 64, 21, 18), (64, 40, 4, 4), 40, mag)
+    y, desc = run_plan(x, w, b, (2, 2), (1, 1), (1, 0), dtype, path=ctr.CTR_PATH_POLYPHASE,
+                       block_n=block_n)
+    np.testing.assert_array_equal(y, reference(x, w, b, (2, 2), (1, 1), (1, 0), dtype), err_msg=desc)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("path", sorted(PATHS))
 def test_random_within_tolerance(path, dtype):

@@ -84,9 +84,8 @@ int tf32_group() {
 // Choose the phase-row tile BN in {64, 128, 256} and the split-K factor: fewest estimated
 // clocks, counting whole waves of tiles over the SMs, a tile's time as the largest of its
 // MMA time, its operand-load time and its output time, and the extra pass over split-K
-// partials.  Grouped
-// accumulation needs BN <= 128 (the running sums of a thread's 128 columns fit its
-// registers).
+// partials.  3xTF32 at BN = 256 keeps its group sums in TMEM beside a single accumulator, so
+// the MMAs pause while each group is folded into the sums (~800 clocks).
 void choose_tiling(ctr_plan_s *pl) {
     const Prec prec = prec_of(pl);
     const int group = prec == Prec::TF32x3 ? tf32_group() : kNoGroup;
@@ -97,6 +96,7 @@ void choose_tiling(ctr_plan_s *pl) {
     // A forced split-K factor is clamped to the number of K slices.
     const int forced = pl->forced_split > 0 ? std::min(pl->forced_split, kb_total) : 0;
     for (int bn : {64, 128, 256}) {
+        if (pl->forced_bn > 0 && bn != pl->forced_bn) continue;
         const int64_t num_r = std::max<int64_t>(1, ceil_div(pl->M_rows, bn));
         for (int sp = 1; sp <= 16; ++sp) {
             if (forced > 0 && sp != forced) continue;
@@ -108,7 +108,8 @@ void choose_tiling(ctr_plan_s *pl) {
             const int64_t waves = ceil_div(tiles, pl->num_sms);
             // Per tile: tensor-pipe time, operand loads at ~50 B per clock per SM from L2,
             // and output writes at ~20 B per clock per SM (the HBM share of one SM).
-            const double mma = kbs * slice_clocks(prec, bn);
+            double mma = kbs * slice_clocks(prec, bn);
+            if (prec == Prec::TF32x3 && bn == 256) mma += 800.0 * std::ceil(kbs / std::min(kbs, (double)group));
             const double load = kbs * (ctr::kBM + bn) * (double)ctr::kBKBytes * op_planes(pl) / 50.0;
             const double epi = ctr::kBM * (double)bn * esize_io(pl) / 20.0 + 300.0;
             const double tile = std::max(mma, std::max(load, epi));
@@ -218,17 +219,18 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 // 2-D tiled tensor map over a row-major [rows][inner] matrix, box [box_rows][128 bytes],
 // 128-byte swizzle (the K-major SWIZZLE_128B operand layout of tcgen05.mma), zero fill.
 bool encode_2d(CUtensorMap *map, const void *base, bool bf16, uint64_t inner, uint64_t rows,
-               uint32_t box_rows) {
+               uint32_t box_rows, int box_bytes) {
     auto fn = get_encode_fn();
-    if (!fn) return false;
+    if (!fn || (box_bytes != 128 && box_bytes != 64)) return false;
     const uint32_t es = bf16 ? 2 : 4;
     cuuint64_t dims[2] = {inner, rows};
     cuuint64_t strides[1] = {inner * es};
-    cuuint32_t box[2] = {(cuuint32_t)(ctr::kBKBytes / es), box_rows};
+    cuuint32_t box[2] = {(cuuint32_t)(box_bytes / es), box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                     2, const_cast<void *>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -304,6 +306,12 @@ int64_t raw_split_stride_of(const ctr_plan_s *pl) {
 // (with timing events around it when given), then the split-K reduce or col2im.  ws holds
 // the staged input and the raw partials at the plan's offsets; status is the device status
 // word the GEMM reports bounded-wait timeouts into.
+// Records a timing event.  Under stream capture it becomes an external event-record node,
+// so every replay of the graph records it (a plain record would only order the graph).
+cudaError_t record_timing(cudaEvent_t ev, cudaStream_t st) {
+    return cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+}
+
 cudaError_t run_tc_path(const ctr_plan_s *pl, const void *x, const void *w_packed,
                         const void *bias, void *y, char *ws, uint32_t *status,
                         cudaEvent_t ev_before, cudaEvent_t ev_after, cudaStream_t st) {
@@ -316,16 +324,18 @@ cudaError_t run_tc_path(const ctr_plan_s *pl, const void *x, const void *w_packe
     const int es = bf16 ? 2 : 4;
     const size_t w_plane = (size_t)pl->M_pad * pl->K_total * es;
     const size_t x_plane = (size_t)pl->N_total * pl->C_in_pad * es;
-    // maps: staged input (128-position boxes), packed weight (block_n-row boxes), lo planes.
+    // maps: staged input (128-position boxes), packed weight (block_n-row boxes), lo planes;
+    // every box is one K slice of the GEMM instantiation wide.
+    const int sb = gemm_slice_bytes(bf16 ? Prec::BF16 : Prec::TF32x3, pl->block_n);
     CUtensorMap maps[4];
-    bool ok = encode_2d(&maps[0], xs, bf16, pl->C_in_pad, pl->N_total, kBM) &&
-              encode_2d(&maps[1], w_packed, bf16, pl->K_total, pl->M_pad, pl->block_n);
+    bool ok = encode_2d(&maps[0], xs, bf16, pl->C_in_pad, pl->N_total, kBM, sb) &&
+              encode_2d(&maps[1], w_packed, bf16, pl->K_total, pl->M_pad, pl->block_n, sb);
     if (!bf16) {
         ok = ok &&
              encode_2d(&maps[2], static_cast<char *>(xs) + x_plane, false, pl->C_in_pad,
-                       pl->N_total, kBM) &&
+                       pl->N_total, kBM, sb) &&
              encode_2d(&maps[3], static_cast<const char *>(w_packed) + w_plane, false,
-                       pl->K_total, pl->M_pad, pl->block_n);
+                       pl->K_total, pl->M_pad, pl->block_n, sb);
     } else {
         maps[2] = maps[0];
         maps[3] = maps[1];
@@ -338,9 +348,9 @@ cudaError_t run_tc_path(const ctr_plan_s *pl, const void *x, const void *w_packe
     gp.num_r_tiles = pl->num_r_tiles;
     gp.splits = pl->splits;
     gp.num_tiles = pl->num_tiles;
-    gp.kb_total = (int)(pl->K_total * es / kBKBytes);
-    gp.kb_per_tap = (int)(pl->C_in_pad * es / kBKBytes);
-    gp.kb_group = pl->kb_group;
+    gp.kb_total = (int)(pl->K_total * es / sb);
+    gp.kb_per_tap = (int)(pl->C_in_pad * es / sb);
+    gp.kb_group = pl->kb_group == kNoGroup ? kNoGroup : pl->kb_group * (kBKBytes / sb);
     gp.mx = (int)pl->m[1];
     gp.Px = pl->P[1];
     const bool fused = pl->path == CTR_PATH_POLYPHASE && pl->splits == 1;
@@ -351,9 +361,9 @@ cudaError_t run_tc_path(const ctr_plan_s *pl, const void *x, const void *w_packe
     gp.raw_split_stride = raw_split_stride_of(pl);
     gp.status = status;
     gp.wait_limit_ns = pl->wait_limit_ns;
-    if (ev_before && (e = cudaEventRecord(ev_before, st)) != cudaSuccess) return e;
+    if (ev_before && (e = record_timing(ev_before, st)) != cudaSuccess) return e;
     if ((e = launch_gemm_tc(pl, maps, gp, st)) != cudaSuccess) return e;
-    if (ev_after && (e = cudaEventRecord(ev_after, st)) != cudaSuccess) return e;
+    if (ev_after && (e = record_timing(ev_after, st)) != cudaSuccess) return e;
     if (pl->path == CTR_PATH_POLYPHASE && !fused)
         return launch_splitk_reduce(pl, raw, gp.epi, gp.raw_ld, gp.raw_split_stride, st);
     if (pl->path == CTR_PATH_COL2IM) return launch_col2im(pl, raw, gp.raw_ld, bias, y, st);
@@ -411,6 +421,7 @@ ctr_status ctr_plan_create(ctr_plan_t *out, int ndim, int64_t N, int64_t C_in, i
     pl->slope = 0.0f;
     pl->forced_path = CTR_PATH_AUTO;
     pl->forced_split = 0;
+    pl->forced_bn = 0;
     pl->wait_limit_ns = 4000000000ull;
     // Unit leading dimension for 1-D.
     pl->in[0] = 1; pl->k[0] = 1; pl->s[0] = 1; pl->p[0] = 0; pl->op[0] = 0;
@@ -460,6 +471,15 @@ ctr_status ctr_plan_set_path(ctr_plan_t pl, int path, int split_k) {
     pl->forced_path = path;
     pl->forced_split = split_k;
     pl->path = choose_path(pl);
+    layout_plan(pl);
+    return CTR_OK;
+}
+
+ctr_status ctr_plan_set_tile(ctr_plan_t pl, int block_n) {
+    if (!pl || (block_n != 0 && block_n != 64 && block_n != 128 && block_n != 256))
+        return CTR_ERR_INVALID_ARG;
+    if (pl->prepared) return CTR_ERR_INVALID_ARG;
+    pl->forced_bn = block_n;
     layout_plan(pl);
     return CTR_OK;
 }
@@ -558,9 +578,9 @@ ctr_status ctr_forward(ctr_plan_t pl, const void *x, const void *w_packed, const
 
     const bool timed = pl->ev_before != nullptr;
     if (pl->path == CTR_PATH_GATHER) {
-        if (timed && cudaEventRecord(pl->ev_before, st) != cudaSuccess) return CTR_ERR_CUDA;
+        if (timed && ctr::record_timing(pl->ev_before, st) != cudaSuccess) return CTR_ERR_CUDA;
         if (ctr::launch_gather(pl, x, w_packed, bias, y, st) != cudaSuccess) return CTR_ERR_CUDA;
-        if (timed && cudaEventRecord(pl->ev_after, st) != cudaSuccess) return CTR_ERR_CUDA;
+        if (timed && ctr::record_timing(pl->ev_after, st) != cudaSuccess) return CTR_ERR_CUDA;
         return CTR_OK;
     }
     if (pl->N_total == 0) {  // empty input on the col2im path: y = bias or zeros

@@ -7,6 +7,7 @@
 //   fill_bias    y = bias (or zeros) for an empty input on the col2im path
 //   copy_weight  the gather path's "packed" weight (a plain copy)
 #include <algorithm>
+#include <type_traits>
 #include <cuda_bf16.h>
 
 #include "ctr_internal.h"
@@ -19,6 +20,7 @@ namespace {
 constexpr int kBlock = 256;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
 unsigned grid_for(int64_t n, int block) {
     const int64_t g = ceil_div(n, block);
@@ -174,105 +176,189 @@ struct StageGeo {
 };
 
 // xs[n][c] with n = (b*Py + py')*Px + px': x[b, c, py' - hy, px' - hx] inside the input and
-// c < C_in, zero elsewhere (the halos are the polyphase conv's padding m - 1).  A block
-// moves 256 consecutive staged positions x 32 channels through shared memory: each warp
-// reads 4 channels along positions (32 loads in flight per lane, coalesced along x) and
-// then writes 32 positions along channels (coalesced along c).  Positions are decoded once
-// per lane and advanced incrementally.  fp32 input is written as tf32 hi and lo planes.
-constexpr int kStagePos = 256;
+// c < C_in, zero elsewhere (the halos are the polyphase conv's padding m - 1).  fp32 input
+// is written as tf32 hi and lo planes.
+//
+// A block transposes one tile of 128 input positions (along x, within one staged row) by
+// kStageC channels (64 bf16 or 32 fp32, i.e. 128 bytes of a staged row) through shared
+// memory:
+//   load   each warp reads whole 16-byte vectors along x (one or two channel rows per
+//          instruction; element loads when the rows are not 16-byte aligned) and writes
+//          them as float4s into tile[c][x];
+//   store  each thread gathers the kOutVec channels of one 16-byte output vector at one
+//          position and writes it; eight consecutive threads cover a 128-byte staged row.
+// The tile is XOR-swizzled by 4-float groups, column group g of channel c stored at
+// g ^ ((c / kOutVec) & 7), so both the float4 writes and the scalar reads of a warp hit 32
+// different banks.  Tiles start at input x = x_first + 128 t with x_first a multiple of 8
+// at or before -hx, so the left halo is covered; staged positions outside [0, Px) are
+// skipped and those outside the input are written as zeros.
+constexpr int kStageThreads = 256;
+constexpr int kStageTP = 128;
 
-__global__ void __launch_bounds__(256) stage_x_kernel(const void *__restrict__ x,
-                                                      void *__restrict__ xs, StageGeo sg) {
-    __shared__ float tile[kStagePos][33];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t n0 = (int64_t)blockIdx.x * kStagePos;
-    const int64_t c0 = (int64_t)blockIdx.y * 32;
-    const int64_t plane = sg.Py * sg.Px;
-    const int64_t hw = sg.H * sg.W;
-    // This lane's first position and its staged coordinates.
-    int64_t n = n0 + lane;
-    int64_t b = n / plane;
-    int64_t rem = n - b * plane;
-    int64_t py = rem / sg.Px;
-    int64_t px = rem - py * sg.Px;
-    int64_t xoff[kStagePos / 32];  // x offset of channel 0 at each of the lane's positions, -1 = zero
+struct StageUnits {
+    int64_t cchunks;   // C_in_pad / kStageC
+    int64_t xtiles;    // tiles of 128 positions per staged row
+    int64_t x_first;   // input x of the first tile of a row
+    int64_t tiles;     // rows * xtiles * cchunks
+};
+
+template <bool BF16, bool VEC>
+__global__ void __launch_bounds__(kStageThreads) stage_x_kernel(const void *__restrict__ x,
+                                                               void *__restrict__ xs,
+                                                               StageGeo sg, StageUnits su) {
+    using T = typename std::conditional<BF16, __nv_bfloat16, float>::type;
+    constexpr int kStageC = BF16 ? 64 : 32;      // channels per tile (128 bytes of a row)
+    constexpr int kInVec = 16 / sizeof(T);       // positions per 16-byte load
+    constexpr int kOutVec = 16 / sizeof(T);      // channels per 16-byte store
+    constexpr int kLoadItems = kStageC * (kStageTP / kInVec) / kStageThreads;
+    constexpr int kStoreItems = kStageTP * (kStageC / kOutVec) / kStageThreads;
+    __shared__ __align__(16) float tile[kStageC][kStageTP];
+    const T *__restrict__ xin = static_cast<const T *>(x);
+    const int64_t lo_off = sg.N_total * sg.C_in_pad;
+
+    for (int64_t t = blockIdx.x; t < su.tiles; t += gridDim.x) {
+        const int64_t cq = t % su.cchunks;
+        const int64_t rest = t / su.cchunks;
+        const int64_t xt = rest % su.xtiles;
+        const int64_t row = rest / su.xtiles;      // b * Py + py'
+        const int64_t b = row / sg.Py;
+        const int64_t yy = row - b * sg.Py - sg.hy;
+        const int64_t xx0 = su.x_first + kStageTP * xt;
+        const int64_t c_base = cq * kStageC;
+        const bool row_in = yy >= 0 && yy < sg.H;
+
 #pragma unroll
-    for (int j = 0; j < kStagePos / 32; ++j) {
-        const int64_t yy = py - sg.hy, xx = px - sg.hx;
-        const bool in = n + 32 * j < sg.N_total && yy >= 0 && yy < sg.H && xx >= 0 && xx < sg.W;
-        xoff[j] = in ? (b * sg.C_in * sg.H + yy) * sg.W + xx : -1;
-        px += 32;
-        while (px >= sg.Px) {
-            px -= sg.Px;
-            if (++py == sg.Py) {
-                py = 0;
-                ++b;
+        for (int it = 0; it < kLoadItems; ++it) {
+            const int i = it * kStageThreads + threadIdx.x;
+            const int c = i / (kStageTP / kInVec);
+            const int v = i % (kStageTP / kInVec);
+            const int64_t xx = xx0 + (int64_t)v * kInVec;
+            const int64_t ch = c_base + c;
+            float val[kInVec];
+#pragma unroll
+            for (int j = 0; j < kInVec; ++j) val[j] = 0.0f;
+            if (row_in && ch < sg.C_in) {
+                const T *src = xin + ((b * sg.C_in + ch) * sg.H + yy) * sg.W;
+                if (VEC && xx >= 0 && xx + kInVec <= sg.W) {
+                    const uint4 r = *reinterpret_cast<const uint4 *>(src + xx);
+                    const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
+                    if constexpr (BF16) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            val[2 * j] = __uint_as_float(w4[j] << 16);
+                            val[2 * j + 1] = __uint_as_float(w4[j] & 0xFFFF0000u);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) val[j] = __uint_as_float(w4[j]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < kInVec; ++j)
+                        if (xx + j >= 0 && xx + j < sg.W) val[j] = static_cast<float>(src[xx + j]);
+                }
+            }
+            const int sw = (c / kOutVec) & 7;
+#pragma unroll
+            for (int q = 0; q < kInVec / 4; ++q) {
+                const int grp = (v * (kInVec / 4) + q) ^ sw;
+                *reinterpret_cast<float4 *>(&tile[c][4 * grp]) =
+                    make_float4(val[4 * q], val[4 * q + 1], val[4 * q + 2], val[4 * q + 3]);
             }
         }
-    }
+        __syncthreads();
+
 #pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-        const int ci = warp * 4 + cc;
-        const int64_t c = c0 + ci;
-        const bool cvalid = c < sg.C_in;
+        for (int it = 0; it < kStoreItems; ++it) {
+            const int i = it * kStageThreads + threadIdx.x;
+            const int p = i / (kStageC / kOutVec);
+            const int cg = i % (kStageC / kOutVec);
+            const int64_t px = xx0 + p + sg.hx;
+            if (px < 0 || px >= sg.Px) continue;
+            const int col = (((p >> 2) ^ (cg & 7)) << 2) | (p & 3);
+            float val[kOutVec];
 #pragma unroll
-        for (int j = 0; j < kStagePos / 32; ++j) {
-            float v = 0.0f;
-            if (cvalid && xoff[j] >= 0) v = load_io(x, xoff[j] + c * hw, sg.bf16);
-            tile[lane + 32 * j][ci] = v;
+            for (int k = 0; k < kOutVec; ++k) val[k] = tile[cg * kOutVec + k][col];
+            const int64_t o = (row * sg.Px + px) * sg.C_in_pad + c_base + cg * kOutVec;
+            if constexpr (BF16) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)   // exact: the values came from bf16
+                    w4[k] = (__float_as_uint(val[2 * k]) >> 16) |
+                            (__float_as_uint(val[2 * k + 1]) & 0xFFFF0000u);
+                *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(xs) + o) =
+                    make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            } else {
+                float hi[4], lo[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    hi[k] = ptx::to_tf32(val[k]);
+                    lo[k] = ptx::to_tf32(val[k] - hi[k]);
+                }
+                *reinterpret_cast<float4 *>(static_cast<float *>(xs) + o) =
+                    make_float4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<float4 *>(static_cast<float *>(xs) + lo_off + o) =
+                    make_float4(lo[0], lo[1], lo[2], lo[3]);
+            }
         }
-    }
-    __syncthreads();
-    const int64_t lo_off = sg.N_total * sg.C_in_pad;
-#pragma unroll 4
-    for (int p = warp; p < kStagePos; p += 8) {
-        const int64_t np = n0 + p;
-        if (np >= sg.N_total) break;
-        const int64_t o = np * sg.C_in_pad + c0 + lane;
-        const float v = tile[p][lane];
-        if (sg.bf16) {
-            static_cast<__nv_bfloat16 *>(xs)[o] = __float2bfloat16_rn(v);
-        } else {
-            const float hi = ptx::to_tf32(v);
-            static_cast<float *>(xs)[o] = hi;
-            static_cast<float *>(xs)[lo_off + o] = ptx::to_tf32(v - hi);
-        }
+        __syncthreads();   // the tile is reused by the next iteration
     }
 }
 
 // -------------------------------------------------------------------------- split-K reduce
 // One thread per (phase position n, 32-row chunk r0): sums the split-K partials
 // raw[z][n][r0 .. r0+31] in a fixed order (z = 0, 1, ...) with 16-byte loads, then runs the
-// same output stage as the fused epilogue.
+// same output stage as the fused epilogue.  The 32 lanes of a warp take 32 consecutive
+// positions of one chunk (positions padded to a multiple of 32; lanes past the end load
+// nothing and store nothing), as the warp-collective output stage requires.
 __global__ void splitk_reduce_kernel(const float *__restrict__ raw, EpiParams ep, int64_t ld,
                                      int64_t split_stride, int splits, int64_t n_rows,
-                                     int64_t r_chunks) {
+                                     int64_t n_pad, int64_t r_chunks) {
     const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= n_rows * r_chunks) return;
-    const int64_t n = idx / r_chunks;
-    const int64_t r0 = (idx - n * r_chunks) * 32;
-    const float4 *p = reinterpret_cast<const float4 *>(raw + n * ld + r0);
+    if (idx >= n_pad * r_chunks) return;   // whole warps: n_pad * r_chunks is a multiple of 32
+    const int64_t rc = idx / n_pad;
+    const int64_t n = idx - rc * n_pad;
+    const int64_t r0 = rc * 32;
+    const bool live = n < n_rows;
     float v[32];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float4 a = p[i];
-        v[4 * i] = a.x;
-        v[4 * i + 1] = a.y;
-        v[4 * i + 2] = a.z;
-        v[4 * i + 3] = a.w;
-    }
-    for (int z = 1; z < splits; ++z) {
-        const float4 *q = reinterpret_cast<const float4 *>(raw + z * split_stride + n * ld + r0);
+    for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+    if (live) {
+        const float4 *p = reinterpret_cast<const float4 *>(raw + n * ld + r0);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float4 a = q[i];
-            v[4 * i] += a.x;
-            v[4 * i + 1] += a.y;
-            v[4 * i + 2] += a.z;
-            v[4 * i + 3] += a.w;
+            const float4 a = p[i];
+            v[4 * i] = a.x;
+            v[4 * i + 1] = a.y;
+            v[4 * i + 2] = a.z;
+            v[4 * i + 3] = a.w;
+        }
+        // Up to four partials' loads in flight at once; the sums still run in split order.
+        for (int z = 1; z < splits; z += 4) {
+            float4 a[4][8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (z + u >= splits) break;
+                const float4 *q =
+                    reinterpret_cast<const float4 *>(raw + (z + u) * split_stride + n * ld + r0);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) a[u][i] = q[i];
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (z + u >= splits) break;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    v[4 * i] += a[u][i].x;
+                    v[4 * i + 1] += a[u][i].y;
+                    v[4 * i + 2] += a[u][i].z;
+                    v[4 * i + 3] += a[u][i].w;
+                }
+            }
         }
     }
-    emit_cols(v, decode_pos(n, ep), r0, ep);
+    // decode_pos marks positions at or past n_rows (= B * Py * Px) invalid.
+    emit_cols(v, decode_pos(n, ep), r0, ep, (int)(threadIdx.x & 31));
 }
 
 // -------------------------------------------------------------------------- col2im
@@ -384,8 +470,25 @@ cudaError_t launch_stage_x(const ctr_plan_s *pl, const void *x, void *xs, cudaSt
     sg.N_total = pl->N_total;
     sg.bf16 = pl->dtype == CTR_BF16 ? 1 : 0;
     if (sg.N_total == 0) return cudaSuccess;
-    dim3 grid((unsigned)ceil_div(sg.N_total, kStagePos), (unsigned)(sg.C_in_pad / 32));
-    stage_x_kernel<<<grid, 256, 0, st>>>(x, xs, sg);
+    StageUnits su;
+    su.cchunks = sg.C_in_pad / (sg.bf16 ? 64 : 32);
+    su.x_first = -round_up(sg.hx, 8);
+    su.xtiles = ceil_div(sg.Px - sg.hx - su.x_first, kStageTP);
+    su.tiles = sg.B * sg.Py * su.xtiles * su.cchunks;
+    const int64_t blocks = std::min<int64_t>(su.tiles, (int64_t)pl->num_sms * 8);
+    const bool vec = (sg.W * (sg.bf16 ? 2 : 4)) % 16 == 0;
+    const dim3 grid((unsigned)blocks);
+    if (sg.bf16) {
+        if (vec)
+            stage_x_kernel<true, true><<<grid, kStageThreads, 0, st>>>(x, xs, sg, su);
+        else
+            stage_x_kernel<true, false><<<grid, kStageThreads, 0, st>>>(x, xs, sg, su);
+    } else {
+        if (vec)
+            stage_x_kernel<false, true><<<grid, kStageThreads, 0, st>>>(x, xs, sg, su);
+        else
+            stage_x_kernel<false, false><<<grid, kStageThreads, 0, st>>>(x, xs, sg, su);
+    }
     count_launches(1);
     return cudaGetLastError();
 }
@@ -393,11 +496,12 @@ cudaError_t launch_stage_x(const ctr_plan_s *pl, const void *x, void *xs, cudaSt
 cudaError_t launch_splitk_reduce(const ctr_plan_s *pl, const float *raw, const EpiParams &ep,
                                  int64_t raw_ld, int64_t split_stride, cudaStream_t st) {
     const int64_t n_rows = pl->N_total;
+    const int64_t n_pad = round_up(n_rows, 32);
     const int64_t r_chunks = ceil_div(std::min<int64_t>(pl->M_rows, raw_ld), 32);
-    const int64_t total = n_rows * r_chunks;
-    if (total == 0) return cudaSuccess;
-    splitk_reduce_kernel<<<grid_for(total, 128), 128, 0, st>>>(raw, ep, raw_ld, split_stride,
-                                                             pl->splits, n_rows, r_chunks);
+    const int64_t total = n_pad * r_chunks;
+    if (n_rows == 0 || r_chunks == 0) return cudaSuccess;
+    splitk_reduce_kernel<<<grid_for(total, 64), 64, 0, st>>>(raw, ep, raw_ld, split_stride,
+                                                             pl->splits, n_rows, n_pad, r_chunks);
     count_launches(1);
     return cudaGetLastError();
 }

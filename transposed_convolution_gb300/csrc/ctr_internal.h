@@ -11,8 +11,9 @@
 
 namespace ctr {
 
-// Tile shape of the tensor-core GEMM: 128 rows (TMEM lanes) x BN columns, K in 128-byte
-// slices (64 bf16 or 32 fp32 per row).
+// Tile shape of the tensor-core GEMM: 128 rows (TMEM lanes) x BN columns.  The packed
+// operands' K extents are multiples of 128 bytes (64 bf16 or 32 fp32); the kernel moves K
+// in slices of 128 or 64 bytes (see gemm_slice_bytes).
 constexpr int kBM = 128;
 constexpr int kBKBytes = 128;
 
@@ -53,8 +54,9 @@ struct EpiParams {
 struct GemmParams {
     int num_p_tiles, num_r_tiles, splits;
     int64_t num_tiles;
+    // K counts below are in the kernel's slices (gemm_slice_bytes of the plan's dtype and BN).
     int kb_total;       // K slices over all taps
-    int kb_per_tap;     // K slices per tap (C_in_pad * esize / 128)
+    int kb_per_tap;     // K slices per tap (C_in_pad * esize / slice bytes)
     int kb_group;       // K slices per tensor-core accumulation group (see gemm_tc.cu)
     int mx;             // taps along x: tap g -> (uy, ux) = (g / mx, g % mx)
     int64_t Px;         // position shift of one tap step along y
@@ -86,6 +88,7 @@ struct ctr_plan_s {
     int path;           // chosen ctr_path (never AUTO)
     int forced_path;
     int forced_split;
+    int forced_bn;      // 0 = automatic phase-row tile
     int prepared;       // ctr_prepack_weight ran (status word allocated)
     int num_sms;
 
@@ -100,7 +103,7 @@ struct ctr_plan_s {
     int64_t N_total;    // GEMM columns = B * P[0] * P[1]
     int block_n;        // phase rows per tile (MMA N): 64, 128 or 256
     int splits;
-    int kb_group;       // K slices per accumulation group; >= slices per tile = no flush
+    int kb_group;       // 128-byte K slices per accumulation group; >= all slices = no flush
     int num_p_tiles;    // tiles of 128 staged positions
     int num_r_tiles;    // tiles of block_n packed weight rows
     int64_t num_tiles;
@@ -140,10 +143,10 @@ cudaError_t launch_fill_bias(const ctr_plan_s *pl, const void *bias, void *y, cu
 cudaError_t launch_gemm_tc(const ctr_plan_s *pl, const CUtensorMap *maps, const GemmParams &gp,
                            cudaStream_t st);
 
-// 2-D tiled tensor map over a row-major [rows][inner] operand matrix, box [box_rows][128
-// bytes], 128-byte swizzle, zero fill (api.cu).
+// 2-D tiled tensor map over a row-major [rows][inner] operand matrix, box [box_rows]
+// [box_bytes], swizzled at box_bytes (128 or 64), zero fill (api.cu).
 bool encode_2d(CUtensorMap *map, const void *base, bool bf16, uint64_t inner, uint64_t rows,
-               uint32_t box_rows);
+               uint32_t box_rows, int box_bytes);
 
 // Output mapping of a tensor-core plan (api.cu).
 EpiParams make_epi(const ctr_plan_s *pl, const void *bias, void *y);
@@ -159,7 +162,13 @@ void count_launches(uint64_t n);
 // Bytes of dynamic shared memory a GEMM instantiation uses.
 size_t gemm_smem_bytes(Prec prec, int block_n);
 
+// Width in bytes (128 or 64) of the K slices a GEMM instantiation loads per pipeline stage:
+// 64 where 128-byte stages would leave fewer than four in shared memory.
+constexpr int gemm_slice_bytes(Prec prec, int block_n) {
+    return prec == Prec::TF32x3 && block_n >= 256 ? 64 : 128;
+}
+
 // Largest phase-row tile whose accumulation groups fit the epilogue's registers.
-constexpr int kMaxGroupedBN = 128;
+constexpr int kMaxGroupedBN = 256;
 
 }  // namespace ctr

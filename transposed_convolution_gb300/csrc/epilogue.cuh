@@ -110,47 +110,68 @@ __device__ __forceinline__ void store_run(T *dst, const float *vals, int wbytes)
     }
 }
 
-// One run of NX phases (jx = 0 .. NX-1 of one (oc, jy)) starting at v[0]: bias, activation,
-// then either vector stores (interior) or per-element stores with bounds checks (row edges).
+// One run of NX consecutive outputs at dst (x = x0 .. x0+NX-1 of one output row) from
+// v[0..NX-1]: bias, activation (slope_eff = 1 when there is none), then aligned vector
+// stores inside the row, or element stores with bounds checks at its edges.
 template <typename T, int NX>
-__device__ __forceinline__ void emit_run(T *__restrict__ y, int64_t row, int64_t x0,
-                                         const float *v, float bias, const EpiParams &e,
+__device__ __forceinline__ void emit_run(T *__restrict__ dst, int64_t x0, const float *v,
+                                         float bias, float slope_eff, const EpiParams &e,
                                          bool interior) {
     float t[NX];
 #pragma unroll
-    for (int i = 0; i < NX; ++i) t[i] = apply_act(v[i] + bias, e.act, e.slope);
+    for (int i = 0; i < NX; ++i) {
+        const float a = v[i] + bias;
+        t[i] = a < 0.0f ? a * slope_eff : a;
+    }
     if (interior) {
-        store_run<T, NX>(y + row + x0, t, e.store_bytes);
+        store_run<T, NX>(dst, t, e.store_bytes);
     } else {
 #pragma unroll
         for (int i = 0; i < NX; ++i)
-            if (x0 + i >= 0 && x0 + i < e.Wout) y[row + x0 + i] = static_cast<T>(t[i]);
+            if (x0 + i >= 0 && x0 + i < e.Wout) dst[i] = static_cast<T>(t[i]);
     }
 }
 
+// Bias of channel oc0 + lane for the first `count` lanes (0 elsewhere), so that a warp can
+// share a chunk's biases by shuffles: one load per lane, issued before any output store.
+__device__ __forceinline__ float lane_bias(const EpiParams &e, int64_t oc0, int count, int lane) {
+    return (e.bias && lane < count && oc0 + lane < e.C_out) ? load_io(e.bias, oc0 + lane, e.out_bf16)
+                                                            : 0.0f;
+}
+
+__device__ __forceinline__ float slope_of(const EpiParams &e) {
+    return e.act == CTR_ACT_LEAKY_RELU ? e.slope : 1.0f;
+}
+
 // Output stage for whole phase sets: S = S_pad = SX * SY <= 32 (SX, SY compile-time), so the
-// 32 columns r0 .. r0+31 of a chunk are 32/S whole channels.
+// 32 columns r0 .. r0+31 of a chunk are G = 32/S whole channels.  Warp-collective: every
+// lane passes the same r0 (its own position in ps).
 template <typename T, int SX, int SY>
 __device__ __forceinline__ void emit_small(const float (&v)[32], const PosInfo &ps, int64_t r0,
-                                           const EpiParams &e) {
+                                           const EpiParams &e, int lane) {
     constexpr int S = SX * SY;
     constexpr int G = 32 / S;
-    T *__restrict__ y = static_cast<T *>(e.y);
     const int64_t oc0 = r0 / S;
+    const float bl = lane_bias(e, oc0, G, lane);
+    const float slope_eff = slope_of(e);
     const int64_t x0 = (int64_t)SX * ps.qx - e.px;
-    const bool interior = x0 >= 0 && x0 + SX <= e.Wout;
     const int64_t oy0 = (int64_t)SY * ps.qy - e.py;
+    const bool interior = x0 >= 0 && x0 + SX <= e.Wout;
+    const int64_t cstride = e.Hout * e.Wout;
+    // Output of (oc0, oy0, x0); rows and channels below are offsets from it.
+    T *__restrict__ base = static_cast<T *>(e.y) + ((ps.b * e.C_out + oc0) * e.Hout + oy0) * e.Wout + x0;
+    // Every lane runs the channel loop (the shuffles need the whole warp); lanes whose
+    // position lies outside the output store nothing.
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-        const int64_t oc = oc0 + g;
-        if (oc >= e.C_out) break;
-        const float bias = e.bias ? load_io(e.bias, oc, e.out_bf16) : 0.0f;
-        const int64_t chan = (ps.b * e.C_out + oc) * e.Hout;
+        if (oc0 + g >= e.C_out) break;   // uniform: oc0 is the same on every lane
+        const float bias = __shfl_sync(0xffffffffu, bl, g);
+        if (!ps.valid) continue;
 #pragma unroll
         for (int jy = 0; jy < SY; ++jy) {
-            const int64_t oy = oy0 + jy;
-            if (oy < 0 || oy >= e.Hout) continue;
-            emit_run<T, SX>(y, (chan + oy) * e.Wout, x0, &v[g * S + jy * SX], bias, e, interior);
+            if (oy0 + jy < 0 || oy0 + jy >= e.Hout) continue;
+            emit_run<T, SX>(base + g * cstride + jy * e.Wout, x0, &v[g * S + jy * SX], bias,
+                            slope_eff, e, interior);
         }
     }
 }
@@ -159,20 +180,22 @@ __device__ __forceinline__ void emit_small(const float (&v)[32], const PosInfo &
 // consecutive phases j0 .. j0+31 of one channel, i.e. 32 consecutive outputs.
 template <typename T>
 __device__ __forceinline__ void emit_large(const float (&v)[32], const PosInfo &ps, int64_t r0,
-                                           const EpiParams &e) {
-    T *__restrict__ y = static_cast<T *>(e.y);
+                                           const EpiParams &e, int lane) {
     const int64_t oc = r0 / e.S_pad;
-    if (oc >= e.C_out) return;
+    const float bias = __shfl_sync(0xffffffffu, lane_bias(e, oc, 1, lane), 0);
+    if (!ps.valid || oc >= e.C_out) return;
     const int64_t j0 = r0 - oc * e.S_pad;
     const int64_t x0 = (int64_t)e.sx * ps.qx + j0 - e.px;
     const bool interior = x0 >= 0 && x0 + 32 <= e.Wout;
-    const float bias = e.bias ? load_io(e.bias, oc, e.out_bf16) : 0.0f;
-    emit_run<T, 32>(y, (ps.b * e.C_out + oc) * e.Wout, x0, v, bias, e, interior);
+    emit_run<T, 32>(static_cast<T *>(e.y) + (ps.b * e.C_out + oc) * e.Wout + x0, x0, v, bias,
+                    slope_of(e), e, interior);
 }
 
 // Any plan: every output element on its own, with the full index map and bounds checks.
 __device__ __forceinline__ void emit_generic(const float (&v)[32], const PosInfo &ps, int64_t r0,
                                              const EpiParams &e) {
+    if (!ps.valid) return;
+    const float slope_eff = slope_of(e);
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
         const int64_t r = r0 + i;
@@ -184,21 +207,22 @@ __device__ __forceinline__ void emit_generic(const float (&v)[32], const PosInfo
         const int64_t ox = (int64_t)e.sx * ps.qx + jx - e.px;
         if (oy < 0 || oy >= e.Hout || ox < 0 || ox >= e.Wout) continue;
         const float bias = e.bias ? load_io(e.bias, oc, e.out_bf16) : 0.0f;
+        const float a = v[i] + bias;
         store_io(e.y, ((ps.b * e.C_out + oc) * e.Hout + oy) * e.Wout + ox,
-                 apply_act(v[i] + bias, e.act, e.slope), e.out_bf16);
+                 a < 0.0f ? a * slope_eff : a, e.out_bf16);
     }
 }
 
 // Output stage for the accumulator columns r0 .. r0+31 (r0 a multiple of 32) of one phase
-// position: v[i] = D[n, r0 + i].  Each thread works on its own position.
+// position per lane: v[i] = D[n, r0 + i].  Warp-collective: all 32 lanes of the warp call
+// it together with the same r0, each with its own position.
 __device__ __forceinline__ void emit_cols(const float (&v)[32], const PosInfo &ps, int64_t r0,
-                                          const EpiParams &e) {
-    if (!ps.valid) return;
+                                          const EpiParams &e, int lane) {
 #define CTR_SMALL(SX, SY)                                                  \
     if (e.out_bf16)                                                        \
-        emit_small<__nv_bfloat16, SX, SY>(v, ps, r0, e);                   \
+        emit_small<__nv_bfloat16, SX, SY>(v, ps, r0, e, lane);             \
     else                                                                   \
-        emit_small<float, SX, SY>(v, ps, r0, e);                           \
+        emit_small<float, SX, SY>(v, ps, r0, e, lane);                     \
     return
     switch (e.kind) {
         case EPI_KIND_1D_S1: CTR_SMALL(1, 1);
@@ -211,9 +235,9 @@ __device__ __forceinline__ void emit_cols(const float (&v)[32], const PosInfo &p
         case EPI_KIND_2D_S4x4: CTR_SMALL(4, 4);
         case EPI_KIND_1D_LARGE:
             if (e.out_bf16)
-                emit_large<__nv_bfloat16>(v, ps, r0, e);
+                emit_large<__nv_bfloat16>(v, ps, r0, e, lane);
             else
-                emit_large<float>(v, ps, r0, e);
+                emit_large<float>(v, ps, r0, e, lane);
             return;
         default:
             emit_generic(v, ps, r0, e);

@@ -15,14 +15,16 @@
 // dimension the packed weight row r (BN = 64, 128 or 256 per tile: TMEM columns), so each
 // epilogue thread owns one output position and writes its phases as contiguous runs.
 //
-// Warp roles (192 threads, one CTA per SM, persistent over output tiles):
+// Warp roles (320 threads, one CTA per SM, persistent over output tiles):
 //   warp 0      one lane issues TMA loads of Xs and A K-slices into a ring of stages;
-//   warp 1      allocates TMEM; one lane issues tcgen05.mma into one of two TMEM
+//   warp 1      allocates TMEM; one lane issues tcgen05.mma into one of several TMEM
 //               accumulators (128 lanes x BN fp32 columns) and commits to mbarriers;
-//   warps 2..5  the epilogue: tcgen05.ld of the accumulator, then either the fused polyphase
+//   warps 2..9  the epilogue: tcgen05.ld of the accumulator, then either the fused polyphase
 //               output stage (bias, activation, interleave, slice; epilogue.cuh) or a raw
-//               fp32 store of D (split-K partials, col2im columns).
-// Two accumulators let the epilogue of tile i overlap the MMAs of tile i + 1.
+//               fp32 store of D (split-K partials, col2im columns).  A warp may read only
+//               the TMEM lane quarter (warp id mod 4); two warps share each quarter, one
+//               taking the first BN/2 columns and the other the rest.
+// Several accumulators let the epilogue of tile i overlap the MMAs of tile i + 1.
 //
 // 3xTF32 (fp32 I/O): both operands come as tf32 hi and lo planes (x = hi + lo, each
 // rounded to tf32) and every K step issues lo*hi + hi*lo + hi*hi into the same fp32
@@ -42,30 +44,39 @@
 namespace ctr {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kEpiWarps = 4;
+constexpr int kThreads = 320;
+constexpr int kEpiWarps = 8;
 constexpr int kSmemMax = 227 * 1024;
 constexpr uint64_t kDrainLimitNs = 2000000000ull;
 
 template <Prec P, int BN>
 struct Cfg {
     static constexpr int kPlanes = P == Prec::TF32x3 ? 2 : 1;
-    static constexpr int kXBytes = kBM * kBKBytes;           // one 128-position Xs slice
-    static constexpr int kWBytes = BN * kBKBytes;            // one BN-row weight slice
+    static constexpr int kSlice = gemm_slice_bytes(P, BN);  // K bytes per row per stage
+    static constexpr int kElems = kSlice / (P == Prec::TF32x3 ? 4 : 2);
+    static constexpr int kKSteps = kSlice / 32;              // MMA K steps of 32 bytes
+    static constexpr int kXBytes = kBM * kSlice;             // one 128-position Xs slice
+    static constexpr int kWBytes = BN * kSlice;              // one BN-row weight slice
     static constexpr int kStageBytes = kPlanes * (kXBytes + kWBytes);
     static constexpr int kBarBytes = 256;
     static constexpr int kStagesRaw = (kSmemMax - 1024 - kBarBytes) / kStageBytes;
     static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
     static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes;
-    // TMEM accumulators: as many BN-column buffers as fit 512 columns, at most 4, so the MMA
-    // can run several tiles ahead of the epilogue when tiles are narrow.
-    static constexpr int kAccBufs = 512 / BN > 4 ? 4 : 512 / BN;
-    static constexpr uint32_t kTmemCols = kAccBufs * BN;
+    // Grouped 3xTF32 accumulation keeps its running sums in a TMEM region of BN columns
+    // beside the accumulators for BN >= 128 (in registers they would not fit the 168 a
+    // thread has with 10 warps per SM), in registers for BN = 64.
+    static constexpr bool kTmemSum = P == Prec::TF32x3 && BN >= 128;
+    // TMEM accumulators: as many BN-column buffers as fit 512 columns (less the sum region),
+    // at most 4, so the MMA can run several tiles ahead of the epilogue.
+    static constexpr int kAccBufs = kTmemSum ? (512 - BN) / BN : (512 / BN > 4 ? 4 : 512 / BN);
+    static constexpr uint32_t kSumCol = kAccBufs * BN;       // first column of the sum region
+    static constexpr uint32_t kTmemCols = kAccBufs * BN + (kTmemSum ? BN : 0);
     static constexpr uint32_t kIdesc =
         ptx::idesc_f32acc(P == Prec::TF32x3 ? ptx::kFmtTF32 : ptx::kFmtBF16, kBM, BN);
     static_assert(kStages >= 2, "at least two pipeline stages");
     static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512,
                   "TMEM allocation is a power of two");
+    static_assert(kAccBufs >= 1, "at least one accumulator");
 };
 
 struct TileCoord {
@@ -171,9 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int kc = kb - g * gp.kb_per_tap;
                     const int uy = g / gp.mx;
                     const int ux = g - uy * gp.mx;
-                    constexpr int kElems = P == Prec::TF32x3 ? 32 : 64;
-                    const int32_t x_k = kc * kElems;
-                    const int32_t w_k = kb * kElems;
+                    const int32_t x_k = kc * C::kElems;
+                    const int32_t w_k = kb * C::kElems;
                     const int32_t x_row = (int32_t)(tc.p0 + (int64_t)uy * gp.Px + ux);
                     const int32_t w_row = (int32_t)tc.r0;
                     ptx::tma_load_2d(x_slice(stage, 0), &mapX, &full[stage], x_k, x_row);
@@ -226,15 +236,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         ptx::tc_fence_after();
-                        const uint64_t xd = ptx::sdesc_k_sw128(ptx::smem_u32(x_slice(stage, 0)));
-                        const uint64_t wd = ptx::sdesc_k_sw128(ptx::smem_u32(w_slice(stage, 0)));
+                        const uint64_t xd = ptx::sdesc_k<C::kSlice>(ptx::smem_u32(x_slice(stage, 0)));
+                        const uint64_t wd = ptx::sdesc_k<C::kSlice>(ptx::smem_u32(w_slice(stage, 0)));
                         uint64_t xdl = 0, wdl = 0;
                         if (P == Prec::TF32x3) {
-                            xdl = ptx::sdesc_k_sw128(ptx::smem_u32(x_slice(stage, 1)));
-                            wdl = ptx::sdesc_k_sw128(ptx::smem_u32(w_slice(stage, 1)));
+                            xdl = ptx::sdesc_k<C::kSlice>(ptx::smem_u32(x_slice(stage, 1)));
+                            wdl = ptx::sdesc_k<C::kSlice>(ptx::smem_u32(w_slice(stage, 1)));
                         }
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {  // four 32-byte K steps per 128-byte slice
+                        for (int k = 0; k < C::kKSteps; ++k) {  // 32-byte K steps of the slice
                             // +2 in the descriptor's start-address field = +32 bytes
                             const uint64_t dk = (uint64_t)(2 * k);
                             if (P == Prec::TF32x3) {
@@ -262,7 +272,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad + 31
+        const int quad = warp & 3;               // TMEM lanes 32*quad .. 32*quad + 31
+        constexpr int kChunks = BN / 64;         // 32-column chunks per warp
+        const int c_base = ((warp - 2) >> 2) * kChunks;  // this warp's first chunk
         const bool fused = gp.epi_mode == EPI_POLYPHASE;
         const uint32_t lane_addr = (uint32_t)(32 * quad) << 16;
         int grp = 0;
@@ -291,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto store_chunk = [&](const TileCoord &tc, const PosInfo &ps, int c, const float (&v)[32]) {
             const int64_t r0 = tc.r0 + 32 * c;
             if (fused) {
-                emit_cols(v, ps, r0, gp.epi);
+                emit_cols(v, ps, r0, gp.epi, lane);
                 return;
             }
             const int64_t pos = tc.p0 + 32 * quad + lane;
@@ -305,39 +317,83 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_ld_32x32b_x32(
                 tmem_base + lane_addr + (uint32_t)((g % C::kAccBufs) * BN + 32 * c), u);
         };
+        auto sum_chunk_ld = [&](int c, uint32_t (&u)[32]) {
+            ptx::tmem_ld_32x32b_x32(tmem_base + lane_addr + C::kSumCol + 32u * c, u);
+        };
         bool ok = true;
         for (int64_t t = blockIdx.x; ok && t < gp.num_tiles; t += gridDim.x) {
             const TileCoord tc = decode_tile(t, gp, BN);
             const int ngroups = (tc.kb1 - tc.kb0 + gp.kb_group - 1) / gp.kb_group;
             PosInfo ps{};
             if (fused) ps = decode_pos(tc.p0 + 32 * quad + lane, gp.epi);
-            if (P != Prec::TF32x3 || BN > kMaxGroupedBN || ngroups == 1) {
-                // One accumulation group: straight from TMEM to the output stage.
-                if (!(ok = wait_group(grp))) break;
+            if (C::kTmemSum && (ngroups > 1 || C::kAccBufs == 1)) {
+                // Each group's partial is added, with fp32 round-to-nearest, into the TMEM sum
+                // region (the first group is copied), and the accumulator is released at once;
+                // the output stage then reads the finished sums.  Same arithmetic, in the
+                // same order, as the register sums below.  (A single group with a single
+                // accumulator goes this way too, to release the accumulator before the
+                // stores.)
+                for (int g = 0; g < ngroups; ++g, ++grp) {
+                    if (!(ok = wait_group(grp))) break;
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                    for (int c = 0; c < kChunks; ++c) {
+                        uint32_t u[32], w[32];
+                        tmem_chunk(grp, c_base + c, u);
+                        if (g > 0) {
+                            sum_chunk_ld(c_base + c, w);
+                            ptx::tmem_wait_ld();
+#pragma unroll
+                            for (int cc = 0; cc < 32; ++cc)
+                                w[cc] = __float_as_uint(__uint_as_float(w[cc]) + __uint_as_float(u[cc]));
+                        } else {
+                            ptx::tmem_wait_ld();
+#pragma unroll
+                            for (int cc = 0; cc < 32; ++cc) w[cc] = u[cc];
+                        }
+                        ptx::tmem_st_32x32b_x32(tmem_base + lane_addr + C::kSumCol + 32u * (c_base + c), w);
+                    }
+                    ptx::tmem_wait_st();
+                    release_group(grp);
+                }
+                if (!ok) break;
+#pragma unroll 1
+                for (int c = 0; c < kChunks; ++c) {
                     uint32_t u[32];
-                    tmem_chunk(grp, c, u);
+                    sum_chunk_ld(c_base + c, u);
                     ptx::tmem_wait_ld();
-                    if (c == BN / 32 - 1) release_group(grp);  // TMEM no longer needed
                     float v[32];
 #pragma unroll
                     for (int cc = 0; cc < 32; ++cc) v[cc] = __uint_as_float(u[cc]);
-                    store_chunk(tc, ps, c, v);
+                    store_chunk(tc, ps, c_base + c, v);
+                }
+            } else if (P != Prec::TF32x3 || ngroups == 1) {
+                // One accumulation group: straight from TMEM to the output stage.
+                if (!(ok = wait_group(grp))) break;
+#pragma unroll 1
+                for (int c = 0; c < kChunks; ++c) {
+                    uint32_t u[32];
+                    tmem_chunk(grp, c_base + c, u);
+                    ptx::tmem_wait_ld();
+                    if (c == kChunks - 1) release_group(grp);  // TMEM no longer needed
+                    float v[32];
+#pragma unroll
+                    for (int cc = 0; cc < 32; ++cc) v[cc] = __uint_as_float(u[cc]);
+                    store_chunk(tc, ps, c_base + c, v);
                 }
                 ++grp;
-            } else if constexpr (P == Prec::TF32x3 && BN <= kMaxGroupedBN) {
+            } else if constexpr (P == Prec::TF32x3 && !C::kTmemSum) {
+                // BN = 64 only.
                 // Several groups: each group's partial leaves TMEM and is added, with fp32
                 // round-to-nearest, into running sums held in registers (this thread's
-                // position, all BN columns of the tile).  Keeps every tensor-core
+                // position, this warp's BN/2 columns of the tile).  Keeps every tensor-core
                 // accumulation chain short; see the group length chosen by the host.
-                float sum[BN / 32][32];
+                float sum[kChunks][32];
                 for (int g = 0; g < ngroups; ++g, ++grp) {
                     if (!(ok = wait_group(grp))) break;
 #pragma unroll
-                    for (int c = 0; c < BN / 32; ++c) {
+                    for (int c = 0; c < kChunks; ++c) {
                         uint32_t u[32];
-                        tmem_chunk(grp, c, u);
+                        tmem_chunk(grp, c_base + c, u);
                         ptx::tmem_wait_ld();
 #pragma unroll
                         for (int cc = 0; cc < 32; ++cc)
@@ -346,19 +402,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     release_group(grp);
                 }
                 if (!ok) break;
-                // One call site keeps store_chunk inlined; the chunk's sums are selected with
-                // compile-time indices so `sum` stays in registers.
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    float v[32];
+                // Unrolled (kChunks <= 2 here), so each chunk's sums die once stored.
 #pragma unroll
-                    for (int c2 = 0; c2 < BN / 32; ++c2)
-                        if (c2 == c) {
-#pragma unroll
-                            for (int cc = 0; cc < 32; ++cc) v[cc] = sum[c2][cc];
-                        }
-                    store_chunk(tc, ps, c, v);
-                }
+                for (int c = 0; c < kChunks; ++c) store_chunk(tc, ps, c_base + c, sum[c]);
             }
         }
     }

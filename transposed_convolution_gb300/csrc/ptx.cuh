@@ -149,19 +149,42 @@ __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor (tcgen05 format) of a K-major operand tile stored with
-// the 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.  Fields: start
-// address >> 4 in bits 0-13, leading byte offset >> 4 in 16-29 (unused for this layout, 1),
-// stride byte offset >> 4 in 32-45, the fixed value 1 in bits 46-47, base offset 0, and
-// the layout type in bits 61-63 (2 = 128-byte swizzle).  The tile base must be 1024-byte
-// aligned; stepping along K inside the 128-byte row adds the byte offset to the start.
-__device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t smem_addr) {
+// The store counterpart: thread i of the warp writes lane (taddr.lane + i), columns
+// taddr.col .. taddr.col + 31.
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+        ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+          "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]),
+          "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]),
+          "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]),
+          "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format) of a K-major operand tile whose rows are
+// RowBytes (128 or 64) wide and stored with the swizzle of that width, as TMA writes them
+// with CU_TENSOR_MAP_SWIZZLE_128B / _64B: 8-row groups 8 * RowBytes apart.  Fields: start
+// address >> 4 in bits 0-13, leading byte offset >> 4 in 16-29 (unused for swizzled K-major
+// layouts, 1), stride byte offset >> 4 in 32-45, the fixed value 1 in bits 46-47, base
+// offset 0, and the layout type in bits 61-63 (2 = 128-byte swizzle, 4 = 64-byte swizzle).
+// The tile base must be aligned to the swizzle pattern's repeat (8 rows); stepping along K
+// inside a row adds the byte offset to the start address.
+template <int RowBytes>
+__device__ __forceinline__ uint64_t sdesc_k(uint32_t smem_addr) {
+    static_assert(RowBytes == 128 || RowBytes == 64, "128- or 64-byte swizzled rows");
+    constexpr uint64_t kLayout = RowBytes == 128 ? 2 : 4;
     uint64_t d = 0;
     d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
     d |= static_cast<uint64_t>(1) << 16;
-    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>((8 * RowBytes) >> 4) << 32;
     d |= static_cast<uint64_t>(1) << 46;
-    d |= static_cast<uint64_t>(2) << 61;
+    d |= kLayout << 61;
     return d;
 }
 
