@@ -75,9 +75,9 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload):
-    """DRAM bytes per launch of the GEMM kernel from the committed ncu summary, or None when
-    there is none or the kernel sources changed since it was taken."""
+def profiled_traffic(workload, layer=0, layers=1):
+    """DRAM bytes per launch of a layer's GEMM kernel from the committed ncu summary, or None
+    when there is none or the kernel sources changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "gemm_tc_%s.md" % workload)
     if not os.path.exists(path):
         return None
@@ -88,8 +88,9 @@ def profiled_traffic(workload):
             vals[k.strip()] = v.strip().strip("`")
     if vals.get("kernel_source_sha256") != kernel_source_hash():
         return None
+    key = "dram_bytes_per_launch" if layers == 1 else "dram_bytes_per_launch_layer%d" % layer
     try:
-        return int(float(vals["dram_bytes_per_launch"]))
+        return int(float(vals[key]))
     except (KeyError, ValueError):
         return None
 
@@ -381,7 +382,7 @@ def run_ours(args, rank, world, local_rank):
     else:
         achieved, peak, unit = L.compulsory_bytes / kern_s / 1e9, peaks["hbm_gbs"], "GB/s"
         peak_note = "HBM copy bandwidth, %s" % peak_src
-    traffic = profiled_traffic(args.workload) if nl == 1 else None
+    traffic = profiled_traffic(args.workload, j, nl)
     clocks = sampler.summary(soak_t0, wall1 + 0.25)
     kname = "gemm_tc_kernel" if sets[0]["plans"][j].path != ctr.CTR_PATH_GATHER else "gather_kernel"
 
