@@ -11,9 +11,10 @@ upsampler (1x512x2000 -> 1x256x16000, kernel 16, stride 8, padding 4, fp32 I/O).
 Timing: W untimed warm-up steps and a ~1 s soak of the same step, then exactly K steps
 bracketed by a barrier and torch.cuda.synchronize() on both sides, each step between CUDA
 events on the launching stream.  Each timed step is the CUDA-graph replay of one captured
-step (the library's own launches; --no-graph times the plain calls), so the device time
-is not inflated by the Python host path; the "e2e" figure goes through the plain public
-call with host copies.  Consecutive steps rotate over enough sets of input,
+step (the library's own launches; --no-graph times the plain calls); the "e2e" figure goes
+through the plain public call with host copies.  The main kernels' own durations (for the
+roofline) come from a second run of the same K steps with an event pair around each of
+them, because an event between two kernels would serialise their programmatic launch.  Consecutive steps rotate over enough sets of input,
 packed weight, workspace and output buffers to exceed twice the L2 size, so no step reads
 data the previous one left in L2.  Under torchrun every rank runs the same workload on its
 own GPU (weak scaling, no collective on the data path); rank 0 prints one JSON line with
@@ -245,10 +246,11 @@ def run_ours(args, rank, world, local_rank):
             p.check()
 
     # Timed region: exactly K steps.  Each step is captured once, untimed, as a CUDA graph
-    # of the library's launches (with its own kernel-timing events, recorded as external
-    # event nodes) and replayed in the timed loop, so the GPU runs the steps back to back
-    # instead of waiting for the Python host path between kernels.  --no-graph times the
-    # plain calls instead.
+    # of the library's launches and replayed in the timed loop (--no-graph times the plain
+    # calls).  Kernels chain by programmatic dependent launch, and an event recorded between
+    # two kernels would serialise them, so the step time (value) is taken over K steps without
+    # per-kernel events, and the main kernels' own durations (roofline) over a second run of
+    # K steps whose captured steps record them (as external event nodes).
     K = args.steps
     nl = len(Ls)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -261,25 +263,30 @@ def run_ours(args, rank, world, local_rank):
             b.record()
     torch.cuda.synchronize()
     launches0 = ctr.ctr_launch_count()
-    graphs = None
+    graphs = graphs_k = None
     if args.graph:
-        graphs = []
+        graphs, graphs_k = [], []
         cap = torch.cuda.Stream()
         for k in range(K):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=cap):
-                run_set(sets[k % nsets], kevs=kev[k])
+                run_set(sets[k % nsets])
             graphs.append(g)
         launches = ctr.ctr_launch_count() - launches0
-        for g in graphs:      # first replays upload the graphs (untimed)
+        for k in range(K):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                run_set(sets[k % nsets], kevs=kev[k])
+            graphs_k.append(g)
+        for g in graphs + graphs_k:   # first replays upload the graphs (untimed)
             g.replay()
         torch.cuda.synchronize()
 
-    def step(k):
+    def step(k, kernel_events=False):
         if graphs is not None:
-            graphs[k].replay()
+            (graphs_k if kernel_events else graphs)[k].replay()
         else:
-            run_set(sets[k % nsets], kevs=kev[k])
+            run_set(sets[k % nsets], kevs=kev[k] if kernel_events else None)
 
     sampler = ClockSampler(local_rank)
     sampler.start()
@@ -305,6 +312,12 @@ def run_ours(args, rank, world, local_rank):
     wall1 = time.time()
     if graphs is None:
         launches = ctr.ctr_launch_count() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    # Kernel durations: the same K steps again, each main kernel between its own events.
+    for k in range(K):
+        step(k, kernel_events=True)
+    torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     time.sleep(0.25)
@@ -403,8 +416,8 @@ def run_ours(args, rank, world, local_rank):
                    "l2": "rotating %d buffer sets, %.0f MB > 2x L2 (%.0f MB)"
                          % (nsets, nsets * set_bytes / 1e6, l2 / 1e6),
                    "parallelism": "replica per GPU" if world > 1 else "single GPU",
-                   "launch": "CUDA graph replay per step" if graphs is not None
-                             else "plain calls",
+                   "launch": ("CUDA graph replay per step" if graphs is not None
+                              else "plain calls") + "; kernel times from a second K-step run",
                    "plan": " | ".join(p.describe() for p in sets[0]["plans"])},
         "pct_of_roofline": round(100.0 * t_roof / (ms_per_step / 1e3), 2),
         "roofline_us": round(t_roof * 1e6, 3),

@@ -112,6 +112,9 @@ ctr_status ctr_plan_set_activation(ctr_plan_t plan, int act, float negative_slop
  * paths (0 = automatic, else 1..16).  Host only.  Must come before ctr_packed_weight_bytes,
  * ctr_workspace_bytes and ctr_prepack_weight, because the packed layout and the workspace
  * depend on the path; calling it after ctr_prepack_weight returns CTR_ERR_INVALID_ARG.
+ * The tensor-core paths index tiles, staged input positions and packed weight rows in 32
+ * bits: a plan that exceeds 2^31 of any of them runs the gather path when chosen
+ * automatically, and forcing a tensor-core path on it returns CTR_ERR_UNSUPPORTED.
  */
 ctr_status ctr_plan_set_path(ctr_plan_t plan, int path, int split_k);
 

@@ -56,3 +56,26 @@ def test_graph_replay_follows_inputs(case):
             assert e0.elapsed_time(e1) > 0.0
     finally:
         plan.close()
+
+
+@pytest.mark.gpu
+def test_timing_events_outside_capture():
+    """The measurement hook on plain (uncaptured) calls: both events record and bracket the
+    main kernel."""
+    import torch
+    plan = ctr.Plan(1, 64, 32, (200,), (16,), 8, 4, 0, dtype=torch.float32)
+    try:
+        plan.prepack(torch.randn(64, 32, 16, device="cuda"))
+        x = torch.randn(1, 64, 200, device="cuda")
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        e1.record()
+        ctr.ctr_plan_set_timing_events(plan.handle, e0.cuda_event, e1.cuda_event)
+        plan.forward(x)
+        ctr.ctr_plan_set_timing_events(plan.handle, None, None)
+        torch.cuda.synchronize()
+        plan.check()
+        assert e0.elapsed_time(e1) > 0.0
+    finally:
+        plan.close()

@@ -181,6 +181,15 @@ void layout_plan(ctr_plan_s *pl) {
     pl->ws_bytes_needed = (pl->ws_stage_bytes || pl->ws_raw_bytes) ? off : 0;
 }
 
+// The tensor-core kernels index tiles, staged positions (with the largest tap shift) and
+// packed rows in 32 bits.
+bool tc_index_fits(const ctr_plan_s *pl) {
+    const int64_t lim = (int64_t)1 << 31;
+    const int64_t shift = pl->P[1] * (pl->m[0] - 1) + pl->m[1];
+    return pl->num_p_tiles * (int64_t)ctr::kBM + shift < lim && pl->num_tiles < lim &&
+           pl->M_pad + 256 < lim;
+}
+
 int choose_path(const ctr_plan_s *pl) {
     if (pl->forced_path != CTR_PATH_AUTO) return pl->forced_path;
     const bool kdiv = (pl->k[0] % pl->s[0] == 0) && (pl->k[1] % pl->s[1] == 0);
@@ -307,9 +316,15 @@ int64_t raw_split_stride_of(const ctr_plan_s *pl) {
 // the staged input and the raw partials at the plan's offsets; status is the device status
 // word the GEMM reports bounded-wait timeouts into.
 // Records a timing event.  Under stream capture it becomes an external event-record node,
-// so every replay of the graph records it (a plain record would only order the graph).
+// so every replay of the graph records it (a plain record would only order the graph);
+// outside capture it is a plain record (the external flag is for capture only).
 cudaError_t record_timing(cudaEvent_t ev, cudaStream_t st) {
-    return cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    const cudaError_t e = cudaStreamIsCapturing(st, &cs);
+    if (e != cudaSuccess) return e;
+    return cs == cudaStreamCaptureStatusActive
+               ? cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal)
+               : cudaEventRecord(ev, st);
 }
 
 cudaError_t run_tc_path(const ctr_plan_s *pl, const void *x, const void *w_packed,
@@ -453,6 +468,10 @@ ctr_status ctr_plan_create(ctr_plan_t *out, int ndim, int64_t N, int64_t C_in, i
     pl->num_sms = query_num_sms();
     pl->path = choose_path(pl);
     layout_plan(pl);
+    if (is_tc_path(pl->path) && !tc_index_fits(pl)) {  // too large for 32-bit tile indexing
+        pl->path = CTR_PATH_GATHER;
+        layout_plan(pl);
+    }
     *out = pl;
     return CTR_OK;
 }
@@ -472,6 +491,11 @@ ctr_status ctr_plan_set_path(ctr_plan_t pl, int path, int split_k) {
     pl->forced_split = split_k;
     pl->path = choose_path(pl);
     layout_plan(pl);
+    if (is_tc_path(pl->path) && !tc_index_fits(pl)) {
+        if (path != CTR_PATH_AUTO) return CTR_ERR_UNSUPPORTED;
+        pl->path = CTR_PATH_GATHER;
+        layout_plan(pl);
+    }
     return CTR_OK;
 }
 

@@ -206,6 +206,8 @@ template <bool BF16, bool VEC>
 __global__ void __launch_bounds__(kStageThreads) stage_x_kernel(const void *__restrict__ x,
                                                                void *__restrict__ xs,
                                                                StageGeo sg, StageUnits su) {
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     using T = typename std::conditional<BF16, __nv_bfloat16, float>::type;
     constexpr int kStageC = BF16 ? 64 : 32;      // channels per tile (128 bytes of a row)
     constexpr int kInVec = 16 / sizeof(T);       // positions per 16-byte load
@@ -314,6 +316,8 @@ __global__ void __launch_bounds__(kStageThreads) stage_x_kernel(const void *__re
 __global__ void splitk_reduce_kernel(const float *__restrict__ raw, EpiParams ep, int64_t ld,
                                      int64_t split_stride, int splits, int64_t n_rows,
                                      int64_t n_pad, int64_t r_chunks) {
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= n_pad * r_chunks) return;   // whole warps: n_pad * r_chunks is a multiple of 32
     const int64_t rc = idx / n_pad;
@@ -369,6 +373,8 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ raw, EpiParams ep
 __global__ void col2im_kernel(const float *__restrict__ col, int64_t ld, int64_t split_stride,
                               int splits, int S_pad, const void *__restrict__ bias,
                               void *__restrict__ y, Geo g, int64_t total) {
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
         const int64_t ox = idx % g.Wo;
@@ -478,17 +484,17 @@ cudaError_t launch_stage_x(const ctr_plan_s *pl, const void *x, void *xs, cudaSt
     const int64_t blocks = std::min<int64_t>(su.tiles, (int64_t)pl->num_sms * 8);
     const bool vec = (sg.W * (sg.bf16 ? 2 : 4)) % 16 == 0;
     const dim3 grid((unsigned)blocks);
+    cudaError_t e;
+#define CTR_STAGE(B, V)                                                                   \
+    if ((e = prefer_max_smem<stage_x_kernel<B, V>>()) != cudaSuccess) return e;          \
+    e = launch_pdl(stage_x_kernel<B, V>, grid, dim3(kStageThreads), 0, st, x, xs, sg, su)
     if (sg.bf16) {
-        if (vec)
-            stage_x_kernel<true, true><<<grid, kStageThreads, 0, st>>>(x, xs, sg, su);
-        else
-            stage_x_kernel<true, false><<<grid, kStageThreads, 0, st>>>(x, xs, sg, su);
+        if (vec) { CTR_STAGE(true, true); } else { CTR_STAGE(true, false); }
     } else {
-        if (vec)
-            stage_x_kernel<false, true><<<grid, kStageThreads, 0, st>>>(x, xs, sg, su);
-        else
-            stage_x_kernel<false, false><<<grid, kStageThreads, 0, st>>>(x, xs, sg, su);
+        if (vec) { CTR_STAGE(false, true); } else { CTR_STAGE(false, false); }
     }
+#undef CTR_STAGE
+    if (e != cudaSuccess) return e;
     count_launches(1);
     return cudaGetLastError();
 }
@@ -500,8 +506,11 @@ cudaError_t launch_splitk_reduce(const ctr_plan_s *pl, const float *raw, const E
     const int64_t r_chunks = ceil_div(std::min<int64_t>(pl->M_rows, raw_ld), 32);
     const int64_t total = n_pad * r_chunks;
     if (n_rows == 0 || r_chunks == 0) return cudaSuccess;
-    splitk_reduce_kernel<<<grid_for(total, 64), 64, 0, st>>>(raw, ep, raw_ld, split_stride,
-                                                             pl->splits, n_rows, n_pad, r_chunks);
+    cudaError_t e = prefer_max_smem<splitk_reduce_kernel>();
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(splitk_reduce_kernel, dim3(grid_for(total, 64)), dim3(64), 0, st, raw, ep,
+                   raw_ld, split_stride, pl->splits, n_rows, n_pad, r_chunks);
+    if (e != cudaSuccess) return e;
     count_launches(1);
     return cudaGetLastError();
 }
@@ -512,9 +521,11 @@ cudaError_t launch_col2im(const ctr_plan_s *pl, const float *col, int64_t col_ld
     const int64_t total = g.B * g.C_out * g.Ho * g.Wo;
     if (total == 0) return cudaSuccess;
     const int64_t split_stride = raw_split_stride_of(pl);
-    col2im_kernel<<<grid_for(total, kBlock), kBlock, 0, st>>>(col, col_ld, split_stride,
-                                                              pl->splits, pl->S_pad, bias, y, g,
-                                                              total);
+    cudaError_t e = prefer_max_smem<col2im_kernel>();
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(col2im_kernel, dim3(grid_for(total, kBlock)), dim3(kBlock), 0, st, col,
+                   col_ld, split_stride, pl->splits, pl->S_pad, bias, y, g, total);
+    if (e != cudaSuccess) return e;
     count_launches(1);
     return cudaGetLastError();
 }

@@ -125,6 +125,38 @@ struct ctr_plan_s {
 
 namespace ctr {
 
+// Launch with programmatic stream serialization: the kernel may be scheduled while the
+// previous kernel of the stream is still running, so it must call ptx::griddep_wait() before
+// its first global memory access; its launch and prologue then overlap the previous
+// kernel's tail instead of following its completion.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
+// Prefer the largest shared-memory carveout for a kernel (once per kernel), so that
+// consecutive kernels of a forward pass do not reconfigure the SMs between them.
+template <auto Kernel>
+cudaError_t prefer_max_smem() {
+    static bool done = false;
+    if (done) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(
+        Kernel, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+    done = e == cudaSuccess;
+    return e;
+}
+
 // Launch wrappers (each returns the cudaGetLastError() of its launches).
 cudaError_t launch_gather(const ctr_plan_s *pl, const void *x, const void *w, const void *bias,
                           void *y, cudaStream_t st);

@@ -43,13 +43,16 @@ struct PosInfo {
     bool valid;
 };
 
+// 32-bit arithmetic: the host keeps positions below 2^31 (see decode_tile).
 __device__ __forceinline__ PosInfo decode_pos(int64_t n, const EpiParams &e) {
     PosInfo p;
-    const int64_t plane = e.Py * e.Px;
-    p.b = n / plane;
-    const int64_t rem = n - p.b * plane;
-    p.qy = rem / e.Px;
-    p.qx = rem - p.qy * e.Px;
+    const uint32_t nn = (uint32_t)n, px = (uint32_t)e.Px, plane = (uint32_t)(e.Py * e.Px);
+    const uint32_t b = nn / plane;
+    const uint32_t rem = nn - b * plane;
+    const uint32_t qy = rem / px;
+    p.b = b;
+    p.qy = qy;
+    p.qx = rem - qy * px;
     p.valid = p.b < e.B && p.qy < e.Qvy && p.qx < e.Qvx;
     return p;
 }
@@ -113,16 +116,21 @@ __device__ __forceinline__ void store_run(T *dst, const float *vals, int wbytes)
 // One run of NX consecutive outputs at dst (x = x0 .. x0+NX-1 of one output row) from
 // v[0..NX-1]: bias, activation (slope_eff = 1 when there is none), then aligned vector
 // stores inside the row, or element stores with bounds checks at its edges.
+// LeakyReLU as one multiply and one max (slope <= 1) or min (slope > 1): equal to
+// (a < 0 ? a * slope : a) for every a, NaN included; slope 1 is the identity.
+__device__ __forceinline__ float leaky(float a, float slope_eff, bool use_min) {
+    const float m = a * slope_eff;
+    return use_min ? fminf(a, m) : fmaxf(a, m);
+}
+
 template <typename T, int NX>
 __device__ __forceinline__ void emit_run(T *__restrict__ dst, int64_t x0, const float *v,
                                          float bias, float slope_eff, const EpiParams &e,
                                          bool interior) {
+    const bool use_min = slope_eff > 1.0f;
     float t[NX];
 #pragma unroll
-    for (int i = 0; i < NX; ++i) {
-        const float a = v[i] + bias;
-        t[i] = a < 0.0f ? a * slope_eff : a;
-    }
+    for (int i = 0; i < NX; ++i) t[i] = leaky(v[i] + bias, slope_eff, use_min);
     if (interior) {
         store_run<T, NX>(dst, t, e.store_bytes);
     } else {
@@ -158,21 +166,26 @@ __device__ __forceinline__ void emit_small(const float (&v)[32], const PosInfo &
     const int64_t oy0 = (int64_t)SY * ps.qy - e.py;
     const bool interior = x0 >= 0 && x0 + SX <= e.Wout;
     const int64_t cstride = e.Hout * e.Wout;
+    // Channels of this chunk inside C_out (the same on every lane) and rows inside the
+    // output for this lane's position, decided once for the chunk.
+    const int64_t g_left = e.C_out - oc0;
+    const int gmax = g_left < G ? (int)g_left : G;
+    bool row_ok[SY];
+#pragma unroll
+    for (int jy = 0; jy < SY; ++jy) row_ok[jy] = ps.valid && oy0 + jy >= 0 && oy0 + jy < e.Hout;
     // Output of (oc0, oy0, x0); rows and channels below are offsets from it.
-    T *__restrict__ base = static_cast<T *>(e.y) + ((ps.b * e.C_out + oc0) * e.Hout + oy0) * e.Wout + x0;
+    T *__restrict__ dst = static_cast<T *>(e.y) + ((ps.b * e.C_out + oc0) * e.Hout + oy0) * e.Wout + x0;
     // Every lane runs the channel loop (the shuffles need the whole warp); lanes whose
     // position lies outside the output store nothing.
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-        if (oc0 + g >= e.C_out) break;   // uniform: oc0 is the same on every lane
+    for (int g = 0; g < G; ++g, dst += cstride) {
+        if (g >= gmax) break;
         const float bias = __shfl_sync(0xffffffffu, bl, g);
-        if (!ps.valid) continue;
 #pragma unroll
-        for (int jy = 0; jy < SY; ++jy) {
-            if (oy0 + jy < 0 || oy0 + jy >= e.Hout) continue;
-            emit_run<T, SX>(base + g * cstride + jy * e.Wout, x0, &v[g * S + jy * SX], bias,
-                            slope_eff, e, interior);
-        }
+        for (int jy = 0; jy < SY; ++jy)
+            if (row_ok[jy])
+                emit_run<T, SX>(dst + jy * e.Wout, x0, &v[g * S + jy * SX], bias, slope_eff, e,
+                                interior);
     }
 }
 
@@ -181,7 +194,7 @@ __device__ __forceinline__ void emit_small(const float (&v)[32], const PosInfo &
 template <typename T>
 __device__ __forceinline__ void emit_large(const float (&v)[32], const PosInfo &ps, int64_t r0,
                                            const EpiParams &e, int lane) {
-    const int64_t oc = r0 / e.S_pad;
+    const int64_t oc = (uint32_t)r0 / (uint32_t)e.S_pad;
     const float bias = __shfl_sync(0xffffffffu, lane_bias(e, oc, 1, lane), 0);
     if (!ps.valid || oc >= e.C_out) return;
     const int64_t j0 = r0 - oc * e.S_pad;
@@ -198,9 +211,9 @@ __device__ __forceinline__ void emit_generic(const float (&v)[32], const PosInfo
     const float slope_eff = slope_of(e);
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-        const int64_t r = r0 + i;
-        const int64_t oc = r / e.S_pad;
-        const int j = (int)(r - oc * e.S_pad);
+        const uint32_t r = (uint32_t)r0 + i;
+        const uint32_t oc = r / (uint32_t)e.S_pad;
+        const int j = (int)(r - oc * (uint32_t)e.S_pad);
         if (oc >= e.C_out || j >= e.S) continue;
         const int jy = j / e.sx, jx = j - (j / e.sx) * e.sx;
         const int64_t oy = (int64_t)e.sy * ps.qy + jy - e.py;

@@ -80,21 +80,26 @@ struct Cfg {
 };
 
 struct TileCoord {
-    int64_t p0, r0;
+    int p0, r0;
     int z, kb0, kb1;
 };
 
-// Tile t -> (row tile fastest, then position tile, then split).
-__device__ __forceinline__ TileCoord decode_tile(int64_t t, const GemmParams &gp, int bn) {
+// Tile t -> (row tile fastest, then position tile, then split).  32-bit arithmetic: the host
+// keeps tiles, positions and rows below 2^31 (64-bit divisions are long software sequences
+// and every role decodes every tile).
+__device__ __forceinline__ TileCoord decode_tile(uint32_t t, const GemmParams &gp, int bn) {
     TileCoord c;
-    const int64_t r_tile = t % gp.num_r_tiles;
-    const int64_t rest = t / gp.num_r_tiles;
-    const int64_t p_tile = rest % gp.num_p_tiles;
-    c.z = (int)(rest / gp.num_p_tiles);
-    c.r0 = r_tile * bn;
-    c.p0 = p_tile * kBM;
-    c.kb0 = (int)((int64_t)c.z * gp.kb_total / gp.splits);
-    c.kb1 = (int)((int64_t)(c.z + 1) * gp.kb_total / gp.splits);
+    const uint32_t nr = (uint32_t)gp.num_r_tiles, np = (uint32_t)gp.num_p_tiles;
+    const uint32_t rest = t / nr;
+    const uint32_t r_tile = t - rest * nr;
+    const uint32_t z = rest / np;
+    const uint32_t p_tile = rest - z * np;
+    c.z = (int)z;
+    c.r0 = (int)(r_tile * (uint32_t)bn);
+    c.p0 = (int)(p_tile * (uint32_t)kBM);
+    const uint32_t kbt = (uint32_t)gp.kb_total, sp = (uint32_t)gp.splits;
+    c.kb0 = (int)(z * kbt / sp);
+    c.kb1 = (int)((z + 1) * kbt / sp);
     return c;
 }
 
@@ -161,6 +166,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
+    // Everything above touched only shared memory, TMEM and the kernel parameters, so it may
+    // overlap the previous kernel of the stream; global memory waits for it.
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     const uint32_t tmem_base = *tmem_slot;
     const uint64_t limit = gp.wait_limit_ns;
 
@@ -171,17 +180,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             int64_t issued = 0;
             for (int64_t t = blockIdx.x; t < gp.num_tiles && !*abort; t += gridDim.x) {
-                const TileCoord tc = decode_tile(t, gp, BN);
+                const TileCoord tc = decode_tile((uint32_t)t, gp, BN);
+                // Tap (uy, ux) and channel slice kc of K slice kb, stepped along with kb.
+                const int g0 = tc.kb0 / gp.kb_per_tap;
+                int kc = tc.kb0 - g0 * gp.kb_per_tap;
+                int uy = g0 / gp.mx;
+                int ux = g0 - uy * gp.mx;
                 for (int kb = tc.kb0; kb < tc.kb1; ++kb) {
                     if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, limit, abort)) {
                         if (!*abort) give_up(abort, gp.status, kStatusTimeoutProducer);
                         break;
                     }
                     ptx::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-                    const int g = kb / gp.kb_per_tap;
-                    const int kc = kb - g * gp.kb_per_tap;
-                    const int uy = g / gp.mx;
-                    const int ux = g - uy * gp.mx;
                     const int32_t x_k = kc * C::kElems;
                     const int32_t w_k = kb * C::kElems;
                     const int32_t x_row = (int32_t)(tc.p0 + (int64_t)uy * gp.Px + ux);
@@ -193,6 +203,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::tma_load_2d(w_slice(stage, 1), &mapW2, &full[stage], w_k, w_row);
                     }
                     ++issued;
+                    if (++kc == gp.kb_per_tap) {
+                        kc = 0;
+                        if (++ux == gp.mx) {
+                            ux = 0;
+                            ++uy;
+                        }
+                    }
                     if (++stage == C::kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -216,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int grp = 0;  // accumulation groups issued by this CTA (selects the TMEM buffer)
             bool ok = true;
             for (int64_t t = blockIdx.x; ok && t < gp.num_tiles && !*abort; t += gridDim.x) {
-                const TileCoord tc = decode_tile(t, gp, BN);
+                const TileCoord tc = decode_tile((uint32_t)t, gp, BN);
                 for (int kb = tc.kb0; ok && kb < tc.kb1; ++grp) {
                     const int kb_end = min(kb + gp.kb_group, tc.kb1);
                     const int acc = grp % C::kAccBufs;
@@ -306,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 emit_cols(v, ps, r0, gp.epi, lane);
                 return;
             }
-            const int64_t pos = tc.p0 + 32 * quad + lane;
+            const int64_t pos = (int64_t)tc.p0 + 32 * quad + lane;
             float4 *dst = reinterpret_cast<float4 *>(gp.raw + (int64_t)tc.z * gp.raw_split_stride +
                                                      pos * gp.raw_ld + r0);
 #pragma unroll
@@ -322,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         bool ok = true;
         for (int64_t t = blockIdx.x; ok && t < gp.num_tiles; t += gridDim.x) {
-            const TileCoord tc = decode_tile(t, gp, BN);
+            const TileCoord tc = decode_tile((uint32_t)t, gp, BN);
             const int ngroups = (tc.kb1 - tc.kb0 + gp.kb_group - 1) / gp.kb_group;
             PosInfo ps{};
             if (fused) ps = decode_pos(tc.p0 + 32 * quad + lane, gp.epi);
@@ -432,8 +449,9 @@ cudaError_t launch_inst(const ctr_plan_s *pl, const CUtensorMap *maps, const Gem
         attr_set = true;
     }
     const int64_t grid = std::min<int64_t>(gp.num_tiles, pl->num_sms);
-    gemm_tc_kernel<P, BN><<<(unsigned)grid, kThreads, C::kSmem, st>>>(maps[0], maps[1], maps[2],
-                                                                      maps[3], gp);
+    const cudaError_t e = launch_pdl(gemm_tc_kernel<P, BN>, dim3((unsigned)grid), dim3(kThreads),
+                                     (size_t)C::kSmem, st, maps[0], maps[1], maps[2], maps[3], gp);
+    if (e != cudaSuccess) return e;
     count_launches(1);
     return cudaGetLastError();
 }

@@ -50,6 +50,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not yet complete may sleep up
+// to hint_ns (waking as soon as the phase completes) instead of returning at once, so a
+// waiting role spends few issue slots while others work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Suspend-time hint of the bounded waits (nanoseconds): long against the time a phase
+// takes to complete, short against any wait limit.
+constexpr uint32_t kWaitHintNs = 20000;
+
 // Wait until the phase of `bar` with the given parity has completed.  Bounded: gives up
 // once limit_ns nanoseconds of global time have passed (at once when limit_ns is 0 and the
 // phase is not complete on the first poll), or as soon as *abort becomes non-zero (abort
@@ -59,11 +79,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
     if (mbar_try_wait(bar, parity)) return true;
     if (limit_ns == 0) return false;
     const uint64_t t0 = globaltimer_ns();
+    const uint32_t hint = limit_ns < kWaitHintNs ? (uint32_t)limit_ns : kWaitHintNs;
     for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, hint)) return true;
         if (abort && *abort) return false;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
+}
+
+// ---------------------------------------------------------------- programmatic dependent launch
+// Wait until the grids this one depends on (the previous kernels of the stream, when this one
+// was launched with programmatic stream serialization) have completed and their memory is
+// visible; a no-op otherwise.  Every kernel calls it before its first global memory access.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Let the next kernel of the stream be scheduled now (it still waits for this grid's
+// completion before touching memory).
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- TMA
