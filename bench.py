@@ -10,9 +10,10 @@ upsampler (1x512x2000 -> 1x256x16000, kernel 16, stride 8, padding 4, fp32 I/O).
 
 Timing: W untimed warm-up steps and a ~1 s soak of the same step, then exactly K steps
 bracketed by a barrier and torch.cuda.synchronize() on both sides, each step between CUDA
-events on the launching stream.  Each timed step is the CUDA-graph replay of one captured
-step (the library's own launches; --no-graph times the plain calls); the "e2e" figure goes
-through the plain public call with host copies.  The main kernels' own durations (for the
+events on the launching stream.  The K timed steps are captured once into one CUDA graph of
+the library's own launches and replayed between two events (--no-graph times plain calls,
+an event pair per step); the "e2e" figure goes through the plain public call with host
+copies, step by step.  The main kernels' own durations (for the
 roofline) come from a second run of the same K steps with an event pair around each of
 them, because an event between two kernels would serialise their programmatic launch.  Consecutive steps rotate over enough sets of input,
 packed weight, workspace and output buffers to exceed twice the L2 size, so no step reads
@@ -245,12 +246,14 @@ def run_ours(args, rank, world, local_rank):
         for p in s["plans"]:
             p.check()
 
-    # Timed region: exactly K steps.  Each step is captured once, untimed, as a CUDA graph
-    # of the library's launches and replayed in the timed loop (--no-graph times the plain
-    # calls).  Kernels chain by programmatic dependent launch, and an event recorded between
-    # two kernels would serialise them, so the step time (value) is taken over K steps without
-    # per-kernel events, and the main kernels' own durations (roofline) over a second run of
-    # K steps whose captured steps record them (as external event nodes).
+    # Timed region: exactly K steps.  The K steps (rotating over the buffer sets) are captured
+    # once, untimed, into one CUDA graph of the library's launches and replayed between two
+    # events, so per-step launch overhead is paid once per K steps (--no-graph times plain
+    # calls, one event pair per step).  Kernels chain by programmatic dependent launch, and an
+    # event recorded between two kernels would serialise them, so the step time (value) comes
+    # from a run without per-kernel events, and the main kernels' own durations (roofline)
+    # from a second run of the same K steps whose captured steps record them (as external
+    # event nodes).
     K = args.steps
     nl = len(Ls)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -263,60 +266,59 @@ def run_ours(args, rank, world, local_rank):
             b.record()
     torch.cuda.synchronize()
     launches0 = ctr.ctr_launch_count()
-    graphs = graphs_k = None
+    graph = graph_k = None
     if args.graph:
-        graphs, graphs_k = [], []
         cap = torch.cuda.Stream()
-        for k in range(K):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=cap):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            for k in range(K):
                 run_set(sets[k % nsets])
-            graphs.append(g)
         launches = ctr.ctr_launch_count() - launches0
-        for k in range(K):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=cap):
+        graph_k = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_k, stream=cap):
+            for k in range(K):
                 run_set(sets[k % nsets], kevs=kev[k])
-            graphs_k.append(g)
-        for g in graphs + graphs_k:   # first replays upload the graphs (untimed)
-            g.replay()
+        graph.replay()            # first replays upload the graphs (untimed)
+        graph_k.replay()
         torch.cuda.synchronize()
 
-    def step(k, kernel_events=False):
-        if graphs is not None:
-            (graphs_k if kernel_events else graphs)[k].replay()
-        else:
+    def steps(kernel_events=False):
+        """All K steps (one graph replay, or K plain steps with an event pair each)."""
+        if graph is not None:
+            (graph_k if kernel_events else graph).replay()
+            return
+        for k in range(K):
+            if not kernel_events:
+                ev[k][0].record()
             run_set(sets[k % nsets], kevs=kev[k] if kernel_events else None)
+            if not kernel_events:
+                ev[k][1].record()
 
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.3)
     soak_t0 = time.time()
-    i = 0
     while time.time() - soak_t0 < args.soak:
-        for _ in range(50):
-            step(i % K)
-            i += 1
+        steps()
         torch.cuda.synchronize()
 
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     launches0 = ctr.ctr_launch_count()
+    t_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
     wall0 = time.time()
-    for k in range(K):
-        ev[k][0].record()
-        step(k)
-        ev[k][1].record()
+    t_ev[0].record()
+    steps()
+    t_ev[1].record()
     torch.cuda.synchronize()
     wall1 = time.time()
-    if graphs is None:
+    if graph is None:
         launches = ctr.ctr_launch_count() - launches0
     if world > 1:
         torch.distributed.barrier()
     # Kernel durations: the same K steps again, each main kernel between its own events.
-    for k in range(K):
-        step(k, kernel_events=True)
+    steps(kernel_events=True)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -326,7 +328,9 @@ def run_ours(args, rank, world, local_rank):
         for p in s["plans"]:
             p.check()
 
-    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_window_ms = t_ev[0].elapsed_time(t_ev[1])
+    step_ms = ([total_window_ms / K] * K if graph is not None
+               else [a.elapsed_time(b) for a, b in ev])
     kern_ms = [sum(kev[k][j][0].elapsed_time(kev[k][j][1]) for k in range(K)) / K
                for j in range(nl)]
     total_ms = sum(step_ms)
@@ -416,7 +420,7 @@ def run_ours(args, rank, world, local_rank):
                    "l2": "rotating %d buffer sets, %.0f MB > 2x L2 (%.0f MB)"
                          % (nsets, nsets * set_bytes / 1e6, l2 / 1e6),
                    "parallelism": "replica per GPU" if world > 1 else "single GPU",
-                   "launch": ("CUDA graph replay per step" if graphs is not None
+                   "launch": ("one CUDA graph of the K steps" if graph is not None
                               else "plain calls") + "; kernel times from a second K-step run",
                    "plan": " | ".join(p.describe() for p in sets[0]["plans"])},
         "pct_of_roofline": round(100.0 * t_roof / (ms_per_step / 1e3), 2),
