@@ -127,18 +127,6 @@ ctr_status ctr_plan_set_path(ctr_plan_t plan, int path, int split_k);
  */
 ctr_status ctr_plan_set_tile(ctr_plan_t plan, int block_n);
 
-/*
- * Choose the tensor-core GEMM's schedule: -1 = automatic (default; never stream-K at
- * present), 0 = one output tile (or split-K part) per CTA at a time, 1 = stream-K: the
- * tiles' K slices are split evenly over
- * one CTA per SM; a CTA finishing a tile adds the other CTAs' fp32 partials in ascending K
- * order, so results are deterministic for a given SM count.  Stream-K applies to the
- * polyphase path without split-K; elsewhere 1 acts as automatic.  A tuning and test
- * override with no counterpart on the pages.  Host only, same ordering rule as
- * ctr_plan_set_path; CTR_ERR_INVALID_ARG for other values or after ctr_prepack_weight.
- */
-ctr_status ctr_plan_set_stream_k(ctr_plan_t plan, int mode);
-
 /* The path the plan will run (a ctr_path other than AUTO), or -1 for a NULL plan. */
 int ctr_plan_get_path(ctr_plan_t plan);
 

@@ -120,44 +120,6 @@ def test_every_tile_width_bit_exact(dtype, block_n):
     np.testing.assert_array_equal(y, reference(x, w, b, (2, 2), (1, 1), (1, 0), dtype), err_msg=desc)
 
 
-@pytest.mark.parametrize("block_n", [64, 128, 256])
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_stream_k_bit_exact(dtype, block_n):
-    """The stream-K schedule: K slices of few tiles spread over every SM, so most tiles are
-    split over several CTAs (partials, finishing CTA adding them), with ragged tiles, 1-D and
-    2-D, and accumulation groups that straddle CTA ranges.  Shapes with fewer (tile, K
-    slice) units than SMs cannot use it and are skipped; each parameter set runs some."""
-    rng = np.random.default_rng(31 + block_n)
-    mag = 2 if dtype == "f32" else 1
-    cases = [((2, 512, 300), (512, 70, 8), 4, 2, 0), ((1, 256, 400), (256, 200, 4), 2, 1, 1),
-             ((2, 256, 30, 30), (256, 40, 4, 4), (2, 2), (1, 1), (1, 0))]
-    ran = 0
-    for xs, ws, s, p, op in cases:
-        x, w, b = _int_inputs(rng, xs, ws, ws[1], mag)
-        y, desc = run_plan(x, w, b, s, p, op, dtype, path=ctr.CTR_PATH_POLYPHASE,
-                           block_n=block_n, stream_k=1)
-        assert "BN %d," % block_n in desc, desc
-        np.testing.assert_array_equal(y, reference(x, w, b, s, p, op, dtype), err_msg=desc)
-        ran += "sched=stream-k" in desc
-    assert ran >= 1
-
-
-def test_stream_k_matches_tiles_on_random_inputs():
-    """Random fp32 inputs: stream-K and the one-tile-per-CTA schedule agree within the fp32
-    tolerance, and stream-K repeats bit for bit."""
-    rng = np.random.default_rng(37)
-    x = rng.standard_normal((1, 256, 300)).astype(np.float32)
-    w = rng.uniform(-0.05, 0.05, (256, 128, 16)).astype(np.float32)
-    b = rng.standard_normal(128).astype(np.float32)
-    y1, d1 = run_plan(x, w, b, 8, 4, 0, "f32", stream_k=1)
-    y2, _ = run_plan(x, w, b, 8, 4, 0, "f32", stream_k=1)
-    y0, d0 = run_plan(x, w, b, 8, 4, 0, "f32", stream_k=0)
-    assert "stream-k" in d1 and "stream-k" not in d0
-    np.testing.assert_array_equal(y1, y2)
-    ref = reference(x, w, b, 8, 4, 0, "f32")
-    assert oracle.rel_l2(y1, ref) <= TOL["f32"] and oracle.rel_l2(y0, ref) <= TOL["f32"]
-
-
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("path", sorted(PATHS))
 def test_random_within_tolerance(path, dtype):

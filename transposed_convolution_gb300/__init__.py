@@ -6,7 +6,7 @@ PyTorch fallback: if the library has not been built the first call raises Import
 any non-OK status from the library raises ``CtrError``.
 
 Low level (same names as the C ABI): ``ctr_plan_create``, ``ctr_plan_set_activation``,
-``ctr_plan_set_path``, ``ctr_plan_set_tile``, ``ctr_plan_set_stream_k``, ``ctr_plan_get_path``, ``ctr_plan_output_shape``,
+``ctr_plan_set_path``, ``ctr_plan_set_tile``, ``ctr_plan_get_path``, ``ctr_plan_output_shape``,
 ``ctr_packed_weight_bytes``, ``ctr_workspace_bytes``, ``ctr_plan_bind_workspace``,
 ``ctr_prepack_weight``, ``ctr_forward``, ``ctr_forward_noalloc``, ``ctr_plan_check``,
 ``ctr_plan_set_wait_limit_ns``,
@@ -52,7 +52,6 @@ SIGNATURES = {
     "ctr_plan_set_activation": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_float]),
     "ctr_plan_set_path": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int]),
     "ctr_plan_set_tile": (ctypes.c_int, [_vp, ctypes.c_int]),
-    "ctr_plan_set_stream_k": (ctypes.c_int, [_vp, ctypes.c_int]),
     "ctr_plan_get_path": (ctypes.c_int, [_vp]),
     "ctr_plan_output_shape": (ctypes.c_int, [_vp, _i64p]),
     "ctr_packed_weight_bytes": (ctypes.c_size_t, [_vp]),
@@ -152,10 +151,6 @@ def ctr_plan_set_path(plan, path, split_k=0):
 
 def ctr_plan_set_tile(plan, block_n):
     _check(lib.ctr_plan_set_tile(plan, int(block_n)), "ctr_plan_set_tile")
-
-
-def ctr_plan_set_stream_k(plan, mode):
-    _check(lib.ctr_plan_set_stream_k(plan, int(mode)), "ctr_plan_set_stream_k")
 
 
 def ctr_plan_get_path(plan) -> int:
@@ -258,7 +253,7 @@ class Plan:
 
     def __init__(self, N, C_in, C_out, in_spatial, kernel, stride=1, padding=0,
                  output_padding=0, dtype=None, negative_slope=None, path=CTR_PATH_AUTO,
-                 split_k=0, device=None, block_n=0, stream_k=-1):
+                 split_k=0, device=None, block_n=0):
         torch = _torch()
         self.ndim = len(in_spatial)
         self.dtype = dtype if dtype is not None else torch.float32
@@ -279,8 +274,6 @@ class Plan:
                 ctr_plan_set_path(self.handle, path, split_k)
             if block_n:
                 ctr_plan_set_tile(self.handle, block_n)
-            if stream_k != -1:
-                ctr_plan_set_stream_k(self.handle, stream_k)
             self.out_spatial = ctr_plan_output_shape(self.handle, self.ndim)
             self.path = ctr_plan_get_path(self.handle)
             self.packed_bytes = ctr_packed_weight_bytes(self.handle)

@@ -92,39 +92,12 @@ void choose_tiling(ctr_plan_s *pl) {
     const int kb_total = (int)(pl->K_total * op_esize(pl) / ctr::kBKBytes);
     const int64_t num_p = std::max<int64_t>(1, ceil_div(pl->N_total, ctr::kBM));
     double best = 1e300;
-    int best_bn = 128, best_sp = 1, best_sk = 0;
+    int best_bn = 128, best_sp = 1;
     // A forced split-K factor is clamped to the number of K slices.
     const int forced = pl->forced_split > 0 ? std::min(pl->forced_split, kb_total) : 0;
-    // Stream-K needs the fused polyphase output stage, one split and a unit per SM.  It is
-    // only used when forced: measured on GB300 it was slower on every workload here (CTAs
-    // at different K offsets of the same weight rows defeat L2 reuse of the weight, and the
-    // cooperative launch does not overlap the staging kernel), so the automatic choice is
-    // between one tile per CTA and split-K.
-    const bool sk_possible = pl->path == CTR_PATH_POLYPHASE && forced <= 1 && pl->forced_sk == 1;
     for (int bn : {64, 128, 256}) {
         if (pl->forced_bn > 0 && bn != pl->forced_bn) continue;
         const int64_t num_r = std::max<int64_t>(1, ceil_div(pl->M_rows, bn));
-        const int64_t tiles1 = num_p * num_r;
-        const bool sk_here = sk_possible && tiles1 * kb_total >= pl->num_sms;
-        if (sk_here) {
-            // All tiles' K slices shared evenly over the SMs: no idle SMs in the last wave;
-            // a tile split over CTAs costs one fp32 partial written (~20 B/clock) and read
-            // back by the finishing CTA (~50 B/clock).
-            const double per_slice = std::max(slice_clocks(prec, bn),
-                                              (ctr::kBM + bn) * (double)ctr::kBKBytes * op_planes(pl) / 50.0);
-            const double units = std::ceil((double)tiles1 * kb_total / pl->num_sms);
-            double t = units * per_slice + 2000.0 + 1500.0;
-            if (prec == Prec::TF32x3 && bn == 256) t += 800.0 * std::ceil(units / std::min(units, (double)group));
-            t += std::ceil((double)tiles1 / pl->num_sms) * ctr::kBM * (double)bn * esize_io(pl) / 20.0;
-            t += ctr::kBM * (double)bn * 4.0 * (1.0 / 20.0 + 1.0 / 50.0);
-            if (pl->forced_sk == 1 || t < best * 0.98) {
-                best = t;
-                best_bn = bn;
-                best_sp = 1;
-                best_sk = 1;
-            }
-        }
-        if (pl->forced_sk == 1 && sk_here) continue;   // forced, and feasible at this BN
         for (int sp = 1; sp <= 16; ++sp) {
             if (forced > 0 && sp != forced) continue;
             if (sp > kb_total) break;
@@ -149,13 +122,11 @@ void choose_tiling(ctr_plan_s *pl) {
                 best = t;
                 best_bn = bn;
                 best_sp = sp;
-                best_sk = 0;
             }
         }
     }
     pl->block_n = best_bn;
     pl->splits = best_sp;
-    pl->stream_k = best_sk;
     pl->kb_group = best_bn <= ctr::kMaxGroupedBN ? group : kNoGroup;
     pl->num_p_tiles = (int)num_p;
     pl->num_r_tiles = (int)std::max<int64_t>(1, ceil_div(pl->M_rows, best_bn));
@@ -167,8 +138,6 @@ void layout_plan(ctr_plan_s *pl) {
     pl->packed_bytes = 0;
     pl->ws_bytes_needed = 0;
     pl->ws_off_stage = pl->ws_stage_bytes = pl->ws_off_raw = pl->ws_raw_bytes = 0;
-    pl->ws_off_sk = pl->ws_sk_bytes = 0;
-    pl->stream_k = 0;
     pl->splits = 1;
     pl->block_n = 0;
     pl->num_tiles = 0;
@@ -208,13 +177,6 @@ void layout_plan(ctr_plan_s *pl) {
         pl->ws_off_raw = off;
         pl->ws_raw_bytes = (size_t)ctr::raw_split_stride_of(pl) * pl->splits * sizeof(float);
         off = align256(off + pl->ws_raw_bytes);
-    }
-    if (pl->stream_k) {
-        // One 128 x BN fp32 partial slot per CTA (one CTA per SM), then a counter per tile.
-        pl->ws_off_sk = off;
-        pl->ws_sk_bytes = align256((size_t)pl->num_sms * ctr::kBM * pl->block_n * sizeof(float)) +
-                          (size_t)pl->num_tiles * sizeof(int);
-        off = align256(off + pl->ws_sk_bytes);
     }
     pl->ws_bytes_needed = (pl->ws_stage_bytes || pl->ws_raw_bytes) ? off : 0;
 }
@@ -371,15 +333,6 @@ cudaError_t run_tc_path(const ctr_plan_s *pl, const void *x, const void *w_packe
     cudaError_t e;
     void *xs = ws + pl->ws_off_stage;
     float *raw = pl->ws_raw_bytes ? reinterpret_cast<float *>(ws + pl->ws_off_raw) : nullptr;
-    int *sk_count = nullptr;
-    if (pl->stream_k) {
-        // Stream-K tile counters start at zero on every call (before the staging kernel, so
-        // the staging -> GEMM programmatic launch is not interrupted).
-        sk_count = reinterpret_cast<int *>(
-            ws + pl->ws_off_sk + align256((size_t)pl->num_sms * kBM * pl->block_n * sizeof(float)));
-        if ((e = cudaMemsetAsync(sk_count, 0, (size_t)pl->num_tiles * sizeof(int), st)) != cudaSuccess)
-            return e;
-    }
     if ((e = launch_stage_x(pl, x, xs, st)) != cudaSuccess) return e;
 
     const bool bf16 = pl->dtype == CTR_BF16;
@@ -423,9 +376,6 @@ cudaError_t run_tc_path(const ctr_plan_s *pl, const void *x, const void *w_packe
     gp.raw_split_stride = raw_split_stride_of(pl);
     gp.status = status;
     gp.wait_limit_ns = pl->wait_limit_ns;
-    gp.stream_k = pl->stream_k;
-    gp.sk_partials = pl->stream_k ? reinterpret_cast<float *>(ws + pl->ws_off_sk) : nullptr;
-    gp.sk_count = sk_count;
     if (ev_before && (e = record_timing(ev_before, st)) != cudaSuccess) return e;
     if ((e = launch_gemm_tc(pl, maps, gp, st)) != cudaSuccess) return e;
     if (ev_after && (e = record_timing(ev_after, st)) != cudaSuccess) return e;
@@ -487,7 +437,6 @@ ctr_status ctr_plan_create(ctr_plan_t *out, int ndim, int64_t N, int64_t C_in, i
     pl->forced_path = CTR_PATH_AUTO;
     pl->forced_split = 0;
     pl->forced_bn = 0;
-    pl->forced_sk = -1;
     pl->wait_limit_ns = 4000000000ull;
     // Unit leading dimension for 1-D.
     pl->in[0] = 1; pl->k[0] = 1; pl->s[0] = 1; pl->p[0] = 0; pl->op[0] = 0;
@@ -550,14 +499,6 @@ ctr_status ctr_plan_set_path(ctr_plan_t pl, int path, int split_k) {
     return CTR_OK;
 }
 
-ctr_status ctr_plan_set_stream_k(ctr_plan_t pl, int mode) {
-    if (!pl || mode < -1 || mode > 1) return CTR_ERR_INVALID_ARG;
-    if (pl->prepared) return CTR_ERR_INVALID_ARG;
-    pl->forced_sk = mode;
-    layout_plan(pl);
-    return CTR_OK;
-}
-
 ctr_status ctr_plan_set_tile(ctr_plan_t pl, int block_n) {
     if (!pl || (block_n != 0 && block_n != 64 && block_n != 128 && block_n != 256))
         return CTR_ERR_INVALID_ARG;
@@ -610,12 +551,11 @@ ctr_status ctr_plan_describe(ctr_plan_t pl, char *buf, size_t len) {
         const EpiParams ep = make_epi(pl, nullptr, nullptr);
         snprintf(buf, len,
                  "path=%s prec=%s rows=%lld(pad %lld, BN %d, %d tiles) positions=%lld(%d tiles) "
-                 "K=%lld splits=%d sched=%s group=%d tiles=%lld sms=%d S=%d/%d taps=%lldx%lld "
+                 "K=%lld splits=%d group=%d tiles=%lld sms=%d S=%d/%d taps=%lldx%lld "
                  "pitch=%lldx%lld epi=%d/%dB packed=%zu ws=%zu",
                  pname, pl->dtype == CTR_BF16 ? "bf16" : "3xtf32", (long long)pl->M_rows,
                  (long long)pl->M_pad, pl->block_n, pl->num_r_tiles, (long long)pl->N_total,
                  pl->num_p_tiles, (long long)pl->K_total, pl->splits,
-                 pl->stream_k ? "stream-k" : "tiles",
                  pl->kb_group == kNoGroup ? 0 : pl->kb_group, (long long)pl->num_tiles,
                  pl->num_sms, pl->S, pl->S_pad, (long long)pl->m[0], (long long)pl->m[1],
                  (long long)pl->P[0], (long long)pl->P[1], ep.kind, ep.store_bytes,

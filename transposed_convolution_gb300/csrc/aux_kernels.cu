@@ -487,7 +487,7 @@ cudaError_t launch_stage_x(const ctr_plan_s *pl, const void *x, void *xs, cudaSt
     cudaError_t e;
 #define CTR_STAGE(B, V)                                                                   \
     if ((e = prefer_max_smem<stage_x_kernel<B, V>>()) != cudaSuccess) return e;          \
-    e = launch_pdl(stage_x_kernel<B, V>, grid, dim3(kStageThreads), 0, st, false, x, xs, sg, su)
+    e = launch_pdl(stage_x_kernel<B, V>, grid, dim3(kStageThreads), 0, st, x, xs, sg, su)
     if (sg.bf16) {
         if (vec) { CTR_STAGE(true, true); } else { CTR_STAGE(true, false); }
     } else {
@@ -508,7 +508,7 @@ cudaError_t launch_splitk_reduce(const ctr_plan_s *pl, const float *raw, const E
     if (n_rows == 0 || r_chunks == 0) return cudaSuccess;
     cudaError_t e = prefer_max_smem<splitk_reduce_kernel>();
     if (e != cudaSuccess) return e;
-    e = launch_pdl(splitk_reduce_kernel, dim3(grid_for(total, 64)), dim3(64), 0, st, false, raw, ep,
+    e = launch_pdl(splitk_reduce_kernel, dim3(grid_for(total, 64)), dim3(64), 0, st, raw, ep,
                    raw_ld, split_stride, pl->splits, n_rows, n_pad, r_chunks);
     if (e != cudaSuccess) return e;
     count_launches(1);
@@ -523,7 +523,7 @@ cudaError_t launch_col2im(const ctr_plan_s *pl, const float *col, int64_t col_ld
     const int64_t split_stride = raw_split_stride_of(pl);
     cudaError_t e = prefer_max_smem<col2im_kernel>();
     if (e != cudaSuccess) return e;
-    e = launch_pdl(col2im_kernel, dim3(grid_for(total, kBlock)), dim3(kBlock), 0, st, false, col,
+    e = launch_pdl(col2im_kernel, dim3(grid_for(total, kBlock)), dim3(kBlock), 0, st, col,
                    col_ld, split_stride, pl->splits, pl->S_pad, bias, y, g, total);
     if (e != cudaSuccess) return e;
     count_launches(1);

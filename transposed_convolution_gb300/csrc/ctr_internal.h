@@ -67,13 +67,6 @@ struct GemmParams {
     int64_t raw_split_stride;
     uint32_t *status;   // device status word (bit flags of bounded waits that gave up)
     uint64_t wait_limit_ns;
-    // Stream-K (stream_k = 1): the num_tiles x kb_total (tile, K slice) units are split into
-    // gridDim.x contiguous ranges, one per CTA.  A tile whose K slices span several CTAs is
-    // finished by the CTA holding its first slice; the others write fp32 partials to their
-    // slot sk_partials[blockIdx.x][128][BN] and count themselves in sk_count[tile].
-    int stream_k;
-    float *sk_partials;
-    int *sk_count;
 };
 
 // Status-word bits set by device code.
@@ -81,7 +74,6 @@ constexpr uint32_t kStatusTimeoutProducer = 1u << 0;
 constexpr uint32_t kStatusTimeoutMma = 1u << 1;
 constexpr uint32_t kStatusTimeoutEpilogue = 1u << 2;
 constexpr uint32_t kStatusTimeoutDrain = 1u << 3;
-constexpr uint32_t kStatusTimeoutStreamK = 1u << 4;
 
 }  // namespace ctr
 
@@ -97,7 +89,6 @@ struct ctr_plan_s {
     int forced_path;
     int forced_split;
     int forced_bn;      // 0 = automatic phase-row tile
-    int forced_sk;      // -1 = automatic, 0 = off, 1 = stream-K
     int prepared;       // ctr_prepack_weight ran (status word allocated)
     int num_sms;
 
@@ -116,7 +107,6 @@ struct ctr_plan_s {
     int num_p_tiles;    // tiles of 128 staged positions
     int num_r_tiles;    // tiles of block_n packed weight rows
     int64_t num_tiles;
-    int stream_k;       // 1: stream-K schedule over num_sms CTAs (see GemmParams)
 
     size_t packed_bytes;
     size_t ws_bytes_needed;
@@ -124,8 +114,6 @@ struct ctr_plan_s {
     size_t ws_stage_bytes;
     size_t ws_off_raw;     // split-K partials or the col2im column buffer
     size_t ws_raw_bytes;
-    size_t ws_off_sk;      // stream-K partial slots, then the per-tile counters
-    size_t ws_sk_bytes;
     void *ws;
     size_t ws_bytes;
 
@@ -141,23 +129,19 @@ namespace ctr {
 // previous kernel of the stream is still running, so it must call ptx::griddep_wait() before
 // its first global memory access; its launch and prologue then overlap the previous
 // kernel's tail instead of following its completion.
-// With cooperative = true the launch also guarantees that all CTAs are resident at once
-// (needed where CTAs wait on one another), or fails.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                       cudaStream_t st, bool cooperative, Args &&...args) {
+                       cudaStream_t st, Args &&...args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeCooperative;
-    attr[1].val.cooperative = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = cooperative ? 2 : 1;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
 }
 

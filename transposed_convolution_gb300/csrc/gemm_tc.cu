@@ -103,78 +103,6 @@ __device__ __forceinline__ TileCoord decode_tile(uint32_t t, const GemmParams &g
     return c;
 }
 
-// A CTA's work items.  Data-parallel and split-K plans: tiles blockIdx.x, blockIdx.x +
-// gridDim.x, ...  Stream-K plans: the segments (tile, K slices [kb0, kb1)) of the CTA's
-// contiguous range of the num_tiles * kb_total units.  Ranges run tile-major in ascending K,
-// so a CTA's only segment that does not start at K slice 0 is its first one, and a tile's
-// first slices belong to the lowest-numbered CTA that holds any of them.
-enum WorkKind : int {
-    WORK_WHOLE = 0,    // all of the tile's K slices: fused output stage
-    WORK_PARTIAL = 1,  // later K slices of a tile: fp32 partial to this CTA's slot
-    WORK_FINISH = 2,   // first K slices: add the later CTAs' partials, then the output stage
-};
-
-struct Work {
-    TileCoord tc;
-    int tile;
-    int kind;
-    int ncontrib;      // WORK_FINISH: CTAs after this one holding the tile's later slices
-};
-
-struct WorkIter {
-    int64_t t;         // data-parallel: next tile
-    int64_t u, u1;     // stream-K: next unit, end of this CTA's range
-};
-
-__device__ __forceinline__ int64_t sk_range_begin(int64_t cta, const GemmParams &gp) {
-    return cta * (gp.num_tiles * (int64_t)gp.kb_total) / gridDim.x;
-}
-
-__device__ __forceinline__ WorkIter work_begin(const GemmParams &gp) {
-    WorkIter it;
-    it.t = blockIdx.x;
-    it.u = it.u1 = 0;
-    if (gp.stream_k) {
-        it.u = sk_range_begin(blockIdx.x, gp);
-        it.u1 = sk_range_begin(blockIdx.x + 1, gp);
-    }
-    return it;
-}
-
-__device__ __forceinline__ bool work_next(WorkIter &it, const GemmParams &gp, int bn, Work &w) {
-    if (!gp.stream_k) {
-        if (it.t >= gp.num_tiles) return false;
-        w.tc = decode_tile((uint32_t)it.t, gp, bn);
-        w.tile = (int)it.t;
-        w.kind = WORK_WHOLE;
-        w.ncontrib = 0;
-        it.t += gridDim.x;
-        return true;
-    }
-    if (it.u >= it.u1) return false;
-    const int64_t KB = gp.kb_total;
-    const int64_t t = it.u / KB;
-    const int64_t k0 = it.u - t * KB;
-    const int64_t k1 = k0 + (it.u1 - it.u) < KB ? k0 + (it.u1 - it.u) : KB;
-    w.tc = decode_tile((uint32_t)t, gp, bn);   // one split: K slices 0 .. KB
-    w.tc.kb0 = (int)k0;
-    w.tc.kb1 = (int)k1;
-    w.tile = (int)t;
-    w.ncontrib = 0;
-    if (k0 > 0) {
-        w.kind = WORK_PARTIAL;
-    } else if (k1 == KB) {
-        w.kind = WORK_WHOLE;
-    } else {
-        w.kind = WORK_FINISH;
-        const int64_t end = (t + 1) * KB;
-        for (int64_t c = blockIdx.x + 1; c < gridDim.x && sk_range_begin(c, gp) < end; ++c)
-            ++w.ncontrib;
-    }
-    it.u += k1 - k0;
-    return true;
-}
-
 __device__ __forceinline__ void give_up(volatile int *abort, uint32_t *status, uint32_t bit) {
     *abort = 1;
     atomicOr(status, bit);
@@ -251,10 +179,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             int64_t issued = 0;
-            WorkIter it = work_begin(gp);
-            Work wk;
-            while (!*abort && work_next(it, gp, BN, wk)) {
-                const TileCoord &tc = wk.tc;
+            for (int64_t t = blockIdx.x; t < gp.num_tiles && !*abort; t += gridDim.x) {
+                const TileCoord tc = decode_tile((uint32_t)t, gp, BN);
                 // Tap (uy, ux) and channel slice kc of K slice kb, stepped along with kb.
                 const int g0 = tc.kb0 / gp.kb_per_tap;
                 int kc = tc.kb0 - g0 * gp.kb_per_tap;
@@ -306,10 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             int grp = 0;  // accumulation groups issued by this CTA (selects the TMEM buffer)
             bool ok = true;
-            WorkIter it = work_begin(gp);
-            Work wk;
-            while (ok && !*abort && work_next(it, gp, BN, wk)) {
-                const TileCoord &tc = wk.tc;
+            for (int64_t t = blockIdx.x; ok && t < gp.num_tiles && !*abort; t += gridDim.x) {
+                const TileCoord tc = decode_tile((uint32_t)t, gp, BN);
                 for (int kb = tc.kb0; ok && kb < tc.kb1; ++grp) {
                     const int kb_end = min(kb + gp.kb_group, tc.kb1);
                     const int acc = grp % C::kAccBufs;
@@ -392,66 +316,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&tmem_empty[g % C::kAccBufs]);
         };
-        // Stream-K: wait (bounded, lane 0 for the warp) until `need` warp signals are counted
-        // for `tile`, then make the partials they published visible to this warp.
-        auto sk_wait = [&](int tile, int need) -> bool {
-            int okw = 1;
-            if (lane == 0) {
-                const volatile int *cnt = gp.sk_count + tile;
-                if (*cnt < need) {
-                    if (limit == 0) {
-                        okw = 0;
-                    } else {
-                        const uint64_t t0 = ptx::globaltimer_ns();
-                        while (*cnt < need) {
-                            if (*abort || ptx::globaltimer_ns() - t0 > limit) {
-                                okw = 0;
-                                break;
-                            }
-                            __nanosleep(256);
-                        }
-                    }
-                    if (!okw && !*abort) give_up(abort, gp.status, kStatusTimeoutStreamK);
-                }
-            }
-            okw = __shfl_sync(0xffffffffu, okw, 0);
-            __syncwarp();
-            __threadfence();
-            return okw != 0;
-        };
         // Output of one 32-column chunk of this thread's position.
-        auto store_chunk = [&](const Work &wk, const PosInfo &ps, int c, const float (&v)[32]) {
-            const TileCoord &tc = wk.tc;
+        auto store_chunk = [&](const TileCoord &tc, const PosInfo &ps, int c, const float (&v)[32]) {
             const int64_t r0 = tc.r0 + 32 * c;
             if (fused) {
-                const int64_t pl = 32 * quad + lane;   // position within the tile
-                if (wk.kind == WORK_PARTIAL) {
-                    float4 *dst = reinterpret_cast<float4 *>(
-                        gp.sk_partials + ((int64_t)blockIdx.x * kBM + pl) * BN + 32 * c);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-                    return;
-                }
-                float t2[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) t2[i] = v[i];
-                if (wk.kind == WORK_FINISH) {
-                    // The later K slices' partials, added in ascending K order (fixed).
-                    for (int j = 1; j <= wk.ncontrib; ++j) {
-                        const float4 *src = reinterpret_cast<const float4 *>(
-                            gp.sk_partials + ((int64_t)(blockIdx.x + j) * kBM + pl) * BN + 32 * c);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float4 a = __ldcg(src + i);
-                            t2[4 * i] += a.x;
-                            t2[4 * i + 1] += a.y;
-                            t2[4 * i + 2] += a.z;
-                            t2[4 * i + 3] += a.w;
-                        }
-                    }
-                }
-                emit_cols(t2, ps, r0, gp.epi, lane);
+                emit_cols(v, ps, r0, gp.epi, lane);
                 return;
             }
             const int64_t pos = (int64_t)tc.p0 + 32 * quad + lane;
@@ -469,11 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_ld_32x32b_x32(tmem_base + lane_addr + C::kSumCol + 32u * c, u);
         };
         bool ok = true;
-        WorkIter it = work_begin(gp);
-        Work wk;
-        while (ok && work_next(it, gp, BN, wk)) {
-            const TileCoord &tc = wk.tc;
-            if (wk.kind == WORK_FINISH && !(ok = sk_wait(wk.tile, kEpiWarps * wk.ncontrib))) break;
+        for (int64_t t = blockIdx.x; ok && t < gp.num_tiles; t += gridDim.x) {
+            const TileCoord tc = decode_tile((uint32_t)t, gp, BN);
             const int ngroups = (tc.kb1 - tc.kb0 + gp.kb_group - 1) / gp.kb_group;
             PosInfo ps{};
             if (fused) ps = decode_pos(tc.p0 + 32 * quad + lane, gp.epi);
@@ -515,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float v[32];
 #pragma unroll
                     for (int cc = 0; cc < 32; ++cc) v[cc] = __uint_as_float(u[cc]);
-                    store_chunk(wk, ps, c_base + c, v);
+                    store_chunk(tc, ps, c_base + c, v);
                 }
             } else if (P != Prec::TF32x3 || ngroups == 1) {
                 // One accumulation group: straight from TMEM to the output stage.
@@ -529,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float v[32];
 #pragma unroll
                     for (int cc = 0; cc < 32; ++cc) v[cc] = __uint_as_float(u[cc]);
-                    store_chunk(wk, ps, c_base + c, v);
+                    store_chunk(tc, ps, c_base + c, v);
                 }
                 ++grp;
             } else if constexpr (P == Prec::TF32x3 && !C::kTmemSum) {
@@ -555,13 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 // Unrolled (kChunks <= 2 here), so each chunk's sums die once stored.
 #pragma unroll
-                for (int c = 0; c < kChunks; ++c) store_chunk(wk, ps, c_base + c, sum[c]);
-            }
-            if (ok && wk.kind == WORK_PARTIAL) {
-                // Publish this warp's share of the partial: its stores, then one count.
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) atomicAdd(gp.sk_count + wk.tile, 1);
+                for (int c = 0; c < kChunks; ++c) store_chunk(tc, ps, c_base + c, sum[c]);
             }
         }
     }
@@ -588,11 +448,9 @@ cudaError_t launch_inst(const ctr_plan_s *pl, const CUtensorMap *maps, const Gem
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    const int64_t grid = gp.stream_k ? pl->num_sms : std::min<int64_t>(gp.num_tiles, pl->num_sms);
-    // Stream-K CTAs wait on one another: one CTA per SM, all resident (cooperative launch).
+    const int64_t grid = std::min<int64_t>(gp.num_tiles, pl->num_sms);
     const cudaError_t e = launch_pdl(gemm_tc_kernel<P, BN>, dim3((unsigned)grid), dim3(kThreads),
-                                     (size_t)C::kSmem, st, gp.stream_k != 0, maps[0], maps[1],
-                                     maps[2], maps[3], gp);
+                                     (size_t)C::kSmem, st, maps[0], maps[1], maps[2], maps[3], gp);
     if (e != cudaSuccess) return e;
     count_launches(1);
     return cudaGetLastError();
