@@ -189,16 +189,16 @@ struct StageGeo {
 //          position and writes it; eight consecutive threads cover a 128-byte staged row.
 // The tile is XOR-swizzled by 4-float groups, column group g of channel c stored at
 // g ^ ((c / kOutVec) & 7), so both the float4 writes and the scalar reads of a warp hit 32
-// different banks.  Tiles start at input x = x_first + 128 t with x_first a multiple of 8
-// at or before -hx, so the left halo is covered; staged positions outside [0, Px) are
-// skipped and those outside the input are written as zeros.
+// different banks.  Tiles start at input x = 128 t (aligned for the 16-byte loads) and cover
+// the input row; the first tile of a staged row also writes the zeros of the left halo
+// (staged positions 0 .. hx-1) and the last one those past the tiles (up to Px).
 constexpr int kStageThreads = 256;
 constexpr int kStageTP = 128;
 
 struct StageUnits {
     int64_t cchunks;   // C_in_pad / kStageC
     int64_t xtiles;    // tiles of 128 positions per staged row
-    int64_t x_first;   // input x of the first tile of a row
+    int64_t x_first;   // input x of the first tile of a row (0)
     int64_t tiles;     // rows * xtiles * cchunks
 };
 
@@ -303,6 +303,23 @@ __global__ void __launch_bounds__(kStageThreads) stage_x_kernel(const void *__re
                     make_float4(lo[0], lo[1], lo[2], lo[3]);
             }
         }
+        // Zeros of the staged positions no tile covers: the left halo (first tile of the
+        // row) and the positions past the last tile (last tile of the row).
+        auto zero_cols = [&](int64_t px_begin, int64_t px_end) {
+            constexpr int kVecs = kStageC / kOutVec;
+            const int64_t n_items = (px_end - px_begin) * kVecs;
+            for (int64_t i = threadIdx.x; i < n_items; i += kStageThreads) {
+                const int64_t px = px_begin + i / kVecs;
+                const int64_t o = (row * sg.Px + px) * sg.C_in_pad + c_base + (i % kVecs) * kOutVec;
+                *reinterpret_cast<uint4 *>(static_cast<T *>(xs) + o) = make_uint4(0u, 0u, 0u, 0u);
+                if constexpr (!BF16)
+                    *reinterpret_cast<uint4 *>(static_cast<float *>(xs) + lo_off + o) =
+                        make_uint4(0u, 0u, 0u, 0u);
+            }
+        };
+        if (xt == 0) zero_cols(0, sg.hx < sg.Px ? sg.hx : sg.Px);
+        if (xt == su.xtiles - 1 && sg.hx + kStageTP * su.xtiles < sg.Px)
+            zero_cols(sg.hx + kStageTP * su.xtiles, sg.Px);
         __syncthreads();   // the tile is reused by the next iteration
     }
 }
@@ -478,8 +495,8 @@ cudaError_t launch_stage_x(const ctr_plan_s *pl, const void *x, void *xs, cudaSt
     if (sg.N_total == 0) return cudaSuccess;
     StageUnits su;
     su.cchunks = sg.C_in_pad / (sg.bf16 ? 64 : 32);
-    su.x_first = -round_up(sg.hx, 8);
-    su.xtiles = ceil_div(sg.Px - sg.hx - su.x_first, kStageTP);
+    su.x_first = 0;
+    su.xtiles = std::max<int64_t>(1, ceil_div(sg.W, kStageTP));
     su.tiles = sg.B * sg.Py * su.xtiles * su.cchunks;
     const int64_t blocks = std::min<int64_t>(su.tiles, (int64_t)pl->num_sms * 8);
     const bool vec = (sg.W * (sg.bf16 ? 2 : 4)) % 16 == 0;
