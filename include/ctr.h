@@ -127,6 +127,27 @@ ctr_status ctr_plan_set_path(ctr_plan_t plan, int path, int split_k);
  */
 ctr_status ctr_plan_set_tile(ctr_plan_t plan, int block_n);
 
+/*
+ * Chain two plans so that `plan`'s output feeds `next`'s input without a staging pass, as
+ * in a decoder's stack of upsampling layers (two ConvTransposes with an activation between:
+ * "[XNNPACK] Lower dense transposed convs as one polyphase conv + depth to space", Test
+ * plan).  Afterwards:
+ *   - ctr_forward(plan, x, w, bias, y = NULL, stream) writes its output, with bias and
+ *     activation applied and rounded to the I/O type, straight into the channels-last
+ *     staged-input layout inside next's workspace (fp32: as tf32 hi and lo planes, exactly
+ *     what next's staging would have made of the torch-layout output), and no y;
+ *   - ctr_forward(next, x = NULL, ...) reads it from there instead of staging an x.
+ * Results are bit-identical to the unchained calls.  Requirements (CTR_ERR_INVALID_ARG
+ * otherwise): both plans on a tensor-core path (polyphase or col2im), the same dtype and
+ * batch, next's C_in equal to plan's C_out and next's input spatial size equal to plan's
+ * output size.  At each forward, next's workspace must be bound (CTR_ERR_NO_WORKSPACE)
+ * and must not overlap plan's (CTR_ERR_INVALID_ARG); the first forward after binding
+ * zeroes next's staged buffer once (its halos stay zero).  Run plan, then next, on the
+ * same stream.  ctr_plan_chain(plan, NULL) unchains; destroying either plan unchains
+ * both.  Host only; no counterpart of the call itself on the pages.
+ */
+ctr_status ctr_plan_chain(ctr_plan_t plan, ctr_plan_t next);
+
 /* The path the plan will run (a ctr_path other than AUTO), or -1 for a NULL plan. */
 int ctr_plan_get_path(ctr_plan_t plan);
 
@@ -165,7 +186,8 @@ ctr_status ctr_prepack_weight(ctr_plan_t plan, const void *w, void *w_packed, vo
  *   y         device output, [N][C_out][out spatial...], written in full
  *   stream    cudaStream_t as void*
  * Asynchronous; launch failures return CTR_ERR_CUDA.  Device-side errors (a bounded wait
- * that gave up) are reported by ctr_plan_check.  x and y must not overlap.
+ * that gave up) are reported by ctr_plan_check.  x and y must not overlap.  For a chained
+ * plan (ctr_plan_chain) y must be NULL; for the plan it feeds, x may be NULL.
  */
 ctr_status ctr_forward(ctr_plan_t plan, const void *x, const void *w_packed, const void *bias,
                        void *y, void *stream);

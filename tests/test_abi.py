@@ -140,3 +140,29 @@ def test_null_plan_queries(ctr):
 
 def test_no_kernel_launched_by_host_calls(ctr):
     assert ctr.ctr_launch_count() == 0
+
+
+def test_chain_validation_without_gpu(ctr):
+    """ctr_plan_chain: compatible plans chain and unchain; mismatched channels, sizes, dtype
+    or path are rejected; destroying either side unchains the other."""
+    bf = ctr.CTR_BF16
+    a = _plan(ctr, 1, 1, 64, 32, [100], [4], [2], [1], [0], bf)      # out 200 x 32 ch
+    b = _plan(ctr, 1, 1, 32, 64, [200], [4], [2], [1], [0], bf)      # in 200 x 32 ch
+    c = _plan(ctr, 1, 1, 16, 64, [200], [4], [2], [1], [0], bf)      # wrong channels
+    d = _plan(ctr, 1, 1, 32, 64, [201], [4], [2], [1], [0], bf)      # wrong length
+    e = _plan(ctr, 1, 1, 32, 64, [200], [4], [2], [1], [0], ctr.CTR_F32)
+    try:
+        ctr.ctr_plan_chain(a, b)
+        for bad in (c, d, e):
+            assert ctr.lib.ctr_plan_chain(a, bad) == ctr.CTR_ERR_INVALID_ARG
+        assert ctr.lib.ctr_plan_chain(a, a) == ctr.CTR_ERR_INVALID_ARG
+        # a chained producer writes no y; without workspaces nothing runs
+        st = ctr.lib.ctr_forward(a, ctypes.c_void_p(256), ctypes.c_void_p(256), None,
+                                 ctypes.c_void_p(256), None)
+        assert st in (ctr.CTR_ERR_NOT_PREPARED, ctr.CTR_ERR_INVALID_ARG)
+        ctr.ctr_plan_chain(a, None)
+        ctr.ctr_plan_chain(a, b)
+    finally:
+        ctr.ctr_plan_destroy(b)          # unchains a
+        for h in (a, c, d, e):
+            ctr.ctr_plan_destroy(h)

@@ -1,0 +1,100 @@
+"""Chained plans (ctr_plan_chain): a plan's output stage writes straight into the next plan's
+staged input, and the next plan runs without staging.  The chained results must equal the
+unchained calls bit for bit (the staged values are the same: bf16 rounding, or the tf32
+hi/lo split of the fp32 output), on repeated calls too (the staged halos stay zero)."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import tdtype
+
+import transposed_convolution_gb300 as ctr
+
+pytestmark = pytest.mark.gpu
+
+# Each chain: dtype, batch, input channels and spatial size, then per layer
+# (C_out, kernel, stride, padding, output_padding, LeakyReLU slope or None).
+CHAINS = [
+    ("bf16", 1, 64, (300,), [(64, 16, 8, 4, 0, 0.1), (32, 16, 8, 4, 0, 0.1)]),       # S8 -> S8
+    ("bf16", 2, 48, (256,), [(40, 4, 2, 1, 0, 0.1), (40, 4, 2, 1, 1, None)]),        # S2, padded C_in
+    ("f32", 1, 64, (200,), [(48, 8, 4, 2, 0, 0.2), (64, 4, 2, 1, 0, None)]),         # S4 -> S2
+    ("f32", 2, 32, (20, 17), [(40, (4, 4), (2, 2), (1, 1), (0, 1), 0.1),
+                              (32, (4, 4), (2, 2), (1, 1), (0, 0), None)]),          # 2-D
+    ("bf16", 1, 32, (100,), [(64, 4, 2, 1, 0, 0.1), (32, 3, 2, 1, 1, None)]),        # col2im next
+    ("bf16", 1, 128, (128,), [(64, 16, 8, 4, 0, 0.1), (64, 4, 2, 1, 0, 0.1),
+                              (32, 4, 2, 1, 0, None)]),                              # three plans
+]
+
+
+def _make(dtype, B, C_in, sp, layers, rng):
+    plans, ws, bs = [], [], []
+    c, s = C_in, tuple(sp)
+    for (co, k, st, p, op, slope) in layers:
+        pl = ctr.Plan(B, c, co, s, k if isinstance(k, tuple) else (k,) * len(s), st, p, op,
+                      dtype=tdtype(dtype), negative_slope=slope)
+        w = torch.from_numpy(rng.uniform(-0.2, 0.2, (c, co) + tuple(pl.kernel)).astype(np.float32))
+        b = torch.from_numpy(rng.standard_normal(co).astype(np.float32))
+        w, b = w.cuda().to(tdtype(dtype)), b.cuda().to(tdtype(dtype))
+        pl.prepack(w)
+        plans.append(pl)
+        ws.append(w)
+        bs.append(b)
+        c, s = co, pl.out_spatial
+    return plans, bs
+
+
+@pytest.mark.parametrize("case", CHAINS, ids=lambda c: "%s-%dd-%dlayers" % (c[0], len(c[3]), len(c[4])))
+def test_chained_equals_unchained(case):
+    dtype, B, C_in, sp, layers = case
+    rng = np.random.default_rng(41)
+    plans, bs = _make(dtype, B, C_in, sp, layers, rng)
+    try:
+        x = torch.from_numpy(rng.standard_normal((B, C_in) + tuple(sp)).astype(np.float32))
+        x = x.cuda().to(tdtype(dtype))
+        # Unchained: every layer through the torch layout.
+        h = x
+        for pl, b in zip(plans, bs):
+            h = pl.forward(h, b)
+        ref = h.float().cpu().numpy()
+        assert plans[0].path == ctr.CTR_PATH_POLYPHASE
+        # Chained: only the first layer stages an input, only the last writes a y.
+        for a, nxt in zip(plans[:-1], plans[1:]):
+            a.chain(nxt)
+        for it in range(2):
+            y = torch.full(plans[-1].out_shape, float("nan"), dtype=tdtype(dtype), device="cuda")
+            assert plans[0].forward(x, bs[0]) is None
+            for pl, b in zip(plans[1:-1], bs[1:-1]):
+                assert pl.forward(None, b) is None
+            plans[-1].forward(None, bs[-1], y=y)
+            torch.cuda.synchronize()
+            for pl in plans:
+                pl.check()
+            np.testing.assert_array_equal(y.float().cpu().numpy(), ref, err_msg="call %d" % it)
+    finally:
+        for pl in plans:
+            pl.close()
+
+
+def test_chain_errors_on_device():
+    """A chained producer refuses a y; a plan fed by a chain still accepts an explicit x."""
+    rng = np.random.default_rng(43)
+    plans, bs = _make("bf16", 1, 64, (128,), [(64, 4, 2, 1, 0, None), (32, 4, 2, 1, 0, None)], rng)
+    try:
+        plans[0].chain(plans[1])
+        x = torch.randn(1, 64, 128, device="cuda").to(torch.bfloat16)
+        with pytest.raises(ValueError):
+            plans[0].forward(x, bs[0], y=torch.empty(plans[0].out_shape, dtype=torch.bfloat16,
+                                                   device="cuda"))
+        st = ctr.lib.ctr_forward(plans[0].handle, x.data_ptr(), plans[0].w_packed.data_ptr(),
+                                 None, x.data_ptr(), None)
+        assert st == ctr.CTR_ERR_INVALID_ARG
+        # plans[1] with its own x: staged normally, same as unchained
+        x1 = torch.randn((1, 64) + plans[0].out_spatial, device="cuda").to(torch.bfloat16)
+        y_a = plans[1].forward(x1, bs[1])
+        plans[0].chain(None)
+        y_b = plans[1].forward(x1, bs[1])
+        torch.cuda.synchronize()
+        assert torch.equal(y_a, y_b)
+    finally:
+        for pl in plans:
+            pl.close()

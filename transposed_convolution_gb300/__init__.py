@@ -6,7 +6,7 @@ PyTorch fallback: if the library has not been built the first call raises Import
 any non-OK status from the library raises ``CtrError``.
 
 Low level (same names as the C ABI): ``ctr_plan_create``, ``ctr_plan_set_activation``,
-``ctr_plan_set_path``, ``ctr_plan_set_tile``, ``ctr_plan_get_path``, ``ctr_plan_output_shape``,
+``ctr_plan_set_path``, ``ctr_plan_set_tile``, ``ctr_plan_chain``, ``ctr_plan_get_path``, ``ctr_plan_output_shape``,
 ``ctr_packed_weight_bytes``, ``ctr_workspace_bytes``, ``ctr_plan_bind_workspace``,
 ``ctr_prepack_weight``, ``ctr_forward``, ``ctr_forward_noalloc``, ``ctr_plan_check``,
 ``ctr_plan_set_wait_limit_ns``,
@@ -52,6 +52,7 @@ SIGNATURES = {
     "ctr_plan_set_activation": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_float]),
     "ctr_plan_set_path": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int]),
     "ctr_plan_set_tile": (ctypes.c_int, [_vp, ctypes.c_int]),
+    "ctr_plan_chain": (ctypes.c_int, [_vp, _vp]),
     "ctr_plan_get_path": (ctypes.c_int, [_vp]),
     "ctr_plan_output_shape": (ctypes.c_int, [_vp, _i64p]),
     "ctr_packed_weight_bytes": (ctypes.c_size_t, [_vp]),
@@ -151,6 +152,10 @@ def ctr_plan_set_path(plan, path, split_k=0):
 
 def ctr_plan_set_tile(plan, block_n):
     _check(lib.ctr_plan_set_tile(plan, int(block_n)), "ctr_plan_set_tile")
+
+
+def ctr_plan_chain(plan, next_plan):
+    _check(lib.ctr_plan_chain(plan, next_plan), "ctr_plan_chain")
 
 
 def ctr_plan_get_path(plan) -> int:
@@ -288,6 +293,8 @@ class Plan:
             self.handle = None
             raise
         self.w_packed = None
+        self.next_plan = None     # chained: this plan's output feeds next_plan's input
+        self.prev_plan = None
 
     @property
     def out_shape(self):
@@ -305,14 +312,29 @@ class Plan:
         ctr_prepack_weight(self.handle, _ptr(w), _ptr(self.w_packed), _stream_ptr(stream))
         return self.w_packed
 
+    def chain(self, next_plan):
+        """Feed this plan's output straight into next_plan's staged input (ctr_plan_chain):
+        afterwards forward() writes no y and returns None, and next_plan.forward(None, ...)
+        takes its input from there.  chain(None) unchains."""
+        ctr_plan_chain(self.handle, next_plan.handle if next_plan is not None else None)
+        if self.next_plan is not None:
+            self.next_plan.prev_plan = None
+        self.next_plan = next_plan
+        if next_plan is not None:
+            next_plan.prev_plan = self
+
     def forward(self, x, bias=None, y=None, stream=None):
         torch = _torch()
         if self.w_packed is None:
             raise RuntimeError("Plan.forward before Plan.prepack")
-        x = self._checked(x, (self.N, self.C_in) + self.in_spatial, "x")
+        if x is not None or self.prev_plan is None:
+            x = self._checked(x, (self.N, self.C_in) + self.in_spatial, "x")
         if bias is not None:
             bias = self._checked(bias, (self.C_out,), "bias")
-        if y is None:
+        if self.next_plan is not None:
+            if y is not None:
+                raise ValueError("a chained plan writes no y")
+        elif y is None:
             y = torch.empty(self.out_shape, dtype=self.dtype, device=self.device)
         else:
             y = self._checked(y, self.out_shape, "y")
@@ -339,8 +361,14 @@ class Plan:
 
     def close(self):
         if getattr(self, "handle", None):
-            ctr_plan_destroy(self.handle)
+            ctr_plan_destroy(self.handle)     # also unchains on the library side
             self.handle = None
+        nxt, prv = getattr(self, "next_plan", None), getattr(self, "prev_plan", None)
+        if nxt is not None:
+            nxt.prev_plan = None
+        if prv is not None:
+            prv.next_plan = None
+        self.next_plan = self.prev_plan = None
 
     def __del__(self):
         try:

@@ -138,6 +138,7 @@ void layout_plan(ctr_plan_s *pl) {
     pl->packed_bytes = 0;
     pl->ws_bytes_needed = 0;
     pl->ws_off_stage = pl->ws_stage_bytes = pl->ws_off_raw = pl->ws_raw_bytes = 0;
+    pl->chain_zeroed_ws = nullptr;   // the staged layout may change
     pl->splits = 1;
     pl->block_n = 0;
     pl->num_tiles = 0;
@@ -179,6 +180,14 @@ void layout_plan(ctr_plan_s *pl) {
         off = align256(off + pl->ws_raw_bytes);
     }
     pl->ws_bytes_needed = (pl->ws_stage_bytes || pl->ws_raw_bytes) ? off : 0;
+}
+
+// Whether pl's output can feed nx's staged input directly (see ctr_plan_chain).
+bool chain_compatible(const ctr_plan_s *pl, const ctr_plan_s *nx) {
+    return pl->path == CTR_PATH_POLYPHASE &&
+           (nx->path == CTR_PATH_POLYPHASE || nx->path == CTR_PATH_COL2IM) &&
+           pl->dtype == nx->dtype && pl->B == nx->B && pl->ndim == nx->ndim &&
+           nx->C_in == pl->C_out && nx->in[0] == pl->out[0] && nx->in[1] == pl->out[1];
 }
 
 // The tensor-core kernels index tiles, staged positions (with the largest tap shift) and
@@ -294,6 +303,8 @@ EpiParams make_epi(const ctr_plan_s *pl, const void *bias, void *y) {
     // position (sx elements), the padding offset and the output row pitch must all be
     // multiples of it, so every thread and row share the same alignment.
     const int es = pl->dtype == CTR_BF16 ? 2 : 4;
+    e.out_staged = 0;
+    e.ys_Px = e.ys_Py = e.ys_hx = e.ys_hy = e.ys_cpad = e.ys_lo = 0;
     e.store_bytes = es;
     for (int w : {16, 8, 4}) {
         if (nx > 0 && (nx * es) % w == 0 && (sx * es) % w == 0 && (pl->p[1] * es) % w == 0 &&
@@ -329,11 +340,12 @@ cudaError_t record_timing(cudaEvent_t ev, cudaStream_t st) {
 
 cudaError_t run_tc_path(const ctr_plan_s *pl, const void *x, const void *w_packed,
                         const void *bias, void *y, char *ws, uint32_t *status,
-                        cudaEvent_t ev_before, cudaEvent_t ev_after, cudaStream_t st) {
+                        cudaEvent_t ev_before, cudaEvent_t ev_after, cudaStream_t st,
+                        const ctr_plan_s *chained_to, bool staged_in) {
     cudaError_t e;
     void *xs = ws + pl->ws_off_stage;
     float *raw = pl->ws_raw_bytes ? reinterpret_cast<float *>(ws + pl->ws_off_raw) : nullptr;
-    if ((e = launch_stage_x(pl, x, xs, st)) != cudaSuccess) return e;
+    if (!staged_in && (e = launch_stage_x(pl, x, xs, st)) != cudaSuccess) return e;
 
     const bool bf16 = pl->dtype == CTR_BF16;
     const int es = bf16 ? 2 : 4;
@@ -371,6 +383,18 @@ cudaError_t run_tc_path(const ctr_plan_s *pl, const void *x, const void *w_packe
     const bool fused = pl->path == CTR_PATH_POLYPHASE && pl->splits == 1;
     gp.epi_mode = fused ? EPI_POLYPHASE : EPI_RAW;
     gp.epi = make_epi(pl, bias, y);
+    if (chained_to) {
+        // Output into the next plan's staged input (its staging geometry).
+        const ctr_plan_s *nx = chained_to;
+        gp.epi.out_staged = 1;
+        gp.epi.y = static_cast<char *>(nx->ws) + nx->ws_off_stage;
+        gp.epi.ys_Py = nx->P[0];
+        gp.epi.ys_Px = nx->P[1];
+        gp.epi.ys_hy = nx->m[0] - 1;
+        gp.epi.ys_hx = nx->m[1] - 1;
+        gp.epi.ys_cpad = nx->C_in_pad;
+        gp.epi.ys_lo = nx->N_total * nx->C_in_pad;
+    }
     gp.raw = raw;
     gp.raw_ld = raw_ld_of(pl);
     gp.raw_split_stride = raw_split_stride_of(pl);
@@ -437,6 +461,8 @@ ctr_status ctr_plan_create(ctr_plan_t *out, int ndim, int64_t N, int64_t C_in, i
     pl->forced_path = CTR_PATH_AUTO;
     pl->forced_split = 0;
     pl->forced_bn = 0;
+    pl->chain_next = pl->chain_prev = nullptr;
+    pl->chain_zeroed_ws = nullptr;
     pl->wait_limit_ns = 4000000000ull;
     // Unit leading dimension for 1-D.
     pl->in[0] = 1; pl->k[0] = 1; pl->s[0] = 1; pl->p[0] = 0; pl->op[0] = 0;
@@ -590,13 +616,23 @@ ctr_status ctr_forward(ctr_plan_t pl, const void *x, const void *w_packed, const
                        void *y, void *stream) {
     if (!pl) return CTR_ERR_INVALID_ARG;
     if (!pl->prepared) return CTR_ERR_NOT_PREPARED;
-    if (!w_packed || !y || (!x && pl->B * pl->C_in * pl->in[0] * pl->in[1] > 0))
+    ctr_plan_s *nx = pl->chain_next;
+    const bool staged_in = !x && pl->chain_prev != nullptr;  // input staged by the previous plan
+    if (!w_packed || (nx ? y != nullptr : y == nullptr)) return CTR_ERR_INVALID_ARG;
+    if (!x && !staged_in && pl->B * pl->C_in * pl->in[0] * pl->in[1] > 0)
         return CTR_ERR_INVALID_ARG;
-    if ((x && !aligned16(x)) || !aligned16(w_packed) || !aligned16(y) ||
+    if ((x && !aligned16(x)) || !aligned16(w_packed) || (y && !aligned16(y)) ||
         (bias && !aligned16(bias)))
         return CTR_ERR_MISALIGNED;
     if (pl->ws_bytes_needed > 0 && (!pl->ws || pl->ws_bytes < pl->ws_bytes_needed))
         return CTR_ERR_NO_WORKSPACE;
+    if (nx) {
+        if (!chain_compatible(pl, nx)) return CTR_ERR_INVALID_ARG;
+        if (!nx->ws || nx->ws_bytes < nx->ws_bytes_needed) return CTR_ERR_NO_WORKSPACE;
+        const uintptr_t a0 = reinterpret_cast<uintptr_t>(pl->ws), a1 = a0 + pl->ws_bytes;
+        const uintptr_t b0 = reinterpret_cast<uintptr_t>(nx->ws), b1 = b0 + nx->ws_bytes;
+        if (a0 < b1 && b0 < a1) return CTR_ERR_INVALID_ARG;
+    }
     if (pl->B == 0) return CTR_OK;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
@@ -610,10 +646,34 @@ ctr_status ctr_forward(ctr_plan_t pl, const void *x, const void *w_packed, const
     if (pl->N_total == 0) {  // empty input on the col2im path: y = bias or zeros
         return ctr::launch_fill_bias(pl, bias, y, st) == cudaSuccess ? CTR_OK : CTR_ERR_CUDA;
     }
-
+    if (nx && nx->chain_zeroed_ws != nx->ws) {
+        // The producer writes only inside the input; the halos and padded channels of the
+        // next plan's staged buffer must be zero (once per bound workspace).
+        if (cudaMemsetAsync(static_cast<char *>(nx->ws) + nx->ws_off_stage, 0, nx->ws_stage_bytes,
+                            st) != cudaSuccess)
+            return CTR_ERR_CUDA;
+        nx->chain_zeroed_ws = nx->ws;
+    }
     const cudaError_t e = ctr::run_tc_path(pl, x, w_packed, bias, y, static_cast<char *>(pl->ws),
-                                           pl->d_status, pl->ev_before, pl->ev_after, st);
+                                           pl->d_status, pl->ev_before, pl->ev_after, st, nx,
+                                           staged_in);
     return e == cudaSuccess ? CTR_OK : CTR_ERR_CUDA;
+}
+
+ctr_status ctr_plan_chain(ctr_plan_t pl, ctr_plan_t nx) {
+    if (!pl) return CTR_ERR_INVALID_ARG;
+    if (!nx) {
+        if (pl->chain_next) pl->chain_next->chain_prev = nullptr;
+        pl->chain_next = nullptr;
+        return CTR_OK;
+    }
+    if (nx == pl || !chain_compatible(pl, nx)) return CTR_ERR_INVALID_ARG;
+    if (nx->chain_prev && nx->chain_prev != pl) return CTR_ERR_INVALID_ARG;
+    if (pl->chain_next && pl->chain_next != nx) pl->chain_next->chain_prev = nullptr;
+    pl->chain_next = nx;
+    nx->chain_prev = pl;
+    nx->chain_zeroed_ws = nullptr;
+    return CTR_OK;
 }
 
 ctr_status ctr_plan_check(ctr_plan_t pl, void *stream) {
@@ -633,6 +693,8 @@ ctr_status ctr_plan_check(ctr_plan_t pl, void *stream) {
 
 void ctr_plan_destroy(ctr_plan_t pl) {
     if (!pl) return;
+    if (pl->chain_next) pl->chain_next->chain_prev = nullptr;
+    if (pl->chain_prev) pl->chain_prev->chain_next = nullptr;
     if (pl->d_status) {
         int cur = 0;
         cudaGetDevice(&cur);

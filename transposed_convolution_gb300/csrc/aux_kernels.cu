@@ -379,7 +379,7 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ raw, EpiParams ep
         }
     }
     // decode_pos marks positions at or past n_rows (= B * Py * Px) invalid.
-    emit_cols(v, decode_pos(n, ep), r0, ep, (int)(threadIdx.x & 31));
+    emit_cols<true>(v, decode_pos(n, ep), r0, ep, (int)(threadIdx.x & 31));
 }
 
 // -------------------------------------------------------------------------- col2im

@@ -46,6 +46,11 @@ struct EpiParams {
     float slope;
     int kind;           // EpiKind
     int store_bytes;    // width of the aligned vector stores of interior runs (16, 8, 4, 2)
+    // Chained output (out_staged = 1): y is the next plan's staged input, channels-last rows
+    // of ys_cpad channels, output (oy, ox) of batch b at row (b*ys_Py + oy + ys_hy)*ys_Px +
+    // ox + ys_hx; fp32 as tf32 hi and lo planes, ys_lo elements apart.
+    int out_staged;
+    int64_t ys_Px, ys_Py, ys_hx, ys_hy, ys_cpad, ys_lo;
 };
 
 // The tensor-core GEMM D[n, r] = sum_k Xs[n + shift(k), k] * A[r, k]: n runs over staged
@@ -117,6 +122,10 @@ struct ctr_plan_s {
     void *ws;
     size_t ws_bytes;
 
+    // Chaining (ctr_plan_chain): this plan's output feeds chain_next's staged input.
+    ctr_plan_s *chain_next;
+    ctr_plan_s *chain_prev;
+    void *chain_zeroed_ws;  // workspace whose staged buffer was zeroed for chained input
     uint32_t *d_status;
     int status_device;
     uint64_t wait_limit_ns;
@@ -183,10 +192,13 @@ bool encode_2d(CUtensorMap *map, const void *base, bool bf16, uint64_t inner, ui
 // Output mapping of a tensor-core plan (api.cu).
 EpiParams make_epi(const ctr_plan_s *pl, const void *bias, void *y);
 
-// Staging, GEMM and reduce/col2im of a tensor-core plan with explicit scratch (api.cu).
+// Staging (skipped when staged_in: a chained producer already wrote the staged input), GEMM
+// and reduce/col2im of a tensor-core plan with explicit scratch (api.cu).  With chained_to
+// set, the output goes to that plan's staged input instead of y.
 cudaError_t run_tc_path(const ctr_plan_s *pl, const void *x, const void *w_packed,
                         const void *bias, void *y, char *ws, uint32_t *status,
-                        cudaEvent_t ev_before, cudaEvent_t ev_after, cudaStream_t st);
+                        cudaEvent_t ev_before, cudaEvent_t ev_after, cudaStream_t st,
+                        const ctr_plan_s *chained_to = nullptr, bool staged_in = false);
 
 // Counter of launched kernels (monotonic, process-wide).
 void count_launches(uint64_t n);

@@ -18,6 +18,7 @@
 #include <cuda_bf16.h>
 
 #include "ctr_internal.h"
+#include "ptx.cuh"
 
 namespace ctr {
 
@@ -226,11 +227,133 @@ __device__ __forceinline__ void emit_generic(const float (&v)[32], const PosInfo
     }
 }
 
+// ------------------------------------------------------------ chained output
+// The same outputs written into the next plan's staged input (EpiParams::out_staged):
+// channels-last, so the G channels of one output position are G consecutive elements.
+// fp32 values are split into tf32 hi and lo planes exactly as the staging kernel does.
+
+// Row of the staged buffer holding output (b, oy, ox).
+__device__ __forceinline__ int64_t staged_row(const EpiParams &e, int64_t b, int64_t oy,
+                                              int64_t ox) {
+    return (b * e.ys_Py + oy + e.ys_hy) * e.ys_Px + ox + e.ys_hx;
+}
+
+// N consecutive channel values at dst (N * sizeof(T)-aligned): one plane for bf16, the hi
+// and lo planes for fp32.
+template <typename T, int N>
+__device__ __forceinline__ void store_channels(T *dst, const float *vals, const EpiParams &e) {
+    constexpr int kBytes = N * (int)sizeof(T) < 16 ? N * (int)sizeof(T) : 16;
+    if constexpr (sizeof(T) == 2) {
+        store_run<T, N>(dst, vals, kBytes);
+    } else {
+        float hi[N], lo[N];
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            hi[i] = ptx::to_tf32(vals[i]);
+            lo[i] = ptx::to_tf32(vals[i] - hi[i]);
+        }
+        store_run<T, N>(dst, hi, kBytes);
+        store_run<T, N>(dst + e.ys_lo, lo, kBytes);
+    }
+}
+
+template <typename T, int SX, int SY>
+__device__ __forceinline__ void emit_small_chain(const float (&v)[32], const PosInfo &ps,
+                                                 int64_t r0, const EpiParams &e, int lane) {
+    constexpr int S = SX * SY;
+    constexpr int G = 32 / S;
+    const int64_t oc0 = r0 / S;
+    const float bl = lane_bias(e, oc0, G, lane);
+    const float slope_eff = slope_of(e);
+    const bool use_min = slope_eff > 1.0f;
+    const int64_t g_left = e.C_out - oc0;
+    const int gmax = g_left < G ? (int)g_left : G;
+    // Bias and activation in place (every lane takes part in the shuffles).
+    float t[32];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const float bias = __shfl_sync(0xffffffffu, bl, g);
+#pragma unroll
+        for (int j = 0; j < S; ++j) t[g * S + j] = leaky(v[g * S + j] + bias, slope_eff, use_min);
+    }
+    if (!ps.valid) return;
+    T *__restrict__ ys = static_cast<T *>(e.y);
+#pragma unroll
+    for (int jy = 0; jy < SY; ++jy) {
+        const int64_t oy = (int64_t)SY * ps.qy + jy - e.py;
+        if (oy < 0 || oy >= e.Hout) continue;
+#pragma unroll
+        for (int jx = 0; jx < SX; ++jx) {
+            const int64_t ox = (int64_t)SX * ps.qx + jx - e.px;
+            if (ox < 0 || ox >= e.Wout) continue;
+            T *dst = ys + staged_row(e, ps.b, oy, ox) * e.ys_cpad + oc0;
+            float c[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) c[g] = t[g * S + jy * SX + jx];
+            if (gmax == G) {
+                store_channels<T, G>(dst, c, e);
+            } else {
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+                    if (g < gmax) store_channels<T, 1>(dst + g, &c[g], e);
+            }
+        }
+    }
+}
+
+// Any plan, element by element.
+__device__ __forceinline__ void emit_generic_chain(const float (&v)[32], const PosInfo &ps,
+                                                   int64_t r0, const EpiParams &e) {
+    if (!ps.valid) return;
+    const float slope_eff = slope_of(e);
+    const bool use_min = slope_eff > 1.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const uint32_t r = (uint32_t)r0 + i;
+        const uint32_t oc = r / (uint32_t)e.S_pad;
+        const int j = (int)(r - oc * (uint32_t)e.S_pad);
+        if (oc >= e.C_out || j >= e.S) continue;
+        const int jy = j / e.sx, jx = j - (j / e.sx) * e.sx;
+        const int64_t oy = (int64_t)e.sy * ps.qy + jy - e.py;
+        const int64_t ox = (int64_t)e.sx * ps.qx + jx - e.px;
+        if (oy < 0 || oy >= e.Hout || ox < 0 || ox >= e.Wout) continue;
+        const float bias = e.bias ? load_io(e.bias, oc, e.out_bf16) : 0.0f;
+        const float val = leaky(v[i] + bias, slope_eff, use_min);
+        const int64_t o = staged_row(e, ps.b, oy, ox) * e.ys_cpad + oc;
+        if (e.out_bf16) {
+            store_channels<__nv_bfloat16, 1>(static_cast<__nv_bfloat16 *>(e.y) + o, &val, e);
+        } else {
+            store_channels<float, 1>(static_cast<float *>(e.y) + o, &val, e);
+        }
+    }
+}
+
 // Output stage for the accumulator columns r0 .. r0+31 (r0 a multiple of 32) of one phase
 // position per lane: v[i] = D[n, r0 + i].  Warp-collective: all 32 lanes of the warp call
-// it together with the same r0, each with its own position.
+// it together with the same r0, each with its own position.  kChain compiles in the chained
+// output (EpiParams::out_staged); kernels without it keep their register budget.
+template <bool kChain>
 __device__ __forceinline__ void emit_cols(const float (&v)[32], const PosInfo &ps, int64_t r0,
                                           const EpiParams &e, int lane) {
+    if (kChain && e.out_staged) {
+#define CTR_CHAIN(SX, SY)                                                  \
+    if (e.out_bf16)                                                        \
+        emit_small_chain<__nv_bfloat16, SX, SY>(v, ps, r0, e, lane);       \
+    else                                                                   \
+        emit_small_chain<float, SX, SY>(v, ps, r0, e, lane);               \
+    return
+        switch (e.kind) {
+            case EPI_KIND_1D_S1: CTR_CHAIN(1, 1);
+            case EPI_KIND_1D_S2: CTR_CHAIN(2, 1);
+            case EPI_KIND_1D_S4: CTR_CHAIN(4, 1);
+            case EPI_KIND_1D_S8: CTR_CHAIN(8, 1);
+            case EPI_KIND_2D_S2x2: CTR_CHAIN(2, 2);
+            default:
+                emit_generic_chain(v, ps, r0, e);
+                return;
+        }
+#undef CTR_CHAIN
+    }
 #define CTR_SMALL(SX, SY)                                                  \
     if (e.out_bf16)                                                        \
         emit_small<__nv_bfloat16, SX, SY>(v, ps, r0, e, lane);             \

@@ -1,461 +1,19 @@
-// gemm_tc.cu -- the hot kernel: a persistent, warp-specialised implicit GEMM on the 5th-
-// generation tensor cores (tcgen05 + TMEM), fed by TMA.
-//
-//   D[n, r] = sum over taps g and input channels ic of Xs[n + shift(g), ic] * A[r, g*C_in_pad + ic]
-//
-// For the polyphase path ("[XNNPACK] Lower dense transposed convs as one polyphase conv +
-// depth to space", Summary) A is the phase-major prepacked weight, Xs the input staged
-// channels-last with m - 1 zero positions on each side, and shift(g) = uy*Px + ux the tap
-// offset, so that the m (or mH*mW) taps of the stride-1 phase convolution are m shifted TMA
-// boxes of the same staged input: the zero halo is the convolution's padding m - 1.  For
-// the col2im path ("[WebGPU] optimizations for audio models", ConvTranspose commit) there
-// is one tap and D is the column buffer X[M, C_in] x W[C_in, k*C_out], transposed.
-//
-// The MMA's M dimension is the phase position n (128 per tile: TMEM lanes) and its N
-// dimension the packed weight row r (BN = 64, 128 or 256 per tile: TMEM columns), so each
-// epilogue thread owns one output position and writes its phases as contiguous runs.
-//
-// Warp roles (320 threads, one CTA per SM, persistent over output tiles):
-//   warp 0      one lane issues TMA loads of Xs and A K-slices into a ring of stages;
-//   warp 1      allocates TMEM; one lane issues tcgen05.mma into one of several TMEM
-//               accumulators (128 lanes x BN fp32 columns) and commits to mbarriers;
-//   warps 2..9  the epilogue: tcgen05.ld of the accumulator, then either the fused polyphase
-//               output stage (bias, activation, interleave, slice; epilogue.cuh) or a raw
-//               fp32 store of D (split-K partials, col2im columns).  A warp may read only
-//               the TMEM lane quarter (warp id mod 4); two warps share each quarter, one
-//               taking the first BN/2 columns and the other the rest.
-// Several accumulators let the epilogue of tile i overlap the MMAs of tile i + 1.
-//
-// 3xTF32 (fp32 I/O): both operands come as tf32 hi and lo planes (x = hi + lo, each
-// rounded to tf32) and every K step issues lo*hi + hi*lo + hi*hi into the same fp32
-// accumulator -- the split of Ootomo and Yokota, "Recovering single precision accuracy from
-// Tensor Cores while surpassing the FP32 theoretical peak performance" (IJHPCA 2022).
-//
-// Every mbarrier wait is bounded (wait_limit_ns of global time).  A wait that gives up sets
-// a bit in the plan's status word and a CTA-wide abort flag; every role then stops, the
-// producer waits for the TMA loads it issued, the MMA warp waits for its MMAs, and TMEM is
-// freed before the CTA exits.
-#include <algorithm>
-
-#include "ctr_internal.h"
-#include "epilogue.cuh"
-#include "ptx.cuh"
+// gemm_tc.cu -- instantiations of the tensor-core GEMM (gemm_tc.cuh) that write the torch
+// layout, and the launch dispatch over precision, tile width and output.
+#include "gemm_tc.cuh"
 
 namespace ctr {
+
+// gemm_tc_chain.cu: the instantiations whose output feeds the next plan's staged input.
+cudaError_t launch_gemm_tc_chain(const ctr_plan_s *pl, const CUtensorMap *maps,
+                                 const GemmParams &gp, cudaStream_t st);
+
 namespace {
-
-constexpr int kThreads = 320;
-constexpr int kEpiWarps = 8;
-constexpr int kSmemMax = 227 * 1024;
-constexpr uint64_t kDrainLimitNs = 2000000000ull;
-
 template <Prec P, int BN>
-struct Cfg {
-    static constexpr int kPlanes = P == Prec::TF32x3 ? 2 : 1;
-    static constexpr int kSlice = gemm_slice_bytes(P, BN);  // K bytes per row per stage
-    static constexpr int kElems = kSlice / (P == Prec::TF32x3 ? 4 : 2);
-    static constexpr int kKSteps = kSlice / 32;              // MMA K steps of 32 bytes
-    static constexpr int kXBytes = kBM * kSlice;             // one 128-position Xs slice
-    static constexpr int kWBytes = BN * kSlice;              // one BN-row weight slice
-    static constexpr int kStageBytes = kPlanes * (kXBytes + kWBytes);
-    static constexpr int kBarBytes = 256;
-    static constexpr int kStagesRaw = (kSmemMax - 1024 - kBarBytes) / kStageBytes;
-    static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
-    static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes;
-    // Grouped 3xTF32 accumulation keeps its running sums in a TMEM region of BN columns
-    // beside the accumulators for BN >= 128 (in registers they would not fit the 168 a
-    // thread has with 10 warps per SM), in registers for BN = 64.
-    static constexpr bool kTmemSum = P == Prec::TF32x3 && BN >= 128;
-    // TMEM accumulators: as many BN-column buffers as fit 512 columns (less the sum region),
-    // at most 4, so the MMA can run several tiles ahead of the epilogue.
-    static constexpr int kAccBufs = kTmemSum ? (512 - BN) / BN : (512 / BN > 4 ? 4 : 512 / BN);
-    static constexpr uint32_t kSumCol = kAccBufs * BN;       // first column of the sum region
-    static constexpr uint32_t kTmemCols = kAccBufs * BN + (kTmemSum ? BN : 0);
-    static constexpr uint32_t kIdesc =
-        ptx::idesc_f32acc(P == Prec::TF32x3 ? ptx::kFmtTF32 : ptx::kFmtBF16, kBM, BN);
-    static_assert(kStages >= 2, "at least two pipeline stages");
-    static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512,
-                  "TMEM allocation is a power of two");
-    static_assert(kAccBufs >= 1, "at least one accumulator");
-};
-
-struct TileCoord {
-    int p0, r0;
-    int z, kb0, kb1;
-};
-
-// Tile t -> (row tile fastest, then position tile, then split).  32-bit arithmetic: the host
-// keeps tiles, positions and rows below 2^31 (64-bit divisions are long software sequences
-// and every role decodes every tile).
-__device__ __forceinline__ TileCoord decode_tile(uint32_t t, const GemmParams &gp, int bn) {
-    TileCoord c;
-    const uint32_t nr = (uint32_t)gp.num_r_tiles, np = (uint32_t)gp.num_p_tiles;
-    const uint32_t rest = t / nr;
-    const uint32_t r_tile = t - rest * nr;
-    const uint32_t z = rest / np;
-    const uint32_t p_tile = rest - z * np;
-    c.z = (int)z;
-    c.r0 = (int)(r_tile * (uint32_t)bn);
-    c.p0 = (int)(p_tile * (uint32_t)kBM);
-    const uint32_t kbt = (uint32_t)gp.kb_total, sp = (uint32_t)gp.splits;
-    c.kb0 = (int)(z * kbt / sp);
-    c.kb1 = (int)((z + 1) * kbt / sp);
-    return c;
+cudaError_t launch_bn(const ctr_plan_s *pl, const CUtensorMap *maps, const GemmParams &gp,
+                      cudaStream_t st) {
+    return launch_inst<P, BN, false>(pl, maps, gp, st);
 }
-
-__device__ __forceinline__ void give_up(volatile int *abort, uint32_t *status, uint32_t bit) {
-    *abort = 1;
-    atomicOr(status, bit);
-}
-
-template <Prec P, int BN>
-__global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapW,
-                   const __grid_constant__ CUtensorMap mapX2,
-                   const __grid_constant__ CUtensorMap mapW2, const GemmParams gp) {
-    using C = Cfg<P, BN>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t *stage_base = smem;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kStages * C::kStageBytes);
-    uint64_t *full = bars;
-    uint64_t *empty = bars + C::kStages;
-    uint64_t *tmem_full = bars + 2 * C::kStages;
-    uint64_t *tmem_empty = tmem_full + C::kAccBufs;
-    uint64_t *drain = tmem_empty + C::kAccBufs;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
-    volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-
-    auto x_slice = [&](int s, int plane) -> uint8_t * {
-        return stage_base + s * C::kStageBytes + plane * C::kXBytes;
-    };
-    auto w_slice = [&](int s, int plane) -> uint8_t * {
-        return stage_base + s * C::kStageBytes + C::kPlanes * C::kXBytes + plane * C::kWBytes;
-    };
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
-            ptx::mbar_init(&full[s], 1);
-            ptx::mbar_init(&empty[s], 1);
-        }
-        for (int a = 0; a < C::kAccBufs; ++a) {
-            ptx::mbar_init(&tmem_full[a], 1);
-            ptx::mbar_init(&tmem_empty[a], kEpiWarps);
-        }
-        ptx::mbar_init(drain, 1);
-        *abort = 0;
-        ptx::fence_mbar_init();
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    }
-    if (warp == 0 && lane == 0) {
-        ptx::tma_prefetch_desc(&mapX);
-        ptx::tma_prefetch_desc(&mapW);
-        if (P == Prec::TF32x3) {
-            ptx::tma_prefetch_desc(&mapX2);
-            ptx::tma_prefetch_desc(&mapW2);
-        }
-    }
-    if (warp == 1) {
-        ptx::tmem_alloc(tmem_slot, C::kTmemCols);
-        ptx::tmem_relinquish();
-    }
-    ptx::tc_fence_before();
-    __syncthreads();
-    ptx::tc_fence_after();
-    // Everything above touched only shared memory, TMEM and the kernel parameters, so it may
-    // overlap the previous kernel of the stream; global memory waits for it.
-    ptx::griddep_wait();
-    ptx::griddep_launch_dependents();
-    const uint32_t tmem_base = *tmem_slot;
-    const uint64_t limit = gp.wait_limit_ns;
-
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            int64_t issued = 0;
-            for (int64_t t = blockIdx.x; t < gp.num_tiles && !*abort; t += gridDim.x) {
-                const TileCoord tc = decode_tile((uint32_t)t, gp, BN);
-                // Tap (uy, ux) and channel slice kc of K slice kb, stepped along with kb.
-                const int g0 = tc.kb0 / gp.kb_per_tap;
-                int kc = tc.kb0 - g0 * gp.kb_per_tap;
-                int uy = g0 / gp.mx;
-                int ux = g0 - uy * gp.mx;
-                for (int kb = tc.kb0; kb < tc.kb1; ++kb) {
-                    if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, limit, abort)) {
-                        if (!*abort) give_up(abort, gp.status, kStatusTimeoutProducer);
-                        break;
-                    }
-                    ptx::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-                    const int32_t x_k = kc * C::kElems;
-                    const int32_t w_k = kb * C::kElems;
-                    const int32_t x_row = (int32_t)(tc.p0 + (int64_t)uy * gp.Px + ux);
-                    const int32_t w_row = (int32_t)tc.r0;
-                    ptx::tma_load_2d(x_slice(stage, 0), &mapX, &full[stage], x_k, x_row);
-                    ptx::tma_load_2d(w_slice(stage, 0), &mapW, &full[stage], w_k, w_row);
-                    if (P == Prec::TF32x3) {
-                        ptx::tma_load_2d(x_slice(stage, 1), &mapX2, &full[stage], x_k, x_row);
-                        ptx::tma_load_2d(w_slice(stage, 1), &mapW2, &full[stage], w_k, w_row);
-                    }
-                    ++issued;
-                    if (++kc == gp.kb_per_tap) {
-                        kc = 0;
-                        if (++ux == gp.mx) {
-                            ux = 0;
-                            ++uy;
-                        }
-                    }
-                    if (++stage == C::kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-            // Wait for the latest load into every stage, so no copy lands after exit.
-            const int64_t pending = issued < C::kStages ? issued : C::kStages;
-            for (int64_t s = 0; s < pending; ++s) {
-                const int64_t idx = issued - 1 - s;
-                if (!ptx::mbar_wait(&full[idx % C::kStages], (uint32_t)((idx / C::kStages) & 1),
-                                    kDrainLimitNs, nullptr))
-                    atomicOr(gp.status, kStatusTimeoutDrain);
-            }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            int grp = 0;  // accumulation groups issued by this CTA (selects the TMEM buffer)
-            bool ok = true;
-            for (int64_t t = blockIdx.x; ok && t < gp.num_tiles && !*abort; t += gridDim.x) {
-                const TileCoord tc = decode_tile((uint32_t)t, gp, BN);
-                for (int kb = tc.kb0; ok && kb < tc.kb1; ++grp) {
-                    const int kb_end = min(kb + gp.kb_group, tc.kb1);
-                    const int acc = grp % C::kAccBufs;
-                    const uint32_t acc_phase = (uint32_t)(grp / C::kAccBufs) & 1u;
-                    if (!ptx::mbar_wait(&tmem_empty[acc], acc_phase ^ 1u, limit, abort)) {
-                        if (!*abort) give_up(abort, gp.status, kStatusTimeoutMma);
-                        ok = false;
-                        break;
-                    }
-                    ptx::tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                    uint32_t accumulate = 0;
-                    for (; kb < kb_end; ++kb) {
-                        if (!ptx::mbar_wait(&full[stage], phase, limit, abort)) {
-                            if (!*abort) give_up(abort, gp.status, kStatusTimeoutMma);
-                            ok = false;
-                            break;
-                        }
-                        ptx::tc_fence_after();
-                        const uint64_t xd = ptx::sdesc_k<C::kSlice>(ptx::smem_u32(x_slice(stage, 0)));
-                        const uint64_t wd = ptx::sdesc_k<C::kSlice>(ptx::smem_u32(w_slice(stage, 0)));
-                        uint64_t xdl = 0, wdl = 0;
-                        if (P == Prec::TF32x3) {
-                            xdl = ptx::sdesc_k<C::kSlice>(ptx::smem_u32(x_slice(stage, 1)));
-                            wdl = ptx::sdesc_k<C::kSlice>(ptx::smem_u32(w_slice(stage, 1)));
-                        }
-#pragma unroll
-                        for (int k = 0; k < C::kKSteps; ++k) {  // 32-byte K steps of the slice
-                            // +2 in the descriptor's start-address field = +32 bytes
-                            const uint64_t dk = (uint64_t)(2 * k);
-                            if (P == Prec::TF32x3) {
-                                ptx::mma_tf32(d_tmem, xdl + dk, wd + dk, C::kIdesc, accumulate);
-                                ptx::mma_tf32(d_tmem, xd + dk, wdl + dk, C::kIdesc, 1u);
-                                ptx::mma_tf32(d_tmem, xd + dk, wd + dk, C::kIdesc, 1u);
-                            } else {
-                                ptx::mma_f16(d_tmem, xd + dk, wd + dk, C::kIdesc, accumulate);
-                            }
-                            accumulate = 1u;
-                        }
-                        ptx::mma_commit(&empty[stage]);  // frees the stage once these MMAs finish
-                        if (++stage == C::kStages) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
-                    }
-                    if (ok) ptx::mma_commit(&tmem_full[acc]);
-                }
-            }
-            // Every MMA issued above completes before TMEM is freed.
-            ptx::mma_commit(drain);
-            if (!ptx::mbar_wait(drain, 0, kDrainLimitNs, nullptr))
-                atomicOr(gp.status, kStatusTimeoutDrain);
-        }
-    } else {
-        // ------------------------------------------------------------ epilogue
-        const int quad = warp & 3;               // TMEM lanes 32*quad .. 32*quad + 31
-        constexpr int kChunks = BN / 64;         // 32-column chunks per warp
-        const int c_base = ((warp - 2) >> 2) * kChunks;  // this warp's first chunk
-        const bool fused = gp.epi_mode == EPI_POLYPHASE;
-        const uint32_t lane_addr = (uint32_t)(32 * quad) << 16;
-        int grp = 0;
-        // Bounded wait of lane 0 on (bar, parity), uniform across the warp.
-        auto warp_wait = [&](uint64_t *bar, uint32_t parity) -> bool {
-            int ok = 1;
-            if (lane == 0) {
-                ok = ptx::mbar_wait(bar, parity, limit, abort) ? 1 : 0;
-                if (!ok && !*abort) give_up(abort, gp.status, kStatusTimeoutEpilogue);
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            __syncwarp();
-            return ok != 0;
-        };
-        auto wait_group = [&](int g) -> bool {
-            const bool ok = warp_wait(&tmem_full[g % C::kAccBufs], (uint32_t)(g / C::kAccBufs) & 1u);
-            if (ok) ptx::tc_fence_after();
-            return ok;
-        };
-        auto release_group = [&](int g) {
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&tmem_empty[g % C::kAccBufs]);
-        };
-        // Output of one 32-column chunk of this thread's position.
-        auto store_chunk = [&](const TileCoord &tc, const PosInfo &ps, int c, const float (&v)[32]) {
-            const int64_t r0 = tc.r0 + 32 * c;
-            if (fused) {
-                emit_cols(v, ps, r0, gp.epi, lane);
-                return;
-            }
-            const int64_t pos = (int64_t)tc.p0 + 32 * quad + lane;
-            float4 *dst = reinterpret_cast<float4 *>(gp.raw + (int64_t)tc.z * gp.raw_split_stride +
-                                                     pos * gp.raw_ld + r0);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-        };
-        auto tmem_chunk = [&](int g, int c, uint32_t (&u)[32]) {
-            ptx::tmem_ld_32x32b_x32(
-                tmem_base + lane_addr + (uint32_t)((g % C::kAccBufs) * BN + 32 * c), u);
-        };
-        auto sum_chunk_ld = [&](int c, uint32_t (&u)[32]) {
-            ptx::tmem_ld_32x32b_x32(tmem_base + lane_addr + C::kSumCol + 32u * c, u);
-        };
-        bool ok = true;
-        for (int64_t t = blockIdx.x; ok && t < gp.num_tiles; t += gridDim.x) {
-            const TileCoord tc = decode_tile((uint32_t)t, gp, BN);
-            const int ngroups = (tc.kb1 - tc.kb0 + gp.kb_group - 1) / gp.kb_group;
-            PosInfo ps{};
-            if (fused) ps = decode_pos(tc.p0 + 32 * quad + lane, gp.epi);
-            if (C::kTmemSum && (ngroups > 1 || C::kAccBufs == 1)) {
-                // Each group's partial is added, with fp32 round-to-nearest, into the TMEM sum
-                // region (the first group is copied), and the accumulator is released at once;
-                // the output stage then reads the finished sums.  Same arithmetic, in the
-                // same order, as the register sums below.  (A single group with a single
-                // accumulator goes this way too, to release the accumulator before the
-                // stores.)
-                for (int g = 0; g < ngroups; ++g, ++grp) {
-                    if (!(ok = wait_group(grp))) break;
-#pragma unroll 1
-                    for (int c = 0; c < kChunks; ++c) {
-                        uint32_t u[32], w[32];
-                        tmem_chunk(grp, c_base + c, u);
-                        if (g > 0) {
-                            sum_chunk_ld(c_base + c, w);
-                            ptx::tmem_wait_ld();
-#pragma unroll
-                            for (int cc = 0; cc < 32; ++cc)
-                                w[cc] = __float_as_uint(__uint_as_float(w[cc]) + __uint_as_float(u[cc]));
-                        } else {
-                            ptx::tmem_wait_ld();
-#pragma unroll
-                            for (int cc = 0; cc < 32; ++cc) w[cc] = u[cc];
-                        }
-                        ptx::tmem_st_32x32b_x32(tmem_base + lane_addr + C::kSumCol + 32u * (c_base + c), w);
-                    }
-                    ptx::tmem_wait_st();
-                    release_group(grp);
-                }
-                if (!ok) break;
-#pragma unroll 1
-                for (int c = 0; c < kChunks; ++c) {
-                    uint32_t u[32];
-                    sum_chunk_ld(c_base + c, u);
-                    ptx::tmem_wait_ld();
-                    float v[32];
-#pragma unroll
-                    for (int cc = 0; cc < 32; ++cc) v[cc] = __uint_as_float(u[cc]);
-                    store_chunk(tc, ps, c_base + c, v);
-                }
-            } else if (P != Prec::TF32x3 || ngroups == 1) {
-                // One accumulation group: straight from TMEM to the output stage.
-                if (!(ok = wait_group(grp))) break;
-#pragma unroll 1
-                for (int c = 0; c < kChunks; ++c) {
-                    uint32_t u[32];
-                    tmem_chunk(grp, c_base + c, u);
-                    ptx::tmem_wait_ld();
-                    if (c == kChunks - 1) release_group(grp);  // TMEM no longer needed
-                    float v[32];
-#pragma unroll
-                    for (int cc = 0; cc < 32; ++cc) v[cc] = __uint_as_float(u[cc]);
-                    store_chunk(tc, ps, c_base + c, v);
-                }
-                ++grp;
-            } else if constexpr (P == Prec::TF32x3 && !C::kTmemSum) {
-                // BN = 64 only.
-                // Several groups: each group's partial leaves TMEM and is added, with fp32
-                // round-to-nearest, into running sums held in registers (this thread's
-                // position, this warp's BN/2 columns of the tile).  Keeps every tensor-core
-                // accumulation chain short; see the group length chosen by the host.
-                float sum[kChunks][32];
-                for (int g = 0; g < ngroups; ++g, ++grp) {
-                    if (!(ok = wait_group(grp))) break;
-#pragma unroll
-                    for (int c = 0; c < kChunks; ++c) {
-                        uint32_t u[32];
-                        tmem_chunk(grp, c_base + c, u);
-                        ptx::tmem_wait_ld();
-#pragma unroll
-                        for (int cc = 0; cc < 32; ++cc)
-                            sum[c][cc] = g == 0 ? __uint_as_float(u[cc]) : sum[c][cc] + __uint_as_float(u[cc]);
-                    }
-                    release_group(grp);
-                }
-                if (!ok) break;
-                // Unrolled (kChunks <= 2 here), so each chunk's sums die once stored.
-#pragma unroll
-                for (int c = 0; c < kChunks; ++c) store_chunk(tc, ps, c_base + c, sum[c]);
-            }
-        }
-    }
-
-    // ---------------------------------------------------------------- teardown
-    __syncwarp();
-    ptx::tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        __syncwarp();
-        ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, C::kTmemCols);
-    }
-}
-
-template <Prec P, int BN>
-cudaError_t launch_inst(const ctr_plan_s *pl, const CUtensorMap *maps, const GemmParams &gp,
-                        cudaStream_t st) {
-    using C = Cfg<P, BN>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<P, BN>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    const int64_t grid = std::min<int64_t>(gp.num_tiles, pl->num_sms);
-    const cudaError_t e = launch_pdl(gemm_tc_kernel<P, BN>, dim3((unsigned)grid), dim3(kThreads),
-                                     (size_t)C::kSmem, st, maps[0], maps[1], maps[2], maps[3], gp);
-    if (e != cudaSuccess) return e;
-    count_launches(1);
-    return cudaGetLastError();
-}
-
 }  // namespace
 
 size_t gemm_smem_bytes(Prec prec, int block_n) {
@@ -469,17 +27,18 @@ size_t gemm_smem_bytes(Prec prec, int block_n) {
 cudaError_t launch_gemm_tc(const ctr_plan_s *pl, const CUtensorMap *maps, const GemmParams &gp,
                            cudaStream_t st) {
     if (gp.num_tiles <= 0) return cudaSuccess;
+    if (gp.epi.out_staged) return launch_gemm_tc_chain(pl, maps, gp, st);
     if (pl->dtype == CTR_BF16) {
         switch (pl->block_n) {
-            case 256: return launch_inst<Prec::BF16, 256>(pl, maps, gp, st);
-            case 128: return launch_inst<Prec::BF16, 128>(pl, maps, gp, st);
-            default: return launch_inst<Prec::BF16, 64>(pl, maps, gp, st);
+            case 256: return launch_bn<Prec::BF16, 256>(pl, maps, gp, st);
+            case 128: return launch_bn<Prec::BF16, 128>(pl, maps, gp, st);
+            default: return launch_bn<Prec::BF16, 64>(pl, maps, gp, st);
         }
     }
     switch (pl->block_n) {
-        case 256: return launch_inst<Prec::TF32x3, 256>(pl, maps, gp, st);
-        case 128: return launch_inst<Prec::TF32x3, 128>(pl, maps, gp, st);
-        default: return launch_inst<Prec::TF32x3, 64>(pl, maps, gp, st);
+        case 256: return launch_bn<Prec::TF32x3, 256>(pl, maps, gp, st);
+        case 128: return launch_bn<Prec::TF32x3, 128>(pl, maps, gp, st);
+        default: return launch_bn<Prec::TF32x3, 64>(pl, maps, gp, st);
     }
 }
 
