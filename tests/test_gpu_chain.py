@@ -26,40 +26,41 @@ CHAINS = [
 ]
 
 
-def _make(dtype, B, C_in, sp, layers, rng):
-    plans, ws, bs = [], [], []
+def _make(dtype, B, C_in, sp, layers, rng, chained):
+    """Plans for the layers (chained before the weights are packed, when asked), their biases
+    and the weights drawn from rng."""
+    plans, bs, ws = [], [], []
     c, s = C_in, tuple(sp)
     for (co, k, st, p, op, slope) in layers:
         pl = ctr.Plan(B, c, co, s, k if isinstance(k, tuple) else (k,) * len(s), st, p, op,
                       dtype=tdtype(dtype), negative_slope=slope)
-        w = torch.from_numpy(rng.uniform(-0.2, 0.2, (c, co) + tuple(pl.kernel)).astype(np.float32))
-        b = torch.from_numpy(rng.standard_normal(co).astype(np.float32))
-        w, b = w.cuda().to(tdtype(dtype)), b.cuda().to(tdtype(dtype))
-        pl.prepack(w)
+        ws.append(rng.uniform(-0.2, 0.2, (c, co) + tuple(pl.kernel)).astype(np.float32))
+        bs.append(torch.from_numpy(rng.standard_normal(co).astype(np.float32)).cuda().to(tdtype(dtype)))
         plans.append(pl)
-        ws.append(w)
-        bs.append(b)
         c, s = co, pl.out_spatial
+    if chained:
+        for a, nxt in zip(plans[:-1], plans[1:]):
+            a.chain(nxt)
+    for pl, w in zip(plans, ws):
+        pl.prepack(torch.from_numpy(w).cuda().to(tdtype(dtype)))
     return plans, bs
 
 
 @pytest.mark.parametrize("case", CHAINS, ids=lambda c: "%s-%dd-%dlayers" % (c[0], len(c[3]), len(c[4])))
 def test_chained_equals_unchained(case):
     dtype, B, C_in, sp, layers = case
-    rng = np.random.default_rng(41)
-    plans, bs = _make(dtype, B, C_in, sp, layers, rng)
+    plans0, bs0 = _make(dtype, B, C_in, sp, layers, np.random.default_rng(41), chained=False)
+    plans, bs = _make(dtype, B, C_in, sp, layers, np.random.default_rng(41), chained=True)
     try:
-        x = torch.from_numpy(rng.standard_normal((B, C_in) + tuple(sp)).astype(np.float32))
-        x = x.cuda().to(tdtype(dtype))
+        x = torch.from_numpy(np.random.default_rng(42).standard_normal((B, C_in) + tuple(sp))
+                             .astype(np.float32)).cuda().to(tdtype(dtype))
         # Unchained: every layer through the torch layout.
         h = x
-        for pl, b in zip(plans, bs):
+        for pl, b in zip(plans0, bs0):
             h = pl.forward(h, b)
         ref = h.float().cpu().numpy()
         assert plans[0].path == ctr.CTR_PATH_POLYPHASE
         # Chained: only the first layer stages an input, only the last writes a y.
-        for a, nxt in zip(plans[:-1], plans[1:]):
-            a.chain(nxt)
         for it in range(2):
             y = torch.full(plans[-1].out_shape, float("nan"), dtype=tdtype(dtype), device="cuda")
             assert plans[0].forward(x, bs[0]) is None
@@ -71,16 +72,17 @@ def test_chained_equals_unchained(case):
                 pl.check()
             np.testing.assert_array_equal(y.float().cpu().numpy(), ref, err_msg="call %d" % it)
     finally:
-        for pl in plans:
+        for pl in plans + plans0:
             pl.close()
 
 
 def test_chain_errors_on_device():
-    """A chained producer refuses a y; a plan fed by a chain still accepts an explicit x."""
+    """A chained producer refuses a y and cannot be re-chained once packed; a plan fed by a
+    chain still accepts an explicit x; a producer whose chain partner is gone refuses to run."""
     rng = np.random.default_rng(43)
-    plans, bs = _make("bf16", 1, 64, (128,), [(64, 4, 2, 1, 0, None), (32, 4, 2, 1, 0, None)], rng)
+    layers = [(64, 4, 2, 1, 0, None), (32, 4, 2, 1, 0, None)]
+    plans, bs = _make("bf16", 1, 64, (128,), layers, rng, chained=True)
     try:
-        plans[0].chain(plans[1])
         x = torch.randn(1, 64, 128, device="cuda").to(torch.bfloat16)
         with pytest.raises(ValueError):
             plans[0].forward(x, bs[0], y=torch.empty(plans[0].out_shape, dtype=torch.bfloat16,
@@ -88,13 +90,22 @@ def test_chain_errors_on_device():
         st = ctr.lib.ctr_forward(plans[0].handle, x.data_ptr(), plans[0].w_packed.data_ptr(),
                                  None, x.data_ptr(), None)
         assert st == ctr.CTR_ERR_INVALID_ARG
-        # plans[1] with its own x: staged normally, same as unchained
+        with pytest.raises(ctr.CtrError):
+            plans[0].chain(None)                      # packed for the chained output
+        # plans[1] with its own x: staged normally, same as an unchained plan
         x1 = torch.randn((1, 64) + plans[0].out_spatial, device="cuda").to(torch.bfloat16)
         y_a = plans[1].forward(x1, bs[1])
-        plans[0].chain(None)
-        y_b = plans[1].forward(x1, bs[1])
+        p1, b1 = _make("bf16", 1, 64, (128,), layers, np.random.default_rng(43), chained=False)
+        y_b = p1[1].forward(x1, b1[1])
         torch.cuda.synchronize()
         assert torch.equal(y_a, y_b)
+        for pl in p1:
+            pl.close()
+        # the consumer destroyed: the producer's phase-major weight has no chain to feed
+        plans[1].close()
+        st = ctr.lib.ctr_forward(plans[0].handle, x.data_ptr(), plans[0].w_packed.data_ptr(),
+                                 None, None, None)
+        assert st == ctr.CTR_ERR_INVALID_ARG
     finally:
         for pl in plans:
             pl.close()

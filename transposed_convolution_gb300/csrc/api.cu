@@ -139,6 +139,7 @@ void layout_plan(ctr_plan_s *pl) {
     pl->ws_bytes_needed = 0;
     pl->ws_off_stage = pl->ws_stage_bytes = pl->ws_off_raw = pl->ws_raw_bytes = 0;
     pl->chain_zeroed_ws = nullptr;   // the staged layout may change
+    pl->row_pm = 0;
     pl->splits = 1;
     pl->block_n = 0;
     pl->num_tiles = 0;
@@ -170,6 +171,12 @@ void layout_plan(ctr_plan_s *pl) {
     pl->K_total = pl->m[0] * pl->m[1] * pl->C_in_pad;
     pl->N_total = pl->B * pl->P[0] * pl->P[1];
     choose_tiling(pl);
+    // A chained producer packs its rows phase-major within each tile, so that the output
+    // stage's 32-row chunks are runs of consecutive channels (contiguous in the next
+    // plan's channels-last staged input).  Needs whole phase sets that divide the tile.
+    pl->row_pm = pl->chain_next && pl->path == CTR_PATH_POLYPHASE && pl->S == pl->S_pad &&
+                 pl->S_pad <= 32 && pl->block_n % pl->S_pad == 0 && pl->block_n / pl->S_pad >= 2;
+    if (pl->row_pm) pl->M_pad = (int64_t)pl->num_r_tiles * pl->block_n;
     pl->packed_bytes = (size_t)pl->M_pad * pl->K_total * op_esize(pl) * op_planes(pl);
     pl->ws_off_stage = 0;
     pl->ws_stage_bytes = (size_t)pl->N_total * pl->C_in_pad * op_esize(pl) * op_planes(pl);
@@ -305,6 +312,7 @@ EpiParams make_epi(const ctr_plan_s *pl, const void *bias, void *y) {
     const int es = pl->dtype == CTR_BF16 ? 2 : 4;
     e.out_staged = 0;
     e.ys_Px = e.ys_Py = e.ys_hx = e.ys_hy = e.ys_cpad = e.ys_lo = 0;
+    e.pm_tc = pl->row_pm ? pl->block_n / pl->S_pad : 0;
     e.store_bytes = es;
     for (int w : {16, 8, 4}) {
         if (nx > 0 && (nx * es) % w == 0 && (sx * es) % w == 0 && (pl->p[1] * es) % w == 0 &&
@@ -617,6 +625,8 @@ ctr_status ctr_forward(ctr_plan_t pl, const void *x, const void *w_packed, const
     if (!pl) return CTR_ERR_INVALID_ARG;
     if (!pl->prepared) return CTR_ERR_NOT_PREPARED;
     ctr_plan_s *nx = pl->chain_next;
+    // A weight packed for a chained output (phase-major rows) needs that chain.
+    if (pl->row_pm && !nx) return CTR_ERR_INVALID_ARG;
     const bool staged_in = !x && pl->chain_prev != nullptr;  // input staged by the previous plan
     if (!w_packed || (nx ? y != nullptr : y == nullptr)) return CTR_ERR_INVALID_ARG;
     if (!x && !staged_in && pl->B * pl->C_in * pl->in[0] * pl->in[1] > 0)
@@ -661,10 +671,11 @@ ctr_status ctr_forward(ctr_plan_t pl, const void *x, const void *w_packed, const
 }
 
 ctr_status ctr_plan_chain(ctr_plan_t pl, ctr_plan_t nx) {
-    if (!pl) return CTR_ERR_INVALID_ARG;
+    if (!pl || pl->prepared) return CTR_ERR_INVALID_ARG;   // the packed row order depends on it
     if (!nx) {
         if (pl->chain_next) pl->chain_next->chain_prev = nullptr;
         pl->chain_next = nullptr;
+        layout_plan(pl);
         return CTR_OK;
     }
     if (nx == pl || !chain_compatible(pl, nx)) return CTR_ERR_INVALID_ARG;
@@ -673,6 +684,7 @@ ctr_status ctr_plan_chain(ctr_plan_t pl, ctr_plan_t nx) {
     pl->chain_next = nx;
     nx->chain_prev = pl;
     nx->chain_zeroed_ws = nullptr;
+    layout_plan(pl);
     return CTR_OK;
 }
 

@@ -123,6 +123,7 @@ struct PackGeo {
     int S, S_pad;
     int polyphase;
     int bf16;
+    int pm_tc, block_n;   // phase-major rows within tiles of block_n rows (pm_tc channels)
 };
 
 // Polyphase rows ("[XNNPACK] Lower dense transposed convs as one polyphase conv + depth to
@@ -133,6 +134,8 @@ struct PackGeo {
 // col2im rows ("[WebGPU] optimizations for audio models", ConvTranspose commit: W[C_in,
 // kH*kW*C_out] prepacked to the GEMM layout):  A[r = oc*S_pad + t, k = ic] = w[ic, oc, t].
 // Padding rows and channels are zero.  fp32 weights are split into tf32 hi and lo planes.
+// A chained producer (pm_tc > 0) orders the rows of each block_n-row tile phase-major
+// instead: tile t, row j * pm_tc + c is phase j of channel t * pm_tc + c.
 __global__ void prepack_kernel(const void *__restrict__ w, void *__restrict__ wp, PackGeo pg) {
     const int64_t total = pg.M_pad * pg.K_total;
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
@@ -141,8 +144,15 @@ __global__ void prepack_kernel(const void *__restrict__ w, void *__restrict__ wp
         const int64_t kk = idx - r * pg.K_total;
         const int64_t g = kk / pg.C_in_pad;
         const int64_t ic = kk - g * pg.C_in_pad;
-        const int64_t oc = r / pg.S_pad;
-        const int64_t j = r - oc * pg.S_pad;
+        int64_t oc, j;
+        if (pg.pm_tc) {
+            const int64_t t = r / pg.block_n, rl = r - t * pg.block_n;
+            j = rl / pg.pm_tc;
+            oc = t * pg.pm_tc + (rl - j * pg.pm_tc);
+        } else {
+            oc = r / pg.S_pad;
+            j = r - oc * pg.S_pad;
+        }
         float v = 0.0f;
         if (oc < pg.C_out && j < pg.S && ic < pg.C_in) {
             int64_t ty, tx;
@@ -473,6 +483,8 @@ cudaError_t launch_prepack(const ctr_plan_s *pl, const void *w, void *w_packed, 
     pg.S_pad = pl->S_pad;
     pg.polyphase = pl->path == CTR_PATH_POLYPHASE ? 1 : 0;
     pg.bf16 = pl->dtype == CTR_BF16 ? 1 : 0;
+    pg.pm_tc = pl->row_pm ? pl->block_n / pl->S_pad : 0;
+    pg.block_n = pl->block_n;
     const int64_t total = pg.M_pad * pg.K_total;
     prepack_kernel<<<grid_for(total, kBlock), kBlock, 0, st>>>(w, w_packed, pg);
     count_launches(1);

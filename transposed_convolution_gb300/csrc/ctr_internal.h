@@ -51,6 +51,10 @@ struct EpiParams {
     // ox + ys_hx; fp32 as tf32 hi and lo planes, ys_lo elements apart.
     int out_staged;
     int64_t ys_Px, ys_Py, ys_hx, ys_hy, ys_cpad, ys_lo;
+    // Phase-major rows (pm_tc > 0, chained producers only): inside each tile of
+    // pm_tc * S_pad rows, row j * pm_tc + c is phase j of the tile's channel c, so a 32-row
+    // chunk holds whole channel runs of one (or a few) phases.
+    int pm_tc;
 };
 
 // The tensor-core GEMM D[n, r] = sum_k Xs[n + shift(k), k] * A[r, k]: n runs over staged
@@ -126,6 +130,7 @@ struct ctr_plan_s {
     ctr_plan_s *chain_next;
     ctr_plan_s *chain_prev;
     void *chain_zeroed_ws;  // workspace whose staged buffer was zeroed for chained input
+    int row_pm;             // packed rows phase-major within each tile (set for chained output)
     uint32_t *d_status;
     int status_device;
     uint64_t wait_limit_ns;

@@ -301,6 +301,52 @@ __device__ __forceinline__ void emit_small_chain(const float (&v)[32], const Pos
     }
 }
 
+// Phase-major rows (EpiParams::pm_tc): the chunk's 32 columns are NJ = 32 / TCR phases of
+// TCR = min(pm_tc, 32) consecutive channels each, so every phase is one run of TCR channel
+// values at one output position.
+template <typename T, int TCR>
+__device__ __forceinline__ void emit_pm_chain(const float (&v)[32], const PosInfo &ps,
+                                              int64_t r0, const EpiParams &e, int lane) {
+    constexpr int NJ = 32 / TCR;
+    const int tc = e.pm_tc;
+    const int bn = tc * e.S_pad;
+    const int64_t tile = r0 / bn;
+    const int rl0 = (int)(r0 - tile * bn);
+    const int j0 = rl0 / tc;
+    const int64_t oc0 = tile * tc + (rl0 - j0 * tc);
+    const float bl = lane_bias(e, oc0, TCR, lane);
+    const float slope_eff = slope_of(e);
+    const bool use_min = slope_eff > 1.0f;
+    const int64_t c_left = e.C_out - oc0;
+    const int cmax = c_left < TCR ? (int)c_left : TCR;
+    float t[32];
+#pragma unroll
+    for (int i = 0; i < TCR; ++i) {
+        const float bias = __shfl_sync(0xffffffffu, bl, i);
+#pragma unroll
+        for (int jj = 0; jj < NJ; ++jj)
+            t[jj * TCR + i] = leaky(v[jj * TCR + i] + bias, slope_eff, use_min);
+    }
+    if (!ps.valid || cmax <= 0) return;
+    T *__restrict__ ys = static_cast<T *>(e.y);
+#pragma unroll
+    for (int jj = 0; jj < NJ; ++jj) {
+        const int j = j0 + jj;
+        const int jy = j / e.sx, jx = j - (j / e.sx) * e.sx;
+        const int64_t oy = (int64_t)e.sy * ps.qy + jy - e.py;
+        const int64_t ox = (int64_t)e.sx * ps.qx + jx - e.px;
+        if (oy < 0 || oy >= e.Hout || ox < 0 || ox >= e.Wout) continue;
+        T *dst = ys + staged_row(e, ps.b, oy, ox) * e.ys_cpad + oc0;
+        if (cmax == TCR) {
+            store_channels<T, TCR>(dst, &t[jj * TCR], e);
+        } else {
+#pragma unroll
+            for (int i = 0; i < TCR; ++i)
+                if (i < cmax) store_channels<T, 1>(dst + i, &t[jj * TCR + i], e);
+        }
+    }
+}
+
 // Any plan, element by element.
 __device__ __forceinline__ void emit_generic_chain(const float (&v)[32], const PosInfo &ps,
                                                    int64_t r0, const EpiParams &e) {
@@ -335,6 +381,22 @@ __device__ __forceinline__ void emit_generic_chain(const float (&v)[32], const P
 template <bool kChain>
 __device__ __forceinline__ void emit_cols(const float (&v)[32], const PosInfo &ps, int64_t r0,
                                           const EpiParams &e, int lane) {
+    if (kChain && e.out_staged && e.pm_tc) {
+#define CTR_PM(TCR)                                                        \
+    if (e.out_bf16)                                                        \
+        emit_pm_chain<__nv_bfloat16, TCR>(v, ps, r0, e, lane);             \
+    else                                                                   \
+        emit_pm_chain<float, TCR>(v, ps, r0, e, lane);                     \
+    return
+        switch (e.pm_tc >= 32 ? 32 : e.pm_tc) {
+            case 2: CTR_PM(2);
+            case 4: CTR_PM(4);
+            case 8: CTR_PM(8);
+            case 16: CTR_PM(16);
+            default: CTR_PM(32);
+        }
+#undef CTR_PM
+    }
     if (kChain && e.out_staged) {
 #define CTR_CHAIN(SX, SY)                                                  \
     if (e.out_bf16)                                                        \
