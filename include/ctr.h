@@ -143,8 +143,11 @@ ctr_status ctr_plan_set_tile(ctr_plan_t plan, int block_n);
  * output size.  At each forward, next's workspace must be bound (CTR_ERR_NO_WORKSPACE)
  * and must not overlap plan's (CTR_ERR_INVALID_ARG); the first forward after binding
  * zeroes next's staged buffer once (its halos stay zero).  Run plan, then next, on the
- * same stream.  ctr_plan_chain(plan, NULL) unchains; destroying either plan unchains
- * both.  Host only; no counterpart of the call itself on the pages.
+ * same stream.  A chained plan packs its weight rows for this output (phase-major within
+ * each tile), so ctr_plan_chain(plan, ...) must come before ctr_prepack_weight(plan)
+ * (CTR_ERR_INVALID_ARG after it), and a plan packed for a chain whose other end was
+ * destroyed refuses to run.  ctr_plan_chain(plan, NULL) unchains; destroying either plan
+ * unchains both.  Host only; no counterpart of the call itself on the pages.
  */
 ctr_status ctr_plan_chain(ctr_plan_t plan, ctr_plan_t next);
 
