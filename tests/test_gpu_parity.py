@@ -120,6 +120,21 @@ def test_every_tile_width_bit_exact(dtype, block_n):
     np.testing.assert_array_equal(y, reference(x, w, b, (2, 2), (1, 1), (1, 0), dtype), err_msg=desc)
 
 
+@pytest.mark.parametrize("block_n", [64, 128, 256])
+def test_all_positive_long_k_within_tolerance(block_n):
+    """The worst case for the tensor core's truncating fp32 accumulation: same-sign products
+    over K = 4096 (2 taps x 2048 channels), where the drift is systematic instead of
+    averaging out.  The grouped accumulation keeps fp32 I/O within rel_l2 1e-5 at every
+    tile width (register sums at 64, TMEM sums at 128 and 256)."""
+    rng = np.random.default_rng(47)
+    x = rng.uniform(0.0, 1.0, (1, 2048, 300)).astype(np.float32)
+    w = rng.uniform(0.0, 1.0, (2048, 64, 16)).astype(np.float32)
+    b = rng.uniform(0.0, 1.0, 64).astype(np.float32)
+    y, desc = run_plan(x, w, b, 8, 4, 0, "f32", path=ctr.CTR_PATH_POLYPHASE, block_n=block_n)
+    err = oracle.rel_l2(y, reference(x, w, b, 8, 4, 0, "f32"))
+    assert err <= TOL["f32"], "rel_l2 %.3g %s" % (err, desc)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("path", sorted(PATHS))
 def test_random_within_tolerance(path, dtype):

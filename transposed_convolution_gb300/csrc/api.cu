@@ -65,12 +65,16 @@ bool is_tc_path(int path) { return path == CTR_PATH_POLYPHASE || path == CTR_PAT
 // Estimated clocks of one K slice of a 128-position x BN-row tile on one SM (tensor pipe).
 double slice_clocks(Prec prec, int bn) { return prec == Prec::TF32x3 ? 6.0 * bn : 2.0 * bn; }
 
-// K slices per tensor-core accumulation group in 3xTF32 mode (256 fp32 K elements).  The
-// tensor core's fp32 accumulation over a long K chain drifts well beyond fp32 summation
-// with round-to-nearest (measured on GB300: rel_l2 2.3e-5 over 3300-element chains), so
-// the kernel moves the partial sum out of TMEM every group and adds it in registers with
-// round-to-nearest; the drift then scales with the group length only.
-constexpr int kTf32Group = 8;
+// 128-byte K slices per tensor-core accumulation group in 3xTF32 mode (512 fp32 K
+// elements).  The tensor core's fp32 accumulation over a long K chain drifts well beyond
+// fp32 summation with round-to-nearest (measured on GB300: rel_l2 2.3e-5 over 3300-element
+// chains, a mean relative bias of -4.6e-5 over 4096 all-positive products), so the kernel
+// moves the partial sum out of TMEM every group and adds it with round-to-nearest; the
+// drift then scales with the group length only.  At 512 elements the all-positive worst
+// case stays below the 1e-5 rel_l2 bound (a GPU test pins it) and random inputs give
+// about 3e-6; 256 elements halve that but fold twice as often, which pauses the MMAs of
+// 256-row tiles (codec upsampler step 46.2 vs 44.3 us).
+constexpr int kTf32Group = 16;
 constexpr int kNoGroup = 1 << 30;
 
 int tf32_group() {
