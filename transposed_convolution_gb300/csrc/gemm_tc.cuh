@@ -74,6 +74,9 @@ struct Cfg {
     // at most 4, so the MMA can run several tiles ahead of the epilogue.
     static constexpr int kAccBufs = kTmemSum ? (512 - BN) / BN : (512 / BN > 4 ? 4 : 512 / BN);
     static constexpr uint32_t kSumCol = kAccBufs * BN;       // first column of the sum region
+    // With a single accumulator the first group of a tile accumulates straight into the
+    // sum region (nothing to fold); the later groups go through the accumulator.
+    static constexpr bool kSumFirst = kTmemSum && kAccBufs == 1;
     static constexpr uint32_t kTmemCols = kAccBufs * BN + (kTmemSum ? BN : 0);
     static constexpr uint32_t kIdesc =
         ptx::idesc_f32acc(P == Prec::TF32x3 ? ptx::kFmtTF32 : ptx::kFmtBF16, kBM, BN);
@@ -128,7 +131,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *tmem_full = bars + 2 * C::kStages;
     uint64_t *tmem_empty = tmem_full + C::kAccBufs;
     uint64_t *drain = tmem_empty + C::kAccBufs;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    uint64_t *sum_full = drain + 1;   // kSumFirst: a tile's first group is in the sum region
+    uint64_t *sum_free = drain + 2;   // kSumFirst: the epilogue has read a tile's sums
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 3);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -151,6 +156,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(&tmem_empty[a], kEpiWarps);
         }
         ptx::mbar_init(drain, 1);
+        ptx::mbar_init(sum_full, 1);
+        ptx::mbar_init(sum_free, kEpiWarps);
         *abort = 0;
         ptx::fence_mbar_init();
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -234,21 +241,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            int grp = 0;  // accumulation groups issued by this CTA (selects the TMEM buffer)
+            int grp = 0;    // accumulator groups issued by this CTA (selects the TMEM buffer)
+            int items = 0;  // tiles issued by this CTA (kSumFirst barrier phases)
             bool ok = true;
-            for (int64_t t = blockIdx.x; ok && t < gp.num_tiles && !*abort; t += gridDim.x) {
+            for (int64_t t = blockIdx.x; ok && t < gp.num_tiles && !*abort; t += gridDim.x, ++items) {
                 const TileCoord tc = decode_tile((uint32_t)t, gp, BN);
-                for (int kb = tc.kb0; ok && kb < tc.kb1; ++grp) {
+                for (int kb = tc.kb0, g = 0; ok && kb < tc.kb1; ++g) {
                     const int kb_end = min(kb + gp.kb_group, tc.kb1);
+                    const bool to_sum = C::kSumFirst && g == 0;
                     const int acc = grp % C::kAccBufs;
-                    const uint32_t acc_phase = (uint32_t)(grp / C::kAccBufs) & 1u;
-                    if (!ptx::mbar_wait(&tmem_empty[acc], acc_phase ^ 1u, limit, abort)) {
-                        if (!*abort) give_up(abort, gp.status, kStatusTimeoutMma);
-                        ok = false;
-                        break;
+                    if (to_sum) {
+                        // The previous tile's sums must have been read.
+                        if (!ptx::mbar_wait(sum_free, ((uint32_t)items & 1u) ^ 1u, limit, abort)) {
+                            if (!*abort) give_up(abort, gp.status, kStatusTimeoutMma);
+                            ok = false;
+                            break;
+                        }
+                    } else {
+                        const uint32_t acc_phase = (uint32_t)(grp / C::kAccBufs) & 1u;
+                        if (!ptx::mbar_wait(&tmem_empty[acc], acc_phase ^ 1u, limit, abort)) {
+                            if (!*abort) give_up(abort, gp.status, kStatusTimeoutMma);
+                            ok = false;
+                            break;
+                        }
                     }
                     ptx::tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                    const uint32_t d_tmem =
+                        tmem_base + (to_sum ? C::kSumCol : (uint32_t)(acc * BN));
                     uint32_t accumulate = 0;
                     for (; kb < kb_end; ++kb) {
                         if (!ptx::mbar_wait(&full[stage], phase, limit, abort)) {
@@ -283,7 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             phase ^= 1u;
                         }
                     }
-                    if (ok) ptx::mma_commit(&tmem_full[acc]);
+                    if (ok) ptx::mma_commit(to_sum ? sum_full : &tmem_full[acc]);
+                    if (!to_sum) ++grp;
                 }
             }
             // Every MMA issued above completes before TMEM is freed.
@@ -299,6 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool fused = gp.epi_mode == EPI_POLYPHASE;
         const uint32_t lane_addr = (uint32_t)(32 * quad) << 16;
         int grp = 0;
+        int items = 0;   // kSumFirst: tiles whose sums this warp has read
         // Bounded wait of lane 0 on (bar, parity), uniform across the warp.
         auto warp_wait = [&](uint64_t *bar, uint32_t parity) -> bool {
             int ok = 1;
@@ -347,14 +368,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int ngroups = (tc.kb1 - tc.kb0 + gp.kb_group - 1) / gp.kb_group;
             PosInfo ps{};
             if (fused) ps = decode_pos(tc.p0 + 32 * quad + lane, gp.epi);
-            if (C::kTmemSum && (ngroups > 1 || C::kAccBufs == 1)) {
+            if (C::kTmemSum && (C::kSumFirst || ngroups > 1)) {
                 // Each group's partial is added, with fp32 round-to-nearest, into the TMEM sum
-                // region (the first group is copied), and the accumulator is released at once;
-                // the output stage then reads the finished sums.  Same arithmetic, in the
-                // same order, as the register sums below.  (A single group with a single
-                // accumulator goes this way too, to release the accumulator before the
-                // stores.)
-                for (int g = 0; g < ngroups; ++g, ++grp) {
+                // region (the first group is copied, or with a single accumulator was
+                // accumulated there directly), and the accumulator is released at once; the
+                // output stage then reads the finished sums.  Same arithmetic, in the same
+                // order, as the register sums below.
+                const int item = items++;
+                for (int g = 0; g < ngroups; ++g) {
+                    if (C::kSumFirst && g == 0) {
+                        if (!(ok = warp_wait(sum_full, (uint32_t)item & 1u))) break;
+                        ptx::tc_fence_after();
+                        continue;
+                    }
                     if (!(ok = wait_group(grp))) break;
 #pragma unroll 1
                     for (int c = 0; c < kChunks; ++c) {
@@ -375,6 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ptx::tmem_wait_st();
                     release_group(grp);
+                    ++grp;
                 }
                 if (!ok) break;
 #pragma unroll 1
@@ -386,6 +413,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int cc = 0; cc < 32; ++cc) v[cc] = __uint_as_float(u[cc]);
                     store_chunk(tc, ps, c_base + c, v);
+                }
+                if constexpr (C::kSumFirst) {   // the sum region may take the next tile
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(sum_free);
                 }
             } else if (P != Prec::TF32x3 || ngroups == 1) {
                 // One accumulation group: straight from TMEM to the output stage.
