@@ -66,6 +66,10 @@ def _load():
             lib.ctr_oracle_conv_transpose.argtypes = (
                 [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]
                 + [_I64P] * 5 + [_F64P] * 4)
+            lib.ctr_oracle_conv_transpose_groups.restype = ctypes.c_int
+            lib.ctr_oracle_conv_transpose_groups.argtypes = (
+                [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]
+                + [_I64P] * 5 + [_F64P] * 4)
             _lib = lib
     return _lib
 
@@ -104,11 +108,13 @@ def landed_pairs(in_sp, kernel, stride, padding, output_padding=0) -> int:
                                                _i64(p), _i64(op)))
 
 
-def conv_transpose(x, w, bias=None, stride=1, padding=0, output_padding=0) -> np.ndarray:
+def conv_transpose(x, w, bias=None, stride=1, padding=0, output_padding=0,
+                   groups=1) -> np.ndarray:
     """ConvTranspose in double.
 
-    x: [B, C_in, L] or [B, C_in, H, W]; w: [C_in, C_out, k] or [C_in, C_out, kH, kW]
-    (un-flipped torch layout); bias: [C_out] or None.  Inputs are converted to float64
+    x: [B, C_in, L] or [B, C_in, H, W]; w: [C_in, C_out/groups, k] or [C_in, C_out/groups,
+    kH, kW] (un-flipped torch layout); bias: [C_out] or None; groups divides C_in and C_out
+    (groups = C_in = C_out is the depthwise case).  Inputs are converted to float64
     exactly (fp32 and bf16 values are representable).  Returns float64
     [B, C_out, L_out] / [B, C_out, H_out, W_out].
     """
@@ -118,7 +124,8 @@ def conv_transpose(x, w, bias=None, stride=1, padding=0, output_padding=0) -> np
     assert ndim in (1, 2) and w.ndim == x.ndim
     B, C_in = x.shape[:2]
     assert w.shape[0] == C_in
-    C_out = w.shape[1]
+    G = int(groups)
+    C_out = w.shape[1] * G
     in_sp = x.shape[2:]
     k = w.shape[2:]
     s = _tuple(stride, ndim)
@@ -133,8 +140,8 @@ def conv_transpose(x, w, bias=None, stride=1, padding=0, output_padding=0) -> np
         bias = np.ascontiguousarray(np.asarray(bias, dtype=np.float64))
         assert bias.shape == (C_out,)
         bptr = bias.ctypes.data_as(_F64P)
-    rc = _load().ctr_oracle_conv_transpose(
-        ndim, B, C_in, C_out, _i64(in_sp), _i64(k), _i64(s), _i64(p), _i64(op),
+    rc = _load().ctr_oracle_conv_transpose_groups(
+        ndim, B, C_in, C_out, G, _i64(in_sp), _i64(k), _i64(s), _i64(p), _i64(op),
         x.ctypes.data_as(_F64P), w.ctypes.data_as(_F64P), bptr, y.ctypes.data_as(_F64P))
     if rc != 0:
         raise ValueError("oracle rejected the arguments (rc=%d)" % rc)

@@ -1,5 +1,6 @@
 /*
- * ctr_oracle.c -- plain CPU oracle for dense (groups = 1) transposed convolution.
+ * ctr_oracle.c -- plain CPU oracle for transposed convolution: dense (groups = 1) and
+ * grouped, including depthwise (groups = C_in = C_out).
  *
  * TEST INFRASTRUCTURE.  Only the test suite, the smoke check and the CPU-baseline leg of
  * the benchmark load this file's library.  The product library never links, loads or
@@ -7,17 +8,19 @@
  *
  * What it computes: the scatter form of ConvTranspose, in double precision.
  *
- *   for every batch b, input channel ic, input position i, output channel oc, tap t
+ *   for every batch b, input channel ic, input position i, output channel oc of ic's
+ *   group, tap t
  *       o = i*s - p + t                                  (per spatial dimension)
- *       if 0 <= o < L_out:  acc[b, oc, o] += x[b, ic, i] * w[ic, oc, t]
+ *       if 0 <= o < L_out:  acc[b, oc, o] += x[b, ic, i] * w[ic, oc - g*C_out/G, t]
  *   y[b, oc, o] = bias[oc] + acc[b, oc, o]               (bias = 0 when absent)
  *
- * with L_out = (L_in - 1)*s - 2p + k + op per dimension and the weight in the un-flipped
- * torch layout w[C_in][C_out][k...].  Sources:
+ * with L_out = (L_in - 1)*s - 2p + k + op per dimension, G groups (input channel ic and
+ * output channel oc belong to group g when ic / (C_in/G) = oc / (C_out/G) = g) and the
+ * weight in the un-flipped torch layout w[C_in][C_out/G][k...].  Sources:
  *   - "[ExecuTorch][WebGPU] Add optimized conv2d op" (PR #20849), Implementation: the
- *     transposed kernel reads the weight un-flipped as [IC, OC/groups, KH, KW] and a tap
- *     reaches an output when (oh + pH - kh*dH) is divisible by the stride and in range --
- *     the gather reading of the same scatter sum;
+ *     transposed kernel reads the weight un-flipped as [IC, OC/groups, KH, KW] (the grouped
+ *     layout) and a tap reaches an output when (oh + pH - kh*dH) is divisible by the
+ *     stride and in range -- the gather reading of the same scatter sum;
  *   - "[XNNPACK] Lower dense transposed convs as one polyphase conv + depth to space"
  *     (PR #25037), Summary: the clean-upscale output size (H-1)s - 2p + k + op;
  *   - "[WebGPU] optimizations for audio models" (PR #33978), ConvTranspose commits: the
@@ -76,19 +79,23 @@ int64_t ctr_oracle_landed_pairs(int ndim, const int64_t *in_sp, const int64_t *k
 }
 
 /*
- * y = ConvTranspose(x, w) + bias, all in double.
+ * y = ConvTranspose(x, w) + bias with G groups, all in double.
  *   x    [B][C_in][in_sp[0]]([in_sp[1]])            contiguous
- *   w    [C_in][C_out][ker[0]]([ker[1]])            contiguous, un-flipped torch layout
+ *   w    [C_in][C_out/G][ker[0]]([ker[1]])          contiguous, un-flipped torch layout
  *   bias [C_out] or NULL
  *   y    [B][C_out][L_out[0]]([L_out[1]])           contiguous, written in full
- * Returns 0 on success, -1 on invalid arguments, -2 when out of host memory.
+ * Returns 0 on success, -1 on invalid arguments (G must divide C_in and C_out), -2 when
+ * out of host memory.
  */
-int ctr_oracle_conv_transpose(int ndim, int64_t B, int64_t C_in, int64_t C_out,
-                              const int64_t *in_sp, const int64_t *ker, const int64_t *str,
-                              const int64_t *pad, const int64_t *opad,
-                              const double *x, const double *w, const double *bias, double *y)
+int ctr_oracle_conv_transpose_groups(int ndim, int64_t B, int64_t C_in, int64_t C_out,
+                                     int64_t G, const int64_t *in_sp, const int64_t *ker,
+                                     const int64_t *str, const int64_t *pad,
+                                     const int64_t *opad, const double *x, const double *w,
+                                     const double *bias, double *y)
 {
     if (ndim < 1 || ndim > 2 || B < 0 || C_in < 1 || C_out < 1) return -1;
+    if (G < 1 || C_in % G != 0 || C_out % G != 0) return -1;
+    const int64_t cin_g = C_in / G, cout_g = C_out / G;
 
     /* Unit height for 1-D. */
     int64_t H = 1, kh = 1, sh = 1, ph = 0, oph = 0;
@@ -128,10 +135,11 @@ int ctr_oracle_conv_transpose(int ndim, int64_t B, int64_t C_in, int64_t C_out,
         const int64_t b = item / (nchunk * C_out);
         const int64_t pos_lo = npos * chunk / nchunk;
         const int64_t pos_hi = npos * (chunk + 1) / nchunk;
+        const int64_t g = oc / cout_g, ocl = oc - g * cout_g;   /* group, channel in it */
         double *acc = part + item * nout;
-        for (int64_t ic = 0; ic < C_in; ++ic) {
+        for (int64_t ic = g * cin_g; ic < (g + 1) * cin_g; ++ic) {
             const double *xp = x + (b * C_in + ic) * npos;
-            const double *wp = w + (ic * C_out + oc) * ntap;
+            const double *wp = w + (ic * cout_g + ocl) * ntap;
             for (int64_t pos = pos_lo; pos < pos_hi; ++pos) {
                 const int64_t iy = pos / W, ix = pos % W;
                 const double xv = xp[pos];
@@ -165,4 +173,14 @@ int ctr_oracle_conv_transpose(int ndim, int64_t B, int64_t C_in, int64_t C_out,
     }
     free(part);
     return 0;
+}
+
+/* Dense transposed convolution: the grouped one with one group. */
+int ctr_oracle_conv_transpose(int ndim, int64_t B, int64_t C_in, int64_t C_out,
+                              const int64_t *in_sp, const int64_t *ker, const int64_t *str,
+                              const int64_t *pad, const int64_t *opad,
+                              const double *x, const double *w, const double *bias, double *y)
+{
+    return ctr_oracle_conv_transpose_groups(ndim, B, C_in, C_out, 1, in_sp, ker, str, pad, opad,
+                                            x, w, bias, y);
 }

@@ -15,7 +15,12 @@ Each ``pin_*`` function takes the ConvTranspose callable under test (normally
   one polyphase conv + depth to space" (Summary): one stride-1 convolution with m taps and
   padding m - 1 computing every phase, then the phase interleave and the padding slice;
 * ``pin_istft_sinusoid`` -- the closed-form iSTFT of a sinusoid framed without a window and
-  overlap-added with a periodic Hann window at hop N/4, which sums to exactly 2.
+  overlap-added with a periodic Hann window at hop N/4, which sums to exactly 2;
+* ``pin_torch_f64_groups`` -- torch's float64 ConvTranspose with groups (2, and depthwise);
+* ``pin_depthwise_k_equals_s`` -- depthwise with kernel = stride and no padding: every input
+  sample times the channel's kernel, laid end to end (an outer product);
+* ``pin_adjoint_groups`` -- the transpose of a grouped forward strided convolution whose
+  dense matrix is built element by element (itself checked against torch's grouped conv1d).
 
 ``tests/test_oracle_pins.py`` runs them on the oracle and, with mistakes planted in copies
 of the oracle source, shows that each planted mistake fails at least one of them.
@@ -45,12 +50,12 @@ def _close(a, b, rtol=1e-12, atol=1e-12):
     assert err <= atol + rtol * scale, "max abs err %.3g (scale %.3g)" % (err, scale)
 
 
-def _torch_ct(x, w, b, s, p, op):
+def _torch_ct(x, w, b, s, p, op, groups=1):
     xt = torch.from_numpy(np.asarray(x, dtype=np.float64))
     wt = torch.from_numpy(np.asarray(w, dtype=np.float64))
     bt = None if b is None else torch.from_numpy(np.asarray(b, dtype=np.float64))
     fn = F.conv_transpose1d if xt.dim() == 3 else F.conv_transpose2d
-    return fn(xt, wt, bt, stride=s, padding=p, output_padding=op).numpy()
+    return fn(xt, wt, bt, stride=s, padding=p, output_padding=op, groups=groups).numpy()
 
 
 def grid_1d(full=False):
@@ -238,5 +243,82 @@ def pin_istft_sinusoid(ct, n_fft=64, frames=12, batch=2, bin_f0=5):
     _close(y[:, 0, lo:hi], 2.0 * sig[:, lo:hi], rtol=1e-12, atol=1e-12)
 
 
-ALL_PINS = [pin_torch_f64_1d, pin_torch_f64_2d, pin_adjoint, pin_hand_cases, pin_matmul,
+def pin_torch_f64_groups(ct):
+    """Grouped and depthwise ConvTranspose against torch float64, 1-D grid subset and 2-D."""
+    n = 0
+    for (L, k, s, p, op) in grid_1d(full=False):
+        n += 1
+        if n % 2:
+            continue
+        for (C_in, C_out, G) in ((4, 6, 2), (4, 4, 4), (3, 3, 3)):
+            x = _rng.standard_normal((2, C_in, L))
+            w = _rng.standard_normal((C_in, C_out // G, k))
+            b = _rng.standard_normal(C_out)
+            _close(ct(x, w, b, s, p, op, groups=G), _torch_ct(x, w, b, s, p, op, groups=G))
+    for (H, W, ky, kx, sy, sx, py, px, G) in ((3, 4, 3, 2, 2, 1, 1, 0, 2), (2, 3, 4, 4, 2, 2, 1, 1, 6)):
+        C = 6
+        x = _rng.standard_normal((1, C, H, W))
+        w = _rng.standard_normal((C, C // G, ky, kx))
+        b = _rng.standard_normal(C)
+        _close(ct(x, w, b, (sy, sx), (py, px), (0, 0), groups=G),
+               _torch_ct(x, w, b, (sy, sx), (py, px), (0, 0), groups=G))
+
+
+def pin_depthwise_k_equals_s(ct):
+    """Depthwise, kernel = stride, no padding: y[b, c, s*i + t] = x[b, c, i] * w[c, 0, t] +
+    bias[c] -- each input sample scales the channel's kernel, the copies laid end to end
+    (and the 2-D analogue per dimension)."""
+    for (B, C, L, s) in ((2, 3, 5, 2), (1, 4, 3, 4), (1, 2, 6, 1)):
+        x = _rng.standard_normal((B, C, L))
+        w = _rng.standard_normal((C, 1, s))
+        b = _rng.standard_normal(C)
+        ref = (x[:, :, :, None] * w[None, :, 0, None, :]).reshape(B, C, L * s) + b[None, :, None]
+        _close(ct(x, w, b, s, 0, 0, groups=C), ref)
+    B, C, H, W, sy, sx = 1, 3, 2, 3, 2, 3
+    x = _rng.standard_normal((B, C, H, W))
+    w = _rng.standard_normal((C, 1, sy, sx))
+    ref = (x[:, :, :, None, :, None] * w[None, :, 0][:, :, None, :, None, :]).reshape(B, C, H * sy, W * sx)
+    _close(ct(x, w, None, (sy, sx), (0, 0), (0, 0), groups=C), ref)
+
+
+def forward_conv_matrix_groups_1d(w, L_in, L_out, s, p, G):
+    """Dense matrix of the grouped forward strided convolution, element by element:
+    Conv(y)[ic, i] = sum over the C_out/G channels oc of ic's group and taps t of
+    w[ic, oc - g*C_out/G, t] * y[oc, i*s - p + t].  Rows (ic, i), columns (oc, o)."""
+    C_in, cout_g, k = w.shape
+    cin_g = C_in // G
+    A = np.zeros((C_in * L_in, cout_g * G * L_out))
+    for ic in range(C_in):
+        g = ic // cin_g
+        for i in range(L_in):
+            for ocl in range(cout_g):
+                oc = g * cout_g + ocl
+                for t in range(k):
+                    o = i * s - p + t
+                    if 0 <= o < L_out:
+                        A[ic * L_in + i, oc * L_out + o] += w[ic, ocl, t]
+    return A
+
+
+def pin_adjoint_groups(ct):
+    """Grouped ConvT is the adjoint of the grouped forward strided conv."""
+    for (L, k, s, p, op, C_in, C_out, G) in ((4, 3, 2, 1, 1, 4, 2, 2), (3, 4, 2, 1, 0, 3, 3, 3),
+                                             (5, 5, 3, 2, 2, 2, 4, 2)):
+        w = _rng.standard_normal((C_in, C_out // G, k))
+        L_out = (L - 1) * s - 2 * p + k + op
+        A = forward_conv_matrix_groups_1d(w, L, L_out, s, p, G)
+        yv = _rng.standard_normal((1, C_out, L_out))
+        ref = F.conv1d(torch.from_numpy(yv), torch.from_numpy(w), stride=s, padding=p,
+                       groups=G).numpy()
+        _close((A @ yv.reshape(-1)).reshape(1, C_in, -1), ref[:, :, :L])
+        M = np.zeros((C_out * L_out, C_in * L))
+        for j in range(C_in * L):
+            e = np.zeros(C_in * L)
+            e[j] = 1.0
+            M[:, j] = ct(e.reshape(1, C_in, L), w, None, s, p, op, groups=G).reshape(-1)
+        _close(M, A.T)
+
+
+ALL_PINS = [pin_torch_f64_groups, pin_depthwise_k_equals_s, pin_adjoint_groups,
+            pin_torch_f64_1d, pin_torch_f64_2d, pin_adjoint, pin_hand_cases, pin_matmul,
             pin_polyphase, pin_istft_sinusoid]

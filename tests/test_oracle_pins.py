@@ -124,8 +124,10 @@ def test_workload_shapes():
 MUTANTS = {
     "dropped_bias": ("const double bv = bias ? bias[oc] : 0.0;", "const double bv = 0.0;"),
     "padding_sign": ("const int64_t ox0 = ix * sw - pw;", "const int64_t ox0 = ix * sw + pw;"),
-    "transposed_weight": ("const double *wp = w + (ic * C_out + oc) * ntap;",
-                          "const double *wp = w + (oc * C_in + ic) * ntap;"),
+    "transposed_weight": ("const double *wp = w + (ic * cout_g + ocl) * ntap;",
+                          "const double *wp = w + (ocl * C_in + ic) * ntap;"),
+    "group_input_channels": ("for (int64_t ic = g * cin_g; ic < (g + 1) * cin_g; ++ic) {",
+                             "for (int64_t ic = 0; ic < cin_g; ++ic) {"),
     "flipped_taps": ("arow[tx] += xv * wrow[tx];", "arow[tx] += xv * wrow[kw - 1 - tx];"),
     "dropped_tap_term_y": ("const int64_t oy = iy * sh - ph + ty;",
                            "const int64_t oy = iy * sh - ph;"),
@@ -138,7 +140,8 @@ MUTANTS = {
 def _oracle_lib(path):
     lib = ctypes.CDLL(path)
     real = oracle._load()
-    for name in ("ctr_oracle_conv_transpose", "ctr_oracle_output_size", "ctr_oracle_landed_pairs"):
+    for name in ("ctr_oracle_conv_transpose", "ctr_oracle_conv_transpose_groups",
+                 "ctr_oracle_output_size", "ctr_oracle_landed_pairs"):
         getattr(lib, name).restype = getattr(real, name).restype
         getattr(lib, name).argtypes = getattr(real, name).argtypes
     saved = oracle._lib
