@@ -50,11 +50,16 @@ DEFAULT_WORKLOAD = "codec_upsampler_f32"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # Nominal dense tensor throughput relative to bf16 (tf32 1.1 vs bf16 2.25 PFLOP/s).
 TF32_OVER_BF16 = 1.1 / 2.25
-KERNEL_SOURCES = ["transposed_convolution_gb300/csrc/gemm_tc.cu",
-                  "transposed_convolution_gb300/csrc/epilogue.cuh",
-                  "transposed_convolution_gb300/csrc/ptx.cuh",
-                  "transposed_convolution_gb300/csrc/gemm_tc.cuh",
-                  "transposed_convolution_gb300/csrc/gemm_tc_chain.cu"]
+# The sources of each profiled kernel: a committed ncu summary holds their hash, and its
+# DRAM traffic is reported only while they are unchanged.
+KERNEL_SOURCES = {
+    "gemm_tc": ["transposed_convolution_gb300/csrc/gemm_tc.cu",
+                "transposed_convolution_gb300/csrc/epilogue.cuh",
+                "transposed_convolution_gb300/csrc/ptx.cuh",
+                "transposed_convolution_gb300/csrc/gemm_tc.cuh",
+                "transposed_convolution_gb300/csrc/gemm_tc_chain.cu"],
+    "depthwise": ["transposed_convolution_gb300/csrc/depthwise.cu"],
+}
 
 
 def dist_env():
@@ -72,26 +77,26 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(kernel="gemm_tc"):
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload, layer=0, layers=1):
-    """DRAM bytes per launch of a layer's GEMM kernel from the committed ncu summary, or None
+def profiled_traffic(workload, layer=0, layers=1, kernel="gemm_tc"):
+    """DRAM bytes per launch of a layer's main kernel from the committed ncu summary, or None
     when there is none or the kernel sources changed since it was taken."""
-    path = os.path.join(ROOT, "profiles", "gemm_tc_%s.md" % workload)
-    if not os.path.exists(path):
+    path = os.path.join(ROOT, "profiles", "%s_%s.md" % (kernel, workload))
+    if kernel not in KERNEL_SOURCES or not os.path.exists(path):
         return None
     vals = {}
     for line in open(path):
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
             vals[k.strip()] = v.strip().strip("`")
-    if vals.get("kernel_source_sha256") != kernel_source_hash():
+    if vals.get("kernel_source_sha256") != kernel_source_hash(kernel):
         return None
     key = "dram_bytes_per_launch" if layers == 1 else "dram_bytes_per_launch_layer%d" % layer
     try:
@@ -201,7 +206,8 @@ def run_ours(args, rank, world, local_rank):
 
     def make_plans():
         plans = [ctr.Plan(L.B, L.C_in, L.C_out, L.in_sp, L.kernel, L.stride, L.padding,
-                          L.output_padding, dtype=tdt, negative_slope=L.act_slope, device=dev)
+                          L.output_padding, dtype=tdt, negative_slope=L.act_slope, device=dev,
+                          groups=L.groups)
                  for L, tdt in zip(Ls, tdts)]
         # A stack of layers runs chained (each layer's output stage writes the next layer's
         # staged input) where the library allows it; --no-chain keeps every tensor in the
@@ -405,7 +411,8 @@ def run_ours(args, rank, world, local_rank):
         xin = layers[0].x
         errs = []
         for j, (li, L) in enumerate(zip(layers, Ls)):
-            ref = oracle.conv_transpose(xin, li.w, li.bias, L.stride, L.padding, L.output_padding)
+            ref = oracle.conv_transpose(xin, li.w, li.bias, L.stride, L.padding, L.output_padding,
+                                        groups=L.groups)
             if L.act_slope is not None:
                 ref = oracle.leaky_relu(ref, L.act_slope)
             if s["plans"][j].next_plan is not None:
@@ -447,9 +454,10 @@ def run_ours(args, rank, world, local_rank):
     else:
         achieved, peak, unit = L.compulsory_bytes / kern_s / 1e9, peaks["hbm_gbs"], "GB/s"
         peak_note = "HBM copy bandwidth, %s" % peak_src
-    traffic = profiled_traffic(args.workload, j, nl)
     clocks = sampler.summary(soak_t0, wall1 + 0.25)
-    kname = "gemm_tc_kernel" if sets[0]["plans"][j].path != ctr.CTR_PATH_GATHER else "gather_kernel"
+    kname = {ctr.CTR_PATH_GATHER: "gather_kernel", ctr.CTR_PATH_DEPTHWISE: "depthwise_kernel"}.get(
+        sets[0]["plans"][j].path, "gemm_tc_kernel")
+    traffic = profiled_traffic(args.workload, j, nl, kname[:-len("_kernel")])
 
     result = {
         "metric": "ConvTranspose GFLOP/s and % of roofline (tensor peak vs HBM) per call",
@@ -512,13 +520,14 @@ def oracle_sample(name, budget_s):
     # Shrink the last input dimension until one call is at most budget/3 seconds.
     for _ in range(12):
         t0 = time.time()
-        oracle.conv_transpose(x, li.w, li.bias, L.stride, L.padding, L.output_padding)
+        oracle.conv_transpose(x, li.w, li.bias, L.stride, L.padding, L.output_padding,
+                              groups=L.groups)
         dt = time.time() - t0
         if dt <= budget_s / 3 or x.shape[-1] <= 8:
             break
         x = x[..., : max(8, x.shape[-1] // 2)]
         desc = "input prefix %s of %s" % (x.shape[-1], L.in_sp[-1])
-    macs = L.B * L.C_in * L.C_out * int(np.prod(L.kernel))
+    macs = L.B * L.C_in * (L.C_out // L.groups) * int(np.prod(L.kernel))
     macs *= int(np.prod(x.shape[2:]))
     return dt, 2.0 * macs, desc, (x, li)
 
@@ -530,7 +539,8 @@ def time_oracle(name, budget_s=12.0):
     reps, total = 0, 0.0
     while total < budget_s and reps < 50:
         t0 = time.time()
-        oracle.conv_transpose(x, li.w, li.bias, L.stride, L.padding, L.output_padding)
+        oracle.conv_transpose(x, li.w, li.bias, L.stride, L.padding, L.output_padding,
+                              groups=L.groups)
         total += time.time() - t0
         reps += 1
     sec = total / reps
@@ -547,11 +557,13 @@ def run_reference(args, rank, world):
     _, flops, desc, (x, li) = oracle_sample(args.workload, 8.0)
     L = li.layer
     for _ in range(min(W, 1)):
-        oracle.conv_transpose(x, li.w, li.bias, L.stride, L.padding, L.output_padding)
+        oracle.conv_transpose(x, li.w, li.bias, L.stride, L.padding, L.output_padding,
+                              groups=L.groups)
     times = []
     for _ in range(K):
         t0 = time.time()
-        oracle.conv_transpose(x, li.w, li.bias, L.stride, L.padding, L.output_padding)
+        oracle.conv_transpose(x, li.w, li.bias, L.stride, L.padding, L.output_padding,
+                              groups=L.groups)
         times.append(time.time() - t0)
         if sum(times) > 120:
             break

@@ -80,7 +80,8 @@ typedef enum {
     CTR_PATH_AUTO = 0,
     CTR_PATH_POLYPHASE = 1,      /* polyphase implicit GEMM on tcgen05 (taps zero-padded to m*s) */
     CTR_PATH_COL2IM = 2,         /* tcgen05 GEMM into an fp32 column buffer, then col2im */
-    CTR_PATH_GATHER = 3          /* direct gather on CUDA cores */
+    CTR_PATH_GATHER = 3,         /* direct gather on CUDA cores (any groups) */
+    CTR_PATH_DEPTHWISE = 4       /* depthwise (groups = C_in = C_out) kernel on CUDA cores */
 } ctr_path;
 
 /*
@@ -103,6 +104,19 @@ ctr_status ctr_plan_create(ctr_plan_t *out, int ndim, int64_t N, int64_t C_in, i
                            const int64_t *in_spatial, const int64_t *kernel,
                            const int64_t *stride, const int64_t *padding,
                            const int64_t *output_padding, int dtype);
+
+/*
+ * Grouped transposed convolution (default 1 group): groups must divide C_in and C_out; the
+ * weight is then [C_in][C_out/groups][k...] and output channel oc sums only the input
+ * channels of its group ("[ExecuTorch][WebGPU] Add optimized conv2d op", Implementation:
+ * the [IC, OC/groups, KH, KW] weight).  groups = C_in = C_out is the depthwise case, run by
+ * a dedicated kernel ("[XNNPACK] Lower dense transposed convs as one polyphase conv + depth
+ * to space", DecomposeDepthwiseConvTransposePass commit: depthwise upsampling filters);
+ * other groups > 1 run on the gather path; the tensor-core paths need one group.  Host only,
+ * same ordering rule as ctr_plan_set_path; CTR_ERR_INVALID_ARG when groups does not divide
+ * both channel counts, after ctr_prepack_weight, or on a chained plan.
+ */
+ctr_status ctr_plan_set_groups(ctr_plan_t plan, int64_t groups);
 
 /* Fuse an activation into the output stage (default CTR_ACT_NONE).  Host only. */
 ctr_status ctr_plan_set_activation(ctr_plan_t plan, int act, float negative_slope);

@@ -5,6 +5,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -46,13 +47,15 @@ def _plan(ctr, *args, **kw):
 
 def test_output_shapes_and_paths_of_the_workloads(ctr):
     import workloads
-    expect_path = {"tiny_1d_f32": ctr.CTR_PATH_GATHER}
+    expect_path = {"tiny_1d_f32": ctr.CTR_PATH_GATHER, "depthwise_2d_bf16": ctr.CTR_PATH_DEPTHWISE}
     for name, layers in workloads.WORKLOADS.items():
         for layer in layers:
             h = _plan(ctr, layer.ndim, layer.B, layer.C_in, layer.C_out, layer.in_sp, layer.kernel,
                       layer.stride, layer.padding, layer.output_padding,
                       ctr.CTR_BF16 if layer.dtype == "bf16" else ctr.CTR_F32)
             try:
+                if layer.groups != 1:
+                    ctr.ctr_plan_set_groups(h, layer.groups)
                 assert ctr.ctr_plan_output_shape(h, layer.ndim) == layer.out_sp
                 assert ctr.ctr_plan_get_path(h) == expect_path.get(name, ctr.CTR_PATH_POLYPHASE)
                 if ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_POLYPHASE:
@@ -166,3 +169,76 @@ def test_chain_validation_without_gpu(ctr):
         ctr.ctr_plan_destroy(b)          # unchains a
         for h in (a, c, d, e):
             ctr.ctr_plan_destroy(h)
+
+
+def test_groups_routing_without_gpu(ctr):
+    """ctr_plan_set_groups: groups must divide both channel counts; groups = C_in runs on the
+    depthwise kernel where its x kernel/stride is compiled, other groups on the gather kernel;
+    the tensor-core paths and the depthwise kernel refuse plans they cannot run, leaving the
+    plan as it was; the packed weight is the grouped torch weight."""
+    bf = ctr.CTR_BF16
+    h = _plan(ctr, 1, 1, 64, 64, [100], [4], [2], [1], [0], bf)
+    try:
+        for bad in (0, -1, 3, 128):
+            assert ctr.lib.ctr_plan_set_groups(h, bad) == ctr.CTR_ERR_INVALID_ARG
+        assert ctr.lib.ctr_plan_set_path(h, ctr.CTR_PATH_DEPTHWISE, 0) == ctr.CTR_ERR_UNSUPPORTED
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_POLYPHASE
+        ctr.ctr_plan_set_groups(h, 64)
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_DEPTHWISE
+        assert ctr.ctr_packed_weight_bytes(h) == 64 * 1 * 4 * 2
+        assert ctr.ctr_workspace_bytes(h) == 0
+        assert "path=depthwise" in ctr.ctr_plan_describe(h)
+        assert "groups=64" in ctr.ctr_plan_describe(h)
+        for p in (ctr.CTR_PATH_POLYPHASE, ctr.CTR_PATH_COL2IM):
+            assert ctr.lib.ctr_plan_set_path(h, p, 0) == ctr.CTR_ERR_UNSUPPORTED
+            assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_DEPTHWISE
+        ctr.ctr_plan_set_path(h, ctr.CTR_PATH_GATHER, 0)
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_GATHER
+        # a forced gather path stays when the groups change; back to one group re-plans
+        ctr.ctr_plan_set_groups(h, 8)
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_GATHER
+        assert ctr.ctr_packed_weight_bytes(h) == 64 * 8 * 4 * 2
+        ctr.ctr_plan_set_path(h, ctr.CTR_PATH_AUTO, 0)
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_GATHER
+        ctr.ctr_plan_set_groups(h, 1)
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_POLYPHASE
+        # a forced tensor-core path refuses groups
+        ctr.ctr_plan_set_path(h, ctr.CTR_PATH_POLYPHASE, 0)
+        assert ctr.lib.ctr_plan_set_groups(h, 64) == ctr.CTR_ERR_UNSUPPORTED
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_POLYPHASE
+        assert ctr.ctr_packed_weight_bytes(h) > 64 * 64 * 4 * 2 // 2
+    finally:
+        ctr.ctr_plan_destroy(h)
+    cases = [  # (ndim, C_in, C_out, groups, in, k, s, p, op, path)
+        (1, 32, 64, 32, [50], [4], [2], [1], [0], ctr.CTR_PATH_DEPTHWISE),     # multiplier 2
+        (2, 16, 16, 16, [20, 20], [4, 4], [2, 2], [1, 1], [0, 0], ctr.CTR_PATH_DEPTHWISE),
+        (2, 16, 16, 16, [20, 20], [3, 3], [2, 2], [1, 1], [1, 1], ctr.CTR_PATH_DEPTHWISE),
+        (2, 16, 16, 16, [20, 20], [5, 16], [3, 8], [2, 4], [0, 0], ctr.CTR_PATH_GATHER),
+        (2, 16, 16, 16, [20, 20], [8, 8], [4, 4], [2, 2], [0, 0], ctr.CTR_PATH_GATHER),
+        (1, 16, 16, 16, [50], [5], [2], [1], [0], ctr.CTR_PATH_GATHER),        # x kernel 5
+        (1, 16, 16, 16, [50], [3], [1], [1], [0], ctr.CTR_PATH_GATHER),        # x stride 1
+        (1, 16, 32, 8, [50], [4], [2], [1], [0], ctr.CTR_PATH_GATHER),         # 2 ch per group
+    ]
+    for nd, ci, co, g, sp, k, s, p, op, path in cases:
+        h = _plan(ctr, nd, 2, ci, co, sp, k, s, p, op, ctr.CTR_F32)
+        try:
+            ctr.ctr_plan_set_groups(h, g)
+            assert ctr.ctr_plan_get_path(h) == path, (nd, ci, co, g, k, s)
+            taps = int(np.prod(k))
+            assert ctr.ctr_packed_weight_bytes(h) == ci * (co // g) * taps * 4
+        finally:
+            ctr.ctr_plan_destroy(h)
+    # chained plans keep one group; a grouped plan does not chain
+    a = _plan(ctr, 1, 1, 64, 32, [100], [4], [2], [1], [0], bf)
+    b = _plan(ctr, 1, 1, 32, 64, [200], [4], [2], [1], [0], bf)
+    c = _plan(ctr, 1, 1, 32, 32, [200], [4], [2], [1], [0], bf)
+    try:
+        ctr.ctr_plan_chain(a, b)
+        assert ctr.lib.ctr_plan_set_groups(a, 2) == ctr.CTR_ERR_INVALID_ARG
+        assert ctr.lib.ctr_plan_set_groups(b, 2) == ctr.CTR_ERR_INVALID_ARG
+        ctr.ctr_plan_chain(a, None)
+        ctr.ctr_plan_set_groups(c, 32)
+        assert ctr.lib.ctr_plan_chain(a, c) == ctr.CTR_ERR_INVALID_ARG
+    finally:
+        for x in (a, b, c):
+            ctr.ctr_plan_destroy(x)

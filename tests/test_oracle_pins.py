@@ -108,7 +108,7 @@ def test_leaky_relu_and_rel_l2():
 
 
 def test_workload_shapes():
-    """Output sizes and the useful-MAC counts of the five workloads."""
+    """Output sizes, useful-MAC counts and compulsory bytes of the workloads."""
     L = workloads.WORKLOADS
     assert L["tiny_1d_f32"][0].out_sp == (128,)
     assert L["codec_upsampler_f32"][0].out_sp == (16000,)
@@ -117,6 +117,11 @@ def test_workload_shapes():
     assert [l.out_sp for l in L["vocoder_stack_bf16"]] == [(8192,), (65536,), (131072,), (262144,)]
     assert 2 * L["codec_upsampler_f32"][0].useful_macs == 8388608000
     assert 2 * L["istft_f32"][0].useful_macs == 46059159552
+    dw = L["depthwise_2d_bf16"][0]
+    assert dw.out_sp == (256, 256)
+    assert 2 * dw.useful_macs == 2 * 4 * 256 * 16 * 128 * 128     # one channel per group
+    assert dw.compulsory_bytes == 2 * (4 * 256 * 128 * 128 + 256 * 16 + 256 + 4 * 256 * 256 * 256)
+    assert workloads.make_layer_inputs(dw, 1).w.shape == (256, 1, 4, 4)
 
 
 # ---------------------------------------------------------------- planted mistakes

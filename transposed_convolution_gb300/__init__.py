@@ -6,7 +6,7 @@ PyTorch fallback: if the library has not been built the first call raises Import
 any non-OK status from the library raises ``CtrError``.
 
 Low level (same names as the C ABI): ``ctr_plan_create``, ``ctr_plan_set_activation``,
-``ctr_plan_set_path``, ``ctr_plan_set_tile``, ``ctr_plan_chain``, ``ctr_plan_get_path``, ``ctr_plan_output_shape``,
+``ctr_plan_set_path``, ``ctr_plan_set_groups``, ``ctr_plan_set_tile``, ``ctr_plan_chain``, ``ctr_plan_get_path``, ``ctr_plan_output_shape``,
 ``ctr_packed_weight_bytes``, ``ctr_workspace_bytes``, ``ctr_plan_bind_workspace``,
 ``ctr_prepack_weight``, ``ctr_forward``, ``ctr_forward_noalloc``, ``ctr_plan_check``,
 ``ctr_plan_set_wait_limit_ns``,
@@ -40,7 +40,9 @@ CTR_PATH_AUTO = 0
 CTR_PATH_POLYPHASE = 1
 CTR_PATH_COL2IM = 2
 CTR_PATH_GATHER = 3
-PATH_NAMES = {CTR_PATH_POLYPHASE: "polyphase", CTR_PATH_COL2IM: "col2im", CTR_PATH_GATHER: "gather"}
+CTR_PATH_DEPTHWISE = 4
+PATH_NAMES = {CTR_PATH_POLYPHASE: "polyphase", CTR_PATH_COL2IM: "col2im", CTR_PATH_GATHER: "gather",
+              CTR_PATH_DEPTHWISE: "depthwise"}
 
 # Every symbol include/ctr.h declares, with (restype, argtypes).
 _vp = ctypes.c_void_p
@@ -51,6 +53,7 @@ SIGNATURES = {
                                        _i64p, ctypes.c_int]),
     "ctr_plan_set_activation": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_float]),
     "ctr_plan_set_path": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int]),
+    "ctr_plan_set_groups": (ctypes.c_int, [_vp, ctypes.c_int64]),
     "ctr_plan_set_tile": (ctypes.c_int, [_vp, ctypes.c_int]),
     "ctr_plan_chain": (ctypes.c_int, [_vp, _vp]),
     "ctr_plan_get_path": (ctypes.c_int, [_vp]),
@@ -148,6 +151,10 @@ def ctr_plan_set_activation(plan, act, negative_slope=0.0):
 
 def ctr_plan_set_path(plan, path, split_k=0):
     _check(lib.ctr_plan_set_path(plan, int(path), int(split_k)), "ctr_plan_set_path")
+
+
+def ctr_plan_set_groups(plan, groups):
+    _check(lib.ctr_plan_set_groups(plan, int(groups)), "ctr_plan_set_groups")
 
 
 def ctr_plan_set_tile(plan, block_n):
@@ -258,7 +265,7 @@ class Plan:
 
     def __init__(self, N, C_in, C_out, in_spatial, kernel, stride=1, padding=0,
                  output_padding=0, dtype=None, negative_slope=None, path=CTR_PATH_AUTO,
-                 split_k=0, device=None, block_n=0):
+                 split_k=0, device=None, block_n=0, groups=1):
         torch = _torch()
         self.ndim = len(in_spatial)
         self.dtype = dtype if dtype is not None else torch.float32
@@ -269,12 +276,15 @@ class Plan:
         self.stride = _tuple(stride, self.ndim)
         self.padding = _tuple(padding, self.ndim)
         self.output_padding = _tuple(output_padding, self.ndim)
+        self.groups = int(groups)
         self.handle = ctr_plan_create(self.ndim, self.N, self.C_in, self.C_out, self.in_spatial,
                                       self.kernel, self.stride, self.padding,
                                       self.output_padding, _dtype_code(self.dtype))
         try:
             if negative_slope is not None:
                 ctr_plan_set_activation(self.handle, CTR_ACT_LEAKY_RELU, negative_slope)
+            if self.groups != 1:
+                ctr_plan_set_groups(self.handle, self.groups)
             if path != CTR_PATH_AUTO or split_k:
                 ctr_plan_set_path(self.handle, path, split_k)
             if block_n:
@@ -304,9 +314,9 @@ class Plan:
         return ctr_plan_describe(self.handle)
 
     def prepack(self, w, stream=None):
-        """Pack the weight [C_in, C_out, k...] (device, plan dtype) into self.w_packed."""
+        """Pack the weight [C_in, C_out/groups, k...] (device, plan dtype) into self.w_packed."""
         torch = _torch()
-        w = self._checked(w, (self.C_in, self.C_out) + self.kernel, "w")
+        w = self._checked(w, (self.C_in, self.C_out // self.groups) + self.kernel, "w")
         self.w_packed = torch.empty(max(self.packed_bytes, 16), dtype=torch.uint8,
                                     device=self.device)
         ctr_prepack_weight(self.handle, _ptr(w), _ptr(self.w_packed), _stream_ptr(stream))
@@ -381,21 +391,22 @@ _plan_cache = {}
 
 
 def conv_transpose(x, w, bias=None, stride=1, padding=0, output_padding=0, negative_slope=None,
-                   path=CTR_PATH_AUTO, split_k=0):
+                   path=CTR_PATH_AUTO, split_k=0, groups=1):
     """ConvTranspose1d/2d of torch CUDA tensors (float32 or bfloat16), like
-    torch.nn.functional.conv_transpose{1,2}d with groups = 1 and dilation = 1, plus an
-    optional fused LeakyReLU.  Plans and packed weights are cached per (shapes, weight)."""
+    torch.nn.functional.conv_transpose{1,2}d with dilation = 1, plus an optional fused
+    LeakyReLU.  Plans and packed weights are cached per (shapes, weight)."""
     ndim = x.dim() - 2
     key = (tuple(x.shape), tuple(w.shape), x.dtype, str(x.device), w.data_ptr(), w._version,
            _tuple(stride, ndim), _tuple(padding, ndim), _tuple(output_padding, ndim),
-           negative_slope, path, split_k)
+           negative_slope, path, split_k, groups)
     plan = _plan_cache.get(key)
     if plan is None:
         if len(_plan_cache) > 64:
             _plan_cache.clear()
-        plan = Plan(x.shape[0], x.shape[1], w.shape[1], tuple(x.shape[2:]), tuple(w.shape[2:]),
-                    stride, padding, output_padding, dtype=x.dtype, negative_slope=negative_slope,
-                    path=path, split_k=split_k, device=x.device)
+        plan = Plan(x.shape[0], x.shape[1], w.shape[1] * groups, tuple(x.shape[2:]),
+                    tuple(w.shape[2:]), stride, padding, output_padding, dtype=x.dtype,
+                    negative_slope=negative_slope, path=path, split_k=split_k, device=x.device,
+                    groups=groups)
         plan.prepack(w.contiguous())
         _plan_cache[key] = plan
     return plan.forward(x.contiguous(), None if bias is None else bias.contiguous())

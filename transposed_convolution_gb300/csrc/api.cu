@@ -147,8 +147,10 @@ void layout_plan(ctr_plan_s *pl) {
     pl->splits = 1;
     pl->block_n = 0;
     pl->num_tiles = 0;
-    if (pl->path == CTR_PATH_GATHER) {
-        pl->packed_bytes = (size_t)(pl->C_in * pl->C_out * pl->k[0] * pl->k[1]) * esize_io(pl);
+    if (pl->path == CTR_PATH_GATHER || pl->path == CTR_PATH_DEPTHWISE) {
+        // The torch weight [C_in][C_out/groups][k...], copied as is.
+        pl->packed_bytes =
+            (size_t)(pl->C_in * (pl->C_out / pl->groups) * pl->k[0] * pl->k[1]) * esize_io(pl);
         pl->S = pl->S_pad = 0;
         return;
     }
@@ -212,6 +214,8 @@ bool tc_index_fits(const ctr_plan_s *pl) {
 
 int choose_path(const ctr_plan_s *pl) {
     if (pl->forced_path != CTR_PATH_AUTO) return pl->forced_path;
+    if (pl->groups > 1)   // the tensor-core paths contract over all input channels
+        return ctr::depthwise_supported(pl) ? CTR_PATH_DEPTHWISE : CTR_PATH_GATHER;
     const bool kdiv = (pl->k[0] % pl->s[0] == 0) && (pl->k[1] % pl->s[1] == 0);
     const int64_t S = pl->s[0] * pl->s[1];
     const int64_t mprod = ceil_div(pl->k[0], pl->s[0]) * ceil_div(pl->k[1], pl->s[1]);
@@ -473,6 +477,7 @@ ctr_status ctr_plan_create(ctr_plan_t *out, int ndim, int64_t N, int64_t C_in, i
     pl->forced_path = CTR_PATH_AUTO;
     pl->forced_split = 0;
     pl->forced_bn = 0;
+    pl->groups = 1;
     pl->chain_next = pl->chain_prev = nullptr;
     pl->chain_zeroed_ws = nullptr;
     pl->wait_limit_ns = 4000000000ull;
@@ -521,20 +526,58 @@ ctr_status ctr_plan_set_activation(ctr_plan_t pl, int act, float slope) {
     return CTR_OK;
 }
 
-ctr_status ctr_plan_set_path(ctr_plan_t pl, int path, int split_k) {
-    if (!pl || path < CTR_PATH_AUTO || path > CTR_PATH_GATHER || split_k < 0 || split_k > 16)
-        return CTR_ERR_INVALID_ARG;
-    if (pl->prepared) return CTR_ERR_INVALID_ARG;
-    pl->forced_path = path;
-    pl->forced_split = split_k;
+// Whether the plan's geometry and groups can run on a forced path.
+bool path_supported(const ctr_plan_s *pl, int path) {
+    if (path == CTR_PATH_DEPTHWISE) return ctr::depthwise_supported(pl);
+    if (is_tc_path(path)) return pl->groups == 1;
+    return true;
+}
+
+// Re-derive the path and layout after a setting changed; a forced path the plan cannot take
+// leaves the previous settings in place and reports CTR_ERR_UNSUPPORTED.
+ctr_status reroute(ctr_plan_s *pl, int forced_path, int forced_split, int64_t groups) {
+    const int old_path = pl->forced_path, old_split = pl->forced_split;
+    const int64_t old_groups = pl->groups;
+    pl->forced_path = forced_path;
+    pl->forced_split = forced_split;
+    pl->groups = groups;
+    bool ok = forced_path == CTR_PATH_AUTO || path_supported(pl, forced_path);
+    if (ok) {
+        pl->path = choose_path(pl);
+        layout_plan(pl);
+        if (is_tc_path(pl->path) && !tc_index_fits(pl)) {
+            ok = forced_path == CTR_PATH_AUTO;
+            if (ok) {
+                pl->path = CTR_PATH_GATHER;
+                layout_plan(pl);
+            }
+        }
+    }
+    if (ok) return CTR_OK;
+    pl->forced_path = old_path;
+    pl->forced_split = old_split;
+    pl->groups = old_groups;
     pl->path = choose_path(pl);
     layout_plan(pl);
     if (is_tc_path(pl->path) && !tc_index_fits(pl)) {
-        if (path != CTR_PATH_AUTO) return CTR_ERR_UNSUPPORTED;
         pl->path = CTR_PATH_GATHER;
         layout_plan(pl);
     }
-    return CTR_OK;
+    return CTR_ERR_UNSUPPORTED;
+}
+
+ctr_status ctr_plan_set_path(ctr_plan_t pl, int path, int split_k) {
+    if (!pl || path < CTR_PATH_AUTO || path > CTR_PATH_DEPTHWISE || split_k < 0 || split_k > 16)
+        return CTR_ERR_INVALID_ARG;
+    if (pl->prepared) return CTR_ERR_INVALID_ARG;
+    return reroute(pl, path, split_k, pl->groups);
+}
+
+ctr_status ctr_plan_set_groups(ctr_plan_t pl, int64_t groups) {
+    if (!pl || groups < 1 || pl->C_in % groups != 0 || pl->C_out % groups != 0)
+        return CTR_ERR_INVALID_ARG;
+    if (pl->prepared || pl->chain_next || pl->chain_prev) return CTR_ERR_INVALID_ARG;
+    return reroute(pl, pl->forced_path, pl->forced_split, groups);
 }
 
 ctr_status ctr_plan_set_tile(ctr_plan_t pl, int block_n) {
@@ -582,9 +625,10 @@ ctr_status ctr_plan_set_timing_events(ctr_plan_t pl, void *before, void *after) 
 
 ctr_status ctr_plan_describe(ctr_plan_t pl, char *buf, size_t len) {
     if (!pl || !buf || len == 0) return CTR_ERR_INVALID_ARG;
-    const char *pname = pl->path == CTR_PATH_POLYPHASE ? "polyphase"
-                        : pl->path == CTR_PATH_COL2IM  ? "col2im"
-                                                       : "gather";
+    const char *pname = pl->path == CTR_PATH_POLYPHASE    ? "polyphase"
+                        : pl->path == CTR_PATH_COL2IM     ? "col2im"
+                        : pl->path == CTR_PATH_DEPTHWISE  ? "depthwise"
+                                                          : "gather";
     if (is_tc_path(pl->path)) {
         const EpiParams ep = make_epi(pl, nullptr, nullptr);
         snprintf(buf, len,
@@ -599,8 +643,8 @@ ctr_status ctr_plan_describe(ctr_plan_t pl, char *buf, size_t len) {
                  (long long)pl->P[0], (long long)pl->P[1], ep.kind, ep.store_bytes,
                  pl->packed_bytes, pl->ws_bytes_needed);
     } else {
-        snprintf(buf, len, "path=%s dtype=%s packed=%zu ws=0", pname,
-                 pl->dtype == CTR_BF16 ? "bf16" : "f32", pl->packed_bytes);
+        snprintf(buf, len, "path=%s dtype=%s groups=%lld packed=%zu ws=0", pname,
+                 pl->dtype == CTR_BF16 ? "bf16" : "f32", (long long)pl->groups, pl->packed_bytes);
     }
     return CTR_OK;
 }
@@ -617,8 +661,8 @@ ctr_status ctr_prepack_weight(ctr_plan_t pl, const void *w, void *w_packed, void
         }
         if (cudaMemset(pl->d_status, 0, sizeof(uint32_t)) != cudaSuccess) return CTR_ERR_CUDA;
     }
-    cudaError_t e = pl->path == CTR_PATH_GATHER ? ctr::launch_copy_weight(pl, w, w_packed, st)
-                                                : ctr::launch_prepack(pl, w, w_packed, st);
+    cudaError_t e = is_tc_path(pl->path) ? ctr::launch_prepack(pl, w, w_packed, st)
+                                         : ctr::launch_copy_weight(pl, w, w_packed, st);
     if (e != cudaSuccess) return CTR_ERR_CUDA;
     pl->prepared = 1;
     return CTR_OK;
@@ -651,9 +695,12 @@ ctr_status ctr_forward(ctr_plan_t pl, const void *x, const void *w_packed, const
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     const bool timed = pl->ev_before != nullptr;
-    if (pl->path == CTR_PATH_GATHER) {
+    if (!is_tc_path(pl->path)) {
         if (timed && ctr::record_timing(pl->ev_before, st) != cudaSuccess) return CTR_ERR_CUDA;
-        if (ctr::launch_gather(pl, x, w_packed, bias, y, st) != cudaSuccess) return CTR_ERR_CUDA;
+        const cudaError_t e = pl->path == CTR_PATH_DEPTHWISE
+                                  ? ctr::launch_depthwise(pl, x, w_packed, bias, y, st)
+                                  : ctr::launch_gather(pl, x, w_packed, bias, y, st);
+        if (e != cudaSuccess) return CTR_ERR_CUDA;
         if (timed && ctr::record_timing(pl->ev_after, st) != cudaSuccess) return CTR_ERR_CUDA;
         return CTR_OK;
     }

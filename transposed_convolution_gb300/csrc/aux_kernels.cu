@@ -3,7 +3,7 @@
 //   stage_x      NC(H)W input -> channels-last rows with zero halos (tf32 hi/lo or bf16)
 //   splitk_reduce  fixed-order sum of split-K partials, then the fused output stage
 //   col2im       gather of the valid taps from the fp32 column buffer
-//   gather       direct ConvTranspose for tiny channel counts
+//   gather       direct ConvTranspose for tiny channel counts and grouped convolutions
 //   fill_bias    y = bias (or zeros) for an empty input on the col2im path
 //   copy_weight  the gather path's "packed" weight (a plain copy)
 #include <algorithm>
@@ -30,6 +30,7 @@ unsigned grid_for(int64_t n, int block) {
 // Geometry of a plan as plain values for the kernels below (2-D form).
 struct Geo {
     int64_t B, C_in, C_out;
+    int64_t cin_g, cout_g;    // channels per group
     int64_t H, W, ky, kx, sy, sx, py, px, Ho, Wo;
     int act;
     float slope;
@@ -41,6 +42,8 @@ Geo geo_of(const ctr_plan_s *pl) {
     g.B = pl->B;
     g.C_in = pl->C_in;
     g.C_out = pl->C_out;
+    g.cin_g = pl->C_in / pl->groups;
+    g.cout_g = pl->C_out / pl->groups;
     g.H = pl->in[0];
     g.W = pl->in[1];
     g.ky = pl->k[0];
@@ -58,10 +61,12 @@ Geo geo_of(const ctr_plan_s *pl) {
 }
 
 // -------------------------------------------------------------------------- gather
-// y[b, oc, oy, ox] = bias[oc] + sum over ic and the taps that reach (oy, ox): a tap ty
-// contributes when (oy + py - ty) is a multiple of sy and the quotient is a valid input row
-// ("[ExecuTorch][WebGPU] Add optimized conv2d op", Implementation: the gather form with the
-// un-flipped weight).  fp32 accumulation on CUDA cores; one thread per output element.
+// y[b, oc, oy, ox] = bias[oc] + sum over the input channels of oc's group and the taps that
+// reach (oy, ox): a tap ty contributes when (oy + py - ty) is a multiple of sy and the
+// quotient is a valid input row ("[ExecuTorch][WebGPU] Add optimized conv2d op",
+// Implementation: the gather form with the un-flipped weight, laid out [IC][OC/groups][k]).
+// fp32 accumulation on CUDA cores, starting from the bias, taps in ascending (ty, tx) order;
+// one thread per output element.
 __global__ void gather_kernel(const void *__restrict__ x, const void *__restrict__ w,
                               const void *__restrict__ bias, void *__restrict__ y, Geo g,
                               int64_t total) {
@@ -73,7 +78,8 @@ __global__ void gather_kernel(const void *__restrict__ x, const void *__restrict
         t /= g.Ho;
         const int64_t oc = t % g.C_out;
         const int64_t b = t / g.C_out;
-        float acc = 0.0f;
+        const int64_t grp = oc / g.cout_g, ic0 = grp * g.cin_g;
+        float acc = bias ? load_io(bias, oc, g.bf16) : 0.0f;
         const int64_t ry = oy + g.py, rx = ox + g.px;
         for (int64_t ty = ry % g.sy; ty < g.ky; ty += g.sy) {
             const int64_t iy = (ry - ty) / g.sy;
@@ -83,16 +89,16 @@ __global__ void gather_kernel(const void *__restrict__ x, const void *__restrict
                 const int64_t ix = (rx - tx) / g.sx;
                 if (ix < 0) break;
                 if (ix >= g.W) continue;
-                const int64_t xoff = ((b * g.C_in) * g.H + iy) * g.W + ix;
-                const int64_t woff = ((oc * g.ky) + ty) * g.kx + tx;
+                const int64_t xoff = ((b * g.C_in + ic0) * g.H + iy) * g.W + ix;
+                const int64_t woff =
+                    (((ic0 * g.cout_g + oc - grp * g.cout_g) * g.ky) + ty) * g.kx + tx;
                 const int64_t xstride = g.H * g.W;
-                const int64_t wstride = g.C_out * g.ky * g.kx;
-                for (int64_t ic = 0; ic < g.C_in; ++ic)
+                const int64_t wstride = g.cout_g * g.ky * g.kx;
+                for (int64_t ic = 0; ic < g.cin_g; ++ic)
                     acc = fmaf(load_io(x, xoff + ic * xstride, g.bf16),
                                load_io(w, woff + ic * wstride, g.bf16), acc);
             }
         }
-        if (bias) acc += load_io(bias, oc, g.bf16);
         store_io(y, idx, apply_act(acc, g.act, g.slope), g.bf16);
     }
 }

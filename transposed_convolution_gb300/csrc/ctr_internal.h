@@ -98,6 +98,7 @@ struct ctr_plan_s {
     int forced_path;
     int forced_split;
     int forced_bn;      // 0 = automatic phase-row tile
+    int64_t groups;     // ctr_plan_set_groups (1 = dense)
     int prepared;       // ctr_prepack_weight ran (status word allocated)
     int num_sms;
 
@@ -186,6 +187,11 @@ int64_t raw_split_stride_of(const ctr_plan_s *pl);
 cudaError_t launch_col2im(const ctr_plan_s *pl, const float *col, int64_t col_ld,
                           const void *bias, void *y, cudaStream_t st);
 cudaError_t launch_fill_bias(const ctr_plan_s *pl, const void *bias, void *y, cudaStream_t st);
+// One input channel per group (groups = C_in, C_out a multiple of it): the depthwise kernel,
+// for the x-direction kernel sizes and strides it is compiled for.
+bool depthwise_supported(const ctr_plan_s *pl);
+cudaError_t launch_depthwise(const ctr_plan_s *pl, const void *x, const void *w, const void *bias,
+                             void *y, cudaStream_t st);
 cudaError_t launch_gemm_tc(const ctr_plan_s *pl, const CUtensorMap *maps, const GemmParams &gp,
                            cudaStream_t st);
 

@@ -77,6 +77,8 @@ extern "C" ctr_status ctr_forward_noalloc(ctr_plan_t pl, const void *x, const vo
         // The gather kernel reads the weight in its torch layout; no scratch is needed.
         return ctr::launch_gather(pl, x, w, bias, y, st) == cudaSuccess ? CTR_OK : CTR_ERR_CUDA;
     }
+    if (pl->path == CTR_PATH_DEPTHWISE)   // so does the depthwise kernel
+        return ctr::launch_depthwise(pl, x, w, bias, y, st) == cudaSuccess ? CTR_OK : CTR_ERR_CUDA;
     void *w_packed = scratch + packed_off;
     if (ctr::launch_prepack(pl, w, w_packed, st) != cudaSuccess) return CTR_ERR_CUDA;
     if (pl->N_total == 0)

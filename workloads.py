@@ -3,14 +3,17 @@
 This module only draws inputs and describes shapes.  It holds none of the convolution's
 arithmetic, and both the CPU oracle and the CUDA path take their inputs from here.
 
-The five workloads stand in for the audio decoders the source pages measure (codec and
-vocoder upsamplers with kernel = 2*stride and the iSTFT overlap-add of a source-separation
-model, "[XNNPACK] Lower dense transposed convs as one polyphase conv + depth to space",
-Summary; "[WebGPU] optimizations for audio models", ConvTranspose commit).  Their trained
-weights and audio are not available, so every tensor is drawn from a seeded generator:
+The first five workloads stand in for the audio decoders the source pages measure (codec
+and vocoder upsamplers with kernel = 2*stride and the iSTFT overlap-add of a
+source-separation model, "[XNNPACK] Lower dense transposed convs as one polyphase conv +
+depth to space", Summary; "[WebGPU] optimizations for audio models", ConvTranspose commit).
+The sixth is the depthwise 4x4 / stride-2 upsampling filter of the image-inpainting network
+the XNNPACK page profiles (DecomposeDepthwiseConvTransposePass commit), at a feature-map
+size chosen to be bound by HBM.  Trained weights, audio and images are not available, so
+every tensor is drawn from a seeded generator:
 
-* x ~ N(0, 1); w ~ U(-1/sqrt(C_in * prod(k)), +1/sqrt(C_in * prod(k))); bias ~ N(0, 0.1)
-  (0.1 read as the standard deviation);
+* x ~ N(0, 1); w ~ U(-1/sqrt(fan_in), +1/sqrt(fan_in)) with fan_in = (C_in / groups) *
+  prod(k); bias ~ N(0, 0.1) (0.1 read as the standard deviation);
 * values are drawn in double and rounded to the I/O precision (fp32, or bf16 with ties to
   even), so both sides see the same exact values;
 * the iSTFT weight is the periodic-Hann-windowed inverse real-DFT basis (N = 4096), with the
@@ -43,6 +46,7 @@ class Layer:
     bias: bool = True
     act_slope: Optional[float] = None   # LeakyReLU negative slope, None = no activation
     weight: str = "uniform"          # "uniform" or "istft"
+    groups: int = 1                  # groups = C_in = C_out: depthwise
 
     @property
     def out_sp(self) -> Tuple[int, ...]:
@@ -51,9 +55,9 @@ class Layer:
 
     @property
     def useful_macs(self) -> int:
-        """B * C_in * C_out * prod(L_in * k): the GEMM count of the X[M, C_in] x
-        W[C_in, k*C_out] formulation."""
-        n = self.B * self.C_in * self.C_out
+        """B * C_in * (C_out / groups) * prod(L_in * k): the GEMM count of the X[M, C_in] x
+        W[C_in, k*C_out] formulation, per group."""
+        n = self.B * self.C_in * (self.C_out // self.groups)
         for d in range(self.ndim):
             n *= self.in_sp[d] * self.kernel[d]
         return n
@@ -67,7 +71,7 @@ class Layer:
         """x + w + bias + y, each once, in the I/O dtype."""
         e = self.elem_bytes
         nx = self.B * self.C_in * int(np.prod(self.in_sp))
-        nw = self.C_in * self.C_out * int(np.prod(self.kernel))
+        nw = self.C_in * (self.C_out // self.groups) * int(np.prod(self.kernel))
         nb = self.C_out if self.bias else 0
         ny = self.B * self.C_out * int(np.prod(self.out_sp))
         return e * (nx + nw + nb + ny)
@@ -77,7 +81,8 @@ class Layer:
         ks = "x".join(str(v) for v in self.kernel)
         ss = "x".join(str(v) for v in self.stride)
         ps = "x".join(str(v) for v in self.padding)
-        return (f"{self.ndim}d B{self.B} {self.C_in}->{self.C_out} L{dims} k{ks} s{ss} p{ps} "
+        g = f" groups{self.groups}" if self.groups != 1 else ""
+        return (f"{self.ndim}d B{self.B} {self.C_in}->{self.C_out}{g} L{dims} k{ks} s{ss} p{ps} "
                 f"{self.dtype}")
 
 
@@ -100,14 +105,16 @@ def _stack() -> List[Layer]:
     return layers
 
 
-# The five workloads, in order.  Index 0 is the tiny case, index 1 the codec upsampler the
-# benchmark times at one GPU.
+# The workloads, in order.  Index 0 is the tiny case, index 1 the codec upsampler the
+# benchmark times at one GPU by default.
 WORKLOADS = {
     "tiny_1d_f32": [_l1(1, 16, 8, 64, 4, 2, 1)],
     "codec_upsampler_f32": [_l1(1, 512, 256, 2000, 16, 8, 4)],
     "istft_f32": [_l1(4, 4098, 1, 343, 4096, 1024, 0, bias=False, weight="istft")],
     "decoder_2d_f32": [Layer(2, 1, 128, 64, (128, 128), (4, 4), (2, 2), (1, 1), (0, 0))],
     "vocoder_stack_bf16": _stack(),
+    "depthwise_2d_bf16": [Layer(2, 4, 256, 256, (128, 128), (4, 4), (2, 2), (1, 1), (0, 0),
+                                dtype="bf16", groups=256)],
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 
@@ -199,9 +206,9 @@ def make_layer_inputs(layer: Layer, seed: int, with_x: bool = True) -> LayerInpu
         assert layer.ndim == 1 and layer.C_out == 1 and layer.C_in == layer.kernel[0] + 2
         w = _cast(istft_basis(layer.kernel[0]), layer.dtype)
     else:
-        a = 1.0 / math.sqrt(layer.C_in * int(np.prod(layer.kernel)))
-        w = _cast(rng.uniform(-a, a, (layer.C_in, layer.C_out) + tuple(layer.kernel)),
-                  layer.dtype)
+        cin_g, cout_g = layer.C_in // layer.groups, layer.C_out // layer.groups
+        a = 1.0 / math.sqrt(cin_g * int(np.prod(layer.kernel)))
+        w = _cast(rng.uniform(-a, a, (layer.C_in, cout_g) + tuple(layer.kernel)), layer.dtype)
     bias = None
     if layer.bias:
         bias = _cast(rng.normal(0.0, 0.1, (layer.C_out,)), layer.dtype)
