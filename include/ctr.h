@@ -35,7 +35,7 @@
  *     allocate, free or synchronise.
  *   - Tensors are contiguous, row-major, in the plan's I/O dtype:
  *         x    [N][C_in][L_in]            or [N][C_in][H][W]
- *         w    [C_in][C_out][k]           or [C_in][C_out][kH][kW]
+ *         w    [C_in][C_out/G][k]         or [C_in][C_out/G][kH][kW]   (G groups, default 1)
  *         bias [C_out]                    (may be NULL)
  *         y    [N][C_out][L_out]          or [N][C_out][H_out][W_out]
  *     and each must start on a 16-byte boundary (CTR_ERR_MISALIGNED otherwise).
@@ -81,7 +81,7 @@ typedef enum {
     CTR_PATH_POLYPHASE = 1,      /* polyphase implicit GEMM on tcgen05 (taps zero-padded to m*s) */
     CTR_PATH_COL2IM = 2,         /* tcgen05 GEMM into an fp32 column buffer, then col2im */
     CTR_PATH_GATHER = 3,         /* direct gather on CUDA cores (any groups) */
-    CTR_PATH_DEPTHWISE = 4       /* depthwise (groups = C_in = C_out) kernel on CUDA cores */
+    CTR_PATH_DEPTHWISE = 4       /* one input channel per group (groups = C_in), CUDA cores */
 } ctr_path;
 
 /*
@@ -109,10 +109,13 @@ ctr_status ctr_plan_create(ctr_plan_t *out, int ndim, int64_t N, int64_t C_in, i
  * Grouped transposed convolution (default 1 group): groups must divide C_in and C_out; the
  * weight is then [C_in][C_out/groups][k...] and output channel oc sums only the input
  * channels of its group ("[ExecuTorch][WebGPU] Add optimized conv2d op", Implementation:
- * the [IC, OC/groups, KH, KW] weight).  groups = C_in = C_out is the depthwise case, run by
- * a dedicated kernel ("[XNNPACK] Lower dense transposed convs as one polyphase conv + depth
- * to space", DecomposeDepthwiseConvTransposePass commit: depthwise upsampling filters);
- * other groups > 1 run on the gather path; the tensor-core paths need one group.  Host only,
+ * the [IC, OC/groups, KH, KW] weight).  groups = C_in (C_out = M * C_in; M = 1 is the
+ * depthwise upsampler of "[XNNPACK] Lower dense transposed convs as one polyphase conv +
+ * depth to space", DecomposeDepthwiseConvTransposePass commit) runs on the depthwise path
+ * (CTR_PATH_DEPTHWISE) for 1-D kernels with k/s in {2/2, 3/2, 4/2, 4/4, 8/4, 8/8, 16/8} and
+ * square 2-D kernels 2x2/2, 3x3/2, 4x4/2, 4x4/4; other grouped plans run on the gather path.
+ * The tensor-core paths need one group: forcing one on a grouped plan, or grouping a plan
+ * forced onto one, returns CTR_ERR_UNSUPPORTED and leaves the plan unchanged.  Host only,
  * same ordering rule as ctr_plan_set_path; CTR_ERR_INVALID_ARG when groups does not divide
  * both channel counts, after ctr_prepack_weight, or on a chained plan.
  */
@@ -129,6 +132,9 @@ ctr_status ctr_plan_set_activation(ctr_plan_t plan, int act, float negative_slop
  * The tensor-core paths index tiles, staged input positions and packed weight rows in 32
  * bits: a plan that exceeds 2^31 of any of them runs the gather path when chosen
  * automatically, and forcing a tensor-core path on it returns CTR_ERR_UNSUPPORTED.
+ * CTR_PATH_DEPTHWISE needs groups = C_in and a compiled geometry (ctr_plan_set_groups),
+ * and the tensor-core paths one group; a path the plan cannot take returns
+ * CTR_ERR_UNSUPPORTED and leaves the plan unchanged.
  */
 ctr_status ctr_plan_set_path(ctr_plan_t plan, int path, int split_k);
 
@@ -187,7 +193,7 @@ ctr_status ctr_plan_bind_workspace(ctr_plan_t plan, void *dev_ptr, size_t bytes)
 
 /*
  * Pack a weight for this plan (once per weight; asynchronous on stream).
- *   w         device, [C_in][C_out][k...] in the plan's dtype
+ *   w         device, [C_in][C_out/groups][k...] in the plan's dtype
  *   w_packed  device, ctr_packed_weight_bytes(plan) bytes, written in full
  * The packed weight is valid only for plans with the same geometry, dtype and path.  The
  * first call on a plan also allocates the plan's 4-byte device status word on the current
