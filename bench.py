@@ -59,6 +59,7 @@ KERNEL_SOURCES = {
                 "transposed_convolution_gb300/csrc/gemm_tc.cuh",
                 "transposed_convolution_gb300/csrc/gemm_tc_chain.cu"],
     "depthwise": ["transposed_convolution_gb300/csrc/depthwise.cu"],
+    "istft": ["transposed_convolution_gb300/csrc/istft.cu"],
 }
 
 
@@ -205,7 +206,9 @@ def run_ours(args, rank, world, local_rank):
     x_dev = t(layers[0].x, tdts[0])
 
     def make_plans():
-        plans = [ctr.Plan(L.B, L.C_in, L.C_out, L.in_sp, L.kernel, L.stride, L.padding,
+        plans = [ctr.Istft(L.B, L.kernel[0], L.stride[0], L.in_sp[0], L.padding[0],
+                           L.output_padding[0], device=dev) if L.kind == "istft" else
+                 ctr.Plan(L.B, L.C_in, L.C_out, L.in_sp, L.kernel, L.stride, L.padding,
                           L.output_padding, dtype=tdt, negative_slope=L.act_slope, device=dev,
                           groups=L.groups)
                  for L, tdt in zip(Ls, tdts)]
@@ -252,14 +255,13 @@ def run_ours(args, rank, world, local_rank):
         inp = s["x"] if x is None else x
         for li_idx, p in enumerate(s["plans"]):
             if kevs is not None:
-                ctr.ctr_plan_set_timing_events(p.handle, kevs[li_idx][0].cuda_event,
-                                               kevs[li_idx][1].cuda_event)
+                p.set_timing_events(kevs[li_idx][0].cuda_event, kevs[li_idx][1].cuda_event)
             if p.next_plan is not None:
                 p.forward(inp, s["b"][li_idx])
             else:
                 p.forward(inp, s["b"][li_idx], y=s["y"][li_idx])
             if kevs is not None:
-                ctr.ctr_plan_set_timing_events(p.handle, None, None)
+                p.set_timing_events(None, None)
             inp = None if p.next_plan is not None else s["y"][li_idx]
         return inp
 
@@ -411,8 +413,8 @@ def run_ours(args, rank, world, local_rank):
         xin = layers[0].x
         errs = []
         for j, (li, L) in enumerate(zip(layers, Ls)):
-            ref = oracle.conv_transpose(xin, li.w, li.bias, L.stride, L.padding, L.output_padding,
-                                        groups=L.groups)
+            ref = oracle.conv_transpose(xin, oracle_weight(li), li.bias, L.stride, L.padding,
+                                        L.output_padding, groups=L.groups)
             if L.act_slope is not None:
                 ref = oracle.leaky_relu(ref, L.act_slope)
             if s["plans"][j].next_plan is not None:
@@ -437,15 +439,19 @@ def run_ours(args, rank, world, local_rank):
                 "3xTF32: %s bf16 burst x nominal tf32/bf16 (1.1/2.25) / 3 products per useful "
                 "MAC" % peak_src)
 
+    def layer_t_tensor(L, pk):
+        # The FFT path's arithmetic is far below the dense contraction it replaces: bytes only.
+        return 0.0 if L.kind == "istft" else 2.0 * L.useful_macs / (pk * 1e12)
+
     t_roof = 0.0
     for L in Ls:
         pk, _ = layer_peak(L)
-        t_roof += max(2.0 * L.useful_macs / (pk * 1e12), L.compulsory_bytes / (peaks["hbm_gbs"] * 1e9))
+        t_roof += max(layer_t_tensor(L, pk), L.compulsory_bytes / (peaks["hbm_gbs"] * 1e9))
     # Dominant kernel: the layer whose main kernel takes longest.
     j = max(range(nl), key=lambda q: kern_ms[q])
     L = Ls[j]
     pk, peak_note = layer_peak(L)
-    t_tensor = 2.0 * L.useful_macs / (pk * 1e12)
+    t_tensor = layer_t_tensor(L, pk)
     t_hbm = L.compulsory_bytes / (peaks["hbm_gbs"] * 1e9)
     bound = "tensor" if t_tensor >= t_hbm else "hbm"
     kern_s = kern_ms[j] / 1e3
@@ -455,9 +461,11 @@ def run_ours(args, rank, world, local_rank):
         achieved, peak, unit = L.compulsory_bytes / kern_s / 1e9, peaks["hbm_gbs"], "GB/s"
         peak_note = "HBM copy bandwidth, %s" % peak_src
     clocks = sampler.summary(soak_t0, wall1 + 0.25)
-    kname = {ctr.CTR_PATH_GATHER: "gather_kernel", ctr.CTR_PATH_DEPTHWISE: "depthwise_kernel"}.get(
-        sets[0]["plans"][j].path, "gemm_tc_kernel")
-    traffic = profiled_traffic(args.workload, j, nl, kname[:-len("_kernel")])
+    kname = {ctr.CTR_PATH_GATHER: "gather_kernel", ctr.CTR_PATH_DEPTHWISE: "depthwise_kernel",
+             -1: "irfft_frames_kernel+istft_ola_kernel"}.get(sets[0]["plans"][j].path,
+                                                               "gemm_tc_kernel")
+    traffic = profiled_traffic(args.workload, j, nl,
+                               "istft" if kname.startswith("irfft") else kname[:-len("_kernel")])
 
     result = {
         "metric": "ConvTranspose GFLOP/s and % of roofline (tensor peak vs HBM) per call",
@@ -479,7 +487,10 @@ def run_ours(args, rank, world, local_rank):
                    "chained_layers": sum(p.next_plan is not None for p in sets[0]["plans"]),
                    "launch": ("one CUDA graph of the K steps" if graph is not None
                               else "plain calls") + "; kernel times from a second K-step run",
-                   "plan": " | ".join(p.describe() for p in sets[0]["plans"])},
+                   "plan": " | ".join(p.describe() for p in sets[0]["plans"]),
+                   **({"flop_count": "the dense ConvTranspose (DFT-basis contraction) that the "
+                                     "inverse FFTs compute"}
+                      if any(L.kind == "istft" for L in Ls) else {})},
         "pct_of_roofline": round(100.0 * t_roof / (ms_per_step / 1e3), 2),
         "roofline_us": round(t_roof * 1e6, 3),
         "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 2),
@@ -508,6 +519,13 @@ def run_ours(args, rank, world, local_rank):
 
 # ------------------------------------------------------------------ oracle (CPU) arm
 
+def oracle_weight(li):
+    """The ConvTranspose weight the oracle takes: the layer's own, or for an inverse-FFT
+    layer the windowed inverse real-DFT basis its window implies."""
+    L = li.layer
+    return workloads.istft_basis(L.kernel[0], li.w) if L.kind == "istft" else li.w
+
+
 def oracle_sample(name, budget_s):
     """Time the oracle on a bounded sample of the workload: the first layer on a prefix of
     the input positions (all of them when that fits the budget).  Returns (seconds per
@@ -516,11 +534,12 @@ def oracle_sample(name, budget_s):
     li = workloads.make_workload(name)[0]
     L = li.layer
     x = li.x
+    w = oracle_weight(li)
     desc = "full layer"
     # Shrink the last input dimension until one call is at most budget/3 seconds.
     for _ in range(12):
         t0 = time.time()
-        oracle.conv_transpose(x, li.w, li.bias, L.stride, L.padding, L.output_padding,
+        oracle.conv_transpose(x, w, li.bias, L.stride, L.padding, L.output_padding,
                               groups=L.groups)
         dt = time.time() - t0
         if dt <= budget_s / 3 or x.shape[-1] <= 8:
@@ -529,17 +548,17 @@ def oracle_sample(name, budget_s):
         desc = "input prefix %s of %s" % (x.shape[-1], L.in_sp[-1])
     macs = L.B * L.C_in * (L.C_out // L.groups) * int(np.prod(L.kernel))
     macs *= int(np.prod(x.shape[2:]))
-    return dt, 2.0 * macs, desc, (x, li)
+    return dt, 2.0 * macs, desc, (x, li, w)
 
 
 def time_oracle(name, budget_s=12.0):
     import oracle
-    dt, flops, desc, (x, li) = oracle_sample(name, budget_s)
+    dt, flops, desc, (x, li, w) = oracle_sample(name, budget_s)
     L = li.layer
     reps, total = 0, 0.0
     while total < budget_s and reps < 50:
         t0 = time.time()
-        oracle.conv_transpose(x, li.w, li.bias, L.stride, L.padding, L.output_padding,
+        oracle.conv_transpose(x, w, li.bias, L.stride, L.padding, L.output_padding,
                               groups=L.groups)
         total += time.time() - t0
         reps += 1
@@ -554,15 +573,15 @@ def run_reference(args, rank, world):
         return None
     K, W = args.steps, args.warmup
     import oracle
-    _, flops, desc, (x, li) = oracle_sample(args.workload, 8.0)
+    _, flops, desc, (x, li, w) = oracle_sample(args.workload, 8.0)
     L = li.layer
     for _ in range(min(W, 1)):
-        oracle.conv_transpose(x, li.w, li.bias, L.stride, L.padding, L.output_padding,
+        oracle.conv_transpose(x, w, li.bias, L.stride, L.padding, L.output_padding,
                               groups=L.groups)
     times = []
     for _ in range(K):
         t0 = time.time()
-        oracle.conv_transpose(x, li.w, li.bias, L.stride, L.padding, L.output_padding,
+        oracle.conv_transpose(x, w, li.bias, L.stride, L.padding, L.output_padding,
                               groups=L.groups)
         times.append(time.time() - t0)
         if sum(times) > 120:

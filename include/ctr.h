@@ -280,6 +280,49 @@ const char *ctr_status_string(ctr_status status);
  * for benchmarks and tests). */
 uint64_t ctr_launch_count(void);
 
+/* ------------------------------------------------------------------------------------
+ * Inverse STFT through an inverse real FFT.
+ *
+ * The same result as ctr_forward on a 1-D plan with C_in = n_fft + 2, C_out = 1, kernel
+ * n_fft, stride hop and the windowed inverse real-DFT basis as weight: channel f of the
+ * input holds the real part of bin f (0 <= f <= n_fft/2), channel n_fft/2 + 1 + f its
+ * imaginary part, and the weight rows are c_f win[t] cos(2 pi f t/N) / N and
+ * -c_f win[t] sin(2 pi f t/N) / N (c_0 = c_{N/2} = 1, else 2).  "[WebGPU] optimizations for
+ * audio models" computes the source-separation model's inverse STFT as that ConvTranspose1d;
+ * here each frame is an inverse real FFT (O(n_fft log n_fft) instead of O(n_fft^2)), times
+ * the window, and the frames are overlap-added at stride hop, sliced by the padding, plus
+ * an optional scalar bias.
+ *
+ *   spec  device, [N][n_fft + 2][frames], fp32 (16-byte aligned)
+ *   y     device, [N][1][L_out], fp32, L_out = (frames - 1)*hop - 2*padding + n_fft
+ *         + output_padding (16-byte aligned)
+ *   window  device, [n_fft] fp32 synthesis window (16-byte aligned)
+ *   bias  device, [1] fp32 or NULL
+ *
+ * n_fft is a power of two in [4, 8192]; hop >= 1; 0 <= output_padding < hop; padding >= 0.
+ * fp32 only: CTR_BF16 returns CTR_ERR_UNSUPPORTED.  The plan owns no device memory: the
+ * caller binds a workspace of ctr_istft_workspace_bytes (twiddles, the scaled window and the
+ * windowed frames, fp32 [N][frames][n_fft]) and sets the window once (a kernel on `stream`);
+ * ctr_istft_forward then launches two kernels (the per-frame FFT, then the overlap-add as a
+ * gather, summing frames in ascending order: deterministic) and never allocates or
+ * synchronises.  Errors as for the ConvTranspose plan; CTR_ERR_NOT_PREPARED before
+ * ctr_istft_set_window (rebinding the workspace clears it).
+ * ------------------------------------------------------------------------------------ */
+typedef struct ctr_istft_s *ctr_istft_t;
+
+ctr_status ctr_istft_create(ctr_istft_t *out, int64_t N, int64_t n_fft, int64_t hop,
+                            int64_t frames, int64_t padding, int64_t output_padding, int dtype);
+ctr_status ctr_istft_output_length(ctr_istft_t plan, int64_t *L_out);
+size_t ctr_istft_workspace_bytes(ctr_istft_t plan);
+ctr_status ctr_istft_bind_workspace(ctr_istft_t plan, void *workspace, size_t bytes);
+ctr_status ctr_istft_set_window(ctr_istft_t plan, const void *window, void *stream);
+ctr_status ctr_istft_forward(ctr_istft_t plan, const void *spec, const void *bias, void *y,
+                             void *stream);
+ctr_status ctr_istft_describe(ctr_istft_t plan, char *buf, size_t len);
+/* As ctr_plan_set_timing_events, around both kernels of ctr_istft_forward. */
+ctr_status ctr_istft_set_timing_events(ctr_istft_t plan, void *before, void *after);
+void ctr_istft_destroy(ctr_istft_t plan);
+
 #ifdef __cplusplus
 }
 #endif

@@ -242,3 +242,38 @@ def test_groups_routing_without_gpu(ctr):
     finally:
         for x in (a, b, c):
             ctr.ctr_plan_destroy(x)
+
+
+def test_istft_plan_without_gpu(ctr):
+    """ctr_istft_*: argument checks, output length, workspace size; no window -> not prepared."""
+    h = ctr.ctr_istft_create(4, 4096, 1024, 343)
+    try:
+        assert ctr.ctr_istft_output_length(h) == 354304
+        ws = ctr.ctr_istft_workspace_bytes(h)
+        assert ws >= 4 * 343 * 4096 * 4 + 4096 * 12
+        assert "n_fft=4096" in ctr.ctr_istft_describe(h)
+        assert ctr.lib.ctr_istft_bind_workspace(h, ctypes.c_void_p(4096 + 8), ws) == \
+            ctr.CTR_ERR_MISALIGNED
+        assert ctr.lib.ctr_istft_bind_workspace(h, ctypes.c_void_p(4096), ws - 1) == \
+            ctr.CTR_ERR_NO_WORKSPACE
+        st = ctr.lib.ctr_istft_forward(h, ctypes.c_void_p(256), None, ctypes.c_void_p(256), None)
+        assert st == ctr.CTR_ERR_NO_WORKSPACE
+        ctr.ctr_istft_bind_workspace(h, ctypes.c_void_p(4096), ws)
+        st = ctr.lib.ctr_istft_forward(h, ctypes.c_void_p(256), None, ctypes.c_void_p(256), None)
+        assert st == ctr.CTR_ERR_NOT_PREPARED
+        assert ctr.lib.ctr_istft_set_timing_events(h, ctypes.c_void_p(16), None) == \
+            ctr.CTR_ERR_INVALID_ARG
+    finally:
+        ctr.ctr_istft_destroy(h)
+    assert ctr.ctr_istft_output_length(ctr.ctr_istft_create(1, 8, 2, 0)) == 6   # (0-1)*2 + 8
+    for bad in [(1, 6, 2, 3, 0, 0), (1, 2, 1, 3, 0, 0), (1, 16384, 4, 3, 0, 0), (1, 16, 0, 3, 0, 0),
+                (1, 16, 4, 3, 0, 4), (1, 16, 4, -1, 0, 0), (-1, 16, 4, 3, 0, 0),
+                (1, 16, 4, 1, 8, 0)]:
+        with pytest.raises(ctr.CtrError) as e:
+            ctr.ctr_istft_create(*bad)
+        assert e.value.status == ctr.CTR_ERR_INVALID_ARG, bad
+    with pytest.raises(ctr.CtrError) as e:
+        ctr.ctr_istft_create(1, 16, 4, 3, 0, 0, ctr.CTR_BF16)
+    assert e.value.status == ctr.CTR_ERR_UNSUPPORTED
+    assert ctr.lib.ctr_istft_workspace_bytes(None) == 0
+    ctr.ctr_istft_destroy(None)

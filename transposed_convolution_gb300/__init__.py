@@ -13,8 +13,14 @@ Low level (same names as the C ABI): ``ctr_plan_create``, ``ctr_plan_set_activat
 ``ctr_plan_set_timing_events``, ``ctr_plan_describe``, ``ctr_plan_destroy``,
 ``ctr_status_string``, ``ctr_launch_count``.
 
-High level: ``Plan`` (a plan with its packed weight and workspace held as torch tensors) and
-``conv_transpose(x, w, bias, stride, padding, output_padding, negative_slope)``.
+Inverse STFT (same names as the C ABI): ``ctr_istft_create``, ``ctr_istft_output_length``,
+``ctr_istft_workspace_bytes``, ``ctr_istft_bind_workspace``, ``ctr_istft_set_window``,
+``ctr_istft_forward``, ``ctr_istft_describe``, ``ctr_istft_set_timing_events``,
+``ctr_istft_destroy``.
+
+High level: ``Plan`` (a plan with its packed weight and workspace held as torch tensors),
+``Istft`` (an inverse-STFT plan with its workspace), and
+``conv_transpose(x, w, bias, stride, padding, output_padding, negative_slope, groups)``.
 """
 from __future__ import annotations
 
@@ -71,6 +77,17 @@ SIGNATURES = {
     "ctr_plan_destroy": (None, [_vp]),
     "ctr_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "ctr_launch_count": (ctypes.c_uint64, []),
+    "ctr_istft_create": (ctypes.c_int, [ctypes.POINTER(_vp), ctypes.c_int64, ctypes.c_int64,
+                                        ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                        ctypes.c_int64, ctypes.c_int]),
+    "ctr_istft_output_length": (ctypes.c_int, [_vp, _i64p]),
+    "ctr_istft_workspace_bytes": (ctypes.c_size_t, [_vp]),
+    "ctr_istft_bind_workspace": (ctypes.c_int, [_vp, _vp, ctypes.c_size_t]),
+    "ctr_istft_set_window": (ctypes.c_int, [_vp, _vp, _vp]),
+    "ctr_istft_forward": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp]),
+    "ctr_istft_describe": (ctypes.c_int, [_vp, ctypes.c_char_p, ctypes.c_size_t]),
+    "ctr_istft_set_timing_events": (ctypes.c_int, [_vp, _vp, _vp]),
+    "ctr_istft_destroy": (None, [_vp]),
 }
 
 
@@ -225,6 +242,51 @@ def ctr_plan_destroy(plan):
     lib.ctr_plan_destroy(plan)
 
 
+def ctr_istft_create(N, n_fft, hop, frames, padding=0, output_padding=0, dtype=CTR_F32):
+    """Returns an inverse-STFT plan handle (int).  Raises CtrError on a non-OK status."""
+    h = _vp()
+    _check(lib.ctr_istft_create(ctypes.byref(h), int(N), int(n_fft), int(hop), int(frames),
+                                int(padding), int(output_padding), int(dtype)),
+           "ctr_istft_create")
+    return h.value
+
+
+def ctr_istft_output_length(plan) -> int:
+    v = ctypes.c_int64()
+    _check(lib.ctr_istft_output_length(plan, ctypes.byref(v)), "ctr_istft_output_length")
+    return int(v.value)
+
+
+def ctr_istft_workspace_bytes(plan) -> int:
+    return int(lib.ctr_istft_workspace_bytes(plan))
+
+
+def ctr_istft_bind_workspace(plan, ptr, nbytes):
+    _check(lib.ctr_istft_bind_workspace(plan, ptr, int(nbytes)), "ctr_istft_bind_workspace")
+
+
+def ctr_istft_set_window(plan, window_ptr, stream):
+    _check(lib.ctr_istft_set_window(plan, window_ptr, stream), "ctr_istft_set_window")
+
+
+def ctr_istft_forward(plan, spec_ptr, bias_ptr, y_ptr, stream):
+    _check(lib.ctr_istft_forward(plan, spec_ptr, bias_ptr, y_ptr, stream), "ctr_istft_forward")
+
+
+def ctr_istft_describe(plan) -> str:
+    buf = ctypes.create_string_buffer(256)
+    _check(lib.ctr_istft_describe(plan, buf, 256), "ctr_istft_describe")
+    return buf.value.decode()
+
+
+def ctr_istft_set_timing_events(plan, before, after):
+    _check(lib.ctr_istft_set_timing_events(plan, before, after), "ctr_istft_set_timing_events")
+
+
+def ctr_istft_destroy(plan):
+    lib.ctr_istft_destroy(plan)
+
+
 # ------------------------------------------------------------------ torch-level helpers
 
 def _torch():
@@ -355,6 +417,9 @@ class Plan:
     def check(self, stream=None):
         ctr_plan_check(self.handle, _stream_ptr(stream))
 
+    def set_timing_events(self, before, after):
+        ctr_plan_set_timing_events(self.handle, before, after)
+
     def set_wait_limit_ns(self, ns):
         ctr_plan_set_wait_limit_ns(self.handle, ns)
 
@@ -379,6 +444,77 @@ class Plan:
         if prv is not None:
             prv.next_plan = None
         self.next_plan = self.prev_plan = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Istft:
+    """An inverse-STFT plan (ctr_istft_*) with its workspace held as a torch tensor: the
+    ConvTranspose1d with the windowed inverse real-DFT basis, computed by inverse real FFTs.
+    spec [N, n_fft + 2, frames] (real parts of bins 0..n_fft/2, then imaginary parts) ->
+    y [N, 1, L_out], float32."""
+
+    def __init__(self, N, n_fft, hop, frames, padding=0, output_padding=0, device=None):
+        torch = _torch()
+        self.N, self.n_fft, self.hop, self.frames = int(N), int(n_fft), int(hop), int(frames)
+        self.device = torch.device(device if device is not None else "cuda")
+        self.dtype = torch.float32
+        self.handle = ctr_istft_create(N, n_fft, hop, frames, padding, output_padding, CTR_F32)
+        try:
+            self.L_out = ctr_istft_output_length(self.handle)
+            self.workspace_bytes = ctr_istft_workspace_bytes(self.handle)
+            self.workspace = torch.empty(max(self.workspace_bytes, 16), dtype=torch.uint8,
+                                         device=self.device)
+            ctr_istft_bind_workspace(self.handle, _ptr(self.workspace), self.workspace_bytes)
+        except Exception:
+            ctr_istft_destroy(self.handle)
+            self.handle = None
+            raise
+        self.out_shape = (self.N, 1, self.L_out)
+        self.window = None
+        # Plan-like attributes, so a caller can hold Istft and Plan objects in one list.
+        self.path = -1
+        self.packed_bytes = 0
+        self.next_plan = self.prev_plan = None
+
+    def set_window(self, window, stream=None):
+        """The synthesis window [n_fft] (float32, device); kept referenced by the plan."""
+        self.window = Plan._checked(self, window, (self.n_fft,), "window")
+        ctr_istft_set_window(self.handle, _ptr(self.window), _stream_ptr(stream))
+
+    prepack = set_window
+
+    def set_timing_events(self, before, after):
+        ctr_istft_set_timing_events(self.handle, before, after)
+
+    def check(self, stream=None):
+        """No device status: the inverse-STFT kernels have no waits that can time out."""
+
+    def forward(self, spec, bias=None, y=None, stream=None):
+        torch = _torch()
+        if self.window is None:
+            raise RuntimeError("Istft.forward before Istft.set_window")
+        spec = Plan._checked(self, spec, (self.N, self.n_fft + 2, self.frames), "spec")
+        if bias is not None:
+            bias = Plan._checked(self, bias, (1,), "bias")
+        if y is None:
+            y = torch.empty(self.out_shape, dtype=self.dtype, device=self.device)
+        else:
+            y = Plan._checked(self, y, self.out_shape, "y")
+        ctr_istft_forward(self.handle, _ptr(spec), _ptr(bias), _ptr(y), _stream_ptr(stream))
+        return y
+
+    def describe(self) -> str:
+        return ctr_istft_describe(self.handle)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            ctr_istft_destroy(self.handle)
+            self.handle = None
 
     def __del__(self):
         try:

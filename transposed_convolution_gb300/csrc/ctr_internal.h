@@ -213,6 +213,8 @@ cudaError_t run_tc_path(const ctr_plan_s *pl, const void *x, const void *w_packe
 
 // Counter of launched kernels (monotonic, process-wide).
 void count_launches(uint64_t n);
+// Records a caller's timing event (an external event node under stream capture).
+cudaError_t record_timing(cudaEvent_t ev, cudaStream_t st);
 
 // Bytes of dynamic shared memory a GEMM instantiation uses.
 size_t gemm_smem_bytes(Prec prec, int block_n);

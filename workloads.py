@@ -9,7 +9,8 @@ source-separation model, "[XNNPACK] Lower dense transposed convs as one polyphas
 depth to space", Summary; "[WebGPU] optimizations for audio models", ConvTranspose commit).
 The sixth is the depthwise 4x4 / stride-2 upsampling filter of the image-inpainting network
 the XNNPACK page profiles (DecomposeDepthwiseConvTransposePass commit), at a feature-map
-size chosen to be bound by HBM.  Trained weights, audio and images are not available, so
+size chosen to be bound by HBM.  The seventh is the iSTFT workload again, computed by
+inverse real FFTs (its weight input is the Hann window; the basis is implied).  Trained weights, audio and images are not available, so
 every tensor is drawn from a seeded generator:
 
 * x ~ N(0, 1); w ~ U(-1/sqrt(fan_in), +1/sqrt(fan_in)) with fan_in = (C_in / groups) *
@@ -47,6 +48,9 @@ class Layer:
     act_slope: Optional[float] = None   # LeakyReLU negative slope, None = no activation
     weight: str = "uniform"          # "uniform" or "istft"
     groups: int = 1                  # groups = C_in = C_out: depthwise
+    kind: str = "conv"               # "conv", or "istft": the same ConvTranspose with the
+                                     # windowed inverse real-DFT basis, computed by FFTs; its
+                                     # weight input is then the window [n_fft]
 
     @property
     def out_sp(self) -> Tuple[int, ...]:
@@ -72,6 +76,8 @@ class Layer:
         e = self.elem_bytes
         nx = self.B * self.C_in * int(np.prod(self.in_sp))
         nw = self.C_in * (self.C_out // self.groups) * int(np.prod(self.kernel))
+        if self.kind == "istft":
+            nw = self.kernel[0]        # the window; the basis is never materialised
         nb = self.C_out if self.bias else 0
         ny = self.B * self.C_out * int(np.prod(self.out_sp))
         return e * (nx + nw + nb + ny)
@@ -115,6 +121,8 @@ WORKLOADS = {
     "vocoder_stack_bf16": _stack(),
     "depthwise_2d_bf16": [Layer(2, 4, 256, 256, (128, 128), (4, 4), (2, 2), (1, 1), (0, 0),
                                 dtype="bf16", groups=256)],
+    "istft_irfft_f32": [_l1(4, 4098, 1, 343, 4096, 1024, 0, bias=False, weight="istft",
+                           kind="istft")],
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 
@@ -136,20 +144,26 @@ def _cast(a: np.ndarray, dtype: str) -> np.ndarray:
     return to_bf16_values(a32) if dtype == "bf16" else a32
 
 
-def istft_basis(n_fft: int = 4096) -> np.ndarray:
-    """Periodic-Hann-windowed inverse real-DFT basis as a ConvTranspose1d weight
-    [n_fft + 2, 1, n_fft] (float64).
+def hann_window(n_fft: int) -> np.ndarray:
+    """Periodic Hann window win[t] = 0.5 - 0.5 cos(2 pi t / N), float64."""
+    t = np.arange(n_fft, dtype=np.int64)
+    return 0.5 - 0.5 * np.cos(2.0 * np.pi * t / n_fft)
+
+
+def istft_basis(n_fft: int = 4096, window: Optional[np.ndarray] = None) -> np.ndarray:
+    """Windowed inverse real-DFT basis as a ConvTranspose1d weight [n_fft + 2, 1, n_fft]
+    (float64); the window defaults to the periodic Hann window.
 
     Channel f (0 <= f <= n_fft/2) carries c_f * win[t] * cos(2 pi f t / N) / N and channel
     n_fft/2 + 1 + f carries -c_f * win[t] * sin(2 pi f t / N) / N, with c_0 = c_{N/2} = 1,
-    other c_f = 2 and win[t] = 0.5 - 0.5 cos(2 pi t / N).  Feeding the real and imaginary
-    parts of a onesided spectrum into these channels gives the windowed inverse real DFT of
-    each frame; a stride of the hop length overlap-adds the frames.
+    other c_f = 2.  Feeding the real and imaginary parts of a onesided spectrum into these
+    channels gives the windowed inverse real DFT of each frame; a stride of the hop length
+    overlap-adds the frames.
     """
     N = n_fft
     nb = N // 2 + 1
     t = np.arange(N, dtype=np.int64)
-    win = 0.5 - 0.5 * np.cos(2.0 * np.pi * t / N)
+    win = hann_window(N) if window is None else np.asarray(window, dtype=np.float64)
     w = np.empty((2 * nb, 1, N), dtype=np.float64)
     for f in range(nb):
         c = 1.0 if f in (0, N // 2) else 2.0
@@ -202,7 +216,9 @@ def make_layer_inputs(layer: Layer, seed: int, with_x: bool = True) -> LayerInpu
     x = None
     if with_x:
         x = _cast(rng.standard_normal((layer.B, layer.C_in) + tuple(layer.in_sp)), layer.dtype)
-    if layer.weight == "istft":
+    if layer.kind == "istft":
+        w = _cast(hann_window(layer.kernel[0]), layer.dtype)
+    elif layer.weight == "istft":
         assert layer.ndim == 1 and layer.C_out == 1 and layer.C_in == layer.kernel[0] + 2
         w = _cast(istft_basis(layer.kernel[0]), layer.dtype)
     else:
