@@ -59,6 +59,8 @@ def _load():
             lib = ctypes.CDLL(build())
             lib.ctr_oracle_output_size.restype = ctypes.c_int64
             lib.ctr_oracle_output_size.argtypes = [ctypes.c_int64] * 5
+            lib.ctr_oracle_output_size_ex.restype = ctypes.c_int64
+            lib.ctr_oracle_output_size_ex.argtypes = [ctypes.c_int64] * 7
             lib.ctr_oracle_max_threads.restype = ctypes.c_int
             lib.ctr_oracle_landed_pairs.restype = ctypes.c_int64
             lib.ctr_oracle_landed_pairs.argtypes = [ctypes.c_int] + [_I64P] * 5
@@ -70,6 +72,10 @@ def _load():
             lib.ctr_oracle_conv_transpose_groups.argtypes = (
                 [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]
                 + [_I64P] * 5 + [_F64P] * 4)
+            lib.ctr_oracle_conv_transpose_ex.restype = ctypes.c_int
+            lib.ctr_oracle_conv_transpose_ex.argtypes = (
+                [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]
+                + [_I64P] * 7 + [_F64P] * 4)
             _lib = lib
     return _lib
 
@@ -92,9 +98,14 @@ def threads() -> int:
     return int(_load().ctr_oracle_max_threads())
 
 
-def output_size(L_in: int, k: int, s: int, p: int, op: int = 0) -> int:
-    """L_out = (L_in - 1)*s - 2p + k + op for one spatial dimension."""
-    return int(_load().ctr_oracle_output_size(L_in, k, s, p, op))
+def output_size(L_in: int, k: int, s: int, p: int, op: int = 0, d: int = 1,
+                p_end=None) -> int:
+    """L_out = (L_in - 1)*s + (k - 1)*d + 1 + op - p - p_end for one spatial dimension
+    (p_end defaults to p: then (L_in - 1)*s - 2p + k + op without dilation)."""
+    if d == 1 and p_end is None:
+        return int(_load().ctr_oracle_output_size(L_in, k, s, p, op))
+    return int(_load().ctr_oracle_output_size_ex(L_in, k, s, d, p, p if p_end is None else p_end,
+                                                 op))
 
 
 def landed_pairs(in_sp, kernel, stride, padding, output_padding=0) -> int:
@@ -109,12 +120,14 @@ def landed_pairs(in_sp, kernel, stride, padding, output_padding=0) -> int:
 
 
 def conv_transpose(x, w, bias=None, stride=1, padding=0, output_padding=0,
-                   groups=1) -> np.ndarray:
+                   groups=1, dilation=1, padding_end=None) -> np.ndarray:
     """ConvTranspose in double.
 
     x: [B, C_in, L] or [B, C_in, H, W]; w: [C_in, C_out/groups, k] or [C_in, C_out/groups,
     kH, kW] (un-flipped torch layout); bias: [C_out] or None; groups divides C_in and C_out
-    (groups = C_in = C_out is the depthwise case).  Inputs are converted to float64
+    (groups = C_in = C_out is the depthwise case).  ``padding`` is the front pad of each
+    spatial dimension and ``padding_end`` the back pad (default: the front pad, torch's
+    symmetric padding); ``dilation`` spaces the taps.  Inputs are converted to float64
     exactly (fp32 and bf16 values are representable).  Returns float64
     [B, C_out, L_out] / [B, C_out, H_out, W_out].
     """
@@ -130,8 +143,11 @@ def conv_transpose(x, w, bias=None, stride=1, padding=0, output_padding=0,
     k = w.shape[2:]
     s = _tuple(stride, ndim)
     p = _tuple(padding, ndim)
+    pe = p if padding_end is None else _tuple(padding_end, ndim)
+    d = _tuple(dilation, ndim)
     op = _tuple(output_padding, ndim)
-    out_sp = tuple(output_size(in_sp[d], k[d], s[d], p[d], op[d]) for d in range(ndim))
+    out_sp = tuple(output_size(in_sp[i], k[i], s[i], p[i], op[i], d[i], pe[i])
+                   for i in range(ndim))
     if min(out_sp) <= 0:
         raise ValueError("empty output for this geometry")
     y = np.empty((B, C_out) + out_sp, dtype=np.float64)
@@ -140,9 +156,16 @@ def conv_transpose(x, w, bias=None, stride=1, padding=0, output_padding=0,
         bias = np.ascontiguousarray(np.asarray(bias, dtype=np.float64))
         assert bias.shape == (C_out,)
         bptr = bias.ctypes.data_as(_F64P)
-    rc = _load().ctr_oracle_conv_transpose_groups(
-        ndim, B, C_in, C_out, G, _i64(in_sp), _i64(k), _i64(s), _i64(p), _i64(op),
-        x.ctypes.data_as(_F64P), w.ctypes.data_as(_F64P), bptr, y.ctypes.data_as(_F64P))
+    lib = _load()
+    if d == (1,) * ndim and pe == p:
+        rc = lib.ctr_oracle_conv_transpose_groups(
+            ndim, B, C_in, C_out, G, _i64(in_sp), _i64(k), _i64(s), _i64(p), _i64(op),
+            x.ctypes.data_as(_F64P), w.ctypes.data_as(_F64P), bptr, y.ctypes.data_as(_F64P))
+    else:
+        rc = lib.ctr_oracle_conv_transpose_ex(
+            ndim, B, C_in, C_out, G, _i64(in_sp), _i64(k), _i64(s), _i64(d), _i64(p), _i64(pe),
+            _i64(op), x.ctypes.data_as(_F64P), w.ctypes.data_as(_F64P), bptr,
+            y.ctypes.data_as(_F64P))
     if rc != 0:
         raise ValueError("oracle rejected the arguments (rc=%d)" % rc)
     return y

@@ -20,7 +20,14 @@ Each ``pin_*`` function takes the ConvTranspose callable under test (normally
 * ``pin_depthwise_k_equals_s`` -- depthwise with kernel = stride and no padding: every input
   sample times the channel's kernel, laid end to end (an outer product);
 * ``pin_adjoint_groups`` -- the transpose of a grouped forward strided convolution whose
-  dense matrix is built element by element (itself checked against torch's grouped conv1d).
+  dense matrix is built element by element (itself checked against torch's grouped conv1d);
+* ``pin_torch_f64_dilation`` -- torch's float64 ConvTranspose with dilation (1-D grid, 2-D
+  with unequal dilations, grouped);
+* ``pin_pad_slice`` -- separate front and back pads: the unpadded result (torch float64,
+  padding 0) with output_padding positions of bias appended, sliced by the two pads;
+* ``pin_adjoint_dilated`` -- the transpose of a dilated forward strided convolution with
+  separate front and back pads, its dense matrix built element by element (itself checked
+  against torch's conv1d on an explicitly padded input).
 
 ``tests/test_oracle_pins.py`` runs them on the oracle and, with mistakes planted in copies
 of the oracle source, shows that each planted mistake fails at least one of them.
@@ -50,12 +57,13 @@ def _close(a, b, rtol=1e-12, atol=1e-12):
     assert err <= atol + rtol * scale, "max abs err %.3g (scale %.3g)" % (err, scale)
 
 
-def _torch_ct(x, w, b, s, p, op, groups=1):
+def _torch_ct(x, w, b, s, p, op, groups=1, dilation=1):
     xt = torch.from_numpy(np.asarray(x, dtype=np.float64))
     wt = torch.from_numpy(np.asarray(w, dtype=np.float64))
     bt = None if b is None else torch.from_numpy(np.asarray(b, dtype=np.float64))
     fn = F.conv_transpose1d if xt.dim() == 3 else F.conv_transpose2d
-    return fn(xt, wt, bt, stride=s, padding=p, output_padding=op, groups=groups).numpy()
+    return fn(xt, wt, bt, stride=s, padding=p, output_padding=op, groups=groups,
+              dilation=dilation).numpy()
 
 
 def grid_1d(full=False):
@@ -159,8 +167,9 @@ def pin_hand_cases(ct):
             x = np.array(case["x"], dtype=np.float64)
         w = np.array(case["w"], dtype=np.float64)
         b = None if case["bias"] is None else np.array(case["bias"], dtype=np.float64)
+        extra = {k: tuple(case[k]) for k in ("dilation", "padding_end") if k in case}
         y = ct(x, w, b, tuple(case["stride"]), tuple(case["padding"]),
-               tuple(case["output_padding"]))
+               tuple(case["output_padding"]), **extra)
         np.testing.assert_array_equal(y, np.array(case["y"], dtype=np.float64),
                                       err_msg=case["name"])
 
@@ -319,6 +328,122 @@ def pin_adjoint_groups(ct):
         _close(M, A.T)
 
 
-ALL_PINS = [pin_torch_f64_groups, pin_depthwise_k_equals_s, pin_adjoint_groups,
+def grid_dilated_1d():
+    """(L_in, k, s, d, p, op) with d in 2..3, s in 1..3, k in 1..4, p in 0..(k-1)d,
+    op < max(s, d) (torch's limit) and L_out > 0."""
+    for d in (2, 3):
+        for s in range(1, 4):
+            for k in range(1, 5):
+                for p in range(0, (k - 1) * d + 1):
+                    for op in range(0, max(s, d)):
+                        for L in (1, 2, 4):
+                            if (L - 1) * s + (k - 1) * d + 1 + op - 2 * p > 0:
+                                yield L, k, s, d, p, op
+
+
+def pin_torch_f64_dilation(ct):
+    for n, (L, k, s, d, p, op) in enumerate(grid_dilated_1d()):
+        C_in, C_out = ((1, 1), (2, 3), (3, 2))[n % 3]
+        x = _rng.standard_normal((1 + n % 2, C_in, L))
+        w = _rng.standard_normal((C_in, C_out, k))
+        b = _rng.standard_normal(C_out) if n % 3 else None
+        _close(ct(x, w, b, s, p, op, dilation=d), _torch_ct(x, w, b, s, p, op, dilation=d))
+    for (H, W, ky, kx, sy, sx, dy, dx, py, px, opy, opx, G) in (
+            (3, 4, 3, 2, 2, 1, 2, 3, 1, 0, 1, 2, 1), (2, 3, 2, 3, 1, 2, 3, 1, 2, 1, 0, 1, 1),
+            (4, 2, 2, 2, 2, 2, 2, 2, 1, 1, 1, 0, 2), (2, 2, 3, 3, 3, 2, 1, 2, 0, 2, 2, 1, 3)):
+        C = 6
+        x = _rng.standard_normal((1, C, H, W))
+        w = _rng.standard_normal((C, C // G, ky, kx))
+        b = _rng.standard_normal(C)
+        args = ((sy, sx), (py, px), (opy, opx))
+        _close(ct(x, w, b, *args, groups=G, dilation=(dy, dx)),
+               _torch_ct(x, w, b, *args, groups=G, dilation=(dy, dx)))
+
+
+def _pad_slice_ref(x, w, b, s, d, pb, pe, op):
+    """The padding slice: torch's unpadded result (padding 0, no output_padding), op more
+    positions of bias (or zeros) at the back of every spatial dimension, then pb positions
+    cut at the front and pe at the back."""
+    full = _torch_ct(x, w, b, s, 0, 0, dilation=d)
+    nd = x.ndim - 2
+    bias_v = np.zeros(full.shape[1]) if b is None else np.asarray(b, dtype=np.float64)
+    grown = np.empty(full.shape[:2] + tuple(full.shape[2 + i] + op[i] for i in range(nd)))
+    grown[...] = bias_v.reshape((1, -1) + (1,) * nd)
+    grown[(slice(None), slice(None)) + tuple(slice(0, full.shape[2 + i]) for i in range(nd))] = full
+    return grown[(slice(None), slice(None)) +
+                 tuple(slice(pb[i], grown.shape[2 + i] - pe[i]) for i in range(nd))]
+
+
+def pin_pad_slice(ct):
+    n = 0
+    for (L, k, s, d) in itertools.product((1, 3, 4), (1, 2, 4), (1, 2, 3), (1, 2)):
+        full = (L - 1) * s + (k - 1) * d + 1
+        for pb in range(0, 3):
+            for pe in range(0, 3):
+                for op in range(0, max(s, d)):
+                    if full + op - pb - pe <= 0:
+                        continue
+                    n += 1
+                    C_in, C_out = ((1, 2), (3, 1), (2, 2))[n % 3]
+                    x = _rng.standard_normal((1, C_in, L))
+                    w = _rng.standard_normal((C_in, C_out, k))
+                    b = _rng.standard_normal(C_out) if n % 2 else None
+                    _close(ct(x, w, b, s, pb, op, dilation=d, padding_end=pe),
+                           _pad_slice_ref(x, w, b, (s,), (d,), (pb,), (pe,), (op,)))
+    for (H, W, ky, kx, sy, sx, dy, dx, pb, pe, op) in (
+            (3, 2, 2, 3, 2, 1, 1, 2, (0, 2), (1, 0), (1, 0)),
+            (2, 4, 3, 2, 1, 2, 2, 1, (2, 0), (0, 1), (0, 1)),
+            (4, 4, 4, 4, 2, 2, 1, 1, (1, 2), (2, 1), (1, 1))):
+        x = _rng.standard_normal((1, 2, H, W))
+        w = _rng.standard_normal((2, 3, ky, kx))
+        b = _rng.standard_normal(3)
+        _close(ct(x, w, b, (sy, sx), pb, op, dilation=(dy, dx), padding_end=pe),
+               _pad_slice_ref(x, w, b, (sy, sx), (dy, dx), pb, pe, op))
+
+
+def forward_conv_matrix_dilated_1d(w, L_in, L_out, s, d, pb):
+    """Dense matrix of the forward strided convolution with dilation d and front pad pb,
+    element by element: Conv(y)[ic, i] = sum_{oc, t} w[ic, oc, t] * y[oc, i*s - pb + t*d]
+    (y = 0 outside [0, L_out)).  Rows (ic, i), columns (oc, o)."""
+    C_in, C_out, k = w.shape
+    A = np.zeros((C_in * L_in, C_out * L_out))
+    for ic in range(C_in):
+        for i in range(L_in):
+            for oc in range(C_out):
+                for t in range(k):
+                    o = i * s - pb + t * d
+                    if 0 <= o < L_out:
+                        A[ic * L_in + i, oc * L_out + o] += w[ic, oc, t]
+    return A
+
+
+def pin_adjoint_dilated(ct):
+    """ConvT with dilation and front/back pads is the adjoint of the dilated forward conv;
+    the output length is (L_in - 1)s + (k - 1)d + 1 + op - pb - pe."""
+    for (L, k, s, d, pb, pe, op) in ((4, 3, 2, 2, 1, 0, 1), (3, 2, 3, 2, 0, 2, 0),
+                                     (5, 3, 1, 3, 2, 1, 2), (2, 4, 2, 1, 2, 0, 1),
+                                     (3, 3, 2, 3, 0, 3, 2)):
+        C_in, C_out = 2, 3
+        w = _rng.standard_normal((C_in, C_out, k))
+        L_out = (L - 1) * s + (k - 1) * d + 1 + op - pb - pe
+        A = forward_conv_matrix_dilated_1d(w, L, L_out, s, d, pb)
+        yv = _rng.standard_normal((1, C_out, L_out))
+        # The forward definition against torch's conv1d on y padded by pb zeros in front and
+        # enough at the back for L outputs.
+        back = max(0, (L - 1) * s + (k - 1) * d + 1 - pb - L_out)
+        ypad = np.pad(yv, ((0, 0), (0, 0), (pb, back)))
+        ref = F.conv1d(torch.from_numpy(ypad), torch.from_numpy(w), stride=s, dilation=d).numpy()
+        _close((A @ yv.reshape(-1)).reshape(1, C_in, -1), ref[:, :, :L])
+        M = np.zeros((C_out * L_out, C_in * L))
+        for j in range(C_in * L):
+            e = np.zeros(C_in * L)
+            e[j] = 1.0
+            out = ct(e.reshape(1, C_in, L), w, None, s, pb, op, dilation=d, padding_end=pe)
+            assert out.shape == (1, C_out, L_out), out.shape
+            M[:, j] = out.reshape(-1)
+        _close(M, A.T)
+
+
+ALL_PINS = [pin_torch_f64_dilation, pin_pad_slice, pin_adjoint_dilated, pin_torch_f64_groups, pin_depthwise_k_equals_s, pin_adjoint_groups,
             pin_torch_f64_1d, pin_torch_f64_2d, pin_adjoint, pin_hand_cases, pin_matmul,
             pin_polyphase, pin_istft_sinusoid]

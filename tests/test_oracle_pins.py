@@ -2,7 +2,8 @@
 
 Runs every check of ``tests/pins.py`` on the oracle, then plants plausible mistakes in copies
 of the oracle's C source (a dropped bias, a wrong padding sign, a transposed weight operand,
-flipped taps, a dropped tap term, a dropped partial sum) and shows that each one fails at
+flipped taps, a dropped tap term, a dropped partial sum, a dropped dilation, an off-by-one tap
+bound, a back pad taken as the front pad) and shows that each one fails at
 least one pin.  The planted copies are compiled into a temporary directory; the committed
 oracle is never modified.
 """
@@ -50,6 +51,21 @@ def test_output_size_matches_torch_shapes():
                                torch.zeros(1, 1, k, dtype=torch.float64),
                                stride=s, padding=p, output_padding=op)
         assert y.shape[-1] == oracle.output_size(L, k, s, p, op)
+
+
+def test_output_size_dilated_matches_torch_shapes():
+    """(L_in - 1)s + (k - 1)d + 1 + op - 2p against torch's output shapes with dilation, and
+    the front/back form against the symmetric one."""
+    import torch
+    import torch.nn.functional as F
+    for (L, k, s, d, p, op) in pins.grid_dilated_1d():
+        y = F.conv_transpose1d(torch.zeros(1, 1, L, dtype=torch.float64),
+                               torch.zeros(1, 1, k, dtype=torch.float64),
+                               stride=s, padding=p, output_padding=op, dilation=d)
+        assert y.shape[-1] == oracle.output_size(L, k, s, p, op, d)
+        assert oracle.output_size(L, k, s, p, op, d, p) == oracle.output_size(L, k, s, p, op, d)
+    assert oracle.output_size(2, 3, 2, 1, 1, 2, 0) == 7
+    assert oracle.output_size(2, 3, 2, 0, 0, 2, 3) == 4
 
 
 def test_landed_count_long_input():
@@ -133,9 +149,18 @@ MUTANTS = {
                           "const double *wp = w + (ocl * C_in + ic) * ntap;"),
     "group_input_channels": ("for (int64_t ic = g * cin_g; ic < (g + 1) * cin_g; ++ic) {",
                              "for (int64_t ic = 0; ic < cin_g; ++ic) {"),
-    "flipped_taps": ("arow[tx] += xv * wrow[tx];", "arow[tx] += xv * wrow[kw - 1 - tx];"),
-    "dropped_tap_term_y": ("const int64_t oy = iy * sh - ph + ty;",
+    "flipped_taps": ("arow[ox0 + tx * dw] += xv * wrow[tx];",
+                     "arow[ox0 + tx * dw] += xv * wrow[kw - 1 - tx];"),
+    "dropped_tap_term_y": ("const int64_t oy = iy * sh - ph + ty * dh;",
                            "const int64_t oy = iy * sh - ph;"),
+    "dropped_dilation_y": ("const int64_t oy = iy * sh - ph + ty * dh;",
+                           "const int64_t oy = iy * sh - ph + ty;"),
+    "tap_bound_floor_x": ("int64_t tx_hi = ox0 < Wo ? (Wo - ox0 + dw - 1) / dw : 0;",
+                          "int64_t tx_hi = ox0 < Wo ? (Wo - ox0) / dw : 0;"),
+    "back_pad_as_front_pad": ("return (L_in - 1) * s + (k - 1) * d + 1 + op - pb - pe;",
+                              "return (L_in - 1) * s + (k - 1) * d + 1 + op - 2 * pb;"),
+    "undilated_output_size": ("return (L_in - 1) * s + (k - 1) * d + 1 + op - pb - pe;",
+                              "return (L_in - 1) * s + k + op - pb - pe;"),
     "dropped_partial_sum": ("for (int64_t c = 0; c < nchunk; ++c) {",
                             "for (int64_t c = 0; c + 1 < nchunk || c == 0; ++c) {"),
 }
@@ -146,7 +171,8 @@ def _oracle_lib(path):
     lib = ctypes.CDLL(path)
     real = oracle._load()
     for name in ("ctr_oracle_conv_transpose", "ctr_oracle_conv_transpose_groups",
-                 "ctr_oracle_output_size", "ctr_oracle_landed_pairs"):
+                 "ctr_oracle_conv_transpose_ex", "ctr_oracle_output_size",
+                 "ctr_oracle_output_size_ex", "ctr_oracle_landed_pairs"):
         getattr(lib, name).restype = getattr(real, name).restype
         getattr(lib, name).argtypes = getattr(real, name).argtypes
     saved = oracle._lib
