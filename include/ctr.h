@@ -94,11 +94,13 @@ typedef enum {
  *   in_spatial     ndim input sizes, each >= 0 (0 = empty input: y = bias or zeros)
  *   kernel         ndim kernel sizes >= 1
  *   stride         ndim strides >= 1
- *   padding        ndim paddings >= 0 (symmetric per dimension; ONNX begin/end pads differ)
+ *   padding        ndim paddings >= 0 (front and back; ctr_plan_set_pads separates them)
  *   output_padding ndim values with 0 <= op < stride (may be NULL = zeros)
  *   dtype          ctr_dtype
- * Every output size must be >= 1.  Dilation and groups are not parameters: dilation 1 and
- * groups 1 only.  Returns CTR_ERR_INVALID_ARG on any violation.
+ * Every output size must be >= 1.  Groups, dilation and separate front/back pads are set
+ * afterwards (ctr_plan_set_groups, ctr_plan_set_dilation, ctr_plan_set_pads; defaults: one
+ * group, dilation 1, the back pad equal to `padding`).  Returns CTR_ERR_INVALID_ARG on any
+ * violation.
  */
 ctr_status ctr_plan_create(ctr_plan_t *out, int ndim, int64_t N, int64_t C_in, int64_t C_out,
                            const int64_t *in_spatial, const int64_t *kernel,
@@ -120,6 +122,38 @@ ctr_status ctr_plan_create(ctr_plan_t *out, int ndim, int64_t N, int64_t C_in, i
  * both channel counts, after ctr_prepack_weight, or on a chained plan.
  */
 ctr_status ctr_plan_set_groups(ctr_plan_t plan, int64_t groups);
+
+/*
+ * Dilation (default 1 per dimension): taps are dil samples apart, so tap t of input i lands
+ * at o = i*s - p_front + t*dil and L_out = (L_in - 1)*s + (k - 1)*dil + 1 + op - p_front -
+ * p_back ("[ExecuTorch][WebGPU] Add optimized conv2d op", Implementation: the gather
+ * condition (oh + pH - kh*dH) divisible by the stride; "[WebGPU] optimizations for audio
+ * models": the ConvTranspose tests with pads, dilations or output_padding).
+ *   dilation  ndim values >= 1
+ * A dilated plan runs the col2im GEMM over its k real taps (C_in >= 16 and k*C_out >= 64)
+ * or the gather kernel; a forced polyphase path packs the zero-inserted kernel of
+ * (k - 1)*dil + 1 taps.  The depthwise path is undilated: forcing it on a dilated plan, or
+ * dilating a plan forced onto it, returns CTR_ERR_UNSUPPORTED and leaves the plan unchanged.
+ * Host only, with the same ordering rule as ctr_plan_set_path; CTR_ERR_INVALID_ARG for a
+ * value < 1, an output size < 1, after ctr_prepack_weight, or on a chained plan (the plan is
+ * then unchanged).
+ */
+ctr_status ctr_plan_set_dilation(ctr_plan_t plan, const int64_t *dilation);
+
+/*
+ * Separate front and back pads per dimension (the ONNX ConvTranspose `pads` attribute:
+ * begin values, then end values), replacing the symmetric `padding` of ctr_plan_create.
+ * The output is the unpadded result with p_front positions cut at the front and p_back at
+ * the back (output_padding positions are added at the back first): L_out = (L_in - 1)*s +
+ * (k - 1)*dil + 1 + op - p_front - p_back.  ("[XNNPACK] Lower dense transposed convs as one
+ * polyphase conv + depth to space", Summary: the padding slice; "[WebGPU] optimizations for
+ * audio models": the ConvTranspose tests with pads.)
+ *   pads_begin, pads_end  ndim values >= 0 each
+ * Every path takes any pads.  Host only, with the same ordering rule as ctr_plan_set_path;
+ * CTR_ERR_INVALID_ARG for a negative pad, an output size < 1, after ctr_prepack_weight, or on
+ * a chained plan (the plan is then unchanged).
+ */
+ctr_status ctr_plan_set_pads(ctr_plan_t plan, const int64_t *pads_begin, const int64_t *pads_end);
 
 /* Fuse an activation into the output stage (default CTR_ACT_NONE).  Host only. */
 ctr_status ctr_plan_set_activation(ctr_plan_t plan, int act, float negative_slope);
@@ -301,11 +335,12 @@ uint64_t ctr_launch_count(void);
  *
  * n_fft is a power of two in [4, 8192]; hop >= 1; 0 <= output_padding < hop; padding >= 0.
  * fp32 only: CTR_BF16 returns CTR_ERR_UNSUPPORTED.  The plan owns no device memory: the
- * caller binds a workspace of ctr_istft_workspace_bytes (twiddles, the scaled window and the
- * windowed frames, fp32 [N][frames][n_fft]) and sets the window once (a kernel on `stream`);
- * ctr_istft_forward then launches two kernels (the per-frame FFT, then the overlap-add as a
- * gather, summing frames in ascending order: deterministic) and never allocates or
- * synchronises.  Errors as for the ConvTranspose plan; CTR_ERR_NOT_PREPARED before
+ * caller binds a workspace of ctr_istft_workspace_bytes (twiddles, the scaled window, the
+ * windowed frames, fp32 [N][frames][n_fft], and the spectra as frame-major complex rows,
+ * [N][frames][n_fft/2 + 2] pairs) and sets the window once (a kernel on `stream`);
+ * ctr_istft_forward then launches three kernels (the spectra to frame-major rows, the
+ * per-frame FFT, then the overlap-add as a gather, summing frames in ascending order:
+ * deterministic) and never allocates or synchronises.  Errors as for the ConvTranspose plan; CTR_ERR_NOT_PREPARED before
  * ctr_istft_set_window (rebinding the workspace clears it).
  * ------------------------------------------------------------------------------------ */
 typedef struct ctr_istft_s *ctr_istft_t;
@@ -319,7 +354,7 @@ ctr_status ctr_istft_set_window(ctr_istft_t plan, const void *window, void *stre
 ctr_status ctr_istft_forward(ctr_istft_t plan, const void *spec, const void *bias, void *y,
                              void *stream);
 ctr_status ctr_istft_describe(ctr_istft_t plan, char *buf, size_t len);
-/* As ctr_plan_set_timing_events, around both kernels of ctr_istft_forward. */
+/* As ctr_plan_set_timing_events, around the kernels of ctr_istft_forward. */
 ctr_status ctr_istft_set_timing_events(ctr_istft_t plan, void *before, void *after);
 void ctr_istft_destroy(ctr_istft_t plan);
 

@@ -24,7 +24,7 @@ def to_dev(a, dtype: str):
 
 def run_plan(x, w, bias, stride, padding, output_padding, dtype="f32", slope=None,
              path=ctr.CTR_PATH_AUTO, split_k=0, check_guards=True, expect_path=None, block_n=0,
-             groups=1):
+             groups=1, dilation=1, padding_end=None):
     """Run one ConvTranspose through the library.  x, w, bias: numpy arrays holding values of
     the I/O dtype.  Returns (y as float64 numpy, plan description)."""
     x = np.asarray(x)
@@ -32,7 +32,7 @@ def run_plan(x, w, bias, stride, padding, output_padding, dtype="f32", slope=Non
     plan = ctr.Plan(x.shape[0], x.shape[1], w.shape[1] * groups, tuple(x.shape[2:]),
                     tuple(w.shape[2:]), stride, padding, output_padding, dtype=tdtype(dtype),
                     negative_slope=slope, path=path, split_k=split_k, block_n=block_n,
-                    groups=groups)
+                    groups=groups, dilation=dilation, padding_end=padding_end)
     try:
         if expect_path is not None:
             assert plan.path == expect_path, plan.describe()
@@ -51,10 +51,12 @@ def run_plan(x, w, bias, stride, padding, output_padding, dtype="f32", slope=Non
         plan.close()
 
 
-def reference(x, w, bias, stride, padding, output_padding, dtype="f32", slope=None, groups=1):
+def reference(x, w, bias, stride, padding, output_padding, dtype="f32", slope=None, groups=1,
+              dilation=1, padding_end=None):
     """Oracle result rounded like the library's output: double sum + bias, then LeakyReLU,
     then one rounding to the I/O dtype."""
-    y = oracle.conv_transpose(x, w, bias, stride, padding, output_padding, groups=groups)
+    y = oracle.conv_transpose(x, w, bias, stride, padding, output_padding, groups=groups,
+                              dilation=dilation, padding_end=padding_end)
     if slope is not None:
         y = oracle.leaky_relu(y, slope)
     return oracle.round_bf16(y) if dtype == "bf16" else oracle.round_f32(y)

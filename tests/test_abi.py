@@ -244,6 +244,81 @@ def test_groups_routing_without_gpu(ctr):
             ctr.ctr_plan_destroy(x)
 
 
+def test_dilation_and_pads_without_gpu(ctr):
+    """ctr_plan_set_dilation / ctr_plan_set_pads: output lengths (L_in - 1)s + (k - 1)d + 1 +
+    op - p_front - p_back as the oracle's, routing of dilated plans (col2im or gather; forced
+    polyphase packs the zero-inserted kernel; the depthwise kernel refuses), and invalid
+    values or forced paths that cannot take them leave the plan unchanged."""
+    import oracle
+    f32 = ctr.CTR_F32
+    arr = ctr._arr
+    h = _plan(ctr, 1, 1, 32, 32, [50], [3], [2], [1], [1], f32)
+    try:
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_COL2IM
+        ctr.ctr_plan_set_dilation(h, [2])
+        assert ctr.ctr_plan_output_shape(h, 1) == (oracle.output_size(50, 3, 2, 1, 1, 2),) == (102,)
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_COL2IM
+        assert "dil=1x2" in ctr.ctr_plan_describe(h)
+        ctr.ctr_plan_set_pads(h, [0], [3])
+        assert ctr.ctr_plan_output_shape(h, 1) == (oracle.output_size(50, 3, 2, 0, 1, 2, 3),)
+        assert "pads=0x0/0x3" in ctr.ctr_plan_describe(h)
+        before = ctr.ctr_plan_output_shape(h, 1)
+        for bad in ([0], [-1]):
+            assert ctr.lib.ctr_plan_set_dilation(h, arr(bad)) == ctr.CTR_ERR_INVALID_ARG
+        assert ctr.lib.ctr_plan_set_pads(h, arr([-1]), arr([0])) == ctr.CTR_ERR_INVALID_ARG
+        assert ctr.lib.ctr_plan_set_pads(h, arr([60]), arr([60])) == ctr.CTR_ERR_INVALID_ARG
+        assert ctr.ctr_plan_output_shape(h, 1) == before
+        # forced polyphase packs (k - 1)d + 1 = 5 dilated taps: m = 3 per phase
+        col2im_packed = ctr.ctr_packed_weight_bytes(h)
+        ctr.ctr_plan_set_path(h, ctr.CTR_PATH_POLYPHASE, 0)
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_POLYPHASE
+        assert "taps=1x3" in ctr.ctr_plan_describe(h)
+        assert ctr.ctr_packed_weight_bytes(h) != col2im_packed
+        ctr.ctr_plan_set_dilation(h, [1])
+        assert "taps=1x2" in ctr.ctr_plan_describe(h)
+    finally:
+        ctr.ctr_plan_destroy(h)
+    # small channel counts: gather; 2-D with unequal dilations
+    h = _plan(ctr, 2, 2, 4, 3, [9, 7], [3, 2], [2, 3], [1, 0], [1, 2], f32)
+    try:
+        ctr.ctr_plan_set_dilation(h, [2, 3])
+        ctr.ctr_plan_set_pads(h, [1, 0], [0, 2])
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_GATHER
+        assert ctr.ctr_plan_output_shape(h, 2) == (oracle.output_size(9, 3, 2, 1, 1, 2, 0),
+                                                   oracle.output_size(7, 2, 3, 0, 2, 3, 2))
+    finally:
+        ctr.ctr_plan_destroy(h)
+    # undilated plans keep their path under any pads
+    h = _plan(ctr, 1, 1, 64, 64, [100], [4], [2], [1], [0], ctr.CTR_BF16)
+    try:
+        ctr.ctr_plan_set_pads(h, [2], [0])
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_POLYPHASE
+        assert ctr.ctr_plan_output_shape(h, 1) == (oracle.output_size(100, 4, 2, 2, 0, 1, 0),)
+        # depthwise: dilation reroutes an automatic plan to gather, refuses a forced one
+        ctr.ctr_plan_set_groups(h, 64)
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_DEPTHWISE
+        ctr.ctr_plan_set_path(h, ctr.CTR_PATH_DEPTHWISE, 0)
+        assert ctr.lib.ctr_plan_set_dilation(h, arr([2])) == ctr.CTR_ERR_UNSUPPORTED
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_DEPTHWISE
+        assert ctr.ctr_plan_output_shape(h, 1) == (oracle.output_size(100, 4, 2, 2, 0, 1, 0),)
+        ctr.ctr_plan_set_path(h, ctr.CTR_PATH_AUTO, 0)
+        ctr.ctr_plan_set_dilation(h, [2])
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_GATHER
+    finally:
+        ctr.ctr_plan_destroy(h)
+    # chained plans keep their geometry
+    a = _plan(ctr, 1, 1, 64, 32, [100], [4], [2], [1], [0], ctr.CTR_BF16)
+    b = _plan(ctr, 1, 1, 32, 64, [200], [4], [2], [1], [0], ctr.CTR_BF16)
+    try:
+        ctr.ctr_plan_chain(a, b)
+        assert ctr.lib.ctr_plan_set_dilation(a, arr([2])) == ctr.CTR_ERR_INVALID_ARG
+        assert ctr.lib.ctr_plan_set_pads(b, arr([1]), arr([2])) == ctr.CTR_ERR_INVALID_ARG
+    finally:
+        ctr.ctr_plan_chain(a, None)
+        ctr.ctr_plan_destroy(a)
+        ctr.ctr_plan_destroy(b)
+
+
 def test_istft_plan_without_gpu(ctr):
     """ctr_istft_*: argument checks, output length, workspace size; no window -> not prepared."""
     h = ctr.ctr_istft_create(4, 4096, 1024, 343)

@@ -6,7 +6,8 @@ PyTorch fallback: if the library has not been built the first call raises Import
 any non-OK status from the library raises ``CtrError``.
 
 Low level (same names as the C ABI): ``ctr_plan_create``, ``ctr_plan_set_activation``,
-``ctr_plan_set_path``, ``ctr_plan_set_groups``, ``ctr_plan_set_tile``, ``ctr_plan_chain``, ``ctr_plan_get_path``, ``ctr_plan_output_shape``,
+``ctr_plan_set_path``, ``ctr_plan_set_groups``, ``ctr_plan_set_dilation``, ``ctr_plan_set_pads``,
+``ctr_plan_set_tile``, ``ctr_plan_chain``, ``ctr_plan_get_path``, ``ctr_plan_output_shape``,
 ``ctr_packed_weight_bytes``, ``ctr_workspace_bytes``, ``ctr_plan_bind_workspace``,
 ``ctr_prepack_weight``, ``ctr_forward``, ``ctr_forward_noalloc``, ``ctr_plan_check``,
 ``ctr_plan_set_wait_limit_ns``,
@@ -60,6 +61,8 @@ SIGNATURES = {
     "ctr_plan_set_activation": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_float]),
     "ctr_plan_set_path": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int]),
     "ctr_plan_set_groups": (ctypes.c_int, [_vp, ctypes.c_int64]),
+    "ctr_plan_set_dilation": (ctypes.c_int, [_vp, _i64p]),
+    "ctr_plan_set_pads": (ctypes.c_int, [_vp, _i64p, _i64p]),
     "ctr_plan_set_tile": (ctypes.c_int, [_vp, ctypes.c_int]),
     "ctr_plan_chain": (ctypes.c_int, [_vp, _vp]),
     "ctr_plan_get_path": (ctypes.c_int, [_vp]),
@@ -172,6 +175,14 @@ def ctr_plan_set_path(plan, path, split_k=0):
 
 def ctr_plan_set_groups(plan, groups):
     _check(lib.ctr_plan_set_groups(plan, int(groups)), "ctr_plan_set_groups")
+
+
+def ctr_plan_set_dilation(plan, dilation):
+    _check(lib.ctr_plan_set_dilation(plan, _arr(dilation)), "ctr_plan_set_dilation")
+
+
+def ctr_plan_set_pads(plan, pads_begin, pads_end):
+    _check(lib.ctr_plan_set_pads(plan, _arr(pads_begin), _arr(pads_end)), "ctr_plan_set_pads")
 
 
 def ctr_plan_set_tile(plan, block_n):
@@ -327,7 +338,7 @@ class Plan:
 
     def __init__(self, N, C_in, C_out, in_spatial, kernel, stride=1, padding=0,
                  output_padding=0, dtype=None, negative_slope=None, path=CTR_PATH_AUTO,
-                 split_k=0, device=None, block_n=0, groups=1):
+                 split_k=0, device=None, block_n=0, groups=1, dilation=1, padding_end=None):
         torch = _torch()
         self.ndim = len(in_spatial)
         self.dtype = dtype if dtype is not None else torch.float32
@@ -339,6 +350,8 @@ class Plan:
         self.padding = _tuple(padding, self.ndim)
         self.output_padding = _tuple(output_padding, self.ndim)
         self.groups = int(groups)
+        self.dilation = _tuple(dilation, self.ndim)
+        self.padding_end = self.padding if padding_end is None else _tuple(padding_end, self.ndim)
         self.handle = ctr_plan_create(self.ndim, self.N, self.C_in, self.C_out, self.in_spatial,
                                       self.kernel, self.stride, self.padding,
                                       self.output_padding, _dtype_code(self.dtype))
@@ -347,6 +360,10 @@ class Plan:
                 ctr_plan_set_activation(self.handle, CTR_ACT_LEAKY_RELU, negative_slope)
             if self.groups != 1:
                 ctr_plan_set_groups(self.handle, self.groups)
+            if self.dilation != (1,) * self.ndim:
+                ctr_plan_set_dilation(self.handle, self.dilation)
+            if self.padding_end != self.padding:
+                ctr_plan_set_pads(self.handle, self.padding, self.padding_end)
             if path != CTR_PATH_AUTO or split_k:
                 ctr_plan_set_path(self.handle, path, split_k)
             if block_n:
@@ -527,14 +544,16 @@ _plan_cache = {}
 
 
 def conv_transpose(x, w, bias=None, stride=1, padding=0, output_padding=0, negative_slope=None,
-                   path=CTR_PATH_AUTO, split_k=0, groups=1):
+                   path=CTR_PATH_AUTO, split_k=0, groups=1, dilation=1, padding_end=None):
     """ConvTranspose1d/2d of torch CUDA tensors (float32 or bfloat16), like
-    torch.nn.functional.conv_transpose{1,2}d with dilation = 1, plus an optional fused
-    LeakyReLU.  Plans and packed weights are cached per (shapes, weight)."""
+    torch.nn.functional.conv_transpose{1,2}d (groups, dilation), plus separate back pads
+    (``padding_end``, ONNX-style; default: ``padding``) and an optional fused LeakyReLU.
+    Plans and packed weights are cached per (shapes, weight)."""
     ndim = x.dim() - 2
     key = (tuple(x.shape), tuple(w.shape), x.dtype, str(x.device), w.data_ptr(), w._version,
            _tuple(stride, ndim), _tuple(padding, ndim), _tuple(output_padding, ndim),
-           negative_slope, path, split_k, groups)
+           negative_slope, path, split_k, groups, _tuple(dilation, ndim),
+           None if padding_end is None else _tuple(padding_end, ndim))
     plan = _plan_cache.get(key)
     if plan is None:
         if len(_plan_cache) > 64:
@@ -542,7 +561,7 @@ def conv_transpose(x, w, bias=None, stride=1, padding=0, output_padding=0, negat
         plan = Plan(x.shape[0], x.shape[1], w.shape[1] * groups, tuple(x.shape[2:]),
                     tuple(w.shape[2:]), stride, padding, output_padding, dtype=x.dtype,
                     negative_slope=negative_slope, path=path, split_k=split_k, device=x.device,
-                    groups=groups)
+                    groups=groups, dilation=dilation, padding_end=padding_end)
         plan.prepack(w.contiguous())
         _plan_cache[key] = plan
     return plan.forward(x.contiguous(), None if bias is None else bias.contiguous())

@@ -137,6 +137,33 @@ void choose_tiling(ctr_plan_s *pl) {
     pl->num_tiles = (int64_t)pl->num_p_tiles * pl->num_r_tiles * pl->splits;
 }
 
+// Extent of the dilated kernel along dimension d: (k - 1)*dil + 1 samples, of which the k
+// taps are every dil-th.
+int64_t dilated_extent(const ctr_plan_s *pl, int d) { return (pl->k[d] - 1) * pl->dil[d] + 1; }
+
+// Output length of dimension d: (L_in - 1)*s + (k - 1)*dil + 1 + op - p_front - p_back,
+// i.e. (L_in - 1)*s - 2p + k + op without dilation and with equal pads.
+int64_t output_length(const ctr_plan_s *pl, int d) {
+    return (pl->in[d] - 1) * pl->s[d] + dilated_extent(pl, d) + pl->op[d] - pl->p[d] - pl->pe[d];
+}
+
+// Output lengths and the element counts derived from them; false when an output length is
+// not positive or a count leaves the supported range (the plan is then left unchanged).
+bool set_output_lengths(ctr_plan_s *pl) {
+    const int64_t kLim = (int64_t)1 << 31;
+    int64_t out[2];
+    int64_t total_out = pl->B * pl->C_out;
+    for (int d = 0; d < 2; ++d) {
+        out[d] = output_length(pl, d);
+        if (out[d] < 1 || out[d] >= kLim) return false;
+        total_out *= out[d];
+        if (total_out >= ((int64_t)1 << 46)) return false;
+    }
+    pl->out[0] = out[0];
+    pl->out[1] = out[1];
+    return true;
+}
+
 // Derive the GEMM geometry, tiling, packed size and workspace layout from the path.
 void layout_plan(ctr_plan_s *pl) {
     pl->packed_bytes = 0;
@@ -158,7 +185,7 @@ void layout_plan(ctr_plan_s *pl) {
     pl->C_in_pad = round_up(pl->C_in, bk);
     if (pl->path == CTR_PATH_POLYPHASE) {
         for (int d = 0; d < 2; ++d) {
-            pl->m[d] = ceil_div(pl->k[d], pl->s[d]);
+            pl->m[d] = ceil_div(dilated_extent(pl, d), pl->s[d]);
             pl->Qv[d] = ceil_div(pl->out[d] + pl->p[d], pl->s[d]);
             pl->P[d] = std::max(pl->in[d] + 2 * (pl->m[d] - 1), pl->Qv[d] + pl->m[d] - 1);
         }
@@ -216,10 +243,15 @@ int choose_path(const ctr_plan_s *pl) {
     if (pl->forced_path != CTR_PATH_AUTO) return pl->forced_path;
     if (pl->groups > 1)   // the tensor-core paths contract over all input channels
         return ctr::depthwise_supported(pl) ? CTR_PATH_DEPTHWISE : CTR_PATH_GATHER;
+    const int64_t T = pl->k[0] * pl->k[1];
+    // Dilated taps: the polyphase rows of the zero-inserted kernel would be mostly zeros
+    // (phases that no tap reaches), so a dilated plan runs the col2im GEMM over its real taps,
+    // or the gather kernel.  Forcing polyphase stays possible (the prepack inserts the zeros).
+    if (pl->dil[0] > 1 || pl->dil[1] > 1)
+        return (pl->C_in >= 16 && T * pl->C_out >= 64) ? CTR_PATH_COL2IM : CTR_PATH_GATHER;
     const bool kdiv = (pl->k[0] % pl->s[0] == 0) && (pl->k[1] % pl->s[1] == 0);
     const int64_t S = pl->s[0] * pl->s[1];
     const int64_t mprod = ceil_div(pl->k[0], pl->s[0]) * ceil_div(pl->k[1], pl->s[1]);
-    const int64_t T = pl->k[0] * pl->k[1];
     if (kdiv) return (S * pl->C_out >= 64 && pl->C_in * mprod >= 16) ? CTR_PATH_POLYPHASE
                                                                     : CTR_PATH_GATHER;
     return (pl->C_in >= 16 && T * pl->C_out >= 64) ? CTR_PATH_COL2IM : CTR_PATH_GATHER;
@@ -483,6 +515,7 @@ ctr_status ctr_plan_create(ctr_plan_t *out, int ndim, int64_t N, int64_t C_in, i
     pl->wait_limit_ns = 4000000000ull;
     // Unit leading dimension for 1-D.
     pl->in[0] = 1; pl->k[0] = 1; pl->s[0] = 1; pl->p[0] = 0; pl->op[0] = 0;
+    pl->dil[0] = pl->dil[1] = 1;
     for (int d = 0; d < ndim; ++d) {
         const int dd = d + (2 - ndim);
         pl->in[dd] = in_spatial[d];
@@ -497,7 +530,8 @@ ctr_status ctr_plan_create(ctr_plan_t *out, int ndim, int64_t N, int64_t C_in, i
                         pl->k[d] < kLim && pl->s[d] >= 1 && pl->s[d] < kLim && pl->p[d] >= 0 &&
                         pl->p[d] < kLim && pl->op[d] >= 0 && pl->op[d] < pl->s[d];
         if (!ok) { delete pl; return CTR_ERR_INVALID_ARG; }
-        pl->out[d] = (pl->in[d] - 1) * pl->s[d] - 2 * pl->p[d] + pl->k[d] + pl->op[d];
+        pl->pe[d] = pl->p[d];
+        pl->out[d] = output_length(pl, d);
         if (pl->out[d] < 1 || pl->out[d] >= kLim) { delete pl; return CTR_ERR_INVALID_ARG; }
         total_out *= pl->out[d];
         total_in *= std::max<int64_t>(pl->in[d], 1);
@@ -580,6 +614,67 @@ ctr_status ctr_plan_set_groups(ctr_plan_t pl, int64_t groups) {
     return reroute(pl, pl->forced_path, pl->forced_split, groups);
 }
 
+// New dilation and pads (2-D form); the output lengths, path and layout follow.  Invalid
+// geometry, or a forced path that cannot take it, leaves the plan as it was.
+ctr_status set_geometry(ctr_plan_s *pl, const int64_t (&dil)[2], const int64_t (&pb)[2],
+                        const int64_t (&pe)[2]) {
+    const int64_t kLim = (int64_t)1 << 31;
+    int64_t old_dil[2], old_p[2], old_pe[2], old_out[2];
+    for (int d = 0; d < 2; ++d) {
+        if (dil[d] < 1 || dil[d] >= kLim || pb[d] < 0 || pb[d] >= kLim || pe[d] < 0 ||
+            pe[d] >= kLim || (pl->k[d] - 1) * dil[d] + 1 >= kLim)
+            return CTR_ERR_INVALID_ARG;
+        old_dil[d] = pl->dil[d];
+        old_p[d] = pl->p[d];
+        old_pe[d] = pl->pe[d];
+        old_out[d] = pl->out[d];
+    }
+    auto restore = [&]() {
+        for (int d = 0; d < 2; ++d) {
+            pl->dil[d] = old_dil[d];
+            pl->p[d] = old_p[d];
+            pl->pe[d] = old_pe[d];
+            pl->out[d] = old_out[d];
+        }
+    };
+    for (int d = 0; d < 2; ++d) {
+        pl->dil[d] = dil[d];
+        pl->p[d] = pb[d];
+        pl->pe[d] = pe[d];
+    }
+    if (!set_output_lengths(pl)) {
+        restore();
+        return CTR_ERR_INVALID_ARG;
+    }
+    const ctr_status st = reroute(pl, pl->forced_path, pl->forced_split, pl->groups);
+    if (st != CTR_OK) {
+        restore();
+        reroute(pl, pl->forced_path, pl->forced_split, pl->groups);
+    }
+    return st;
+}
+
+ctr_status ctr_plan_set_dilation(ctr_plan_t pl, const int64_t *dilation) {
+    if (!pl || !dilation) return CTR_ERR_INVALID_ARG;
+    if (pl->prepared || pl->chain_next || pl->chain_prev) return CTR_ERR_INVALID_ARG;
+    int64_t dil[2] = {1, 1};
+    for (int d = 0; d < pl->ndim; ++d) dil[d + (2 - pl->ndim)] = dilation[d];
+    const int64_t pb[2] = {pl->p[0], pl->p[1]}, pe[2] = {pl->pe[0], pl->pe[1]};
+    return set_geometry(pl, dil, pb, pe);
+}
+
+ctr_status ctr_plan_set_pads(ctr_plan_t pl, const int64_t *pads_begin, const int64_t *pads_end) {
+    if (!pl || !pads_begin || !pads_end) return CTR_ERR_INVALID_ARG;
+    if (pl->prepared || pl->chain_next || pl->chain_prev) return CTR_ERR_INVALID_ARG;
+    int64_t pb[2] = {0, 0}, pe[2] = {0, 0};
+    for (int d = 0; d < pl->ndim; ++d) {
+        pb[d + (2 - pl->ndim)] = pads_begin[d];
+        pe[d + (2 - pl->ndim)] = pads_end[d];
+    }
+    const int64_t dil[2] = {pl->dil[0], pl->dil[1]};
+    return set_geometry(pl, dil, pb, pe);
+}
+
 ctr_status ctr_plan_set_tile(ctr_plan_t pl, int block_n) {
     if (!pl || (block_n != 0 && block_n != 64 && block_n != 128 && block_n != 256))
         return CTR_ERR_INVALID_ARG;
@@ -645,6 +740,13 @@ ctr_status ctr_plan_describe(ctr_plan_t pl, char *buf, size_t len) {
     } else {
         snprintf(buf, len, "path=%s dtype=%s groups=%lld packed=%zu ws=0", pname,
                  pl->dtype == CTR_BF16 ? "bf16" : "f32", (long long)pl->groups, pl->packed_bytes);
+    }
+    if (pl->dil[0] > 1 || pl->dil[1] > 1 || pl->p[0] != pl->pe[0] || pl->p[1] != pl->pe[1]) {
+        const size_t used = strlen(buf);
+        if (used + 1 < len)
+            snprintf(buf + used, len - used, " dil=%lldx%lld pads=%lldx%lld/%lldx%lld",
+                     (long long)pl->dil[0], (long long)pl->dil[1], (long long)pl->p[0],
+                     (long long)pl->p[1], (long long)pl->pe[0], (long long)pl->pe[1]);
     }
     return CTR_OK;
 }

@@ -32,6 +32,7 @@ struct Geo {
     int64_t B, C_in, C_out;
     int64_t cin_g, cout_g;    // channels per group
     int64_t H, W, ky, kx, sy, sx, py, px, Ho, Wo;
+    int64_t dy, dx;           // dilation
     int act;
     float slope;
     int bf16;
@@ -54,6 +55,8 @@ Geo geo_of(const ctr_plan_s *pl) {
     g.px = pl->p[1];
     g.Ho = pl->out[0];
     g.Wo = pl->out[1];
+    g.dy = pl->dil[0];
+    g.dx = pl->dil[1];
     g.act = pl->act;
     g.slope = pl->slope;
     g.bf16 = pl->dtype == CTR_BF16 ? 1 : 0;
@@ -62,11 +65,23 @@ Geo geo_of(const ctr_plan_s *pl) {
 
 // -------------------------------------------------------------------------- gather
 // y[b, oc, oy, ox] = bias[oc] + sum over the input channels of oc's group and the taps that
-// reach (oy, ox): a tap ty contributes when (oy + py - ty) is a multiple of sy and the
+// reach (oy, ox): a tap ty contributes when (oy + py - ty*dy) is a multiple of sy and the
 // quotient is a valid input row ("[ExecuTorch][WebGPU] Add optimized conv2d op",
-// Implementation: the gather form with the un-flipped weight, laid out [IC][OC/groups][k]).
-// fp32 accumulation on CUDA cores, starting from the bias, taps in ascending (ty, tx) order;
-// one thread per output element.
+// Implementation: the gather form with the un-flipped weight, laid out [IC][OC/groups][k],
+// and the dilation dH).  fp32 accumulation on CUDA cores, starting from the bias, taps in
+// ascending (ty, tx) order; one thread per output element.
+//
+// Taps of one output along a dimension: r = o + p is the unpadded position, tap t reaches it
+// from input (r - t*d)/s when that is a whole number in range.  Without dilation the first
+// such tap is r mod s and the next ones follow every s taps; with dilation every tap is
+// tested.  r - t*d only falls as t grows, so the loop ends at the first negative one.
+struct TapRange {
+    int64_t t0, step;
+};
+
+__device__ __forceinline__ TapRange tap_range(int64_t r, int64_t s, int64_t d) {
+    return d == 1 ? TapRange{r % s, s} : TapRange{0, 1};
+}
 __global__ void gather_kernel(const void *__restrict__ x, const void *__restrict__ w,
                               const void *__restrict__ bias, void *__restrict__ y, Geo g,
                               int64_t total) {
@@ -81,13 +96,18 @@ __global__ void gather_kernel(const void *__restrict__ x, const void *__restrict
         const int64_t grp = oc / g.cout_g, ic0 = grp * g.cin_g;
         float acc = bias ? load_io(bias, oc, g.bf16) : 0.0f;
         const int64_t ry = oy + g.py, rx = ox + g.px;
-        for (int64_t ty = ry % g.sy; ty < g.ky; ty += g.sy) {
-            const int64_t iy = (ry - ty) / g.sy;
-            if (iy < 0) break;
+        const TapRange try_ = tap_range(ry, g.sy, g.dy), trx = tap_range(rx, g.sx, g.dx);
+        for (int64_t ty = try_.t0; ty < g.ky; ty += try_.step) {
+            const int64_t ny = ry - ty * g.dy;
+            if (ny < 0) break;
+            if (ny % g.sy) continue;
+            const int64_t iy = ny / g.sy;
             if (iy >= g.H) continue;
-            for (int64_t tx = rx % g.sx; tx < g.kx; tx += g.sx) {
-                const int64_t ix = (rx - tx) / g.sx;
-                if (ix < 0) break;
+            for (int64_t tx = trx.t0; tx < g.kx; tx += trx.step) {
+                const int64_t nx = rx - tx * g.dx;
+                if (nx < 0) break;
+                if (nx % g.sx) continue;
+                const int64_t ix = nx / g.sx;
                 if (ix >= g.W) continue;
                 const int64_t xoff = ((b * g.C_in + ic0) * g.H + iy) * g.W + ix;
                 const int64_t woff =
@@ -126,6 +146,7 @@ __global__ void copy_bytes_kernel(const uint4 *__restrict__ src, uint4 *__restri
 struct PackGeo {
     int64_t M_pad, K_total, C_in_pad, C_in, C_out;
     int64_t ky, kx, sy, sx, my, mx;
+    int64_t dy, dx;       // dilation (polyphase rows of the zero-inserted kernel)
     int S, S_pad;
     int polyphase;
     int bf16;
@@ -137,6 +158,9 @@ struct PackGeo {
 //   A[r = oc*S_pad + jy*sx + jx, k = (uy*mx + ux)*C_in_pad + ic]
 //       = w[ic, oc, sy*(my-1-uy) + jy, sx*(mx-1-ux) + jx]    (0 past the kernel: the kernel
 //                                                               is zero-padded to m*s taps)
+// With dilation the polyphase rows come from the zero-inserted kernel: a dilated tap index
+// e (per dimension) holds w[.., e / dil] when e is a multiple of dil and e / dil < k, and
+// zero otherwise.
 // col2im rows ("[WebGPU] optimizations for audio models", ConvTranspose commit: W[C_in,
 // kH*kW*C_out] prepacked to the GEMM layout):  A[r = oc*S_pad + t, k = ic] = w[ic, oc, t].
 // Padding rows and channels are zero.  fp32 weights are split into tf32 hi and lo planes.
@@ -167,6 +191,9 @@ __global__ void prepack_kernel(const void *__restrict__ w, void *__restrict__ wp
                 const int64_t uy = g / pg.mx, ux = g - (g / pg.mx) * pg.mx;
                 ty = pg.sy * (pg.my - 1 - uy) + jy;
                 tx = pg.sx * (pg.mx - 1 - ux) + jx;
+                // Dilated tap index -> real tap (past the kernel when between taps).
+                ty = ty % pg.dy ? pg.ky : ty / pg.dy;
+                tx = tx % pg.dx ? pg.kx : tx / pg.dx;
             } else {
                 ty = j / pg.kx;
                 tx = j - ty * pg.kx;
@@ -418,13 +445,18 @@ __global__ void col2im_kernel(const float *__restrict__ col, int64_t ld, int64_t
         const int64_t b = t / g.C_out;
         float acc = bias ? load_io(bias, oc, g.bf16) : 0.0f;
         const int64_t ry = oy + g.py, rx = ox + g.px;
-        for (int64_t ty = ry % g.sy; ty < g.ky; ty += g.sy) {
-            const int64_t iy = (ry - ty) / g.sy;
-            if (iy < 0) break;
+        const TapRange try_ = tap_range(ry, g.sy, g.dy), trx = tap_range(rx, g.sx, g.dx);
+        for (int64_t ty = try_.t0; ty < g.ky; ty += try_.step) {
+            const int64_t ny = ry - ty * g.dy;
+            if (ny < 0) break;
+            if (ny % g.sy) continue;
+            const int64_t iy = ny / g.sy;
             if (iy >= g.H) continue;
-            for (int64_t tx = rx % g.sx; tx < g.kx; tx += g.sx) {
-                const int64_t ix = (rx - tx) / g.sx;
-                if (ix < 0) break;
+            for (int64_t tx = trx.t0; tx < g.kx; tx += trx.step) {
+                const int64_t nx = rx - tx * g.dx;
+                if (nx < 0) break;
+                if (nx % g.sx) continue;
+                const int64_t ix = nx / g.sx;
                 if (ix >= g.W) continue;
                 const int64_t r = oc * S_pad + ty * g.kx + tx;
                 const int64_t n = (b * g.H + iy) * g.W + ix;
@@ -485,6 +517,8 @@ cudaError_t launch_prepack(const ctr_plan_s *pl, const void *w, void *w_packed, 
     pg.sx = pl->s[1];
     pg.my = pl->m[0];
     pg.mx = pl->m[1];
+    pg.dy = pl->dil[0];
+    pg.dx = pl->dil[1];
     pg.S = pl->S;
     pg.S_pad = pl->S_pad;
     pg.polyphase = pl->path == CTR_PATH_POLYPHASE ? 1 : 0;

@@ -91,6 +91,8 @@ struct ctr_plan_s {
     int ndim;
     int64_t B, C_in, C_out;
     int64_t in[2], k[2], s[2], p[2], op[2], out[2];
+    int64_t dil[2];     // dilation (ctr_plan_set_dilation; 1 = none)
+    int64_t pe[2];      // back pad (ctr_plan_set_pads; p is the front pad; default pe = p)
     int dtype;
     int act;
     float slope;
