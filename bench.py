@@ -462,10 +462,10 @@ def run_ours(args, rank, world, local_rank):
         peak_note = "HBM copy bandwidth, %s" % peak_src
     clocks = sampler.summary(soak_t0, wall1 + 0.25)
     kname = {ctr.CTR_PATH_GATHER: "gather_kernel", ctr.CTR_PATH_DEPTHWISE: "depthwise_kernel",
-             -1: "irfft_frames_kernel+istft_ola_kernel"}.get(sets[0]["plans"][j].path,
-                                                               "gemm_tc_kernel")
+             -1: "spectrum_rows_kernel+irfft_frames_kernel+istft_ola_kernel"}.get(
+                 sets[0]["plans"][j].path, "gemm_tc_kernel")
     traffic = profiled_traffic(args.workload, j, nl,
-                               "istft" if kname.startswith("irfft") else kname[:-len("_kernel")])
+                               "istft" if kname.startswith("spectrum_rows") else kname[:-len("_kernel")])
 
     result = {
         "metric": "ConvTranspose GFLOP/s and % of roofline (tensor peak vs HBM) per call",

@@ -21,9 +21,11 @@
 //   x[2n+1] = 1/N sum_{k<M} (X_k - conj(X_{M-k})) e^{2 pi i k/N}   e^{2 pi i k n / M}
 // (split the sum over f into k and k + M).  Both bracketed sequences E_k, O_k are spectra of
 // real sequences, so z = IDFT_M(E + i O), unnormalised, holds N x[2n] in its real part and
-// N x[2n+1] in its imaginary part.  The length-M inverse transform is a Stockham autosort FFT
-// in shared memory (radix-4 stages and one radix-2 stage when log2 M is odd; Govindaraju et
-// al., "High performance discrete Fourier transforms on graphics processors", SC 2008).
+// N x[2n+1] in its imaginary part.  The length-M inverse transform is a mixed-radix Stockham
+// autosort FFT between two shared-memory buffers (Govindaraju et al., "High performance
+// discrete Fourier transforms on graphics processors", SC 2008): radix-16 passes, with one
+// radix-2, -4 or -8 pass first when log2 M is not a multiple of 4, each butterfly's R points
+// held in registers, so M = 2048 takes three passes over shared memory.
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
@@ -37,7 +39,7 @@ struct ctr_istft_s {
     int dtype;
     int fpb;                 // frames per block of the FFT kernel
     size_t smem;             // its dynamic shared memory
-    size_t off_tw, off_win, off_frames, ws_needed;
+    size_t off_tw, off_win, off_frames, off_rows, ws_needed;
     void *ws;
     size_t ws_bytes;
     int window_set;
@@ -72,40 +74,208 @@ __global__ void istft_init_kernel(float2 *__restrict__ tw, float *__restrict__ w
 struct FftGeo {
     int T, C;                // frames, input channels (N + 2)
     int N, M, logM;          // frame length, half length, log2(M)
+    int Mp;                  // pitch of the spectrum rows: M + 2 pairs (16-byte rows)
+    int Ms;                  // pitch of a frame's FFT buffer in shared memory (padded indices)
     int fpb;                 // frames per block
 };
 
-// One block transforms fpb consecutive frames of one batch item: loads their onesided
-// spectra, folds each into Z = E + iO (above), runs the inverse Stockham FFT and writes the
-// windowed frames, fp32, to frames[b][t][N].
+// Onesided spectra, channel-major [b][c][t] (c < M + 1: real part of bin c, else imaginary
+// part of bin c - M - 1), to frame-major complex rows Z[b][t][f] = (Re X_f, Im X_f), f <= M,
+// rows of Mp float2.  One 32-bin x 32-frame tile per block through shared memory: a warp
+// reads 32 consecutive frames of one channel and writes 32 consecutive bins of one frame, so
+// both sides are coalesced (the FFT kernel then copies whole rows).  Every load of a thread
+// is issued before the first shared-memory store.
+constexpr int kTile = 32;
+
+__global__ void __launch_bounds__(256)
+spectrum_rows_kernel(const float *__restrict__ spec, float2 *__restrict__ Z, FftGeo g) {
+    __shared__ float re[kTile][kTile + 1], im[kTile][kTile + 1];
+    const int b = blockIdx.z;
+    const int f0 = blockIdx.y * kTile, t0 = blockIdx.x * kTile;
+    const int lx = threadIdx.x & 31, ly = threadIdx.x >> 5;
+    const int M = g.M;
+    const float *sb = spec + (int64_t)b * g.C * g.T;
+    float a[kTile / 8], c[kTile / 8];
+#pragma unroll
+    for (int i = 0; i < kTile / 8; ++i) {
+        const int f = f0 + ly + 8 * i, t = t0 + lx;
+        const bool in = f <= M && t < g.T;
+        a[i] = in ? __ldg(sb + (int64_t)f * g.T + t) : 0.0f;
+        c[i] = in ? __ldg(sb + (int64_t)(M + 1 + f) * g.T + t) : 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < kTile / 8; ++i) {
+        re[ly + 8 * i][lx] = a[i];
+        im[ly + 8 * i][lx] = c[i];
+    }
+    __syncthreads();
+    float2 *zb = Z + (int64_t)b * g.T * g.Mp;
+#pragma unroll
+    for (int i = 0; i < kTile / 8; ++i) {
+        const int r = ly + 8 * i;
+        const int t = t0 + r, f = f0 + lx;
+        if (t < g.T && f <= M) zb[(int64_t)t * g.Mp + f] = make_float2(re[lx][r], im[lx][r]);
+    }
+}
+
+__device__ __forceinline__ void cp_async8(void *smem_dst, const void *gmem_src) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(d), "l"(gmem_src) : "memory");
+}
+
+// Shared-memory position of FFT element i: one pad entry after every 16, so that the strided
+// accesses of the passes (stride 16 pairs in the first radix-16 pass) spread over all banks.
+__device__ __forceinline__ int sidx(int i) { return i + (i >> 4); }
+
+// In-place inverse DFT of R points, v[q] <- sum_r v[r] e^{+2 pi i r q / R}, natural order.
+__device__ __forceinline__ void idft4(float2 &u0, float2 &u1, float2 &u2, float2 &u3) {
+    const float2 a0 = cadd(u0, u2), a1 = csub(u0, u2);
+    const float2 a2 = cadd(u1, u3), a3 = times_i(csub(u1, u3));   // e^{+2 pi i / 4} = i
+    u0 = cadd(a0, a2);
+    u1 = cadd(a1, a3);
+    u2 = csub(a0, a2);
+    u3 = csub(a1, a3);
+}
+
+// e^{+2 pi i m / 16} for m = 1 .. 9 (cos and sin of multiples of pi/8).
+__device__ __forceinline__ float2 w16(int m) {
+    constexpr float c1 = 0.92387953251128674f, s1 = 0.38268343236508979f,
+                    h = 0.70710678118654752f;
+    switch (m) {
+        case 1: return make_float2(c1, s1);
+        case 2: return make_float2(h, h);
+        case 3: return make_float2(s1, c1);
+        case 4: return make_float2(0.0f, 1.0f);
+        case 6: return make_float2(-h, h);
+        case 9: return make_float2(-c1, -s1);
+        default: return make_float2(1.0f, 0.0f);
+    }
+}
+
+template <int R>
+__device__ __forceinline__ void idft(float2 (&v)[R]) {
+    if constexpr (R == 2) {
+        const float2 a = v[0];
+        v[0] = cadd(a, v[1]);
+        v[1] = csub(a, v[1]);
+    } else if constexpr (R == 4) {
+        idft4(v[0], v[1], v[2], v[3]);
+    } else if constexpr (R == 8) {
+        // Even and odd points: two 4-point transforms, then V_q = E_q + w^q O_q and
+        // V_{q+4} = E_q - w^q O_q with w = e^{+2 pi i / 8}.
+        idft4(v[0], v[2], v[4], v[6]);
+        idft4(v[1], v[3], v[5], v[7]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float2 o = q == 0 ? v[1] : cmul(v[2 * q + 1], w16(2 * q));
+            const float2 e = v[2 * q];
+            v[2 * q] = cadd(e, o);
+            v[2 * q + 1] = csub(e, o);
+        }
+        // v[2q] holds V_q, v[2q+1] holds V_{q+4}: back to natural order.
+        float2 t[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            t[q] = v[2 * q];
+            t[q + 4] = v[2 * q + 1];
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = t[q];
+    } else {
+        static_assert(R == 16, "radix 2, 4, 8 or 16");
+        // r = 4 r1 + r2, q = q1 + 4 q2: 4-point transforms over r1 for each r2, the twiddle
+        // e^{+2 pi i r2 q1 / 16}, then 4-point transforms over r2 for each q1.
+#pragma unroll
+        for (int r2 = 0; r2 < 4; ++r2) idft4(v[r2], v[4 + r2], v[8 + r2], v[12 + r2]);
+        // v[4 q1 + r2] now holds A[r2][q1].
+#pragma unroll
+        for (int r2 = 1; r2 < 4; ++r2)
+#pragma unroll
+            for (int q1 = 1; q1 < 4; ++q1) v[4 * q1 + r2] = cmul(v[4 * q1 + r2], w16(r2 * q1));
+#pragma unroll
+        for (int q1 = 0; q1 < 4; ++q1) idft4(v[4 * q1], v[4 * q1 + 1], v[4 * q1 + 2], v[4 * q1 + 3]);
+        // v[4 q1 + q2] now holds V[q1 + 4 q2]: transpose the 4x4 index.
+        float2 t[16];
+#pragma unroll
+        for (int q1 = 0; q1 < 4; ++q1)
+#pragma unroll
+            for (int q2 = 0; q2 < 4; ++q2) t[q1 + 4 * q2] = v[4 * q1 + q2];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) v[q] = t[q];
+    }
+}
+
+// One Stockham pass of radix R over fpb frames, Ns points already combined: butterfly j reads
+// in[j + r M/R], twiddles point r by w^r, w = e^{2 pi i (j mod Ns)/(Ns R)} = tw[(j mod Ns) N/(Ns R)],
+// takes the R-point inverse DFT and writes out[(j - j mod Ns) R + j mod Ns + q Ns].
+template <int R>
+__device__ __forceinline__ void fft_pass(const float2 *in, float2 *out, const float2 *tw,
+                                         const FftGeo &g, int Ns) {
+    constexpr int kLogR = R == 2 ? 1 : R == 4 ? 2 : R == 8 ? 3 : 4;
+    const int lognb = g.logM - kLogR;
+    const int nb = 1 << lognb;
+    const int tstep = g.N / (Ns * R);
+    const int total = nb * g.fpb;
+    for (int i = threadIdx.x; i < total; i += blockDim.x) {
+        const int f = i >> lognb, j = i & (nb - 1);
+        const float2 *I = in + (size_t)f * g.Ms;
+        float2 *O = out + (size_t)f * g.Ms;
+        const int k = j & (Ns - 1);
+        float2 v[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) v[r] = I[sidx(j + r * nb)];
+        if (Ns > 1) {
+            // w^r for w = e^{2 pi i k/(Ns R)}: w^{4a} from the table, w^{4a+b} = w^{4a} w^b
+            // with w^2 = w w and w^3 = w^2 w (at most three roundings each), so a butterfly
+            // loads R/4 twiddles (one for R = 2) instead of R - 1.
+            float2 wr[R];
+            wr[1] = __ldg(&tw[k * tstep]);
+            if constexpr (R >= 4) {
+                wr[2] = cmul(wr[1], wr[1]);
+                wr[3] = cmul(wr[2], wr[1]);
+            }
+#pragma unroll
+            for (int a = 1; a < R / 4; ++a) {
+                const float2 wa = __ldg(&tw[4 * a * k * tstep]);
+                wr[4 * a] = wa;
+                wr[4 * a + 1] = cmul(wa, wr[1]);
+                wr[4 * a + 2] = cmul(wa, wr[2]);
+                wr[4 * a + 3] = cmul(wa, wr[3]);
+            }
+#pragma unroll
+            for (int r = 1; r < R; ++r) v[r] = cmul(v[r], wr[r]);
+        }
+        idft<R>(v);
+        const int o = (j - k) * R + k;
+#pragma unroll
+        for (int q = 0; q < R; ++q) O[sidx(o + q * Ns)] = v[q];
+    }
+}
+
+// One block transforms fpb consecutive frames of one batch item: copies their spectrum rows,
+// folds each into Z = E + iO (above), runs the inverse Stockham FFT and writes the windowed
+// frames, fp32, to frames[b][t][N].
 __global__ void __launch_bounds__(kFftBlock)
-irfft_frames_kernel(const float *__restrict__ spec, const float2 *__restrict__ tw,
+irfft_frames_kernel(const float2 *__restrict__ Zrows, const float2 *__restrict__ tw,
                     const float *__restrict__ win, float *__restrict__ frames, FftGeo g) {
     extern __shared__ __align__(16) unsigned char fft_smem[];
-    const int M = g.M, N = g.N, fpb = g.fpb;
-    float2 *bufA = reinterpret_cast<float2 *>(fft_smem);       // [fpb][M + 1]
-    float2 *bufB = bufA + (size_t)fpb * (M + 1);                // [fpb][M + 1]
+    const int M = g.M, N = g.N, fpb = g.fpb, Ms = g.Ms;
+    float2 *bufA = reinterpret_cast<float2 *>(fft_smem);       // [fpb][Ms]
+    float2 *bufB = bufA + (size_t)fpb * Ms;                     // [fpb][Ms]
     const int b = blockIdx.y;
     const int t0 = blockIdx.x * fpb;
     const int tid = threadIdx.x;
-    const float *sp = spec + (int64_t)b * g.C * g.T;
 
-    // 1. Spectra: bin f's real part in channel f, its imaginary part in channel M + 1 + f.
-    //    Frame fastest, so a warp reads runs of consecutive frames of a channel.  4-byte
-    //    cp.async copies: every load of the block is in flight at once.
-    const int nload = 2 * (M + 1) * fpb;
-    for (int i = tid; i < nload; i += kFftBlock) {
-        const int c = i / fpb, f = i - c * fpb;
+    // 1. Spectrum rows (bins 0..M), all copies in flight at once; frames past the end are
+    //    zeros.  Pairs 2m, 2m + 1 stay adjacent under sidx, so each copy moves 8 bytes.
+    for (int f = 0; f < fpb; ++f) {
         const int t = t0 + f;
-        float2 *X = bufA + (size_t)f * (M + 1);
-        float *dst = c <= M ? &X[c].x : &X[c - (M + 1)].y;
+        float2 *dst = bufA + (size_t)f * Ms;
         if (t < g.T) {
-            const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
-            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(d),
-                         "l"(sp + (int64_t)c * g.T + t)
-                         : "memory");
+            const float2 *src = Zrows + ((int64_t)b * g.T + t) * g.Mp;
+            for (int i = tid; i <= M; i += kFftBlock) cp_async8(dst + sidx(i), src + i);
         } else {
-            *dst = 0.0f;
+            for (int i = tid; i <= M; i += kFftBlock) dst[sidx(i)] = make_float2(0.f, 0.f);
         }
     }
     asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
@@ -114,96 +284,93 @@ irfft_frames_kernel(const float *__restrict__ spec, const float2 *__restrict__ t
     // 2. Z_k = E_k + i O_k in place; a thread owns the pair (k, M - k), which read each other.
     //    Im X_0 and Im X_M do not enter (their basis rows are zero).
     const int npair = M / 2 + 1;
-    for (int i = tid; i < npair * fpb; i += kFftBlock) {
-        const int f = i / npair, k = i - f * npair;
-        float2 *X = bufA + (size_t)f * (M + 1);
-        const int j = M - k;
-        if (k == 0) {
-            const float x0 = X[0].x, xm = X[M].x;
-            X[0] = make_float2(x0 + xm, x0 - xm);
-        } else {
-            const float2 xk = X[k], xj = X[j];
-            const float2 ek = cadd(xk, conjf2(xj)), ok = cmul(csub(xk, conjf2(xj)), tw[k]);
-            X[k] = cadd(ek, times_i(ok));
-            if (j != k) {
-                const float2 ej = cadd(xj, conjf2(xk)), oj = cmul(csub(xj, conjf2(xk)), tw[j]);
-                X[j] = cadd(ej, times_i(oj));
+    for (int f = 0; f < fpb; ++f) {
+        float2 *X = bufA + (size_t)f * Ms;
+        for (int k = tid; k < npair; k += kFftBlock) {
+            const int j = M - k;
+            if (k == 0) {
+                const float x0 = X[0].x, xm = X[sidx(M)].x;
+                X[0] = make_float2(x0 + xm, x0 - xm);
+            } else {
+                const float2 xk = X[sidx(k)], xj = X[sidx(j)];
+                const float2 ek = cadd(xk, conjf2(xj)), ok = cmul(csub(xk, conjf2(xj)), __ldg(&tw[k]));
+                X[sidx(k)] = cadd(ek, times_i(ok));
+                if (j != k) {
+                    const float2 ej = cadd(xj, conjf2(xk)), oj = cmul(csub(xj, conjf2(xk)), __ldg(&tw[j]));
+                    X[sidx(j)] = cadd(ej, times_i(oj));
+                }
             }
         }
     }
     __syncthreads();
 
-    // 3. Inverse FFT of length M (sign +).  Stage with radix R after Ns points are combined:
-    //    butterfly j reads in[j + r M/R], twiddles point r by e^{2 pi i r (j mod Ns)/(Ns R)},
-    //    takes the R-point DFT and writes out[(j - j mod Ns) R + j mod Ns + r Ns].
+    // 3. Inverse FFT of length M (sign +): one radix-2/4/8 pass for log2 M mod 4, then
+    //    radix-16 passes.
     float2 *in = bufA, *out = bufB;
     int Ns = 1;
-    if (g.logM & 1) {   // one radix-2 stage first (Ns = 1: no twiddles)
-        const int half = M / 2;
-        for (int i = tid; i < half * fpb; i += kFftBlock) {
-            const int f = i / half, j = i - f * half;
-            const float2 *I = in + (size_t)f * (M + 1);
-            float2 *O = out + (size_t)f * (M + 1);
-            const float2 a = I[j], c = I[j + half];
-            O[2 * j] = cadd(a, c);
-            O[2 * j + 1] = csub(a, c);
-        }
+    const int first = g.logM & 3;
+    if (first) {
+        if (first == 1) fft_pass<2>(in, out, tw, g, 1);
+        else if (first == 2) fft_pass<4>(in, out, tw, g, 1);
+        else fft_pass<8>(in, out, tw, g, 1);
         __syncthreads();
         float2 *t = in; in = out; out = t;
-        Ns = 2;
+        Ns = 1 << first;
     }
-    for (; Ns < M; Ns *= 4) {
-        const int quarter = M / 4;
-        const int tstep = N / (Ns * 4);    // e^{2 pi i r k / (4 Ns)} = tw[r k tstep]
-        for (int i = tid; i < quarter * fpb; i += kFftBlock) {
-            const int f = i / quarter, j = i - f * quarter;
-            const float2 *I = in + (size_t)f * (M + 1);
-            float2 *O = out + (size_t)f * (M + 1);
-            const int k = j & (Ns - 1);
-            float2 v0 = I[j], v1 = I[j + quarter], v2 = I[j + 2 * quarter], v3 = I[j + 3 * quarter];
-            if (Ns > 1) {
-                v1 = cmul(v1, tw[k * tstep]);
-                v2 = cmul(v2, tw[2 * k * tstep]);
-                v3 = cmul(v3, tw[3 * k * tstep]);
-            }
-            // 4-point inverse DFT: W = e^{+2 pi i / 4} = i.
-            const float2 a0 = cadd(v0, v2), a1 = csub(v0, v2);
-            const float2 a2 = cadd(v1, v3), a3 = times_i(csub(v1, v3));
-            const int o = (j - k) * 4 + k;
-            O[o] = cadd(a0, a2);
-            O[o + Ns] = cadd(a1, a3);
-            O[o + 2 * Ns] = csub(a0, a2);
-            O[o + 3 * Ns] = csub(a1, a3);
-        }
+    for (; Ns < M; Ns *= 16) {
+        fft_pass<16>(in, out, tw, g, Ns);
         __syncthreads();
         float2 *t = in; in = out; out = t;
     }
 
     // 4. frame[2n] = win[2n] Re z_n / N, frame[2n + 1] = win[2n + 1] Im z_n / N.
-    for (int i = tid; i < M * fpb; i += kFftBlock) {
-        const int f = i / M, n = i - f * M;
+    for (int f = 0; f < fpb; ++f) {
         const int t = t0 + f;
-        if (t >= g.T) continue;
-        const float2 z = in[(size_t)f * (M + 1) + n];
-        const float2 w2 = reinterpret_cast<const float2 *>(win)[n];
-        reinterpret_cast<float2 *>(frames + ((int64_t)b * g.T + t) * N)[n] =
-            make_float2(z.x * w2.x, z.y * w2.y);
+        if (t >= g.T) break;
+        const float2 *zr = in + (size_t)f * Ms;
+        float2 *fr = reinterpret_cast<float2 *>(frames + ((int64_t)b * g.T + t) * N);
+        for (int n = tid; n < M; n += kFftBlock) {
+            const float2 z = zr[sidx(n)];
+            const float2 w2 = __ldg(reinterpret_cast<const float2 *>(win) + n);
+            fr[n] = make_float2(z.x * w2.x, z.y * w2.y);
+        }
     }
 }
 
 struct OlaGeo {
     int T, N, hop, pad, L_out;
+    int vec;                 // 4 consecutive outputs per thread with 16-byte accesses
 };
 
 // y[b, 0, n'] = bias + sum over the frames k that cover n = n' + pad of frame_k[n - k hop],
 // in ascending k (the overlap-add of the transposed convolution, as a gather: no atomics).
 // blockIdx.y is the batch item; positions and frame offsets are 32-bit (checked at plan
-// creation), the batch item's base 64-bit.
+// creation), the batch item's base 64-bit.  With hop, pad, N and L_out multiples of 4 a
+// thread sums four consecutive outputs, which share their frames, with float4 loads and one
+// float4 store (the same sums in the same order).
 __global__ void istft_ola_kernel(const float *__restrict__ frames, const float *__restrict__ bias,
                                  float *__restrict__ y, OlaGeo g) {
     const float b0 = bias ? bias[0] : 0.0f;
     const float *fb = frames + (int64_t)blockIdx.y * g.T * g.N;
     float *yb = y + (int64_t)blockIdx.y * g.L_out;
+    if (g.vec) {
+        const int nq = g.L_out / 4;
+        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nq; i += gridDim.x * blockDim.x) {
+            const int n = 4 * i + g.pad;
+            const int k_hi = min(g.T - 1, n / g.hop);
+            const int k_lo = n >= g.N ? (n - g.N) / g.hop + 1 : 0;
+            float4 acc = make_float4(b0, b0, b0, b0);
+            for (int k = k_lo; k <= k_hi; ++k) {
+                const float4 v = __ldg(reinterpret_cast<const float4 *>(fb + (int64_t)k * (g.N - g.hop) + n));
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+            reinterpret_cast<float4 *>(yb)[i] = acc;
+        }
+        return;
+    }
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < g.L_out; i += gridDim.x * blockDim.x) {
         const int n = i + g.pad;
         const int k_hi = min(g.T - 1, n / g.hop);
@@ -215,6 +382,9 @@ __global__ void istft_ola_kernel(const float *__restrict__ frames, const float *
 }
 
 bool is_pow2(int64_t v) { return v > 0 && (v & (v - 1)) == 0; }
+// Shared-memory pitch of one frame's FFT buffer: padded positions of bins 0..M (sidx(M) + 1),
+// rounded up to an even count so every frame's buffer starts 16-byte aligned.
+int64_t fft_pitch(int64_t M) { return ((M + (M >> 4) + 1) + 1) & ~(int64_t)1; }
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 bool aligned16p(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -254,11 +424,12 @@ ctr_status ctr_istft_create(ctr_istft_t *out, int64_t N, int64_t n_fft, int64_t 
     p->dtype = dtype;
     const int64_t M = n_fft / 2;
     p->fpb = (int)std::min<int64_t>(16, std::max<int64_t>(1, 4096 / M));   // ~64 KB a block
-    p->smem = (size_t)p->fpb * 2 * (M + 1) * sizeof(float2);
+    p->smem = (size_t)p->fpb * 2 * fft_pitch(M) * sizeof(float2);
     p->off_tw = 0;
     p->off_win = align256((size_t)n_fft * sizeof(float2));
     p->off_frames = p->off_win + align256((size_t)n_fft * sizeof(float));
-    p->ws_needed = p->off_frames + (size_t)(N * frames * n_fft) * sizeof(float);
+    p->off_rows = p->off_frames + align256((size_t)(N * frames * n_fft) * sizeof(float));
+    p->ws_needed = p->off_rows + (size_t)(N * frames * (M + 2)) * sizeof(float2);
     *out = p;
     return CTR_OK;
 }
@@ -320,14 +491,20 @@ ctr_status ctr_istft_forward(ctr_istft_t p, const void *spec, const void *bias, 
         g.C = (int)(p->n_fft + 2);
         g.N = (int)p->n_fft;
         g.M = g.N / 2;
+        g.Mp = g.M + 2;
+        g.Ms = (int)fft_pitch(g.M);
         g.logM = 0;
         while ((1 << g.logM) < g.M) ++g.logM;
         g.fpb = p->fpb;
+        float2 *rows = reinterpret_cast<float2 *>(ws + p->off_rows);
+        const dim3 tgrid((unsigned)((p->frames + kTile - 1) / kTile),
+                         (unsigned)((g.M + 1 + kTile - 1) / kTile), (unsigned)p->B);
+        spectrum_rows_kernel<<<tgrid, 256, 0, st>>>(static_cast<const float *>(spec), rows, g);
         const dim3 grid((unsigned)((p->frames + p->fpb - 1) / p->fpb), (unsigned)p->B);
         irfft_frames_kernel<<<grid, kFftBlock, p->smem, st>>>(
-            static_cast<const float *>(spec), reinterpret_cast<const float2 *>(ws + p->off_tw),
+            rows, reinterpret_cast<const float2 *>(ws + p->off_tw),
             reinterpret_cast<const float *>(ws + p->off_win), frames, g);
-        count_launches(1);
+        count_launches(2);
         if (cudaGetLastError() != cudaSuccess) return CTR_ERR_CUDA;
     }
     OlaGeo o;
@@ -336,8 +513,10 @@ ctr_status ctr_istft_forward(ctr_istft_t p, const void *spec, const void *bias, 
     o.hop = (int)p->hop;
     o.pad = (int)p->pad;
     o.L_out = (int)p->L_out;
-    const dim3 ogrid((unsigned)std::min<int64_t>((p->L_out + 255) / 256, (int64_t)1 << 20),
-                     (unsigned)p->B);
+    o.vec = (p->hop % 4 == 0 && p->pad % 4 == 0 && p->n_fft % 4 == 0 && p->L_out % 4 == 0) ? 1 : 0;
+    const int64_t per_thread = o.vec ? 4 : 1;
+    const int64_t oblocks = (p->L_out / per_thread + 255) / 256;
+    const dim3 ogrid((unsigned)std::min<int64_t>(oblocks, (int64_t)1 << 20), (unsigned)p->B);
     istft_ola_kernel<<<ogrid, 256, 0, st>>>(frames, static_cast<const float *>(bias),
                                             static_cast<float *>(y), o);
     count_launches(1);
