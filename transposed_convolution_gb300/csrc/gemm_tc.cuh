@@ -17,7 +17,8 @@
 // dimension the packed weight row r (BN = 64, 128 or 256 per tile: TMEM columns), so each
 // epilogue thread owns one output position and writes its phases as contiguous runs.
 //
-// Warp roles (320 threads, one CTA per SM, persistent over output tiles):
+// Warp roles (320 threads, one CTA per SM -- two for bf16 tiles of 64 rows -- persistent over
+// output tiles):
 //   warp 0      one lane issues TMA loads of Xs and A K-slices into a ring of stages;
 //   warp 1      allocates TMEM; one lane issues tcgen05.mma into one of several TMEM
 //               accumulators (128 lanes x BN fp32 columns) and commits to mbarriers;
@@ -51,6 +52,13 @@ namespace {
 constexpr int kThreads = 320;
 constexpr int kEpiWarps = 8;
 constexpr int kSmemMax = 227 * 1024;
+
+// CTAs per SM.  A bf16 tile of 64 phase rows has only a few K slices, and its output stage
+// (one 32-column chunk per epilogue warp) takes far longer than its MMAs and loads: the
+// eight epilogue warps are issue-bound on their dependent arithmetic and store chains.  Two
+// CTAs per SM double the epilogue warps and independent tile pipelines an SM interleaves,
+// each CTA with half the shared memory (fewer stages) and 256 TMEM columns.
+constexpr int ctas_per_sm(Prec P, int BN) { return (P == Prec::BF16 && BN == 64) ? 2 : 1; }
 constexpr uint64_t kDrainLimitNs = 2000000000ull;
 
 template <Prec P, int BN>
@@ -63,7 +71,10 @@ struct Cfg {
     static constexpr int kWBytes = BN * kSlice;              // one BN-row weight slice
     static constexpr int kStageBytes = kPlanes * (kXBytes + kWBytes);
     static constexpr int kBarBytes = 256;
-    static constexpr int kStagesRaw = (kSmemMax - 1024 - kBarBytes) / kStageBytes;
+    static constexpr int kCtas = ctas_per_sm(P, BN);
+    // Two CTAs share an SM's 228 KB (each also reserves 1 KB for the system).
+    static constexpr int kSmemBudget = kCtas == 1 ? kSmemMax : 112 * 1024;
+    static constexpr int kStagesRaw = (kSmemBudget - 1024 - kBarBytes) / kStageBytes;
     static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
     static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes;
     // Grouped 3xTF32 accumulation keeps its running sums in a TMEM region of BN columns
@@ -72,7 +83,9 @@ struct Cfg {
     static constexpr bool kTmemSum = P == Prec::TF32x3 && BN >= 128;
     // TMEM accumulators: as many BN-column buffers as fit 512 columns (less the sum region),
     // at most 4, so the MMA can run several tiles ahead of the epilogue.
-    static constexpr int kAccBufs = kTmemSum ? (512 - BN) / BN : (512 / BN > 4 ? 4 : 512 / BN);
+    static constexpr int kTmemBudget = 512 / kCtas;   // TMEM columns of one CTA
+    static constexpr int kAccBufs = kTmemSum ? (kTmemBudget - BN) / BN
+                                             : (kTmemBudget / BN > 4 ? 4 : kTmemBudget / BN);
     static constexpr uint32_t kSumCol = kAccBufs * BN;       // first column of the sum region
     // With a single accumulator the first group of a tile accumulates straight into the
     // sum region (nothing to fold); the later groups go through the accumulator.
@@ -116,7 +129,7 @@ __device__ __forceinline__ void give_up(volatile int *abort, uint32_t *status, u
 }
 
 template <Prec P, int BN, bool CHAIN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapW,
                    const __grid_constant__ CUtensorMap mapX2,
                    const __grid_constant__ CUtensorMap mapW2, const GemmParams gp) {
@@ -484,7 +497,7 @@ cudaError_t launch_inst(const ctr_plan_s *pl, const CUtensorMap *maps, const Gem
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    const int64_t grid = std::min<int64_t>(gp.num_tiles, pl->num_sms);
+    const int64_t grid = std::min<int64_t>(gp.num_tiles, (int64_t)pl->num_sms * C::kCtas);
     const cudaError_t e = launch_pdl(gemm_tc_kernel<P, BN, CHAIN>, dim3((unsigned)grid),
                                      dim3(kThreads), (size_t)C::kSmem, st, maps[0], maps[1],
                                      maps[2], maps[3], gp);
