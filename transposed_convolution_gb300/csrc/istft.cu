@@ -360,12 +360,28 @@ __global__ void istft_ola_kernel(const float *__restrict__ frames, const float *
             const int k_hi = min(g.T - 1, n / g.hop);
             const int k_lo = n >= g.N ? (n - g.N) / g.hop + 1 : 0;
             float4 acc = make_float4(b0, b0, b0, b0);
-            for (int k = k_lo; k <= k_hi; ++k) {
-                const float4 v = __ldg(reinterpret_cast<const float4 *>(fb + (int64_t)k * (g.N - g.hop) + n));
-                acc.x += v.x;
-                acc.y += v.y;
-                acc.z += v.z;
-                acc.w += v.w;
+            // Up to four frames' loads in flight before the first add (hop = N/4 has four);
+            // any further frames follow one by one.  The sums keep ascending k.
+            float4 v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                v[q] = k_lo + q <= k_hi
+                           ? __ldg(reinterpret_cast<const float4 *>(fb + (int64_t)(k_lo + q) * (g.N - g.hop) + n))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (k_lo + q > k_hi) break;
+                acc.x += v[q].x;
+                acc.y += v[q].y;
+                acc.z += v[q].z;
+                acc.w += v[q].w;
+            }
+            for (int k = k_lo + 4; k <= k_hi; ++k) {
+                const float4 u = __ldg(reinterpret_cast<const float4 *>(fb + (int64_t)k * (g.N - g.hop) + n));
+                acc.x += u.x;
+                acc.y += u.y;
+                acc.z += u.z;
+                acc.w += u.w;
             }
             reinterpret_cast<float4 *>(yb)[i] = acc;
         }
