@@ -155,6 +155,44 @@ ctr_status ctr_plan_set_dilation(ctr_plan_t plan, const int64_t *dilation);
  */
 ctr_status ctr_plan_set_pads(ctr_plan_t plan, const int64_t *pads_begin, const int64_t *pads_end);
 
+/*
+ * Streaming 1-D ConvTranspose (default off): the input arrives as consecutive chunks of
+ * L_in frames (a streaming audio decoder's upsampler), and each ctr_forward emits the
+ * s*L_in output samples that its frames complete.  Concatenated, the outputs of a stream are
+ * the unpadded ConvTranspose of the concatenated input, (L - 1)*s + k samples, without its
+ * last k - s ("[XNNPACK] Lower dense transposed convs as one polyphase conv + depth to
+ * space", Test plan and the Phonon fix: the overlap-add of a streaming decoder).  Those last
+ * samples come out with the following chunk; zero frames flush them at the end of a stream.
+ *
+ * The polyphase form makes the state an input state. Output phase position q reads frames
+ * q - (m - 1) .. q (m = ceil(k/s)). So the plan carries each batch item's last m - 1
+ * input frames in its workspace and puts them in front of the next chunk. The
+ * not-yet-complete output samples are not held back. Any chunk length works, including
+ * chunks shorter than m - 1 frames.
+ *
+ * Requires: 1-D, padding = output_padding = 0, k >= s, one group, no dilation,
+ * m - 1 <= 16, and the polyphase path.  The path is forced; a plan that cannot take it returns
+ * CTR_ERR_UNSUPPORTED and stays unchanged.  Afterwards ctr_plan_output_shape reports
+ * s*L_in. ctr_workspace_bytes includes the carried frames, B*(m - 1) staged rows.
+ * ctr_plan_stream_reset must zero them before the first ctr_forward, after every
+ * ctr_plan_bind_workspace, and to start a new stream (CTR_ERR_NOT_PREPARED otherwise).
+ * Calls of one stream must run in stream order, one at a time: each reads the frames the
+ * previous one carried.  ctr_forward_noalloc refuses streaming plans
+ * (CTR_ERR_UNSUPPORTED).
+ *
+ * Host only, with the same ordering rule as ctr_plan_set_path.  CTR_ERR_INVALID_ARG for
+ * enable not 0 or 1, after ctr_prepack_weight, or on a chained plan.  Once streaming, a
+ * plan refuses ctr_plan_set_groups, _set_dilation, _set_pads and ctr_plan_chain
+ * (CTR_ERR_INVALID_ARG), and ctr_plan_set_path with any path but the polyphase one
+ * (CTR_ERR_UNSUPPORTED).  enable = 0 restores the plain plan.
+ */
+ctr_status ctr_plan_set_streaming(ctr_plan_t plan, int enable);
+
+/* Zero a streaming plan's carried input frames (asynchronous on `stream`): the next
+ * ctr_forward starts a new stream.  CTR_ERR_INVALID_ARG when the plan is not streaming,
+ * CTR_ERR_NO_WORKSPACE when its workspace is unbound or too small. */
+ctr_status ctr_plan_stream_reset(ctr_plan_t plan, void *stream);
+
 /* Fuse an activation into the output stage (default CTR_ACT_NONE).  Host only. */
 ctr_status ctr_plan_set_activation(ctr_plan_t plan, int act, float negative_slope);
 

@@ -319,6 +319,64 @@ def test_dilation_and_pads_without_gpu(ctr):
         ctr.ctr_plan_destroy(b)
 
 
+def test_streaming_plan_without_gpu(ctr):
+    """ctr_plan_set_streaming: 1-D polyphase plans without padding emit s*L_in samples a call,
+    carry B*(m - 1) staged frames in the workspace, and refuse what they cannot stream."""
+    f32, bf = ctr.CTR_F32, ctr.CTR_BF16
+    h = _plan(ctr, 1, 2, 64, 32, [50], [16], [8], [0], [0], bf)
+    try:
+        ws0 = ctr.ctr_workspace_bytes(h)
+        ctr.ctr_plan_set_streaming(h, 1)
+        assert ctr.ctr_plan_output_shape(h, 1) == (8 * 50,)
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_POLYPHASE
+        assert ctr.ctr_workspace_bytes(h) >= ws0 + 2 * 1 * 64 * 2   # B * (m - 1) rows
+        for bad in (lambda: ctr.lib.ctr_plan_set_groups(h, 2),
+                    lambda: ctr.lib.ctr_plan_set_dilation(h, ctr._arr([2])),
+                    lambda: ctr.lib.ctr_plan_set_pads(h, ctr._arr([1]), ctr._arr([1]))):
+            assert bad() == ctr.CTR_ERR_INVALID_ARG
+        assert ctr.lib.ctr_plan_set_path(h, ctr.CTR_PATH_GATHER, 0) == ctr.CTR_ERR_UNSUPPORTED
+        assert ctr.lib.ctr_plan_set_streaming(h, 2) == ctr.CTR_ERR_INVALID_ARG
+        ctr.ctr_plan_set_streaming(h, 0)
+        assert ctr.ctr_plan_output_shape(h, 1) == (49 * 8 + 16,)
+        assert ctr.lib.ctr_plan_stream_reset(h, None) == ctr.CTR_ERR_INVALID_ARG
+    finally:
+        ctr.ctr_plan_destroy(h)
+    # k mod s != 0 and tiny channels: forced onto the zero-padded polyphase path
+    h = _plan(ctr, 1, 1, 32, 32, [40], [5], [2], [0], [0], f32)
+    try:
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_COL2IM
+        ctr.ctr_plan_set_streaming(h, 1)
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_POLYPHASE
+        assert ctr.ctr_plan_output_shape(h, 1) == (80,)
+    finally:
+        ctr.ctr_plan_destroy(h)
+    for args in ([2, 1, 64, 32, [8, 8], [4, 4], [2, 2], [0, 0], [0, 0], f32],   # 2-D
+                 [1, 1, 64, 32, [50], [4], [2], [1], [0], f32],                  # padding
+                 [1, 1, 64, 32, [50], [4], [2], [0], [1], f32],                  # output_padding
+                 [1, 1, 64, 32, [50], [2], [4], [0], [0], f32],                  # k < s
+                 [1, 1, 64, 32, [50], [40], [2], [0], [0], f32]):                # m - 1 > 16
+        h = _plan(ctr, *args)
+        try:
+            out = ctr.ctr_plan_output_shape(h, args[0])
+            assert ctr.lib.ctr_plan_set_streaming(h, 1) == ctr.CTR_ERR_UNSUPPORTED
+            assert ctr.ctr_plan_output_shape(h, args[0]) == out
+        finally:
+            ctr.ctr_plan_destroy(h)
+    a = _plan(ctr, 1, 1, 64, 32, [100], [4], [2], [0], [0], bf)
+    b = _plan(ctr, 1, 1, 32, 64, [202], [4], [2], [0], [0], bf)
+    try:
+        ctr.ctr_plan_set_streaming(a, 1)
+        assert ctr.lib.ctr_plan_chain(a, b) == ctr.CTR_ERR_INVALID_ARG
+        ctr.ctr_plan_set_streaming(a, 0)
+        ctr.ctr_plan_chain(a, b)
+        assert ctr.lib.ctr_plan_set_streaming(a, 1) == ctr.CTR_ERR_INVALID_ARG
+        assert ctr.lib.ctr_plan_set_streaming(b, 1) == ctr.CTR_ERR_INVALID_ARG
+    finally:
+        ctr.ctr_plan_chain(a, None)
+        ctr.ctr_plan_destroy(a)
+        ctr.ctr_plan_destroy(b)
+
+
 def test_istft_plan_without_gpu(ctr):
     """ctr_istft_*: argument checks, output length, workspace size; no window -> not prepared."""
     h = ctr.ctr_istft_create(4, 4096, 1024, 343)

@@ -7,6 +7,7 @@ any non-OK status from the library raises ``CtrError``.
 
 Low level (same names as the C ABI): ``ctr_plan_create``, ``ctr_plan_set_activation``,
 ``ctr_plan_set_path``, ``ctr_plan_set_groups``, ``ctr_plan_set_dilation``, ``ctr_plan_set_pads``,
+``ctr_plan_set_streaming``, ``ctr_plan_stream_reset``,
 ``ctr_plan_set_tile``, ``ctr_plan_chain``, ``ctr_plan_get_path``, ``ctr_plan_output_shape``,
 ``ctr_packed_weight_bytes``, ``ctr_workspace_bytes``, ``ctr_plan_bind_workspace``,
 ``ctr_prepack_weight``, ``ctr_forward``, ``ctr_forward_noalloc``, ``ctr_plan_check``,
@@ -63,6 +64,8 @@ SIGNATURES = {
     "ctr_plan_set_groups": (ctypes.c_int, [_vp, ctypes.c_int64]),
     "ctr_plan_set_dilation": (ctypes.c_int, [_vp, _i64p]),
     "ctr_plan_set_pads": (ctypes.c_int, [_vp, _i64p, _i64p]),
+    "ctr_plan_set_streaming": (ctypes.c_int, [_vp, ctypes.c_int]),
+    "ctr_plan_stream_reset": (ctypes.c_int, [_vp, _vp]),
     "ctr_plan_set_tile": (ctypes.c_int, [_vp, ctypes.c_int]),
     "ctr_plan_chain": (ctypes.c_int, [_vp, _vp]),
     "ctr_plan_get_path": (ctypes.c_int, [_vp]),
@@ -183,6 +186,14 @@ def ctr_plan_set_dilation(plan, dilation):
 
 def ctr_plan_set_pads(plan, pads_begin, pads_end):
     _check(lib.ctr_plan_set_pads(plan, _arr(pads_begin), _arr(pads_end)), "ctr_plan_set_pads")
+
+
+def ctr_plan_set_streaming(plan, enable):
+    _check(lib.ctr_plan_set_streaming(plan, int(enable)), "ctr_plan_set_streaming")
+
+
+def ctr_plan_stream_reset(plan, stream):
+    _check(lib.ctr_plan_stream_reset(plan, stream), "ctr_plan_stream_reset")
 
 
 def ctr_plan_set_tile(plan, block_n):
@@ -338,7 +349,8 @@ class Plan:
 
     def __init__(self, N, C_in, C_out, in_spatial, kernel, stride=1, padding=0,
                  output_padding=0, dtype=None, negative_slope=None, path=CTR_PATH_AUTO,
-                 split_k=0, device=None, block_n=0, groups=1, dilation=1, padding_end=None):
+                 split_k=0, device=None, block_n=0, groups=1, dilation=1, padding_end=None,
+                 streaming=False):
         torch = _torch()
         self.ndim = len(in_spatial)
         self.dtype = dtype if dtype is not None else torch.float32
@@ -364,6 +376,9 @@ class Plan:
                 ctr_plan_set_dilation(self.handle, self.dilation)
             if self.padding_end != self.padding:
                 ctr_plan_set_pads(self.handle, self.padding, self.padding_end)
+            self.streaming = bool(streaming)
+            if self.streaming:
+                ctr_plan_set_streaming(self.handle, 1)
             if path != CTR_PATH_AUTO or split_k:
                 ctr_plan_set_path(self.handle, path, split_k)
             if block_n:
@@ -377,6 +392,8 @@ class Plan:
                 self.workspace = torch.empty(self.workspace_bytes, dtype=torch.uint8,
                                              device=self.device)
                 ctr_plan_bind_workspace(self.handle, _ptr(self.workspace), self.workspace_bytes)
+            if self.streaming:
+                ctr_plan_stream_reset(self.handle, _stream_ptr(None))
         except Exception:
             ctr_plan_destroy(self.handle)
             self.handle = None
@@ -430,6 +447,10 @@ class Plan:
         ctr_forward(self.handle, _ptr(x), _ptr(self.w_packed), _ptr(bias), _ptr(y),
                     _stream_ptr(stream))
         return y
+
+    def stream_reset(self, stream=None):
+        """Start a new stream: zero the carried input frames (streaming plans)."""
+        ctr_plan_stream_reset(self.handle, _stream_ptr(stream))
 
     def check(self, stream=None):
         ctr_plan_check(self.handle, _stream_ptr(stream))

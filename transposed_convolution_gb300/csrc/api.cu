@@ -144,6 +144,9 @@ int64_t dilated_extent(const ctr_plan_s *pl, int d) { return (pl->k[d] - 1) * pl
 // Output length of dimension d: (L_in - 1)*s + (k - 1)*dil + 1 + op - p_front - p_back,
 // i.e. (L_in - 1)*s - 2p + k + op without dilation and with equal pads.
 int64_t output_length(const ctr_plan_s *pl, int d) {
+    // A streaming plan emits the s*L_in samples its input frames complete (see
+    // ctr_plan_set_streaming); its padding is 0.
+    if (pl->streaming && d == 1) return pl->in[1] * pl->s[1];
     return (pl->in[d] - 1) * pl->s[d] + dilated_extent(pl, d) + pl->op[d] - pl->p[d] - pl->pe[d];
 }
 
@@ -218,6 +221,13 @@ void layout_plan(ctr_plan_s *pl) {
         pl->ws_off_raw = off;
         pl->ws_raw_bytes = (size_t)ctr::raw_split_stride_of(pl) * pl->splits * sizeof(float);
         off = align256(off + pl->ws_raw_bytes);
+    }
+    pl->ws_off_state = pl->ws_state_bytes = 0;
+    if (pl->streaming && pl->m[1] > 1) {
+        pl->ws_off_state = off;
+        pl->ws_state_bytes =
+            (size_t)pl->B * (pl->m[1] - 1) * pl->C_in_pad * op_esize(pl) * op_planes(pl);
+        off = align256(off + pl->ws_state_bytes);
     }
     pl->ws_bytes_needed = (pl->ws_stage_bytes || pl->ws_raw_bytes) ? off : 0;
 }
@@ -394,6 +404,9 @@ cudaError_t run_tc_path(const ctr_plan_s *pl, const void *x, const void *w_packe
     void *xs = ws + pl->ws_off_stage;
     float *raw = pl->ws_raw_bytes ? reinterpret_cast<float *>(ws + pl->ws_off_raw) : nullptr;
     if (!staged_in && (e = launch_stage_x(pl, x, xs, st)) != cudaSuccess) return e;
+    if (pl->streaming &&
+        (e = launch_stream_state(pl, xs, ws + pl->ws_off_state, st)) != cudaSuccess)
+        return e;
 
     const bool bf16 = pl->dtype == CTR_BF16;
     const int es = bf16 ? 2 : 4;
@@ -604,13 +617,16 @@ ctr_status ctr_plan_set_path(ctr_plan_t pl, int path, int split_k) {
     if (!pl || path < CTR_PATH_AUTO || path > CTR_PATH_DEPTHWISE || split_k < 0 || split_k > 16)
         return CTR_ERR_INVALID_ARG;
     if (pl->prepared) return CTR_ERR_INVALID_ARG;
+    if (pl->streaming && path != CTR_PATH_POLYPHASE && path != CTR_PATH_AUTO)
+        return CTR_ERR_UNSUPPORTED;   // the carried frames are polyphase halo rows
+    if (pl->streaming) path = CTR_PATH_POLYPHASE;
     return reroute(pl, path, split_k, pl->groups);
 }
 
 ctr_status ctr_plan_set_groups(ctr_plan_t pl, int64_t groups) {
     if (!pl || groups < 1 || pl->C_in % groups != 0 || pl->C_out % groups != 0)
         return CTR_ERR_INVALID_ARG;
-    if (pl->prepared || pl->chain_next || pl->chain_prev) return CTR_ERR_INVALID_ARG;
+    if (pl->prepared || pl->chain_next || pl->chain_prev || pl->streaming) return CTR_ERR_INVALID_ARG;
     return reroute(pl, pl->forced_path, pl->forced_split, groups);
 }
 
@@ -656,7 +672,7 @@ ctr_status set_geometry(ctr_plan_s *pl, const int64_t (&dil)[2], const int64_t (
 
 ctr_status ctr_plan_set_dilation(ctr_plan_t pl, const int64_t *dilation) {
     if (!pl || !dilation) return CTR_ERR_INVALID_ARG;
-    if (pl->prepared || pl->chain_next || pl->chain_prev) return CTR_ERR_INVALID_ARG;
+    if (pl->prepared || pl->chain_next || pl->chain_prev || pl->streaming) return CTR_ERR_INVALID_ARG;
     int64_t dil[2] = {1, 1};
     for (int d = 0; d < pl->ndim; ++d) dil[d + (2 - pl->ndim)] = dilation[d];
     const int64_t pb[2] = {pl->p[0], pl->p[1]}, pe[2] = {pl->pe[0], pl->pe[1]};
@@ -665,7 +681,7 @@ ctr_status ctr_plan_set_dilation(ctr_plan_t pl, const int64_t *dilation) {
 
 ctr_status ctr_plan_set_pads(ctr_plan_t pl, const int64_t *pads_begin, const int64_t *pads_end) {
     if (!pl || !pads_begin || !pads_end) return CTR_ERR_INVALID_ARG;
-    if (pl->prepared || pl->chain_next || pl->chain_prev) return CTR_ERR_INVALID_ARG;
+    if (pl->prepared || pl->chain_next || pl->chain_prev || pl->streaming) return CTR_ERR_INVALID_ARG;
     int64_t pb[2] = {0, 0}, pe[2] = {0, 0};
     for (int d = 0; d < pl->ndim; ++d) {
         pb[d + (2 - pl->ndim)] = pads_begin[d];
@@ -673,6 +689,52 @@ ctr_status ctr_plan_set_pads(ctr_plan_t pl, const int64_t *pads_begin, const int
     }
     const int64_t dil[2] = {pl->dil[0], pl->dil[1]};
     return set_geometry(pl, dil, pb, pe);
+}
+
+ctr_status ctr_plan_set_streaming(ctr_plan_t pl, int enable) {
+    if (!pl || (enable != 0 && enable != 1)) return CTR_ERR_INVALID_ARG;
+    if (pl->prepared || pl->chain_next || pl->chain_prev) return CTR_ERR_INVALID_ARG;
+    if (enable == pl->streaming) return CTR_OK;
+    if (!enable) {
+        pl->streaming = 0;
+        pl->stream_ready = 0;
+        set_output_lengths(pl);
+        return reroute(pl, CTR_PATH_AUTO, pl->forced_split, pl->groups);
+    }
+    // 1-D, no padding or output_padding, k >= s, one group, undilated, and a carry of at
+    // most kMaxStreamCarry frames on the polyphase path.
+    if (pl->ndim != 1 || pl->p[1] != 0 || pl->pe[1] != 0 || pl->op[1] != 0 || pl->k[1] < pl->s[1] ||
+        pl->groups != 1 || pl->dil[1] != 1 || ceil_div(pl->k[1], pl->s[1]) - 1 > ctr::kMaxStreamCarry)
+        return CTR_ERR_UNSUPPORTED;
+    if (pl->in[1] < 1) return CTR_ERR_INVALID_ARG;
+    const int64_t old_out = pl->out[1];
+    pl->streaming = 1;
+    if (!set_output_lengths(pl)) {
+        pl->streaming = 0;
+        pl->out[1] = old_out;
+        return CTR_ERR_INVALID_ARG;
+    }
+    const ctr_status st = reroute(pl, CTR_PATH_POLYPHASE, pl->forced_split, pl->groups);
+    if (st != CTR_OK) {
+        pl->streaming = 0;
+        pl->out[1] = old_out;
+        reroute(pl, CTR_PATH_AUTO, pl->forced_split, pl->groups);
+        return st;
+    }
+    pl->stream_ready = 0;
+    return CTR_OK;
+}
+
+ctr_status ctr_plan_stream_reset(ctr_plan_t pl, void *stream) {
+    if (!pl || !pl->streaming) return CTR_ERR_INVALID_ARG;
+    if (pl->ws_bytes_needed > 0 && (!pl->ws || pl->ws_bytes < pl->ws_bytes_needed))
+        return CTR_ERR_NO_WORKSPACE;
+    if (pl->ws_state_bytes &&
+        cudaMemsetAsync(static_cast<char *>(pl->ws) + pl->ws_off_state, 0, pl->ws_state_bytes,
+                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return CTR_ERR_CUDA;
+    pl->stream_ready = 1;
+    return CTR_OK;
 }
 
 ctr_status ctr_plan_set_tile(ctr_plan_t pl, int block_n) {
@@ -702,6 +764,7 @@ ctr_status ctr_plan_bind_workspace(ctr_plan_t pl, void *ptr, size_t bytes) {
     if (bytes < pl->ws_bytes_needed) return CTR_ERR_NO_WORKSPACE;
     pl->ws = ptr;
     pl->ws_bytes = bytes;
+    pl->stream_ready = 0;   // the carried frames live in the workspace
     return CTR_OK;
 }
 
@@ -786,6 +849,7 @@ ctr_status ctr_forward(ctr_plan_t pl, const void *x, const void *w_packed, const
         return CTR_ERR_MISALIGNED;
     if (pl->ws_bytes_needed > 0 && (!pl->ws || pl->ws_bytes < pl->ws_bytes_needed))
         return CTR_ERR_NO_WORKSPACE;
+    if (pl->streaming && !pl->stream_ready) return CTR_ERR_NOT_PREPARED;
     if (nx) {
         if (!chain_compatible(pl, nx)) return CTR_ERR_INVALID_ARG;
         if (!nx->ws || nx->ws_bytes < nx->ws_bytes_needed) return CTR_ERR_NO_WORKSPACE;
@@ -831,7 +895,8 @@ ctr_status ctr_plan_chain(ctr_plan_t pl, ctr_plan_t nx) {
         layout_plan(pl);
         return CTR_OK;
     }
-    if (nx == pl || !chain_compatible(pl, nx)) return CTR_ERR_INVALID_ARG;
+    if (nx == pl || !chain_compatible(pl, nx) || pl->streaming || nx->streaming)
+        return CTR_ERR_INVALID_ARG;
     if (nx->chain_prev && nx->chain_prev != pl) return CTR_ERR_INVALID_ARG;
     if (pl->chain_next && pl->chain_next != nx) pl->chain_next->chain_prev = nullptr;
     pl->chain_next = nx;

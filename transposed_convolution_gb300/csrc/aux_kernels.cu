@@ -425,6 +425,48 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ raw, EpiParams ep
     emit_cols<true>(v, decode_pos(n, ep), r0, ep, (int)(threadIdx.x & 31));
 }
 
+// -------------------------------------------------------------------------- streaming
+// A streaming 1-D plan computes its call's s*L output samples from the staged input with the
+// previous call's last m - 1 frames in the leading halo (the polyphase conv reads frames
+// q - (m - 1) .. q for phase position q).  One thread per (batch item, staged element column
+// c, plane): it reads the carried frames and the new last frames first, then writes the halo
+// and the new carried frames, so no element is read after another thread wrote it.  With
+// fewer than m - 1 new frames the older carried frames shift down.
+//   staged rows of batch item b: b*P + r, r = (m - 1) + frame;  state rows: b*(m - 1) + i
+template <typename E>
+__global__ void stream_state_kernel(E *__restrict__ xs, E *__restrict__ state, int64_t B,
+                                    int64_t P, int64_t L, int carry, int64_t row_elems,
+                                    int64_t xs_plane, int64_t st_plane, int planes) {
+    const int64_t total = B * row_elems * planes;
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t c = idx % row_elems;
+        const int64_t rest = idx / row_elems;
+        const int plane = (int)(rest % planes);
+        const int64_t b = rest / planes;
+        E *xp = xs + plane * xs_plane + b * P * row_elems + c;
+        E *sp = state + plane * st_plane + b * carry * row_elems + c;
+        E old[kMaxStreamCarry], nxt[kMaxStreamCarry];
+#pragma unroll
+        for (int i = 0; i < kMaxStreamCarry; ++i) {
+            if (i >= carry) break;
+            old[i] = sp[(int64_t)i * row_elems];
+        }
+#pragma unroll
+        for (int i = 0; i < kMaxStreamCarry; ++i) {
+            if (i >= carry) break;
+            // frame L - carry + i of this call: staged row L + i, or an older carried frame
+            nxt[i] = L + i < carry ? old[L + i] : xp[(L + i) * row_elems];
+        }
+#pragma unroll
+        for (int i = 0; i < kMaxStreamCarry; ++i) {
+            if (i >= carry) break;
+            xp[(int64_t)i * row_elems] = old[i];
+            sp[(int64_t)i * row_elems] = nxt[i];
+        }
+    }
+}
+
 // -------------------------------------------------------------------------- col2im
 // y[b, oc, oy, ox] = bias + sum of col[(b, iy, ix), (oc, ty, tx)] over the taps that reach
 // (oy, ox) (the same divisibility rule as the gather kernel), summed over split-K partials
@@ -527,6 +569,27 @@ cudaError_t launch_prepack(const ctr_plan_s *pl, const void *w, void *w_packed, 
     pg.block_n = pl->block_n;
     const int64_t total = pg.M_pad * pg.K_total;
     prepack_kernel<<<grid_for(total, kBlock), kBlock, 0, st>>>(w, w_packed, pg);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_stream_state(const ctr_plan_s *pl, void *xs, void *state, cudaStream_t st) {
+    const int carry = (int)(pl->m[1] - 1);
+    if (carry <= 0) return cudaSuccess;
+    const bool bf16 = pl->dtype == CTR_BF16;
+    const int planes = bf16 ? 1 : 2;
+    const int64_t xs_plane = pl->N_total * pl->C_in_pad;         // elements per staged plane
+    const int64_t st_plane = pl->B * carry * pl->C_in_pad;
+    const int64_t total = pl->B * pl->C_in_pad * planes;
+    if (bf16) {
+        stream_state_kernel<uint16_t><<<grid_for(total, kBlock), kBlock, 0, st>>>(
+            static_cast<uint16_t *>(xs), static_cast<uint16_t *>(state), pl->B, pl->P[1],
+            pl->in[1], carry, pl->C_in_pad, xs_plane, st_plane, planes);
+    } else {
+        stream_state_kernel<uint32_t><<<grid_for(total, kBlock), kBlock, 0, st>>>(
+            static_cast<uint32_t *>(xs), static_cast<uint32_t *>(state), pl->B, pl->P[1],
+            pl->in[1], carry, pl->C_in_pad, xs_plane, st_plane, planes);
+    }
     count_launches(1);
     return cudaGetLastError();
 }

@@ -93,6 +93,8 @@ struct ctr_plan_s {
     int64_t in[2], k[2], s[2], p[2], op[2], out[2];
     int64_t dil[2];     // dilation (ctr_plan_set_dilation; 1 = none)
     int64_t pe[2];      // back pad (ctr_plan_set_pads; p is the front pad; default pe = p)
+    int streaming;      // ctr_plan_set_streaming: carries the last m - 1 input frames
+    int stream_ready;   // the carried frames were zeroed (ctr_plan_stream_reset)
     int dtype;
     int act;
     float slope;
@@ -126,6 +128,8 @@ struct ctr_plan_s {
     size_t ws_stage_bytes;
     size_t ws_off_raw;     // split-K partials or the col2im column buffer
     size_t ws_raw_bytes;
+    size_t ws_off_state;   // streaming: the last m - 1 staged input frames of each batch item
+    size_t ws_state_bytes;
     void *ws;
     size_t ws_bytes;
 
@@ -181,6 +185,11 @@ cudaError_t launch_copy_weight(const ctr_plan_s *pl, const void *w, void *w_pack
                                cudaStream_t st);
 cudaError_t launch_prepack(const ctr_plan_s *pl, const void *w, void *w_packed, cudaStream_t st);
 cudaError_t launch_stage_x(const ctr_plan_s *pl, const void *x, void *xs, cudaStream_t st);
+// Streaming plans: move the carried input frames into the staged input's leading halo and
+// this call's last m - 1 frames into the carried state.
+cudaError_t launch_stream_state(const ctr_plan_s *pl, void *xs, void *state, cudaStream_t st);
+// Most frames a streaming plan carries (m - 1).
+constexpr int kMaxStreamCarry = 16;
 cudaError_t launch_splitk_reduce(const ctr_plan_s *pl, const float *raw, const EpiParams &ep,
                                  int64_t raw_ld, int64_t split_stride, cudaStream_t st);
 // Leading dimension (floats) and split stride of the raw [z][n][r] buffer of a plan.

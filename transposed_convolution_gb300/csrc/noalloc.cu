@@ -53,6 +53,7 @@ cudaError_t scratch_address(void **out) {
 extern "C" ctr_status ctr_forward_noalloc(ctr_plan_t pl, const void *x, const void *w,
                                           const void *bias, void *y, void *stream) {
     if (!pl || pl->chain_next) return CTR_ERR_INVALID_ARG;   // chaining needs bound workspaces
+    if (pl->streaming) return CTR_ERR_UNSUPPORTED;   // carried frames need a bound workspace
     if (!w || !y || (!x && pl->B * pl->C_in * pl->in[0] * pl->in[1] > 0))
         return CTR_ERR_INVALID_ARG;
     if ((x && !aligned16(x)) || !aligned16(w) || !aligned16(y) || (bias && !aligned16(bias)))
