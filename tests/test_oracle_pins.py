@@ -68,6 +68,29 @@ def test_output_size_dilated_matches_torch_shapes():
     assert oracle.output_size(2, 3, 2, 0, 0, 2, 3) == 4
 
 
+def test_streaming_chunks_with_carried_frames_equal_whole_input():
+    """The streaming reading: with the last m - 1 frames of the previous chunk (zeros at the
+    start) put in front of each chunk, the s*L samples at s*(m - 1) .. s*(m - 1 + L) of that
+    extended chunk's unpadded ConvTranspose are exactly samples s*c*L .. s*(c + 1)*L of the
+    whole input's.  Chunks shorter than m - 1 take older frames along."""
+    rng = np.random.default_rng(17)
+    for (C_in, C_out, k, s, L, nchunks) in ((3, 2, 16, 8, 5, 4), (2, 3, 6, 2, 1, 6),
+                                            (2, 2, 5, 2, 3, 3), (1, 2, 4, 4, 2, 3)):
+        m = -(-k // s)
+        x = rng.standard_normal((2, C_in, L * nchunks))
+        w = rng.standard_normal((C_in, C_out, k))
+        b = rng.standard_normal(C_out)
+        whole = oracle.conv_transpose(x, w, b, s, 0, 0)
+        carried = np.zeros((2, C_in, m - 1))
+        for c in range(nchunks):
+            chunk = x[:, :, c * L:(c + 1) * L]
+            ext = np.concatenate([carried, chunk], axis=2)
+            y = oracle.conv_transpose(ext, w, b, s, 0, 0)[:, :, s * (m - 1):s * (m - 1 + L)]
+            np.testing.assert_allclose(y, whole[:, :, s * c * L:s * (c + 1) * L], rtol=1e-12,
+                                       atol=1e-12)
+            carried = ext[:, :, ext.shape[2] - (m - 1):]
+
+
 def test_landed_count_long_input():
     """"[WebGPU] optimizations for audio models", review of the chunked col2im: X =
     [1, 16, 262144], W = [16, 1, 4096], stride 1 has about 1e9 contributions after the GEMM
