@@ -184,7 +184,7 @@ ctr_status ctr_plan_set_pads(ctr_plan_t plan, const int64_t *pads_begin, const i
  * enable not 0 or 1, after ctr_prepack_weight, or on a chained plan.  Once streaming, a
  * plan refuses ctr_plan_set_groups, _set_dilation, _set_pads and ctr_plan_chain
  * (CTR_ERR_INVALID_ARG), and ctr_plan_set_path with any path but the polyphase one
- * (CTR_ERR_UNSUPPORTED).  enable = 0 restores the plain plan.
+ * (CTR_ERR_UNSUPPORTED).  enable = 0 restores the plain plan, with the automatic path.
  */
 ctr_status ctr_plan_set_streaming(ctr_plan_t plan, int enable);
 

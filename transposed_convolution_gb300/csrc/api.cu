@@ -626,7 +626,8 @@ ctr_status ctr_plan_set_path(ctr_plan_t pl, int path, int split_k) {
 ctr_status ctr_plan_set_groups(ctr_plan_t pl, int64_t groups) {
     if (!pl || groups < 1 || pl->C_in % groups != 0 || pl->C_out % groups != 0)
         return CTR_ERR_INVALID_ARG;
-    if (pl->prepared || pl->chain_next || pl->chain_prev || pl->streaming) return CTR_ERR_INVALID_ARG;
+    if (pl->prepared || pl->chain_next || pl->chain_prev || pl->streaming)
+        return CTR_ERR_INVALID_ARG;
     return reroute(pl, pl->forced_path, pl->forced_split, groups);
 }
 
@@ -672,7 +673,8 @@ ctr_status set_geometry(ctr_plan_s *pl, const int64_t (&dil)[2], const int64_t (
 
 ctr_status ctr_plan_set_dilation(ctr_plan_t pl, const int64_t *dilation) {
     if (!pl || !dilation) return CTR_ERR_INVALID_ARG;
-    if (pl->prepared || pl->chain_next || pl->chain_prev || pl->streaming) return CTR_ERR_INVALID_ARG;
+    if (pl->prepared || pl->chain_next || pl->chain_prev || pl->streaming)
+        return CTR_ERR_INVALID_ARG;
     int64_t dil[2] = {1, 1};
     for (int d = 0; d < pl->ndim; ++d) dil[d + (2 - pl->ndim)] = dilation[d];
     const int64_t pb[2] = {pl->p[0], pl->p[1]}, pe[2] = {pl->pe[0], pl->pe[1]};
@@ -681,7 +683,8 @@ ctr_status ctr_plan_set_dilation(ctr_plan_t pl, const int64_t *dilation) {
 
 ctr_status ctr_plan_set_pads(ctr_plan_t pl, const int64_t *pads_begin, const int64_t *pads_end) {
     if (!pl || !pads_begin || !pads_end) return CTR_ERR_INVALID_ARG;
-    if (pl->prepared || pl->chain_next || pl->chain_prev || pl->streaming) return CTR_ERR_INVALID_ARG;
+    if (pl->prepared || pl->chain_next || pl->chain_prev || pl->streaming)
+        return CTR_ERR_INVALID_ARG;
     int64_t pb[2] = {0, 0}, pe[2] = {0, 0};
     for (int d = 0; d < pl->ndim; ++d) {
         pb[d + (2 - pl->ndim)] = pads_begin[d];
@@ -703,11 +706,13 @@ ctr_status ctr_plan_set_streaming(ctr_plan_t pl, int enable) {
     }
     // 1-D, no padding or output_padding, k >= s, one group, undilated, and a carry of at
     // most kMaxStreamCarry frames on the polyphase path.
-    if (pl->ndim != 1 || pl->p[1] != 0 || pl->pe[1] != 0 || pl->op[1] != 0 || pl->k[1] < pl->s[1] ||
-        pl->groups != 1 || pl->dil[1] != 1 || ceil_div(pl->k[1], pl->s[1]) - 1 > ctr::kMaxStreamCarry)
+    if (pl->ndim != 1 || pl->p[1] != 0 || pl->pe[1] != 0 || pl->op[1] != 0 ||
+        pl->k[1] < pl->s[1] || pl->groups != 1 || pl->dil[1] != 1 ||
+        ceil_div(pl->k[1], pl->s[1]) - 1 > ctr::kMaxStreamCarry)
         return CTR_ERR_UNSUPPORTED;
     if (pl->in[1] < 1) return CTR_ERR_INVALID_ARG;
     const int64_t old_out = pl->out[1];
+    const int old_path = pl->forced_path;
     pl->streaming = 1;
     if (!set_output_lengths(pl)) {
         pl->streaming = 0;
@@ -715,10 +720,10 @@ ctr_status ctr_plan_set_streaming(ctr_plan_t pl, int enable) {
         return CTR_ERR_INVALID_ARG;
     }
     const ctr_status st = reroute(pl, CTR_PATH_POLYPHASE, pl->forced_split, pl->groups);
-    if (st != CTR_OK) {
+    if (st != CTR_OK) {   // the plan as it was, its forced path included
         pl->streaming = 0;
         pl->out[1] = old_out;
-        reroute(pl, CTR_PATH_AUTO, pl->forced_split, pl->groups);
+        reroute(pl, old_path, pl->forced_split, pl->groups);
         return st;
     }
     pl->stream_ready = 0;
