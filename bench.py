@@ -1,26 +1,33 @@
 """Benchmark: ConvTranspose GFLOP/s and fraction of roofline per call on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--all]
+                    [--workload NAME] [--no-graph]
 
-One step is one ctr_forward over one batch of the workload (input staging, the tensor-core
-GEMM with its fused output stage, and for split-K plans the reduce), with the weight packed
-beforehand as a deployed layer would have it.  The default workload is the codec-decoder
-upsampler (1x512x2000 -> 1x256x16000, kernel 16, stride 8, padding 4, fp32 I/O).
+One step is one forward pass of a workload (input staging, the tensor-core GEMM with its
+fused output stage, and for split-K plans the reduce; every layer of a stack, chained), with
+the weight packed beforehand as a deployed layer would have it.
 
-Timing: W untimed warm-up steps and a ~1 s soak of the same step, then exactly K steps
-bracketed by a barrier and torch.cuda.synchronize() on both sides, each step between CUDA
-events on the launching stream.  The K timed steps are captured once into one CUDA graph of
-the library's own launches and replayed between two events (--no-graph times plain calls,
-an event pair per step); the "e2e" figure goes through the plain public call, with each
-step's host->device and device->host copies on their own streams overlapping the forward
-passes of neighbouring steps (a streaming caller).  The main kernels' own durations (for the
-roofline) come from a second run of the same K steps with an event pair around each of
-them, because an event between two kernels would serialise their programmatic launch.  Consecutive steps rotate over enough sets of input,
-packed weight, workspace and output buffers to exceed twice the L2 size, so no step reads
-data the previous one left in L2.  Under torchrun every rank runs the same workload on its
-own GPU (weak scaling, no collective on the data path); rank 0 prints one JSON line with
-the maximum time over ranks.
+With no --workload the headline is the iSTFT overlap-add as a ConvTranspose1d (4 x 4098 ->
+1 channel, 343 frames, kernel 4096, hop 1024, fp32 I/O), the largest of the five
+configurations, and the line carries a ``per_config`` block that measures every
+configuration the same way: the tiny 16 -> 8 layer, the codec upsampler, the iSTFT, the 2-D
+decoder layer and the bf16 vocoder stack (chained), plus the iSTFT by inverse FFTs and the
+depthwise layer.  --workload NAME measures one workload only.
+
+Timing: W untimed warm-up steps and a short soak, then exactly K steps bracketed by a
+barrier and torch.cuda.synchronize() on both sides, between CUDA events on the launching
+stream.  The K timed steps are captured once into one CUDA graph of the library's own
+launches and replayed between two events; ``us_per_call_plain`` times the same K steps as
+plain library calls (an event pair per step, the median reported), which is what a caller
+of ctr_forward sees.  The main kernels' own durations (for the roofline) come from a
+further replay of the same K steps with an event pair around each of them, because an event
+between two kernels would serialise their programmatic launch.  Consecutive steps rotate
+over enough sets of input, packed weight, workspace and output buffers to exceed twice the
+L2 size, so no step reads data the previous one left in L2.  The "e2e" figure goes through
+the plain public call, with each step's host->device and device->host copies on their own
+streams overlapping the forward passes of neighbouring steps.  Under torchrun every rank
+runs the same workloads on its own GPU (weak scaling, no collective on the data path); rank
+0 prints one JSON line with the maximum times over ranks.
 
 --impl reference times the CPU oracle (double precision, OpenMP on the host cores) on a
 bounded sample of the same workload: the reference arm of this benchmark.
@@ -46,9 +53,16 @@ import numpy as np  # noqa: E402
 
 import workloads  # noqa: E402
 
-DEFAULT_WORKLOAD = "codec_upsampler_f32"
+METRIC = "ConvTranspose GFLOP/s and % of roofline (tensor peak vs HBM) per call"
+HEADLINE = "istft_f32"
+# The five configurations (tiny layer, codec upsampler, iSTFT, 2-D decoder, vocoder stack),
+# then the two further workloads: the iSTFT by inverse FFTs and the depthwise layer.
+CONFIGS = ["tiny_1d_f32", "codec_upsampler_f32", "istft_f32", "decoder_2d_f32",
+           "vocoder_stack_bf16"]
+EXTRAS = ["istft_irfft_f32", "depthwise_2d_bf16"]
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# Nominal dense tensor throughput relative to bf16 (tf32 1.1 vs bf16 2.25 PFLOP/s).
+# Nominal dense tensor throughput relative to bf16 (tf32 1.1 vs bf16 2.25 PFLOP/s): the tf32
+# peak when it could not be measured in this run.
 TF32_OVER_BF16 = 1.1 / 2.25
 # The sources of each profiled kernel: a committed ncu summary holds their hash, and its
 # DRAM traffic is reported only while they are unchanged.
@@ -60,6 +74,7 @@ KERNEL_SOURCES = {
                 "transposed_convolution_gb300/csrc/gemm_tc_chain.cu"],
     "depthwise": ["transposed_convolution_gb300/csrc/depthwise.cu"],
     "istft": ["transposed_convolution_gb300/csrc/istft.cu"],
+    "gather": ["transposed_convolution_gb300/csrc/aux_kernels.cu"],
 }
 
 
@@ -87,8 +102,8 @@ def kernel_source_hash(kernel="gemm_tc"):
 
 
 def profiled_traffic(workload, layer=0, layers=1, kernel="gemm_tc"):
-    """DRAM bytes per launch of a layer's main kernel from the committed ncu summary, or None
-    when there is none or the kernel sources changed since it was taken."""
+    """DRAM bytes (read + written) per launch of a layer's main kernel from the committed ncu
+    summary, or None when there is none or the kernel sources changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "%s_%s.md" % (kernel, workload))
     if kernel not in KERNEL_SOURCES or not os.path.exists(path):
         return None
@@ -104,6 +119,24 @@ def profiled_traffic(workload, layer=0, layers=1, kernel="gemm_tc"):
         return int(float(vals[key]))
     except (KeyError, ValueError):
         return None
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the CPU-baseline record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=5).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
 
 
 # ------------------------------------------------------------------ clocks
@@ -170,13 +203,21 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ our arm
 
-def max_over_ranks(values, device):
+def max_over_ranks(values, device, world):
     """Element-wise maximum of a list of floats over all ranks of the default process group
     (the slowest rank sets the job's time)."""
+    if world <= 1:
+        return list(values)
     import torch
     t = torch.tensor(list(values), dtype=torch.float64, device=device)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return [float(v) for v in t]
+
+
+def barrier(world):
+    if world > 1:
+        import torch
+        torch.distributed.barrier()
 
 
 def aggregate_rate(world, units_per_rank, ms):
@@ -185,22 +226,66 @@ def aggregate_rate(world, units_per_rank, ms):
     return world * units_per_rank / (ms / 1e3) / 1e9
 
 
-def run_ours(args, rank, world, local_rank):
+def measure_tf32_peak(dev):
+    """Dense tf32 tensor throughput of this GPU in TFLOP/s, measured the way the bf16 peak
+    is: torch.matmul of two fp32 8192 x 8192 matrices with TF32 allowed, best of 10, CUDA
+    events.  None when the measurement fails."""
+    import torch
+    old = torch.backends.cuda.matmul.allow_tf32
+    try:
+        torch.backends.cuda.matmul.allow_tf32 = True
+        n = 8192
+        a = torch.randn(n, n, device=dev)
+        b = torch.randn(n, n, device=dev)
+        for _ in range(3):
+            torch.matmul(a, b)
+        torch.cuda.synchronize(dev)
+        best = float("inf")
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch.matmul(a, b)
+            e1.record()
+            torch.cuda.synchronize(dev)
+            best = min(best, e0.elapsed_time(e1))
+        del a, b
+        torch.cuda.empty_cache()
+        return 2.0 * n ** 3 / (best / 1e3) / 1e12
+    except Exception:
+        return None
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = old
+
+
+def layer_peak(L, peaks, peak_src, tf32_tflops):
+    """Tensor peak (TFLOP/s of useful MACs x 2) for a layer and where it comes from."""
+    if L.dtype == "bf16":
+        return peaks["bf16_tflops"], "bf16 dense, %s burst" % peak_src
+    if tf32_tflops:
+        return (tf32_tflops / 3.0,
+                "3xTF32: tf32 dense measured in this run (torch.matmul fp32 8192^3, TF32, best of "
+                "10) / 3 products per useful MAC")
+    return (peaks["bf16_tflops"] * TF32_OVER_BF16 / 3.0,
+            "3xTF32: %s bf16 burst x nominal tf32/bf16 (1.1/2.25) / 3 products per useful "
+            "MAC" % peak_src)
+
+
+def measure_workload(name, args, env, headline):
+    """Time one workload on this rank's GPU: graph-replayed steps, plain calls, main-kernel
+    durations, end to end through the public API, and parity against the oracle.  Returns
+    the raw figures (times already the maximum over ranks)."""
     import torch
     import transposed_convolution_gb300 as ctr
 
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    layers = workloads.make_workload(args.workload)
+    dev, world, rank = env["dev"], env["world"], env["rank"]
+    layers = workloads.make_workload(name)
     Ls = [li.layer for li in layers]
     tdts = [torch.bfloat16 if L.dtype == "bf16" else torch.float32 for L in Ls]
 
     def t(a, tdt):
         return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev).to(tdt)
 
-    # Buffer sets to rotate over: more than twice the L2 size in total.
-    props = torch.cuda.get_device_properties(dev)
-    l2 = getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20
+    l2 = env["l2"]
     w_dev = [t(li.w, tdt) for li, tdt in zip(layers, tdts)]
     b_dev = [t(li.bias, tdt) for li, tdt in zip(layers, tdts)]
     x_dev = t(layers[0].x, tdts[0])
@@ -272,14 +357,6 @@ def run_ours(args, rank, world, local_rank):
         for p in s["plans"]:
             p.check()
 
-    # Timed region: exactly K steps.  The K steps (rotating over the buffer sets) are captured
-    # once, untimed, into one CUDA graph of the library's launches and replayed between two
-    # events, so per-step launch overhead is paid once per K steps (--no-graph times plain
-    # calls, one event pair per step).  Kernels chain by programmatic dependent launch, and an
-    # event recorded between two kernels would serialise them, so the step time (value) comes
-    # from a run without per-kernel events, and the main kernels' own durations (roofline)
-    # from a second run of the same K steps whose captured steps record them (as external
-    # event nodes).
     K = args.steps
     nl = len(Ls)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -291,8 +368,13 @@ def run_ours(args, rank, world, local_rank):
             a.record()
             b.record()
     torch.cuda.synchronize()
+
+    # The K steps (rotating over the buffer sets) captured once, untimed, into one CUDA graph
+    # of the library's launches (and again with each main kernel between its own events,
+    # recorded as external event nodes).
     launches0 = ctr.ctr_launch_count()
     graph = graph_k = None
+    launches = 0
     if args.graph:
         cap = torch.cuda.Stream()
         graph = torch.cuda.CUDAGraph()
@@ -308,11 +390,7 @@ def run_ours(args, rank, world, local_rank):
         graph_k.replay()
         torch.cuda.synchronize()
 
-    def steps(kernel_events=False):
-        """All K steps (one graph replay, or K plain steps with an event pair each)."""
-        if graph is not None:
-            (graph_k if kernel_events else graph).replay()
-            return
+    def plain_steps(kernel_events=False):
         for k in range(K):
             if not kernel_events:
                 ev[k][0].record()
@@ -320,48 +398,54 @@ def run_ours(args, rank, world, local_rank):
             if not kernel_events:
                 ev[k][1].record()
 
-    sampler = ClockSampler(local_rank)
-    sampler.start()
-    time.sleep(0.3)
+    soak = args.soak if headline else min(args.soak, 0.3)
     soak_t0 = time.time()
-    while time.time() - soak_t0 < args.soak:
-        steps()
+    while time.time() - soak_t0 < soak:
+        if graph is not None:
+            graph.replay()
+        else:
+            plain_steps()
         torch.cuda.synchronize()
 
-    if world > 1:
-        torch.distributed.barrier()
+    # Timed region: exactly K steps.
+    barrier(world)
     torch.cuda.synchronize()
     launches0 = ctr.ctr_launch_count()
     t_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
     wall0 = time.time()
     t_ev[0].record()
-    steps()
+    if graph is not None:
+        graph.replay()
+    else:
+        plain_steps()
     t_ev[1].record()
     torch.cuda.synchronize()
     wall1 = time.time()
     if graph is None:
         launches = ctr.ctr_launch_count() - launches0
-    if world > 1:
-        torch.distributed.barrier()
+    barrier(world)
+    total_ms = t_ev[0].elapsed_time(t_ev[1])
+    # Plain calls: the same K steps without the graph, an event pair per step.
+    if graph is not None:
+        plain_steps()
+        torch.cuda.synchronize()
+    plain_ms = sorted(a.elapsed_time(b) for a, b in ev)
+    plain_median = plain_ms[len(plain_ms) // 2]
+    barrier(world)
     # Kernel durations: the same K steps again, each main kernel between its own events.
-    steps(kernel_events=True)
+    if graph_k is not None:
+        graph_k.replay()
+    else:
+        plain_steps(kernel_events=True)
     torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    time.sleep(0.25)
-    sampler.stop()
+    barrier(world)
     for s in sets:
         for p in s["plans"]:
             p.check()
-
-    total_window_ms = t_ev[0].elapsed_time(t_ev[1])
-    step_ms = ([total_window_ms / K] * K if graph is not None
-               else [a.elapsed_time(b) for a, b in ev])
     kern_ms = [sum(kev[k][j][0].elapsed_time(kev[k][j][1]) for k in range(K)) / K
                for j in range(nl)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        total_ms, *kern_ms = max_over_ranks([total_ms] + kern_ms, dev)
+    total_ms, plain_median, *kern_ms = max_over_ranks([total_ms, plain_median] + kern_ms,
+                                                       dev, world)
 
     # End to end through the public API, as a streaming caller runs it: every step copies
     # its x from pinned host memory, runs the forward passes (Plan.forward, no graph) and
@@ -369,11 +453,10 @@ def run_ours(args, rank, world, local_rank):
     # k's upload and step k-1's download overlap the forward passes; events order each
     # buffer's reuse (a set's x is overwritten only after its previous forward read it, its
     # y only after its previous download).  Time per step = whole run / steps.
-    n_e2e = max(3, min(K, 50))
+    n_e2e = max(3, min(K, 50 if headline else 20))
     x_hosts = [torch.from_numpy(np.ascontiguousarray(layers[0].x)).to(tdts[0]).pin_memory()
                for _ in range(2)]
     y_hosts = [torch.empty(sets[0]["y"][-1].shape, dtype=tdts[-1]).pin_memory() for _ in range(2)]
-    x_host, y_host = x_hosts[0], y_hosts[0]
     main_stream = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     ev_in = [torch.cuda.Event() for _ in range(n_e2e)]
@@ -402,10 +485,12 @@ def run_ours(args, rank, world, local_rank):
     main_stream.wait_event(ev_out[n_e2e - 1])
     e_end.record(main_stream)
     torch.cuda.synchronize()
-    e2e_ms = e_start.elapsed_time(e_end) / n_e2e
+    e2e_ms = max_over_ranks([e_start.elapsed_time(e_end) / n_e2e], dev, world)[0]
 
-    # Parity of this run's output against the oracle, layer by layer with the library's
-    # own previous output as input (computed after timing).
+    # Parity of this run's output against the oracle, layer by layer (computed after
+    # timing).  An unchained layer takes the library's own previous output as input; through
+    # a chain (no intermediate y) the oracle carries on from its own output rounded to the
+    # I/O type, and the chain's last layer is compared.
     parity = None
     if rank == 0 and args.parity:
         import oracle
@@ -418,8 +503,6 @@ def run_ours(args, rank, world, local_rank):
             if L.act_slope is not None:
                 ref = oracle.leaky_relu(ref, L.act_slope)
             if s["plans"][j].next_plan is not None:
-                # Chained: no y of this layer; the oracle carries on from its own output
-                # rounded to the I/O type, and the last layer is compared.
                 xin = oracle.round_bf16(ref) if L.dtype == "bf16" else oracle.round_f32(ref)
                 continue
             got = s["y"][j].float().cpu().numpy()
@@ -427,94 +510,96 @@ def run_ours(args, rank, world, local_rank):
             xin = got
         parity = max(errs)
 
+    paths = [p.path for p in sets[0]["plans"]]
+    describe = [p.describe() for p in sets[0]["plans"]]
+    chained = sum(p.next_plan is not None for p in sets[0]["plans"])
+    h2d = int(x_hosts[0].numel() * x_hosts[0].element_size())
+    d2h = int(y_hosts[0].numel() * y_hosts[0].element_size())
+    for s in sets:
+        for p in s["plans"]:
+            p.close()
+    del sets, w_dev, b_dev, x_dev, x_hosts, y_hosts
+    graph = graph_k = None
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return {
+        "name": name, "Ls": Ls, "K": K, "ms_per_step": total_ms / K,
+        "plain_ms": plain_median, "kern_ms": kern_ms, "e2e_ms": e2e_ms, "n_e2e": n_e2e,
+        "h2d": h2d, "d2h": d2h, "parity": parity, "paths": paths, "describe": describe,
+        "chained": chained, "nsets": nsets, "set_bytes": set_bytes, "prepack_ms": prepack_ms,
+        "launches": int(launches), "window": (soak_t0, wall1), "wall_timed": wall1 - wall0,
+    }
+
+
+def summarize(m, env):
+    """Roofline, GFLOP/s and kernel figures of one measured workload."""
+    import transposed_convolution_gb300 as ctr
+    peaks, peak_src, tf32 = env["peaks"], env["peak_src"], env["tf32_tflops"]
+    Ls = m["Ls"]
+    is_fft = any(L.kind == "istft" for L in Ls)
     flops = sum(2.0 * L.useful_macs for L in Ls)
     bytes_c = sum(L.compulsory_bytes for L in Ls)
-    ms_per_step = total_ms / K
-    peaks, peak_src = load_peaks()
+    step_s = m["ms_per_step"] / 1e3
 
-    def layer_peak(L):
-        if L.dtype == "bf16":
-            return peaks["bf16_tflops"], "bf16 dense, %s burst" % peak_src
-        return (peaks["bf16_tflops"] * TF32_OVER_BF16 / 3.0,
-                "3xTF32: %s bf16 burst x nominal tf32/bf16 (1.1/2.25) / 3 products per useful "
-                "MAC" % peak_src)
-
-    def layer_t_tensor(L, pk):
+    def t_tensor(L, pk):
         # The FFT path's arithmetic is far below the dense contraction it replaces: bytes only.
         return 0.0 if L.kind == "istft" else 2.0 * L.useful_macs / (pk * 1e12)
 
     t_roof = 0.0
     for L in Ls:
-        pk, _ = layer_peak(L)
-        t_roof += max(layer_t_tensor(L, pk), L.compulsory_bytes / (peaks["hbm_gbs"] * 1e9))
-    # Dominant kernel: the layer whose main kernel takes longest.
-    j = max(range(nl), key=lambda q: kern_ms[q])
+        pk, _ = layer_peak(L, peaks, peak_src, tf32)
+        t_roof += max(t_tensor(L, pk), L.compulsory_bytes / (peaks["hbm_gbs"] * 1e9))
+    j = max(range(len(Ls)), key=lambda q: m["kern_ms"][q])
     L = Ls[j]
-    pk, peak_note = layer_peak(L)
-    t_tensor = layer_t_tensor(L, pk)
-    t_hbm = L.compulsory_bytes / (peaks["hbm_gbs"] * 1e9)
-    bound = "tensor" if t_tensor >= t_hbm else "hbm"
-    kern_s = kern_ms[j] / 1e3
+    pk, peak_note = layer_peak(L, peaks, peak_src, tf32)
+    tt = t_tensor(L, pk)
+    th = L.compulsory_bytes / (peaks["hbm_gbs"] * 1e9)
+    bound = "tensor" if tt >= th else "hbm"
+    kern_s = m["kern_ms"][j] / 1e3
     if bound == "tensor":
         achieved, peak, unit = 2.0 * L.useful_macs / kern_s / 1e12, pk, "TFLOP/s"
+        nominal = peaks["bf16_tflops"] * TF32_OVER_BF16 / 3.0 if L.dtype == "f32" else pk
     else:
         achieved, peak, unit = L.compulsory_bytes / kern_s / 1e9, peaks["hbm_gbs"], "GB/s"
         peak_note = "HBM copy bandwidth, %s" % peak_src
-    clocks = sampler.summary(soak_t0, wall1 + 0.25)
+        nominal = peak
+    path = m["paths"][j]
     kname = {ctr.CTR_PATH_GATHER: "gather_kernel", ctr.CTR_PATH_DEPTHWISE: "depthwise_kernel",
              -1: "spectrum_rows_kernel+irfft_frames_kernel+istft_ola_kernel"}.get(
-                 sets[0]["plans"][j].path, "gemm_tc_kernel")
-    traffic = profiled_traffic(args.workload, j, nl,
-                               "istft" if kname.startswith("spectrum_rows") else kname[:-len("_kernel")])
-
-    result = {
-        "metric": "ConvTranspose GFLOP/s and % of roofline (tensor peak vs HBM) per call",
-        "value": round(aggregate_rate(world, flops, ms_per_step), 1),
-        "unit": "GFLOP/s",
-        "n_gpus": world,
-        "steps": K,
-        "warmup": args.warmup,
-        "ms_per_step": round(ms_per_step, 5),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "3xtf32-fp32acc" if Ls[0].dtype == "f32" else "bf16-fp32acc",
-        "data": "synthetic (seeded; workloads.py)",
-        "config": {"workload": args.workload, "shape": "; ".join(L.describe() for L in Ls),
-                   "l2": "rotating %d buffer sets, %.0f MB > 2x L2 (%.0f MB)"
-                         % (nsets, nsets * set_bytes / 1e6, l2 / 1e6),
-                   "parallelism": "replica per GPU" if world > 1 else "single GPU",
-                   "chained_layers": sum(p.next_plan is not None for p in sets[0]["plans"]),
-                   "launch": ("one CUDA graph of the K steps" if graph is not None
-                              else "plain calls") + "; kernel times from a second K-step run",
-                   "plan": " | ".join(p.describe() for p in sets[0]["plans"]),
-                   **({"flop_count": "the dense ConvTranspose (DFT-basis contraction) that the "
-                                     "inverse FFTs compute"}
-                      if any(L.kind == "istft" for L in Ls) else {})},
-        "pct_of_roofline": round(100.0 * t_roof / (ms_per_step / 1e3), 2),
+                 path, "gemm_tc_kernel")
+    kfile = {ctr.CTR_PATH_GATHER: "gather", ctr.CTR_PATH_DEPTHWISE: "depthwise",
+             -1: "istft"}.get(path, "gemm_tc")
+    traffic = profiled_traffic(m["name"], j, len(Ls), kfile)
+    roof = {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 2),
+            "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic,
+            "kernel": kname, "layer": j, "kernel_us": round(m["kern_ms"][j] * 1e3, 3),
+            "peak_source": peak_note + (", of measured" if peak_src == "measured" else
+                                        ", of fallback")}
+    if bound == "tensor" and L.dtype == "f32":
+        roof["frac_vs_nominal_tf32_ratio"] = round(achieved / nominal, 4)
+    out = {
+        "us_per_call": round(m["ms_per_step"] * 1e3, 3),
+        "us_per_call_plain": round(m["plain_ms"] * 1e3, 3),
+        "gflops": None if is_fft else round(flops / step_s / 1e9, 1),
+        "pct_of_roofline": round(100.0 * t_roof / step_s, 2),
         "roofline_us": round(t_roof * 1e6, 3),
-        "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 2),
-                     "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": kname, "layer": j, "kernel_us": round(kern_ms[j] * 1e3, 3),
-                     "peak_source": peak_note},
-        "layer_kernel_us": [round(v * 1e3, 3) for v in kern_ms],
-        "e2e": {"value": round(aggregate_rate(world, flops, e2e_ms), 1), "unit": "GFLOP/s",
-                "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
-                "d2h_bytes_per_step": int(y_host.numel() * y_host.element_size()),
-                "ms_per_step": round(e2e_ms, 5), "steps": n_e2e,
-                "copies": "own streams, overlapping the forward passes"},
-        "gpu_launches": int(launches),
-        "launches_per_step": launches / K,
-        "clocks": clocks,
-        "prepack_ms": round(prepack_ms, 4),
-        "parity_rel_l2": parity,
-        "compulsory_bytes": bytes_c,
-        "wall_s_timed": round(wall1 - wall0, 4),
+        "roofline": roof,
+        "layer_kernel_us": [round(v * 1e3, 3) for v in m["kern_ms"]],
+        "parity_rel_l2": m["parity"],
+        "parity_tolerance": 1e-2 if Ls[-1].dtype == "bf16" else 1e-5,
+        "e2e_us_per_call": round(m["e2e_ms"] * 1e3, 3),
+        "prepack_us": round(m["prepack_ms"] * 1e3, 2),
+        "launches_per_step": m["launches"] / m["K"],
+        "shape": "; ".join(x.describe() for x in Ls),
+        "plan": " | ".join(m["describe"]),
     }
-    for s in sets:
-        for p in s["plans"]:
-            p.close()
-    return result
+    if is_fft:
+        out["hbm_frac_step"] = round(bytes_c / step_s / 1e9 / peaks["hbm_gbs"], 4)
+        out["note"] = ("inverse real FFTs: the dense contraction's flops are not performed, so "
+                       "no GFLOP/s; the roofline is the compulsory bytes at the HBM bandwidth")
+    if m["chained"]:
+        out["chained_layers"] = m["chained"]
+    return out, flops, bytes_c
 
 
 # ------------------------------------------------------------------ oracle (CPU) arm
@@ -526,79 +611,184 @@ def oracle_weight(li):
     return workloads.istft_basis(L.kernel[0], li.w) if L.kind == "istft" else li.w
 
 
-def oracle_sample(name, budget_s):
-    """Time the oracle on a bounded sample of the workload: the first layer on a prefix of
-    the input positions (all of them when that fits the budget).  Returns (seconds per
-    call, useful flops per call, sample description)."""
+def _oracle_call(x, li, w):
     import oracle
+    L = li.layer
+    oracle.conv_transpose(x, w, li.bias, L.stride, L.padding, L.output_padding, groups=L.groups)
+
+
+def oracle_sample(name, budget_s, start_len=None):
+    """A bounded sample of the workload for the oracle: its first layer on a prefix of the
+    input positions (all of them when one call fits budget_s / 3 seconds).  Returns (seconds
+    per call, useful flops per call, sample description, (x, layer inputs, weight))."""
     li = workloads.make_workload(name)[0]
     L = li.layer
-    x = li.x
     w = oracle_weight(li)
-    desc = "full layer"
-    # Shrink the last input dimension until one call is at most budget/3 seconds.
-    for _ in range(12):
+    x = li.x
+    if start_len is not None and start_len < x.shape[-1]:
+        x = x[..., : max(8, int(start_len))]
+    for _ in range(16):
         t0 = time.time()
-        oracle.conv_transpose(x, w, li.bias, L.stride, L.padding, L.output_padding,
-                              groups=L.groups)
+        _oracle_call(x, li, w)
         dt = time.time() - t0
         if dt <= budget_s / 3 or x.shape[-1] <= 8:
             break
         x = x[..., : max(8, x.shape[-1] // 2)]
-        desc = "input prefix %s of %s" % (x.shape[-1], L.in_sp[-1])
+    desc = ("first layer, " if len(workloads.WORKLOADS[name]) > 1 else "") + (
+        "full layer" if x.shape[-1] == L.in_sp[-1]
+        else "input prefix %d of %d positions" % (x.shape[-1], L.in_sp[-1]))
     macs = L.B * L.C_in * (L.C_out // L.groups) * int(np.prod(L.kernel))
     macs *= int(np.prod(x.shape[2:]))
     return dt, 2.0 * macs, desc, (x, li, w)
 
 
-def time_oracle(name, budget_s=12.0):
+def time_oracle(name, budget_s, threads=0, start_len=None):
+    """Oracle GFLOP/s on a bounded sample of the workload (threads <= 0: all host cores)."""
     import oracle
-    dt, flops, desc, (x, li, w) = oracle_sample(name, budget_s)
-    L = li.layer
-    reps, total = 0, 0.0
-    while total < budget_s and reps < 50:
-        t0 = time.time()
-        oracle.conv_transpose(x, w, li.bias, L.stride, L.padding, L.output_padding,
-                              groups=L.groups)
-        total += time.time() - t0
-        reps += 1
-    sec = total / reps
-    return {"value": round(flops / sec / 1e9, 3), "unit": "GFLOP/s", "cores": oracle.threads(),
-            "kind": "oracle", "sample": "%s of %s, %d calls, %.2f s each" % (desc, name, reps, sec),
-            "sec_per_call": sec}
+    oracle.set_threads(threads)
+    try:
+        dt, flops, desc, (x, li, w) = oracle_sample(name, budget_s, start_len)
+        reps, total = 0, 0.0
+        while total < budget_s and reps < 50:
+            t0 = time.time()
+            _oracle_call(x, li, w)
+            total += time.time() - t0
+            reps += 1
+        sec = total / reps
+        return {"value": round(flops / sec / 1e9, 3), "unit": "GFLOP/s",
+                "cores": oracle.threads(), "kind": "oracle",
+                "sample": "%s of %s, %d calls, %.3f s each" % (desc, name, reps, sec),
+                "sample_len": int(x.shape[-1]), "sec_per_call": sec}
+    finally:
+        oracle.set_threads(0)
+
+
+def cpu_baseline(name, budget_s):
+    """The oracle on all host cores and on one core, with the host's core count and CPU."""
+    allc = time_oracle(name, budget_s)
+    # One core takes about `cores` times longer: start from a prefix that keeps a call
+    # within a third of the budget.
+    shrink = allc["sec_per_call"] * allc["cores"] / (budget_s / 3)
+    start = allc["sample_len"] if shrink <= 1 else max(8, int(allc["sample_len"] / shrink))
+    one = time_oracle(name, budget_s, threads=1, start_len=start)
+    out = {k: allc[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    out["one_core"] = {k: one[k] for k in ("value", "unit", "cores", "sample")}
+    out["nproc"] = os.cpu_count()
+    out["cpu_model"] = cpu_model()
+    return out
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return None
     K, W = args.steps, args.warmup
-    import oracle
-    _, flops, desc, (x, li, w) = oracle_sample(args.workload, 8.0)
+    name = args.workload or HEADLINE
+    _, flops, desc, (x, li, w) = oracle_sample(name, 8.0)
     L = li.layer
     for _ in range(min(W, 1)):
-        oracle.conv_transpose(x, w, li.bias, L.stride, L.padding, L.output_padding,
-                              groups=L.groups)
+        _oracle_call(x, li, w)
     times = []
     for _ in range(K):
         t0 = time.time()
-        oracle.conv_transpose(x, w, li.bias, L.stride, L.padding, L.output_padding,
-                              groups=L.groups)
+        _oracle_call(x, li, w)
         times.append(time.time() - t0)
         if sum(times) > 120:
             break
     sec = sum(times) / len(times)
     v = round(flops / sec / 1e9, 3)
+    import oracle
     return {
-        "impl": "reference",
-        "metric": "ConvTranspose GFLOP/s and % of roofline (tensor peak vs HBM) per call",
+        "impl": "reference", "metric": METRIC,
         "value": v, "unit": "GFLOP/s", "n_gpus": world, "steps": len(times), "warmup": W,
         "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; workloads.py)",
-        "config": {"workload": args.workload, "shape": L.describe(), "sample": desc},
+        "config": {"workload": name, "shape": L.describe(), "sample": desc},
         "cpu_baseline": {"value": v, "unit": "GFLOP/s", "cores": oracle.threads(),
-                         "kind": "oracle", "sample": desc},
+                         "kind": "oracle", "sample": desc, "nproc": os.cpu_count(),
+                         "cpu_model": cpu_model()},
         "e2e": {"value": v, "unit": "GFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+
+
+# ------------------------------------------------------------------ main
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    props = torch.cuda.get_device_properties(dev)
+    peaks, peak_src = load_peaks()
+    env = {"dev": dev, "world": world, "rank": rank,
+           "l2": getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20,
+           "peaks": peaks, "peak_src": peak_src}
+    names = [args.workload] if args.workload else CONFIGS + EXTRAS
+    head = args.workload or HEADLINE
+    env["tf32_tflops"] = (measure_tf32_peak(dev)
+                          if any(L.dtype == "f32" for n in names
+                                 for L in workloads.WORKLOADS[n]) else None)
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    measured = {}
+    # The headline first (with the full soak), then every other workload.
+    for name in [head] + [n for n in names if n != head]:
+        measured[name] = measure_workload(name, args, env, headline=(name == head))
+    time.sleep(0.25)
+    sampler.stop()
+
+    m = measured[head]
+    summ, flops, bytes_c = summarize(m, env)
+    Ls = m["Ls"]
+    clocks = sampler.summary(*m["window"])
+    result = {
+        "metric": METRIC,
+        "value": round(aggregate_rate(world, flops, m["ms_per_step"]), 1),
+        "unit": "GFLOP/s",
+        "n_gpus": world,
+        "steps": m["K"],
+        "warmup": args.warmup,
+        "ms_per_step": round(m["ms_per_step"], 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32 I/O, 3xTF32 products, fp32 accumulate" if Ls[0].dtype == "f32"
+                 else "bf16 I/O, bf16 products, fp32 accumulate",
+        "data": "synthetic (seeded; workloads.py)",
+        "config": {"workload": head, "shape": summ["shape"],
+                   "l2": "rotating %d buffer sets, %.0f MB > 2x L2 (%.0f MB)"
+                         % (m["nsets"], m["nsets"] * m["set_bytes"] / 1e6, env["l2"] / 1e6),
+                   "parallelism": "replica per GPU" if world > 1 else "single GPU",
+                   "chained_layers": m["chained"],
+                   "launch": ("one CUDA graph of the K steps" if args.graph else "plain calls")
+                             + "; kernel times from a further K-step run",
+                   "plan": summ["plan"]},
+        "us_per_call": summ["us_per_call"],
+        "us_per_call_plain": summ["us_per_call_plain"],
+        "pct_of_roofline": summ["pct_of_roofline"],
+        "roofline_us": summ["roofline_us"],
+        "roofline": summ["roofline"],
+        "layer_kernel_us": summ["layer_kernel_us"],
+        "e2e": {"value": round(aggregate_rate(world, flops, m["e2e_ms"]), 1), "unit": "GFLOP/s",
+                "h2d_bytes_per_step": m["h2d"], "d2h_bytes_per_step": m["d2h"],
+                "ms_per_step": round(m["e2e_ms"], 5), "steps": m["n_e2e"],
+                "copies": "own streams, overlapping the forward passes"},
+        "gpu_launches": m["launches"],
+        "launches_per_step": m["launches"] / m["K"],
+        "clocks": clocks,
+        "prepack_ms": round(m["prepack_ms"], 4),
+        "parity_rel_l2": m["parity"],
+        "compulsory_bytes": bytes_c,
+        "wall_s_timed": round(m["wall_timed"], 4),
+        "tf32_tflops_measured": (round(env["tf32_tflops"], 1) if env["tf32_tflops"] else None),
+    }
+    if len(measured) > 1:
+        per = {}
+        for name in names:
+            s, _, _ = summarize(measured[name], env)
+            s["clocks"] = sampler.summary(*measured[name]["window"])
+            per[name] = s
+        result["per_config"] = per
+    return result
 
 
 def main():
@@ -607,7 +797,9 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=workloads.WORKLOAD_ORDER)
+    ap.add_argument("--workload", default=None, choices=workloads.WORKLOAD_ORDER,
+                    help="measure one workload only (default: the iSTFT headline plus every "
+                         "configuration in per_config)")
     ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed load before timing")
     ap.add_argument("--no-parity", dest="parity", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
@@ -632,8 +824,11 @@ def main():
     res = run_ours(args, rank, world, local_rank)
     if rank == 0:
         if args.cpu_baseline and world == 1:
-            cb = time_oracle(args.workload)
-            res["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+            head = args.workload or HEADLINE
+            res["cpu_baseline"] = cpu_baseline(head, 6.0)
+            for name, entry in res.get("per_config", {}).items():
+                entry["cpu_baseline"] = (res["cpu_baseline"] if name == head
+                                         else cpu_baseline(name, 2.0))
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch

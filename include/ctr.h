@@ -184,7 +184,8 @@ ctr_status ctr_plan_set_pads(ctr_plan_t plan, const int64_t *pads_begin, const i
  * enable not 0 or 1, after ctr_prepack_weight, or on a chained plan.  Once streaming, a
  * plan refuses ctr_plan_set_groups, _set_dilation, _set_pads and ctr_plan_chain
  * (CTR_ERR_INVALID_ARG), and ctr_plan_set_path with any path but the polyphase one
- * (CTR_ERR_UNSUPPORTED).  enable = 0 restores the plain plan, with the automatic path.
+ * (CTR_ERR_UNSUPPORTED).  enable = 0 restores the plain plan, with the path it had before
+ * streaming was turned on (the automatic path, or the one ctr_plan_set_path forced).
  */
 ctr_status ctr_plan_set_streaming(ctr_plan_t plan, int enable);
 
@@ -307,16 +308,18 @@ ctr_status ctr_forward(ctr_plan_t plan, const void *x, const void *w_packed, con
  * current; make that first call before any stream capture.  Every call shares the one
  * array: calls whose GPU work overlaps (different streams, or several host threads) race on
  * it and must be serialised by the caller.  Bounded-wait timeouts are recorded in the
- * array's status word, which this call clears and never reads back (it does not
- * synchronise).  Returns as ctr_forward otherwise.
+ * array's status word, which every call clears at its start (this call does not
+ * synchronise); ctr_plan_check of any plan, on the same device, reads and clears it, so a
+ * check right after a call reports that call's timeout.  Returns as ctr_forward otherwise.
  */
 ctr_status ctr_forward_noalloc(ctr_plan_t plan, const void *x, const void *w, const void *bias,
                                void *y, void *stream);
 
 /*
- * Synchronise stream, then read and clear the plan's device status word.  Returns CTR_OK,
- * CTR_ERR_DEVICE_TIMEOUT when a kernel's bounded wait gave up since the last check (its
- * output is then incomplete), or CTR_ERR_CUDA.
+ * Synchronise stream, then read and clear the plan's device status word, and the status word
+ * of ctr_forward_noalloc's scratch on the current device once an allocation-free call has
+ * run there.  Returns CTR_OK, CTR_ERR_DEVICE_TIMEOUT when a kernel's bounded wait gave up
+ * since the last check (its output is then incomplete), or CTR_ERR_CUDA.
  */
 ctr_status ctr_plan_check(ctr_plan_t plan, void *stream);
 

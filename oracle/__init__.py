@@ -62,6 +62,8 @@ def _load():
             lib.ctr_oracle_output_size_ex.restype = ctypes.c_int64
             lib.ctr_oracle_output_size_ex.argtypes = [ctypes.c_int64] * 7
             lib.ctr_oracle_max_threads.restype = ctypes.c_int
+            lib.ctr_oracle_set_threads.restype = None
+            lib.ctr_oracle_set_threads.argtypes = [ctypes.c_int]
             lib.ctr_oracle_landed_pairs.restype = ctypes.c_int64
             lib.ctr_oracle_landed_pairs.argtypes = [ctypes.c_int] + [_I64P] * 5
             lib.ctr_oracle_conv_transpose.restype = ctypes.c_int
@@ -96,6 +98,12 @@ def _tuple(v, ndim):
 def threads() -> int:
     """OpenMP threads the oracle uses."""
     return int(_load().ctr_oracle_max_threads())
+
+
+def set_threads(n: int) -> None:
+    """Run the oracle on n threads (n <= 0: the OpenMP default).  The result does not depend
+    on the thread count; only the CPU-baseline timing uses this."""
+    _load().ctr_oracle_set_threads(int(n))
 
 
 def output_size(L_in: int, k: int, s: int, p: int, op: int = 0, d: int = 1,

@@ -74,6 +74,20 @@ int ctr_oracle_max_threads(void)
 #endif
 }
 
+/* Run the parallel loops on n threads (n >= 1), or on the OpenMP default when n <= 0.
+ * Only the speed changes: every item sums into its own accumulator and the items are
+ * combined in a fixed order, so the result is the same on any number of threads. */
+void ctr_oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    static int default_threads = 0;
+    if (default_threads == 0) default_threads = omp_get_max_threads();
+    omp_set_num_threads(n >= 1 ? n : default_threads);
+#else
+    (void)n;
+#endif
+}
+
 /* Number of (input position, tap) pairs, over all spatial dimensions, that land inside
  * the output: the count of scalar contributions per (input channel, output channel)
  * pair.  Returns -1 on invalid geometry. */

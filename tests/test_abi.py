@@ -362,6 +362,21 @@ def test_streaming_plan_without_gpu(ctr):
             assert ctr.ctr_plan_output_shape(h, args[0]) == out
         finally:
             ctr.ctr_plan_destroy(h)
+    # A path forced before streaming comes back when streaming is turned off.
+    h = _plan(ctr, 1, 1, 64, 32, [50], [4], [2], [0], [0], f32)
+    try:
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_POLYPHASE
+        ctr.ctr_plan_set_path(h, ctr.CTR_PATH_GATHER, 0)
+        ctr.ctr_plan_set_streaming(h, 1)
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_POLYPHASE
+        ctr.ctr_plan_set_streaming(h, 0)
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_GATHER
+        ctr.ctr_plan_set_path(h, ctr.CTR_PATH_AUTO, 0)
+        ctr.ctr_plan_set_streaming(h, 1)
+        ctr.ctr_plan_set_streaming(h, 0)
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_POLYPHASE
+    finally:
+        ctr.ctr_plan_destroy(h)
     a = _plan(ctr, 1, 1, 64, 32, [100], [4], [2], [0], [0], bf)
     b = _plan(ctr, 1, 1, 32, 64, [202], [4], [2], [0], [0], bf)
     try:

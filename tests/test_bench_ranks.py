@@ -34,7 +34,7 @@ def _worker(rank, world, port, out):
         assert bench.dist_env() == (rank, world, rank)
         # Rank r reports step time 10 + r and layer times that peak on different ranks.
         mine = [10.0 + rank, 3.0 - rank, 1.0 + 2.0 * rank]
-        out[rank] = bench.max_over_ranks(mine, "cpu")
+        out[rank] = bench.max_over_ranks(mine, "cpu", world)
 
         class A:
             steps, warmup, workload = 1, 3, "tiny_1d_f32"

@@ -80,3 +80,67 @@ def test_noalloc_matches_forward_twice(case):
             np.testing.assert_array_equal(got, ref)
     finally:
         plan.close()
+
+
+def _polyphase_case(rng):
+    """A small fp32 polyphase plan with its device inputs (split-K 1, so the GEMM's fused
+    output stage writes y)."""
+    import torch
+    import workloads
+    x = torch.from_numpy(workloads._cast(rng.standard_normal((1, 64, 300)), "f32")).cuda()
+    w = torch.from_numpy(workloads._cast(rng.uniform(-0.1, 0.1, (64, 32, 16)), "f32")).cuda()
+    b = torch.from_numpy(workloads._cast(rng.normal(0.0, 0.1, 32), "f32")).cuda()
+    plan = ctr.Plan(1, 64, 32, (300,), (16,), 8, 4, 0, path=ctr.CTR_PATH_POLYPHASE, split_k=1)
+    return plan, x, w, b
+
+
+@pytest.mark.gpu
+def test_noalloc_leaves_free_device_memory_unchanged():
+    """After a first call (which looks up the scratch array's address), further calls change
+    the device's free memory by nothing: they allocate no device memory."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    _ensure_lib()
+    plan, x, w, b = _polyphase_case(np.random.default_rng(7))
+    try:
+        y = torch.empty(plan.out_shape, dtype=torch.float32, device="cuda")
+        stream = ctr._stream_ptr(None)
+        args = (plan.handle, ctr._ptr(x), ctr._ptr(w), ctr._ptr(b), ctr._ptr(y), stream)
+        ctr.ctr_forward_noalloc(*args)
+        torch.cuda.synchronize()
+        free0, _ = torch.cuda.mem_get_info()
+        for _ in range(5):
+            ctr.ctr_forward_noalloc(*args)
+        torch.cuda.synchronize()
+        free1, _ = torch.cuda.mem_get_info()
+        assert free1 == free0
+    finally:
+        plan.close()
+
+
+@pytest.mark.gpu
+def test_noalloc_timeout_is_reported_by_plan_check():
+    """A 0 ns wait limit makes the GEMM's bounded waits give up on a healthy run: the
+    allocation-free call records the timeout in its scratch status word and ctr_plan_check
+    reports it; with the normal limit the next call is correct and the check is clean."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import oracle
+    _ensure_lib()
+    plan, x, w, b = _polyphase_case(np.random.default_rng(8))
+    try:
+        y = torch.empty(plan.out_shape, dtype=torch.float32, device="cuda")
+        stream = ctr._stream_ptr(None)
+        args = (plan.handle, ctr._ptr(x), ctr._ptr(w), ctr._ptr(b), ctr._ptr(y), stream)
+        plan.set_wait_limit_ns(0)
+        ctr.ctr_forward_noalloc(*args)
+        assert ctr.lib.ctr_plan_check(plan.handle, stream) == ctr.CTR_ERR_DEVICE_TIMEOUT
+        plan.set_wait_limit_ns(4_000_000_000)
+        ctr.ctr_forward_noalloc(*args)
+        assert ctr.lib.ctr_plan_check(plan.handle, stream) == ctr.CTR_OK
+        ref = oracle.conv_transpose(x.cpu().numpy(), w.cpu().numpy(), b.cpu().numpy(), 8, 4, 0)
+        assert oracle.rel_l2(y.cpu().numpy(), ref) <= 1e-5
+    finally:
+        plan.close()

@@ -520,6 +520,7 @@ ctr_status ctr_plan_create(ctr_plan_t *out, int ndim, int64_t N, int64_t C_in, i
     pl->act = CTR_ACT_NONE;
     pl->slope = 0.0f;
     pl->forced_path = CTR_PATH_AUTO;
+    pl->stream_saved_path = CTR_PATH_AUTO;
     pl->forced_split = 0;
     pl->forced_bn = 0;
     pl->groups = 1;
@@ -699,10 +700,11 @@ ctr_status ctr_plan_set_streaming(ctr_plan_t pl, int enable) {
     if (pl->prepared || pl->chain_next || pl->chain_prev) return CTR_ERR_INVALID_ARG;
     if (enable == pl->streaming) return CTR_OK;
     if (!enable) {
+        // Back to the plain plan, with the path the caller forced before streaming (if any).
         pl->streaming = 0;
         pl->stream_ready = 0;
         set_output_lengths(pl);
-        return reroute(pl, CTR_PATH_AUTO, pl->forced_split, pl->groups);
+        return reroute(pl, pl->stream_saved_path, pl->forced_split, pl->groups);
     }
     // 1-D, no padding or output_padding, k >= s, one group, undilated, and a carry of at
     // most kMaxStreamCarry frames on the polyphase path.
@@ -726,6 +728,7 @@ ctr_status ctr_plan_set_streaming(ctr_plan_t pl, int enable) {
         reroute(pl, old_path, pl->forced_split, pl->groups);
         return st;
     }
+    pl->stream_saved_path = old_path;
     pl->stream_ready = 0;
     return CTR_OK;
 }
@@ -911,19 +914,32 @@ ctr_status ctr_plan_chain(ctr_plan_t pl, ctr_plan_t nx) {
     return CTR_OK;
 }
 
+// Reads a device status word and clears it when set; true when it was set.
+static ctr_status read_and_clear(uint32_t *word, bool *was_set) {
+    uint32_t v = 0;
+    if (cudaMemcpy(&v, word, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return CTR_ERR_CUDA;
+    *was_set = v != 0;
+    if (v != 0 && cudaMemset(word, 0, sizeof(uint32_t)) != cudaSuccess) return CTR_ERR_CUDA;
+    return CTR_OK;
+}
+
 ctr_status ctr_plan_check(ctr_plan_t pl, void *stream) {
     if (!pl) return CTR_ERR_INVALID_ARG;
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return CTR_ERR_CUDA;
-    if (!pl->d_status) return CTR_OK;
-    uint32_t v = 0;
-    if (cudaMemcpy(&v, pl->d_status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
-        return CTR_ERR_CUDA;
-    if (v != 0) {
-        if (cudaMemset(pl->d_status, 0, sizeof(uint32_t)) != cudaSuccess) return CTR_ERR_CUDA;
-        return CTR_ERR_DEVICE_TIMEOUT;
+    bool timeout = false, set = false;
+    ctr_status st;
+    if (pl->d_status) {
+        if ((st = read_and_clear(pl->d_status, &set)) != CTR_OK) return st;
+        timeout = timeout || set;
     }
-    return CTR_OK;
+    // The allocation-free entry point reports into its scratch array's status word.
+    if (uint32_t *w = ctr::noalloc_status_word()) {
+        if ((st = read_and_clear(w, &set)) != CTR_OK) return st;
+        timeout = timeout || set;
+    }
+    return timeout ? CTR_ERR_DEVICE_TIMEOUT : CTR_OK;
 }
 
 void ctr_plan_destroy(ctr_plan_t pl) {

@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/ctr.h"
+#include "per_device.h"
 
 namespace ctr {
 
@@ -94,6 +95,7 @@ struct ctr_plan_s {
     int64_t dil[2];     // dilation (ctr_plan_set_dilation; 1 = none)
     int64_t pe[2];      // back pad (ctr_plan_set_pads; p is the front pad; default pe = p)
     int streaming;      // ctr_plan_set_streaming: carries the last m - 1 input frames
+    int stream_saved_path;  // the forced path before streaming was turned on (restored after)
     int stream_ready;   // the carried frames were zeroed (ctr_plan_stream_reset)
     int dtype;
     int act;
@@ -166,16 +168,26 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
 }
 
-// Prefer the largest shared-memory carveout for a kernel (once per kernel), so that
-// consecutive kernels of a forward pass do not reconfigure the SMs between them.
+// The current device's ordinal, or -1 when it cannot be read (set-up then runs every time).
+inline int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    return dev;
+}
+
+// Prefer the largest shared-memory carveout for a kernel (once per kernel and device: the
+// attribute belongs to the current device's context), so that consecutive kernels of a
+// forward pass do not reconfigure the SMs between them.
 template <auto Kernel>
 cudaError_t prefer_max_smem() {
-    static bool done = false;
-    if (done) return cudaSuccess;
-    const cudaError_t e = cudaFuncSetAttribute(
-        Kernel, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
-    done = e == cudaSuccess;
-    return e;
+    static PerDeviceOnce once;
+    return once.run(current_device(), cudaSuccess, [] {
+        return cudaFuncSetAttribute(Kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                    (int)cudaSharedmemCarveoutMaxShared);
+    });
 }
 
 // Launch wrappers (each returns the cudaGetLastError() of its launches).
@@ -224,6 +236,9 @@ cudaError_t run_tc_path(const ctr_plan_s *pl, const void *x, const void *w_packe
 
 // Counter of launched kernels (monotonic, process-wide).
 void count_launches(uint64_t n);
+// Device address of ctr_forward_noalloc's status word on the current device, or nullptr when
+// no allocation-free call has looked up its scratch on this device yet (noalloc.cu).
+uint32_t *noalloc_status_word();
 // Records a caller's timing event (an external event node under stream capture).
 cudaError_t record_timing(cudaEvent_t ev, cudaStream_t st);
 

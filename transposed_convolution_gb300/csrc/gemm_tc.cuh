@@ -490,13 +490,14 @@ template <Prec P, int BN, bool CHAIN>
 cudaError_t launch_inst(const ctr_plan_s *pl, const CUtensorMap *maps, const GemmParams &gp,
                         cudaStream_t st) {
     using C = Cfg<P, BN>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<P, BN, CHAIN>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    // The dynamic shared-memory limit belongs to the current device's context: set it once
+    // per device.
+    static PerDeviceOnce once;
+    cudaError_t ea = once.run(current_device(), cudaSuccess, [] {
+        return cudaFuncSetAttribute(gemm_tc_kernel<P, BN, CHAIN>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    });
+    if (ea != cudaSuccess) return ea;
     const int64_t grid = std::min<int64_t>(gp.num_tiles, (int64_t)pl->num_sms * C::kCtas);
     const cudaError_t e = launch_pdl(gemm_tc_kernel<P, BN, CHAIN>, dim3((unsigned)grid),
                                      dim3(kThreads), (size_t)C::kSmem, st, maps[0], maps[1],

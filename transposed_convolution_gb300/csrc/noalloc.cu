@@ -50,6 +50,19 @@ cudaError_t scratch_address(void **out) {
 
 }  // namespace
 
+namespace ctr {
+uint32_t *noalloc_status_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    return static_cast<uint32_t *>(g_scratch_addr[dev]);
+}
+}  // namespace ctr
+
 extern "C" ctr_status ctr_forward_noalloc(ctr_plan_t pl, const void *x, const void *w,
                                           const void *bias, void *y, void *stream) {
     if (!pl || pl->chain_next) return CTR_ERR_INVALID_ARG;   // chaining needs bound workspaces
