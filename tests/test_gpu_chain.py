@@ -1,14 +1,23 @@
 """Chained plans (ctr_plan_chain): a plan's output stage writes straight into the next plan's
-staged input, and the next plan runs without staging.  The chained results must equal the
-unchained calls bit for bit (the staged values are the same: bf16 rounding, or the tf32
-hi/lo split of the fp32 output), on repeated calls too (the staged halos stay zero)."""
+staged input, and the next plan runs without staging.
+
+* The chained results must equal the unchained calls bit for bit (the staged values are the
+  same: bf16 rounding, or the tf32 hi/lo split of the fp32 output), on repeated calls too
+  (the staged halos stay zero).
+* Against the oracle, run stage by stage with the output of each stage rounded to the I/O
+  type (the value the next stage reads): within rel_l2 <= 1e-5 (fp32 I/O) or <= 1e-2 (bf16)
+  on random inputs, bit for bit on small-integer inputs (every product and partial sum is
+  then exact), and at full size on the vocoder stack the benchmark runs chained.
+"""
 import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import tdtype
+from gpu_helpers import TOL, reference, tdtype, to_dev
 
+import oracle
 import transposed_convolution_gb300 as ctr
+import workloads
 
 pytestmark = pytest.mark.gpu
 
@@ -26,24 +35,56 @@ CHAINS = [
 ]
 
 
-def _make(dtype, B, C_in, sp, layers, rng, chained):
+def _make(dtype, B, C_in, sp, layers, rng, chained, integer=False, host=None):
     """Plans for the layers (chained before the weights are packed, when asked), their biases
-    and the weights drawn from rng."""
+    and the weights drawn from rng (small integers when `integer`); the host copies (weight,
+    bias as numpy values of the I/O type) are appended to `host` when given."""
     plans, bs, ws = [], [], []
     c, s = C_in, tuple(sp)
     for (co, k, st, p, op, slope) in layers:
         pl = ctr.Plan(B, c, co, s, k if isinstance(k, tuple) else (k,) * len(s), st, p, op,
                       dtype=tdtype(dtype), negative_slope=slope)
-        ws.append(rng.uniform(-0.2, 0.2, (c, co) + tuple(pl.kernel)).astype(np.float32))
-        bs.append(torch.from_numpy(rng.standard_normal(co).astype(np.float32)).cuda().to(tdtype(dtype)))
+        if integer:
+            w = rng.integers(-2, 3, (c, co) + tuple(pl.kernel)).astype(np.float32)
+            b = rng.integers(-2, 3, co).astype(np.float32)
+        else:
+            w = workloads._cast(rng.uniform(-0.2, 0.2, (c, co) + tuple(pl.kernel)), dtype)
+            b = workloads._cast(rng.standard_normal(co), dtype)
+        ws.append(w)
+        bs.append(to_dev(b, dtype))
+        if host is not None:
+            host.append((w, b))
         plans.append(pl)
         c, s = co, pl.out_spatial
     if chained:
         for a, nxt in zip(plans[:-1], plans[1:]):
             a.chain(nxt)
     for pl, w in zip(plans, ws):
-        pl.prepack(torch.from_numpy(w).cuda().to(tdtype(dtype)))
+        pl.prepack(to_dev(w, dtype))
     return plans, bs
+
+
+def _run_chain(plans, bs, x, dtype):
+    """One chained forward pass: only the first layer stages an input, only the last writes
+    a y (NaN-filled beforehand, so an unwritten output shows)."""
+    y = torch.full(plans[-1].out_shape, float("nan"), dtype=tdtype(dtype), device="cuda")
+    assert plans[0].forward(x, bs[0]) is None
+    for pl, b in zip(plans[1:-1], bs[1:-1]):
+        assert pl.forward(None, b) is None
+    plans[-1].forward(None, bs[-1], y=y)
+    torch.cuda.synchronize()
+    for pl in plans:
+        pl.check()
+    return y.float().cpu().numpy().astype(np.float64)
+
+
+def _oracle_chain(x, layers, host, dtype):
+    """The oracle stage by stage: each stage's double result plus bias, LeakyReLU, rounded to
+    the I/O type, is the next stage's input."""
+    h = np.asarray(x, dtype=np.float64)
+    for (co, k, st, p, op, slope), (w, b) in zip(layers, host):
+        h = reference(h, w, b, st, p, op, dtype, slope=slope)
+    return h
 
 
 @pytest.mark.parametrize("case", CHAINS, ids=lambda c: "%s-%dd-%dlayers" % (c[0], len(c[3]), len(c[4])))
@@ -106,6 +147,87 @@ def test_chain_errors_on_device():
         st = ctr.lib.ctr_forward(plans[0].handle, x.data_ptr(), plans[0].w_packed.data_ptr(),
                                  None, None, None)
         assert st == ctr.CTR_ERR_INVALID_ARG
+    finally:
+        for pl in plans:
+            pl.close()
+
+
+@pytest.mark.parametrize("case", CHAINS, ids=lambda c: "%s-%dd-%dlayers" % (c[0], len(c[3]), len(c[4])))
+def test_chained_matches_oracle(case):
+    """Random inputs: the chain's last output against the oracle run stage by stage."""
+    dtype, B, C_in, sp, layers = case
+    host = []
+    plans, bs = _make(dtype, B, C_in, sp, layers, np.random.default_rng(51), chained=True,
+                      host=host)
+    try:
+        x = workloads._cast(np.random.default_rng(52).standard_normal((B, C_in) + tuple(sp)), dtype)
+        got = _run_chain(plans, bs, to_dev(x, dtype), dtype)
+        ref = _oracle_chain(x, layers, host, dtype)
+        assert not np.isnan(got).any()
+        err = oracle.rel_l2(got, ref)
+        assert err <= TOL[dtype], "rel_l2 %.3g" % err
+    finally:
+        for pl in plans:
+            pl.close()
+
+
+# Small-integer chains: |x|, |w|, |bias| <= 2 and LeakyReLU slopes that are powers of two, so
+# every product and partial sum of every stage is exact and both sides round the same values.
+INT_CHAINS = [
+    ("bf16", 1, 32, (70,), [(32, 4, 2, 1, 0, 0.25), (32, 4, 2, 1, 0, None)]),        # odd pads
+    ("bf16", 2, 16, (40,), [(24, 16, 8, 4, 0, 0.5), (32, 4, 2, 1, 1, 0.25),
+                            (32, 4, 2, 0, 0, None)]),                                # S8, S2, op
+    ("f32", 1, 32, (50,), [(32, 8, 4, 2, 0, 0.25), (32, 4, 2, 1, 0, None)]),
+    ("f32", 1, 16, (9, 13), [(16, (4, 4), (2, 2), (1, 1), (0, 0), 0.5),
+                             (16, (4, 4), (2, 2), (1, 1), (1, 0), None)]),           # 2-D
+    ("bf16", 1, 32, (30,), [(64, 4, 2, 1, 0, 0.25), (32, 3, 2, 1, 1, None)]),        # col2im next
+]
+
+
+@pytest.mark.parametrize("case", INT_CHAINS,
+                         ids=lambda c: "%s-%dd-%dlayers" % (c[0], len(c[3]), len(c[4])))
+def test_integer_chain_bit_exact(case):
+    dtype, B, C_in, sp, layers = case
+    host = []
+    rng = np.random.default_rng(61)
+    plans, bs = _make(dtype, B, C_in, sp, layers, rng, chained=True, integer=True, host=host)
+    try:
+        x = rng.integers(-2, 3, (B, C_in) + tuple(sp)).astype(np.float32)
+        for it in range(2):
+            got = _run_chain(plans, bs, to_dev(x, dtype), dtype)
+            np.testing.assert_array_equal(got, _oracle_chain(x, layers, host, dtype),
+                                          err_msg="call %d" % it)
+    finally:
+        for pl in plans:
+            pl.close()
+
+
+def test_vocoder_stack_chained_full_size():
+    """The four bf16 upsamplers of the vocoder stack (512 -> 32 channels, 1024 -> 262144
+    samples, LeakyReLU(0.1) after the first three), chained as the benchmark runs them,
+    against the oracle run stage by stage with bf16 rounding between stages."""
+    stages = workloads.make_workload("vocoder_stack_bf16")
+    plans, bs = [], []
+    try:
+        for li in stages:
+            L = li.layer
+            plans.append(ctr.Plan(L.B, L.C_in, L.C_out, L.in_sp, L.kernel, L.stride, L.padding,
+                                  L.output_padding, dtype=torch.bfloat16,
+                                  negative_slope=L.act_slope))
+            bs.append(to_dev(li.bias, "bf16"))
+        for a, nxt in zip(plans[:-1], plans[1:]):
+            a.chain(nxt)
+        for pl, li in zip(plans, stages):
+            pl.prepack(to_dev(li.w, "bf16"))
+        got = _run_chain(plans, bs, to_dev(stages[0].x, "bf16"), "bf16")
+        h = stages[0].x.astype(np.float64)
+        for li in stages:
+            L = li.layer
+            h = reference(h, li.w, li.bias, L.stride, L.padding, L.output_padding, "bf16",
+                          slope=L.act_slope)
+        err = oracle.rel_l2(got, h)
+        print("chained vocoder stack rel_l2 %.3g | %s" % (err, " | ".join(p.describe() for p in plans)))
+        assert err <= TOL["bf16"]
     finally:
         for pl in plans:
             pl.close()
