@@ -155,6 +155,35 @@ ctr_status ctr_plan_set_dilation(ctr_plan_t plan, const int64_t *dilation);
  */
 ctr_status ctr_plan_set_pads(ctr_plan_t plan, const int64_t *pads_begin, const int64_t *pads_end);
 
+typedef enum {
+    CTR_AUTO_PAD_NOTSET = 0,      /* explicit pads (ctr_plan_create / ctr_plan_set_pads) */
+    CTR_AUTO_PAD_SAME_UPPER = 1,  /* output = input * stride, odd total padding: extra at the end */
+    CTR_AUTO_PAD_SAME_LOWER = 2,  /* output = input * stride, odd total padding: extra in front */
+    CTR_AUTO_PAD_VALID = 3        /* no padding */
+} ctr_auto_pad;
+
+/*
+ * The ONNX ConvTranspose `auto_pad` and `output_shape` attributes ("[WebGPU] optimizations
+ * for audio models": the ConvTranspose tests run the ONNX operator's attributes), resolved
+ * into the front and back pads of ctr_plan_set_pads.  Per dimension, with the plan's stride
+ * s, kernel k, dilation d and output_padding op, the unpadded output has
+ * full = (L_in - 1)*s + (k - 1)*d + 1 + op samples, and
+ *   - output_shape given (any auto_pad): total = full - output_shape;
+ *   - else SAME_UPPER / SAME_LOWER: total = full - L_in*s;
+ *   - else VALID: no padding (total = 0);  NOTSET: the plan keeps its pads.
+ * SAME_UPPER puts total/2 (rounded down) in front and the rest at the end; every other
+ * setting puts the rest in front and total/2 at the end.  So the output is the unpadded
+ * result's samples front .. full - back - 1, of length output_shape (or L_in*s).
+ *   auto_pad      a ctr_auto_pad value
+ *   output_shape  ndim output sizes, or NULL
+ * A negative total (an output longer than the unpadded result) would need negative pads:
+ * CTR_ERR_UNSUPPORTED.  Set dilation first (ctr_plan_set_dilation): the pads depend on it.
+ * Host only, with the same ordering rule as ctr_plan_set_path; CTR_ERR_INVALID_ARG for an
+ * unknown auto_pad, an output size < 1, after ctr_prepack_weight, or on a chained or
+ * streaming plan (the plan is then unchanged).
+ */
+ctr_status ctr_plan_set_auto_pad(ctr_plan_t plan, int auto_pad, const int64_t *output_shape);
+
 /*
  * Streaming 1-D ConvTranspose (default off): the input arrives as consecutive chunks of
  * L_in frames (a streaming audio decoder's upsampler), and each ctr_forward emits the
@@ -210,6 +239,30 @@ ctr_status ctr_plan_set_activation(ctr_plan_t plan, int act, float negative_slop
  * CTR_ERR_UNSUPPORTED and leaves the plan unchanged.
  */
 ctr_status ctr_plan_set_path(ctr_plan_t plan, int path, int split_k);
+
+typedef enum {
+    CTR_PHASE_AUTO = 0,      /* the library chooses (below) */
+    CTR_PHASE_UNPADDED = 1,  /* phases of the unpadded output, the padding sliced at the store */
+    CTR_PHASE_OUTPUT = 2     /* phases of the output itself, the padding folded into the taps */
+} ctr_phase_origin;
+
+/*
+ * Where the polyphase path's phase positions start.  "[XNNPACK] Lower dense transposed convs
+ * as one polyphase conv + depth to space" (Summary) computes the phases of the unpadded
+ * output and slices the padding off afterwards (CTR_PHASE_UNPADDED): output o = s*q + j - p,
+ * so with p mod s != 0 every run of s phases starts at an odd offset and the output stage
+ * writes elements one by one.  CTR_PHASE_OUTPUT re-indexes the phases by the output itself,
+ * o = s*Q + J: with p = s*pq + pm, phase J takes the taps s*(m-1-v) + J + pm of the kernel
+ * (zero where that is outside it), which needs one more tap per phase when pm > 0, and reads
+ * input Q + pq - (m-1) + v.  Both compute the same sums of the same products; only zero
+ * products are added or removed.  CTR_PHASE_AUTO takes the output phases when p mod s = 0
+ * (no extra tap) and otherwise when the layer is bound by its output stores rather than by
+ * its products (estimated from the tile model), for a plan whose output is not chained.
+ * Streaming plans keep the unpadded phases.  A tuning and test override: host only, with the
+ * same ordering rule as ctr_plan_set_path; CTR_ERR_INVALID_ARG for another value or after
+ * ctr_prepack_weight.  Ignored by the paths other than polyphase.
+ */
+ctr_status ctr_plan_set_phase_origin(ctr_plan_t plan, int origin);
 
 /*
  * Force the phase-row tile of the tensor-core paths: the number of packed weight rows one

@@ -24,7 +24,7 @@ def to_dev(a, dtype: str):
 
 def run_plan(x, w, bias, stride, padding, output_padding, dtype="f32", slope=None,
              path=ctr.CTR_PATH_AUTO, split_k=0, check_guards=True, expect_path=None, block_n=0,
-             groups=1, dilation=1, padding_end=None):
+             groups=1, dilation=1, padding_end=None, phase_origin=ctr.CTR_PHASE_AUTO):
     """Run one ConvTranspose through the library.  x, w, bias: numpy arrays holding values of
     the I/O dtype.  Returns (y as float64 numpy, plan description)."""
     x = np.asarray(x)
@@ -32,7 +32,8 @@ def run_plan(x, w, bias, stride, padding, output_padding, dtype="f32", slope=Non
     plan = ctr.Plan(x.shape[0], x.shape[1], w.shape[1] * groups, tuple(x.shape[2:]),
                     tuple(w.shape[2:]), stride, padding, output_padding, dtype=tdtype(dtype),
                     negative_slope=slope, path=path, split_k=split_k, block_n=block_n,
-                    groups=groups, dilation=dilation, padding_end=padding_end)
+                    groups=groups, dilation=dilation, padding_end=padding_end,
+                    phase_origin=phase_origin)
     try:
         if expect_path is not None:
             assert plan.path == expect_path, plan.describe()

@@ -14,6 +14,9 @@ Each ``pin_*`` function takes the ConvTranspose callable under test (normally
 * ``pin_polyphase`` -- the polyphase identity of "[XNNPACK] Lower dense transposed convs as
   one polyphase conv + depth to space" (Summary): one stride-1 convolution with m taps and
   padding m - 1 computing every phase, then the phase interleave and the padding slice;
+* ``pin_output_phases`` -- the same polyphase sum re-indexed by the output's own phases:
+  with p = s*pq + pm, phase J of output position Q takes the taps s*(m-1-v) + J + pm of the
+  kernel over m (+1 when pm > 0) input positions Q + pq - (m-1) + v, with no slice;
 * ``pin_istft_sinusoid`` -- the closed-form iSTFT of a sinusoid framed without a window and
   overlap-added with a periodic Hann window at hop N/4, which sums to exactly 2;
 * ``pin_torch_f64_groups`` -- torch's float64 ConvTranspose with groups (2, and depthwise);
@@ -237,6 +240,42 @@ def pin_polyphase(ct):
         _close(ct(x, w, b, s, p, op), ref)
 
 
+def output_phase_restatement(x, w, b, s, p, op):
+    """1-D polyphase form over the output's own phases, in double.  With m = ceil(k/s) and
+    p = s*pq + pm (0 <= pm < s), output position Q's phase J is
+        y[oc, s*Q + J] = sum_{v < m'} sum_ic x[ic, Q + pq - (m - 1) + v] * w[ic, oc, s*(m - 1 - v) + J + pm]
+    with m' = m + (1 if pm > 0 else 0) taps, w = 0 outside [0, k) and x = 0 outside [0, L).
+    The output needs no padding slice: its phases start at output 0."""
+    B, C_in, L = x.shape
+    _, C_out, k = w.shape
+    m = -(-k // s)
+    pq, pm = divmod(p, s)
+    taps = m + (1 if pm else 0)
+    L_out = (L - 1) * s - 2 * p + k + op
+    Qv = -(-L_out // s)
+    y = np.zeros((B, C_out, Qv * s))
+    for Q in range(Qv):
+        for J in range(s):
+            for v in range(taps):
+                i = Q + pq - (m - 1) + v
+                t = s * (m - 1 - v) + J + pm
+                if 0 <= i < L and 0 <= t < k:
+                    y[:, :, s * Q + J] += np.einsum("bc,co->bo", x[:, :, i], w[:, :, t])
+    y = y[:, :, :L_out]
+    if b is not None:
+        y = y + b[None, :, None]
+    return y
+
+
+def pin_output_phases(ct):
+    for (L, k, s, p, op) in grid_1d(full=False):
+        C_in, C_out = 2, 3
+        x = _rng.standard_normal((2, C_in, L))
+        w = _rng.standard_normal((C_in, C_out, k))
+        b = _rng.standard_normal(C_out)
+        _close(ct(x, w, b, s, p, op), output_phase_restatement(x, w, b, s, p, op))
+
+
 def pin_istft_sinusoid(ct, n_fft=64, frames=12, batch=2, bin_f0=5):
     """The onesided spectra of a sinusoid's frames (rectangular window, hop N/4) fed through
     ConvTranspose1d with the Hann-windowed inverse real-DFT basis give 2 * the sinusoid on
@@ -446,4 +485,4 @@ def pin_adjoint_dilated(ct):
 
 ALL_PINS = [pin_torch_f64_dilation, pin_pad_slice, pin_adjoint_dilated, pin_torch_f64_groups, pin_depthwise_k_equals_s, pin_adjoint_groups,
             pin_torch_f64_1d, pin_torch_f64_2d, pin_adjoint, pin_hand_cases, pin_matmul,
-            pin_polyphase, pin_istft_sinusoid]
+            pin_polyphase, pin_output_phases, pin_istft_sinusoid]

@@ -392,6 +392,44 @@ def test_streaming_plan_without_gpu(ctr):
         ctr.ctr_plan_destroy(b)
 
 
+def test_auto_pad_without_gpu(ctr):
+    """ONNX auto_pad / output_shape resolve into front and back pads: SAME_* give
+    L_in * stride outputs with an odd total padding's extra sample at the end (UPPER) or in
+    front (LOWER); an explicit output_shape sets the total; VALID pads nothing; a longer
+    output than the unpadded result is refused and leaves the plan as it was."""
+    f32 = ctr.CTR_F32
+    # 1-D, k = 3, s = 2, L = 5: unpadded length (5 - 1)*2 + 3 = 11, SAME target 10 (total 1)
+    for mode, front, back in ((ctr.CTR_AUTO_PAD_SAME_UPPER, 0, 1),
+                              (ctr.CTR_AUTO_PAD_SAME_LOWER, 1, 0)):
+        h = _plan(ctr, 1, 1, 32, 64, [5], [3], [2], [0], [0], f32)
+        try:
+            ctr.ctr_plan_set_auto_pad(h, mode)
+            assert ctr.ctr_plan_output_shape(h, 1) == (10,)
+            d = ctr.ctr_plan_describe(h)
+            assert "pads=0x%d/0x%d" % (front, back) in d, d
+        finally:
+            ctr.ctr_plan_destroy(h)
+    # 2-D with dilation 2 in x: unpadded (4-1)*2 + (3-1)*2 + 1 = 11 along x, 4x4/s2 along y
+    h = _plan(ctr, 2, 1, 32, 64, [4, 4], [4, 3], [2, 2], [0, 0], [0, 1], f32)
+    try:
+        ctr.ctr_plan_set_dilation(h, ctr._arr([1, 2]))
+        ctr.ctr_plan_set_auto_pad(h, ctr.CTR_AUTO_PAD_SAME_UPPER)
+        assert ctr.ctr_plan_output_shape(h, 2) == (8, 8)       # totals 2 and 4 (op 1 included)
+        assert "pads=1x2/1x2" in ctr.ctr_plan_describe(h)
+        ctr.ctr_plan_set_auto_pad(h, ctr.CTR_AUTO_PAD_NOTSET, [9, 7])   # totals 1 and 5
+        assert ctr.ctr_plan_output_shape(h, 2) == (9, 7)
+        assert "pads=1x3/0x2" in ctr.ctr_plan_describe(h)
+        ctr.ctr_plan_set_auto_pad(h, ctr.CTR_AUTO_PAD_VALID)
+        assert ctr.ctr_plan_output_shape(h, 2) == (10, 12)
+        # longer than the unpadded result: refused, plan unchanged
+        assert ctr.lib.ctr_plan_set_auto_pad(h, 0, ctr._arr([11, 12])) == ctr.CTR_ERR_UNSUPPORTED
+        assert ctr.ctr_plan_output_shape(h, 2) == (10, 12)
+        assert ctr.lib.ctr_plan_set_auto_pad(h, 4, None) == ctr.CTR_ERR_INVALID_ARG
+        assert ctr.lib.ctr_plan_set_auto_pad(h, 0, ctr._arr([0, 5])) == ctr.CTR_ERR_INVALID_ARG
+    finally:
+        ctr.ctr_plan_destroy(h)
+
+
 def test_istft_plan_without_gpu(ctr):
     """ctr_istft_*: argument checks, output length, workspace size; no window -> not prepared."""
     h = ctr.ctr_istft_create(4, 4096, 1024, 343)

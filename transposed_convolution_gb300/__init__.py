@@ -7,8 +7,8 @@ any non-OK status from the library raises ``CtrError``.
 
 Low level (same names as the C ABI): ``ctr_plan_create``, ``ctr_plan_set_activation``,
 ``ctr_plan_set_path``, ``ctr_plan_set_groups``, ``ctr_plan_set_dilation``, ``ctr_plan_set_pads``,
-``ctr_plan_set_streaming``, ``ctr_plan_stream_reset``,
-``ctr_plan_set_tile``, ``ctr_plan_chain``, ``ctr_plan_get_path``, ``ctr_plan_output_shape``,
+``ctr_plan_set_auto_pad``, ``ctr_plan_set_streaming``, ``ctr_plan_stream_reset``,
+``ctr_plan_set_tile``, ``ctr_plan_set_phase_origin``, ``ctr_plan_chain``, ``ctr_plan_get_path``, ``ctr_plan_output_shape``,
 ``ctr_packed_weight_bytes``, ``ctr_workspace_bytes``, ``ctr_plan_bind_workspace``,
 ``ctr_prepack_weight``, ``ctr_forward``, ``ctr_forward_noalloc``, ``ctr_plan_check``,
 ``ctr_plan_set_wait_limit_ns``,
@@ -49,6 +49,13 @@ CTR_PATH_POLYPHASE = 1
 CTR_PATH_COL2IM = 2
 CTR_PATH_GATHER = 3
 CTR_PATH_DEPTHWISE = 4
+CTR_AUTO_PAD_NOTSET = 0
+CTR_AUTO_PAD_SAME_UPPER = 1
+CTR_AUTO_PAD_SAME_LOWER = 2
+CTR_AUTO_PAD_VALID = 3
+CTR_PHASE_AUTO = 0
+CTR_PHASE_UNPADDED = 1
+CTR_PHASE_OUTPUT = 2
 PATH_NAMES = {CTR_PATH_POLYPHASE: "polyphase", CTR_PATH_COL2IM: "col2im", CTR_PATH_GATHER: "gather",
               CTR_PATH_DEPTHWISE: "depthwise"}
 
@@ -64,9 +71,11 @@ SIGNATURES = {
     "ctr_plan_set_groups": (ctypes.c_int, [_vp, ctypes.c_int64]),
     "ctr_plan_set_dilation": (ctypes.c_int, [_vp, _i64p]),
     "ctr_plan_set_pads": (ctypes.c_int, [_vp, _i64p, _i64p]),
+    "ctr_plan_set_auto_pad": (ctypes.c_int, [_vp, ctypes.c_int, _i64p]),
     "ctr_plan_set_streaming": (ctypes.c_int, [_vp, ctypes.c_int]),
     "ctr_plan_stream_reset": (ctypes.c_int, [_vp, _vp]),
     "ctr_plan_set_tile": (ctypes.c_int, [_vp, ctypes.c_int]),
+    "ctr_plan_set_phase_origin": (ctypes.c_int, [_vp, ctypes.c_int]),
     "ctr_plan_chain": (ctypes.c_int, [_vp, _vp]),
     "ctr_plan_get_path": (ctypes.c_int, [_vp]),
     "ctr_plan_output_shape": (ctypes.c_int, [_vp, _i64p]),
@@ -188,6 +197,11 @@ def ctr_plan_set_pads(plan, pads_begin, pads_end):
     _check(lib.ctr_plan_set_pads(plan, _arr(pads_begin), _arr(pads_end)), "ctr_plan_set_pads")
 
 
+def ctr_plan_set_auto_pad(plan, auto_pad, output_shape=None):
+    _check(lib.ctr_plan_set_auto_pad(plan, auto_pad, None if output_shape is None
+                                     else _arr(output_shape)), "ctr_plan_set_auto_pad")
+
+
 def ctr_plan_set_streaming(plan, enable):
     _check(lib.ctr_plan_set_streaming(plan, int(enable)), "ctr_plan_set_streaming")
 
@@ -198,6 +212,10 @@ def ctr_plan_stream_reset(plan, stream):
 
 def ctr_plan_set_tile(plan, block_n):
     _check(lib.ctr_plan_set_tile(plan, int(block_n)), "ctr_plan_set_tile")
+
+
+def ctr_plan_set_phase_origin(plan, origin):
+    _check(lib.ctr_plan_set_phase_origin(plan, origin), "ctr_plan_set_phase_origin")
 
 
 def ctr_plan_chain(plan, next_plan):
@@ -350,7 +368,8 @@ class Plan:
     def __init__(self, N, C_in, C_out, in_spatial, kernel, stride=1, padding=0,
                  output_padding=0, dtype=None, negative_slope=None, path=CTR_PATH_AUTO,
                  split_k=0, device=None, block_n=0, groups=1, dilation=1, padding_end=None,
-                 streaming=False):
+                 streaming=False, phase_origin=CTR_PHASE_AUTO, auto_pad=CTR_AUTO_PAD_NOTSET,
+                 output_shape=None):
         torch = _torch()
         self.ndim = len(in_spatial)
         self.dtype = dtype if dtype is not None else torch.float32
@@ -376,6 +395,8 @@ class Plan:
                 ctr_plan_set_dilation(self.handle, self.dilation)
             if self.padding_end != self.padding:
                 ctr_plan_set_pads(self.handle, self.padding, self.padding_end)
+            if auto_pad != CTR_AUTO_PAD_NOTSET or output_shape is not None:
+                ctr_plan_set_auto_pad(self.handle, auto_pad, output_shape)
             self.streaming = bool(streaming)
             if self.streaming:
                 ctr_plan_set_streaming(self.handle, 1)
@@ -383,6 +404,8 @@ class Plan:
                 ctr_plan_set_path(self.handle, path, split_k)
             if block_n:
                 ctr_plan_set_tile(self.handle, block_n)
+            if phase_origin != CTR_PHASE_AUTO:
+                ctr_plan_set_phase_origin(self.handle, phase_origin)
             self.out_spatial = ctr_plan_output_shape(self.handle, self.ndim)
             self.path = ctr_plan_get_path(self.handle)
             self.packed_bytes = ctr_packed_weight_bytes(self.handle)

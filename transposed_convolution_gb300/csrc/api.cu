@@ -90,7 +90,7 @@ int tf32_group() {
 // MMA time, its operand-load time and its output time, and the extra pass over split-K
 // partials.  3xTF32 at BN = 256 keeps its group sums in TMEM beside a single accumulator, so
 // the MMAs pause while each group is folded into the sums (~800 clocks).
-void choose_tiling(ctr_plan_s *pl) {
+double choose_tiling(ctr_plan_s *pl, double epi_factor = 1.0) {
     const Prec prec = prec_of(pl);
     const int group = prec == Prec::TF32x3 ? tf32_group() : kNoGroup;
     const int kb_total = (int)(pl->K_total * op_esize(pl) / ctr::kBKBytes);
@@ -115,7 +115,7 @@ void choose_tiling(ctr_plan_s *pl) {
             double mma = kbs * slice_clocks(prec, bn);
             if (prec == Prec::TF32x3 && bn == 256) mma += 800.0 * std::ceil(kbs / std::min(kbs, (double)group));
             const double load = kbs * (ctr::kBM + bn) * (double)ctr::kBKBytes * op_planes(pl) / 50.0;
-            const double epi = ctr::kBM * (double)bn * esize_io(pl) / 20.0 + 300.0;
+            const double epi = epi_factor * ctr::kBM * (double)bn * esize_io(pl) / 20.0 + 300.0;
             const double tile = std::max(mma, std::max(load, epi));
             double t = (double)waves * tile + 2000.0;
             if (sp > 1 || pl->path == CTR_PATH_COL2IM) {
@@ -135,6 +135,7 @@ void choose_tiling(ctr_plan_s *pl) {
     pl->num_p_tiles = (int)num_p;
     pl->num_r_tiles = (int)std::max<int64_t>(1, ceil_div(pl->M_rows, best_bn));
     pl->num_tiles = (int64_t)pl->num_p_tiles * pl->num_r_tiles * pl->splits;
+    return best;
 }
 
 // Extent of the dilated kernel along dimension d: (k - 1)*dil + 1 samples, of which the k
@@ -167,6 +168,74 @@ bool set_output_lengths(ctr_plan_s *pl) {
     return true;
 }
 
+// Phase geometry of the polyphase path per dimension (see ctr_plan_s): taps, halos, tap base,
+// output offset, valid phase positions and the staged pitch, for unpadded phases
+// (out_phases = 0) or output phases (1).
+void phase_geometry(ctr_plan_s *pl, int out_phases) {
+    for (int d = 0; d < 2; ++d) {
+        const int64_t s = pl->s[d], mk = ceil_div(dilated_extent(pl, d), s);
+        pl->mk[d] = mk;
+        if (out_phases) {
+            const int64_t pq = pl->p[d] / s, pm = pl->p[d] - pq * s;
+            const int64_t c0 = pq - (mk - 1);    // input index of tap 0 at phase position 0
+            pl->m[d] = mk + (pm > 0 ? 1 : 0);
+            pl->pm[d] = pm;
+            pl->hf[d] = std::max<int64_t>(0, -c0);
+            pl->rb[d] = std::max<int64_t>(0, c0);
+            pl->ep[d] = 0;
+            pl->Qv[d] = ceil_div(pl->out[d], s);
+            pl->P[d] = std::max(pl->hf[d] + pl->in[d], pl->rb[d] + pl->Qv[d] + pl->m[d] - 1);
+        } else {
+            pl->m[d] = mk;
+            pl->pm[d] = 0;
+            pl->hf[d] = mk - 1;
+            pl->rb[d] = 0;
+            pl->ep[d] = pl->p[d];
+            pl->Qv[d] = ceil_div(pl->out[d] + pl->p[d], s);
+            pl->P[d] = std::max(pl->in[d] + 2 * (mk - 1), pl->Qv[d] + mk - 1);
+        }
+    }
+}
+
+// Bytes of the widest aligned store of an interior output run (see make_epi): the run length
+// (the x stride), the output offset of the phase map and the output row pitch must all be
+// multiples of it.  Element size when nothing wider fits.
+int run_store_bytes(const ctr_plan_s *pl, int64_t ex) {
+    const int es = esize_io(pl);
+    const int64_t run = pl->s[1] * es;
+    for (int w : {16, 8, 4})
+        if (run % w == 0 && (ex * es) % w == 0 && (pl->out[1] * es) % w == 0) return w;
+    return es;
+}
+
+// Output phases when they cost no extra tap (p mod s = 0 in every dimension), and otherwise
+// when the tile model, with element-wise stores priced at 2.5x (bf16) or 1.5x (fp32) the
+// vector rate, expects them to be faster: a layer bound by its output stores rather than by
+// its products.  A chained output goes to the next plan's channels-last staged input, where
+// the runs of one position are channels, so it gains nothing from aligned runs.
+int choose_phase_origin(ctr_plan_s *pl) {
+    if (pl->streaming) return 0;   // the carried frames are the unpadded form's halo rows
+    if (pl->forced_origin == CTR_PHASE_UNPADDED) return 0;
+    if (pl->forced_origin == CTR_PHASE_OUTPUT) return 1;
+    if (pl->p[0] % pl->s[0] == 0 && pl->p[1] % pl->s[1] == 0) return 1;
+    if (pl->chain_next) return 0;
+    const int es = esize_io(pl);
+    const int w_pad = run_store_bytes(pl, pl->p[1]);
+    const double f_pad = w_pad > es ? 1.0 : (es == 2 ? 2.5 : 1.5);
+    const auto estimate = [&](int out_phases, double factor) {
+        phase_geometry(pl, out_phases);
+        pl->S_pad = (int)(pl->S <= ctr::kBM ? next_pow2(pl->S) : round_up(pl->S, ctr::kBM));
+        pl->M_rows = pl->C_out * pl->S_pad;
+        pl->M_pad = round_up(pl->M_rows, 64);
+        pl->K_total = pl->m[0] * pl->m[1] * pl->C_in_pad;
+        pl->N_total = pl->B * pl->P[0] * pl->P[1];
+        return choose_tiling(pl, factor);
+    };
+    const double t_pad = estimate(0, f_pad);
+    const double t_out = estimate(1, 1.0);
+    return t_out < t_pad ? 1 : 0;
+}
+
 // Derive the GEMM geometry, tiling, packed size and workspace layout from the path.
 void layout_plan(ctr_plan_s *pl) {
     pl->packed_bytes = 0;
@@ -187,15 +256,15 @@ void layout_plan(ctr_plan_s *pl) {
     const int bk = bk_elems(pl);
     pl->C_in_pad = round_up(pl->C_in, bk);
     if (pl->path == CTR_PATH_POLYPHASE) {
-        for (int d = 0; d < 2; ++d) {
-            pl->m[d] = ceil_div(dilated_extent(pl, d), pl->s[d]);
-            pl->Qv[d] = ceil_div(pl->out[d] + pl->p[d], pl->s[d]);
-            pl->P[d] = std::max(pl->in[d] + 2 * (pl->m[d] - 1), pl->Qv[d] + pl->m[d] - 1);
-        }
         pl->S = (int)(pl->s[0] * pl->s[1]);
+        pl->out_phases = choose_phase_origin(pl);
+        phase_geometry(pl, pl->out_phases);
     } else {  // col2im: plain GEMM over input positions, rows (oc, tap)
+        pl->out_phases = 0;
         for (int d = 0; d < 2; ++d) {
-            pl->m[d] = 1;
+            pl->m[d] = pl->mk[d] = 1;
+            pl->pm[d] = pl->hf[d] = pl->rb[d] = 0;
+            pl->ep[d] = pl->p[d];
             pl->Qv[d] = pl->in[d];
             pl->P[d] = pl->in[d];
         }
@@ -244,7 +313,7 @@ bool chain_compatible(const ctr_plan_s *pl, const ctr_plan_s *nx) {
 // packed rows in 32 bits.
 bool tc_index_fits(const ctr_plan_s *pl) {
     const int64_t lim = (int64_t)1 << 31;
-    const int64_t shift = pl->P[1] * (pl->m[0] - 1) + pl->m[1];
+    const int64_t shift = pl->P[1] * (pl->rb[0] + pl->m[0] - 1) + pl->rb[1] + pl->m[1];
     return pl->num_p_tiles * (int64_t)ctr::kBM + shift < lim && pl->num_tiles < lim &&
            pl->M_pad + 256 < lim;
 }
@@ -316,8 +385,8 @@ EpiParams make_epi(const ctr_plan_s *pl, const void *bias, void *y) {
     e.S_pad = pl->S_pad;
     e.sy = (int)pl->s[0];
     e.sx = (int)pl->s[1];
-    e.py = (int)pl->p[0];
-    e.px = (int)pl->p[1];
+    e.py = (int)pl->ep[0];
+    e.px = (int)pl->ep[1];
     e.Py = pl->P[0];
     e.Px = pl->P[1];
     e.Qvy = pl->Qv[0];
@@ -365,7 +434,7 @@ EpiParams make_epi(const ctr_plan_s *pl, const void *bias, void *y) {
     e.pm_tc = pl->row_pm ? pl->block_n / pl->S_pad : 0;
     e.store_bytes = es;
     for (int w : {16, 8, 4}) {
-        if (nx > 0 && (nx * es) % w == 0 && (sx * es) % w == 0 && (pl->p[1] * es) % w == 0 &&
+        if (nx > 0 && (nx * es) % w == 0 && (sx * es) % w == 0 && (e.px * es) % w == 0 &&
             (pl->out[1] * es) % w == 0) {
             e.store_bytes = w;
             break;
@@ -441,6 +510,7 @@ cudaError_t run_tc_path(const ctr_plan_s *pl, const void *x, const void *w_packe
     gp.kb_group = pl->kb_group == kNoGroup ? kNoGroup : pl->kb_group * (kBKBytes / sb);
     gp.mx = (int)pl->m[1];
     gp.Px = pl->P[1];
+    gp.shift0 = pl->rb[0] * pl->P[1] + pl->rb[1];
     const bool fused = pl->path == CTR_PATH_POLYPHASE && pl->splits == 1;
     gp.epi_mode = fused ? EPI_POLYPHASE : EPI_RAW;
     gp.epi = make_epi(pl, bias, y);
@@ -451,8 +521,8 @@ cudaError_t run_tc_path(const ctr_plan_s *pl, const void *x, const void *w_packe
         gp.epi.y = static_cast<char *>(nx->ws) + nx->ws_off_stage;
         gp.epi.ys_Py = nx->P[0];
         gp.epi.ys_Px = nx->P[1];
-        gp.epi.ys_hy = nx->m[0] - 1;
-        gp.epi.ys_hx = nx->m[1] - 1;
+        gp.epi.ys_hy = nx->hf[0];
+        gp.epi.ys_hx = nx->hf[1];
         gp.epi.ys_cpad = nx->C_in_pad;
         gp.epi.ys_lo = nx->N_total * nx->C_in_pad;
     }
@@ -520,6 +590,7 @@ ctr_status ctr_plan_create(ctr_plan_t *out, int ndim, int64_t N, int64_t C_in, i
     pl->act = CTR_ACT_NONE;
     pl->slope = 0.0f;
     pl->forced_path = CTR_PATH_AUTO;
+    pl->forced_origin = CTR_PHASE_AUTO;
     pl->stream_saved_path = CTR_PATH_AUTO;
     pl->forced_split = 0;
     pl->forced_bn = 0;
@@ -695,6 +766,36 @@ ctr_status ctr_plan_set_pads(ctr_plan_t pl, const int64_t *pads_begin, const int
     return set_geometry(pl, dil, pb, pe);
 }
 
+ctr_status ctr_plan_set_auto_pad(ctr_plan_t pl, int auto_pad, const int64_t *output_shape) {
+    if (!pl || auto_pad < CTR_AUTO_PAD_NOTSET || auto_pad > CTR_AUTO_PAD_VALID)
+        return CTR_ERR_INVALID_ARG;
+    if (pl->prepared || pl->chain_next || pl->chain_prev || pl->streaming)
+        return CTR_ERR_INVALID_ARG;
+    if (!output_shape && auto_pad == CTR_AUTO_PAD_NOTSET) return CTR_OK;   // explicit pads stay
+    int64_t pb[2] = {0, 0}, pe[2] = {0, 0};
+    for (int d = 2 - pl->ndim; d < 2; ++d) {
+        const int64_t full = (pl->in[d] - 1) * pl->s[d] + dilated_extent(pl, d) + pl->op[d];
+        int64_t total = 0;
+        if (output_shape) {
+            const int64_t want = output_shape[d - (2 - pl->ndim)];
+            if (want < 1) return CTR_ERR_INVALID_ARG;
+            total = full - want;
+        } else if (auto_pad != CTR_AUTO_PAD_VALID) {
+            total = full - pl->in[d] * pl->s[d];
+        }
+        if (total < 0) return CTR_ERR_UNSUPPORTED;
+        if (auto_pad == CTR_AUTO_PAD_SAME_UPPER) {
+            pb[d] = total / 2;
+            pe[d] = total - pb[d];
+        } else {
+            pe[d] = total / 2;
+            pb[d] = total - pe[d];
+        }
+    }
+    const int64_t dil[2] = {pl->dil[0], pl->dil[1]};
+    return set_geometry(pl, dil, pb, pe);
+}
+
 ctr_status ctr_plan_set_streaming(ctr_plan_t pl, int enable) {
     if (!pl || (enable != 0 && enable != 1)) return CTR_ERR_INVALID_ARG;
     if (pl->prepared || pl->chain_next || pl->chain_prev) return CTR_ERR_INVALID_ARG;
@@ -742,6 +843,19 @@ ctr_status ctr_plan_stream_reset(ctr_plan_t pl, void *stream) {
                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return CTR_ERR_CUDA;
     pl->stream_ready = 1;
+    return CTR_OK;
+}
+
+ctr_status ctr_plan_set_phase_origin(ctr_plan_t pl, int origin) {
+    if (!pl || origin < CTR_PHASE_AUTO || origin > CTR_PHASE_OUTPUT) return CTR_ERR_INVALID_ARG;
+    if (pl->prepared) return CTR_ERR_INVALID_ARG;
+    pl->forced_origin = origin;
+    layout_plan(pl);
+    if (is_tc_path(pl->path) && !tc_index_fits(pl)) {
+        pl->forced_origin = CTR_PHASE_AUTO;
+        layout_plan(pl);
+        return CTR_ERR_UNSUPPORTED;
+    }
     return CTR_OK;
 }
 
@@ -799,13 +913,14 @@ ctr_status ctr_plan_describe(ctr_plan_t pl, char *buf, size_t len) {
         const EpiParams ep = make_epi(pl, nullptr, nullptr);
         snprintf(buf, len,
                  "path=%s prec=%s rows=%lld(pad %lld, BN %d, %d tiles) positions=%lld(%d tiles) "
-                 "K=%lld splits=%d group=%d tiles=%lld sms=%d S=%d/%d taps=%lldx%lld "
+                 "K=%lld splits=%d group=%d tiles=%lld sms=%d S=%d/%d taps=%lldx%lld%s "
                  "pitch=%lldx%lld epi=%d/%dB packed=%zu ws=%zu",
                  pname, pl->dtype == CTR_BF16 ? "bf16" : "3xtf32", (long long)pl->M_rows,
                  (long long)pl->M_pad, pl->block_n, pl->num_r_tiles, (long long)pl->N_total,
                  pl->num_p_tiles, (long long)pl->K_total, pl->splits,
                  pl->kb_group == kNoGroup ? 0 : pl->kb_group, (long long)pl->num_tiles,
                  pl->num_sms, pl->S, pl->S_pad, (long long)pl->m[0], (long long)pl->m[1],
+                 pl->out_phases ? " out-phases" : "",
                  (long long)pl->P[0], (long long)pl->P[1], ep.kind, ep.store_bytes,
                  pl->packed_bytes, pl->ws_bytes_needed);
     } else {

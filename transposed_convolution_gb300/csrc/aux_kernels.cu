@@ -146,6 +146,8 @@ __global__ void copy_bytes_kernel(const uint4 *__restrict__ src, uint4 *__restri
 struct PackGeo {
     int64_t M_pad, K_total, C_in_pad, C_in, C_out;
     int64_t ky, kx, sy, sx, my, mx;
+    int64_t mky, mkx;     // phase taps of the kernel (my, mx count one more with a folded pm)
+    int64_t pmy, pmx;     // padding remainder folded into the taps (output phases)
     int64_t dy, dx;       // dilation (polyphase rows of the zero-inserted kernel)
     int S, S_pad;
     int polyphase;
@@ -156,8 +158,11 @@ struct PackGeo {
 // Polyphase rows ("[XNNPACK] Lower dense transposed convs as one polyphase conv + depth to
 // space", Summary: phase-major ordering, taps flipped within a phase):
 //   A[r = oc*S_pad + jy*sx + jx, k = (uy*mx + ux)*C_in_pad + ic]
-//       = w[ic, oc, sy*(my-1-uy) + jy, sx*(mx-1-ux) + jx]    (0 past the kernel: the kernel
-//                                                               is zero-padded to m*s taps)
+//       = w[ic, oc, sy*(mky-1-uy) + jy + pmy, sx*(mkx-1-ux) + jx + pmx]
+// with 0 outside the kernel (the kernel is zero-padded to m*s taps).  pm = 0 gives the
+// pages' phases of the unpadded output; pm = p mod s the phases of the output itself, whose
+// phase j is the unpadded output's phase j + pm (the next position's phase j + pm - s when
+// that reaches s, hence the extra tap).
 // With dilation the polyphase rows come from the zero-inserted kernel: a dilated tap index
 // e (per dimension) holds w[.., e / dil] when e is a multiple of dil and e / dil < k, and
 // zero otherwise.
@@ -189,11 +194,12 @@ __global__ void prepack_kernel(const void *__restrict__ w, void *__restrict__ wp
             if (pg.polyphase) {
                 const int64_t jy = j / pg.sx, jx = j - (j / pg.sx) * pg.sx;
                 const int64_t uy = g / pg.mx, ux = g - (g / pg.mx) * pg.mx;
-                ty = pg.sy * (pg.my - 1 - uy) + jy;
-                tx = pg.sx * (pg.mx - 1 - ux) + jx;
-                // Dilated tap index -> real tap (past the kernel when between taps).
-                ty = ty % pg.dy ? pg.ky : ty / pg.dy;
-                tx = tx % pg.dx ? pg.kx : tx / pg.dx;
+                ty = pg.sy * (pg.mky - 1 - uy) + jy + pg.pmy;
+                tx = pg.sx * (pg.mkx - 1 - ux) + jx + pg.pmx;
+                // Dilated tap index -> real tap (past the kernel when before the first tap or
+                // between taps).
+                ty = (ty < 0 || ty % pg.dy) ? pg.ky : ty / pg.dy;
+                tx = (tx < 0 || tx % pg.dx) ? pg.kx : tx / pg.dx;
             } else {
                 ty = j / pg.kx;
                 tx = j - ty * pg.kx;
@@ -219,8 +225,9 @@ struct StageGeo {
 };
 
 // xs[n][c] with n = (b*Py + py')*Px + px': x[b, c, py' - hy, px' - hx] inside the input and
-// c < C_in, zero elsewhere (the halos are the polyphase conv's padding m - 1).  fp32 input
-// is written as tf32 hi and lo planes.
+// c < C_in, zero elsewhere (the front halos hy, hx are the polyphase conv's padding m - 1,
+// less the phase positions the output phases skip).  fp32 input is written as tf32 hi and lo
+// planes.
 //
 // A block transposes one tile of 128 input positions (along x, within one staged row) by
 // kStageC channels (64 bf16 or 32 fp32, i.e. 128 bytes of a staged row) through shared
@@ -422,7 +429,7 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ raw, EpiParams ep
         }
     }
     // decode_pos marks positions at or past n_rows (= B * Py * Px) invalid.
-    emit_cols<true>(v, decode_pos(n, ep), r0, ep, (int)(threadIdx.x & 31));
+    emit_cols<kOutBoth, kIoAny>(v, decode_pos(n, ep), r0, ep, (int)(threadIdx.x & 31));
 }
 
 // -------------------------------------------------------------------------- streaming
@@ -559,6 +566,10 @@ cudaError_t launch_prepack(const ctr_plan_s *pl, const void *w, void *w_packed, 
     pg.sx = pl->s[1];
     pg.my = pl->m[0];
     pg.mx = pl->m[1];
+    pg.mky = pl->mk[0];
+    pg.mkx = pl->mk[1];
+    pg.pmy = pl->pm[0];
+    pg.pmx = pl->pm[1];
     pg.dy = pl->dil[0];
     pg.dx = pl->dil[1];
     pg.S = pl->S;
@@ -603,8 +614,8 @@ cudaError_t launch_stage_x(const ctr_plan_s *pl, const void *x, void *xs, cudaSt
     sg.W = pl->in[1];
     sg.Py = pl->P[0];
     sg.Px = pl->P[1];
-    sg.hy = pl->m[0] - 1;
-    sg.hx = pl->m[1] - 1;
+    sg.hy = pl->hf[0];
+    sg.hx = pl->hf[1];
     sg.N_total = pl->N_total;
     sg.bf16 = pl->dtype == CTR_BF16 ? 1 : 0;
     if (sg.N_total == 0) return cudaSuccess;

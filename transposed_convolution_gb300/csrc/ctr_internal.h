@@ -70,6 +70,7 @@ struct GemmParams {
     int kb_group;       // K slices per tensor-core accumulation group (see gemm_tc.cu)
     int mx;             // taps along x: tap g -> (uy, ux) = (g / mx, g % mx)
     int64_t Px;         // position shift of one tap step along y
+    int64_t shift0;     // staged row of tap 0 relative to the position (rb_y*Px + rb_x)
     int epi_mode;
     EpiParams epi;
     float *raw;         // EPI_RAW: D goes to raw[z][n][r] with leading dimension raw_ld
@@ -108,8 +109,24 @@ struct ctr_plan_s {
     int prepared;       // ctr_prepack_weight ran (status word allocated)
     int num_sms;
 
-    // Tensor-core GEMM geometry (polyphase and col2im paths).
-    int64_t m[2];       // taps per phase per dim (polyphase), 1 for col2im
+    // Tensor-core GEMM geometry (polyphase and col2im paths).  Per dimension the GEMM's
+    // phase position Q and tap v read staged input row Q + rb + v, i.e. input index
+    // Q + rb - hf + v; D[Q, (oc, j)] lands at output s*Q + j - ep.
+    //   unpadded phases (the pages' form): Q indexes the unpadded output's phases, the
+    //     packed tap of (v, j) is s*(mk-1-v) + j, hf = mk - 1, rb = 0, ep = p (the padding
+    //     slice is applied at the store);
+    //   output phases: Q indexes the output's own phases; with p = s*pq + pm the packed tap
+    //     of (v, j) is s*(mk-1-v) + j + pm (zero outside the kernel), one more tap when
+    //     pm > 0, hf = max(0, mk-1-pq), rb = max(0, pq-(mk-1)), ep = 0: every output run
+    //     starts at s*Q, so the stores are aligned whatever the padding.
+    int64_t m[2];       // GEMM taps per dim (polyphase), 1 for col2im
+    int64_t mk[2];      // phase taps of the kernel, ceil(dilated extent / s)
+    int64_t pm[2];      // padding remainder folded into the packed taps (output phases)
+    int64_t hf[2];      // zero rows in front of the input in the staged layout
+    int64_t rb[2];      // staged row of tap 0 relative to the phase position
+    int64_t ep[2];      // output offset of the phase map (padding sliced at the store)
+    int out_phases;     // 1: output phases, 0: unpadded phases
+    int forced_origin;  // ctr_plan_set_phase_origin (CTR_PHASE_AUTO = choose)
     int64_t Qv[2];      // valid phase columns per dim
     int64_t P[2];       // staged pitch per dim (with halos)
     int S, S_pad;       // phases (polyphase) or taps (col2im) per output channel, padded

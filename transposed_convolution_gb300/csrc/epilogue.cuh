@@ -152,15 +152,184 @@ __device__ __forceinline__ float slope_of(const EpiParams &e) {
     return e.act == CTR_ACT_LEAKY_RELU ? e.slope : 1.0f;
 }
 
+// ------------------------------------------------------------ fast chunk output
+// Most chunks lie wholly inside the output: their channels exist and every lane's outputs
+// are inside the output rows and columns.  The warp then takes a straight-line path, in
+// place on the accumulator values: per block of channels whose biases fill one vector load
+// (the same address on every lane: a broadcast), the bias is added, the activation applied
+// and every run stored at a compile-time width.  No per-channel or per-run branches, so the
+// compiler can interleave the channels' independent arithmetic and stores.  Other chunks
+// take the element-wise paths.
+
+// Biases of channels oc0 .. oc0+N-1 (all inside C_out) in one load of N * sizeof(T) <= 16
+// bytes, or zeros.  oc0 is a multiple of N (a power of two) and the bias pointer 16-byte
+// aligned, so the load is aligned.
+template <typename T, int N>
+__device__ __forceinline__ void load_bias_vec(const EpiParams &e, int64_t oc0, float (&b)[N]) {
+    static_assert(N * sizeof(T) <= 16, "one vector load");
+    if (!e.bias) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) b[i] = 0.0f;
+        return;
+    }
+    const T *src = static_cast<const T *>(e.bias) + oc0;
+    if constexpr (sizeof(T) == 2 && N == 8) {
+        const uint4 q = __ldg(reinterpret_cast<const uint4 *>(src));
+        const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            b[2 * k] = __uint_as_float(w4[k] << 16);
+            b[2 * k + 1] = __uint_as_float(w4[k] & 0xFFFF0000u);
+        }
+    } else if constexpr (sizeof(T) == 2 && N == 4) {
+        const uint2 q = __ldg(reinterpret_cast<const uint2 *>(src));
+        b[0] = __uint_as_float(q.x << 16);
+        b[1] = __uint_as_float(q.x & 0xFFFF0000u);
+        b[2] = __uint_as_float(q.y << 16);
+        b[3] = __uint_as_float(q.y & 0xFFFF0000u);
+    } else if constexpr (sizeof(T) == 4 && N == 4) {
+        const float4 q = __ldg(reinterpret_cast<const float4 *>(src));
+        b[0] = q.x;
+        b[1] = q.y;
+        b[2] = q.z;
+        b[3] = q.w;
+    } else if constexpr (sizeof(T) == 4 && N == 2) {
+        const float2 q = __ldg(reinterpret_cast<const float2 *>(src));
+        b[0] = q.x;
+        b[1] = q.y;
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i) b[i] = static_cast<float>(src[i]);
+    }
+}
+
+// Channels per bias load: as many as fill 16 bytes, at most G.
+template <typename T, int G>
+__host__ __device__ constexpr int bias_block() {
+    return G < (int)(16 / sizeof(T)) ? G : (int)(16 / sizeof(T));
+}
+
+// v[i] = act(v[i] + bias) for the n values at v (ACT: LeakyReLU with slope sl).
+template <bool ACT, int N>
+__device__ __forceinline__ void add_bias_act(float *v, float bias, float sl) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const float a = v[i] + bias;
+        v[i] = ACT ? (a < 0.0f ? a * sl : a) : a;
+    }
+}
+
+// N consecutive outputs at dst as VW-byte stores (dst VW-aligned).
+template <typename T, int N, int VW>
+__device__ __forceinline__ void store_vec(T *dst, const float *vals) {
+    constexpr int kPer = VW / (int)sizeof(T);   // elements per store
+    static_assert(N % kPer == 0, "run length is a multiple of the store width");
+    if constexpr (sizeof(T) == 4) {
+#pragma unroll
+        for (int i = 0; i < N; i += kPer) {
+            if constexpr (kPer == 4)
+                *reinterpret_cast<float4 *>(dst + i) =
+                    make_float4(vals[i], vals[i + 1], vals[i + 2], vals[i + 3]);
+            else if constexpr (kPer == 2)
+                *reinterpret_cast<float2 *>(dst + i) = make_float2(vals[i], vals[i + 1]);
+            else
+                dst[i] = vals[i];
+        }
+    } else {
+        if constexpr (kPer == 1) {
+#pragma unroll
+            for (int i = 0; i < N; ++i) dst[i] = __float2bfloat16_rn(vals[i]);
+        } else {
+            uint32_t u[N / 2];
+#pragma unroll
+            for (int i = 0; i < N; i += 2) {
+                __nv_bfloat162 h = __floats2bfloat162_rn(vals[i], vals[i + 1]);
+                u[i / 2] = *reinterpret_cast<uint32_t *>(&h);
+            }
+#pragma unroll
+            for (int i = 0; i < N / 2; i += kPer / 2) {
+                if constexpr (kPer == 8)
+                    *reinterpret_cast<uint4 *>(dst + 2 * i) =
+                        make_uint4(u[i], u[i + 1], u[i + 2], u[i + 3]);
+                else if constexpr (kPer == 4)
+                    *reinterpret_cast<uint2 *>(dst + 2 * i) = make_uint2(u[i], u[i + 1]);
+                else
+                    *reinterpret_cast<uint32_t *>(dst + 2 * i) = u[i];
+            }
+        }
+    }
+}
+
+// The whole-chunk output of emit_small: G = 32/S channels of SY runs of SX outputs each, the
+// runs of channel g at dst + g*cstride + jy*wout, stored VW bytes at a time.
+template <typename T, int SX, int SY, int VW, bool ACT>
+__device__ __forceinline__ void small_chunk_fast(float (&v)[32], T *__restrict__ dst, int64_t oc0,
+                                                 int64_t cstride, int64_t wout,
+                                                 const EpiParams &e) {
+    constexpr int S = SX * SY, G = 32 / S, GB = bias_block<T, G>();
+#pragma unroll
+    for (int g0 = 0; g0 < G; g0 += GB) {
+        float b[GB];
+        load_bias_vec<T, GB>(e, oc0 + g0, b);
+#pragma unroll
+        for (int g = 0; g < GB; ++g) {
+            add_bias_act<ACT, S>(&v[(g0 + g) * S], b[g], e.slope);
+#pragma unroll
+            for (int jy = 0; jy < SY; ++jy)
+                store_vec<T, SX, VW>(dst + (g0 + g) * cstride + jy * wout, &v[(g0 + g) * S + jy * SX]);
+        }
+    }
+}
+
+template <typename T, int SX, int SY, int VW>
+__device__ __forceinline__ void small_chunk_fast_act(float (&v)[32], T *__restrict__ dst,
+                                                     int64_t oc0, int64_t cstride, int64_t wout,
+                                                     const EpiParams &e) {
+    if (e.act == CTR_ACT_LEAKY_RELU)
+        small_chunk_fast<T, SX, SY, VW, true>(v, dst, oc0, cstride, wout, e);
+    else
+        small_chunk_fast<T, SX, SY, VW, false>(v, dst, oc0, cstride, wout, e);
+}
+
 // Output stage for whole phase sets: S = S_pad = SX * SY <= 32 (SX, SY compile-time), so the
 // 32 columns r0 .. r0+31 of a chunk are G = 32/S whole channels.  Warp-collective: every
 // lane passes the same r0 (its own position in ps).
 template <typename T, int SX, int SY>
-__device__ __forceinline__ void emit_small(const float (&v)[32], const PosInfo &ps, int64_t r0,
+__device__ __forceinline__ void emit_small(float (&v)[32], const PosInfo &ps, int64_t r0,
                                            const EpiParams &e, int lane) {
     constexpr int S = SX * SY;
     constexpr int G = 32 / S;
+    constexpr int kRunBytes = SX * (int)sizeof(T);
     const int64_t oc0 = r0 / S;
+    {
+        const int64_t fx0 = (int64_t)SX * ps.qx - e.px, fy0 = (int64_t)SY * ps.qy - e.py;
+        const bool inside = ps.valid && fx0 >= 0 && fx0 + SX <= e.Wout && fy0 >= 0 &&
+                            fy0 + SY <= e.Hout;
+        if (__all_sync(0xffffffffu, inside) && oc0 + G <= e.C_out) {
+            T *dst = static_cast<T *>(e.y) + ((ps.b * e.C_out + oc0) * e.Hout + fy0) * e.Wout + fx0;
+            const int64_t cs = e.Hout * e.Wout;
+            if constexpr (kRunBytes % 16 == 0) {
+                if (e.store_bytes == 16) {
+                    small_chunk_fast_act<T, SX, SY, 16>(v, dst, oc0, cs, e.Wout, e);
+                    return;
+                }
+            }
+            if constexpr (kRunBytes % 8 == 0) {
+                if (e.store_bytes == 8) {
+                    small_chunk_fast_act<T, SX, SY, 8>(v, dst, oc0, cs, e.Wout, e);
+                    return;
+                }
+            }
+            if constexpr (kRunBytes % 4 == 0 && sizeof(T) == 2) {
+                if (e.store_bytes == 4) {
+                    small_chunk_fast_act<T, SX, SY, 4>(v, dst, oc0, cs, e.Wout, e);
+                    return;
+                }
+            }
+            small_chunk_fast_act<T, SX, SY, (int)sizeof(T)>(v, dst, oc0, cs, e.Wout, e);
+            return;
+        }
+    }
     const float bl = lane_bias(e, oc0, G, lane);
     const float slope_eff = slope_of(e);
     const int64_t x0 = (int64_t)SX * ps.qx - e.px;
@@ -301,11 +470,40 @@ __device__ __forceinline__ void emit_small_chain(const float (&v)[32], const Pos
     }
 }
 
+// The whole-chunk output of emit_pm_chain: NJ = 32/TCR phases starting at phase (jy0, jx0),
+// each a run of TCR channel values at one position of the staged input.
+template <typename T, int TCR, bool ACT>
+__device__ __forceinline__ void pm_chain_fast(float (&v)[32], const PosInfo &ps, int jy0, int jx0,
+                                              int64_t oc0, const EpiParams &e) {
+    constexpr int NJ = 32 / TCR, GB = bias_block<T, TCR>();
+    T *__restrict__ ys = static_cast<T *>(e.y);
+    // Staged row of phase (jy, jx): ((ybase + jy) * ys_Px + xbase + jx).
+    const int64_t ybase = ps.b * e.ys_Py + (int64_t)e.sy * ps.qy - e.py + e.ys_hy;
+    const int64_t xbase = (int64_t)e.sx * ps.qx - e.px + e.ys_hx;
+#pragma unroll
+    for (int c0 = 0; c0 < TCR; c0 += GB) {
+        float b[GB];
+        load_bias_vec<T, GB>(e, oc0 + c0, b);
+        int jy = jy0, jx = jx0;
+#pragma unroll
+        for (int jj = 0; jj < NJ; ++jj) {
+#pragma unroll
+            for (int i = 0; i < GB; ++i) add_bias_act<ACT, 1>(&v[jj * TCR + c0 + i], b[i], e.slope);
+            const int64_t row = (ybase + jy) * e.ys_Px + xbase + jx;
+            store_channels<T, GB>(ys + row * e.ys_cpad + oc0 + c0, &v[jj * TCR + c0], e);
+            if (++jx == e.sx) {
+                jx = 0;
+                ++jy;
+            }
+        }
+    }
+}
+
 // Phase-major rows (EpiParams::pm_tc): the chunk's 32 columns are NJ = 32 / TCR phases of
 // TCR = min(pm_tc, 32) consecutive channels each, so every phase is one run of TCR channel
 // values at one output position.
 template <typename T, int TCR>
-__device__ __forceinline__ void emit_pm_chain(const float (&v)[32], const PosInfo &ps,
+__device__ __forceinline__ void emit_pm_chain(float (&v)[32], const PosInfo &ps,
                                               int64_t r0, const EpiParams &e, int lane) {
     constexpr int NJ = 32 / TCR;
     const int tc = e.pm_tc;
@@ -314,6 +512,33 @@ __device__ __forceinline__ void emit_pm_chain(const float (&v)[32], const PosInf
     const int rl0 = (int)(r0 - tile * bn);
     const int j0 = rl0 / tc;
     const int64_t oc0 = tile * tc + (rl0 - j0 * tc);
+    {
+        // Fast path: all TCR channels exist and every phase of the chunk lands inside the
+        // output for every lane.  The NJ phases are NJ runs of TCR channel values, stored per
+        // block of channels whose biases fill one vector load.
+        const int jy0 = j0 / e.sx, jx0 = j0 - jy0 * e.sx;
+        bool inside = ps.valid;
+        {
+            int jy = jy0, jx = jx0;
+#pragma unroll
+            for (int jj = 0; jj < NJ; ++jj) {
+                const int64_t oy = (int64_t)e.sy * ps.qy + jy - e.py;
+                const int64_t ox = (int64_t)e.sx * ps.qx + jx - e.px;
+                inside = inside && oy >= 0 && oy < e.Hout && ox >= 0 && ox < e.Wout;
+                if (++jx == e.sx) {
+                    jx = 0;
+                    ++jy;
+                }
+            }
+        }
+        if (__all_sync(0xffffffffu, inside) && oc0 + TCR <= e.C_out) {
+            if (e.act == CTR_ACT_LEAKY_RELU)
+                pm_chain_fast<T, TCR, true>(v, ps, jy0, jx0, oc0, e);
+            else
+                pm_chain_fast<T, TCR, false>(v, ps, jy0, jx0, oc0, e);
+            return;
+        }
+    }
     const float bl = lane_bias(e, oc0, TCR, lane);
     const float slope_eff = slope_of(e);
     const bool use_min = slope_eff > 1.0f;
@@ -374,74 +599,77 @@ __device__ __forceinline__ void emit_generic_chain(const float (&v)[32], const P
     }
 }
 
+// Which output stages a kernel compiles: the torch-layout output, the chained output into the
+// next plan's staged input (EpiParams::out_staged), or both; and for which I/O type.  A GEMM
+// instantiation takes one of each (its precision fixes the type), so it keeps its register
+// budget; the split-K reduce takes everything.
+enum : int { kOutPlain = 1, kOutChain = 2, kOutBoth = 3 };
+enum : int { kIoAny = 0, kIoF32 = 1, kIoBF16 = 2 };
+
 // Output stage for the accumulator columns r0 .. r0+31 (r0 a multiple of 32) of one phase
-// position per lane: v[i] = D[n, r0 + i].  Warp-collective: all 32 lanes of the warp call
-// it together with the same r0, each with its own position.  kChain compiles in the chained
-// output (EpiParams::out_staged); kernels without it keep their register budget.
-template <bool kChain>
-__device__ __forceinline__ void emit_cols(const float (&v)[32], const PosInfo &ps, int64_t r0,
+// position per lane: v[i] = D[n, r0 + i] (overwritten).  Warp-collective: all 32 lanes of the
+// warp call it together with the same r0, each with its own position.
+template <int kOut, int kIo>
+__device__ __forceinline__ void emit_cols(float (&v)[32], const PosInfo &ps, int64_t r0,
                                           const EpiParams &e, int lane) {
-    if (kChain && e.out_staged && e.pm_tc) {
-#define CTR_PM(TCR)                                                        \
-    if (e.out_bf16)                                                        \
-        emit_pm_chain<__nv_bfloat16, TCR>(v, ps, r0, e, lane);             \
-    else                                                                   \
-        emit_pm_chain<float, TCR>(v, ps, r0, e, lane);                     \
-    return
-        switch (e.pm_tc >= 32 ? 32 : e.pm_tc) {
-            case 2: CTR_PM(2);
-            case 4: CTR_PM(4);
-            case 8: CTR_PM(8);
-            case 16: CTR_PM(16);
-            default: CTR_PM(32);
+// CTR_IO(FN, (T, args...), (args...)): call FN<T, args...> for the kernel's I/O type(s).
+#define CTR_IO_CALL(FN, TARGS) FN<CTR_IO_EXPAND TARGS>(v, ps, r0, e, lane)
+#define CTR_IO_EXPAND(...) __VA_ARGS__
+#define CTR_IO(FN, BF_ARGS, F_ARGS)                                        \
+    do {                                                                   \
+        if constexpr (kIo == kIoBF16) {                                    \
+            CTR_IO_CALL(FN, BF_ARGS);                                      \
+        } else if constexpr (kIo == kIoF32) {                              \
+            CTR_IO_CALL(FN, F_ARGS);                                       \
+        } else if (e.out_bf16) {                                           \
+            CTR_IO_CALL(FN, BF_ARGS);                                      \
+        } else {                                                           \
+            CTR_IO_CALL(FN, F_ARGS);                                       \
+        }                                                                  \
+        return;                                                            \
+    } while (0)
+    if constexpr ((kOut & kOutChain) != 0) {
+        if (kOut == kOutChain || e.out_staged) {
+            if (e.pm_tc) {
+                switch (e.pm_tc >= 32 ? 32 : e.pm_tc) {
+                    case 2: CTR_IO(emit_pm_chain, (__nv_bfloat16, 2), (float, 2));
+                    case 4: CTR_IO(emit_pm_chain, (__nv_bfloat16, 4), (float, 4));
+                    case 8: CTR_IO(emit_pm_chain, (__nv_bfloat16, 8), (float, 8));
+                    case 16: CTR_IO(emit_pm_chain, (__nv_bfloat16, 16), (float, 16));
+                    default: CTR_IO(emit_pm_chain, (__nv_bfloat16, 32), (float, 32));
+                }
+            }
+            switch (e.kind) {
+                case EPI_KIND_1D_S1: CTR_IO(emit_small_chain, (__nv_bfloat16, 1, 1), (float, 1, 1));
+                case EPI_KIND_1D_S2: CTR_IO(emit_small_chain, (__nv_bfloat16, 2, 1), (float, 2, 1));
+                case EPI_KIND_1D_S4: CTR_IO(emit_small_chain, (__nv_bfloat16, 4, 1), (float, 4, 1));
+                case EPI_KIND_1D_S8: CTR_IO(emit_small_chain, (__nv_bfloat16, 8, 1), (float, 8, 1));
+                case EPI_KIND_2D_S2x2: CTR_IO(emit_small_chain, (__nv_bfloat16, 2, 2), (float, 2, 2));
+                default:
+                    emit_generic_chain(v, ps, r0, e);
+                    return;
+            }
         }
-#undef CTR_PM
     }
-    if (kChain && e.out_staged) {
-#define CTR_CHAIN(SX, SY)                                                  \
-    if (e.out_bf16)                                                        \
-        emit_small_chain<__nv_bfloat16, SX, SY>(v, ps, r0, e, lane);       \
-    else                                                                   \
-        emit_small_chain<float, SX, SY>(v, ps, r0, e, lane);               \
-    return
+    if constexpr ((kOut & kOutPlain) != 0) {
         switch (e.kind) {
-            case EPI_KIND_1D_S1: CTR_CHAIN(1, 1);
-            case EPI_KIND_1D_S2: CTR_CHAIN(2, 1);
-            case EPI_KIND_1D_S4: CTR_CHAIN(4, 1);
-            case EPI_KIND_1D_S8: CTR_CHAIN(8, 1);
-            case EPI_KIND_2D_S2x2: CTR_CHAIN(2, 2);
+            case EPI_KIND_1D_S1: CTR_IO(emit_small, (__nv_bfloat16, 1, 1), (float, 1, 1));
+            case EPI_KIND_1D_S2: CTR_IO(emit_small, (__nv_bfloat16, 2, 1), (float, 2, 1));
+            case EPI_KIND_1D_S4: CTR_IO(emit_small, (__nv_bfloat16, 4, 1), (float, 4, 1));
+            case EPI_KIND_1D_S8: CTR_IO(emit_small, (__nv_bfloat16, 8, 1), (float, 8, 1));
+            case EPI_KIND_1D_S16: CTR_IO(emit_small, (__nv_bfloat16, 16, 1), (float, 16, 1));
+            case EPI_KIND_1D_S32: CTR_IO(emit_small, (__nv_bfloat16, 32, 1), (float, 32, 1));
+            case EPI_KIND_2D_S2x2: CTR_IO(emit_small, (__nv_bfloat16, 2, 2), (float, 2, 2));
+            case EPI_KIND_2D_S4x4: CTR_IO(emit_small, (__nv_bfloat16, 4, 4), (float, 4, 4));
+            case EPI_KIND_1D_LARGE: CTR_IO(emit_large, (__nv_bfloat16), (float));
             default:
-                emit_generic_chain(v, ps, r0, e);
+                emit_generic(v, ps, r0, e);
                 return;
         }
-#undef CTR_CHAIN
     }
-#define CTR_SMALL(SX, SY)                                                  \
-    if (e.out_bf16)                                                        \
-        emit_small<__nv_bfloat16, SX, SY>(v, ps, r0, e, lane);             \
-    else                                                                   \
-        emit_small<float, SX, SY>(v, ps, r0, e, lane);                     \
-    return
-    switch (e.kind) {
-        case EPI_KIND_1D_S1: CTR_SMALL(1, 1);
-        case EPI_KIND_1D_S2: CTR_SMALL(2, 1);
-        case EPI_KIND_1D_S4: CTR_SMALL(4, 1);
-        case EPI_KIND_1D_S8: CTR_SMALL(8, 1);
-        case EPI_KIND_1D_S16: CTR_SMALL(16, 1);
-        case EPI_KIND_1D_S32: CTR_SMALL(32, 1);
-        case EPI_KIND_2D_S2x2: CTR_SMALL(2, 2);
-        case EPI_KIND_2D_S4x4: CTR_SMALL(4, 4);
-        case EPI_KIND_1D_LARGE:
-            if (e.out_bf16)
-                emit_large<__nv_bfloat16>(v, ps, r0, e, lane);
-            else
-                emit_large<float>(v, ps, r0, e, lane);
-            return;
-        default:
-            emit_generic(v, ps, r0, e);
-            return;
-    }
-#undef CTR_SMALL
+#undef CTR_IO
+#undef CTR_IO_CALL
+#undef CTR_IO_EXPAND
 }
 
 }  // namespace ctr

@@ -128,6 +128,27 @@ __device__ __forceinline__ void give_up(volatile int *abort, uint32_t *status, u
     atomicOr(status, bit);
 }
 
+// Output of one 32-column chunk (columns tc.r0 + 32c ..) of this thread's position: the fused
+// polyphase output stage, or the raw fp32 values (split-K partials, col2im columns).  A
+// function of its own, force-inlined, so that v stays in registers.
+template <Prec P, bool CHAIN>
+__device__ __forceinline__ void store_chunk_out(const GemmParams &gp, const TileCoord &tc,
+                                                const PosInfo &ps, bool fused, int quad, int lane,
+                                                int c, float (&v)[32]) {
+    const int64_t r0 = tc.r0 + 32 * c;
+    if (fused) {
+        emit_cols<CHAIN ? kOutChain : kOutPlain, P == Prec::BF16 ? kIoBF16 : kIoF32>(
+            v, ps, r0, gp.epi, lane);
+        return;
+    }
+    const int64_t pos = (int64_t)tc.p0 + 32 * quad + lane;
+    float4 *dst = reinterpret_cast<float4 *>(gp.raw + (int64_t)tc.z * gp.raw_split_stride +
+                                             pos * gp.raw_ld + r0);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+}
+
 template <Prec P, int BN, bool CHAIN>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapW,
@@ -218,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
                     ptx::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
                     const int32_t x_k = kc * C::kElems;
                     const int32_t w_k = kb * C::kElems;
-                    const int32_t x_row = (int32_t)(tc.p0 + (int64_t)uy * gp.Px + ux);
+                    const int32_t x_row = (int32_t)(tc.p0 + gp.shift0 + (int64_t)uy * gp.Px + ux);
                     const int32_t w_row = (int32_t)tc.r0;
                     ptx::tma_load_2d(x_slice(stage, 0), &mapX, &full[stage], x_k, x_row);
                     ptx::tma_load_2d(w_slice(stage, 0), &mapW, &full[stage], w_k, w_row);
@@ -354,20 +375,6 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&tmem_empty[g % C::kAccBufs]);
         };
-        // Output of one 32-column chunk of this thread's position.
-        auto store_chunk = [&](const TileCoord &tc, const PosInfo &ps, int c, const float (&v)[32]) {
-            const int64_t r0 = tc.r0 + 32 * c;
-            if (fused) {
-                emit_cols<CHAIN>(v, ps, r0, gp.epi, lane);
-                return;
-            }
-            const int64_t pos = (int64_t)tc.p0 + 32 * quad + lane;
-            float4 *dst = reinterpret_cast<float4 *>(gp.raw + (int64_t)tc.z * gp.raw_split_stride +
-                                                     pos * gp.raw_ld + r0);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-        };
         auto tmem_chunk = [&](int g, int c, uint32_t (&u)[32]) {
             ptx::tmem_ld_32x32b_x32(
                 tmem_base + lane_addr + (uint32_t)((g % C::kAccBufs) * BN + 32 * c), u);
@@ -425,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
                     float v[32];
 #pragma unroll
                     for (int cc = 0; cc < 32; ++cc) v[cc] = __uint_as_float(u[cc]);
-                    store_chunk(tc, ps, c_base + c, v);
+                    store_chunk_out<P, CHAIN>(gp, tc, ps, fused, quad, lane, c_base + c, v);
                 }
                 if constexpr (C::kSumFirst) {   // the sum region may take the next tile
                     ptx::tc_fence_before();
@@ -439,12 +446,12 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
                 for (int c = 0; c < kChunks; ++c) {
                     uint32_t u[32];
                     tmem_chunk(grp, c_base + c, u);
-                    ptx::tmem_wait_ld();
+                    ptx::tmem_wait_ld_regs(u);
                     if (c == kChunks - 1) release_group(grp);  // TMEM no longer needed
                     float v[32];
 #pragma unroll
                     for (int cc = 0; cc < 32; ++cc) v[cc] = __uint_as_float(u[cc]);
-                    store_chunk(tc, ps, c_base + c, v);
+                    store_chunk_out<P, CHAIN>(gp, tc, ps, fused, quad, lane, c_base + c, v);
                 }
                 ++grp;
             } else if constexpr (P == Prec::TF32x3 && !C::kTmemSum) {
@@ -470,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
                 if (!ok) break;
                 // Unrolled (kChunks <= 2 here), so each chunk's sums die once stored.
 #pragma unroll
-                for (int c = 0; c < kChunks; ++c) store_chunk(tc, ps, c_base + c, sum[c]);
+                for (int c = 0; c < kChunks; ++c) store_chunk_out<P, CHAIN>(gp, tc, ps, fused, quad, lane, c_base + c, sum[c]);
             }
         }
     }
