@@ -38,6 +38,7 @@
  *         w    [C_in][C_out/G][k]         or [C_in][C_out/G][kH][kW]   (G groups, default 1)
  *         bias [C_out]                    (may be NULL)
  *         y    [N][C_out][L_out]          or [N][C_out][H_out][W_out]
+ *     (x and y channels last with ctr_plan_set_layout(plan, CTR_LAYOUT_NHWC))
  *     and each must start on a 16-byte boundary (CTR_ERR_MISALIGNED otherwise).
  *   - A plan is not thread-safe: calls on one plan must not overlap on the host.  Two
  *     ctr_forward calls on one plan that run concurrently on the GPU (different streams)
@@ -68,7 +69,12 @@ typedef enum {
 
 typedef enum {
     CTR_F32 = 0,   /* fp32 I/O; tensor-core products as 3xTF32 (hi/lo split), fp32 accumulate */
-    CTR_BF16 = 1   /* bf16 I/O; bf16 tensor-core products, fp32 accumulate, one final rounding */
+    CTR_BF16 = 1,  /* bf16 I/O; bf16 tensor-core products, fp32 accumulate, one final rounding */
+    CTR_F16 = 2    /* fp16 I/O; fp16 tensor-core products, fp32 accumulate and intermediates,
+                      one final rounding ("[WebGPU] optimizations for audio models", review
+                      commits: for float16 the packed weight and the K-padded input stay in the
+                      I/O type while sums and column buffers are f32).  Not on the depthwise
+                      kernel (grouped fp16 plans run the gather kernel) nor the iSTFT plan. */
 } ctr_dtype;
 
 typedef enum {
@@ -96,7 +102,7 @@ typedef enum {
  *   stride         ndim strides >= 1
  *   padding        ndim paddings >= 0 (front and back; ctr_plan_set_pads separates them)
  *   output_padding ndim values with 0 <= op < stride (may be NULL = zeros)
- *   dtype          ctr_dtype
+ *   dtype          ctr_dtype (CTR_F32, CTR_BF16 or CTR_F16)
  * Every output size must be >= 1.  Groups, dilation and separate front/back pads are set
  * afterwards (ctr_plan_set_groups, ctr_plan_set_dilation, ctr_plan_set_pads; defaults: one
  * group, dilation 1, the back pad equal to `padding`).  Returns CTR_ERR_INVALID_ARG on any
@@ -154,6 +160,26 @@ ctr_status ctr_plan_set_dilation(ctr_plan_t plan, const int64_t *dilation);
  * a chained plan (the plan is then unchanged).
  */
 ctr_status ctr_plan_set_pads(ctr_plan_t plan, const int64_t *pads_begin, const int64_t *pads_end);
+
+typedef enum {
+    CTR_LAYOUT_NCHW = 0,   /* x [N][C_in][spatial...], y [N][C_out][out spatial...] (default) */
+    CTR_LAYOUT_NHWC = 1    /* channels last: x [N][spatial...][C_in], y [N][out spatial...][C_out] */
+} ctr_layout;
+
+/*
+ * Memory layout of x and y (default CTR_LAYOUT_NCHW); the weight keeps its torch layout.
+ * Channels-last tensors are what image and audio pipelines often hold ("[XNNPACK] Lower dense
+ * transposed convs as one polyphase conv + depth to space": the inpainting network's profile
+ * spends a quarter of its time in NCHW <-> NHWC transposes around the deconvolutions).  The
+ * tensor-core paths stage an NHWC input with a row copy (their staged operand is channels-last
+ * already) and write an NHWC output from the same output stage that feeds a chained plan; the
+ * gather kernel indexes NHWC directly.  The depthwise kernel is NCHW only (a grouped NHWC plan
+ * runs the gather kernel) and so are streaming plans.  Host only, with the same ordering rule
+ * as ctr_plan_set_path; CTR_ERR_INVALID_ARG for another value or after ctr_prepack_weight;
+ * CTR_ERR_UNSUPPORTED on a streaming plan or one forced onto the depthwise path (the plan is
+ * then unchanged).
+ */
+ctr_status ctr_plan_set_layout(ctr_plan_t plan, int layout);
 
 typedef enum {
     CTR_AUTO_PAD_NOTSET = 0,      /* explicit pads (ctr_plan_create / ctr_plan_set_pads) */

@@ -10,7 +10,7 @@ bias, following the gather condition and the un-flipped weight layout of "[Execu
 Add optimized conv2d op" (Implementation) and the bias-first accumulation of "[WebGPU]
 optimizations for audio models" (ConvTranspose commits).  This module only marshals numpy
 arrays into that library and adds the element-wise helpers the tests need (rounding to the
-I/O precision, LeakyReLU, the rel_l2 metric).
+I/O precision (fp32, bf16, fp16), LeakyReLU, the rel_l2 metric).
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against something other than
 itself: torch's float64 CPU ConvTranspose, the adjoint of a forward convolution built
@@ -207,6 +207,27 @@ def round_bf16(a) -> np.ndarray:
         e = np.maximum(e, -125)
         q = np.ldexp(np.rint(np.ldexp(x, 8 - e)), e - 8)
         q = np.where(np.abs(q) > _BF16_MAX, np.copysign(np.inf, x), q)
+    return np.where(np.isfinite(x), q, x)
+
+
+_F16_MAX = 65504.0
+
+
+def round_f16(a) -> np.ndarray:
+    """Round a double straight to the nearest IEEE binary16 value (ties to even); returned as
+    float64.
+
+    binary16 keeps 11 significant bits and exponents -14 .. 15: for |x| in [2**(e-1), 2**e)
+    the spacing is 2**(e-11); below the smallest normal (2**-14) it stays 2**-24.  Values
+    past the largest finite value (65504) after rounding become +-inf; NaN and inf pass
+    through.
+    """
+    x = np.asarray(a, dtype=np.float64)
+    with np.errstate(over="ignore", invalid="ignore"):
+        _, e = np.frexp(x)
+        e = np.maximum(e, -13)
+        q = np.ldexp(np.rint(np.ldexp(x, 11 - e)), e - 11)
+        q = np.where(np.abs(q) > _F16_MAX, np.copysign(np.inf, x), q)
     return np.where(np.isfinite(x), q, x)
 
 

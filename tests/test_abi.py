@@ -392,6 +392,36 @@ def test_streaming_plan_without_gpu(ctr):
         ctr.ctr_plan_destroy(b)
 
 
+def test_f16_plans_without_gpu(ctr):
+    """CTR_F16 plans: the tensor-core paths pack one 16-bit plane like bf16; grouped fp16
+    plans run the gather kernel (no depthwise kernel for fp16); the iSTFT plan refuses fp16;
+    an unknown dtype code is invalid."""
+    f16, bf = ctr.CTR_F16, ctr.CTR_BF16
+    a = _plan(ctr, 1, 1, 512, 256, [2000], [16], [8], [4], [0], f16)
+    b = _plan(ctr, 1, 1, 512, 256, [2000], [16], [8], [4], [0], bf)
+    try:
+        assert ctr.ctr_plan_get_path(a) == ctr.CTR_PATH_POLYPHASE
+        assert "prec=f16" in ctr.ctr_plan_describe(a)
+        assert ctr.ctr_packed_weight_bytes(a) == ctr.ctr_packed_weight_bytes(b)
+        assert ctr.ctr_workspace_bytes(a) == ctr.ctr_workspace_bytes(b)
+    finally:
+        ctr.ctr_plan_destroy(a)
+        ctr.ctr_plan_destroy(b)
+    h = _plan(ctr, 2, 1, 16, 16, [9, 12], [4, 4], [2, 2], [1, 1], [0, 0], f16)
+    try:
+        ctr.ctr_plan_set_groups(h, 16)
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_GATHER
+        assert ctr.lib.ctr_plan_set_path(h, ctr.CTR_PATH_DEPTHWISE, 0) == ctr.CTR_ERR_UNSUPPORTED
+    finally:
+        ctr.ctr_plan_destroy(h)
+    ist = ctypes.c_void_p()
+    assert ctr.lib.ctr_istft_create(ctypes.byref(ist), 1, 64, 16, 9, 0, 0, f16) == ctr.CTR_ERR_UNSUPPORTED
+    out = ctypes.c_void_p()
+    args = [ctypes.byref(out), 1, 1, 16, 8, ctr._arr([64]), ctr._arr([4]), ctr._arr([2]),
+            ctr._arr([1]), None, 3]
+    assert ctr.lib.ctr_plan_create(*args) == ctr.CTR_ERR_INVALID_ARG
+
+
 def test_auto_pad_without_gpu(ctr):
     """ONNX auto_pad / output_shape resolve into front and back pads: SAME_* give
     L_in * stride outputs with an odd total padding's extra sample at the end (UPPER) or in

@@ -229,3 +229,34 @@ def test_planted_mistake_fails_a_pin(mutant):
         assert failed, "planted mistake %s passed every pin" % mutant
     finally:
         shutil.rmtree(tmp)
+
+
+def test_round_f16_hand_cases():
+    """Round-to-nearest-even into binary16 at the places a plausible mistake shows: ties at
+    1 (even mantissa stays, odd rounds up), the overflow threshold (65520 is the tie between
+    65504 and 2**16, whose mantissa is even, so it overflows to inf), the subnormal spacing
+    2**-24 and its ties, signs, and values that pass through."""
+    cases = [
+        (1.0 + 2.0 ** -11, 1.0),                      # tie, 1.0 has an even mantissa
+        (1.0 + 3 * 2.0 ** -11, 1.0 + 2.0 ** -9),      # tie, 1 + 2**-10 is odd: round up
+        (1.0 + 2.0 ** -11 + 2.0 ** -40, 1.0 + 2.0 ** -10),   # just above the tie
+        (2048.0 + 1.0, 2048.0), (2048.0 + 3.0, 2052.0),      # spacing 2 above 2048
+        (65504.0, 65504.0), (65519.99, 65504.0), (65520.0, np.inf), (-65520.0, -np.inf),
+        (2.0 ** -24, 2.0 ** -24), (2.0 ** -25, 0.0), (3 * 2.0 ** -25, 2.0 ** -23),
+        (2.0 ** -14 - 2.0 ** -25, 2.0 ** -14),              # top subnormal tie rounds to normal
+        (-0.1, -0.0999755859375), (np.inf, np.inf), (-3.0, -3.0),
+    ]
+    for x, want in cases:
+        got = float(oracle.round_f16(x))
+        assert got == want, (x, got, want)
+    assert np.isnan(oracle.round_f16(np.nan))
+
+
+def test_round_f16_matches_numpy_conversion():
+    """numpy's float64 -> float16 conversion is an independent, correctly rounded
+    implementation; the two agree on doubles over the whole binary16 range."""
+    rng = np.random.default_rng(23)
+    x = rng.standard_normal(200000) * np.exp2(rng.integers(-30, 17, 200000).astype(np.float64))
+    got = oracle.round_f16(x)
+    ref = x.astype(np.float16).astype(np.float64)
+    np.testing.assert_array_equal(got, ref)

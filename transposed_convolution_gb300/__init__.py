@@ -7,7 +7,7 @@ any non-OK status from the library raises ``CtrError``.
 
 Low level (same names as the C ABI): ``ctr_plan_create``, ``ctr_plan_set_activation``,
 ``ctr_plan_set_path``, ``ctr_plan_set_groups``, ``ctr_plan_set_dilation``, ``ctr_plan_set_pads``,
-``ctr_plan_set_auto_pad``, ``ctr_plan_set_streaming``, ``ctr_plan_stream_reset``,
+``ctr_plan_set_auto_pad``, ``ctr_plan_set_layout``, ``ctr_plan_set_streaming``, ``ctr_plan_stream_reset``,
 ``ctr_plan_set_tile``, ``ctr_plan_set_phase_origin``, ``ctr_plan_chain``, ``ctr_plan_get_path``, ``ctr_plan_output_shape``,
 ``ctr_packed_weight_bytes``, ``ctr_workspace_bytes``, ``ctr_plan_bind_workspace``,
 ``ctr_prepack_weight``, ``ctr_forward``, ``ctr_forward_noalloc``, ``ctr_plan_check``,
@@ -42,6 +42,7 @@ CTR_ERR_NOT_PREPARED = 7
 
 CTR_F32 = 0
 CTR_BF16 = 1
+CTR_F16 = 2
 CTR_ACT_NONE = 0
 CTR_ACT_LEAKY_RELU = 1
 CTR_PATH_AUTO = 0
@@ -49,6 +50,8 @@ CTR_PATH_POLYPHASE = 1
 CTR_PATH_COL2IM = 2
 CTR_PATH_GATHER = 3
 CTR_PATH_DEPTHWISE = 4
+CTR_LAYOUT_NCHW = 0
+CTR_LAYOUT_NHWC = 1
 CTR_AUTO_PAD_NOTSET = 0
 CTR_AUTO_PAD_SAME_UPPER = 1
 CTR_AUTO_PAD_SAME_LOWER = 2
@@ -72,6 +75,7 @@ SIGNATURES = {
     "ctr_plan_set_dilation": (ctypes.c_int, [_vp, _i64p]),
     "ctr_plan_set_pads": (ctypes.c_int, [_vp, _i64p, _i64p]),
     "ctr_plan_set_auto_pad": (ctypes.c_int, [_vp, ctypes.c_int, _i64p]),
+    "ctr_plan_set_layout": (ctypes.c_int, [_vp, ctypes.c_int]),
     "ctr_plan_set_streaming": (ctypes.c_int, [_vp, ctypes.c_int]),
     "ctr_plan_stream_reset": (ctypes.c_int, [_vp, _vp]),
     "ctr_plan_set_tile": (ctypes.c_int, [_vp, ctypes.c_int]),
@@ -195,6 +199,10 @@ def ctr_plan_set_dilation(plan, dilation):
 
 def ctr_plan_set_pads(plan, pads_begin, pads_end):
     _check(lib.ctr_plan_set_pads(plan, _arr(pads_begin), _arr(pads_end)), "ctr_plan_set_pads")
+
+
+def ctr_plan_set_layout(plan, layout):
+    _check(lib.ctr_plan_set_layout(plan, layout), "ctr_plan_set_layout")
 
 
 def ctr_plan_set_auto_pad(plan, auto_pad, output_shape=None):
@@ -340,7 +348,10 @@ def _dtype_code(dt):
         return CTR_F32
     if dt == torch.bfloat16:
         return CTR_BF16
-    raise TypeError("transposed_convolution_gb300 supports float32 and bfloat16, got %s" % dt)
+    if dt == torch.float16:
+        return CTR_F16
+    raise TypeError("transposed_convolution_gb300 supports float32, bfloat16 and float16, got %s"
+                    % dt)
 
 
 def _stream_ptr(stream):
@@ -369,7 +380,7 @@ class Plan:
                  output_padding=0, dtype=None, negative_slope=None, path=CTR_PATH_AUTO,
                  split_k=0, device=None, block_n=0, groups=1, dilation=1, padding_end=None,
                  streaming=False, phase_origin=CTR_PHASE_AUTO, auto_pad=CTR_AUTO_PAD_NOTSET,
-                 output_shape=None):
+                 output_shape=None, layout="nchw"):
         torch = _torch()
         self.ndim = len(in_spatial)
         self.dtype = dtype if dtype is not None else torch.float32
@@ -383,10 +394,15 @@ class Plan:
         self.groups = int(groups)
         self.dilation = _tuple(dilation, self.ndim)
         self.padding_end = self.padding if padding_end is None else _tuple(padding_end, self.ndim)
+        if layout not in ("nchw", "nhwc"):
+            raise ValueError("layout must be 'nchw' or 'nhwc'")
+        self.nhwc = layout == "nhwc"
         self.handle = ctr_plan_create(self.ndim, self.N, self.C_in, self.C_out, self.in_spatial,
                                       self.kernel, self.stride, self.padding,
                                       self.output_padding, _dtype_code(self.dtype))
         try:
+            if self.nhwc:
+                ctr_plan_set_layout(self.handle, CTR_LAYOUT_NHWC)
             if negative_slope is not None:
                 ctr_plan_set_activation(self.handle, CTR_ACT_LEAKY_RELU, negative_slope)
             if self.groups != 1:
@@ -426,7 +442,15 @@ class Plan:
         self.prev_plan = None
 
     @property
+    def in_shape(self):
+        if self.nhwc:
+            return (self.N,) + self.in_spatial + (self.C_in,)
+        return (self.N, self.C_in) + self.in_spatial
+
+    @property
     def out_shape(self):
+        if self.nhwc:
+            return (self.N,) + tuple(self.out_spatial) + (self.C_out,)
         return (self.N, self.C_out) + tuple(self.out_spatial)
 
     def describe(self) -> str:
@@ -457,7 +481,7 @@ class Plan:
         if self.w_packed is None:
             raise RuntimeError("Plan.forward before Plan.prepack")
         if x is not None or self.prev_plan is None:
-            x = self._checked(x, (self.N, self.C_in) + self.in_spatial, "x")
+            x = self._checked(x, self.in_shape, "x")
         if bias is not None:
             bias = self._checked(bias, (self.C_out,), "bias")
         if self.next_plan is not None:

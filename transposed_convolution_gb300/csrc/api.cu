@@ -52,13 +52,16 @@ int query_num_sms() {
     return n > 0 ? n : 152;
 }
 
-Prec prec_of(const ctr_plan_s *pl) { return pl->dtype == CTR_BF16 ? Prec::BF16 : Prec::TF32x3; }
-int esize_io(const ctr_plan_s *pl) { return pl->dtype == CTR_BF16 ? 2 : 4; }
+Prec prec_of(const ctr_plan_s *pl) {
+    return pl->dtype == CTR_BF16 ? Prec::BF16 : pl->dtype == CTR_F16 ? Prec::F16 : Prec::TF32x3;
+}
+bool io16(const ctr_plan_s *pl) { return pl->dtype != CTR_F32; }
+int esize_io(const ctr_plan_s *pl) { return io16(pl) ? 2 : 4; }
 // Elements of one 128-byte K slice in the GEMM operands.
-int bk_elems(const ctr_plan_s *pl) { return pl->dtype == CTR_BF16 ? 64 : 32; }
+int bk_elems(const ctr_plan_s *pl) { return io16(pl) ? 64 : 32; }
 // Bytes per element of one GEMM operand plane, and number of planes (hi/lo for 3xTF32).
-int op_esize(const ctr_plan_s *pl) { return pl->dtype == CTR_BF16 ? 2 : 4; }
-int op_planes(const ctr_plan_s *pl) { return pl->dtype == CTR_BF16 ? 1 : 2; }
+int op_esize(const ctr_plan_s *pl) { return io16(pl) ? 2 : 4; }
+int op_planes(const ctr_plan_s *pl) { return io16(pl) ? 1 : 2; }
 
 bool is_tc_path(int path) { return path == CTR_PATH_POLYPHASE || path == CTR_PATH_COL2IM; }
 
@@ -236,6 +239,10 @@ int choose_phase_origin(ctr_plan_s *pl) {
     return t_out < t_pad ? 1 : 0;
 }
 
+// A channels-last y whose rows of C_out channels are whole 16-byte vectors: the vectorised
+// channels-last output stages apply; otherwise the element-wise one does.
+bool nhwc_out_vector(const ctr_plan_s *pl) { return (pl->C_out * esize_io(pl)) % 16 == 0; }
+
 // Derive the GEMM geometry, tiling, packed size and workspace layout from the path.
 void layout_plan(ctr_plan_s *pl) {
     pl->packed_bytes = 0;
@@ -279,8 +286,11 @@ void layout_plan(ctr_plan_s *pl) {
     // A chained producer packs its rows phase-major within each tile, so that the output
     // stage's 32-row chunks are runs of consecutive channels (contiguous in the next
     // plan's channels-last staged input).  Needs whole phase sets that divide the tile.
-    pl->row_pm = pl->chain_next && pl->path == CTR_PATH_POLYPHASE && pl->S == pl->S_pad &&
-                 pl->S_pad <= 32 && pl->block_n % pl->S_pad == 0 && pl->block_n / pl->S_pad >= 2;
+    // A channels-last y is written by the same output stage, when its rows of C_out channels
+    // keep the 16-byte vector stores aligned.
+    pl->row_pm = (pl->chain_next || (pl->nhwc && nhwc_out_vector(pl))) &&
+                 pl->path == CTR_PATH_POLYPHASE && pl->S == pl->S_pad && pl->S_pad <= 32 &&
+                 pl->block_n % pl->S_pad == 0 && pl->block_n / pl->S_pad >= 2;
     if (pl->row_pm) pl->M_pad = (int64_t)pl->num_r_tiles * pl->block_n;
     pl->packed_bytes = (size_t)pl->M_pad * pl->K_total * op_esize(pl) * op_planes(pl);
     pl->ws_off_stage = 0;
@@ -362,17 +372,19 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 
 // 2-D tiled tensor map over a row-major [rows][inner] matrix, box [box_rows][128 bytes],
 // 128-byte swizzle (the K-major SWIZZLE_128B operand layout of tcgen05.mma), zero fill.
-bool encode_2d(CUtensorMap *map, const void *base, bool bf16, uint64_t inner, uint64_t rows,
+bool encode_2d(CUtensorMap *map, const void *base, int io, uint64_t inner, uint64_t rows,
                uint32_t box_rows, int box_bytes) {
     auto fn = get_encode_fn();
     if (!fn || (box_bytes != 128 && box_bytes != 64)) return false;
-    const uint32_t es = bf16 ? 2 : 4;
+    const uint32_t es = io == IO_F32 ? 4 : 2;
+    const CUtensorMapDataType dt = io == IO_BF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                   : io == IO_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     cuuint64_t dims[2] = {inner, rows};
     cuuint64_t strides[1] = {inner * es};
     cuuint32_t box[2] = {(cuuint32_t)(box_bytes / es), box_rows};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                    2, const_cast<void *>(base), dims, strides, box, estr,
+    CUresult r = fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE,
                     box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -397,7 +409,7 @@ EpiParams make_epi(const ctr_plan_s *pl, const void *bias, void *y) {
     e.Wout = pl->out[1];
     e.bias = bias;
     e.y = y;
-    e.out_bf16 = pl->dtype == CTR_BF16 ? 1 : 0;
+    e.io = pl->dtype;   // the ctr_dtype codes are the IoType codes
     e.act = pl->act;
     e.slope = pl->slope;
     // Output-stage variant: whole phase sets per 32-column chunk when S = S_pad is a power
@@ -425,12 +437,14 @@ EpiParams make_epi(const ctr_plan_s *pl, const void *bias, void *y) {
         e.kind = sx == 2 ? EPI_KIND_2D_S2x2 : EPI_KIND_2D_S4x4;
         nx = (int)sx;
     }
+    if (pl->nhwc && !nhwc_out_vector(pl)) e.kind = EPI_KIND_GENERIC;
     // Widest aligned store of an interior run: the run length, the run-to-run step of one
     // position (sx elements), the padding offset and the output row pitch must all be
     // multiples of it, so every thread and row share the same alignment.
-    const int es = pl->dtype == CTR_BF16 ? 2 : 4;
+    const int es = esize_io(pl);
     e.out_staged = 0;
     e.ys_Px = e.ys_Py = e.ys_hx = e.ys_hy = e.ys_cpad = e.ys_lo = 0;
+    e.ys_tf32 = 0;
     e.pm_tc = pl->row_pm ? pl->block_n / pl->S_pad : 0;
     e.store_bytes = es;
     for (int w : {16, 8, 4}) {
@@ -465,6 +479,58 @@ cudaError_t record_timing(cudaEvent_t ev, cudaStream_t st) {
                : cudaEventRecord(ev, st);
 }
 
+// The GEMM's shared-memory pipeline for a plan: the instantiation's default stage ring, or
+// the shared-X mode for 16-bit 1-D polyphase plans with several taps.  In that mode a stage
+// holds one X box of 128 + (taps - 1) staged rows (rounded up to 8) per channel slice,
+// which every tap reads through a shifted descriptor, instead of one 128-row box per tap;
+// the whole weight tile stays resident when the plan has one row tile and it fits beside
+// two X boxes.  It is taken when it keeps more tiles in flight than the default ring: the
+// small-K layers whose loads, not their MMAs, set the pace.
+void set_pipeline_layout(const ctr_plan_s *pl, GemmParams *gp) {
+    const Prec prec = prec_of(pl);
+    const GemmLayout lay = gemm_layout(prec, pl->block_n);
+    gp->xshare = 0;
+    gp->wres = 0;
+    gp->x_rows = kBM;
+    gp->nstages = lay.stages;
+    gp->stage_bytes = lay.stage_bytes;
+    gp->wres_off = 0;
+    gp->bar_off = lay.stages * lay.stage_bytes;
+    gp->smem_bytes = 1024 + gp->bar_off + kGemmBarBytes;
+    if (!is_16bit(prec) || pl->path != CTR_PATH_POLYPHASE || pl->splits != 1 ||
+        pl->m[0] != 1 || pl->m[1] < 2)
+        return;
+    const int x_rows = (int)((kBM + pl->m[1] - 1 + 7) / 8 * 8);
+    if (x_rows > 256) return;
+    const int64_t x_bytes = (int64_t)x_rows * lay.slice_bytes;
+    const int64_t kb_total = pl->K_total * 2 / lay.slice_bytes;
+    const int64_t kb_per_tap = pl->C_in_pad * 2 / lay.slice_bytes;
+    const int64_t avail = lay.smem_budget - 1024 - kGemmBarBytes;
+    const int64_t w_tile = kb_total * lay.w_box_bytes;
+    int64_t stages, stage_bytes;
+    int wres = 0;
+    if (pl->num_r_tiles == 1 && w_tile + 2 * x_bytes <= avail) {
+        wres = 1;
+        stage_bytes = x_bytes;
+        stages = (avail - w_tile) / x_bytes;
+    } else {
+        stage_bytes = x_bytes + pl->m[1] * lay.w_box_bytes;
+        stages = avail / stage_bytes;
+    }
+    stages = std::min<int64_t>(stages, kGemmMaxStages);
+    const double tiles_default = (double)lay.stages / (double)kb_total;
+    const double tiles_shared = (double)stages / (double)kb_per_tap;
+    if (stages < 2 || tiles_shared < 1.2 * tiles_default) return;
+    gp->xshare = 1;
+    gp->wres = wres;
+    gp->x_rows = x_rows;
+    gp->nstages = (int)stages;
+    gp->stage_bytes = (int)stage_bytes;
+    gp->wres_off = (int)(stages * stage_bytes);
+    gp->bar_off = gp->wres_off + (wres ? (int)w_tile : 0);
+    gp->smem_bytes = 1024 + gp->bar_off + kGemmBarBytes;
+}
+
 cudaError_t run_tc_path(const ctr_plan_s *pl, const void *x, const void *w_packed,
                         const void *bias, void *y, char *ws, uint32_t *status,
                         cudaEvent_t ev_before, cudaEvent_t ev_after, cudaStream_t st,
@@ -472,26 +538,31 @@ cudaError_t run_tc_path(const ctr_plan_s *pl, const void *x, const void *w_packe
     cudaError_t e;
     void *xs = ws + pl->ws_off_stage;
     float *raw = pl->ws_raw_bytes ? reinterpret_cast<float *>(ws + pl->ws_off_raw) : nullptr;
-    if (!staged_in && (e = launch_stage_x(pl, x, xs, st)) != cudaSuccess) return e;
+    if (!staged_in && (e = pl->nhwc ? launch_stage_nhwc(pl, x, xs, st)
+                                    : launch_stage_x(pl, x, xs, st)) != cudaSuccess)
+        return e;
     if (pl->streaming &&
         (e = launch_stream_state(pl, xs, ws + pl->ws_off_state, st)) != cudaSuccess)
         return e;
 
-    const bool bf16 = pl->dtype == CTR_BF16;
-    const int es = bf16 ? 2 : 4;
+    const bool h16 = io16(pl);   // bf16 or fp16 operands, one plane
+    const int es = esize_io(pl);
     const size_t w_plane = (size_t)pl->M_pad * pl->K_total * es;
     const size_t x_plane = (size_t)pl->N_total * pl->C_in_pad * es;
     // maps: staged input (128-position boxes), packed weight (block_n-row boxes), lo planes;
     // every box is one K slice of the GEMM instantiation wide.
-    const int sb = gemm_slice_bytes(bf16 ? Prec::BF16 : Prec::TF32x3, pl->block_n);
+    const int sb = gemm_slice_bytes(prec_of(pl), pl->block_n);
+    GemmParams gp;
+    std::memset(&gp, 0, sizeof(gp));
+    set_pipeline_layout(pl, &gp);
     CUtensorMap maps[4];
-    bool ok = encode_2d(&maps[0], xs, bf16, pl->C_in_pad, pl->N_total, kBM, sb) &&
-              encode_2d(&maps[1], w_packed, bf16, pl->K_total, pl->M_pad, pl->block_n, sb);
-    if (!bf16) {
+    bool ok = encode_2d(&maps[0], xs, pl->dtype, pl->C_in_pad, pl->N_total, (uint32_t)gp.x_rows, sb) &&
+              encode_2d(&maps[1], w_packed, pl->dtype, pl->K_total, pl->M_pad, pl->block_n, sb);
+    if (!h16) {
         ok = ok &&
-             encode_2d(&maps[2], static_cast<char *>(xs) + x_plane, false, pl->C_in_pad,
+             encode_2d(&maps[2], static_cast<char *>(xs) + x_plane, IO_F32, pl->C_in_pad,
                        pl->N_total, kBM, sb) &&
-             encode_2d(&maps[3], static_cast<const char *>(w_packed) + w_plane, false,
+             encode_2d(&maps[3], static_cast<const char *>(w_packed) + w_plane, IO_F32,
                        pl->K_total, pl->M_pad, pl->block_n, sb);
     } else {
         maps[2] = maps[0];
@@ -499,8 +570,6 @@ cudaError_t run_tc_path(const ctr_plan_s *pl, const void *x, const void *w_packe
     }
     if (!ok) return cudaErrorInvalidValue;
 
-    GemmParams gp;
-    std::memset(&gp, 0, sizeof(gp));
     gp.num_p_tiles = pl->num_p_tiles;
     gp.num_r_tiles = pl->num_r_tiles;
     gp.splits = pl->splits;
@@ -525,6 +594,17 @@ cudaError_t run_tc_path(const ctr_plan_s *pl, const void *x, const void *w_packe
         gp.epi.ys_hx = nx->hf[1];
         gp.epi.ys_cpad = nx->C_in_pad;
         gp.epi.ys_lo = nx->N_total * nx->C_in_pad;
+        gp.epi.ys_tf32 = nx->dtype == CTR_F32;
+    } else if (pl->nhwc) {
+        // A channels-last y: the same channels-last output stage, on y itself.
+        gp.epi.out_staged = 1;
+        gp.epi.y = y;
+        gp.epi.ys_Py = pl->out[0];
+        gp.epi.ys_Px = pl->out[1];
+        gp.epi.ys_hy = gp.epi.ys_hx = 0;
+        gp.epi.ys_cpad = pl->C_out;
+        gp.epi.ys_lo = 0;
+        gp.epi.ys_tf32 = 0;
     }
     gp.raw = raw;
     gp.raw_ld = raw_ld_of(pl);
@@ -576,7 +656,7 @@ ctr_status ctr_plan_create(ctr_plan_t *out, int ndim, int64_t N, int64_t C_in, i
     if (ndim != 1 && ndim != 2) return CTR_ERR_INVALID_ARG;
     if (!in_spatial || !kernel || !stride || !padding) return CTR_ERR_INVALID_ARG;
     if (N < 0 || C_in < 1 || C_out < 1) return CTR_ERR_INVALID_ARG;
-    if (dtype != CTR_F32 && dtype != CTR_BF16) return CTR_ERR_INVALID_ARG;
+    if (dtype != CTR_F32 && dtype != CTR_BF16 && dtype != CTR_F16) return CTR_ERR_INVALID_ARG;
     const int64_t kLim = (int64_t)1 << 31;
     if (N >= kLim || C_in >= kLim || C_out >= kLim) return CTR_ERR_INVALID_ARG;
 
@@ -766,6 +846,21 @@ ctr_status ctr_plan_set_pads(ctr_plan_t pl, const int64_t *pads_begin, const int
     return set_geometry(pl, dil, pb, pe);
 }
 
+ctr_status ctr_plan_set_layout(ctr_plan_t pl, int layout) {
+    if (!pl || (layout != CTR_LAYOUT_NCHW && layout != CTR_LAYOUT_NHWC)) return CTR_ERR_INVALID_ARG;
+    if (pl->prepared) return CTR_ERR_INVALID_ARG;
+    const int nhwc = layout == CTR_LAYOUT_NHWC;
+    if (nhwc == pl->nhwc) return CTR_OK;
+    if (nhwc && (pl->streaming || pl->forced_path == CTR_PATH_DEPTHWISE)) return CTR_ERR_UNSUPPORTED;
+    pl->nhwc = nhwc;
+    const ctr_status st = reroute(pl, pl->forced_path, pl->forced_split, pl->groups);
+    if (st != CTR_OK) {
+        pl->nhwc = !nhwc;
+        reroute(pl, pl->forced_path, pl->forced_split, pl->groups);
+    }
+    return st;
+}
+
 ctr_status ctr_plan_set_auto_pad(ctr_plan_t pl, int auto_pad, const int64_t *output_shape) {
     if (!pl || auto_pad < CTR_AUTO_PAD_NOTSET || auto_pad > CTR_AUTO_PAD_VALID)
         return CTR_ERR_INVALID_ARG;
@@ -809,7 +904,7 @@ ctr_status ctr_plan_set_streaming(ctr_plan_t pl, int enable) {
     }
     // 1-D, no padding or output_padding, k >= s, one group, undilated, and a carry of at
     // most kMaxStreamCarry frames on the polyphase path.
-    if (pl->ndim != 1 || pl->p[1] != 0 || pl->pe[1] != 0 || pl->op[1] != 0 ||
+    if (pl->ndim != 1 || pl->nhwc || pl->p[1] != 0 || pl->pe[1] != 0 || pl->op[1] != 0 ||
         pl->k[1] < pl->s[1] || pl->groups != 1 || pl->dil[1] != 1 ||
         ceil_div(pl->k[1], pl->s[1]) - 1 > ctr::kMaxStreamCarry)
         return CTR_ERR_UNSUPPORTED;
@@ -915,7 +1010,8 @@ ctr_status ctr_plan_describe(ctr_plan_t pl, char *buf, size_t len) {
                  "path=%s prec=%s rows=%lld(pad %lld, BN %d, %d tiles) positions=%lld(%d tiles) "
                  "K=%lld splits=%d group=%d tiles=%lld sms=%d S=%d/%d taps=%lldx%lld%s "
                  "pitch=%lldx%lld epi=%d/%dB packed=%zu ws=%zu",
-                 pname, pl->dtype == CTR_BF16 ? "bf16" : "3xtf32", (long long)pl->M_rows,
+                 pname, pl->dtype == CTR_BF16 ? "bf16" : pl->dtype == CTR_F16 ? "f16" : "3xtf32",
+                 (long long)pl->M_rows,
                  (long long)pl->M_pad, pl->block_n, pl->num_r_tiles, (long long)pl->N_total,
                  pl->num_p_tiles, (long long)pl->K_total, pl->splits,
                  pl->kb_group == kNoGroup ? 0 : pl->kb_group, (long long)pl->num_tiles,
@@ -925,7 +1021,21 @@ ctr_status ctr_plan_describe(ctr_plan_t pl, char *buf, size_t len) {
                  pl->packed_bytes, pl->ws_bytes_needed);
     } else {
         snprintf(buf, len, "path=%s dtype=%s groups=%lld packed=%zu ws=0", pname,
-                 pl->dtype == CTR_BF16 ? "bf16" : "f32", (long long)pl->groups, pl->packed_bytes);
+                 pl->dtype == CTR_BF16 ? "bf16" : pl->dtype == CTR_F16 ? "f16" : "f32",
+                 (long long)pl->groups, pl->packed_bytes);
+    }
+    if (is_tc_path(pl->path) && pl->block_n > 0) {
+        GemmParams gp;
+        std::memset(&gp, 0, sizeof(gp));
+        ctr::set_pipeline_layout(pl, &gp);
+        const size_t used = strlen(buf);
+        if (used + 1 < len)
+            snprintf(buf + used, len - used, " stages=%d%s", gp.nstages,
+                     gp.xshare ? (gp.wres ? " shared-x resident-w" : " shared-x") : "");
+    }
+    if (pl->nhwc) {
+        const size_t used = strlen(buf);
+        if (used + 1 < len) snprintf(buf + used, len - used, " nhwc");
     }
     if (pl->dil[0] > 1 || pl->dil[1] > 1 || pl->p[0] != pl->pe[0] || pl->p[1] != pl->pe[1]) {
         const size_t used = strlen(buf);
@@ -962,7 +1072,7 @@ ctr_status ctr_forward(ctr_plan_t pl, const void *x, const void *w_packed, const
     if (!pl->prepared) return CTR_ERR_NOT_PREPARED;
     ctr_plan_s *nx = pl->chain_next;
     // A weight packed for a chained output (phase-major rows) needs that chain.
-    if (pl->row_pm && !nx) return CTR_ERR_INVALID_ARG;
+    if (pl->row_pm && !nx && !pl->nhwc) return CTR_ERR_INVALID_ARG;
     const bool staged_in = !x && pl->chain_prev != nullptr;  // input staged by the previous plan
     if (!w_packed || (nx ? y != nullptr : y == nullptr)) return CTR_ERR_INVALID_ARG;
     if (!x && !staged_in && pl->B * pl->C_in * pl->in[0] * pl->in[1] > 0)

@@ -35,7 +35,8 @@ struct Geo {
     int64_t dy, dx;           // dilation
     int act;
     float slope;
-    int bf16;
+    int io;           // IoType of x, w, bias and y
+    int nhwc;         // x and y channels last
 };
 
 Geo geo_of(const ctr_plan_s *pl) {
@@ -59,7 +60,8 @@ Geo geo_of(const ctr_plan_s *pl) {
     g.dx = pl->dil[1];
     g.act = pl->act;
     g.slope = pl->slope;
-    g.bf16 = pl->dtype == CTR_BF16 ? 1 : 0;
+    g.io = pl->dtype;   // IoType
+    g.nhwc = pl->nhwc;
     return g;
 }
 
@@ -82,19 +84,39 @@ struct TapRange {
 __device__ __forceinline__ TapRange tap_range(int64_t r, int64_t s, int64_t d) {
     return d == 1 ? TapRange{r % s, s} : TapRange{0, 1};
 }
+// Output element idx of a plan's y, NCHW or NHWC order.
+struct OutIdx {
+    int64_t b, oc, oy, ox;
+};
+__device__ __forceinline__ OutIdx out_index(int64_t idx, const Geo &g) {
+    OutIdx o;
+    if (g.nhwc) {
+        o.oc = idx % g.C_out;
+        int64_t t = idx / g.C_out;
+        o.ox = t % g.Wo;
+        t /= g.Wo;
+        o.oy = t % g.Ho;
+        o.b = t / g.Ho;
+    } else {
+        o.ox = idx % g.Wo;
+        int64_t t = idx / g.Wo;
+        o.oy = t % g.Ho;
+        t /= g.Ho;
+        o.oc = t % g.C_out;
+        o.b = t / g.C_out;
+    }
+    return o;
+}
+
 __global__ void gather_kernel(const void *__restrict__ x, const void *__restrict__ w,
                               const void *__restrict__ bias, void *__restrict__ y, Geo g,
                               int64_t total) {
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t ox = idx % g.Wo;
-        int64_t t = idx / g.Wo;
-        const int64_t oy = t % g.Ho;
-        t /= g.Ho;
-        const int64_t oc = t % g.C_out;
-        const int64_t b = t / g.C_out;
+        const OutIdx o = out_index(idx, g);
+        const int64_t ox = o.ox, oy = o.oy, oc = o.oc, b = o.b;
         const int64_t grp = oc / g.cout_g, ic0 = grp * g.cin_g;
-        float acc = bias ? load_io(bias, oc, g.bf16) : 0.0f;
+        float acc = bias ? load_io(bias, oc, g.io) : 0.0f;
         const int64_t ry = oy + g.py, rx = ox + g.px;
         const TapRange try_ = tap_range(ry, g.sy, g.dy), trx = tap_range(rx, g.sx, g.dx);
         for (int64_t ty = try_.t0; ty < g.ky; ty += try_.step) {
@@ -109,17 +131,19 @@ __global__ void gather_kernel(const void *__restrict__ x, const void *__restrict
                 if (nx % g.sx) continue;
                 const int64_t ix = nx / g.sx;
                 if (ix >= g.W) continue;
-                const int64_t xoff = ((b * g.C_in + ic0) * g.H + iy) * g.W + ix;
+                // input channel ic0 at (b, iy, ix) and the step between input channels
+                const int64_t xoff = g.nhwc ? ((b * g.H + iy) * g.W + ix) * g.C_in + ic0
+                                            : ((b * g.C_in + ic0) * g.H + iy) * g.W + ix;
+                const int64_t xstride = g.nhwc ? 1 : g.H * g.W;
                 const int64_t woff =
                     (((ic0 * g.cout_g + oc - grp * g.cout_g) * g.ky) + ty) * g.kx + tx;
-                const int64_t xstride = g.H * g.W;
                 const int64_t wstride = g.cout_g * g.ky * g.kx;
                 for (int64_t ic = 0; ic < g.cin_g; ++ic)
-                    acc = fmaf(load_io(x, xoff + ic * xstride, g.bf16),
-                               load_io(w, woff + ic * wstride, g.bf16), acc);
+                    acc = fmaf(load_io(x, xoff + ic * xstride, g.io),
+                               load_io(w, woff + ic * wstride, g.io), acc);
             }
         }
-        store_io(y, idx, apply_act(acc, g.act, g.slope), g.bf16);
+        store_io(y, idx, apply_act(acc, g.act, g.slope), g.io);
     }
 }
 
@@ -127,9 +151,9 @@ __global__ void fill_bias_kernel(const void *__restrict__ bias, void *__restrict
                                  int64_t total) {
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t oc = (idx / (g.Ho * g.Wo)) % g.C_out;
-        const float v = bias ? load_io(bias, oc, g.bf16) : 0.0f;
-        store_io(y, idx, apply_act(v, g.act, g.slope), g.bf16);
+        const int64_t oc = out_index(idx, g).oc;
+        const float v = bias ? load_io(bias, oc, g.io) : 0.0f;
+        store_io(y, idx, apply_act(v, g.act, g.slope), g.io);
     }
 }
 
@@ -151,7 +175,7 @@ struct PackGeo {
     int64_t dy, dx;       // dilation (polyphase rows of the zero-inserted kernel)
     int S, S_pad;
     int polyphase;
-    int bf16;
+    int io;               // IoType of the weight and the packed operand
     int pm_tc, block_n;   // phase-major rows within tiles of block_n rows (pm_tc channels)
 };
 
@@ -205,10 +229,12 @@ __global__ void prepack_kernel(const void *__restrict__ w, void *__restrict__ wp
                 tx = j - ty * pg.kx;
             }
             if (ty < pg.ky && tx < pg.kx)
-                v = load_io(w, ((ic * pg.C_out + oc) * pg.ky + ty) * pg.kx + tx, pg.bf16);
+                v = load_io(w, ((ic * pg.C_out + oc) * pg.ky + ty) * pg.kx + tx, pg.io);
         }
-        if (pg.bf16) {
+        if (pg.io == IO_BF16) {
             static_cast<__nv_bfloat16 *>(wp)[idx] = __float2bfloat16_rn(v);  // exact: v is bf16
+        } else if (pg.io == IO_F16) {
+            static_cast<__half *>(wp)[idx] = __float2half_rn(v);             // exact: v is fp16
         } else {
             const float hi = ptx::to_tf32(v);
             const float lo = ptx::to_tf32(v - hi);
@@ -221,7 +247,7 @@ __global__ void prepack_kernel(const void *__restrict__ w, void *__restrict__ wp
 // -------------------------------------------------------------------------- stage_x
 struct StageGeo {
     int64_t B, C_in, C_in_pad, H, W, Py, Px, hy, hx, N_total;
-    int bf16;
+    int b16;   // 16-bit elements (bf16 or fp16), else fp32
 };
 
 // xs[n][c] with n = (b*Py + py')*Px + px': x[b, c, py' - hy, px' - hx] inside the input and
@@ -252,13 +278,16 @@ struct StageUnits {
     int64_t tiles;     // rows * xtiles * cchunks
 };
 
-template <bool BF16, bool VEC>
+template <bool B16, bool VEC>
 __global__ void __launch_bounds__(kStageThreads) stage_x_kernel(const void *__restrict__ x,
                                                                void *__restrict__ xs,
                                                                StageGeo sg, StageUnits su) {
     ptx::griddep_wait();
     ptx::griddep_launch_dependents();
-    using T = typename std::conditional<BF16, __nv_bfloat16, float>::type;
+    // 16-bit inputs (bf16 or fp16) are moved as raw 16-bit payloads: placed in the high half
+    // of an fp32 word in shared memory and taken back out unchanged, whatever the format.
+    constexpr bool BF16 = B16;
+    using T = typename std::conditional<B16, uint16_t, float>::type;
     constexpr int kStageC = BF16 ? 64 : 32;      // channels per tile (128 bytes of a row)
     constexpr int kInVec = 16 / sizeof(T);       // positions per 16-byte load
     constexpr int kOutVec = 16 / sizeof(T);      // channels per 16-byte store
@@ -307,7 +336,12 @@ __global__ void __launch_bounds__(kStageThreads) stage_x_kernel(const void *__re
                 } else {
 #pragma unroll
                     for (int j = 0; j < kInVec; ++j)
-                        if (xx + j >= 0 && xx + j < sg.W) val[j] = static_cast<float>(src[xx + j]);
+                        if (xx + j >= 0 && xx + j < sg.W) {
+                            if constexpr (BF16)
+                                val[j] = __uint_as_float((uint32_t)src[xx + j] << 16);
+                            else
+                                val[j] = src[xx + j];
+                        }
                 }
             }
             const int sw = (c / kOutVec) & 7;
@@ -338,7 +372,7 @@ __global__ void __launch_bounds__(kStageThreads) stage_x_kernel(const void *__re
                 for (int k = 0; k < 4; ++k)   // exact: the values came from bf16
                     w4[k] = (__float_as_uint(val[2 * k]) >> 16) |
                             (__float_as_uint(val[2 * k + 1]) & 0xFFFF0000u);
-                *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(xs) + o) =
+                *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(xs) + o) =
                     make_uint4(w4[0], w4[1], w4[2], w4[3]);
             } else {
                 float hi[4], lo[4];
@@ -371,6 +405,63 @@ __global__ void __launch_bounds__(kStageThreads) stage_x_kernel(const void *__re
         if (xt == su.xtiles - 1 && sg.hx + kStageTP * su.xtiles < sg.Px)
             zero_cols(sg.hx + kStageTP * su.xtiles, sg.Px);
         __syncthreads();   // the tile is reused by the next iteration
+    }
+}
+
+// -------------------------------------------------------------------------- stage_nhwc
+// The staged operand from a channels-last x: staged row n = (b*Py + py')*Px + px' holds
+// x[b, py' - hy, px' - hx, 0 .. C_in) followed by zeros up to C_in_pad, or zeros outside the
+// input.  One thread per 16-byte vector of a staged row: consecutive threads read and write
+// consecutive bytes of one position.  fp32 input becomes tf32 hi and lo planes; 16-bit input
+// is moved as raw payloads.  VEC: x rows are whole 16-byte vectors (C_in * esize % 16 == 0).
+template <bool B16, bool VEC>
+__global__ void __launch_bounds__(256) stage_nhwc_kernel(const void *__restrict__ x,
+                                                         void *__restrict__ xs, StageGeo sg,
+                                                         int64_t total) {
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
+    using E = typename std::conditional<B16, uint16_t, uint32_t>::type;
+    constexpr int kVec = 16 / (int)sizeof(E);           // elements per vector
+    const int64_t vpr = sg.C_in_pad / kVec;             // vectors per staged row
+    const int64_t lo_off = sg.N_total * sg.C_in_pad;    // elements to the lo plane
+    const E *__restrict__ xe = static_cast<const E *>(x);
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t n = i / vpr;
+        const int64_t c0 = (i - n * vpr) * kVec;
+        const int64_t row = n / sg.Px;                  // b*Py + py'
+        const int64_t px = n - row * sg.Px;
+        const int64_t b = row / sg.Py;
+        const int64_t yy = row - b * sg.Py - sg.hy, xx = px - sg.hx;
+        E v[kVec];
+#pragma unroll
+        for (int k = 0; k < kVec; ++k) v[k] = 0;
+        if (yy >= 0 && yy < sg.H && xx >= 0 && xx < sg.W && c0 < sg.C_in) {
+            const E *src = xe + ((b * sg.H + yy) * sg.W + xx) * sg.C_in + c0;
+            if (VEC && c0 + kVec <= sg.C_in) {
+                const uint4 q = *reinterpret_cast<const uint4 *>(src);
+                *reinterpret_cast<uint4 *>(v) = q;
+            } else {
+#pragma unroll
+                for (int k = 0; k < kVec; ++k)
+                    if (c0 + k < sg.C_in) v[k] = src[k];
+            }
+        }
+        const int64_t o = n * sg.C_in_pad + c0;
+        if constexpr (B16) {
+            *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(xs) + o) = *reinterpret_cast<uint4 *>(v);
+        } else {
+            float hi[4], lo[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float f = __uint_as_float(v[k]);
+                hi[k] = ptx::to_tf32(f);
+                lo[k] = ptx::to_tf32(f - hi[k]);
+            }
+            *reinterpret_cast<float4 *>(static_cast<float *>(xs) + o) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<float4 *>(static_cast<float *>(xs) + lo_off + o) =
+                make_float4(lo[0], lo[1], lo[2], lo[3]);
+        }
     }
 }
 
@@ -486,13 +577,9 @@ __global__ void col2im_kernel(const float *__restrict__ col, int64_t ld, int64_t
     ptx::griddep_launch_dependents();
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t ox = idx % g.Wo;
-        int64_t t = idx / g.Wo;
-        const int64_t oy = t % g.Ho;
-        t /= g.Ho;
-        const int64_t oc = t % g.C_out;
-        const int64_t b = t / g.C_out;
-        float acc = bias ? load_io(bias, oc, g.bf16) : 0.0f;
+        const OutIdx o = out_index(idx, g);
+        const int64_t ox = o.ox, oy = o.oy, oc = o.oc, b = o.b;
+        float acc = bias ? load_io(bias, oc, g.io) : 0.0f;
         const int64_t ry = oy + g.py, rx = ox + g.px;
         const TapRange try_ = tap_range(ry, g.sy, g.dy), trx = tap_range(rx, g.sx, g.dx);
         for (int64_t ty = try_.t0; ty < g.ky; ty += try_.step) {
@@ -513,7 +600,7 @@ __global__ void col2im_kernel(const float *__restrict__ col, int64_t ld, int64_t
                 for (int z = 0; z < splits; ++z) acc += p[(int64_t)z * split_stride];
             }
         }
-        store_io(y, idx, apply_act(acc, g.act, g.slope), g.bf16);
+        store_io(y, idx, apply_act(acc, g.act, g.slope), g.io);
     }
 }
 
@@ -575,7 +662,7 @@ cudaError_t launch_prepack(const ctr_plan_s *pl, const void *w, void *w_packed, 
     pg.S = pl->S;
     pg.S_pad = pl->S_pad;
     pg.polyphase = pl->path == CTR_PATH_POLYPHASE ? 1 : 0;
-    pg.bf16 = pl->dtype == CTR_BF16 ? 1 : 0;
+    pg.io = pl->dtype;
     pg.pm_tc = pl->row_pm ? pl->block_n / pl->S_pad : 0;
     pg.block_n = pl->block_n;
     const int64_t total = pg.M_pad * pg.K_total;
@@ -587,7 +674,7 @@ cudaError_t launch_prepack(const ctr_plan_s *pl, const void *w, void *w_packed, 
 cudaError_t launch_stream_state(const ctr_plan_s *pl, void *xs, void *state, cudaStream_t st) {
     const int carry = (int)(pl->m[1] - 1);
     if (carry <= 0) return cudaSuccess;
-    const bool bf16 = pl->dtype == CTR_BF16;
+    const bool bf16 = pl->dtype != CTR_F32;   // 16-bit elements (bf16 or fp16), one plane
     const int planes = bf16 ? 1 : 2;
     const int64_t xs_plane = pl->N_total * pl->C_in_pad;         // elements per staged plane
     const int64_t st_plane = pl->B * carry * pl->C_in_pad;
@@ -617,21 +704,54 @@ cudaError_t launch_stage_x(const ctr_plan_s *pl, const void *x, void *xs, cudaSt
     sg.hy = pl->hf[0];
     sg.hx = pl->hf[1];
     sg.N_total = pl->N_total;
-    sg.bf16 = pl->dtype == CTR_BF16 ? 1 : 0;
+    sg.b16 = pl->dtype != CTR_F32;
     if (sg.N_total == 0) return cudaSuccess;
     StageUnits su;
-    su.cchunks = sg.C_in_pad / (sg.bf16 ? 64 : 32);
+    su.cchunks = sg.C_in_pad / (sg.b16 ? 64 : 32);
     su.x_first = 0;
     su.xtiles = std::max<int64_t>(1, ceil_div(sg.W, kStageTP));
     su.tiles = sg.B * sg.Py * su.xtiles * su.cchunks;
     const int64_t blocks = std::min<int64_t>(su.tiles, (int64_t)pl->num_sms * 8);
-    const bool vec = (sg.W * (sg.bf16 ? 2 : 4)) % 16 == 0;
+    const bool vec = (sg.W * (sg.b16 ? 2 : 4)) % 16 == 0;
     const dim3 grid((unsigned)blocks);
     cudaError_t e;
 #define CTR_STAGE(B, V)                                                                   \
     if ((e = prefer_max_smem<stage_x_kernel<B, V>>()) != cudaSuccess) return e;          \
     e = launch_pdl(stage_x_kernel<B, V>, grid, dim3(kStageThreads), 0, st, x, xs, sg, su)
-    if (sg.bf16) {
+    if (sg.b16) {
+        if (vec) { CTR_STAGE(true, true); } else { CTR_STAGE(true, false); }
+    } else {
+        if (vec) { CTR_STAGE(false, true); } else { CTR_STAGE(false, false); }
+    }
+#undef CTR_STAGE
+    if (e != cudaSuccess) return e;
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_stage_nhwc(const ctr_plan_s *pl, const void *x, void *xs, cudaStream_t st) {
+    StageGeo sg;
+    sg.B = pl->B;
+    sg.C_in = pl->C_in;
+    sg.C_in_pad = pl->C_in_pad;
+    sg.H = pl->in[0];
+    sg.W = pl->in[1];
+    sg.Py = pl->P[0];
+    sg.Px = pl->P[1];
+    sg.hy = pl->hf[0];
+    sg.hx = pl->hf[1];
+    sg.N_total = pl->N_total;
+    sg.b16 = pl->dtype != CTR_F32;
+    if (sg.N_total == 0) return cudaSuccess;
+    const int es = sg.b16 ? 2 : 4;
+    const int64_t total = sg.N_total * sg.C_in_pad * es / 16;
+    const bool vec = (sg.C_in * es) % 16 == 0;
+    const dim3 grid(grid_for(total, kBlock));
+    cudaError_t e;
+#define CTR_STAGE(B, V)                                                                   \
+    if ((e = prefer_max_smem<stage_nhwc_kernel<B, V>>()) != cudaSuccess) return e;       \
+    e = launch_pdl(stage_nhwc_kernel<B, V>, grid, dim3(kBlock), 0, st, x, xs, sg, total)
+    if (sg.b16) {
         if (vec) { CTR_STAGE(true, true); } else { CTR_STAGE(true, false); }
     } else {
         if (vec) { CTR_STAGE(false, true); } else { CTR_STAGE(false, false); }

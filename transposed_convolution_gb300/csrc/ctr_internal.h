@@ -18,7 +18,11 @@ namespace ctr {
 constexpr int kBM = 128;
 constexpr int kBKBytes = 128;
 
-enum class Prec : int { BF16 = 0, TF32x3 = 1 };
+enum class Prec : int { BF16 = 0, TF32x3 = 1, F16 = 2 };
+constexpr bool is_16bit(Prec p) { return p != Prec::TF32x3; }
+
+// I/O element type of a plan: the ctr_dtype code (CTR_F32, CTR_BF16, CTR_F16).
+enum IoType : int { IO_F32 = 0, IO_BF16 = 1, IO_F16 = 2 };
 enum EpiMode : int { EPI_POLYPHASE = 0, EPI_RAW = 1 };
 
 // Output-stage variants (chosen per plan on the host; see epilogue.cuh).
@@ -42,7 +46,7 @@ struct EpiParams {
     int64_t B, C_out, Hout, Wout;
     const void *bias;   // [C_out] in the I/O dtype, or nullptr
     void *y;
-    int out_bf16;       // 1: bf16 I/O, 0: fp32
+    int io;             // IoType of bias and y
     int act;            // ctr_act
     float slope;
     int kind;           // EpiKind
@@ -50,8 +54,11 @@ struct EpiParams {
     // Chained output (out_staged = 1): y is the next plan's staged input, channels-last rows
     // of ys_cpad channels, output (oy, ox) of batch b at row (b*ys_Py + oy + ys_hy)*ys_Px +
     // ox + ys_hx; fp32 as tf32 hi and lo planes, ys_lo elements apart.
+    // The same output path writes a channels-last (NHWC) y: then ys_* describe y itself (no
+    // halos, C_out channels per row) and ys_tf32 = 0 stores plain values.
     int out_staged;
     int64_t ys_Px, ys_Py, ys_hx, ys_hy, ys_cpad, ys_lo;
+    int ys_tf32;        // fp32 values as tf32 hi and lo planes (a staged operand)
     // Phase-major rows (pm_tc > 0, chained producers only): inside each tile of
     // pm_tc * S_pad rows, row j * pm_tc + c is phase j of the tile's channel c, so a 32-row
     // chunk holds whole channel runs of one (or a few) phases.
@@ -78,7 +85,25 @@ struct GemmParams {
     int64_t raw_split_stride;
     uint32_t *status;   // device status word (bit flags of bounded waits that gave up)
     uint64_t wait_limit_ns;
+    // Pipeline layout in shared memory (set by the host for the launch, see gemm_tc.cuh):
+    // nstages stages of stage_bytes from a 1024-byte-aligned base, the barriers at bar_off.
+    int nstages, stage_bytes, bar_off, smem_bytes;
+    // Shared-X mode (1-D, 16-bit operands): a stage holds one X box of x_rows staged rows
+    // (128 positions plus the taps' shifts) for one channel slice, and every tap's MMA reads
+    // it through a descriptor that starts tap rows further down; the stage also holds the
+    // taps' weight slices, unless the whole weight tile stays resident (wres) at wres_off.
+    int xshare, x_rows, wres, wres_off;
 };
+
+// Shared-memory layout of one GEMM instantiation (gemm_tc.cu): default stage count and
+// bytes, the dynamic shared-memory budget of one CTA, and the bytes of one K slice of a
+// 128-position X box and of a block_n-row weight box (one plane).
+struct GemmLayout {
+    int stages, stage_bytes, smem_budget, slice_bytes, x_box_bytes, w_box_bytes, planes;
+};
+GemmLayout gemm_layout(Prec prec, int block_n);
+constexpr int kGemmMaxStages = 12;
+constexpr int kGemmBarBytes = 512;
 
 // Status-word bits set by device code.
 constexpr uint32_t kStatusTimeoutProducer = 1u << 0;
@@ -95,6 +120,7 @@ struct ctr_plan_s {
     int64_t in[2], k[2], s[2], p[2], op[2], out[2];
     int64_t dil[2];     // dilation (ctr_plan_set_dilation; 1 = none)
     int64_t pe[2];      // back pad (ctr_plan_set_pads; p is the front pad; default pe = p)
+    int nhwc;           // ctr_plan_set_layout: x and y channels last
     int streaming;      // ctr_plan_set_streaming: carries the last m - 1 input frames
     int stream_saved_path;  // the forced path before streaming was turned on (restored after)
     int stream_ready;   // the carried frames were zeroed (ctr_plan_stream_reset)
@@ -214,6 +240,8 @@ cudaError_t launch_copy_weight(const ctr_plan_s *pl, const void *w, void *w_pack
                                cudaStream_t st);
 cudaError_t launch_prepack(const ctr_plan_s *pl, const void *w, void *w_packed, cudaStream_t st);
 cudaError_t launch_stage_x(const ctr_plan_s *pl, const void *x, void *xs, cudaStream_t st);
+// The same staged operand from a channels-last (NHWC) x.
+cudaError_t launch_stage_nhwc(const ctr_plan_s *pl, const void *x, void *xs, cudaStream_t st);
 // Streaming plans: move the carried input frames into the staged input's leading halo and
 // this call's last m - 1 frames into the carried state.
 cudaError_t launch_stream_state(const ctr_plan_s *pl, void *xs, void *state, cudaStream_t st);
@@ -235,13 +263,17 @@ cudaError_t launch_depthwise(const ctr_plan_s *pl, const void *x, const void *w,
 cudaError_t launch_gemm_tc(const ctr_plan_s *pl, const CUtensorMap *maps, const GemmParams &gp,
                            cudaStream_t st);
 
-// 2-D tiled tensor map over a row-major [rows][inner] operand matrix, box [box_rows]
-// [box_bytes], swizzled at box_bytes (128 or 64), zero fill (api.cu).
-bool encode_2d(CUtensorMap *map, const void *base, bool bf16, uint64_t inner, uint64_t rows,
+// 2-D tiled tensor map over a row-major [rows][inner] operand matrix of IoType io, box
+// [box_rows][box_bytes], swizzled at box_bytes (128 or 64), zero fill (api.cu).
+bool encode_2d(CUtensorMap *map, const void *base, int io, uint64_t inner, uint64_t rows,
                uint32_t box_rows, int box_bytes);
 
 // Output mapping of a tensor-core plan (api.cu).
 EpiParams make_epi(const ctr_plan_s *pl, const void *bias, void *y);
+
+// The GEMM's shared-memory pipeline for a plan (api.cu): stage count and size, barrier
+// offset, the shared-X and resident-weight modes.
+void set_pipeline_layout(const ctr_plan_s *pl, GemmParams *gp);
 
 // Staging (skipped when staged_in: a chained producer already wrote the staged input), GEMM
 // and reduce/col2im of a tensor-core plan with explicit scratch (api.cu).  With chained_to

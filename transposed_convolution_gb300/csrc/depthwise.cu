@@ -346,6 +346,8 @@ cudaError_t launch_typed(const ctr_plan_s *pl, const void *x, const void *w, con
 
 bool depthwise_supported(const ctr_plan_s *pl) {
     if (pl->groups != pl->C_in || pl->C_out % pl->C_in != 0) return false;
+    if (pl->dtype == CTR_F16) return false;   // compiled for fp32 and bf16; fp16 uses gather
+    if (pl->nhwc) return false;               // planes of NCHW tensors; NHWC uses gather
     if (pl->dil[0] != 1 || pl->dil[1] != 1) return false;   // taps compiled undilated
     // Planes, and offsets inside an input or output plane, in 32 bits.
     const int64_t lim = (int64_t)1 << 30;

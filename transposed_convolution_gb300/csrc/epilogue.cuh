@@ -16,20 +16,60 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "ctr_internal.h"
 #include "ptx.cuh"
 
 namespace ctr {
 
-__device__ __forceinline__ float load_io(const void *p, int64_t i, int bf16) {
-    return bf16 ? __bfloat162float(static_cast<const __nv_bfloat16 *>(p)[i])
-                : static_cast<const float *>(p)[i];
+// ------------------------------------------------------------ I/O element types
+// fp32, bf16 and fp16 values: conversions from fp32 round to nearest, ties to even.
+template <typename T> __device__ __forceinline__ T io_from_float(float v);
+template <> __device__ __forceinline__ float io_from_float<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 io_from_float<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+template <> __device__ __forceinline__ __half io_from_float<__half>(float v) {
+    return __float2half_rn(v);
+}
+// Two 16-bit values in one 32-bit word, a in the low half.
+template <typename T> __device__ __forceinline__ uint32_t io_pack2(float a, float b);
+template <> __device__ __forceinline__ uint32_t io_pack2<__nv_bfloat16>(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+template <> __device__ __forceinline__ uint32_t io_pack2<__half>(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+// The low and high 16-bit values of a word, as fp32 (exact).
+template <typename T> __device__ __forceinline__ float io_lo(uint32_t w);
+template <typename T> __device__ __forceinline__ float io_hi(uint32_t w);
+template <> __device__ __forceinline__ float io_lo<__nv_bfloat16>(uint32_t w) {
+    return __uint_as_float(w << 16);
+}
+template <> __device__ __forceinline__ float io_hi<__nv_bfloat16>(uint32_t w) {
+    return __uint_as_float(w & 0xFFFF0000u);
+}
+template <> __device__ __forceinline__ float io_lo<__half>(uint32_t w) {
+    return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu)));
+}
+template <> __device__ __forceinline__ float io_hi<__half>(uint32_t w) {
+    return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
 }
 
-__device__ __forceinline__ void store_io(void *p, int64_t i, float v, int bf16) {
-    if (bf16)
+__device__ __forceinline__ float load_io(const void *p, int64_t i, int io) {
+    if (io == IO_BF16) return __bfloat162float(static_cast<const __nv_bfloat16 *>(p)[i]);
+    if (io == IO_F16) return __half2float(static_cast<const __half *>(p)[i]);
+    return static_cast<const float *>(p)[i];
+}
+
+__device__ __forceinline__ void store_io(void *p, int64_t i, float v, int io) {
+    if (io == IO_BF16)
         static_cast<__nv_bfloat16 *>(p)[i] = __float2bfloat16_rn(v);
+    else if (io == IO_F16)
+        static_cast<__half *>(p)[i] = __float2half_rn(v);
     else
         static_cast<float *>(p)[i] = v;
 }
@@ -83,10 +123,7 @@ __device__ __forceinline__ void store_run(T *dst, const float *vals, int wbytes)
             if (wbytes >= 4) {
                 uint32_t u[N / 2];
 #pragma unroll
-                for (int i = 0; i < N; i += 2) {
-                    __nv_bfloat162 h = __floats2bfloat162_rn(vals[i], vals[i + 1]);
-                    u[i / 2] = *reinterpret_cast<uint32_t *>(&h);
-                }
+                for (int i = 0; i < N; i += 2) u[i / 2] = io_pack2<T>(vals[i], vals[i + 1]);
                 if constexpr (N % 8 == 0) {
                     if (wbytes == 16) {
 #pragma unroll
@@ -110,7 +147,7 @@ __device__ __forceinline__ void store_run(T *dst, const float *vals, int wbytes)
             }
         }
 #pragma unroll
-        for (int i = 0; i < N; ++i) dst[i] = __float2bfloat16_rn(vals[i]);
+        for (int i = 0; i < N; ++i) dst[i] = io_from_float<T>(vals[i]);
     }
 }
 
@@ -137,14 +174,14 @@ __device__ __forceinline__ void emit_run(T *__restrict__ dst, int64_t x0, const 
     } else {
 #pragma unroll
         for (int i = 0; i < NX; ++i)
-            if (x0 + i >= 0 && x0 + i < e.Wout) dst[i] = static_cast<T>(t[i]);
+            if (x0 + i >= 0 && x0 + i < e.Wout) dst[i] = io_from_float<T>(t[i]);
     }
 }
 
 // Bias of channel oc0 + lane for the first `count` lanes (0 elsewhere), so that a warp can
 // share a chunk's biases by shuffles: one load per lane, issued before any output store.
 __device__ __forceinline__ float lane_bias(const EpiParams &e, int64_t oc0, int count, int lane) {
-    return (e.bias && lane < count && oc0 + lane < e.C_out) ? load_io(e.bias, oc0 + lane, e.out_bf16)
+    return (e.bias && lane < count && oc0 + lane < e.C_out) ? load_io(e.bias, oc0 + lane, e.io)
                                                             : 0.0f;
 }
 
@@ -178,15 +215,15 @@ __device__ __forceinline__ void load_bias_vec(const EpiParams &e, int64_t oc0, f
         const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            b[2 * k] = __uint_as_float(w4[k] << 16);
-            b[2 * k + 1] = __uint_as_float(w4[k] & 0xFFFF0000u);
+            b[2 * k] = io_lo<T>(w4[k]);
+            b[2 * k + 1] = io_hi<T>(w4[k]);
         }
     } else if constexpr (sizeof(T) == 2 && N == 4) {
         const uint2 q = __ldg(reinterpret_cast<const uint2 *>(src));
-        b[0] = __uint_as_float(q.x << 16);
-        b[1] = __uint_as_float(q.x & 0xFFFF0000u);
-        b[2] = __uint_as_float(q.y << 16);
-        b[3] = __uint_as_float(q.y & 0xFFFF0000u);
+        b[0] = io_lo<T>(q.x);
+        b[1] = io_hi<T>(q.x);
+        b[2] = io_lo<T>(q.y);
+        b[3] = io_hi<T>(q.y);
     } else if constexpr (sizeof(T) == 4 && N == 4) {
         const float4 q = __ldg(reinterpret_cast<const float4 *>(src));
         b[0] = q.x;
@@ -238,14 +275,11 @@ __device__ __forceinline__ void store_vec(T *dst, const float *vals) {
     } else {
         if constexpr (kPer == 1) {
 #pragma unroll
-            for (int i = 0; i < N; ++i) dst[i] = __float2bfloat16_rn(vals[i]);
+            for (int i = 0; i < N; ++i) dst[i] = io_from_float<T>(vals[i]);
         } else {
             uint32_t u[N / 2];
 #pragma unroll
-            for (int i = 0; i < N; i += 2) {
-                __nv_bfloat162 h = __floats2bfloat162_rn(vals[i], vals[i + 1]);
-                u[i / 2] = *reinterpret_cast<uint32_t *>(&h);
-            }
+            for (int i = 0; i < N; i += 2) u[i / 2] = io_pack2<T>(vals[i], vals[i + 1]);
 #pragma unroll
             for (int i = 0; i < N / 2; i += kPer / 2) {
                 if constexpr (kPer == 8)
@@ -389,10 +423,10 @@ __device__ __forceinline__ void emit_generic(const float (&v)[32], const PosInfo
         const int64_t oy = (int64_t)e.sy * ps.qy + jy - e.py;
         const int64_t ox = (int64_t)e.sx * ps.qx + jx - e.px;
         if (oy < 0 || oy >= e.Hout || ox < 0 || ox >= e.Wout) continue;
-        const float bias = e.bias ? load_io(e.bias, oc, e.out_bf16) : 0.0f;
+        const float bias = e.bias ? load_io(e.bias, oc, e.io) : 0.0f;
         const float a = v[i] + bias;
         store_io(e.y, ((ps.b * e.C_out + oc) * e.Hout + oy) * e.Wout + ox,
-                 a < 0.0f ? a * slope_eff : a, e.out_bf16);
+                 a < 0.0f ? a * slope_eff : a, e.io);
     }
 }
 
@@ -407,14 +441,18 @@ __device__ __forceinline__ int64_t staged_row(const EpiParams &e, int64_t b, int
     return (b * e.ys_Py + oy + e.ys_hy) * e.ys_Px + ox + e.ys_hx;
 }
 
-// N consecutive channel values at dst (N * sizeof(T)-aligned): one plane for bf16, the hi
-// and lo planes for fp32.
+// N consecutive channel values at dst (N * sizeof(T)-aligned): one plane for 16-bit types;
+// for fp32 the tf32 hi and lo planes of a staged operand, or the values of a channels-last y.
 template <typename T, int N>
 __device__ __forceinline__ void store_channels(T *dst, const float *vals, const EpiParams &e) {
     constexpr int kBytes = N * (int)sizeof(T) < 16 ? N * (int)sizeof(T) : 16;
     if constexpr (sizeof(T) == 2) {
         store_run<T, N>(dst, vals, kBytes);
     } else {
+        if (!e.ys_tf32) {   // a channels-last y: the values themselves
+            store_run<T, N>(dst, vals, kBytes);
+            return;
+        }
         float hi[N], lo[N];
 #pragma unroll
         for (int i = 0; i < N; ++i) {
@@ -588,11 +626,13 @@ __device__ __forceinline__ void emit_generic_chain(const float (&v)[32], const P
         const int64_t oy = (int64_t)e.sy * ps.qy + jy - e.py;
         const int64_t ox = (int64_t)e.sx * ps.qx + jx - e.px;
         if (oy < 0 || oy >= e.Hout || ox < 0 || ox >= e.Wout) continue;
-        const float bias = e.bias ? load_io(e.bias, oc, e.out_bf16) : 0.0f;
+        const float bias = e.bias ? load_io(e.bias, oc, e.io) : 0.0f;
         const float val = leaky(v[i] + bias, slope_eff, use_min);
         const int64_t o = staged_row(e, ps.b, oy, ox) * e.ys_cpad + oc;
-        if (e.out_bf16) {
+        if (e.io == IO_BF16) {
             store_channels<__nv_bfloat16, 1>(static_cast<__nv_bfloat16 *>(e.y) + o, &val, e);
+        } else if (e.io == IO_F16) {
+            store_channels<__half, 1>(static_cast<__half *>(e.y) + o, &val, e);
         } else {
             store_channels<float, 1>(static_cast<float *>(e.y) + o, &val, e);
         }
@@ -604,7 +644,7 @@ __device__ __forceinline__ void emit_generic_chain(const float (&v)[32], const P
 // instantiation takes one of each (its precision fixes the type), so it keeps its register
 // budget; the split-K reduce takes everything.
 enum : int { kOutPlain = 1, kOutChain = 2, kOutBoth = 3 };
-enum : int { kIoAny = 0, kIoF32 = 1, kIoBF16 = 2 };
+enum : int { kIoAny = 0, kIoF32 = 1, kIoBF16 = 2, kIoF16 = 3 };
 
 // Output stage for the accumulator columns r0 .. r0+31 (r0 a multiple of 32) of one phase
 // position per lane: v[i] = D[n, r0 + i] (overwritten).  Warp-collective: all 32 lanes of the
@@ -612,17 +652,22 @@ enum : int { kIoAny = 0, kIoF32 = 1, kIoBF16 = 2 };
 template <int kOut, int kIo>
 __device__ __forceinline__ void emit_cols(float (&v)[32], const PosInfo &ps, int64_t r0,
                                           const EpiParams &e, int lane) {
-// CTR_IO(FN, (T, args...), (args...)): call FN<T, args...> for the kernel's I/O type(s).
+// CTR_IO(FN, (bf16, args...), (fp16, args...), (fp32, args...)): call FN<T, args...> for
+// the kernel's I/O type(s).
 #define CTR_IO_CALL(FN, TARGS) FN<CTR_IO_EXPAND TARGS>(v, ps, r0, e, lane)
 #define CTR_IO_EXPAND(...) __VA_ARGS__
-#define CTR_IO(FN, BF_ARGS, F_ARGS)                                        \
+#define CTR_IO(FN, BF_ARGS, H_ARGS, F_ARGS)                                \
     do {                                                                   \
         if constexpr (kIo == kIoBF16) {                                    \
             CTR_IO_CALL(FN, BF_ARGS);                                      \
+        } else if constexpr (kIo == kIoF16) {                              \
+            CTR_IO_CALL(FN, H_ARGS);                                       \
         } else if constexpr (kIo == kIoF32) {                              \
             CTR_IO_CALL(FN, F_ARGS);                                       \
-        } else if (e.out_bf16) {                                           \
+        } else if (e.io == IO_BF16) {                                      \
             CTR_IO_CALL(FN, BF_ARGS);                                      \
+        } else if (e.io == IO_F16) {                                       \
+            CTR_IO_CALL(FN, H_ARGS);                                       \
         } else {                                                           \
             CTR_IO_CALL(FN, F_ARGS);                                       \
         }                                                                  \
@@ -632,19 +677,19 @@ __device__ __forceinline__ void emit_cols(float (&v)[32], const PosInfo &ps, int
         if (kOut == kOutChain || e.out_staged) {
             if (e.pm_tc) {
                 switch (e.pm_tc >= 32 ? 32 : e.pm_tc) {
-                    case 2: CTR_IO(emit_pm_chain, (__nv_bfloat16, 2), (float, 2));
-                    case 4: CTR_IO(emit_pm_chain, (__nv_bfloat16, 4), (float, 4));
-                    case 8: CTR_IO(emit_pm_chain, (__nv_bfloat16, 8), (float, 8));
-                    case 16: CTR_IO(emit_pm_chain, (__nv_bfloat16, 16), (float, 16));
-                    default: CTR_IO(emit_pm_chain, (__nv_bfloat16, 32), (float, 32));
+                    case 2: CTR_IO(emit_pm_chain, (__nv_bfloat16, 2), (__half, 2), (float, 2));
+                    case 4: CTR_IO(emit_pm_chain, (__nv_bfloat16, 4), (__half, 4), (float, 4));
+                    case 8: CTR_IO(emit_pm_chain, (__nv_bfloat16, 8), (__half, 8), (float, 8));
+                    case 16: CTR_IO(emit_pm_chain, (__nv_bfloat16, 16), (__half, 16), (float, 16));
+                    default: CTR_IO(emit_pm_chain, (__nv_bfloat16, 32), (__half, 32), (float, 32));
                 }
             }
             switch (e.kind) {
-                case EPI_KIND_1D_S1: CTR_IO(emit_small_chain, (__nv_bfloat16, 1, 1), (float, 1, 1));
-                case EPI_KIND_1D_S2: CTR_IO(emit_small_chain, (__nv_bfloat16, 2, 1), (float, 2, 1));
-                case EPI_KIND_1D_S4: CTR_IO(emit_small_chain, (__nv_bfloat16, 4, 1), (float, 4, 1));
-                case EPI_KIND_1D_S8: CTR_IO(emit_small_chain, (__nv_bfloat16, 8, 1), (float, 8, 1));
-                case EPI_KIND_2D_S2x2: CTR_IO(emit_small_chain, (__nv_bfloat16, 2, 2), (float, 2, 2));
+                case EPI_KIND_1D_S1: CTR_IO(emit_small_chain, (__nv_bfloat16, 1, 1), (__half, 1, 1), (float, 1, 1));
+                case EPI_KIND_1D_S2: CTR_IO(emit_small_chain, (__nv_bfloat16, 2, 1), (__half, 2, 1), (float, 2, 1));
+                case EPI_KIND_1D_S4: CTR_IO(emit_small_chain, (__nv_bfloat16, 4, 1), (__half, 4, 1), (float, 4, 1));
+                case EPI_KIND_1D_S8: CTR_IO(emit_small_chain, (__nv_bfloat16, 8, 1), (__half, 8, 1), (float, 8, 1));
+                case EPI_KIND_2D_S2x2: CTR_IO(emit_small_chain, (__nv_bfloat16, 2, 2), (__half, 2, 2), (float, 2, 2));
                 default:
                     emit_generic_chain(v, ps, r0, e);
                     return;
@@ -653,15 +698,15 @@ __device__ __forceinline__ void emit_cols(float (&v)[32], const PosInfo &ps, int
     }
     if constexpr ((kOut & kOutPlain) != 0) {
         switch (e.kind) {
-            case EPI_KIND_1D_S1: CTR_IO(emit_small, (__nv_bfloat16, 1, 1), (float, 1, 1));
-            case EPI_KIND_1D_S2: CTR_IO(emit_small, (__nv_bfloat16, 2, 1), (float, 2, 1));
-            case EPI_KIND_1D_S4: CTR_IO(emit_small, (__nv_bfloat16, 4, 1), (float, 4, 1));
-            case EPI_KIND_1D_S8: CTR_IO(emit_small, (__nv_bfloat16, 8, 1), (float, 8, 1));
-            case EPI_KIND_1D_S16: CTR_IO(emit_small, (__nv_bfloat16, 16, 1), (float, 16, 1));
-            case EPI_KIND_1D_S32: CTR_IO(emit_small, (__nv_bfloat16, 32, 1), (float, 32, 1));
-            case EPI_KIND_2D_S2x2: CTR_IO(emit_small, (__nv_bfloat16, 2, 2), (float, 2, 2));
-            case EPI_KIND_2D_S4x4: CTR_IO(emit_small, (__nv_bfloat16, 4, 4), (float, 4, 4));
-            case EPI_KIND_1D_LARGE: CTR_IO(emit_large, (__nv_bfloat16), (float));
+            case EPI_KIND_1D_S1: CTR_IO(emit_small, (__nv_bfloat16, 1, 1), (__half, 1, 1), (float, 1, 1));
+            case EPI_KIND_1D_S2: CTR_IO(emit_small, (__nv_bfloat16, 2, 1), (__half, 2, 1), (float, 2, 1));
+            case EPI_KIND_1D_S4: CTR_IO(emit_small, (__nv_bfloat16, 4, 1), (__half, 4, 1), (float, 4, 1));
+            case EPI_KIND_1D_S8: CTR_IO(emit_small, (__nv_bfloat16, 8, 1), (__half, 8, 1), (float, 8, 1));
+            case EPI_KIND_1D_S16: CTR_IO(emit_small, (__nv_bfloat16, 16, 1), (__half, 16, 1), (float, 16, 1));
+            case EPI_KIND_1D_S32: CTR_IO(emit_small, (__nv_bfloat16, 32, 1), (__half, 32, 1), (float, 32, 1));
+            case EPI_KIND_2D_S2x2: CTR_IO(emit_small, (__nv_bfloat16, 2, 2), (__half, 2, 2), (float, 2, 2));
+            case EPI_KIND_2D_S4x4: CTR_IO(emit_small, (__nv_bfloat16, 4, 4), (__half, 4, 4), (float, 4, 4));
+            case EPI_KIND_1D_LARGE: CTR_IO(emit_large, (__nv_bfloat16), (__half), (float));
             default:
                 emit_generic(v, ps, r0, e);
                 return;

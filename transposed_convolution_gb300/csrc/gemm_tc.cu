@@ -7,6 +7,9 @@ namespace ctr {
 // gemm_tc_chain.cu: the instantiations whose output feeds the next plan's staged input.
 cudaError_t launch_gemm_tc_chain(const ctr_plan_s *pl, const CUtensorMap *maps,
                                  const GemmParams &gp, cudaStream_t st);
+// gemm_tc_f16.cu: the fp16 instantiations (both outputs).
+cudaError_t launch_gemm_tc_f16(const ctr_plan_s *pl, const CUtensorMap *maps,
+                               const GemmParams &gp, cudaStream_t st);
 
 namespace {
 template <Prec P, int BN>
@@ -16,8 +19,25 @@ cudaError_t launch_bn(const ctr_plan_s *pl, const CUtensorMap *maps, const GemmP
 }
 }  // namespace
 
+namespace {
+template <Prec P, int BN>
+GemmLayout layout_of() {
+    using C = Cfg<P, BN>;
+    return GemmLayout{C::kStages, C::kStageBytes, C::kSmemBudget, C::kSlice, C::kXBytes,
+                      C::kWBytes, C::kPlanes};
+}
+}  // namespace
+
+GemmLayout gemm_layout(Prec prec, int block_n) {
+    if (is_16bit(prec))   // fp16 and bf16 instantiations have the same layout
+        return block_n == 256 ? layout_of<Prec::BF16, 256>()
+               : block_n == 128 ? layout_of<Prec::BF16, 128>() : layout_of<Prec::BF16, 64>();
+    return block_n == 256 ? layout_of<Prec::TF32x3, 256>()
+           : block_n == 128 ? layout_of<Prec::TF32x3, 128>() : layout_of<Prec::TF32x3, 64>();
+}
+
 size_t gemm_smem_bytes(Prec prec, int block_n) {
-    if (prec == Prec::BF16)
+    if (is_16bit(prec))
         return block_n == 256 ? Cfg<Prec::BF16, 256>::kSmem
                : block_n == 128 ? Cfg<Prec::BF16, 128>::kSmem : Cfg<Prec::BF16, 64>::kSmem;
     return block_n == 256 ? Cfg<Prec::TF32x3, 256>::kSmem
@@ -27,6 +47,7 @@ size_t gemm_smem_bytes(Prec prec, int block_n) {
 cudaError_t launch_gemm_tc(const ctr_plan_s *pl, const CUtensorMap *maps, const GemmParams &gp,
                            cudaStream_t st) {
     if (gp.num_tiles <= 0) return cudaSuccess;
+    if (pl->dtype == CTR_F16) return launch_gemm_tc_f16(pl, maps, gp, st);
     if (gp.epi.out_staged) return launch_gemm_tc_chain(pl, maps, gp, st);
     if (pl->dtype == CTR_BF16) {
         switch (pl->block_n) {

@@ -58,7 +58,7 @@ constexpr int kSmemMax = 227 * 1024;
 // eight epilogue warps are issue-bound on their dependent arithmetic and store chains.  Two
 // CTAs per SM double the epilogue warps and independent tile pipelines an SM interleaves,
 // each CTA with half the shared memory (fewer stages) and 256 TMEM columns.
-constexpr int ctas_per_sm(Prec P, int BN) { return (P == Prec::BF16 && BN == 64) ? 2 : 1; }
+constexpr int ctas_per_sm(Prec P, int BN) { return (is_16bit(P) && BN == 64) ? 2 : 1; }
 constexpr uint64_t kDrainLimitNs = 2000000000ull;
 
 template <Prec P, int BN>
@@ -70,7 +70,7 @@ struct Cfg {
     static constexpr int kXBytes = kBM * kSlice;             // one 128-position Xs slice
     static constexpr int kWBytes = BN * kSlice;              // one BN-row weight slice
     static constexpr int kStageBytes = kPlanes * (kXBytes + kWBytes);
-    static constexpr int kBarBytes = 256;
+    static constexpr int kBarBytes = kGemmBarBytes;
     static constexpr int kCtas = ctas_per_sm(P, BN);
     // Two CTAs share an SM's 228 KB (each also reserves 1 KB for the system).
     static constexpr int kSmemBudget = kCtas == 1 ? kSmemMax : 112 * 1024;
@@ -91,8 +91,8 @@ struct Cfg {
     // sum region (nothing to fold); the later groups go through the accumulator.
     static constexpr bool kSumFirst = kTmemSum && kAccBufs == 1;
     static constexpr uint32_t kTmemCols = kAccBufs * BN + (kTmemSum ? BN : 0);
-    static constexpr uint32_t kIdesc =
-        ptx::idesc_f32acc(P == Prec::TF32x3 ? ptx::kFmtTF32 : ptx::kFmtBF16, kBM, BN);
+    static constexpr uint32_t kIdesc = ptx::idesc_f32acc(
+        P == Prec::TF32x3 ? ptx::kFmtTF32 : (P == Prec::F16 ? ptx::kFmtF16 : ptx::kFmtBF16), kBM, BN);
     static_assert(kStages >= 2, "at least two pipeline stages");
     static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512,
                   "TMEM allocation is a power of two");
@@ -137,7 +137,8 @@ __device__ __forceinline__ void store_chunk_out(const GemmParams &gp, const Tile
                                                 int c, float (&v)[32]) {
     const int64_t r0 = tc.r0 + 32 * c;
     if (fused) {
-        emit_cols<CHAIN ? kOutChain : kOutPlain, P == Prec::BF16 ? kIoBF16 : kIoF32>(
+        emit_cols<CHAIN ? kOutChain : kOutPlain,
+                  P == Prec::BF16 ? kIoBF16 : (P == Prec::F16 ? kIoF16 : kIoF32)>(
             v, ps, r0, gp.epi, lane);
         return;
     }
@@ -159,29 +160,32 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *stage_base = smem;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kStages * C::kStageBytes);
+    // The stage ring (nst stages of stage_bytes), then the barriers; the host sizes both.
+    const int nst = gp.nstages;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + gp.bar_off);
     uint64_t *full = bars;
-    uint64_t *empty = bars + C::kStages;
-    uint64_t *tmem_full = bars + 2 * C::kStages;
+    uint64_t *empty = bars + kGemmMaxStages;
+    uint64_t *tmem_full = bars + 2 * kGemmMaxStages;
     uint64_t *tmem_empty = tmem_full + C::kAccBufs;
     uint64_t *drain = tmem_empty + C::kAccBufs;
     uint64_t *sum_full = drain + 1;   // kSumFirst: a tile's first group is in the sum region
     uint64_t *sum_free = drain + 2;   // kSumFirst: the epilogue has read a tile's sums
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 3);
+    uint64_t *w_full = drain + 3;     // shared-X mode: the resident weight has landed
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 4);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     auto x_slice = [&](int s, int plane) -> uint8_t * {
-        return stage_base + s * C::kStageBytes + plane * C::kXBytes;
+        return stage_base + s * gp.stage_bytes + plane * C::kXBytes;
     };
     auto w_slice = [&](int s, int plane) -> uint8_t * {
-        return stage_base + s * C::kStageBytes + C::kPlanes * C::kXBytes + plane * C::kWBytes;
+        return stage_base + s * gp.stage_bytes + C::kPlanes * C::kXBytes + plane * C::kWBytes;
     };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
+        for (int s = 0; s < nst; ++s) {
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], 1);
         }
@@ -192,6 +196,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
         ptx::mbar_init(drain, 1);
         ptx::mbar_init(sum_full, 1);
         ptx::mbar_init(sum_free, kEpiWarps);
+        ptx::mbar_init(w_full, 1);
         *abort = 0;
         ptx::fence_mbar_init();
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -224,7 +229,50 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
             int stage = 0;
             uint32_t phase = 0;
             int64_t issued = 0;
-            for (int64_t t = blockIdx.x; t < gp.num_tiles && !*abort; t += gridDim.x) {
+            bool w_issued = false;
+            if constexpr (P != Prec::TF32x3) {
+                if (gp.xshare) {
+                    // Shared-X mode: per tile and channel slice kc, one X box of x_rows rows at
+                    // the tile's first tap row; the taps' weight slices with it, or the whole
+                    // weight tile once, up front, when it stays resident.
+                    const int x_bytes = gp.x_rows * C::kSlice;
+                    const int taps = gp.mx;
+                    if (gp.wres) {
+                        uint8_t *wr = stage_base + gp.wres_off;
+                        ptx::mbar_arrive_expect_tx(w_full, (uint32_t)(gp.kb_total * C::kWBytes));
+                        for (int kb = 0; kb < gp.kb_total; ++kb)
+                            ptx::tma_load_2d(wr + kb * C::kWBytes, &mapW, w_full, kb * C::kElems, 0);
+                        w_issued = true;
+                    }
+                    const uint32_t stage_tx =
+                        (uint32_t)(x_bytes + (gp.wres ? 0 : taps * C::kWBytes));
+                    for (int64_t t = blockIdx.x; t < gp.num_tiles && !*abort; t += gridDim.x) {
+                        const TileCoord tc = decode_tile((uint32_t)t, gp, BN);
+                        for (int kc = 0; kc < gp.kb_per_tap; ++kc) {
+                            if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, limit, abort)) {
+                                if (!*abort) give_up(abort, gp.status, kStatusTimeoutProducer);
+                                break;
+                            }
+                            ptx::mbar_arrive_expect_tx(&full[stage], stage_tx);
+                            uint8_t *st = stage_base + stage * gp.stage_bytes;
+                            ptx::tma_load_2d(st, &mapX, &full[stage], kc * C::kElems,
+                                             (int32_t)(tc.p0 + gp.shift0));
+                            if (!gp.wres)
+                                for (int g = 0; g < taps; ++g)
+                                    ptx::tma_load_2d(st + x_bytes + g * C::kWBytes, &mapW,
+                                                     &full[stage],
+                                                     (g * gp.kb_per_tap + kc) * C::kElems,
+                                                     (int32_t)tc.r0);
+                            ++issued;
+                            if (++stage == nst) {
+                                stage = 0;
+                                phase ^= 1u;
+                            }
+                        }
+                    }
+                }
+            }
+            for (int64_t t = blockIdx.x; !gp.xshare && t < gp.num_tiles && !*abort; t += gridDim.x) {
                 const TileCoord tc = decode_tile((uint32_t)t, gp, BN);
                 // Tap (uy, ux) and channel slice kc of K slice kb, stepped along with kb.
                 const int g0 = tc.kb0 / gp.kb_per_tap;
@@ -255,20 +303,22 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
                             ++uy;
                         }
                     }
-                    if (++stage == C::kStages) {
+                    if (++stage == nst) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
             // Wait for the latest load into every stage, so no copy lands after exit.
-            const int64_t pending = issued < C::kStages ? issued : C::kStages;
+            const int64_t pending = issued < nst ? issued : nst;
             for (int64_t s = 0; s < pending; ++s) {
                 const int64_t idx = issued - 1 - s;
-                if (!ptx::mbar_wait(&full[idx % C::kStages], (uint32_t)((idx / C::kStages) & 1),
+                if (!ptx::mbar_wait(&full[idx % nst], (uint32_t)((idx / nst) & 1),
                                     kDrainLimitNs, nullptr))
                     atomicOr(gp.status, kStatusTimeoutDrain);
             }
+            if (w_issued && !ptx::mbar_wait(w_full, 0, kDrainLimitNs, nullptr))
+                atomicOr(gp.status, kStatusTimeoutDrain);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -278,7 +328,62 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
             int grp = 0;    // accumulator groups issued by this CTA (selects the TMEM buffer)
             int items = 0;  // tiles issued by this CTA (kSumFirst barrier phases)
             bool ok = true;
-            for (int64_t t = blockIdx.x; ok && t < gp.num_tiles && !*abort; t += gridDim.x, ++items) {
+            if constexpr (P != Prec::TF32x3) {
+                if (gp.xshare) {
+                    // Shared-X mode: one accumulation group per tile; for every channel slice
+                    // the taps read the same X box, tap g starting g rows further down (a
+                    // K-major 128-byte-swizzled operand may start at any row of its
+                    // 1024-byte-aligned box: the swizzle follows the address bits).
+                    const int x_bytes = gp.x_rows * C::kSlice;
+                    const int taps = gp.mx;
+                    uint8_t *wr = stage_base + gp.wres_off;
+                    if (gp.wres && !ptx::mbar_wait(w_full, 0, limit, abort)) {
+                        if (!*abort) give_up(abort, gp.status, kStatusTimeoutMma);
+                        ok = false;
+                    }
+                    for (int64_t t = blockIdx.x; ok && t < gp.num_tiles && !*abort; t += gridDim.x) {
+                        const int acc = grp % C::kAccBufs;
+                        const uint32_t acc_phase = (uint32_t)(grp / C::kAccBufs) & 1u;
+                        if (!ptx::mbar_wait(&tmem_empty[acc], acc_phase ^ 1u, limit, abort)) {
+                            if (!*abort) give_up(abort, gp.status, kStatusTimeoutMma);
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                        uint32_t accumulate = 0;
+                        for (int kc = 0; kc < gp.kb_per_tap; ++kc) {
+                            if (!ptx::mbar_wait(&full[stage], phase, limit, abort)) {
+                                if (!*abort) give_up(abort, gp.status, kStatusTimeoutMma);
+                                ok = false;
+                                break;
+                            }
+                            ptx::tc_fence_after();
+                            uint8_t *st = stage_base + stage * gp.stage_bytes;
+                            for (int g = 0; g < taps; ++g) {
+                                const uint64_t xd = ptx::sdesc_k<C::kSlice>(ptx::smem_u32(st + g * C::kSlice));
+                                const uint8_t *wsl = gp.wres ? wr + (g * gp.kb_per_tap + kc) * C::kWBytes
+                                                             : st + x_bytes + g * C::kWBytes;
+                                const uint64_t wd = ptx::sdesc_k<C::kSlice>(ptx::smem_u32(wsl));
+#pragma unroll
+                                for (int k = 0; k < C::kKSteps; ++k) {
+                                    const uint64_t dk = (uint64_t)(2 * k);
+                                    ptx::mma_f16(d_tmem, xd + dk, wd + dk, C::kIdesc, accumulate);
+                                    accumulate = 1u;
+                                }
+                            }
+                            ptx::mma_commit(&empty[stage]);
+                            if (++stage == nst) {
+                                stage = 0;
+                                phase ^= 1u;
+                            }
+                        }
+                        if (ok) ptx::mma_commit(&tmem_full[acc]);
+                        ++grp;
+                    }
+                }
+            }
+            for (int64_t t = blockIdx.x; !gp.xshare && ok && t < gp.num_tiles && !*abort; t += gridDim.x, ++items) {
                 const TileCoord tc = decode_tile((uint32_t)t, gp, BN);
                 for (int kb = tc.kb0, g = 0; ok && kb < tc.kb1; ++g) {
                     const int kb_end = min(kb + gp.kb_group, tc.kb1);
@@ -331,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
                             accumulate = 1u;
                         }
                         ptx::mma_commit(&empty[stage]);  // frees the stage once these MMAs finish
-                        if (++stage == C::kStages) {
+                        if (++stage == nst) {
                             stage = 0;
                             phase ^= 1u;
                         }
@@ -502,12 +607,14 @@ cudaError_t launch_inst(const ctr_plan_s *pl, const CUtensorMap *maps, const Gem
     static PerDeviceOnce once;
     cudaError_t ea = once.run(current_device(), cudaSuccess, [] {
         return cudaFuncSetAttribute(gemm_tc_kernel<P, BN, CHAIN>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBudget);
     });
     if (ea != cudaSuccess) return ea;
+    if (gp.nstages < 2 || gp.nstages > kGemmMaxStages || gp.smem_bytes > C::kSmemBudget)
+        return cudaErrorInvalidValue;
     const int64_t grid = std::min<int64_t>(gp.num_tiles, (int64_t)pl->num_sms * C::kCtas);
     const cudaError_t e = launch_pdl(gemm_tc_kernel<P, BN, CHAIN>, dim3((unsigned)grid),
-                                     dim3(kThreads), (size_t)C::kSmem, st, maps[0], maps[1],
+                                     dim3(kThreads), (size_t)gp.smem_bytes, st, maps[0], maps[1],
                                      maps[2], maps[3], gp);
     if (e != cudaSuccess) return e;
     count_launches(1);

@@ -415,7 +415,7 @@ ctr_status ctr_istft_create(ctr_istft_t *out, int64_t N, int64_t n_fft, int64_t 
                             int64_t frames, int64_t padding, int64_t output_padding, int dtype) {
     if (!out) return CTR_ERR_INVALID_ARG;
     *out = nullptr;
-    if (dtype != CTR_F32 && dtype != CTR_BF16) return CTR_ERR_INVALID_ARG;
+    if (dtype != CTR_F32 && dtype != CTR_BF16 && dtype != CTR_F16) return CTR_ERR_INVALID_ARG;
     if (N < 0 || frames < 0 || hop < 1 || padding < 0 || output_padding < 0 ||
         output_padding >= hop || !is_pow2(n_fft) || n_fft < 4 || n_fft > 8192)
         return CTR_ERR_INVALID_ARG;

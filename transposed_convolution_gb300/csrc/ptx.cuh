@@ -136,7 +136,8 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, cta_group::1.  kind::f16 (bf16 operands) or kind::tf32.
+// D[tmem] (+)= A[smem] * B[smem]^T, cta_group::1.  kind::f16 (bf16 or fp16 operands, both the
+// same) or kind::tf32.
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                         uint32_t idesc, uint32_t accumulate) {
     asm volatile(
@@ -239,11 +240,13 @@ __device__ __forceinline__ uint64_t sdesc_k(uint32_t smem_addr) {
 
 // Instruction descriptor for kind::f16 / kind::tf32 with an fp32 accumulator, both operands
 // K-major, dense: D format (1 = f32) in bits 4-5, A format in 7-9, B format in 10-12
-// (f16 kind: 1 = bf16; tf32 kind: 2 = tf32), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+// (f16 kind: 0 = fp16, 1 = bf16; tf32 kind: 2 = tf32), N >> 3 in bits 17-22, M >> 4 in
+// bits 24-28.  A and B always have the same format.
 __host__ __device__ constexpr uint32_t idesc_f32acc(uint32_t ab_format, int M, int N) {
     return (1u << 4) | (ab_format << 7) | (ab_format << 10) |
            (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
+constexpr uint32_t kFmtF16 = 0;
 constexpr uint32_t kFmtBF16 = 1;
 constexpr uint32_t kFmtTF32 = 2;
 

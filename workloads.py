@@ -43,7 +43,7 @@ class Layer:
     stride: Tuple[int, ...]
     padding: Tuple[int, ...]
     output_padding: Tuple[int, ...]
-    dtype: str = "f32"              # "f32" or "bf16"
+    dtype: str = "f32"              # "f32", "bf16" or "f16"
     bias: bool = True
     act_slope: Optional[float] = None   # LeakyReLU negative slope, None = no activation
     weight: str = "uniform"          # "uniform" or "istft"
@@ -140,8 +140,15 @@ def to_bf16_values(a: np.ndarray) -> np.ndarray:
 
 
 def _cast(a: np.ndarray, dtype: str) -> np.ndarray:
+    """Values drawn in double, rounded to fp32, then (bf16, f16) to the 16-bit I/O type, ties
+    to even; returned as float32 holding those values."""
     a32 = np.asarray(a, dtype=np.float64).astype(np.float32)
-    return to_bf16_values(a32) if dtype == "bf16" else a32
+    if dtype == "bf16":
+        return to_bf16_values(a32)
+    if dtype == "f16":
+        with np.errstate(over="ignore"):
+            return a32.astype(np.float16).astype(np.float32)
+    return a32
 
 
 def hann_window(n_fft: int) -> np.ndarray:
