@@ -323,6 +323,32 @@ ctr_status ctr_plan_set_tile(ctr_plan_t plan, int block_n);
  */
 ctr_status ctr_plan_chain(ctr_plan_t plan, ctr_plan_t next);
 
+/*
+ * Run a chained pair of layers -- plan and the plan it is chained to (ctr_plan_chain) -- as
+ * one kernel that keeps the first layer's output in shared memory as the second layer's
+ * operand, instead of writing it to the second plan's staged input and reading it back
+ * (the two-layer stack of "[XNNPACK] Lower dense transposed convs as one polyphase conv +
+ * depth to space", Test plan).  The result is bit-identical to ctr_forward(plan, x, ...)
+ * followed by ctr_forward(next, NULL, ...).
+ *   x            plan's input as for ctr_forward (NULL when a chained previous plan staged it)
+ *   w_packed, bias        plan's packed weight and bias
+ *   next_w_packed, next_bias   the next plan's
+ *   y            the next plan's output
+ * Needs (CTR_ERR_UNSUPPORTED otherwise, see ctr_plan_fusable): 1-D, bf16 or fp16, both on
+ * the polyphase path without split-K; plan with stride >= 2 and exactly 64 output channels
+ * in one tile of 128 phase rows; next with 64 input channels, one row tile of 64 or 128
+ * rows, an NCHW output and no further chain.  Both plans prepacked (CTR_ERR_NOT_PREPARED)
+ * and plan's workspace bound (CTR_ERR_NO_WORKSPACE); the next plan's workspace is not used.
+ * Asynchronous on stream; device-side timeouts are reported by ctr_plan_check(plan, ...).
+ * No counterpart of the call itself on the pages.
+ */
+ctr_status ctr_forward_fused(ctr_plan_t plan, const void *x, const void *w_packed,
+                             const void *bias, const void *next_w_packed,
+                             const void *next_bias, void *y, void *stream);
+
+/* 1 when ctr_forward_fused can run plan and the plan it is chained to, else 0. */
+int ctr_plan_fusable(ctr_plan_t plan);
+
 /* The path the plan will run (a ctr_path other than AUTO), or -1 for a NULL plan. */
 int ctr_plan_get_path(ctr_plan_t plan);
 

@@ -24,16 +24,22 @@ def to_dev(a, dtype: str):
 
 def run_plan(x, w, bias, stride, padding, output_padding, dtype="f32", slope=None,
              path=ctr.CTR_PATH_AUTO, split_k=0, check_guards=True, expect_path=None, block_n=0,
-             groups=1, dilation=1, padding_end=None, phase_origin=ctr.CTR_PHASE_AUTO):
+             groups=1, dilation=1, padding_end=None, phase_origin=ctr.CTR_PHASE_AUTO,
+             layout="nchw"):
     """Run one ConvTranspose through the library.  x, w, bias: numpy arrays holding values of
-    the I/O dtype.  Returns (y as float64 numpy, plan description)."""
+    the I/O dtype, x in NCHW order (transposed to channels last on the way in, and y back,
+    when layout is "nhwc").  Returns (y as float64 numpy in NCHW order, plan description)."""
     x = np.asarray(x)
     ndim = x.ndim - 2
     plan = ctr.Plan(x.shape[0], x.shape[1], w.shape[1] * groups, tuple(x.shape[2:]),
                     tuple(w.shape[2:]), stride, padding, output_padding, dtype=tdtype(dtype),
                     negative_slope=slope, path=path, split_k=split_k, block_n=block_n,
                     groups=groups, dilation=dilation, padding_end=padding_end,
-                    phase_origin=phase_origin)
+                    phase_origin=phase_origin, layout=layout)
+    to_last = (0,) + tuple(range(2, 2 + ndim)) + (1,)
+    to_first = (0, 1 + ndim) + tuple(range(1, 1 + ndim))
+    if layout == "nhwc":
+        x = np.ascontiguousarray(np.transpose(x, to_last))
     try:
         if expect_path is not None:
             assert plan.path == expect_path, plan.describe()
@@ -47,6 +53,8 @@ def run_plan(x, w, bias, stride, padding, output_padding, dtype="f32", slope=Non
             g = torch.cat([buf[:GUARD], buf[GUARD + n:]]).float().cpu().numpy()
             assert np.all(np.isnan(g)), "library wrote outside y"
         out = y.float().cpu().numpy().astype(np.float64)
+        if layout == "nhwc":
+            out = np.ascontiguousarray(np.transpose(out, to_first))
         return out, plan.describe()
     finally:
         plan.close()

@@ -422,6 +422,45 @@ def test_f16_plans_without_gpu(ctr):
     assert ctr.lib.ctr_plan_create(*args) == ctr.CTR_ERR_INVALID_ARG
 
 
+def test_layout_without_gpu(ctr):
+    """ctr_plan_set_layout: NHWC keeps the path and sizes of the tensor-core and gather paths;
+    a grouped depthwise geometry goes to gather; streaming and a forced depthwise path refuse
+    it and stay as they were; an unknown value is invalid."""
+    f32, bf = ctr.CTR_F32, ctr.CTR_BF16
+    h = _plan(ctr, 1, 1, 512, 256, [2000], [16], [8], [4], [0], f32)
+    try:
+        ws = ctr.ctr_workspace_bytes(h)
+        ctr.ctr_plan_set_layout(h, ctr.CTR_LAYOUT_NHWC)
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_POLYPHASE
+        assert ctr.ctr_workspace_bytes(h) == ws and " nhwc" in ctr.ctr_plan_describe(h)
+        assert ctr.lib.ctr_plan_set_layout(h, 2) == ctr.CTR_ERR_INVALID_ARG
+        ctr.ctr_plan_set_layout(h, ctr.CTR_LAYOUT_NCHW)
+        assert " nhwc" not in ctr.ctr_plan_describe(h)
+    finally:
+        ctr.ctr_plan_destroy(h)
+    h = _plan(ctr, 2, 1, 16, 16, [9, 12], [4, 4], [2, 2], [1, 1], [0, 0], bf)
+    try:
+        ctr.ctr_plan_set_groups(h, 16)
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_DEPTHWISE
+        ctr.ctr_plan_set_layout(h, ctr.CTR_LAYOUT_NHWC)
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_GATHER
+        ctr.ctr_plan_set_layout(h, ctr.CTR_LAYOUT_NCHW)
+        ctr.ctr_plan_set_path(h, ctr.CTR_PATH_DEPTHWISE, 0)
+        assert ctr.lib.ctr_plan_set_layout(h, ctr.CTR_LAYOUT_NHWC) == ctr.CTR_ERR_UNSUPPORTED
+        assert ctr.ctr_plan_get_path(h) == ctr.CTR_PATH_DEPTHWISE
+    finally:
+        ctr.ctr_plan_destroy(h)
+    h = _plan(ctr, 1, 1, 64, 32, [50], [16], [8], [0], [0], bf)
+    try:
+        ctr.ctr_plan_set_streaming(h, 1)
+        assert ctr.lib.ctr_plan_set_layout(h, ctr.CTR_LAYOUT_NHWC) == ctr.CTR_ERR_UNSUPPORTED
+        ctr.ctr_plan_set_streaming(h, 0)
+        ctr.ctr_plan_set_layout(h, ctr.CTR_LAYOUT_NHWC)
+        assert ctr.lib.ctr_plan_set_streaming(h, 1) == ctr.CTR_ERR_UNSUPPORTED
+    finally:
+        ctr.ctr_plan_destroy(h)
+
+
 def test_auto_pad_without_gpu(ctr):
     """ONNX auto_pad / output_shape resolve into front and back pads: SAME_* give
     L_in * stride outputs with an odd total padding's extra sample at the end (UPPER) or in

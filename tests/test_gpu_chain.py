@@ -202,6 +202,37 @@ def test_integer_chain_bit_exact(case):
             pl.close()
 
 
+def test_chained_split_k_ragged_channels_bit_exact():
+    """A chained producer with split-K and a channel count that leaves the last phase-major
+    row tile partly empty (40 channels in tiles of 16): the reduce must visit every packed
+    row, since the last tile's channels are spread over its whole width."""
+    rng = np.random.default_rng(67)
+    for dtype in ("f32", "bf16"):
+        p1 = ctr.Plan(2, 150, 40, (300,), (8,), 4, 2, 0, dtype=tdtype(dtype), split_k=3,
+                      path=ctr.CTR_PATH_POLYPHASE)
+        p2 = ctr.Plan(2, 40, 64, p1.out_spatial, (4,), 2, 1, 0, dtype=tdtype(dtype))
+        try:
+            p1.chain(p2)
+            x = rng.integers(-1, 2, (2, 150, 300)).astype(np.float32)
+            w1 = rng.integers(-1, 2, (150, 40, 8)).astype(np.float32)
+            w2 = rng.integers(-1, 2, (40, 64, 4)).astype(np.float32)
+            b1 = rng.integers(-1, 2, 40).astype(np.float32)
+            b2 = rng.integers(-1, 2, 64).astype(np.float32)
+            p1.prepack(to_dev(w1, dtype))
+            p2.prepack(to_dev(w2, dtype))
+            y = torch.full(p2.out_shape, float("nan"), dtype=tdtype(dtype), device="cuda")
+            p1.forward(to_dev(x, dtype), to_dev(b1, dtype))
+            p2.forward(None, to_dev(b2, dtype), y=y)
+            p1.check()
+            p2.check()
+            h = reference(x, w1, b1, 4, 2, 0, dtype)
+            np.testing.assert_array_equal(y.float().cpu().numpy(), reference(h, w2, b2, 2, 1, 0, dtype),
+                                          err_msg="%s | %s" % (p1.describe(), p2.describe()))
+        finally:
+            p1.close()
+            p2.close()
+
+
 def test_vocoder_stack_chained_full_size():
     """The four bf16 upsamplers of the vocoder stack (512 -> 32 channels, 1024 -> 262144
     samples, LeakyReLU(0.1) after the first three), chained as the benchmark runs them,

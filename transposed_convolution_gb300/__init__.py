@@ -10,7 +10,8 @@ Low level (same names as the C ABI): ``ctr_plan_create``, ``ctr_plan_set_activat
 ``ctr_plan_set_auto_pad``, ``ctr_plan_set_layout``, ``ctr_plan_set_streaming``, ``ctr_plan_stream_reset``,
 ``ctr_plan_set_tile``, ``ctr_plan_set_phase_origin``, ``ctr_plan_chain``, ``ctr_plan_get_path``, ``ctr_plan_output_shape``,
 ``ctr_packed_weight_bytes``, ``ctr_workspace_bytes``, ``ctr_plan_bind_workspace``,
-``ctr_prepack_weight``, ``ctr_forward``, ``ctr_forward_noalloc``, ``ctr_plan_check``,
+``ctr_prepack_weight``, ``ctr_forward``, ``ctr_forward_noalloc``, ``ctr_forward_fused``,
+``ctr_plan_fusable``, ``ctr_plan_check``,
 ``ctr_plan_set_wait_limit_ns``,
 ``ctr_plan_set_timing_events``, ``ctr_plan_describe``, ``ctr_plan_destroy``,
 ``ctr_status_string``, ``ctr_launch_count``.
@@ -89,6 +90,8 @@ SIGNATURES = {
     "ctr_prepack_weight": (ctypes.c_int, [_vp, _vp, _vp, _vp]),
     "ctr_forward": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp]),
     "ctr_forward_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp]),
+    "ctr_forward_fused": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "ctr_plan_fusable": (ctypes.c_int, [_vp]),
     "ctr_plan_check": (ctypes.c_int, [_vp, _vp]),
     "ctr_plan_set_wait_limit_ns": (ctypes.c_int, [_vp, ctypes.c_uint64]),
     "ctr_plan_set_timing_events": (ctypes.c_int, [_vp, _vp, _vp]),
@@ -265,6 +268,16 @@ def ctr_forward_noalloc(plan, x_ptr, w_ptr, bias_ptr, y_ptr, stream):
     passed in its torch layout and packed on every call (see include/ctr.h)."""
     _check(lib.ctr_forward_noalloc(plan, x_ptr, w_ptr, bias_ptr, y_ptr, stream),
            "ctr_forward_noalloc")
+
+
+def ctr_forward_fused(plan, x_ptr, w_packed_ptr, bias_ptr, next_w_packed_ptr, next_bias_ptr,
+                      y_ptr, stream):
+    _check(lib.ctr_forward_fused(plan, x_ptr, w_packed_ptr, bias_ptr, next_w_packed_ptr,
+                                 next_bias_ptr, y_ptr, stream), "ctr_forward_fused")
+
+
+def ctr_plan_fusable(plan) -> bool:
+    return bool(lib.ctr_plan_fusable(plan))
 
 
 def ctr_plan_check(plan, stream):
@@ -493,6 +506,34 @@ class Plan:
             y = self._checked(y, self.out_shape, "y")
         ctr_forward(self.handle, _ptr(x), _ptr(self.w_packed), _ptr(bias), _ptr(y),
                     _stream_ptr(stream))
+        return y
+
+    @property
+    def fusable(self):
+        """Whether forward_fused can run this plan and the plan it is chained to."""
+        return ctr_plan_fusable(self.handle)
+
+    def forward_fused(self, x, bias=None, next_bias=None, y=None, stream=None):
+        """This plan and the chained next plan in one kernel (ctr_forward_fused): the same
+        result as forward(x, bias) then next_plan.forward(None, next_bias, y)."""
+        torch = _torch()
+        nxt = self.next_plan
+        if nxt is None:
+            raise ValueError("forward_fused needs a chained next plan")
+        if self.w_packed is None or nxt.w_packed is None:
+            raise RuntimeError("forward_fused before prepack")
+        if x is not None or self.prev_plan is None:
+            x = self._checked(x, self.in_shape, "x")
+        if bias is not None:
+            bias = self._checked(bias, (self.C_out,), "bias")
+        if next_bias is not None:
+            next_bias = nxt._checked(next_bias, (nxt.C_out,), "next_bias")
+        if y is None:
+            y = torch.empty(nxt.out_shape, dtype=nxt.dtype, device=nxt.device)
+        else:
+            y = nxt._checked(y, nxt.out_shape, "y")
+        ctr_forward_fused(self.handle, _ptr(x), _ptr(self.w_packed), _ptr(bias),
+                          _ptr(nxt.w_packed), _ptr(next_bias), _ptr(y), _stream_ptr(stream))
         return y
 
     def stream_reset(self, stream=None):

@@ -1120,6 +1120,38 @@ ctr_status ctr_forward(ctr_plan_t pl, const void *x, const void *w_packed, const
     return e == cudaSuccess ? CTR_OK : CTR_ERR_CUDA;
 }
 
+int ctr_plan_fusable(ctr_plan_t pl) { return pl && ctr::fused_pair_supported(pl) ? 1 : 0; }
+
+ctr_status ctr_forward_fused(ctr_plan_t pl, const void *x, const void *w_packed, const void *bias,
+                             const void *next_w_packed, const void *next_bias, void *y,
+                             void *stream) {
+    if (!pl || !pl->chain_next) return CTR_ERR_INVALID_ARG;
+    ctr_plan_s *nx = pl->chain_next;
+    if (!pl->prepared || !nx->prepared) return CTR_ERR_NOT_PREPARED;
+    if (!ctr::fused_pair_supported(pl)) return CTR_ERR_UNSUPPORTED;
+    const bool staged_in = !x && pl->chain_prev != nullptr;
+    if (!w_packed || !next_w_packed || !y) return CTR_ERR_INVALID_ARG;
+    if (!x && !staged_in && pl->B * pl->C_in * pl->in[0] * pl->in[1] > 0)
+        return CTR_ERR_INVALID_ARG;
+    if ((x && !aligned16(x)) || !aligned16(w_packed) || !aligned16(next_w_packed) ||
+        !aligned16(y) || (bias && !aligned16(bias)) || (next_bias && !aligned16(next_bias)))
+        return CTR_ERR_MISALIGNED;
+    if (!pl->ws || pl->ws_bytes < pl->ws_bytes_needed) return CTR_ERR_NO_WORKSPACE;
+    if (pl->B == 0) return CTR_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(pl->ws);
+    void *xs = ws + pl->ws_off_stage;
+    cudaError_t e = cudaSuccess;
+    if (!staged_in)
+        e = pl->nhwc ? ctr::launch_stage_nhwc(pl, x, xs, st) : ctr::launch_stage_x(pl, x, xs, st);
+    if (e != cudaSuccess) return CTR_ERR_CUDA;
+    if (pl->ev_before && ctr::record_timing(pl->ev_before, st) != cudaSuccess) return CTR_ERR_CUDA;
+    e = ctr::launch_fused_pair(pl, xs, w_packed, bias, next_w_packed, next_bias, y, st);
+    if (e != cudaSuccess) return CTR_ERR_CUDA;
+    if (pl->ev_after && ctr::record_timing(pl->ev_after, st) != cudaSuccess) return CTR_ERR_CUDA;
+    return CTR_OK;
+}
+
 ctr_status ctr_plan_chain(ctr_plan_t pl, ctr_plan_t nx) {
     if (!pl || pl->prepared) return CTR_ERR_INVALID_ARG;   // the packed row order depends on it
     if (!nx) {

@@ -766,7 +766,11 @@ cudaError_t launch_splitk_reduce(const ctr_plan_s *pl, const float *raw, const E
                                  int64_t raw_ld, int64_t split_stride, cudaStream_t st) {
     const int64_t n_rows = pl->N_total;
     const int64_t n_pad = round_up(n_rows, 32);
-    const int64_t r_chunks = ceil_div(std::min<int64_t>(pl->M_rows, raw_ld), 32);
+    // Channel-major rows: the first M_rows rows hold every output.  Phase-major rows (a
+    // chained or channels-last output) spread the last tile's channels over its whole width,
+    // so every packed row is visited; the output stage skips the padding channels.
+    const int64_t r_rows = pl->row_pm ? raw_ld : std::min<int64_t>(pl->M_rows, raw_ld);
+    const int64_t r_chunks = ceil_div(r_rows, 32);
     const int64_t total = n_pad * r_chunks;
     if (n_rows == 0 || r_chunks == 0) return cudaSuccess;
     cudaError_t e = prefer_max_smem<splitk_reduce_kernel>();

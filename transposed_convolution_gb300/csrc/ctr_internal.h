@@ -283,6 +283,13 @@ cudaError_t run_tc_path(const ctr_plan_s *pl, const void *x, const void *w_packe
                         cudaEvent_t ev_before, cudaEvent_t ev_after, cudaStream_t st,
                         const ctr_plan_s *chained_to = nullptr, bool staged_in = false);
 
+// Two chained 1-D layers in one kernel (fused_pair.cu): whether a plan and the plan it is
+// chained to qualify, and the launch (xs: the first plan's staged input).
+bool fused_pair_supported(const ctr_plan_s *a);
+cudaError_t launch_fused_pair(const ctr_plan_s *a, const void *xs, const void *wa_packed,
+                              const void *bias_a, const void *wb_packed, const void *bias_b,
+                              void *y, cudaStream_t st);
+
 // Counter of launched kernels (monotonic, process-wide).
 void count_launches(uint64_t n);
 // Device address of ctr_forward_noalloc's status word on the current device, or nullptr when
