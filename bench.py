@@ -314,6 +314,18 @@ def measure_workload(name, args, env, headline):
         set_bytes += p.packed_bytes + p.workspace_bytes
         if p.next_plan is None:   # a chained layer's y is never written
             set_bytes += int(np.prod(p.out_shape)) * L.elem_bytes
+    # Launch groups: a chained pair the library can run as one kernel (ctr_forward_fused)
+    # runs fused unless --no-fuse; every other layer is a group of its own.
+    groups, i = [], 0
+    while i < len(probe):
+        p = probe[i]
+        if (args.fuse and p.next_plan is not None and i + 1 < len(probe)
+                and p.next_plan is probe[i + 1] and p.fusable):
+            groups.append((i, i + 1))
+            i += 2
+        else:
+            groups.append((i,))
+            i += 1
     for p in probe:
         p.close()
     nsets = max(2, int(math.ceil(2.0 * l2 / set_bytes)) + 1)
@@ -338,16 +350,26 @@ def measure_workload(name, args, env, headline):
 
     def run_set(s, x=None, kevs=None):
         inp = s["x"] if x is None else x
-        for li_idx, p in enumerate(s["plans"]):
+        for gi, grp in enumerate(groups):
+            li_idx = grp[0]
+            p = s["plans"][li_idx]
             if kevs is not None:
-                p.set_timing_events(kevs[li_idx][0].cuda_event, kevs[li_idx][1].cuda_event)
-            if p.next_plan is not None:
+                p.set_timing_events(kevs[gi][0].cuda_event, kevs[gi][1].cuda_event)
+            if len(grp) == 2:
+                last = grp[1]
+                nxt = s["plans"][last]
+                if nxt.next_plan is not None:
+                    raise RuntimeError("a fused pair ends a chain")
+                p.forward_fused(inp, s["b"][li_idx], s["b"][last], y=s["y"][last])
+                inp = s["y"][last]
+            elif p.next_plan is not None:
                 p.forward(inp, s["b"][li_idx])
+                inp = None
             else:
                 p.forward(inp, s["b"][li_idx], y=s["y"][li_idx])
+                inp = s["y"][li_idx]
             if kevs is not None:
                 p.set_timing_events(None, None)
-            inp = None if p.next_plan is not None else s["y"][li_idx]
         return inp
 
     for i in range(args.warmup):
@@ -358,7 +380,7 @@ def measure_workload(name, args, env, headline):
             p.check()
 
     K = args.steps
-    nl = len(Ls)
+    nl = len(groups)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
     kev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -510,7 +532,7 @@ def measure_workload(name, args, env, headline):
             xin = got
         parity = max(errs)
 
-    paths = [p.path for p in sets[0]["plans"]]
+    paths = [sets[0]["plans"][g[0]].path for g in groups]
     describe = [p.describe() for p in sets[0]["plans"]]
     chained = sum(p.next_plan is not None for p in sets[0]["plans"])
     h2d = int(x_hosts[0].numel() * x_hosts[0].element_size())
@@ -527,6 +549,7 @@ def measure_workload(name, args, env, headline):
         "plain_ms": plain_median, "kern_ms": kern_ms, "e2e_ms": e2e_ms, "n_e2e": n_e2e,
         "h2d": h2d, "d2h": d2h, "parity": parity, "paths": paths, "describe": describe,
         "chained": chained, "nsets": nsets, "set_bytes": set_bytes, "prepack_ms": prepack_ms,
+        "groups": groups,
         "launches": int(launches), "window": (soak_t0, wall1), "wall_timed": wall1 - wall0,
     }
 
@@ -549,18 +572,27 @@ def summarize(m, env):
     for L in Ls:
         pk, _ = layer_peak(L, peaks, peak_src, tf32)
         t_roof += max(t_tensor(L, pk), L.compulsory_bytes / (peaks["hbm_gbs"] * 1e9))
-    j = max(range(len(Ls)), key=lambda q: m["kern_ms"][q])
-    L = Ls[j]
+    # The dominant launch group (one kernel: a layer, or a fused pair of layers).  A fused
+    # pair's algorithmic bytes are its first layer's input, both weights and biases and its
+    # last layer's output: the intermediate is not moved.
+    groups = m["groups"]
+    j = max(range(len(groups)), key=lambda q: m["kern_ms"][q])
+    grp = groups[j]
+    L = Ls[grp[0]]
+    g_layers = [Ls[i] for i in grp]
+    g_macs = sum(x.useful_macs for x in g_layers)
+    g_bytes = (sum(x.compulsory_bytes for x in g_layers)
+               - sum(x.out_bytes for x in g_layers[:-1]) - sum(x.in_bytes for x in g_layers[1:]))
     pk, peak_note = layer_peak(L, peaks, peak_src, tf32)
-    tt = t_tensor(L, pk)
-    th = L.compulsory_bytes / (peaks["hbm_gbs"] * 1e9)
+    tt = 0.0 if L.kind == "istft" else 2.0 * g_macs / (pk * 1e12)
+    th = g_bytes / (peaks["hbm_gbs"] * 1e9)
     bound = "tensor" if tt >= th else "hbm"
     kern_s = m["kern_ms"][j] / 1e3
     if bound == "tensor":
-        achieved, peak, unit = 2.0 * L.useful_macs / kern_s / 1e12, pk, "TFLOP/s"
+        achieved, peak, unit = 2.0 * g_macs / kern_s / 1e12, pk, "TFLOP/s"
         nominal = peaks["bf16_tflops"] * TF32_OVER_BF16 / 3.0 if L.dtype == "f32" else pk
     else:
-        achieved, peak, unit = L.compulsory_bytes / kern_s / 1e9, peaks["hbm_gbs"], "GB/s"
+        achieved, peak, unit = g_bytes / kern_s / 1e9, peaks["hbm_gbs"], "GB/s"
         peak_note = "HBM copy bandwidth, %s" % peak_src
         nominal = peak
     path = m["paths"][j]
@@ -569,10 +601,12 @@ def summarize(m, env):
                  path, "gemm_tc_kernel")
     kfile = {ctr.CTR_PATH_GATHER: "gather", ctr.CTR_PATH_DEPTHWISE: "depthwise",
              -1: "istft"}.get(path, "gemm_tc")
-    traffic = profiled_traffic(m["name"], j, len(Ls), kfile)
+    traffic = profiled_traffic(m["name"], j, len(groups), kfile)
     roof = {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 2),
             "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic,
-            "kernel": kname, "layer": j, "kernel_us": round(m["kern_ms"][j] * 1e3, 3),
+            "kernel": kname if len(grp) == 1 else "fused_pair_kernel",
+            "layer": list(grp) if len(grp) > 1 else grp[0],
+            "kernel_us": round(m["kern_ms"][j] * 1e3, 3),
             "peak_source": peak_note + (", of measured" if peak_src == "measured" else
                                         ", of fallback")}
     if bound == "tensor" and L.dtype == "f32":
@@ -585,6 +619,7 @@ def summarize(m, env):
         "roofline_us": round(t_roof * 1e6, 3),
         "roofline": roof,
         "layer_kernel_us": [round(v * 1e3, 3) for v in m["kern_ms"]],
+        "launch_groups": [list(g) for g in groups],
         "parity_rel_l2": m["parity"],
         "parity_tolerance": 1e-2 if Ls[-1].dtype == "bf16" else 1e-5,
         "e2e_us_per_call": round(m["e2e_ms"] * 1e3, 3),
@@ -805,6 +840,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-chain", dest="chain", action="store_false",
                     help="run a stack's layers unchained (every intermediate in torch layout)")
+    ap.add_argument("--no-fuse", dest="fuse", action="store_false",
+                    help="run a fusable chained pair as two launches instead of one")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="time plain library calls instead of CUDA-graph replays of them")
     args = ap.parse_args()

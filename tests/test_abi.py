@@ -461,6 +461,44 @@ def test_layout_without_gpu(ctr):
         ctr.ctr_plan_destroy(h)
 
 
+def test_fusable_pairs_without_gpu(ctr):
+    """ctr_plan_fusable: a chained bf16/fp16 pair 128 -> 64 -> 32 with stride 2 qualifies;
+    fp32, a middle width other than 64, an unchained plan or a further chain do not; the
+    fused call refuses what does not qualify before launching anything."""
+    def pair(dt, c1=64, c2=32, k=4, s=2):
+        a = _plan(ctr, 1, 1, 128, c1, [500], [k], [s], [1], [0], dt)
+        b = _plan(ctr, 1, 1, c1, c2, [ctr.ctr_plan_output_shape(a, 1)[0]], [4], [2], [1], [0], dt)
+        ctr.ctr_plan_chain(a, b)
+        return a, b
+    for dt, want in ((ctr.CTR_BF16, 1), (ctr.CTR_F16, 1), (ctr.CTR_F32, 0)):
+        a, b = pair(dt)
+        try:
+            assert ctr.lib.ctr_plan_fusable(a) == want, ctr.ctr_plan_describe(a)
+            assert ctr.lib.ctr_plan_fusable(b) == 0
+        finally:
+            ctr.ctr_plan_destroy(a)
+            ctr.ctr_plan_destroy(b)
+    a, b = pair(ctr.CTR_BF16, c1=32)
+    try:
+        assert ctr.lib.ctr_plan_fusable(a) == 0
+    finally:
+        ctr.ctr_plan_destroy(a)
+        ctr.ctr_plan_destroy(b)
+    a, b = pair(ctr.CTR_BF16)
+    c = _plan(ctr, 1, 1, 32, 64, [ctr.ctr_plan_output_shape(b, 1)[0]], [4], [2], [1], [0], ctr.CTR_BF16)
+    try:
+        ctr.ctr_plan_chain(b, c)
+        assert ctr.lib.ctr_plan_fusable(a) == 0      # the second plan feeds a third
+        p = ctypes.c_void_p(1 << 20)
+        assert ctr.lib.ctr_forward_fused(a, p, p, None, p, None, p, None) == ctr.CTR_ERR_NOT_PREPARED
+        ctr.ctr_plan_chain(a, None)
+        assert ctr.lib.ctr_forward_fused(a, p, p, None, p, None, p, None) == ctr.CTR_ERR_INVALID_ARG
+    finally:
+        ctr.ctr_plan_chain(b, None)
+        for h in (a, b, c):
+            ctr.ctr_plan_destroy(h)
+
+
 def test_auto_pad_without_gpu(ctr):
     """ONNX auto_pad / output_shape resolve into front and back pads: SAME_* give
     L_in * stride outputs with an odd total padding's extra sample at the end (UPPER) or in

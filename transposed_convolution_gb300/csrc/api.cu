@@ -93,8 +93,15 @@ int tf32_group() {
 // MMA time, its operand-load time and its output time, and the extra pass over split-K
 // partials.  3xTF32 at BN = 256 keeps its group sums in TMEM beside a single accumulator, so
 // the MMAs pause while each group is folded into the sums (~800 clocks).
+// The tile a plan needs to run as one half of a fused chained pair (ctr_forward_fused):
+// 128 rows for the first layer, its 64 channels x 2 phases in one tile; the second layer's
+// rows in one tile of 64 or 128; both without split-K.  0 when the plan is not half of a
+// pair of that shape (then the tile model chooses freely).
+int fused_pair_bn(const ctr_plan_s *pl);
+
 double choose_tiling(ctr_plan_s *pl, double epi_factor = 1.0) {
     const Prec prec = prec_of(pl);
+    const int pair_bn = fused_pair_bn(pl);
     const int group = prec == Prec::TF32x3 ? tf32_group() : kNoGroup;
     const int kb_total = (int)(pl->K_total * op_esize(pl) / ctr::kBKBytes);
     const int64_t num_p = std::max<int64_t>(1, ceil_div(pl->N_total, ctr::kBM));
@@ -104,9 +111,11 @@ double choose_tiling(ctr_plan_s *pl, double epi_factor = 1.0) {
     const int forced = pl->forced_split > 0 ? std::min(pl->forced_split, kb_total) : 0;
     for (int bn : {64, 128, 256}) {
         if (pl->forced_bn > 0 && bn != pl->forced_bn) continue;
+        if (pl->forced_bn == 0 && pair_bn > 0 && bn != pair_bn) continue;
         const int64_t num_r = std::max<int64_t>(1, ceil_div(pl->M_rows, bn));
         for (int sp = 1; sp <= 16; ++sp) {
             if (forced > 0 && sp != forced) continue;
+            if (forced == 0 && pair_bn > 0 && sp != 1) continue;
             if (sp > kb_total) break;
             if (sp > 1 && forced == 0 && kb_total / sp < 4) break;
             const double kbs = (double)ceil_div(kb_total, sp);
@@ -169,6 +178,23 @@ bool set_output_lengths(ctr_plan_s *pl) {
     pl->out[0] = out[0];
     pl->out[1] = out[1];
     return true;
+}
+
+// Whether a chained pair has the shape the fused kernel takes (fused_pair.cu checks the
+// rest, shared memory included): 16-bit 1-D polyphase layers, the first of stride 2 with 64
+// output channels, the second with 64 input channels, at most 128 phase rows, an NCHW
+// output and no further chain.
+bool fusable_shape(const ctr_plan_s *a, const ctr_plan_s *b) {
+    return a && b && a->dtype == b->dtype && a->dtype != CTR_F32 && a->ndim == 1 &&
+           b->ndim == 1 && a->path == CTR_PATH_POLYPHASE && b->path == CTR_PATH_POLYPHASE &&
+           a->s[1] == 2 && a->C_out == 64 && b->C_in == 64 && b->C_out * b->s[1] <= 128 &&
+           !b->chain_next && !b->nhwc && !a->streaming && a->dil[1] == 1 && b->dil[1] == 1;
+}
+
+int fused_pair_bn(const ctr_plan_s *pl) {
+    if (fusable_shape(pl, pl->chain_next)) return 128;
+    if (fusable_shape(pl->chain_prev, pl)) return pl->C_out * pl->s[1] <= 64 ? 64 : 128;
+    return 0;
 }
 
 // Phase geometry of the polyphase path per dimension (see ctr_plan_s): taps, halos, tap base,
@@ -1155,9 +1181,11 @@ ctr_status ctr_forward_fused(ctr_plan_t pl, const void *x, const void *w_packed,
 ctr_status ctr_plan_chain(ctr_plan_t pl, ctr_plan_t nx) {
     if (!pl || pl->prepared) return CTR_ERR_INVALID_ARG;   // the packed row order depends on it
     if (!nx) {
-        if (pl->chain_next) pl->chain_next->chain_prev = nullptr;
+        ctr_plan_s *old = pl->chain_next;
+        if (old) old->chain_prev = nullptr;
         pl->chain_next = nullptr;
         layout_plan(pl);
+        if (old && !old->prepared) layout_plan(old);
         return CTR_OK;
     }
     if (nx == pl || !chain_compatible(pl, nx) || pl->streaming || nx->streaming)
@@ -1168,6 +1196,7 @@ ctr_status ctr_plan_chain(ctr_plan_t pl, ctr_plan_t nx) {
     nx->chain_prev = pl;
     nx->chain_zeroed_ws = nullptr;
     layout_plan(pl);
+    if (!nx->prepared) layout_plan(nx);   // a fusable pair picks the fused kernel's tiles
     return CTR_OK;
 }
 

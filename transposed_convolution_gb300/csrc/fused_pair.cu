@@ -51,7 +51,7 @@ struct FusedParams {
     float slopeA;
     // layer B
     int tapsB, x_rows_B, c0B;
-    int64_t PB;
+    int64_t PB, QvB;
     EpiParams epiB;
     // shared memory: A's X stages, the resident weights, B's operand boxes, barriers
     int nstages, stage_bytes, wa_off, wb_off, bx_off, bar_off, smem_bytes;
@@ -390,7 +390,11 @@ __global__ void __launch_bounds__(kFThreads, 1)
             const int bb = n & 1;
             if (!warp_wait(&tB_full[bb], ((uint32_t)n >> 1) & 1u)) break;
             ptx::tc_fence_after();
-            const PosInfo ps = decode_pos(b * fp.PB + q0 + 32 * quad + lane, fp.epiB);
+            // A tile lies inside one batch item: its positions past the item's valid phase
+            // positions would otherwise decode as the next item's.
+            const int64_t qb = q0 + 32 * quad + lane;
+            PosInfo ps = decode_pos(b * fp.PB + qb, fp.epiB);
+            if (qb >= fp.QvB) ps.valid = false;
 #pragma unroll 1
             for (int c = 0; c < BNB / 32; ++c) {
                 uint32_t u[32];
@@ -513,6 +517,7 @@ cudaError_t launch_fused_pair(const ctr_plan_s *a, const void *xs, const void *w
     fp.tapsB = (int)b->m[1];
     fp.c0B = (int)(b->rb[1] - b->hf[1]);
     fp.PB = b->P[1];
+    fp.QvB = b->Qv[1];
     fp.epiB = make_epi(b, bias_b, y);
     fp.status = a->d_status;
     fp.wait_limit_ns = a->wait_limit_ns;

@@ -82,6 +82,16 @@ class Layer:
         ny = self.B * self.C_out * int(np.prod(self.out_sp))
         return e * (nx + nw + nb + ny)
 
+    @property
+    def in_bytes(self) -> int:
+        """x in the I/O dtype."""
+        return self.elem_bytes * self.B * self.C_in * int(np.prod(self.in_sp))
+
+    @property
+    def out_bytes(self) -> int:
+        """y in the I/O dtype."""
+        return self.elem_bytes * self.B * self.C_out * int(np.prod(self.out_sp))
+
     def describe(self) -> str:
         dims = "x".join(str(v) for v in self.in_sp)
         ks = "x".join(str(v) for v in self.kernel)
