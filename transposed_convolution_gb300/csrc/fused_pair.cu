@@ -13,11 +13,13 @@
 //               tap shifts);
 //   warp 1      issues A's MMAs for tile t, then B's MMAs for tile t - 1, so the tensor
 //               cores run A while the mid warps convert the previous tile;
-//   warps 2..5  ("mid") read A's accumulator, add A's bias, apply its activation, round to
+//   warps 2..9  ("mid") read A's accumulator, add A's bias, apply its activation, round to
 //               the I/O type and write the values as B's K-major, 128-byte-swizzled operand
 //               box in shared memory: row r holds A's output a0 + r (zeros outside A's
-//               output), every channel of it (one 128-byte row);
-//   warps 6..9  run B's output stage (epilogue.cuh) on B's accumulator.
+//               output), every channel of it (one 128-byte row); two warps per TMEM lane
+//               quarter, one phase each;
+//   warps 10..17 run B's output stage (epilogue.cuh) on B's accumulator, two warps per lane
+//               quarter splitting its columns.
 // Both MMAs read their operand boxes through descriptors that start tap rows further down
 // (a K-major 128-byte-swizzled operand may start at any row of its 1024-byte-aligned box).
 // The result is bit-identical to the two chained launches: the same products in the same
@@ -36,7 +38,9 @@
 namespace ctr {
 namespace {
 
-constexpr int kFThreads = 320;
+constexpr int kFThreads = 576;
+constexpr int kMidWarps = 8;     // warps 2..9
+constexpr int kOutWarps = 8;     // warps 10..17
 constexpr int kFMaxStages = 8;
 constexpr int kRowBytes = 128;   // one K slice of 64 16-bit channels
 constexpr uint64_t kFDrainNs = 2000000000ull;
@@ -166,11 +170,11 @@ __global__ void __launch_bounds__(kFThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(&tA_full[a], 1);
-            ptx::mbar_init(&tA_empty[a], 4);
-            ptx::mbar_init(&bx_full[a], 4);
+            ptx::mbar_init(&tA_empty[a], kMidWarps);
+            ptx::mbar_init(&bx_full[a], kMidWarps);
             ptx::mbar_init(&bx_free[a], 1);
             ptx::mbar_init(&tB_full[a], 1);
-            ptx::mbar_init(&tB_empty[a], 4);
+            ptx::mbar_init(&tB_empty[a], kOutWarps);
         }
         ptx::mbar_init(w_full, 1);
         ptx::mbar_init(drain, 1);
@@ -247,21 +251,22 @@ __global__ void __launch_bounds__(kFThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            bool ok = ptx::mbar_wait(w_full, 0, limit, abort);
-            if (!ok && !*abort) f_give_up(abort, fp.status, kStatusTimeoutMma);
+        // The whole warp runs the loop; one elected lane issues each tcgen05 instruction.
+        {
+            bool ok = ptx::mbar_wait_warp(w_full, 0, limit, abort);
+            if (!ok && lane == 0 && !*abort) f_give_up(abort, fp.status, kStatusTimeoutMma);
             int stage = 0;
             uint32_t phase = 0;
             int na = 0, nb = 0;   // A and B tiles issued by this CTA
             auto issue_A = [&]() -> bool {
                 const int acc = na & 1;
-                if (!ptx::mbar_wait(&tA_empty[acc], (((uint32_t)na >> 1) & 1u) ^ 1u, limit, abort))
+                if (!ptx::mbar_wait_warp(&tA_empty[acc], (((uint32_t)na >> 1) & 1u) ^ 1u, limit, abort))
                     return false;
                 ptx::tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(acc * BNA);
                 uint32_t accumulate = 0;
                 for (int kc = 0; kc < fp.kbA_per_tap; ++kc) {
-                    if (!ptx::mbar_wait(&full[stage], phase, limit, abort)) return false;
+                    if (!ptx::mbar_wait_warp(&full[stage], phase, limit, abort)) return false;
                     ptx::tc_fence_after();
                     uint8_t *st = smem + stage * fp.stage_bytes;
                     for (int g = 0; g < fp.tapsA; ++g) {
@@ -270,25 +275,25 @@ __global__ void __launch_bounds__(kFThreads, 1)
                             ptx::smem_u32(wa + (g * fp.kbA_per_tap + kc) * BNA * kRowBytes));
 #pragma unroll
                         for (int k = 0; k < kKSteps; ++k) {
-                            ptx::mma_f16(d, xd + 2 * k, wd + 2 * k, kIdescA, accumulate);
+                            if (ptx::elect_one()) ptx::mma_f16(d, xd + 2 * k, wd + 2 * k, kIdescA, accumulate);
                             accumulate = 1u;
                         }
                     }
-                    ptx::mma_commit(&empty[stage]);
+                    if (ptx::elect_one()) ptx::mma_commit(&empty[stage]);
                     if (++stage == nst) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
-                ptx::mma_commit(&tA_full[acc]);
+                if (ptx::elect_one()) ptx::mma_commit(&tA_full[acc]);
                 ++na;
                 return true;
             };
             auto issue_B = [&]() -> bool {
                 const int bb = nb & 1;
                 const uint32_t par = ((uint32_t)nb >> 1) & 1u;
-                if (!ptx::mbar_wait(&bx_full[bb], par, limit, abort)) return false;
-                if (!ptx::mbar_wait(&tB_empty[bb], par ^ 1u, limit, abort)) return false;
+                if (!ptx::mbar_wait_warp(&bx_full[bb], par, limit, abort)) return false;
+                if (!ptx::mbar_wait_warp(&tB_empty[bb], par ^ 1u, limit, abort)) return false;
                 ptx::tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(2 * BNA + bb * BNB);
                 uint8_t *box = bx + bb * box_bytes;
@@ -298,27 +303,32 @@ __global__ void __launch_bounds__(kFThreads, 1)
                     const uint64_t wd = ptx::sdesc_k<kRowBytes>(ptx::smem_u32(wb + g * BNB * kRowBytes));
 #pragma unroll
                     for (int k = 0; k < kKSteps; ++k) {
-                        ptx::mma_f16(d, xd + 2 * k, wd + 2 * k, kIdescB, accumulate);
+                        if (ptx::elect_one()) ptx::mma_f16(d, xd + 2 * k, wd + 2 * k, kIdescB, accumulate);
                         accumulate = 1u;
                     }
                 }
-                ptx::mma_commit(&bx_free[bb]);
-                ptx::mma_commit(&tB_full[bb]);
+                if (ptx::elect_one()) {
+                    ptx::mma_commit(&bx_free[bb]);
+                    ptx::mma_commit(&tB_full[bb]);
+                }
                 ++nb;
                 return true;
             };
-            for (int t = blockIdx.x; ok && t < fp.num_tiles && !*abort; t += gridDim.x) {
+            for (int t = blockIdx.x; ok && t < fp.num_tiles && !ptx::abort_warp(abort); t += gridDim.x) {
                 ok = issue_A();
                 if (ok && na > 1) ok = issue_B();   // the previous tile's B
             }
             if (ok && nb < na) ok = issue_B();
-            if (!ok && !*abort) f_give_up(abort, fp.status, kStatusTimeoutMma);
-            ptx::mma_commit(drain);
-            if (!ptx::mbar_wait(drain, 0, kFDrainNs, nullptr)) atomicOr(fp.status, kStatusTimeoutDrain);
+            if (!ok && lane == 0 && !*abort) f_give_up(abort, fp.status, kStatusTimeoutMma);
+            if (ptx::elect_one()) ptx::mma_commit(drain);
+            __syncwarp();
+            if (!ptx::mbar_wait_warp(drain, 0, kFDrainNs, nullptr) && lane == 0)
+                atomicOr(fp.status, kStatusTimeoutDrain);
         }
-    } else if (warp < 6) {
+    } else if (warp < 2 + kMidWarps) {
         // ------------------------------------------------------------ mid: A -> B's operand
         const int quad = warp & 3;
+        const int half = (warp - 2) >> 2;   // which half of A's columns (one phase)
         const uint32_t lane_addr = (uint32_t)(32 * quad) << 16;
         const bool act = fp.actA == CTR_ACT_LEAKY_RELU;
         int n = 0;
@@ -343,7 +353,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
             uint8_t *box = bx + acc * box_bytes;
             const int64_t QA = qa0 + 32 * quad + lane;
 #pragma unroll 1
-            for (int c = 0; c < BNA / 32; ++c) {
+            for (int c = half * (BNA / 64); c < (half + 1) * (BNA / 64); ++c) {
                 uint32_t u[32];
                 ptx::tmem_ld_32x32b_x32(tmem_base + lane_addr + (uint32_t)(acc * BNA + 32 * c), u);
                 ptx::tmem_wait_ld_regs(u);
@@ -371,6 +381,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     } else {
         // ------------------------------------------------------------ final: B's output
         const int quad = warp & 3;
+        const int half = (warp - 2 - kMidWarps) >> 2;   // which half of B's columns
         const uint32_t lane_addr = (uint32_t)(32 * quad) << 16;
         constexpr int kIo = P == Prec::F16 ? kIoF16 : kIoBF16;
         int n = 0;
@@ -395,12 +406,13 @@ __global__ void __launch_bounds__(kFThreads, 1)
             const int64_t qb = q0 + 32 * quad + lane;
             PosInfo ps = decode_pos(b * fp.PB + qb, fp.epiB);
             if (qb >= fp.QvB) ps.valid = false;
+            constexpr int kCh = BNB / 64;   // chunks per warp
 #pragma unroll 1
-            for (int c = 0; c < BNB / 32; ++c) {
+            for (int c = half * kCh; c < (half + 1) * kCh; ++c) {
                 uint32_t u[32];
                 ptx::tmem_ld_32x32b_x32(tmem_base + lane_addr + (uint32_t)(2 * BNA + bb * BNB + 32 * c), u);
                 ptx::tmem_wait_ld_regs(u);
-                if (c == BNB / 32 - 1) {
+                if (c == (half + 1) * kCh - 1) {
                     ptx::tc_fence_before();
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(&tB_empty[bb]);

@@ -322,7 +322,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs the loop; one elected lane issues each tcgen05 instruction.
+        {
             int stage = 0;
             uint32_t phase = 0;
             int grp = 0;    // accumulator groups issued by this CTA (selects the TMEM buffer)
@@ -337,15 +338,15 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
                     const int x_bytes = gp.x_rows * C::kSlice;
                     const int taps = gp.mx;
                     uint8_t *wr = stage_base + gp.wres_off;
-                    if (gp.wres && !ptx::mbar_wait(w_full, 0, limit, abort)) {
-                        if (!*abort) give_up(abort, gp.status, kStatusTimeoutMma);
+                    if (gp.wres && !ptx::mbar_wait_warp(w_full, 0, limit, abort)) {
+                        if (lane == 0 && !*abort) give_up(abort, gp.status, kStatusTimeoutMma);
                         ok = false;
                     }
-                    for (int64_t t = blockIdx.x; ok && t < gp.num_tiles && !*abort; t += gridDim.x) {
+                    for (int64_t t = blockIdx.x; ok && t < gp.num_tiles && !ptx::abort_warp(abort); t += gridDim.x) {
                         const int acc = grp % C::kAccBufs;
                         const uint32_t acc_phase = (uint32_t)(grp / C::kAccBufs) & 1u;
-                        if (!ptx::mbar_wait(&tmem_empty[acc], acc_phase ^ 1u, limit, abort)) {
-                            if (!*abort) give_up(abort, gp.status, kStatusTimeoutMma);
+                        if (!ptx::mbar_wait_warp(&tmem_empty[acc], acc_phase ^ 1u, limit, abort)) {
+                            if (lane == 0 && !*abort) give_up(abort, gp.status, kStatusTimeoutMma);
                             ok = false;
                             break;
                         }
@@ -353,8 +354,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
                         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                         uint32_t accumulate = 0;
                         for (int kc = 0; kc < gp.kb_per_tap; ++kc) {
-                            if (!ptx::mbar_wait(&full[stage], phase, limit, abort)) {
-                                if (!*abort) give_up(abort, gp.status, kStatusTimeoutMma);
+                            if (!ptx::mbar_wait_warp(&full[stage], phase, limit, abort)) {
+                                if (lane == 0 && !*abort) give_up(abort, gp.status, kStatusTimeoutMma);
                                 ok = false;
                                 break;
                             }
@@ -368,22 +369,23 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
 #pragma unroll
                                 for (int k = 0; k < C::kKSteps; ++k) {
                                     const uint64_t dk = (uint64_t)(2 * k);
-                                    ptx::mma_f16(d_tmem, xd + dk, wd + dk, C::kIdesc, accumulate);
+                                    if (ptx::elect_one())
+                                        ptx::mma_f16(d_tmem, xd + dk, wd + dk, C::kIdesc, accumulate);
                                     accumulate = 1u;
                                 }
                             }
-                            ptx::mma_commit(&empty[stage]);
+                            if (ptx::elect_one()) ptx::mma_commit(&empty[stage]);
                             if (++stage == nst) {
                                 stage = 0;
                                 phase ^= 1u;
                             }
                         }
-                        if (ok) ptx::mma_commit(&tmem_full[acc]);
+                        if (ok && ptx::elect_one()) ptx::mma_commit(&tmem_full[acc]);
                         ++grp;
                     }
                 }
             }
-            for (int64_t t = blockIdx.x; !gp.xshare && ok && t < gp.num_tiles && !*abort; t += gridDim.x, ++items) {
+            for (int64_t t = blockIdx.x; !gp.xshare && ok && t < gp.num_tiles && !ptx::abort_warp(abort); t += gridDim.x, ++items) {
                 const TileCoord tc = decode_tile((uint32_t)t, gp, BN);
                 for (int kb = tc.kb0, g = 0; ok && kb < tc.kb1; ++g) {
                     const int kb_end = min(kb + gp.kb_group, tc.kb1);
@@ -391,15 +393,15 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
                     const int acc = grp % C::kAccBufs;
                     if (to_sum) {
                         // The previous tile's sums must have been read.
-                        if (!ptx::mbar_wait(sum_free, ((uint32_t)items & 1u) ^ 1u, limit, abort)) {
-                            if (!*abort) give_up(abort, gp.status, kStatusTimeoutMma);
+                        if (!ptx::mbar_wait_warp(sum_free, ((uint32_t)items & 1u) ^ 1u, limit, abort)) {
+                            if (lane == 0 && !*abort) give_up(abort, gp.status, kStatusTimeoutMma);
                             ok = false;
                             break;
                         }
                     } else {
                         const uint32_t acc_phase = (uint32_t)(grp / C::kAccBufs) & 1u;
-                        if (!ptx::mbar_wait(&tmem_empty[acc], acc_phase ^ 1u, limit, abort)) {
-                            if (!*abort) give_up(abort, gp.status, kStatusTimeoutMma);
+                        if (!ptx::mbar_wait_warp(&tmem_empty[acc], acc_phase ^ 1u, limit, abort)) {
+                            if (lane == 0 && !*abort) give_up(abort, gp.status, kStatusTimeoutMma);
                             ok = false;
                             break;
                         }
@@ -409,8 +411,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
                         tmem_base + (to_sum ? C::kSumCol : (uint32_t)(acc * BN));
                     uint32_t accumulate = 0;
                     for (; kb < kb_end; ++kb) {
-                        if (!ptx::mbar_wait(&full[stage], phase, limit, abort)) {
-                            if (!*abort) give_up(abort, gp.status, kStatusTimeoutMma);
+                        if (!ptx::mbar_wait_warp(&full[stage], phase, limit, abort)) {
+                            if (lane == 0 && !*abort) give_up(abort, gp.status, kStatusTimeoutMma);
                             ok = false;
                             break;
                         }
@@ -427,27 +429,32 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
                             // +2 in the descriptor's start-address field = +32 bytes
                             const uint64_t dk = (uint64_t)(2 * k);
                             if (P == Prec::TF32x3) {
-                                ptx::mma_tf32(d_tmem, xdl + dk, wd + dk, C::kIdesc, accumulate);
-                                ptx::mma_tf32(d_tmem, xd + dk, wdl + dk, C::kIdesc, 1u);
-                                ptx::mma_tf32(d_tmem, xd + dk, wd + dk, C::kIdesc, 1u);
+                                if (ptx::elect_one()) {
+                                    ptx::mma_tf32(d_tmem, xdl + dk, wd + dk, C::kIdesc, accumulate);
+                                    ptx::mma_tf32(d_tmem, xd + dk, wdl + dk, C::kIdesc, 1u);
+                                    ptx::mma_tf32(d_tmem, xd + dk, wd + dk, C::kIdesc, 1u);
+                                }
                             } else {
-                                ptx::mma_f16(d_tmem, xd + dk, wd + dk, C::kIdesc, accumulate);
+                                if (ptx::elect_one())
+                                    ptx::mma_f16(d_tmem, xd + dk, wd + dk, C::kIdesc, accumulate);
                             }
                             accumulate = 1u;
                         }
-                        ptx::mma_commit(&empty[stage]);  // frees the stage once these MMAs finish
+                        if (ptx::elect_one())
+                            ptx::mma_commit(&empty[stage]);  // frees the stage once these MMAs finish
                         if (++stage == nst) {
                             stage = 0;
                             phase ^= 1u;
                         }
                     }
-                    if (ok) ptx::mma_commit(to_sum ? sum_full : &tmem_full[acc]);
+                    if (ok && ptx::elect_one()) ptx::mma_commit(to_sum ? sum_full : &tmem_full[acc]);
                     if (!to_sum) ++grp;
                 }
             }
             // Every MMA issued above completes before TMEM is freed.
-            ptx::mma_commit(drain);
-            if (!ptx::mbar_wait(drain, 0, kDrainLimitNs, nullptr))
+            if (ptx::elect_one()) ptx::mma_commit(drain);
+            __syncwarp();
+            if (!ptx::mbar_wait_warp(drain, 0, kDrainLimitNs, nullptr) && lane == 0)
                 atomicOr(gp.status, kStatusTimeoutDrain);
         }
     } else {
