@@ -480,6 +480,11 @@ EpiParams make_epi(const ctr_plan_s *pl, const void *bias, void *y) {
             break;
         }
     }
+    // Runs of sx = 2 outputs at odd columns (px odd): each lane stores its second output with
+    // its right neighbour's first, an aligned pair, when rows keep that alignment (even Wout)
+    // and y is aligned to two elements.
+    e.shift2 = (e.kind == EPI_KIND_1D_S2 || e.kind == EPI_KIND_2D_S2x2) && (e.px & 1) &&
+               pl->out[1] % 2 == 0 && reinterpret_cast<uintptr_t>(y) % (2 * es) == 0;
     return e;
 }
 
@@ -1035,7 +1040,7 @@ ctr_status ctr_plan_describe(ctr_plan_t pl, char *buf, size_t len) {
         snprintf(buf, len,
                  "path=%s prec=%s rows=%lld(pad %lld, BN %d, %d tiles) positions=%lld(%d tiles) "
                  "K=%lld splits=%d group=%d tiles=%lld sms=%d S=%d/%d taps=%lldx%lld%s "
-                 "pitch=%lldx%lld epi=%d/%dB packed=%zu ws=%zu",
+                 "pitch=%lldx%lld epi=%d/%dB%s packed=%zu ws=%zu",
                  pname, pl->dtype == CTR_BF16 ? "bf16" : pl->dtype == CTR_F16 ? "f16" : "3xtf32",
                  (long long)pl->M_rows,
                  (long long)pl->M_pad, pl->block_n, pl->num_r_tiles, (long long)pl->N_total,
@@ -1044,6 +1049,8 @@ ctr_status ctr_plan_describe(ctr_plan_t pl, char *buf, size_t len) {
                  pl->num_sms, pl->S, pl->S_pad, (long long)pl->m[0], (long long)pl->m[1],
                  pl->out_phases ? " out-phases" : "",
                  (long long)pl->P[0], (long long)pl->P[1], ep.kind, ep.store_bytes,
+                 ep.shift2 && pl->path == CTR_PATH_POLYPHASE && !pl->chain_next && !pl->nhwc
+                     ? " pairs" : "",
                  pl->packed_bytes, pl->ws_bytes_needed);
     } else {
         snprintf(buf, len, "path=%s dtype=%s groups=%lld packed=%zu ws=0", pname,

@@ -51,6 +51,7 @@ struct EpiParams {
     float slope;
     int kind;           // EpiKind
     int store_bytes;    // width of the aligned vector stores of interior runs (16, 8, 4, 2)
+    int shift2;         // sx = 2 runs at odd columns stored as pairs across lanes (epilogue.cuh)
     // Chained output (out_staged = 1): y is the next plan's staged input, channels-last rows
     // of ys_cpad channels, output (oy, ox) of batch b at row (b*ys_Py + oy + ys_hy)*ys_Px +
     // ox + ys_hx; fp32 as tf32 hi and lo planes, ys_lo elements apart.

@@ -325,6 +325,64 @@ __device__ __forceinline__ void small_chunk_fast_act(float (&v)[32], T *__restri
         small_chunk_fast<T, SX, SY, VW, false>(v, dst, oc0, cstride, wout, e);
 }
 
+// Stride-2 columns with an odd px: a thread's two outputs of a row start at the odd column
+// x0 = 2 qx - px, so neither they nor any pair of them is aligned for a 2-element store.
+// Consecutive lanes hold consecutive qx of one output row, so the aligned pair (x0 + 1,
+// x0 + 2) is this lane's second output and the next lane's first: each lane takes its right
+// neighbour's first value by a shuffle and stores the pair at the even column x0 + 1.  A
+// first output no left neighbour covers (lane 0, qx = 0, or a neighbour whose pair fell
+// outside the row), and a second output with no pair, are stored alone.  Needs an even Wout
+// and y aligned to two elements (every pair column is then aligned); every lane runs the
+// channel and row loops for the shuffles, stores are predicated per lane.
+template <typename T, int SY>
+__device__ __forceinline__ void emit_small_shift2(float (&v)[32], const PosInfo &ps, int64_t r0,
+                                                  const EpiParams &e, int lane) {
+    constexpr int S = 2 * SY, G = 32 / S;
+    const int64_t oc0 = r0 / S;
+    const int64_t x0 = 2 * ps.qx - e.px;
+    const int64_t oy0 = (int64_t)SY * ps.qy - e.py;
+    // The next lane holds qx + 1 of the same row when this position is valid and qx + 1 is
+    // a valid column position (Qvx <= the row pitch Px, so the row does not change).
+    const bool next_adj = ps.valid && lane < 31 && ps.qx + 1 < e.Qvx;
+    const bool pair = next_adj && x0 + 1 >= 0 && x0 + 2 < e.Wout;
+    const bool prev_pair = __shfl_up_sync(0xffffffffu, pair, 1) && lane > 0;
+    const bool first = ps.valid && !prev_pair && x0 >= 0 && x0 < e.Wout;
+    const bool second = ps.valid && !pair && x0 + 1 >= 0 && x0 + 1 < e.Wout;
+    const bool any_single = __any_sync(0xffffffffu, first || second);
+    const float bl = lane_bias(e, oc0, G, lane);
+    const float slope_eff = slope_of(e);
+    const bool use_min = slope_eff > 1.0f;
+    const int64_t g_left = e.C_out - oc0;
+    const int gmax = g_left < G ? (int)g_left : G;
+    bool row_ok[SY];
+#pragma unroll
+    for (int jy = 0; jy < SY; ++jy) row_ok[jy] = ps.valid && oy0 + jy >= 0 && oy0 + jy < e.Hout;
+    const int64_t cstride = e.Hout * e.Wout;
+    T *__restrict__ dst = static_cast<T *>(e.y) + ((ps.b * e.C_out + oc0) * e.Hout + oy0) * e.Wout + x0;
+#pragma unroll
+    for (int g = 0; g < G; ++g, dst += cstride) {
+        if (g >= gmax) break;
+        const float bias = __shfl_sync(0xffffffffu, bl, g);
+#pragma unroll
+        for (int jy = 0; jy < SY; ++jy) {
+            const float a = leaky(v[g * S + 2 * jy] + bias, slope_eff, use_min);
+            const float b = leaky(v[g * S + 2 * jy + 1] + bias, slope_eff, use_min);
+            const float n = __shfl_down_sync(0xffffffffu, a, 1);
+            T *row = dst + jy * e.Wout;
+            if (row_ok[jy]) {
+                if (pair) {
+                    const float pv[2] = {b, n};
+                    store_vec<T, 2, 2 * (int)sizeof(T)>(row + 1, pv);
+                }
+                if (any_single) {
+                    if (first) row[0] = io_from_float<T>(a);
+                    if (second) row[1] = io_from_float<T>(b);
+                }
+            }
+        }
+    }
+}
+
 // Output stage for whole phase sets: S = S_pad = SX * SY <= 32 (SX, SY compile-time), so the
 // 32 columns r0 .. r0+31 of a chunk are G = 32/S whole channels.  Warp-collective: every
 // lane passes the same r0 (its own position in ps).
@@ -335,6 +393,12 @@ __device__ __forceinline__ void emit_small(float (&v)[32], const PosInfo &ps, in
     constexpr int G = 32 / S;
     constexpr int kRunBytes = SX * (int)sizeof(T);
     const int64_t oc0 = r0 / S;
+    if constexpr (SX == 2) {
+        if (e.shift2) {
+            emit_small_shift2<T, SY>(v, ps, r0, e, lane);
+            return;
+        }
+    }
     {
         const int64_t fx0 = (int64_t)SX * ps.qx - e.px, fy0 = (int64_t)SY * ps.qy - e.py;
         const bool inside = ps.valid && fx0 >= 0 && fx0 + SX <= e.Wout && fy0 >= 0 &&
