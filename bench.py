@@ -68,6 +68,7 @@ TF32_OVER_BF16 = 1.1 / 2.25
 # DRAM traffic is reported only while they are unchanged.
 KERNEL_SOURCES = {
     "gemm_tc": ["transposed_convolution_gb300/csrc/gemm_tc.cu",
+                "transposed_convolution_gb300/csrc/gemm_tc_f16.cu",
                 "transposed_convolution_gb300/csrc/epilogue.cuh",
                 "transposed_convolution_gb300/csrc/ptx.cuh",
                 "transposed_convolution_gb300/csrc/gemm_tc.cuh",
@@ -75,6 +76,9 @@ KERNEL_SOURCES = {
     "depthwise": ["transposed_convolution_gb300/csrc/depthwise.cu"],
     "istft": ["transposed_convolution_gb300/csrc/istft.cu"],
     "gather": ["transposed_convolution_gb300/csrc/aux_kernels.cu"],
+    "fused_pair": ["transposed_convolution_gb300/csrc/fused_pair.cu",
+                   "transposed_convolution_gb300/csrc/epilogue.cuh",
+                   "transposed_convolution_gb300/csrc/ptx.cuh"],
 }
 
 
@@ -102,8 +106,11 @@ def kernel_source_hash(kernel="gemm_tc"):
 
 
 def profiled_traffic(workload, layer=0, layers=1, kernel="gemm_tc"):
-    """DRAM bytes (read + written) per launch of a layer's main kernel from the committed ncu
-    summary, or None when there is none or the kernel sources changed since it was taken."""
+    """Bytes moved per launch of a launch group's main kernel from the committed ncu summary:
+    DRAM reads plus the sectors the SMs wrote into L2 (each written line reaches DRAM when
+    it is evicted; a partly written sector counts whole, so the write term is an upper
+    bound).  None when there is no summary or the kernel sources changed since it was
+    taken."""
     path = os.path.join(ROOT, "profiles", "%s_%s.md" % (kernel, workload))
     if kernel not in KERNEL_SOURCES or not os.path.exists(path):
         return None
@@ -601,6 +608,8 @@ def summarize(m, env):
                  path, "gemm_tc_kernel")
     kfile = {ctr.CTR_PATH_GATHER: "gather", ctr.CTR_PATH_DEPTHWISE: "depthwise",
              -1: "istft"}.get(path, "gemm_tc")
+    if len(grp) > 1:
+        kfile = "fused_pair"
     traffic = profiled_traffic(m["name"], j, len(groups), kfile)
     roof = {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 2),
             "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic,
