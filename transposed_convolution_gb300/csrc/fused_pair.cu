@@ -125,7 +125,10 @@ __device__ __forceinline__ void mid_chunk(float (&v)[32], uint8_t *box, int x_ro
     }
 }
 
-template <Prec P, int BNA, int BNB>
+// KIND: layer B's output-stage variant compiled alone (EPI_KIND_1D_S2, the stride-2 layers),
+// or -1 for the run-time dispatch over every variant.  One variant keeps the output warps'
+// code small.
+template <Prec P, int BNA, int BNB, int KIND>
 __global__ void __launch_bounds__(kFThreads, 1)
     fused_pair_kernel(const __grid_constant__ CUtensorMap mapXA,
                       const __grid_constant__ CUtensorMap mapWA,
@@ -420,7 +423,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 float v[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(u[i]);
-                emit_cols<kOutPlain, kIo>(v, ps, 32 * c, fp.epiB, lane);
+                if constexpr (KIND == EPI_KIND_1D_S2)
+                    emit_small<T, 2, 1>(v, ps, 32 * c, fp.epiB, lane);
+                else
+                    emit_cols<kOutPlain, kIo>(v, ps, 32 * c, fp.epiB, lane);
             }
         }
     }
@@ -435,17 +441,17 @@ __global__ void __launch_bounds__(kFThreads, 1)
     }
 }
 
-template <Prec P, int BNA, int BNB>
+template <Prec P, int BNA, int BNB, int KIND>
 cudaError_t launch_fused_inst(const ctr_plan_s *a, const CUtensorMap *maps, const FusedParams &fp,
                               cudaStream_t st) {
     static PerDeviceOnce once;
     cudaError_t e = once.run(current_device(), cudaSuccess, [] {
-        return cudaFuncSetAttribute(fused_pair_kernel<P, BNA, BNB>,
+        return cudaFuncSetAttribute(fused_pair_kernel<P, BNA, BNB, KIND>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     });
     if (e != cudaSuccess) return e;
     const int grid = std::min(fp.num_tiles, a->num_sms);
-    e = launch_pdl(fused_pair_kernel<P, BNA, BNB>, dim3((unsigned)grid), dim3(kFThreads),
+    e = launch_pdl(fused_pair_kernel<P, BNA, BNB, KIND>, dim3((unsigned)grid), dim3(kFThreads),
                    (size_t)fp.smem_bytes, st, maps[0], maps[1], maps[2], fp);
     if (e != cudaSuccess) return e;
     count_launches(1);
@@ -535,11 +541,18 @@ cudaError_t launch_fused_pair(const ctr_plan_s *a, const void *xs, const void *w
     fp.wait_limit_ns = a->wait_limit_ns;
     if (fp.num_tiles <= 0) return cudaSuccess;
     const bool f16 = a->dtype == CTR_F16;
+    if (fp.epiB.kind == EPI_KIND_1D_S2) {
+        if (b->block_n == 64)
+            return f16 ? launch_fused_inst<Prec::F16, 128, 64, EPI_KIND_1D_S2>(a, maps, fp, st)
+                       : launch_fused_inst<Prec::BF16, 128, 64, EPI_KIND_1D_S2>(a, maps, fp, st);
+        return f16 ? launch_fused_inst<Prec::F16, 128, 128, EPI_KIND_1D_S2>(a, maps, fp, st)
+                   : launch_fused_inst<Prec::BF16, 128, 128, EPI_KIND_1D_S2>(a, maps, fp, st);
+    }
     if (b->block_n == 64)
-        return f16 ? launch_fused_inst<Prec::F16, 128, 64>(a, maps, fp, st)
-                   : launch_fused_inst<Prec::BF16, 128, 64>(a, maps, fp, st);
-    return f16 ? launch_fused_inst<Prec::F16, 128, 128>(a, maps, fp, st)
-               : launch_fused_inst<Prec::BF16, 128, 128>(a, maps, fp, st);
+        return f16 ? launch_fused_inst<Prec::F16, 128, 64, -1>(a, maps, fp, st)
+                   : launch_fused_inst<Prec::BF16, 128, 64, -1>(a, maps, fp, st);
+    return f16 ? launch_fused_inst<Prec::F16, 128, 128, -1>(a, maps, fp, st)
+               : launch_fused_inst<Prec::BF16, 128, 128, -1>(a, maps, fp, st);
 }
 
 }  // namespace ctr
