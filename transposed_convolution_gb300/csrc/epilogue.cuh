@@ -341,9 +341,12 @@ __device__ __forceinline__ void emit_small_shift2(float (&v)[32], const PosInfo 
     const int64_t oc0 = r0 / S;
     const int64_t x0 = 2 * ps.qx - e.px;
     const int64_t oy0 = (int64_t)SY * ps.qy - e.py;
-    // The next lane holds qx + 1 of the same row when this position is valid and qx + 1 is
-    // a valid column position (Qvx <= the row pitch Px, so the row does not change).
-    const bool next_adj = ps.valid && lane < 31 && ps.qx + 1 < e.Qvx;
+    // The next lane holds qx + 1 of the same row when both positions are valid and qx + 1
+    // is a valid column position (Qvx <= the row pitch Px, so the row does not change).  The
+    // neighbour's own flag is asked for: a caller may mark positions invalid beyond what
+    // decode_pos knows (the end of a tile that does not end a row).
+    const bool next_valid = __shfl_down_sync(0xffffffffu, ps.valid, 1);
+    const bool next_adj = ps.valid && next_valid && lane < 31 && ps.qx + 1 < e.Qvx;
     const bool pair = next_adj && x0 + 1 >= 0 && x0 + 2 < e.Wout;
     const bool prev_pair = __shfl_up_sync(0xffffffffu, pair, 1) && lane > 0;
     const bool first = ps.valid && !prev_pair && x0 >= 0 && x0 < e.Wout;

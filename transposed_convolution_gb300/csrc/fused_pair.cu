@@ -47,6 +47,7 @@ constexpr uint64_t kFDrainNs = 2000000000ull;
 
 struct FusedParams {
     int tiles_per_batch, num_tiles;
+    int tile_q;   // B phase positions per tile (128, or up to 256 with two MMA groups)
     // layer A
     int kbA_per_tap, tapsA, x_rows_A, rbA, sA, epA;
     int64_t PA, LA_out;
@@ -128,7 +129,10 @@ __device__ __forceinline__ void mid_chunk(float (&v)[32], uint8_t *box, int x_ro
 // KIND: layer B's output-stage variant compiled alone (EPI_KIND_1D_S2, the stride-2 layers),
 // or -1 for the run-time dispatch over every variant.  One variant keeps the output warps'
 // code small.
-template <Prec P, int BNA, int BNB, int KIND>
+// NG: B's MMA groups of 128 positions per tile.  With NG = 2 a tile covers fp.tile_q <= 256
+// of B's positions, fed by all sA * 128 outputs of A's 128-position tile (with NG = 1 only
+// 128 + taps - 1 of them are used, and the neighbouring tile computes the rest again).
+template <Prec P, int BNA, int BNB, int KIND, int NG>
 __global__ void __launch_bounds__(kFThreads, 1)
     fused_pair_kernel(const __grid_constant__ CUtensorMap mapXA,
                       const __grid_constant__ CUtensorMap mapWA,
@@ -137,9 +141,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
     constexpr uint32_t kFmt = P == Prec::F16 ? ptx::kFmtF16 : ptx::kFmtBF16;
     constexpr uint32_t kIdescA = ptx::idesc_f32acc(kFmt, kBM, BNA);
     constexpr uint32_t kIdescB = ptx::idesc_f32acc(kFmt, kBM, BNB);
-    constexpr uint32_t kTmemCols = 2 * (BNA + BNB) <= 256 ? 256 : 512;
+    constexpr uint32_t kTmemCols = 2 * (BNA + NG * BNB) <= 256 ? 256 : 512;
     constexpr int kKSteps = kRowBytes / 32;
-    static_assert(2 * (BNA + BNB) <= 512, "two accumulators of each layer fit TMEM");
+    static_assert(2 * (BNA + NG * BNB) <= 512, "two accumulators of each layer fit TMEM");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -206,7 +210,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     // B's operand box and the first A position qa0 whose outputs cover it.
     auto tile_geo = [&](int t, int64_t &b, int64_t &q0, int64_t &a0, int64_t &qa0) {
         b = t / fp.tiles_per_batch;
-        q0 = (int64_t)(t - b * fp.tiles_per_batch) * kBM;
+        q0 = (int64_t)(t - b * fp.tiles_per_batch) * fp.tile_q;
         a0 = q0 + fp.c0B;
         qa0 = floor_div(a0 + fp.epA, fp.sA);
     };
@@ -298,16 +302,20 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 if (!ptx::mbar_wait_warp(&bx_full[bb], par, limit, abort)) return false;
                 if (!ptx::mbar_wait_warp(&tB_empty[bb], par ^ 1u, limit, abort)) return false;
                 ptx::tc_fence_after();
-                const uint32_t d = tmem_base + (uint32_t)(2 * BNA + bb * BNB);
                 uint8_t *box = bx + bb * box_bytes;
-                uint32_t accumulate = 0;
-                for (int g = 0; g < fp.tapsB; ++g) {
-                    const uint64_t xd = ptx::sdesc_k<kRowBytes>(ptx::smem_u32(box + g * kRowBytes));
-                    const uint64_t wd = ptx::sdesc_k<kRowBytes>(ptx::smem_u32(wb + g * BNB * kRowBytes));
 #pragma unroll
-                    for (int k = 0; k < kKSteps; ++k) {
-                        if (ptx::elect_one()) ptx::mma_f16(d, xd + 2 * k, wd + 2 * k, kIdescB, accumulate);
-                        accumulate = 1u;
+                for (int h = 0; h < NG; ++h) {   // group h: positions 128h .. 128h + 127
+                    const uint32_t d = tmem_base + (uint32_t)(2 * BNA + (bb * NG + h) * BNB);
+                    uint32_t accumulate = 0;
+                    for (int g = 0; g < fp.tapsB; ++g) {
+                        const uint64_t xd = ptx::sdesc_k<kRowBytes>(
+                            ptx::smem_u32(box + (kBM * h + g) * kRowBytes));
+                        const uint64_t wd = ptx::sdesc_k<kRowBytes>(ptx::smem_u32(wb + g * BNB * kRowBytes));
+#pragma unroll
+                        for (int k = 0; k < kKSteps; ++k) {
+                            if (ptx::elect_one()) ptx::mma_f16(d, xd + 2 * k, wd + 2 * k, kIdescB, accumulate);
+                            accumulate = 1u;
+                        }
                     }
                 }
                 if (ptx::elect_one()) {
@@ -404,18 +412,23 @@ __global__ void __launch_bounds__(kFThreads, 1)
             const int bb = n & 1;
             if (!warp_wait(&tB_full[bb], ((uint32_t)n >> 1) & 1u)) break;
             ptx::tc_fence_after();
+            constexpr int kCh = BNB / 64;   // chunks per warp and group
+#pragma unroll 1
+            for (int h = 0; h < NG; ++h) {
             // A tile lies inside one batch item: its positions past the item's valid phase
-            // positions would otherwise decode as the next item's.
-            const int64_t qb = q0 + 32 * quad + lane;
+            // positions (or past the tile's tile_q positions) would otherwise decode as the
+            // next item's or the next tile's.
+            const int64_t qi = kBM * h + 32 * quad + lane;
+            const int64_t qb = q0 + qi;
             PosInfo ps = decode_pos(b * fp.PB + qb, fp.epiB);
-            if (qb >= fp.QvB) ps.valid = false;
-            constexpr int kCh = BNB / 64;   // chunks per warp
+            if (qb >= fp.QvB || qi >= fp.tile_q) ps.valid = false;
 #pragma unroll 1
             for (int c = half * kCh; c < (half + 1) * kCh; ++c) {
                 uint32_t u[32];
-                ptx::tmem_ld_32x32b_x32(tmem_base + lane_addr + (uint32_t)(2 * BNA + bb * BNB + 32 * c), u);
+                ptx::tmem_ld_32x32b_x32(
+                    tmem_base + lane_addr + (uint32_t)(2 * BNA + (bb * NG + h) * BNB + 32 * c), u);
                 ptx::tmem_wait_ld_regs(u);
-                if (c == (half + 1) * kCh - 1) {
+                if (h == NG - 1 && c == (half + 1) * kCh - 1) {
                     ptx::tc_fence_before();
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(&tB_empty[bb]);
@@ -427,6 +440,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
                     emit_small<T, 2, 1>(v, ps, 32 * c, fp.epiB, lane);
                 else
                     emit_cols<kOutPlain, kIo>(v, ps, 32 * c, fp.epiB, lane);
+            }
             }
         }
     }
@@ -441,28 +455,29 @@ __global__ void __launch_bounds__(kFThreads, 1)
     }
 }
 
-template <Prec P, int BNA, int BNB, int KIND>
+template <Prec P, int BNA, int BNB, int KIND, int NG>
 cudaError_t launch_fused_inst(const ctr_plan_s *a, const CUtensorMap *maps, const FusedParams &fp,
                               cudaStream_t st) {
     static PerDeviceOnce once;
     cudaError_t e = once.run(current_device(), cudaSuccess, [] {
-        return cudaFuncSetAttribute(fused_pair_kernel<P, BNA, BNB, KIND>,
+        return cudaFuncSetAttribute(fused_pair_kernel<P, BNA, BNB, KIND, NG>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     });
     if (e != cudaSuccess) return e;
     const int grid = std::min(fp.num_tiles, a->num_sms);
-    e = launch_pdl(fused_pair_kernel<P, BNA, BNB, KIND>, dim3((unsigned)grid), dim3(kFThreads),
+    e = launch_pdl(fused_pair_kernel<P, BNA, BNB, KIND, NG>, dim3((unsigned)grid), dim3(kFThreads),
                    (size_t)fp.smem_bytes, st, maps[0], maps[1], maps[2], fp);
     if (e != cudaSuccess) return e;
     count_launches(1);
     return cudaGetLastError();
 }
 
-// Shared-memory layout of a fused pair; false when it does not fit.
-bool fused_layout(const ctr_plan_s *a, const ctr_plan_s *b, FusedParams *fp) {
+// Shared-memory layout of a fused pair with ng MMA groups of B per tile; false when it does
+// not fit.
+bool fused_layout(const ctr_plan_s *a, const ctr_plan_s *b, int ng, FusedParams *fp) {
     const int64_t x_rows_A = (kBM + a->m[1] - 1 + 7) / 8 * 8;
-    const int64_t x_rows_B = (kBM + b->m[1] - 1 + 7) / 8 * 8;
-    if (x_rows_A > 256 || x_rows_B > 256) return false;
+    const int64_t x_rows_B = (ng * kBM + b->m[1] - 1 + 7) / 8 * 8;
+    if (x_rows_A > 256 || x_rows_B > ng * kBM + 128) return false;
     const int64_t kbA_per_tap = a->C_in_pad / 64;
     const int64_t kbA_total = kbA_per_tap * a->m[1];
     const int64_t wa = kbA_total * a->block_n * kRowBytes;
@@ -506,8 +521,22 @@ bool fused_pair_supported(const ctr_plan_s *a) {
         return false;
     FusedParams fp;
     std::memset(&fp, 0, sizeof(fp));
-    return fused_layout(a, b, &fp);
+    return fused_layout(a, b, 1, &fp);
 }
+
+namespace {
+
+// B positions per tile with two MMA groups: A's 128-position tile gives sA * 128 operand rows
+// starting up to sA - 1 rows before the tile's first row, and B's last position reads
+// taps_B - 1 rows past its own; 0 when two groups do not apply (B's accumulators of 128
+// columns would not fit TMEM twice, or the tile would not be longer than one group).
+int64_t wide_tile_q(const ctr_plan_s *a, const ctr_plan_s *b) {
+    if (b->block_n != 64) return 0;
+    const int64_t q = std::min<int64_t>(2 * kBM, kBM * a->s[1] - (a->s[1] - 1) - (b->m[1] - 1));
+    return q > kBM ? q : 0;
+}
+
+}  // namespace
 
 cudaError_t launch_fused_pair(const ctr_plan_s *a, const void *xs, const void *wa_packed,
                               const void *bias_a, const void *wb_packed, const void *bias_b,
@@ -515,13 +544,21 @@ cudaError_t launch_fused_pair(const ctr_plan_s *a, const void *xs, const void *w
     const ctr_plan_s *b = a->chain_next;
     FusedParams fp;
     std::memset(&fp, 0, sizeof(fp));
-    if (!fused_layout(a, b, &fp)) return cudaErrorInvalidValue;
+    int64_t tile_q = wide_tile_q(a, b);
+    int ng = 2;
+    if (tile_q == 0 || !fused_layout(a, b, 2, &fp)) {
+        std::memset(&fp, 0, sizeof(fp));
+        ng = 1;
+        tile_q = kBM;
+        if (!fused_layout(a, b, 1, &fp)) return cudaErrorInvalidValue;
+    }
     CUtensorMap maps[3];
     if (!encode_2d(&maps[0], xs, a->dtype, a->C_in_pad, a->N_total, (uint32_t)fp.x_rows_A, kRowBytes) ||
         !encode_2d(&maps[1], wa_packed, a->dtype, a->K_total, a->M_pad, (uint32_t)a->block_n, kRowBytes) ||
         !encode_2d(&maps[2], wb_packed, b->dtype, b->K_total, b->M_pad, (uint32_t)b->block_n, kRowBytes))
         return cudaErrorInvalidValue;
-    fp.tiles_per_batch = (int)((b->Qv[1] + kBM - 1) / kBM);
+    fp.tile_q = (int)tile_q;
+    fp.tiles_per_batch = (int)((b->Qv[1] + tile_q - 1) / tile_q);
     fp.num_tiles = (int)(b->B * fp.tiles_per_batch);
     fp.tapsA = (int)a->m[1];
     fp.rbA = (int)a->rb[1];
@@ -541,18 +578,22 @@ cudaError_t launch_fused_pair(const ctr_plan_s *a, const void *xs, const void *w
     fp.wait_limit_ns = a->wait_limit_ns;
     if (fp.num_tiles <= 0) return cudaSuccess;
     const bool f16 = a->dtype == CTR_F16;
-    if (fp.epiB.kind == EPI_KIND_1D_S2) {
-        if (b->block_n == 64)
-            return f16 ? launch_fused_inst<Prec::F16, 128, 64, EPI_KIND_1D_S2>(a, maps, fp, st)
-                       : launch_fused_inst<Prec::BF16, 128, 64, EPI_KIND_1D_S2>(a, maps, fp, st);
-        return f16 ? launch_fused_inst<Prec::F16, 128, 128, EPI_KIND_1D_S2>(a, maps, fp, st)
-                   : launch_fused_inst<Prec::BF16, 128, 128, EPI_KIND_1D_S2>(a, maps, fp, st);
+    const bool s2 = fp.epiB.kind == EPI_KIND_1D_S2;
+    if (ng == 2) {   // B tiles of 64 rows (wide_tile_q)
+        if (s2)
+            return f16 ? launch_fused_inst<Prec::F16, 128, 64, EPI_KIND_1D_S2, 2>(a, maps, fp, st)
+                       : launch_fused_inst<Prec::BF16, 128, 64, EPI_KIND_1D_S2, 2>(a, maps, fp, st);
+        return f16 ? launch_fused_inst<Prec::F16, 128, 64, -1, 2>(a, maps, fp, st)
+                   : launch_fused_inst<Prec::BF16, 128, 64, -1, 2>(a, maps, fp, st);
     }
     if (b->block_n == 64)
-        return f16 ? launch_fused_inst<Prec::F16, 128, 64, -1>(a, maps, fp, st)
-                   : launch_fused_inst<Prec::BF16, 128, 64, -1>(a, maps, fp, st);
-    return f16 ? launch_fused_inst<Prec::F16, 128, 128, -1>(a, maps, fp, st)
-               : launch_fused_inst<Prec::BF16, 128, 128, -1>(a, maps, fp, st);
+        return f16 ? launch_fused_inst<Prec::F16, 128, 64, -1, 1>(a, maps, fp, st)
+                   : launch_fused_inst<Prec::BF16, 128, 64, -1, 1>(a, maps, fp, st);
+    if (s2)
+        return f16 ? launch_fused_inst<Prec::F16, 128, 128, EPI_KIND_1D_S2, 1>(a, maps, fp, st)
+                   : launch_fused_inst<Prec::BF16, 128, 128, EPI_KIND_1D_S2, 1>(a, maps, fp, st);
+    return f16 ? launch_fused_inst<Prec::F16, 128, 128, -1, 1>(a, maps, fp, st)
+               : launch_fused_inst<Prec::BF16, 128, 128, -1, 1>(a, maps, fp, st);
 }
 
 }  // namespace ctr
