@@ -11,8 +11,9 @@
 //   warp 0      loads both packed weights once (they stay resident) and, per tile and
 //               input channel slice, one box of A's staged input (128 positions plus A's
 //               tap shifts);
-//   warp 1      issues A's MMAs for tile t, then B's MMAs for tile t - 1, so the tensor
-//               cores run A while the mid warps convert the previous tile;
+//   warp 1      issues A's MMAs, tile after tile, and warp 18 B's, each as soon as its
+//               operands and accumulator are free, so the tensor cores run one layer's
+//               MMAs while the mid warps convert the other's tile;
 //   warps 2..9  ("mid") read A's accumulator, add A's bias, apply its activation, round to
 //               the I/O type and write the values as B's K-major, 128-byte-swizzled operand
 //               box in shared memory: row r holds A's output a0 + r (zeros outside A's
@@ -38,9 +39,10 @@
 namespace ctr {
 namespace {
 
-constexpr int kFThreads = 576;
+constexpr int kFThreads = 608;
 constexpr int kMidWarps = 8;     // warps 2..9
 constexpr int kOutWarps = 8;     // warps 10..17
+constexpr int kBWarp = 18;       // issues B's MMAs (warp 1 issues A's)
 constexpr int kFMaxStages = 8;
 constexpr int kRowBytes = 128;   // one K slice of 64 16-bit channels
 constexpr uint64_t kFDrainNs = 2000000000ull;
@@ -162,8 +164,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
     uint64_t *tB_full = bx_free + 2;               // [2]
     uint64_t *tB_empty = tB_full + 2;              // [2], one arrival per final warp
     uint64_t *w_full = tB_empty + 2;
-    uint64_t *drain = w_full + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    uint64_t *drain = w_full + 1;      // warp 1's MMAs done
+    uint64_t *drainB = drain + 1;      // warp 18's MMAs done
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drainB + 1);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -185,6 +188,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
         }
         ptx::mbar_init(w_full, 1);
         ptx::mbar_init(drain, 1);
+        ptx::mbar_init(drainB, 1);
         *abort = 0;
         ptx::fence_mbar_init();
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -256,24 +260,28 @@ __global__ void __launch_bounds__(kFThreads, 1)
             }
             if (!ptx::mbar_wait(w_full, 0, kFDrainNs, nullptr)) atomicOr(fp.status, kStatusTimeoutDrain);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        // The whole warp runs the loop; one elected lane issues each tcgen05 instruction.
-        {
-            bool ok = ptx::mbar_wait_warp(w_full, 0, limit, abort);
-            if (!ok && lane == 0 && !*abort) f_give_up(abort, fp.status, kStatusTimeoutMma);
+    } else if (warp == 1 || warp == kBWarp) {
+        // ------------------------------------------------------------ MMA issuers
+        // Warp 1 issues A's MMAs, warp 18 B's.  Each whole warp runs its loop; one elected
+        // lane issues each tcgen05 instruction, and each warp commits and drains its own.
+        const bool is_a = warp == 1;
+        bool ok = ptx::mbar_wait_warp(w_full, 0, limit, abort);
+        if (!ok && lane == 0 && !*abort) f_give_up(abort, fp.status, kStatusTimeoutMma);
+        if (is_a) {
             int stage = 0;
             uint32_t phase = 0;
-            int na = 0, nb = 0;   // A and B tiles issued by this CTA
-            auto issue_A = [&]() -> bool {
+            int na = 0;   // A tiles issued by this CTA
+            for (int t = blockIdx.x; ok && t < fp.num_tiles && !ptx::abort_warp(abort);
+                 t += gridDim.x, ++na) {
                 const int acc = na & 1;
-                if (!ptx::mbar_wait_warp(&tA_empty[acc], (((uint32_t)na >> 1) & 1u) ^ 1u, limit, abort))
-                    return false;
+                if (!(ok = ptx::mbar_wait_warp(&tA_empty[acc], (((uint32_t)na >> 1) & 1u) ^ 1u,
+                                               limit, abort)))
+                    break;
                 ptx::tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(acc * BNA);
                 uint32_t accumulate = 0;
                 for (int kc = 0; kc < fp.kbA_per_tap; ++kc) {
-                    if (!ptx::mbar_wait_warp(&full[stage], phase, limit, abort)) return false;
+                    if (!(ok = ptx::mbar_wait_warp(&full[stage], phase, limit, abort))) break;
                     ptx::tc_fence_after();
                     uint8_t *st = smem + stage * fp.stage_bytes;
                     for (int g = 0; g < fp.tapsA; ++g) {
@@ -292,15 +300,17 @@ __global__ void __launch_bounds__(kFThreads, 1)
                         phase ^= 1u;
                     }
                 }
+                if (!ok) break;
                 if (ptx::elect_one()) ptx::mma_commit(&tA_full[acc]);
-                ++na;
-                return true;
-            };
-            auto issue_B = [&]() -> bool {
+            }
+        } else {
+            int nb = 0;   // B tiles issued by this CTA
+            for (int t = blockIdx.x; ok && t < fp.num_tiles && !ptx::abort_warp(abort);
+                 t += gridDim.x, ++nb) {
                 const int bb = nb & 1;
                 const uint32_t par = ((uint32_t)nb >> 1) & 1u;
-                if (!ptx::mbar_wait_warp(&bx_full[bb], par, limit, abort)) return false;
-                if (!ptx::mbar_wait_warp(&tB_empty[bb], par ^ 1u, limit, abort)) return false;
+                if (!(ok = ptx::mbar_wait_warp(&bx_full[bb], par, limit, abort))) break;
+                if (!(ok = ptx::mbar_wait_warp(&tB_empty[bb], par ^ 1u, limit, abort))) break;
                 ptx::tc_fence_after();
                 uint8_t *box = bx + bb * box_bytes;
 #pragma unroll
@@ -322,20 +332,14 @@ __global__ void __launch_bounds__(kFThreads, 1)
                     ptx::mma_commit(&bx_free[bb]);
                     ptx::mma_commit(&tB_full[bb]);
                 }
-                ++nb;
-                return true;
-            };
-            for (int t = blockIdx.x; ok && t < fp.num_tiles && !ptx::abort_warp(abort); t += gridDim.x) {
-                ok = issue_A();
-                if (ok && na > 1) ok = issue_B();   // the previous tile's B
             }
-            if (ok && nb < na) ok = issue_B();
-            if (!ok && lane == 0 && !*abort) f_give_up(abort, fp.status, kStatusTimeoutMma);
-            if (ptx::elect_one()) ptx::mma_commit(drain);
-            __syncwarp();
-            if (!ptx::mbar_wait_warp(drain, 0, kFDrainNs, nullptr) && lane == 0)
-                atomicOr(fp.status, kStatusTimeoutDrain);
         }
+        if (!ok && lane == 0 && !*abort) f_give_up(abort, fp.status, kStatusTimeoutMma);
+        uint64_t *my_drain = is_a ? drain : drainB;
+        if (ptx::elect_one()) ptx::mma_commit(my_drain);
+        __syncwarp();
+        if (!ptx::mbar_wait_warp(my_drain, 0, kFDrainNs, nullptr) && lane == 0)
+            atomicOr(fp.status, kStatusTimeoutDrain);
     } else if (warp < 2 + kMidWarps) {
         // ------------------------------------------------------------ mid: A -> B's operand
         const int quad = warp & 3;
