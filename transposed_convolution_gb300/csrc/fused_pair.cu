@@ -5,9 +5,11 @@
 // transposed convs as one polyphase conv + depth to space", Test plan: two deconvolutions
 // with an activation between; Summary: each layer one polyphase convolution) writes every
 // intermediate to memory and reads it back.  For two small-channel layers that traffic is
-// most of their bytes.  Here one CTA computes, per tile of 128 output phase positions of the
-// second layer (B), the slab of first-layer (A) outputs those positions read -- 128 + taps - 1
-// rows -- and never stores it:
+// most of their bytes.  Here one CTA computes, per tile of the second layer's (B's) output
+// phase positions, the slab of first-layer (A) outputs those positions read, and never
+// stores it.  A tile is A's 128 positions; B's tile is 128 positions (one MMA group) or, when
+// B's accumulators are 64 columns wide, up to 253 (two groups of 128), which uses all of the
+// 2 x 128 outputs of A's tile:
 //   warp 0      loads both packed weights once (they stay resident) and, per tile and
 //               input channel slice, one box of A's staged input (128 positions plus A's
 //               tap shifts);
@@ -20,7 +22,8 @@
 //               output), every channel of it (one 128-byte row); two warps per TMEM lane
 //               quarter, one phase each;
 //   warps 10..17 run B's output stage (epilogue.cuh) on B's accumulator, two warps per lane
-//               quarter splitting its columns.
+//               quarter splitting its columns;
+//   warp 18     issues B's MMAs.
 // Both MMAs read their operand boxes through descriptors that start tap rows further down
 // (a K-major 128-byte-swizzled operand may start at any row of its 1024-byte-aligned box).
 // The result is bit-identical to the two chained launches: the same products in the same
