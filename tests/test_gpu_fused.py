@@ -51,7 +51,10 @@ CASES = [  # (B, C0, L, C2, kA, sA, pA, kB, sB, pB, B's phase origin)
     (1, 128, 1000, 32, 4, 2, 1, 4, 2, 1, ctr.CTR_PHASE_AUTO),
     (2, 128, 257, 32, 4, 2, 1, 4, 2, 1, ctr.CTR_PHASE_AUTO),
     (1, 96, 130, 64, 4, 2, 1, 4, 2, 1, ctr.CTR_PHASE_UNPADDED),
-    (2, 96, 700, 32, 4, 2, 1, 4, 2, 1, ctr.CTR_PHASE_UNPADDED),  # wide tiles, paired stores
+    (2, 96, 700, 32, 4, 2, 1, 4, 2, 1, ctr.CTR_PHASE_UNPADDED),  # paired stores
+    # long rows: two MMA groups per tile, several tiles per CTA, tiles ending inside a row,
+    # paired stores
+    (2, 96, 20000, 32, 4, 2, 1, 4, 2, 1, ctr.CTR_PHASE_UNPADDED),
     (1, 64, 300, 32, 6, 2, 2, 6, 2, 2, ctr.CTR_PHASE_AUTO),
     (1, 128, 77, 32, 4, 2, 0, 4, 2, 0, ctr.CTR_PHASE_AUTO),
     (1, 60, 161, 32, 8, 2, 3, 8, 2, 3, ctr.CTR_PHASE_AUTO),     # 4 and 5 taps, ragged C0
