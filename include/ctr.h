@@ -106,7 +106,9 @@ typedef enum {
  * Every output size must be >= 1.  Groups, dilation and separate front/back pads are set
  * afterwards (ctr_plan_set_groups, ctr_plan_set_dilation, ctr_plan_set_pads; defaults: one
  * group, dilation 1, the back pad equal to `padding`).  Returns CTR_ERR_INVALID_ARG on any
- * violation.
+ * violation.  A layer whose pads are only valid once separated or dilated (a front pad that,
+ * taken on both sides, would leave no output) is created with zero padding and given its
+ * pads by ctr_plan_set_pads, after ctr_plan_set_dilation.
  */
 ctr_status ctr_plan_create(ctr_plan_t *out, int ndim, int64_t N, int64_t C_in, int64_t C_out,
                            const int64_t *in_spatial, const int64_t *kernel,

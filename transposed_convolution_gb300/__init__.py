@@ -410,8 +410,12 @@ class Plan:
         if layout not in ("nchw", "nhwc"):
             raise ValueError("layout must be 'nchw' or 'nhwc'")
         self.nhwc = layout == "nhwc"
+        # With separate back pads or dilation the plan is created unpadded and given its pads
+        # afterwards: the symmetric front padding alone may leave no output.
+        separate = self.padding_end != self.padding or self.dilation != (1,) * self.ndim
         self.handle = ctr_plan_create(self.ndim, self.N, self.C_in, self.C_out, self.in_spatial,
-                                      self.kernel, self.stride, self.padding,
+                                      self.kernel, self.stride,
+                                      (0,) * self.ndim if separate else self.padding,
                                       self.output_padding, _dtype_code(self.dtype))
         try:
             if self.nhwc:
@@ -422,7 +426,7 @@ class Plan:
                 ctr_plan_set_groups(self.handle, self.groups)
             if self.dilation != (1,) * self.ndim:
                 ctr_plan_set_dilation(self.handle, self.dilation)
-            if self.padding_end != self.padding:
+            if separate:
                 ctr_plan_set_pads(self.handle, self.padding, self.padding_end)
             if auto_pad != CTR_AUTO_PAD_NOTSET or output_shape is not None:
                 ctr_plan_set_auto_pad(self.handle, auto_pad, output_shape)
