@@ -268,13 +268,20 @@ def layer_peak(L, peaks, peak_src, tf32_tflops):
     """Tensor peak (TFLOP/s of useful MACs x 2) for a layer and where it comes from."""
     if L.dtype == "bf16":
         return peaks["bf16_tflops"], "bf16 dense, %s burst" % peak_src
+    # fp32 I/O: every useful MAC costs one tf32 MAC (hi*hi) and two bf16 MACs (the cross
+    # products), so the peak is 1 / (1/P_tf32 + 2/P_bf16).
     if tf32_tflops:
-        return (tf32_tflops / 3.0,
-                "3xTF32: tf32 dense measured in this run (torch.matmul fp32 8192^3, TF32, best of "
-                "10) / 3 products per useful MAC")
-    return (peaks["bf16_tflops"] * TF32_OVER_BF16 / 3.0,
-            "3xTF32: %s bf16 burst x nominal tf32/bf16 (1.1/2.25) / 3 products per useful "
-            "MAC" % peak_src)
+        return (split_peak(tf32_tflops, peaks["bf16_tflops"]),
+                "fp32 split: 1/(1/P_tf32 + 2/P_bf16), P_tf32 measured in this run "
+                "(torch.matmul fp32 8192^3, TF32, best of 10), P_bf16 %s burst" % peak_src)
+    return (split_peak(peaks["bf16_tflops"] * TF32_OVER_BF16, peaks["bf16_tflops"]),
+            "fp32 split: 1/(1/P_tf32 + 2/P_bf16), P_bf16 %s burst, P_tf32 = P_bf16 x nominal "
+            "tf32/bf16 (1.1/2.25)" % peak_src)
+
+
+def split_peak(p_tf32, p_bf16):
+    """Useful-MAC throughput of the fp32 split (one tf32 and two bf16 MACs per MAC)."""
+    return 1.0 / (1.0 / p_tf32 + 2.0 / p_bf16)
 
 
 def measure_workload(name, args, env, headline):
@@ -597,7 +604,8 @@ def summarize(m, env):
     kern_s = m["kern_ms"][j] / 1e3
     if bound == "tensor":
         achieved, peak, unit = 2.0 * g_macs / kern_s / 1e12, pk, "TFLOP/s"
-        nominal = peaks["bf16_tflops"] * TF32_OVER_BF16 / 3.0 if L.dtype == "f32" else pk
+        nominal = (split_peak(peaks["bf16_tflops"] * TF32_OVER_BF16, peaks["bf16_tflops"])
+                   if L.dtype == "f32" else pk)
     else:
         achieved, peak, unit = g_bytes / kern_s / 1e9, peaks["hbm_gbs"], "GB/s"
         peak_note = "HBM copy bandwidth, %s" % peak_src
@@ -795,7 +803,7 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32 I/O, 3xTF32 products, fp32 accumulate" if Ls[0].dtype == "f32"
+        "dtype": "f32 I/O, tf32 + bf16 split products, fp32 accumulate" if Ls[0].dtype == "f32"
                  else "bf16 I/O, bf16 products, fp32 accumulate",
         "data": "synthetic (seeded; workloads.py)",
         "config": {"workload": head, "shape": summ["shape"],

@@ -68,7 +68,9 @@ typedef enum {
 } ctr_status;
 
 typedef enum {
-    CTR_F32 = 0,   /* fp32 I/O; tensor-core products as 3xTF32 (hi/lo split), fp32 accumulate */
+    CTR_F32 = 0,   /* fp32 I/O; each operand split as hi = tf32(v), lo = v - hi: hi*hi as a tf32
+                      tensor-core product, hi*lo + lo*hi as bf16 products, fp32 accumulate
+                      (rel_l2 within 1e-5 of fp32 arithmetic) */
     CTR_BF16 = 1,  /* bf16 I/O; bf16 tensor-core products, fp32 accumulate, one final rounding */
     CTR_F16 = 2    /* fp16 I/O; fp16 tensor-core products, fp32 accumulate and intermediates,
                       one final rounding ("[WebGPU] optimizations for audio models", review
@@ -308,7 +310,7 @@ ctr_status ctr_plan_set_tile(ctr_plan_t plan, int block_n);
  * plan).  Afterwards:
  *   - ctr_forward(plan, x, w, bias, y = NULL, stream) writes its output, with bias and
  *     activation applied and rounded to the I/O type, straight into the channels-last
- *     staged-input layout inside next's workspace (fp32: as tf32 hi and lo planes, exactly
+ *     staged-input layout inside next's workspace (fp32: as its tf32 and bf16-pair planes, exactly
  *     what next's staging would have made of the torch-layout output), and no y;
  *   - ctr_forward(next, x = NULL, ...) reads it from there instead of staging an x.
  * Results are bit-identical to the unchained calls.  Requirements (CTR_ERR_INVALID_ARG

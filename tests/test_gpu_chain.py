@@ -2,7 +2,7 @@
 staged input, and the next plan runs without staging.
 
 * The chained results must equal the unchained calls bit for bit (the staged values are the
-  same: bf16 rounding, or the tf32 hi/lo split of the fp32 output), on repeated calls too
+  same: bf16 rounding, or the tf32 and bf16-pair split of the fp32 output), on repeated calls too
   (the staged halos stay zero).
 * Against the oracle, run stage by stage with the output of each stage rounded to the I/O
   type (the value the next stage reads): within rel_l2 <= 1e-5 (fp32 I/O) or <= 1e-2 (bf16)

@@ -3,7 +3,7 @@
 * integer-exact grids: small-integer inputs make every product and partial sum exact in
   fp32, tf32 and bf16, so every path must equal the oracle bit for bit;
 * tile, split-K and ragged-edge shapes, bit-exact the same way;
-* random inputs within rel_l2 <= 1e-5 (fp32 I/O, 3xTF32) or <= 1e-2 (bf16 I/O);
+* random inputs within rel_l2 <= 1e-5 (fp32 I/O, tf32 + bf16 split) or <= 1e-2 (bf16 I/O);
 * the five workloads at full size, in the configuration the benchmark times;
 * the iSTFT of a sinusoid at full size, against its closed form;
 * edge cases of the pages: empty input, one input step, m = 1 and 3, k = 2s at s = 2, 4, 5,
@@ -98,7 +98,7 @@ def test_tiles_and_split_k_bit_exact(dtype, split_k):
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_every_tile_width_bit_exact(dtype, block_n):
     """Each phase-row tile width of the GEMM (its own kernel instantiation: slice width,
-    stage count, TMEM accumulators, and at 256 columns in 3xTF32 the TMEM-resident group
+    stage count, TMEM accumulators, and at 256 columns in fp32 the TMEM-resident group
     sums) with enough K for several accumulation groups, with and without split-K."""
     rng = np.random.default_rng(11 + block_n)
     mag = 2 if dtype == "f32" else 1

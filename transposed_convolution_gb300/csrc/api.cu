@@ -53,22 +53,25 @@ int query_num_sms() {
 }
 
 Prec prec_of(const ctr_plan_s *pl) {
-    return pl->dtype == CTR_BF16 ? Prec::BF16 : pl->dtype == CTR_F16 ? Prec::F16 : Prec::TF32x3;
+    return pl->dtype == CTR_BF16 ? Prec::BF16 : pl->dtype == CTR_F16 ? Prec::F16 : Prec::F32;
 }
 bool io16(const ctr_plan_s *pl) { return pl->dtype != CTR_F32; }
 int esize_io(const ctr_plan_s *pl) { return io16(pl) ? 2 : 4; }
 // Elements of one 128-byte K slice in the GEMM operands.
 int bk_elems(const ctr_plan_s *pl) { return io16(pl) ? 64 : 32; }
-// Bytes per element of one GEMM operand plane, and number of planes (hi/lo for 3xTF32).
+// Bytes per element of one GEMM operand plane, and number of planes (fp32: the tf32 plane
+// and the plane of bf16 cross words).
 int op_esize(const ctr_plan_s *pl) { return io16(pl) ? 2 : 4; }
 int op_planes(const ctr_plan_s *pl) { return io16(pl) ? 1 : 2; }
 
 bool is_tc_path(int path) { return path == CTR_PATH_POLYPHASE || path == CTR_PATH_COL2IM; }
 
 // Estimated clocks of one K slice of a 128-position x BN-row tile on one SM (tensor pipe).
-double slice_clocks(Prec prec, int bn) { return prec == Prec::TF32x3 ? 6.0 * bn : 2.0 * bn; }
+// fp32: a tf32 MMA and a bf16 MMA of twice the K per 32-byte K step, each at half the rate
+// of a 16-bit MMA over the slice.
+double slice_clocks(Prec prec, int bn) { return prec == Prec::F32 ? 4.0 * bn : 2.0 * bn; }
 
-// 128-byte K slices per tensor-core accumulation group in 3xTF32 mode (512 fp32 K
+// 128-byte K slices per tensor-core accumulation group for fp32 I/O (512 fp32 K
 // elements).  The tensor core's fp32 accumulation over a long K chain drifts well beyond
 // fp32 summation with round-to-nearest (measured on GB300: rel_l2 2.3e-5 over 3300-element
 // chains, a mean relative bias of -4.6e-5 over 4096 all-positive products), so the kernel
@@ -89,10 +92,8 @@ int tf32_group() {
 }
 
 // Choose the phase-row tile BN in {64, 128, 256} and the split-K factor: fewest estimated
-// clocks, counting whole waves of tiles over the SMs, a tile's time as the largest of its
-// MMA time, its operand-load time and its output time, and the extra pass over split-K
-// partials.  3xTF32 at BN = 256 keeps its group sums in TMEM beside a single accumulator, so
-// the MMAs pause while each group is folded into the sums (~800 clocks).
+// clocks, counting whole waves of tiles over the SMs, a tile's time from its MMA time, its
+// operand-load time and its output time, and the extra pass over split-K partials.
 // The tile a plan needs to run as one half of a fused chained pair (ctr_forward_fused):
 // 128 rows for the first layer, its 64 channels x 2 phases in one tile; the second layer's
 // rows in one tile of 64 or 128; both without split-K.  0 when the plan is not half of a
@@ -102,7 +103,7 @@ int fused_pair_bn(const ctr_plan_s *pl);
 double choose_tiling(ctr_plan_s *pl, double epi_factor = 1.0) {
     const Prec prec = prec_of(pl);
     const int pair_bn = fused_pair_bn(pl);
-    const int group = prec == Prec::TF32x3 ? tf32_group() : kNoGroup;
+    const int group = prec == Prec::F32 ? tf32_group() : kNoGroup;
     const int kb_total = (int)(pl->K_total * op_esize(pl) / ctr::kBKBytes);
     const int64_t num_p = std::max<int64_t>(1, ceil_div(pl->N_total, ctr::kBM));
     double best = 1e300;
@@ -122,17 +123,35 @@ double choose_tiling(ctr_plan_s *pl, double epi_factor = 1.0) {
             if (bn > ctr::kMaxGroupedBN && kbs > group) continue;
             const int64_t tiles = num_p * num_r * sp;
             const int64_t waves = ceil_div(tiles, pl->num_sms);
-            // Per tile: tensor-pipe time, operand loads at ~50 B per clock per SM from L2,
-            // and output writes at ~20 B per clock per SM (the HBM share of one SM).
-            double mma = kbs * slice_clocks(prec, bn);
-            if (prec == Prec::TF32x3 && bn == 256) mma += 800.0 * std::ceil(kbs / std::min(kbs, (double)group));
-            const double load = kbs * (ctr::kBM + bn) * (double)ctr::kBKBytes * op_planes(pl) / 50.0;
+            // Per tile: tensor-pipe time, operand loads from L2, and output writes at ~20 B
+            // per clock per SM (the HBM share of one SM).
+            const double mma = kbs * slice_clocks(prec, bn);
             const double epi = epi_factor * ctr::kBM * (double)bn * esize_io(pl) / 20.0 + 300.0;
-            const double tile = std::max(mma, std::max(load, epi));
-            double t = (double)waves * tile + 2000.0;
+            double t;
+            if (prec == Prec::F32) {
+                // Two operand planes.  Fitted to forced-tile timings on GB300 with operands
+                // coming from HBM (inputs and weights rotated past twice the L2): 256-row
+                // tiles load at ~55 B per clock per SM, smaller ones at ~65.  A 256-row tile
+                // has one accumulator: its output stage does not overlap the next work
+                // unit's MMAs, and folding each accumulation group into the sums pauses
+                // them (~600 clocks).
+                const double load = kbs * (ctr::kBM + bn) * (double)ctr::kBKBytes * 2 / (bn == 256 ? 55.0 : 65.0);
+                double unit = std::max(mma, load);
+                if (bn == 256) {
+                    unit += 600.0 * (std::ceil(kbs / std::min(kbs, (double)group)) - 1.0);
+                    t = (double)waves * (unit + epi) + 2000.0;
+                } else {
+                    t = (double)waves * std::max(unit, epi) + epi + 2000.0;
+                }
+            } else {
+                // One plane, operand loads at ~50 B per clock per SM.
+                const double load = kbs * (ctr::kBM + bn) * (double)ctr::kBKBytes / 50.0;
+                t = (double)waves * std::max(mma, std::max(load, epi)) + 2000.0;
+            }
             if (sp > 1 || pl->path == CTR_PATH_COL2IM) {
-                // partials written once and read once, ~3.5 KB per clock for the whole GPU
-                t += (double)(sp + 1) * num_p * ctr::kBM * num_r * bn * 4.0 / 3500.0;
+                // partials written once and read once by the reduce (or col2im) pass, ~1.25
+                // KB per clock for the whole GPU (measured: split-K 2 against 1)
+                t += (double)(sp + 1) * num_p * ctr::kBM * num_r * bn * 4.0 / 1250.0;
             }
             if (t < best * 0.98) {
                 best = t;
@@ -1041,7 +1060,7 @@ ctr_status ctr_plan_describe(ctr_plan_t pl, char *buf, size_t len) {
                  "path=%s prec=%s rows=%lld(pad %lld, BN %d, %d tiles) positions=%lld(%d tiles) "
                  "K=%lld splits=%d group=%d tiles=%lld sms=%d S=%d/%d taps=%lldx%lld%s "
                  "pitch=%lldx%lld epi=%d/%dB%s packed=%zu ws=%zu",
-                 pname, pl->dtype == CTR_BF16 ? "bf16" : pl->dtype == CTR_F16 ? "f16" : "3xtf32",
+                 pname, pl->dtype == CTR_BF16 ? "bf16" : pl->dtype == CTR_F16 ? "f16" : "tf32+bf16x",
                  (long long)pl->M_rows,
                  (long long)pl->M_pad, pl->block_n, pl->num_r_tiles, (long long)pl->N_total,
                  pl->num_p_tiles, (long long)pl->K_total, pl->splits,

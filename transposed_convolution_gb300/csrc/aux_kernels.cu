@@ -1,6 +1,6 @@
 // aux_kernels.cu -- the non-tensor-core kernels of the library:
 //   prepack      torch weight -> phase-major GEMM rows (polyphase) or (oc, tap) rows (col2im)
-//   stage_x      NC(H)W input -> channels-last rows with zero halos (tf32 hi/lo or bf16)
+//   stage_x      NC(H)W input -> channels-last rows with zero halos (tf32 + cross, or 16-bit)
 //   splitk_reduce  fixed-order sum of split-K partials, then the fused output stage
 //   col2im       gather of the valid taps from the fp32 column buffer
 //   gather       direct ConvTranspose for tiny channel counts and grouped convolutions
@@ -192,7 +192,8 @@ struct PackGeo {
 // zero otherwise.
 // col2im rows ("[WebGPU] optimizations for audio models", ConvTranspose commit: W[C_in,
 // kH*kW*C_out] prepacked to the GEMM layout):  A[r = oc*S_pad + t, k = ic] = w[ic, oc, t].
-// Padding rows and channels are zero.  fp32 weights are split into tf32 hi and lo planes.
+// Padding rows and channels are zero.  fp32 weights are split into a tf32 plane and a plane
+// of bf16 cross words (ptx::split_w).
 // A chained producer (pm_tc > 0) orders the rows of each block_n-row tile phase-major
 // instead: tile t, row j * pm_tc + c is phase j of channel t * pm_tc + c.
 __global__ void prepack_kernel(const void *__restrict__ w, void *__restrict__ wp, PackGeo pg) {
@@ -236,10 +237,9 @@ __global__ void prepack_kernel(const void *__restrict__ w, void *__restrict__ wp
         } else if (pg.io == IO_F16) {
             static_cast<__half *>(wp)[idx] = __float2half_rn(v);             // exact: v is fp16
         } else {
-            const float hi = ptx::to_tf32(v);
-            const float lo = ptx::to_tf32(v - hi);
-            static_cast<float *>(wp)[idx] = hi;
-            static_cast<float *>(wp)[total + idx] = lo;
+            uint32_t cross;
+            static_cast<float *>(wp)[idx] = ptx::split_w(v, cross);
+            static_cast<uint32_t *>(wp)[total + idx] = cross;
         }
     }
 }
@@ -252,8 +252,8 @@ struct StageGeo {
 
 // xs[n][c] with n = (b*Py + py')*Px + px': x[b, c, py' - hy, px' - hx] inside the input and
 // c < C_in, zero elsewhere (the front halos hy, hx are the polyphase conv's padding m - 1,
-// less the phase positions the output phases skip).  fp32 input is written as tf32 hi and lo
-// planes.
+// less the phase positions the output phases skip).  fp32 input is written as a tf32 plane
+// and a plane of bf16 cross words (ptx::split_x).
 //
 // A block transposes one tile of 128 input positions (along x, within one staged row) by
 // kStageC channels (64 bf16 or 32 fp32, i.e. 128 bytes of a staged row) through shared
@@ -375,16 +375,14 @@ __global__ void __launch_bounds__(kStageThreads) stage_x_kernel(const void *__re
                 *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(xs) + o) =
                     make_uint4(w4[0], w4[1], w4[2], w4[3]);
             } else {
-                float hi[4], lo[4];
+                float hi[4];
+                uint32_t cr[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    hi[k] = ptx::to_tf32(val[k]);
-                    lo[k] = ptx::to_tf32(val[k] - hi[k]);
-                }
+                for (int k = 0; k < 4; ++k) hi[k] = ptx::split_x(val[k], cr[k]);
                 *reinterpret_cast<float4 *>(static_cast<float *>(xs) + o) =
                     make_float4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<float4 *>(static_cast<float *>(xs) + lo_off + o) =
-                    make_float4(lo[0], lo[1], lo[2], lo[3]);
+                *reinterpret_cast<uint4 *>(static_cast<float *>(xs) + lo_off + o) =
+                    make_uint4(cr[0], cr[1], cr[2], cr[3]);
             }
         }
         // Zeros of the staged positions no tile covers: the left halo (first tile of the
@@ -412,7 +410,7 @@ __global__ void __launch_bounds__(kStageThreads) stage_x_kernel(const void *__re
 // The staged operand from a channels-last x: staged row n = (b*Py + py')*Px + px' holds
 // x[b, py' - hy, px' - hx, 0 .. C_in) followed by zeros up to C_in_pad, or zeros outside the
 // input.  One thread per 16-byte vector of a staged row: consecutive threads read and write
-// consecutive bytes of one position.  fp32 input becomes tf32 hi and lo planes; 16-bit input
+// consecutive bytes of one position.  fp32 input becomes the tf32 and cross planes; 16-bit input
 // is moved as raw payloads.  VEC: x rows are whole 16-byte vectors (C_in * esize % 16 == 0).
 template <bool B16, bool VEC>
 __global__ void __launch_bounds__(256) stage_nhwc_kernel(const void *__restrict__ x,
@@ -423,7 +421,7 @@ __global__ void __launch_bounds__(256) stage_nhwc_kernel(const void *__restrict_
     using E = typename std::conditional<B16, uint16_t, uint32_t>::type;
     constexpr int kVec = 16 / (int)sizeof(E);           // elements per vector
     const int64_t vpr = sg.C_in_pad / kVec;             // vectors per staged row
-    const int64_t lo_off = sg.N_total * sg.C_in_pad;    // elements to the lo plane
+    const int64_t lo_off = sg.N_total * sg.C_in_pad;    // elements to the cross plane
     const E *__restrict__ xe = static_cast<const E *>(x);
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -451,76 +449,93 @@ __global__ void __launch_bounds__(256) stage_nhwc_kernel(const void *__restrict_
         if constexpr (B16) {
             *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(xs) + o) = *reinterpret_cast<uint4 *>(v);
         } else {
-            float hi[4], lo[4];
+            float hi[4];
+            uint32_t cr[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float f = __uint_as_float(v[k]);
-                hi[k] = ptx::to_tf32(f);
-                lo[k] = ptx::to_tf32(f - hi[k]);
-            }
+            for (int k = 0; k < 4; ++k) hi[k] = ptx::split_x(__uint_as_float(v[k]), cr[k]);
             *reinterpret_cast<float4 *>(static_cast<float *>(xs) + o) = make_float4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<float4 *>(static_cast<float *>(xs) + lo_off + o) =
-                make_float4(lo[0], lo[1], lo[2], lo[3]);
+            *reinterpret_cast<uint4 *>(static_cast<float *>(xs) + lo_off + o) =
+                make_uint4(cr[0], cr[1], cr[2], cr[3]);
         }
     }
 }
 
 // -------------------------------------------------------------------------- split-K reduce
-// One thread per (phase position n, 32-row chunk r0): sums the split-K partials
-// raw[z][n][r0 .. r0+31] in a fixed order (z = 0, 1, ...) with 16-byte loads, then runs the
-// same output stage as the fused epilogue.  The 32 lanes of a warp take 32 consecutive
-// positions of one chunk (positions padded to a multiple of 32; lanes past the end load
-// nothing and store nothing), as the warp-collective output stage requires.
-__global__ void splitk_reduce_kernel(const float *__restrict__ raw, EpiParams ep, int64_t ld,
-                                     int64_t split_stride, int splits, int64_t n_rows,
-                                     int64_t n_pad, int64_t r_chunks) {
+// One warp per (32 consecutive phase positions, 32-row chunk r0): sums the split-K partials
+// raw[z][n][r0 .. r0+31] in a fixed order (z = 0, 1, ...), then runs the same output stage as
+// the fused epilogue, which wants lane i to hold position n0 + i (positions padded to a
+// multiple of 32; lanes past the end store nothing).  The partials are read coalesced: each
+// 16-byte load instruction covers four positions' whole 128-byte runs (lane l: position
+// n0 + 4i + l/8, rows r0 + 4(l%8) ..), and the sums reach their lanes through a 32 x 33
+// shared tile (conflict-free both ways).  Each sum is the same sequence of fp32 additions as
+// one thread per position would make.
+constexpr int kReduceThreads = 64;
+
+__global__ void __launch_bounds__(kReduceThreads)
+    splitk_reduce_kernel(const float *__restrict__ raw, EpiParams ep, int64_t ld,
+                         int64_t split_stride, int splits, int64_t n_rows, int64_t n_pad,
+                         int64_t r_chunks) {
+    __shared__ float tile[kReduceThreads / 32][32][33];
     ptx::griddep_wait();
     ptx::griddep_launch_dependents();
     const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= n_pad * r_chunks) return;   // whole warps: n_pad * r_chunks is a multiple of 32
+    const int lane = (int)(threadIdx.x & 31);
+    float(*t)[33] = tile[threadIdx.x >> 5];
     const int64_t rc = idx / n_pad;
-    const int64_t n = idx - rc * n_pad;
+    const int64_t n = idx - rc * n_pad;     // this lane's position in the output stage
+    const int64_t n0 = n - lane;
     const int64_t r0 = rc * 32;
-    const bool live = n < n_rows;
-    float v[32];
+    const int c4 = 4 * (lane & 7);
+    const float *base = raw + r0 + c4;
+    int64_t off[8];
+    bool live[8];
+    float4 sum[8];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-    if (live) {
-        const float4 *p = reinterpret_cast<const float4 *>(raw + n * ld + r0);
+    for (int i = 0; i < 8; ++i) {
+        const int64_t np = n0 + 4 * i + (lane >> 3);
+        live[i] = np < n_rows;
+        off[i] = np * ld;
+        sum[i] = live[i] ? *reinterpret_cast<const float4 *>(base + off[i])
+                         : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+    // Two partials' loads in flight at once; the additions still run in split order.
+    for (int z = 1; z < splits; z += 2) {
+        float4 a[2][8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float4 a = p[i];
-            v[4 * i] = a.x;
-            v[4 * i + 1] = a.y;
-            v[4 * i + 2] = a.z;
-            v[4 * i + 3] = a.w;
+        for (int u = 0; u < 2; ++u) {
+            if (z + u >= splits) break;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                a[u][i] = live[i] ? *reinterpret_cast<const float4 *>(base + (z + u) * split_stride + off[i])
+                                  : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
-        // Up to four partials' loads in flight at once; the sums still run in split order.
-        for (int z = 1; z < splits; z += 4) {
-            float4 a[4][8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                if (z + u >= splits) break;
-                const float4 *q =
-                    reinterpret_cast<const float4 *>(raw + (z + u) * split_stride + n * ld + r0);
+        for (int u = 0; u < 2; ++u) {
+            if (z + u >= splits) break;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) a[u][i] = q[i];
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                if (z + u >= splits) break;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    v[4 * i] += a[u][i].x;
-                    v[4 * i + 1] += a[u][i].y;
-                    v[4 * i + 2] += a[u][i].z;
-                    v[4 * i + 3] += a[u][i].w;
-                }
+            for (int i = 0; i < 8; ++i) {
+                sum[i].x += a[u][i].x;
+                sum[i].y += a[u][i].y;
+                sum[i].z += a[u][i].z;
+                sum[i].w += a[u][i].w;
             }
         }
     }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float *row = t[4 * i + (lane >> 3)] + c4;
+        row[0] = sum[i].x;
+        row[1] = sum[i].y;
+        row[2] = sum[i].z;
+        row[3] = sum[i].w;
+    }
+    __syncwarp();
+    float v[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) v[r] = t[lane][r];
     // decode_pos marks positions at or past n_rows (= B * Py * Px) invalid.
-    emit_cols<kOutBoth, kIoAny>(v, decode_pos(n, ep), r0, ep, (int)(threadIdx.x & 31));
+    emit_cols<kOutBoth, kIoAny>(v, decode_pos(n, ep), r0, ep, lane);
 }
 
 // -------------------------------------------------------------------------- streaming
@@ -775,7 +790,8 @@ cudaError_t launch_splitk_reduce(const ctr_plan_s *pl, const float *raw, const E
     if (n_rows == 0 || r_chunks == 0) return cudaSuccess;
     cudaError_t e = prefer_max_smem<splitk_reduce_kernel>();
     if (e != cudaSuccess) return e;
-    e = launch_pdl(splitk_reduce_kernel, dim3(grid_for(total, 64)), dim3(64), 0, st, raw, ep,
+    e = launch_pdl(splitk_reduce_kernel, dim3(grid_for(total, kReduceThreads)),
+                   dim3(kReduceThreads), 0, st, raw, ep,
                    raw_ld, split_stride, pl->splits, n_rows, n_pad, r_chunks);
     if (e != cudaSuccess) return e;
     count_launches(1);

@@ -18,8 +18,8 @@ namespace ctr {
 constexpr int kBM = 128;
 constexpr int kBKBytes = 128;
 
-enum class Prec : int { BF16 = 0, TF32x3 = 1, F16 = 2 };
-constexpr bool is_16bit(Prec p) { return p != Prec::TF32x3; }
+enum class Prec : int { BF16 = 0, F32 = 1, F16 = 2 };
+constexpr bool is_16bit(Prec p) { return p != Prec::F32; }
 
 // I/O element type of a plan: the ctr_dtype code (CTR_F32, CTR_BF16, CTR_F16).
 enum IoType : int { IO_F32 = 0, IO_BF16 = 1, IO_F16 = 2 };
@@ -54,12 +54,12 @@ struct EpiParams {
     int shift2;         // sx = 2 runs at odd columns stored as pairs across lanes (epilogue.cuh)
     // Chained output (out_staged = 1): y is the next plan's staged input, channels-last rows
     // of ys_cpad channels, output (oy, ox) of batch b at row (b*ys_Py + oy + ys_hy)*ys_Px +
-    // ox + ys_hx; fp32 as tf32 hi and lo planes, ys_lo elements apart.
+    // ox + ys_hx; fp32 as the tf32 and cross planes (ptx::split_x), ys_lo elements apart.
     // The same output path writes a channels-last (NHWC) y: then ys_* describe y itself (no
     // halos, C_out channels per row) and ys_tf32 = 0 stores plain values.
     int out_staged;
     int64_t ys_Px, ys_Py, ys_hx, ys_hy, ys_cpad, ys_lo;
-    int ys_tf32;        // fp32 values as tf32 hi and lo planes (a staged operand)
+    int ys_tf32;        // fp32 values as the tf32 and cross planes (a staged operand)
     // Phase-major rows (pm_tc > 0, chained producers only): inside each tile of
     // pm_tc * S_pad rows, row j * pm_tc + c is phase j of the tile's channel c, so a 32-row
     // chunk holds whole channel runs of one (or a few) phases.
@@ -303,9 +303,12 @@ cudaError_t record_timing(cudaEvent_t ev, cudaStream_t st);
 size_t gemm_smem_bytes(Prec prec, int block_n);
 
 // Width in bytes (128 or 64) of the K slices a GEMM instantiation loads per pipeline stage:
-// 64 where 128-byte stages would leave fewer than four in shared memory.
+// 64 where 128-byte stages would leave only two in shared memory (fp32 operands, 256-row
+// tiles).  Four 48 KB stages hide the latency of operands that come from HBM better than two
+// of 96 KB (measured on GB300 with cold L2: codec upsampler 42.6 against 47.0 us), although
+// a 128-byte TMA box row moves more bytes per L2 request than a 64-byte one.
 constexpr int gemm_slice_bytes(Prec prec, int block_n) {
-    return prec == Prec::TF32x3 && block_n >= 256 ? 64 : 128;
+    return prec == Prec::F32 && block_n >= 256 ? 64 : 128;
 }
 
 // Largest phase-row tile whose accumulation groups fit the epilogue's registers.

@@ -500,7 +500,7 @@ __device__ __forceinline__ void emit_generic(const float (&v)[32], const PosInfo
 // ------------------------------------------------------------ chained output
 // The same outputs written into the next plan's staged input (EpiParams::out_staged):
 // channels-last, so the G channels of one output position are G consecutive elements.
-// fp32 values are split into tf32 hi and lo planes exactly as the staging kernel does.
+// fp32 values are split into the tf32 and cross planes exactly as the staging kernel does.
 
 // Row of the staged buffer holding output (b, oy, ox).
 __device__ __forceinline__ int64_t staged_row(const EpiParams &e, int64_t b, int64_t oy,
@@ -509,7 +509,7 @@ __device__ __forceinline__ int64_t staged_row(const EpiParams &e, int64_t b, int
 }
 
 // N consecutive channel values at dst (N * sizeof(T)-aligned): one plane for 16-bit types;
-// for fp32 the tf32 hi and lo planes of a staged operand, or the values of a channels-last y.
+// for fp32 the tf32 and cross planes of a staged operand, or the values of a channels-last y.
 template <typename T, int N>
 __device__ __forceinline__ void store_channels(T *dst, const float *vals, const EpiParams &e) {
     constexpr int kBytes = N * (int)sizeof(T) < 16 ? N * (int)sizeof(T) : 16;
@@ -520,14 +520,15 @@ __device__ __forceinline__ void store_channels(T *dst, const float *vals, const 
             store_run<T, N>(dst, vals, kBytes);
             return;
         }
-        float hi[N], lo[N];
+        float hi[N], cr[N];
 #pragma unroll
         for (int i = 0; i < N; ++i) {
-            hi[i] = ptx::to_tf32(vals[i]);
-            lo[i] = ptx::to_tf32(vals[i] - hi[i]);
+            uint32_t c;
+            hi[i] = ptx::split_x(vals[i], c);
+            cr[i] = __uint_as_float(c);
         }
         store_run<T, N>(dst, hi, kBytes);
-        store_run<T, N>(dst + e.ys_lo, lo, kBytes);
+        store_run<T, N>(dst + e.ys_lo, cr, kBytes);
     }
 }
 

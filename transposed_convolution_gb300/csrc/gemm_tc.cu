@@ -32,16 +32,16 @@ GemmLayout gemm_layout(Prec prec, int block_n) {
     if (is_16bit(prec))   // fp16 and bf16 instantiations have the same layout
         return block_n == 256 ? layout_of<Prec::BF16, 256>()
                : block_n == 128 ? layout_of<Prec::BF16, 128>() : layout_of<Prec::BF16, 64>();
-    return block_n == 256 ? layout_of<Prec::TF32x3, 256>()
-           : block_n == 128 ? layout_of<Prec::TF32x3, 128>() : layout_of<Prec::TF32x3, 64>();
+    return block_n == 256 ? layout_of<Prec::F32, 256>()
+           : block_n == 128 ? layout_of<Prec::F32, 128>() : layout_of<Prec::F32, 64>();
 }
 
 size_t gemm_smem_bytes(Prec prec, int block_n) {
     if (is_16bit(prec))
         return block_n == 256 ? Cfg<Prec::BF16, 256>::kSmem
                : block_n == 128 ? Cfg<Prec::BF16, 128>::kSmem : Cfg<Prec::BF16, 64>::kSmem;
-    return block_n == 256 ? Cfg<Prec::TF32x3, 256>::kSmem
-           : block_n == 128 ? Cfg<Prec::TF32x3, 128>::kSmem : Cfg<Prec::TF32x3, 64>::kSmem;
+    return block_n == 256 ? Cfg<Prec::F32, 256>::kSmem
+           : block_n == 128 ? Cfg<Prec::F32, 128>::kSmem : Cfg<Prec::F32, 64>::kSmem;
 }
 
 cudaError_t launch_gemm_tc(const ctr_plan_s *pl, const CUtensorMap *maps, const GemmParams &gp,
@@ -57,9 +57,9 @@ cudaError_t launch_gemm_tc(const ctr_plan_s *pl, const CUtensorMap *maps, const 
         }
     }
     switch (pl->block_n) {
-        case 256: return launch_bn<Prec::TF32x3, 256>(pl, maps, gp, st);
-        case 128: return launch_bn<Prec::TF32x3, 128>(pl, maps, gp, st);
-        default: return launch_bn<Prec::TF32x3, 64>(pl, maps, gp, st);
+        case 256: return launch_bn<Prec::F32, 256>(pl, maps, gp, st);
+        case 128: return launch_bn<Prec::F32, 128>(pl, maps, gp, st);
+        default: return launch_bn<Prec::F32, 64>(pl, maps, gp, st);
     }
 }
 

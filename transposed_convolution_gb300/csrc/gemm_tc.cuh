@@ -29,10 +29,17 @@
 //               taking the first BN/2 columns and the other the rest.
 // Several accumulators let the epilogue of tile i overlap the MMAs of tile i + 1.
 //
-// 3xTF32 (fp32 I/O): both operands come as tf32 hi and lo planes (x = hi + lo, each
-// rounded to tf32) and every K step issues lo*hi + hi*lo + hi*hi into the same fp32
-// accumulator -- the split of Ootomo and Yokota, "Recovering single precision accuracy from
-// Tensor Cores while surpassing the FP32 theoretical peak performance" (IJHPCA 2022).
+// fp32 I/O: each operand value v is split as hi = tf32(v) and lo = v - hi, the idea of Ootomo
+// and Yokota, "Recovering single precision accuracy from Tensor Cores while surpassing the
+// FP32 theoretical peak performance" (IJHPCA 2022), who issue hi*hi, hi*lo and lo*hi as three
+// tf32 MMAs.  Here the two cross products are one kind::f16 MMA on bf16 pairs instead: every
+// 32-byte K step issues that bf16 MMA (16 bf16 = 8 K elements x (hi, lo), from the second
+// operand plane; ptx::split_x / split_w) and then the tf32 MMA of hi*hi (8 K elements, first
+// plane) into the same fp32 accumulator.  The bf16 MMA of K 16 takes the tensor pipe as long
+// as the tf32 MMA of K 8, so a K step costs two tf32 MMA times instead of three, and the
+// shared-memory operand reads drop by the same third.  The bf16 roundings of the cross terms
+// (each below 2^-11 of the product) cost at most about 2^-17 of a product's value, well
+// inside fp32 I/O's accuracy bound.
 //
 // Every mbarrier wait is bounded (wait_limit_ns of global time).  A wait that gives up sets
 // a bit in the plan's status word and a CTA-wide abort flag; every role then stops, the
@@ -63,9 +70,9 @@ constexpr uint64_t kDrainLimitNs = 2000000000ull;
 
 template <Prec P, int BN>
 struct Cfg {
-    static constexpr int kPlanes = P == Prec::TF32x3 ? 2 : 1;
+    static constexpr int kPlanes = P == Prec::F32 ? 2 : 1;
     static constexpr int kSlice = gemm_slice_bytes(P, BN);  // K bytes per row per stage
-    static constexpr int kElems = kSlice / (P == Prec::TF32x3 ? 4 : 2);
+    static constexpr int kElems = kSlice / (P == Prec::F32 ? 4 : 2);
     static constexpr int kKSteps = kSlice / 32;              // MMA K steps of 32 bytes
     static constexpr int kXBytes = kBM * kSlice;             // one 128-position Xs slice
     static constexpr int kWBytes = BN * kSlice;              // one BN-row weight slice
@@ -77,10 +84,10 @@ struct Cfg {
     static constexpr int kStagesRaw = (kSmemBudget - 1024 - kBarBytes) / kStageBytes;
     static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
     static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes;
-    // Grouped 3xTF32 accumulation keeps its running sums in a TMEM region of BN columns
+    // Grouped fp32 accumulation keeps its running sums in a TMEM region of BN columns
     // beside the accumulators for BN >= 128 (in registers they would not fit the 168 a
     // thread has with 10 warps per SM), in registers for BN = 64.
-    static constexpr bool kTmemSum = P == Prec::TF32x3 && BN >= 128;
+    static constexpr bool kTmemSum = P == Prec::F32 && BN >= 128;
     // TMEM accumulators: as many BN-column buffers as fit 512 columns (less the sum region),
     // at most 4, so the MMA can run several tiles ahead of the epilogue.
     static constexpr int kTmemBudget = 512 / kCtas;   // TMEM columns of one CTA
@@ -92,7 +99,9 @@ struct Cfg {
     static constexpr bool kSumFirst = kTmemSum && kAccBufs == 1;
     static constexpr uint32_t kTmemCols = kAccBufs * BN + (kTmemSum ? BN : 0);
     static constexpr uint32_t kIdesc = ptx::idesc_f32acc(
-        P == Prec::TF32x3 ? ptx::kFmtTF32 : (P == Prec::F16 ? ptx::kFmtF16 : ptx::kFmtBF16), kBM, BN);
+        P == Prec::F32 ? ptx::kFmtTF32 : (P == Prec::F16 ? ptx::kFmtF16 : ptx::kFmtBF16), kBM, BN);
+    // fp32 I/O: the cross products' MMA (bf16 pairs of the second operand plane).
+    static constexpr uint32_t kIdescCross = ptx::idesc_f32acc(ptx::kFmtBF16, kBM, BN);
     static_assert(kStages >= 2, "at least two pipeline stages");
     static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512,
                   "TMEM allocation is a power of two");
@@ -204,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
     if (warp == 0 && lane == 0) {
         ptx::tma_prefetch_desc(&mapX);
         ptx::tma_prefetch_desc(&mapW);
-        if (P == Prec::TF32x3) {
+        if (P == Prec::F32) {
             ptx::tma_prefetch_desc(&mapX2);
             ptx::tma_prefetch_desc(&mapW2);
         }
@@ -230,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
             uint32_t phase = 0;
             int64_t issued = 0;
             bool w_issued = false;
-            if constexpr (P != Prec::TF32x3) {
+            if constexpr (P != Prec::F32) {
                 if (gp.xshare) {
                     // Shared-X mode: per tile and channel slice kc, one X box of x_rows rows at
                     // the tile's first tap row; the taps' weight slices with it, or the whole
@@ -291,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
                     const int32_t w_row = (int32_t)tc.r0;
                     ptx::tma_load_2d(x_slice(stage, 0), &mapX, &full[stage], x_k, x_row);
                     ptx::tma_load_2d(w_slice(stage, 0), &mapW, &full[stage], w_k, w_row);
-                    if (P == Prec::TF32x3) {
+                    if (P == Prec::F32) {
                         ptx::tma_load_2d(x_slice(stage, 1), &mapX2, &full[stage], x_k, x_row);
                         ptx::tma_load_2d(w_slice(stage, 1), &mapW2, &full[stage], w_k, w_row);
                     }
@@ -329,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
             int grp = 0;    // accumulator groups issued by this CTA (selects the TMEM buffer)
             int items = 0;  // tiles issued by this CTA (kSumFirst barrier phases)
             bool ok = true;
-            if constexpr (P != Prec::TF32x3) {
+            if constexpr (P != Prec::F32) {
                 if (gp.xshare) {
                     // Shared-X mode: one accumulation group per tile; for every channel slice
                     // the taps read the same X box, tap g starting g rows further down (a
@@ -420,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
                         const uint64_t xd = ptx::sdesc_k<C::kSlice>(ptx::smem_u32(x_slice(stage, 0)));
                         const uint64_t wd = ptx::sdesc_k<C::kSlice>(ptx::smem_u32(w_slice(stage, 0)));
                         uint64_t xdl = 0, wdl = 0;
-                        if (P == Prec::TF32x3) {
+                        if (P == Prec::F32) {
                             xdl = ptx::sdesc_k<C::kSlice>(ptx::smem_u32(x_slice(stage, 1)));
                             wdl = ptx::sdesc_k<C::kSlice>(ptx::smem_u32(w_slice(stage, 1)));
                         }
@@ -428,10 +437,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
                         for (int k = 0; k < C::kKSteps; ++k) {  // 32-byte K steps of the slice
                             // +2 in the descriptor's start-address field = +32 bytes
                             const uint64_t dk = (uint64_t)(2 * k);
-                            if (P == Prec::TF32x3) {
+                            if (P == Prec::F32) {
                                 if (ptx::elect_one()) {
-                                    ptx::mma_tf32(d_tmem, xdl + dk, wd + dk, C::kIdesc, accumulate);
-                                    ptx::mma_tf32(d_tmem, xd + dk, wdl + dk, C::kIdesc, 1u);
+                                    ptx::mma_f16(d_tmem, xdl + dk, wdl + dk, C::kIdescCross, accumulate);
                                     ptx::mma_tf32(d_tmem, xd + dk, wd + dk, C::kIdesc, 1u);
                                 }
                             } else {
@@ -551,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(sum_free);
                 }
-            } else if (P != Prec::TF32x3 || ngroups == 1) {
+            } else if (P != Prec::F32 || ngroups == 1) {
                 // One accumulation group: straight from TMEM to the output stage.
                 if (!(ok = wait_group(grp))) break;
 #pragma unroll 1
@@ -566,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
                     store_chunk_out<P, CHAIN>(gp, tc, ps, fused, quad, lane, c_base + c, v);
                 }
                 ++grp;
-            } else if constexpr (P == Prec::TF32x3 && !C::kTmemSum) {
+            } else if constexpr (P == Prec::F32 && !C::kTmemSum) {
                 // BN = 64 only.
                 // Several groups: each group's partial leaves TMEM and is added, with fp32
                 // round-to-nearest, into running sums held in registers (this thread's

@@ -14,9 +14,9 @@ cudaError_t launch_gemm_tc_chain(const ctr_plan_s *pl, const CUtensorMap *maps,
         }
     }
     switch (pl->block_n) {
-        case 256: return launch_inst<Prec::TF32x3, 256, true>(pl, maps, gp, st);
-        case 128: return launch_inst<Prec::TF32x3, 128, true>(pl, maps, gp, st);
-        default: return launch_inst<Prec::TF32x3, 64, true>(pl, maps, gp, st);
+        case 256: return launch_inst<Prec::F32, 256, true>(pl, maps, gp, st);
+        case 128: return launch_inst<Prec::F32, 128, true>(pl, maps, gp, st);
+        default: return launch_inst<Prec::F32, 64, true>(pl, maps, gp, st);
     }
 }
 

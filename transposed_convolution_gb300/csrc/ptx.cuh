@@ -286,5 +286,32 @@ __device__ __forceinline__ float to_tf32(float x) {
     return __uint_as_float(r);
 }
 
+// fp32 operands on the tensor cores.  A value v is split into hi = tf32(v), which the
+// kind::tf32 MMA reads from the first operand plane, and lo = v - hi (exact in fp32).  The
+// second plane holds, per K element, one 32-bit word of two bf16 halves, bf16(hi) and
+// bf16(lo), read by one kind::f16 MMA of twice the K: the input operand's word has bf16(hi)
+// in its low half (the lower K index), the weight's has bf16(lo) there, so the products
+// pair crosswise and the MMA adds hi_x * lo_w + lo_x * hi_w.  The dropped lo_x * lo_w is
+// below 2^-22 of x * w, each cross product is off by at most about 2^-18 of it (two bf16
+// roundings of a term below 2^-11 of it), and the three products of the 3xTF32 split (hi *
+// hi, hi * lo, lo * hi in tf32) take one tf32 and one bf16 MMA here.
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo_half, float hi_half) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi_half), "f"(lo_half));
+    return r;
+}
+// Input operand: returns tf32(v) and sets the cross word (bf16(hi) low, bf16(lo) high).
+__device__ __forceinline__ float split_x(float v, uint32_t &cross) {
+    const float hi = to_tf32(v);
+    cross = bf16x2_rn(hi, v - hi);
+    return hi;
+}
+// Weight operand: returns tf32(v) and sets the cross word (bf16(lo) low, bf16(hi) high).
+__device__ __forceinline__ float split_w(float v, uint32_t &cross) {
+    const float hi = to_tf32(v);
+    cross = bf16x2_rn(v - hi, hi);
+    return hi;
+}
+
 }  // namespace ptx
 }  // namespace ctr
