@@ -129,13 +129,12 @@ double choose_tiling(ctr_plan_s *pl, double epi_factor = 1.0) {
             const double epi = epi_factor * ctr::kBM * (double)bn * esize_io(pl) / 20.0 + 300.0;
             double t;
             if (prec == Prec::F32) {
-                // Two operand planes.  Fitted to forced-tile timings on GB300 with operands
-                // coming from HBM (inputs and weights rotated past twice the L2): 256-row
-                // tiles load at ~55 B per clock per SM, smaller ones at ~65.  A 256-row tile
-                // has one accumulator: its output stage does not overlap the next work
-                // unit's MMAs, and folding each accumulation group into the sums pauses
-                // them (~600 clocks).
-                const double load = kbs * (ctr::kBM + bn) * (double)ctr::kBKBytes * 2 / (bn == 256 ? 55.0 : 65.0);
+                // Two operand planes, loaded at ~65 B per clock per SM (fitted to forced-tile
+                // timings on GB300 with operands coming from HBM: inputs and weights rotated
+                // past twice the L2).  A 256-row tile has one accumulator: its output stage
+                // does not overlap the next work unit's MMAs, and folding each accumulation
+                // group into the sums pauses them (~600 clocks).
+                const double load = kbs * (ctr::kBM + bn) * (double)ctr::kBKBytes * 2 / 65.0;
                 double unit = std::max(mma, load);
                 if (bn == 256) {
                     unit += 600.0 * (std::ceil(kbs / std::min(kbs, (double)group)) - 1.0);

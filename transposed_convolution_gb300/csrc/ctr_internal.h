@@ -14,7 +14,7 @@ namespace ctr {
 
 // Tile shape of the tensor-core GEMM: 128 rows (TMEM lanes) x BN columns.  The packed
 // operands' K extents are multiples of 128 bytes (64 bf16 or 32 fp32); the kernel moves K
-// in slices of 128 or 64 bytes (see gemm_slice_bytes).
+// in slices of 128 bytes (see gemm_slice_bytes).
 constexpr int kBM = 128;
 constexpr int kBKBytes = 128;
 
@@ -302,14 +302,12 @@ cudaError_t record_timing(cudaEvent_t ev, cudaStream_t st);
 // Bytes of dynamic shared memory a GEMM instantiation uses.
 size_t gemm_smem_bytes(Prec prec, int block_n);
 
-// Width in bytes (128 or 64) of the K slices a GEMM instantiation loads per pipeline stage:
-// 64 where 128-byte stages would leave only two in shared memory (fp32 operands, 256-row
-// tiles).  Four 48 KB stages hide the latency of operands that come from HBM better than two
-// of 96 KB (measured on GB300 with cold L2: codec upsampler 42.6 against 47.0 us), although
-// a 128-byte TMA box row moves more bytes per L2 request than a 64-byte one.
-constexpr int gemm_slice_bytes(Prec prec, int block_n) {
-    return prec == Prec::F32 && block_n >= 256 ? 64 : 128;
-}
+// Width in bytes of the K slices a GEMM instantiation loads: 128, one 128-byte swizzle row.
+// A TMA box row costs about the same whatever its width, so 128-byte rows move more bytes per
+// SM than 64-byte ones (measured on GB300: 51 against 33 B per clock with four 48 KB stages
+// in flight).  fp32 256-row tiles put one operand plane in each stage (gemm_tc.cuh), which
+// keeps four stages for operands that come from HBM.
+constexpr int gemm_slice_bytes(Prec, int) { return 128; }
 
 // Largest phase-row tile whose accumulation groups fit the epilogue's registers.
 constexpr int kMaxGroupedBN = 256;

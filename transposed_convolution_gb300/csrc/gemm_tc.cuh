@@ -76,7 +76,13 @@ struct Cfg {
     static constexpr int kKSteps = kSlice / 32;              // MMA K steps of 32 bytes
     static constexpr int kXBytes = kBM * kSlice;             // one 128-position Xs slice
     static constexpr int kWBytes = BN * kSlice;              // one BN-row weight slice
-    static constexpr int kStageBytes = kPlanes * (kXBytes + kWBytes);
+    // fp32 256-row tiles: each stage holds one operand plane of a K slice (the tf32 plane or
+    // the cross plane), so four 48 KB stages of 128-byte rows fit; a K slice takes two
+    // stages.  Otherwise a stage holds every plane of its K slice.
+    static constexpr bool kPlaneStages = P == Prec::F32 && BN >= 256;
+    static constexpr int kStagePlanes = kPlaneStages ? 1 : kPlanes;
+    static constexpr int kStagesPerSlice = kPlaneStages ? kPlanes : 1;
+    static constexpr int kStageBytes = kStagePlanes * (kXBytes + kWBytes);
     static constexpr int kBarBytes = kGemmBarBytes;
     static constexpr int kCtas = ctas_per_sm(P, BN);
     // Two CTAs share an SM's 228 KB (each also reserves 1 KB for the system).
@@ -190,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
         return stage_base + s * gp.stage_bytes + plane * C::kXBytes;
     };
     auto w_slice = [&](int s, int plane) -> uint8_t * {
-        return stage_base + s * gp.stage_bytes + C::kPlanes * C::kXBytes + plane * C::kWBytes;
+        return stage_base + s * gp.stage_bytes + C::kStagePlanes * C::kXBytes + plane * C::kWBytes;
     };
 
     if (threadIdx.x == 0) {
@@ -288,33 +294,42 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
                 int kc = tc.kb0 - g0 * gp.kb_per_tap;
                 int uy = g0 / gp.mx;
                 int ux = g0 - uy * gp.mx;
-                for (int kb = tc.kb0; kb < tc.kb1; ++kb) {
-                    if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, limit, abort)) {
-                        if (!*abort) give_up(abort, gp.status, kStatusTimeoutProducer);
-                        break;
-                    }
-                    ptx::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+                bool stop = false;
+                for (int kb = tc.kb0; kb < tc.kb1 && !stop; ++kb) {
                     const int32_t x_k = kc * C::kElems;
                     const int32_t w_k = kb * C::kElems;
                     const int32_t x_row = (int32_t)(tc.p0 + gp.shift0 + (int64_t)uy * gp.Px + ux);
                     const int32_t w_row = (int32_t)tc.r0;
-                    ptx::tma_load_2d(x_slice(stage, 0), &mapX, &full[stage], x_k, x_row);
-                    ptx::tma_load_2d(w_slice(stage, 0), &mapW, &full[stage], w_k, w_row);
-                    if (P == Prec::F32) {
-                        ptx::tma_load_2d(x_slice(stage, 1), &mapX2, &full[stage], x_k, x_row);
-                        ptx::tma_load_2d(w_slice(stage, 1), &mapW2, &full[stage], w_k, w_row);
+                    for (int sp = 0; sp < C::kStagesPerSlice; ++sp) {
+                        if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, limit, abort)) {
+                            if (!*abort) give_up(abort, gp.status, kStatusTimeoutProducer);
+                            stop = true;
+                            break;
+                        }
+                        ptx::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+                        if constexpr (C::kPlaneStages) {
+                            ptx::tma_load_2d(x_slice(stage, 0), sp ? &mapX2 : &mapX, &full[stage], x_k, x_row);
+                            ptx::tma_load_2d(w_slice(stage, 0), sp ? &mapW2 : &mapW, &full[stage], w_k, w_row);
+                        } else {
+                            ptx::tma_load_2d(x_slice(stage, 0), &mapX, &full[stage], x_k, x_row);
+                            ptx::tma_load_2d(w_slice(stage, 0), &mapW, &full[stage], w_k, w_row);
+                            if (P == Prec::F32) {
+                                ptx::tma_load_2d(x_slice(stage, 1), &mapX2, &full[stage], x_k, x_row);
+                                ptx::tma_load_2d(w_slice(stage, 1), &mapW2, &full[stage], w_k, w_row);
+                            }
+                        }
+                        ++issued;
+                        if (++stage == nst) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
-                    ++issued;
                     if (++kc == gp.kb_per_tap) {
                         kc = 0;
                         if (++ux == gp.mx) {
                             ux = 0;
                             ++uy;
                         }
-                    }
-                    if (++stage == nst) {
-                        stage = 0;
-                        phase ^= 1u;
                     }
                 }
             }
@@ -419,40 +434,51 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
                     const uint32_t d_tmem =
                         tmem_base + (to_sum ? C::kSumCol : (uint32_t)(acc * BN));
                     uint32_t accumulate = 0;
-                    for (; kb < kb_end; ++kb) {
-                        if (!ptx::mbar_wait_warp(&full[stage], phase, limit, abort)) {
-                            if (lane == 0 && !*abort) give_up(abort, gp.status, kStatusTimeoutMma);
-                            ok = false;
-                            break;
-                        }
-                        ptx::tc_fence_after();
-                        const uint64_t xd = ptx::sdesc_k<C::kSlice>(ptx::smem_u32(x_slice(stage, 0)));
-                        const uint64_t wd = ptx::sdesc_k<C::kSlice>(ptx::smem_u32(w_slice(stage, 0)));
-                        uint64_t xdl = 0, wdl = 0;
-                        if (P == Prec::F32) {
-                            xdl = ptx::sdesc_k<C::kSlice>(ptx::smem_u32(x_slice(stage, 1)));
-                            wdl = ptx::sdesc_k<C::kSlice>(ptx::smem_u32(w_slice(stage, 1)));
-                        }
-#pragma unroll
-                        for (int k = 0; k < C::kKSteps; ++k) {  // 32-byte K steps of the slice
-                            // +2 in the descriptor's start-address field = +32 bytes
-                            const uint64_t dk = (uint64_t)(2 * k);
-                            if (P == Prec::F32) {
-                                if (ptx::elect_one()) {
-                                    ptx::mma_f16(d_tmem, xdl + dk, wdl + dk, C::kIdescCross, accumulate);
-                                    ptx::mma_tf32(d_tmem, xd + dk, wd + dk, C::kIdesc, 1u);
-                                }
-                            } else {
-                                if (ptx::elect_one())
-                                    ptx::mma_f16(d_tmem, xd + dk, wd + dk, C::kIdesc, accumulate);
+                    for (; ok && kb < kb_end; ++kb) {
+                        for (int sp = 0; sp < C::kStagesPerSlice; ++sp) {
+                            if (!ptx::mbar_wait_warp(&full[stage], phase, limit, abort)) {
+                                if (lane == 0 && !*abort) give_up(abort, gp.status, kStatusTimeoutMma);
+                                ok = false;
+                                break;
                             }
-                            accumulate = 1u;
-                        }
-                        if (ptx::elect_one())
-                            ptx::mma_commit(&empty[stage]);  // frees the stage once these MMAs finish
-                        if (++stage == nst) {
-                            stage = 0;
-                            phase ^= 1u;
+                            ptx::tc_fence_after();
+                            const uint64_t xd = ptx::sdesc_k<C::kSlice>(ptx::smem_u32(x_slice(stage, 0)));
+                            const uint64_t wd = ptx::sdesc_k<C::kSlice>(ptx::smem_u32(w_slice(stage, 0)));
+                            uint64_t xdl = 0, wdl = 0;
+                            if (P == Prec::F32 && !C::kPlaneStages) {
+                                xdl = ptx::sdesc_k<C::kSlice>(ptx::smem_u32(x_slice(stage, 1)));
+                                wdl = ptx::sdesc_k<C::kSlice>(ptx::smem_u32(w_slice(stage, 1)));
+                            }
+#pragma unroll
+                            for (int k = 0; k < C::kKSteps; ++k) {  // 32-byte K steps of the slice
+                                // +2 in the descriptor's start-address field = +32 bytes
+                                const uint64_t dk = (uint64_t)(2 * k);
+                                if constexpr (C::kPlaneStages) {
+                                    // the tf32 plane's stage first (hi*hi), then the cross
+                                    // plane's (hi*lo + lo*hi)
+                                    if (ptx::elect_one()) {
+                                        if (sp == 0)
+                                            ptx::mma_tf32(d_tmem, xd + dk, wd + dk, C::kIdesc, accumulate);
+                                        else
+                                            ptx::mma_f16(d_tmem, xd + dk, wd + dk, C::kIdescCross, 1u);
+                                    }
+                                } else if (P == Prec::F32) {
+                                    if (ptx::elect_one()) {
+                                        ptx::mma_f16(d_tmem, xdl + dk, wdl + dk, C::kIdescCross, accumulate);
+                                        ptx::mma_tf32(d_tmem, xd + dk, wd + dk, C::kIdesc, 1u);
+                                    }
+                                } else {
+                                    if (ptx::elect_one())
+                                        ptx::mma_f16(d_tmem, xd + dk, wd + dk, C::kIdesc, accumulate);
+                                }
+                                accumulate = 1u;
+                            }
+                            if (ptx::elect_one())
+                                ptx::mma_commit(&empty[stage]);  // frees the stage once these MMAs finish
+                            if (++stage == nst) {
+                                stage = 0;
+                                phase ^= 1u;
+                            }
                         }
                     }
                     if (ok && ptx::elect_one()) ptx::mma_commit(to_sum ? sum_full : &tmem_full[acc]);
