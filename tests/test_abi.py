@@ -570,3 +570,25 @@ def test_istft_plan_without_gpu(ctr):
     assert e.value.status == ctr.CTR_ERR_UNSUPPORTED
     assert ctr.lib.ctr_istft_workspace_bytes(None) == 0
     ctr.ctr_istft_destroy(None)
+
+
+def test_tile_model_choices_without_gpu(ctr):
+    """The tile model's (BN, split-K) for the fp32 shapes its constants were fitted to: for
+    each, the fastest of the BN 64/128/256 x split-K grid in forced-tile timings on GB300
+    with inputs and weights cold in HBM (the benchmark's regime)."""
+    cases = [  # (ndim, B, C_in, C_out, L, k, s, p) -> (BN, splits)
+        ((1, 1, 512, 256, [2000], [16], [8], [4]), (256, 1)),           # codec upsampler
+        ((2, 1, 128, 64, [128, 128], [4, 4], [2, 2], [1, 1]), (256, 1)),  # 2-D decoder
+        ((1, 4, 4098, 1, [343], [4096], [1024], [0]), (256, 3)),        # iSTFT
+        ((1, 2, 256, 128, [1500], [8], [4], [2]), (128, 1)),
+        ((1, 1, 1024, 64, [4000], [4], [2], [1]), (128, 4)),
+    ]
+    for (nd, B, ci, co, L, k, s, p), (bn, sp) in cases:
+        h = _plan(ctr, nd, B, ci, co, L, k, s, p, [0] * nd, ctr.CTR_F32)
+        try:
+            d = ctr.ctr_plan_describe(h)
+            if "sms=152 " not in d:
+                pytest.skip("the model's choices are pinned for 152 SMs: " + d)
+            assert "BN %d," % bn in d and "splits=%d " % sp in d, d
+        finally:
+            ctr.ctr_plan_destroy(h)
