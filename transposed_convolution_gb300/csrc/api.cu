@@ -91,6 +91,19 @@ int tf32_group() {
     return v > 0 ? v : kNoGroup;
 }
 
+// Whether the GEMM runs in X-ring mode (gemm_tc.cuh): fp32 polyphase plans on 256-row
+// tiles with at least four taps along x.  The taps of one tap row then share one staged-
+// input box of 128 + mx - 1 rows (at most 256, a TMA box's height), and the split-K units
+// take whole channel slices.  The operand bytes per K slice drop (by 24% at four taps), but
+// the weight ring then holds 128 KB instead of 192, and an SM's TMA feed follows the bytes
+// in flight: measured on GB300 with operands in HBM, the iSTFT (four taps) ran 163.9 ->
+// 161.8 us and two-tap layers 2-3% slower, hence the four-tap threshold.
+bool xring_eligible(const ctr_plan_s *pl, int bn, int splits) {
+    if (prec_of(pl) != Prec::F32 || pl->path != CTR_PATH_POLYPHASE || bn != 256) return false;
+    if (pl->m[1] < 4 || ctr::kBM + pl->m[1] - 1 > 256) return false;
+    return splits <= pl->C_in_pad * 4 / ctr::kBKBytes;
+}
+
 // Choose the phase-row tile BN in {64, 128, 256} and the split-K factor: fewest estimated
 // clocks, counting whole waves of tiles over the SMs, a tile's time from its MMA time, its
 // operand-load time and its output time, and the extra pass over split-K partials.
@@ -546,6 +559,27 @@ void set_pipeline_layout(const ctr_plan_s *pl, GemmParams *gp) {
     gp->wres_off = 0;
     gp->bar_off = lay.stages * lay.stage_bytes;
     gp->smem_bytes = 1024 + gp->bar_off + kGemmBarBytes;
+    gp->xring = 0;
+    gp->xring_off = 0;
+    gp->my = (int)pl->m[0];
+    if (xring_eligible(pl, pl->block_n, pl->splits)) {
+        // X-ring mode: the weight ring of one-plane, one-tap stages, then two X slots (a
+        // box of both planes each), then the barriers.
+        const int x_rows = (int)((kBM + pl->m[1] - 1 + 7) / 8 * 8);
+        const int64_t slot_bytes = 2 * (int64_t)x_rows * lay.slice_bytes;
+        const int64_t avail = lay.smem_budget - 1024 - kGemmBarBytes - 2 * slot_bytes;
+        const int64_t stages = std::min<int64_t>(avail / lay.w_box_bytes, kGemmMaxStages);
+        if (stages >= 3) {
+            gp->xring = 1;
+            gp->x_rows = x_rows;
+            gp->nstages = (int)stages;
+            gp->stage_bytes = lay.w_box_bytes;
+            gp->xring_off = (int)(stages * lay.w_box_bytes);
+            gp->bar_off = gp->xring_off + (int)(2 * slot_bytes);
+            gp->smem_bytes = 1024 + gp->bar_off + kGemmBarBytes;
+        }
+        return;
+    }
     if (!is_16bit(prec) || pl->path != CTR_PATH_POLYPHASE || pl->splits != 1 ||
         pl->m[0] != 1 || pl->m[1] < 2)
         return;
@@ -610,7 +644,7 @@ cudaError_t run_tc_path(const ctr_plan_s *pl, const void *x, const void *w_packe
     if (!h16) {
         ok = ok &&
              encode_2d(&maps[2], static_cast<char *>(xs) + x_plane, IO_F32, pl->C_in_pad,
-                       pl->N_total, kBM, sb) &&
+                       pl->N_total, (uint32_t)gp.x_rows, sb) &&
              encode_2d(&maps[3], static_cast<const char *>(w_packed) + w_plane, IO_F32,
                        pl->K_total, pl->M_pad, pl->block_n, sb);
     } else {
@@ -1082,7 +1116,8 @@ ctr_status ctr_plan_describe(ctr_plan_t pl, char *buf, size_t len) {
         const size_t used = strlen(buf);
         if (used + 1 < len)
             snprintf(buf + used, len - used, " stages=%d%s", gp.nstages,
-                     gp.xshare ? (gp.wres ? " shared-x resident-w" : " shared-x") : "");
+                     gp.xring ? " x-ring"
+                              : gp.xshare ? (gp.wres ? " shared-x resident-w" : " shared-x") : "");
     }
     if (pl->nhwc) {
         const size_t used = strlen(buf);

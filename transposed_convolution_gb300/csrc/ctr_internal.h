@@ -94,6 +94,12 @@ struct GemmParams {
     // it through a descriptor that starts tap rows further down; the stage also holds the
     // taps' weight slices, unless the whole weight tile stays resident (wres) at wres_off.
     int xshare, x_rows, wres, wres_off;
+    // X-ring mode (fp32 256-row tiles with four or more taps along x): the X boxes (x_rows rows,
+    // both operand planes) of one channel slice and tap row sit in a ring of two slots at
+    // xring_off, read by that row's mx taps through row-shifted descriptors; the weight
+    // boxes (one plane of one tap) stream through the nstages-stage ring.  K is walked as
+    // slices s = kc * (my * mx) + tap, so a split-K unit covers whole channel slices.
+    int xring, xring_off, my;
 };
 
 // Shared-memory layout of one GEMM instantiation (gemm_tc.cu): default stage count and

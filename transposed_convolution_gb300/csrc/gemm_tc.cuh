@@ -132,7 +132,14 @@ __device__ __forceinline__ TileCoord decode_tile(uint32_t t, const GemmParams &g
     c.z = (int)z;
     c.r0 = (int)(r_tile * (uint32_t)bn);
     c.p0 = (int)(p_tile * (uint32_t)kBM);
-    const uint32_t kbt = (uint32_t)gp.kb_total, sp = (uint32_t)gp.splits;
+    const uint32_t sp = (uint32_t)gp.splits;
+    if (gp.xring) {   // whole channel slices per split: slices kc * taps + tap
+        const uint32_t kpt = (uint32_t)gp.kb_per_tap, taps = (uint32_t)(gp.mx * gp.my);
+        c.kb0 = (int)((z * kpt / sp) * taps);
+        c.kb1 = (int)(((z + 1) * kpt / sp) * taps);
+        return c;
+    }
+    const uint32_t kbt = (uint32_t)gp.kb_total;
     c.kb0 = (int)(z * kbt / sp);
     c.kb1 = (int)((z + 1) * kbt / sp);
     return c;
@@ -186,7 +193,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
     uint64_t *sum_full = drain + 1;   // kSumFirst: a tile's first group is in the sum region
     uint64_t *sum_free = drain + 2;   // kSumFirst: the epilogue has read a tile's sums
     uint64_t *w_full = drain + 3;     // shared-X mode: the resident weight has landed
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 4);
+    uint64_t *xfull = drain + 4;      // X-ring mode: slot 0/1 holds its box
+    uint64_t *xempty = drain + 6;     // X-ring mode: slot 0/1 may be refilled
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 8);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -212,6 +221,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
         ptx::mbar_init(sum_full, 1);
         ptx::mbar_init(sum_free, kEpiWarps);
         ptx::mbar_init(w_full, 1);
+        for (int q = 0; q < 2; ++q) {
+            ptx::mbar_init(&xfull[q], 1);
+            ptx::mbar_init(&xempty[q], 1);
+        }
         *abort = 0;
         ptx::fence_mbar_init();
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -287,7 +300,63 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
                     }
                 }
             }
-            for (int64_t t = blockIdx.x; !gp.xshare && t < gp.num_tiles && !*abort; t += gridDim.x) {
+            int64_t x_issued = 0;
+            if constexpr (C::kPlaneStages) {
+                if (gp.xring) {
+                    // X-ring mode: per channel slice kc and tap row uy, one X box of both
+                    // planes into the next ring slot; then per tap of the row and per plane,
+                    // one weight box into the stage ring.
+                    uint8_t *xr = stage_base + gp.xring_off;
+                    const int x_bytes = gp.x_rows * C::kSlice;   // one plane of a box
+                    const int taps = gp.mx * gp.my;
+                    int slot = 0;
+                    uint32_t xphase = 0;
+                    bool stop = false;
+                    for (int64_t t = blockIdx.x; t < gp.num_tiles && !*abort && !stop; t += gridDim.x) {
+                        const TileCoord tc = decode_tile((uint32_t)t, gp, BN);
+                        for (int kb = tc.kb0; kb < tc.kb1 && !stop; ++kb) {
+                            const int kc = kb / taps;
+                            const int g = kb - kc * taps;
+                            const int uy = g / gp.mx;
+                            if (g == uy * gp.mx) {
+                                if (!ptx::mbar_wait(&xempty[slot], xphase ^ 1u, limit, abort)) {
+                                    if (!*abort) give_up(abort, gp.status, kStatusTimeoutProducer);
+                                    stop = true;
+                                    break;
+                                }
+                                ptx::mbar_arrive_expect_tx(&xfull[slot], (uint32_t)(2 * x_bytes));
+                                uint8_t *xb = xr + slot * 2 * x_bytes;
+                                const int32_t x_k = kc * C::kElems;
+                                const int32_t x_row = (int32_t)(tc.p0 + gp.shift0 + (int64_t)uy * gp.Px);
+                                ptx::tma_load_2d(xb, &mapX, &xfull[slot], x_k, x_row);
+                                ptx::tma_load_2d(xb + x_bytes, &mapX2, &xfull[slot], x_k, x_row);
+                                ++x_issued;
+                                if (++slot == 2) {
+                                    slot = 0;
+                                    xphase ^= 1u;
+                                }
+                            }
+                            const int32_t w_k = (g * gp.kb_per_tap + kc) * C::kElems;
+                            for (int pl = 0; pl < 2; ++pl) {
+                                if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, limit, abort)) {
+                                    if (!*abort) give_up(abort, gp.status, kStatusTimeoutProducer);
+                                    stop = true;
+                                    break;
+                                }
+                                ptx::mbar_arrive_expect_tx(&full[stage], (uint32_t)C::kWBytes);
+                                ptx::tma_load_2d(stage_base + stage * gp.stage_bytes, pl ? &mapW2 : &mapW,
+                                                 &full[stage], w_k, (int32_t)tc.r0);
+                                ++issued;
+                                if (++stage == nst) {
+                                    stage = 0;
+                                    phase ^= 1u;
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+            for (int64_t t = blockIdx.x; !gp.xshare && !gp.xring && t < gp.num_tiles && !*abort; t += gridDim.x) {
                 const TileCoord tc = decode_tile((uint32_t)t, gp, BN);
                 // Tap (uy, ux) and channel slice kc of K slice kb, stepped along with kb.
                 const int g0 = tc.kb0 / gp.kb_per_tap;
@@ -343,6 +412,12 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
             }
             if (w_issued && !ptx::mbar_wait(w_full, 0, kDrainLimitNs, nullptr))
                 atomicOr(gp.status, kStatusTimeoutDrain);
+            const int64_t x_pending = x_issued < 2 ? x_issued : 2;
+            for (int64_t q = 0; q < x_pending; ++q) {
+                const int64_t idx = x_issued - 1 - q;
+                if (!ptx::mbar_wait(&xfull[idx % 2], (uint32_t)((idx / 2) & 1), kDrainLimitNs, nullptr))
+                    atomicOr(gp.status, kStatusTimeoutDrain);
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -409,7 +484,96 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(P, BN))
                     }
                 }
             }
-            for (int64_t t = blockIdx.x; !gp.xshare && ok && t < gp.num_tiles && !ptx::abort_warp(abort); t += gridDim.x, ++items) {
+            if constexpr (C::kPlaneStages) {
+                if (gp.xring) {
+                    // X-ring mode: tap ux of a row reads the row's X box through a descriptor
+                    // that starts ux rows further down; the box's slot is released after the
+                    // row's last tap.
+                    const uint8_t *xr = stage_base + gp.xring_off;
+                    const int x_bytes = gp.x_rows * C::kSlice;
+                    const int taps = gp.mx * gp.my;
+                    int slot = 0;
+                    uint32_t xphase = 0;
+                    for (int64_t t = blockIdx.x; ok && t < gp.num_tiles && !ptx::abort_warp(abort); t += gridDim.x, ++items) {
+                        const TileCoord tc = decode_tile((uint32_t)t, gp, BN);
+                        for (int kb = tc.kb0, gi = 0; ok && kb < tc.kb1; ++gi) {
+                            const int kb_end = min(kb + gp.kb_group, tc.kb1);
+                            const bool to_sum = C::kSumFirst && gi == 0;
+                            const int acc = grp % C::kAccBufs;
+                            if (to_sum) {
+                                if (!ptx::mbar_wait_warp(sum_free, ((uint32_t)items & 1u) ^ 1u, limit, abort)) {
+                                    if (lane == 0 && !*abort) give_up(abort, gp.status, kStatusTimeoutMma);
+                                    ok = false;
+                                    break;
+                                }
+                            } else {
+                                const uint32_t acc_phase = (uint32_t)(grp / C::kAccBufs) & 1u;
+                                if (!ptx::mbar_wait_warp(&tmem_empty[acc], acc_phase ^ 1u, limit, abort)) {
+                                    if (lane == 0 && !*abort) give_up(abort, gp.status, kStatusTimeoutMma);
+                                    ok = false;
+                                    break;
+                                }
+                            }
+                            ptx::tc_fence_after();
+                            const uint32_t d_tmem =
+                                tmem_base + (to_sum ? C::kSumCol : (uint32_t)(acc * BN));
+                            uint32_t accumulate = 0;
+                            for (; ok && kb < kb_end; ++kb) {
+                                const int kc = kb / taps;
+                                const int g = kb - kc * taps;
+                                const int ux = g % gp.mx;
+                                if (ux == 0) {
+                                    if (!ptx::mbar_wait_warp(&xfull[slot], xphase, limit, abort)) {
+                                        if (lane == 0 && !*abort) give_up(abort, gp.status, kStatusTimeoutMma);
+                                        ok = false;
+                                        break;
+                                    }
+                                    ptx::tc_fence_after();
+                                }
+                                const uint8_t *xb = xr + slot * 2 * x_bytes + ux * C::kSlice;
+                                for (int pl = 0; pl < 2; ++pl) {
+                                    if (!ptx::mbar_wait_warp(&full[stage], phase, limit, abort)) {
+                                        if (lane == 0 && !*abort) give_up(abort, gp.status, kStatusTimeoutMma);
+                                        ok = false;
+                                        break;
+                                    }
+                                    ptx::tc_fence_after();
+                                    const uint64_t xd = ptx::sdesc_k<C::kSlice>(ptx::smem_u32(xb + pl * x_bytes));
+                                    const uint64_t wd = ptx::sdesc_k<C::kSlice>(
+                                        ptx::smem_u32(stage_base + stage * gp.stage_bytes));
+#pragma unroll
+                                    for (int k = 0; k < C::kKSteps; ++k) {
+                                        const uint64_t dk = (uint64_t)(2 * k);
+                                        if (ptx::elect_one()) {
+                                            if (pl == 0)
+                                                ptx::mma_tf32(d_tmem, xd + dk, wd + dk, C::kIdesc, accumulate);
+                                            else
+                                                ptx::mma_f16(d_tmem, xd + dk, wd + dk, C::kIdescCross, 1u);
+                                        }
+                                        accumulate = 1u;
+                                    }
+                                    if (ptx::elect_one()) ptx::mma_commit(&empty[stage]);
+                                    if (++stage == nst) {
+                                        stage = 0;
+                                        phase ^= 1u;
+                                    }
+                                }
+                                if (!ok) break;
+                                if (ux == gp.mx - 1) {   // the row's taps are issued: free its box
+                                    if (ptx::elect_one()) ptx::mma_commit(&xempty[slot]);
+                                    if (++slot == 2) {
+                                        slot = 0;
+                                        xphase ^= 1u;
+                                    }
+                                }
+                            }
+                            if (ok && ptx::elect_one()) ptx::mma_commit(to_sum ? sum_full : &tmem_full[acc]);
+                            if (!to_sum) ++grp;
+                        }
+                    }
+                }
+            }
+            for (int64_t t = blockIdx.x; !gp.xshare && !gp.xring && ok && t < gp.num_tiles && !ptx::abort_warp(abort); t += gridDim.x, ++items) {
                 const TileCoord tc = decode_tile((uint32_t)t, gp, BN);
                 for (int kb = tc.kb0, g = 0; ok && kb < tc.kb1; ++g) {
                     const int kb_end = min(kb + gp.kb_group, tc.kb1);
