@@ -592,3 +592,26 @@ def test_tile_model_choices_without_gpu(ctr):
             assert "BN %d," % bn in d and "splits=%d " % sp in d, d
         finally:
             ctr.ctr_plan_destroy(h)
+
+
+def test_xring_mode_selection_without_gpu(ctr):
+    """fp32 polyphase plans on 256-row tiles with four or more taps along x run the GEMM in
+    X-ring mode, while a split-K factor leaves every unit at least one channel slice; two-tap
+    layers, 16-bit I/O and other tile widths keep the default stage ring."""
+    def desc(args, dtype=None, bn=256, split=0):
+        nd = len(args[3])
+        h = _plan(ctr, nd, *args, [0] * nd, ctr.CTR_F32 if dtype is None else dtype)
+        try:
+            ctr.ctr_plan_set_path(h, ctr.CTR_PATH_POLYPHASE, split)
+            ctr.ctr_plan_set_tile(h, bn)
+            return ctr.ctr_plan_describe(h)
+        finally:
+            ctr.ctr_plan_destroy(h)
+    four_taps = (1, 64, 40, [300], [16], [4], [0])      # C_in 64: two channel slices
+    assert " x-ring" in desc(four_taps)
+    assert " x-ring" in desc(four_taps, split=2)
+    assert " x-ring" not in desc(four_taps, split=3)    # a unit would get no channel slice
+    assert " x-ring" not in desc(four_taps, bn=128)
+    assert " x-ring" not in desc(four_taps, dtype=ctr.CTR_BF16)
+    assert " x-ring" not in desc((1, 64, 40, [300], [8], [4], [0]))   # two taps
+    assert " x-ring" in desc((4, 4098, 1, [343], [4096], [1024], [0]), bn=0)   # the iSTFT, auto
