@@ -45,13 +45,15 @@ def _flush_chunks(k, s, L):
     return -(-(m - 1) // L) if m > 1 else 0
 
 
-def _run_stream(case, chunks, b, w, split_k=0):
+def _run_stream(case, chunks, b, w, split_k=0, block_n=0, expect_mode=None):
     """Feed the chunks through one streaming plan; returns the concatenated output (float64)."""
     name, B, C_in, C_out, k, s, L, _, dtype, slope = case
     plan = ctr.Plan(B, C_in, C_out, (L,), (k,), s, 0, 0, dtype=tdtype(dtype),
-                    negative_slope=slope, streaming=True, split_k=split_k)
+                    negative_slope=slope, streaming=True, split_k=split_k, block_n=block_n)
     try:
         assert plan.path == ctr.CTR_PATH_POLYPHASE, plan.describe()
+        if expect_mode is not None:
+            assert expect_mode in plan.describe(), plan.describe()
         assert plan.out_shape == (B, C_out, s * L)
         plan.prepack(to_dev(w, dtype))
         outs = []
@@ -124,6 +126,15 @@ def test_stream_random_matches_oracle_and_whole_input(case):
     finally:
         whole.close()
     np.testing.assert_array_equal(y, yw)
+
+
+def test_stream_fp32_xring_integer_exact():
+    """An fp32 stream on 256-row tiles with four taps: the GEMM runs in X-ring mode (the taps
+    share one box of the staged input, whose leading halo holds the carried frames)."""
+    case = ("k16_s4_f32_xring", 1, 64, 64, 16, 4, 29, 4, "f32", None)
+    xs, w, b = _inputs(case, True, 13)
+    y = _run_stream(case, xs, b, w, block_n=256, expect_mode=" x-ring")
+    np.testing.assert_array_equal(y, _reference(case, xs, w, b))
 
 
 def test_stream_reset_starts_a_new_stream():
