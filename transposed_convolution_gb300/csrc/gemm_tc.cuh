@@ -33,13 +33,22 @@
 // and Yokota, "Recovering single precision accuracy from Tensor Cores while surpassing the
 // FP32 theoretical peak performance" (IJHPCA 2022), who issue hi*hi, hi*lo and lo*hi as three
 // tf32 MMAs.  Here the two cross products are one kind::f16 MMA on bf16 pairs instead: every
-// 32-byte K step issues that bf16 MMA (16 bf16 = 8 K elements x (hi, lo), from the second
-// operand plane; ptx::split_x / split_w) and then the tf32 MMA of hi*hi (8 K elements, first
-// plane) into the same fp32 accumulator.  The bf16 MMA of K 16 takes the tensor pipe as long
-// as the tf32 MMA of K 8, so a K step costs two tf32 MMA times instead of three, and the
+// 32-byte K step issues a bf16 MMA (16 bf16 = 8 K elements x (hi, lo), from the second
+// operand plane; ptx::split_x / split_w) and a tf32 MMA of hi*hi (8 K elements, first plane)
+// into the same fp32 accumulator.  The bf16 MMA of K 16 takes the tensor pipe as long as the
+// tf32 MMA of K 8, so a K step costs two tf32 MMA times instead of three, and the
 // shared-memory operand reads drop by the same third.  The bf16 roundings of the cross terms
 // (each below 2^-11 of the product) cost at most about 2^-17 of a product's value, well
 // inside fp32 I/O's accuracy bound.
+//
+// Stage layouts.  By default a stage holds one K slice (128 bytes of K) of every operand
+// plane: the X box of the tap and the BN-row weight box.  fp32 256-row tiles hold one plane
+// per stage instead (the tf32 plane's stage, then the cross plane's: four 48 KB stages fit),
+// and with four or more taps along x they run in X-ring mode: the taps of one tap row read
+// one shared X box (128 + mx - 1 rows, both planes) from a two-slot ring of its own, through
+// descriptors that start one row further down per tap, while one-plane weight boxes stream
+// through the stage ring.  16-bit 1-D plans may run in shared-X mode (set_pipeline_layout):
+// one X box per channel slice in each stage, read by every tap the same way.
 //
 // Every mbarrier wait is bounded (wait_limit_ns of global time).  A wait that gives up sets
 // a bit in the plan's status word and a CTA-wide abort flag; every role then stops, the
